@@ -1,0 +1,301 @@
+"""Python shim over the plain-C CPU oracle (``lsa_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and
+the bench's CPU-baseline leg are the only callers.  The CUDA library never
+imports, links or calls anything here, and nothing here imports the CUDA
+library.  Inputs are host numpy arrays (bf16 as uint16 bit patterns, FP8 as
+uint8 bit patterns) or CPU torch tensors; every result is computed in fp64 by
+the C code from those inputs.
+
+Parity status per function (what pins each one is listed in the tests):
+  bf16_round, e4m3_decode, summaries, block_scores, topk, attend_tokens,
+  lse_merge, decode (single stage and coarse-to-fine), dense -- all pinned.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lsa_oracle.c")
+_LIB = os.path.join(_HERE, "liblsa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, no fast-math; OpenMP when the
+    compiler supports it).  Returns the path of the shared library."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-Wall", "-o", _LIB + ".tmp", _SRC, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+class _Cache(C.Structure):
+    _fields_ = [("num_pages", C.c_int32), ("num_kv_heads", C.c_int32),
+                ("block_size", C.c_int32), ("dk", C.c_int32), ("dv", C.c_int32),
+                ("k", C.c_void_p), ("v", C.c_void_p), ("k8", C.c_void_p),
+                ("k8_scale", C.c_void_p)]
+
+
+class _Params(C.Structure):
+    _fields_ = [("batch", C.c_int32), ("num_q_heads", C.c_int32), ("max_blocks", C.c_int32),
+                ("k_blocks", C.c_int32), ("sink", C.c_int32), ("recent", C.c_int32),
+                ("scale", C.c_double), ("c2f_candidates", C.c_int32),
+                ("c2f_tokens", C.c_int32)]
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = C.CDLL(build())
+            P, I = C.c_void_p, C.c_int32
+            lib.orc_bf16_to_f64.argtypes = [C.c_uint16]
+            lib.orc_bf16_to_f64.restype = C.c_double
+            lib.orc_f64_to_bf16.argtypes = [C.c_double]
+            lib.orc_f64_to_bf16.restype = C.c_uint16
+            lib.orc_e4m3_to_f64.argtypes = [C.c_uint8]
+            lib.orc_e4m3_to_f64.restype = C.c_double
+            lib.orc_summaries.argtypes = [P, C.c_int, P, P, I, I, P, P]
+            lib.orc_block_scores.argtypes = [P, P, C.c_int, P, P, P, P, P]
+            lib.orc_topk.argtypes = [P, I, I, P]
+            lib.orc_fine_scores.argtypes = [P, P, P, P, C.c_int, C.c_int, C.c_int64, P, P, P]
+            lib.orc_decode.argtypes = [P, P, P, P, P, P, P, P, C.c_int, P, P, P, P]
+            lib.orc_dense.argtypes = [P, P, P, P, P, P, P]
+            lib.orc_attend_tokens.argtypes = [P, P, P, C.c_int64, P, C.c_int, C.c_double, P, P]
+            lib.orc_lse_merge.argtypes = [C.c_int, C.c_int, P, P, P, P]
+            lib.orc_lse_merge.restype = None
+            for f in ("orc_summaries", "orc_block_scores", "orc_topk", "orc_fine_scores",
+                      "orc_decode", "orc_dense", "orc_attend_tokens"):
+                getattr(lib, f).restype = C.c_int
+            _lib = lib
+    return _lib
+
+
+_ERR = {1: "page id out of range", 2: "invalid argument", 3: "out of memory"}
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise RuntimeError(f"oracle error {rc}: {_ERR.get(rc, '?')}")
+
+
+def _np(x, dtype) -> np.ndarray:
+    """Host, C-contiguous numpy view/copy of a numpy array or torch tensor.
+    bf16 tensors become uint16 bit patterns, fp8 tensors uint8 patterns."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            t = x.detach()
+            if t.device.type != "cpu":
+                t = t.cpu()
+            if t.dtype == torch.bfloat16:
+                t = t.contiguous().view(torch.int16)
+            elif t.dtype in (torch.float8_e4m3fn,):
+                t = t.contiguous().view(torch.uint8)
+            x = t.contiguous().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(x)
+    if a.dtype != dtype:
+        if dtype == np.uint16 and a.dtype == np.int16:
+            a = a.view(np.uint16)
+        else:
+            a = a.astype(dtype)
+    return a
+
+
+def _p(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+class Cache:
+    """Host copy of a paged cache: k [P, Hkv, b, dk] bf16, v [P, Hkv, b, dv]
+    bf16 (V aliased on a latent cache is passed as the copy k[..., :dv]),
+    optional FP8 index keys k8 [P, Hkv, b, dk] and scales [P, Hkv, b]."""
+
+    def __init__(self, k, v=None, k8=None, k8_scale=None, dv: Optional[int] = None):
+        self.k = _np(k, np.uint16) if k is not None else None
+        if v is None and k is not None and dv is not None:
+            v = self.k[..., :dv]
+        self.v = _np(v, np.uint16) if v is not None else None
+        self.k8 = _np(k8, np.uint8) if k8 is not None else None
+        self.k8_scale = _np(k8_scale, np.float32) if k8_scale is not None else None
+        ref = self.k if self.k is not None else self.k8
+        P, H, b, dk = ref.shape
+        self.shape = (P, H, b, dk)
+        self.dv = self.v.shape[-1] if self.v is not None else dk
+        self._c = _Cache(P, H, b, dk, self.dv, _p(self.k), _p(self.v), _p(self.k8),
+                         _p(self.k8_scale))
+
+    @property
+    def ref(self):
+        return C.byref(self._c)
+
+
+def _params(batch, num_q_heads, max_blocks, k_blocks=0, sink=0, recent=0, scale=1.0,
+            c2f_candidates=0, c2f_tokens=0):
+    return _Params(batch, num_q_heads, max_blocks, k_blocks, sink, recent, float(scale),
+                   c2f_candidates, c2f_tokens)
+
+
+# ---------------------------------------------------------------- formats
+
+def bf16_round(x: float) -> int:
+    """double -> bf16 bit pattern, round to nearest even (one rounding)."""
+    return int(_load().orc_f64_to_bf16(float(x)))
+
+
+def bf16_value(bits: int) -> float:
+    return float(_load().orc_bf16_to_f64(int(bits) & 0xFFFF))
+
+
+def e4m3_decode(code: int) -> float:
+    return float(_load().orc_e4m3_to_f64(int(code) & 0xFF))
+
+
+# ---------------------------------------------------------------- steps
+
+def summaries(cache: Cache, page_table, seq_lens, use_index_keys: bool = False):
+    """bf16 mean-key summaries [P, Hkv, dk] (uint16 bits) of every full
+    block the page tables reference, and the [P] mask of pages written."""
+    lib = _load()
+    pt = _np(page_table, np.int32)
+    lens = _np(seq_lens, np.int32)
+    P, H, b, dk = cache.shape
+    out = np.zeros((P, H, dk), dtype=np.uint16)
+    valid = np.zeros((P,), dtype=np.uint8)
+    _check(lib.orc_summaries(cache.ref, int(use_index_keys), _p(pt), _p(lens), pt.shape[0],
+                             pt.shape[1], _p(out), _p(valid)))
+    return out, valid.astype(bool)
+
+
+def block_scores(q, cache: Cache, summ, page_table, seq_lens, num_q_heads, sink, recent,
+                 use_index_keys: bool = False):
+    """fp64 block scores [B, Hkv, max_blocks]; -inf for non-candidates.
+    ``summ`` = oracle summaries (uint16 bits) or None to compute from keys."""
+    lib = _load()
+    qa = _np(q, np.uint16)
+    pt = _np(page_table, np.int32)
+    lens = _np(seq_lens, np.int32)
+    s = None if summ is None else _np(summ, np.uint16)
+    B, maxb = pt.shape
+    prm = _params(B, num_q_heads, maxb, 0, sink, recent)
+    out = np.empty((B, cache.shape[1], maxb), dtype=np.float64)
+    _check(lib.orc_block_scores(_p(qa), cache.ref, int(use_index_keys), _p(s), _p(pt), _p(lens),
+                                C.byref(prm), _p(out)))
+    return out
+
+
+def topk(scores, k: int) -> np.ndarray:
+    """Row-wise top-k of a [rows, n] array by (score desc, index asc), -inf
+    and NaN excluded; indices ascending, -1 padded.  Scores are taken as fp64
+    (an fp32 input converts exactly)."""
+    lib = _load()
+    s = np.ascontiguousarray(np.asarray(scores, dtype=np.float64))
+    s2 = s.reshape(-1, s.shape[-1])
+    out = np.empty((s2.shape[0], k), dtype=np.int32)
+    for i in range(s2.shape[0]):
+        row = np.ascontiguousarray(s2[i])
+        o = np.empty((k,), dtype=np.int32)
+        _check(lib.orc_topk(_p(row), row.shape[0], k, _p(o)))
+        out[i] = o
+    return out.reshape(s.shape[:-1] + (k,))
+
+
+def fine_scores(q, index_cache: Cache, page_table, num_q_heads, r: int, h: int, blocks):
+    """fp64 FP8 rescoring of every token of ``blocks`` (request r, KV head h):
+    returns (scores, token positions)."""
+    lib = _load()
+    qa = _np(q, np.uint16)
+    pt = _np(page_table, np.int32)
+    bl = np.ascontiguousarray(np.asarray(blocks, dtype=np.int64))
+    b = index_cache.shape[2]
+    prm = _params(pt.shape[0], num_q_heads, pt.shape[1])
+    f = np.empty((bl.shape[0] * b,), dtype=np.float64)
+    t = np.empty((bl.shape[0] * b,), dtype=np.int64)
+    _check(lib.orc_fine_scores(_p(qa), index_cache.ref, _p(pt), C.byref(prm), r, h, bl.shape[0],
+                               _p(bl), _p(f), _p(t)))
+    return f, t
+
+
+def decode(q, cache: Cache, page_table, seq_lens, *, num_q_heads, k_blocks, sink, recent, scale,
+           summ=None, index_cache: Optional[Cache] = None, index_summ=None,
+           c2f_candidates: int = 0, c2f_tokens: int = 0, nthreads: int = 1):
+    """The whole decode step.  Returns dict(out [B,Hq,dv] uint16 bf16 bits,
+    lse [B,Hq] fp64, sel [B,Hkv,ksel] int32, cand [B,Hkv,C] int32 or None)."""
+    lib = _load()
+    qa = _np(q, np.uint16)
+    pt = _np(page_table, np.int32)
+    lens = _np(seq_lens, np.int32)
+    s = None if summ is None else _np(summ, np.uint16)
+    isum = None if index_summ is None else _np(index_summ, np.uint16)
+    B, maxb = pt.shape
+    Hkv = cache.shape[1]
+    prm = _params(B, num_q_heads, maxb, k_blocks, sink, recent, scale, c2f_candidates, c2f_tokens)
+    ksel = c2f_tokens if c2f_candidates > 0 else k_blocks
+    out = np.zeros((B, num_q_heads, cache.dv), dtype=np.uint16)
+    lse = np.zeros((B, num_q_heads), dtype=np.float64)
+    sel = np.zeros((B, Hkv, max(ksel, 0)), dtype=np.int32)
+    cand = np.zeros((B, Hkv, c2f_candidates), dtype=np.int32) if c2f_candidates > 0 else None
+    _check(lib.orc_decode(_p(qa), cache.ref, _p(s), index_cache.ref if index_cache else None,
+                          _p(isum), _p(pt), _p(lens), C.byref(prm), int(nthreads), _p(out),
+                          _p(lse), _p(sel), _p(cand)))
+    return dict(out=out, lse=lse, sel=sel, cand=cand)
+
+
+def dense(q, cache: Cache, page_table, seq_lens, *, num_q_heads, scale):
+    """Dense attention over all L tokens (bf16 bits out, fp64 lse)."""
+    lib = _load()
+    qa = _np(q, np.uint16)
+    pt = _np(page_table, np.int32)
+    lens = _np(seq_lens, np.int32)
+    B, maxb = pt.shape
+    prm = _params(B, num_q_heads, maxb, scale=scale)
+    out = np.zeros((B, num_q_heads, cache.dv), dtype=np.uint16)
+    lse = np.zeros((B, num_q_heads), dtype=np.float64)
+    _check(lib.orc_dense(_p(qa), cache.ref, _p(pt), _p(lens), C.byref(prm), _p(out), _p(lse)))
+    return dict(out=out, lse=lse)
+
+
+def attend_tokens(q_head, cache: Cache, page_table_row, tokens, h: int, scale: float):
+    """fp64 attention of one query head (fp64 vector) over explicit tokens."""
+    lib = _load()
+    qd = np.ascontiguousarray(np.asarray(q_head, dtype=np.float64))
+    ptr = _np(page_table_row, np.int32)
+    tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
+    o = np.empty((cache.dv,), dtype=np.float64)
+    lse = np.empty((1,), dtype=np.float64)
+    _check(lib.orc_attend_tokens(_p(qd), cache.ref, _p(ptr), tok.shape[0], _p(tok), int(h),
+                                 float(scale), _p(o), _p(lse)))
+    return o, float(lse[0])
+
+
+def lse_merge(o_parts, lse_parts):
+    lib = _load()
+    o = np.ascontiguousarray(np.asarray(o_parts, dtype=np.float64))
+    l = np.ascontiguousarray(np.asarray(lse_parts, dtype=np.float64))
+    n, dv = o.shape
+    oo = np.empty((dv,), dtype=np.float64)
+    lo = np.empty((1,), dtype=np.float64)
+    lib.orc_lse_merge(n, dv, _p(o), _p(l), _p(oo), _p(lo))
+    return oo, float(lo[0])
+
+
+def bf16_bits_to_f64(a) -> np.ndarray:
+    """Decode a uint16 bf16 bit-pattern array to fp64 (bit shift only)."""
+    a = np.asarray(a).astype(np.uint32) << 16
+    return a.view(np.float32).astype(np.float64)

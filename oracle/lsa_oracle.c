@@ -1,0 +1,648 @@
+/*
+ * lsa_oracle.c -- plain, slow, obviously-correct CPU oracle for the
+ * block-sparse decode step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The test suite, the smoke check and the bench's
+ * CPU-baseline leg are the only callers.  It shares no source, header, table
+ * or helper with the CUDA library; the two meet only through the seeded
+ * input generator (the `workloads` package), which holds none of the
+ * method's arithmetic.
+ *
+ * Everything is computed in double precision from the bf16 / e4m3 inputs.
+ * The method, as the pages define it:
+ *
+ *   summary   k_bar_j = mean of the b keys of block j, built once the block
+ *             is full (Vortex blog post, "Block top-k attention", Figure 1
+ *             and the forward_cache of the vFlow listing); stored as bf16.
+ *   score     s_j = q . k_bar_j (Vortex, block top-k equation), summed over
+ *             the query heads of a KV head's GQA group (the vFlow listing
+ *             reduces the GeMM output over the head dimension; a sum equals
+ *             that mean times the group size, which orders blocks the same).
+ *   select    I = top-k_j(s_j), ties to the lower block index, with the sink
+ *             tokens and the most recent tokens always attended (ByteCross,
+ *             Figure 1 caption and Appendix A "Scored selection"; Vortex
+ *             cites StreamingLLM for sinks plus a recent window).
+ *   attend    o = softmax(q K_T^T * scale) V_T over the attended token set T
+ *             (Vortex, block top-k equation).
+ *   coarse-to-fine: a coarse top-C over block summaries of the index keys,
+ *             then an exact rescoring of every token of the C blocks with its
+ *             FP8 e4m3 index key and per-token scale, keeping the top tokens
+ *             (LeanSparse, Section 5 "Coarse-to-fine decode indexing",
+ *             Figure 9; 132-byte FP8 key + scale).
+ *   merge     partial results over a partition of T combine by log-sum-exp
+ *             (ByteCross, Appendix A: sink call and window call merged by
+ *             log-sum-exp).
+ *
+ * Readings where the pages leave a step open are stated beside each step.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------ */
+/* Number formats                                                      */
+/* ------------------------------------------------------------------ */
+
+/* bf16 bit pattern -> double (bf16 is the top half of an IEEE binary32). */
+double orc_bf16_to_f64(uint16_t h)
+{
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* double -> bf16, round to nearest, ties to even, in one rounding step.
+ * bf16 keeps 8 significant bits; normal numbers start at 2^-126 and the
+ * subnormal spacing is 2^-133 (binary32's exponent range). */
+uint16_t orc_f64_to_bf16(double x)
+{
+    if (isnan(x))
+        return 0x7fc0;
+    uint16_t s = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (isinf(a))
+        return s | 0x7f80;
+    if (a == 0.0)
+        return s;
+    int e;
+    (void)frexp(a, &e);            /* a = m * 2^e, m in [0.5, 1) */
+    int qe = e - 8;                /* spacing of 8-significant-bit numbers */
+    if (qe < -133)
+        qe = -133;
+    double r = nearbyint(ldexp(a, -qe));   /* default mode: ties to even */
+    double y = ldexp(r, qe);
+    if (y >= 0x1p128)
+        return s | 0x7f80;
+    float f = (float)y;            /* exact: y is a bf16 value */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return s | (uint16_t)(u >> 16);
+}
+
+/* OCP FP8 E4M3 ("fn": no infinities, S.1111.111 is NaN), bias 7. */
+double orc_e4m3_to_f64(uint8_t c)
+{
+    int sgn = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    double v = (e == 0) ? ldexp((double)m, -9)         /* m/8 * 2^-6      */
+                        : ldexp((double)(8 + m), e - 10); /* (1+m/8) 2^(e-7) */
+    return sgn ? -v : v;
+}
+
+/* ------------------------------------------------------------------ */
+/* Inputs                                                              */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    int32_t num_pages, num_kv_heads, block_size, dk, dv;
+    const uint16_t *k;        /* [P, Hkv, b, dk] bf16, contiguous       */
+    const uint16_t *v;        /* [P, Hkv, b, dv] bf16, contiguous       */
+    const uint8_t *k8;        /* [P, Hkv, b, dk] e4m3 index keys or NULL */
+    const float *k8_scale;    /* [P, Hkv, b] per-token scale or NULL     */
+} orc_cache;
+
+typedef struct {
+    int32_t batch, num_q_heads, max_blocks;
+    int32_t k_blocks;          /* scored blocks to select, forced excluded */
+    int32_t sink, recent;      /* forced token ranges                      */
+    double scale;              /* softmax scale                            */
+    int32_t c2f_candidates;    /* 0: single stage                          */
+    int32_t c2f_tokens;
+} orc_params;
+
+enum { ORC_OK = 0, ORC_BAD_PAGE = 1, ORC_BAD_ARG = 2, ORC_NOMEM = 3 };
+
+static double key_elem(const orc_cache *c, int use_k8, int64_t p, int h, int t, int i)
+{
+    int64_t base = ((p * c->num_kv_heads + h) * (int64_t)c->block_size + t);
+    if (use_k8)
+        return (double)c->k8_scale[base] * orc_e4m3_to_f64(c->k8[base * c->dk + i]);
+    return orc_bf16_to_f64(c->k[base * c->dk + i]);
+}
+
+static double val_elem(const orc_cache *c, int64_t p, int h, int t, int i)
+{
+    int64_t base = ((p * c->num_kv_heads + h) * (int64_t)c->block_size + t);
+    return orc_bf16_to_f64(c->v[base * c->dv + i]);
+}
+
+/* Forced ranges F = [0, sink_end) U [rec_start, L), with the recent range
+ * clipped so that the two never overlap.  Reading: when L < sink + recent
+ * the two ranges cover every token. */
+static void forced_ranges(int64_t L, int32_t sink, int32_t recent,
+                          int64_t *sink_end, int64_t *rec_start)
+{
+    int64_t se = sink < L ? sink : L;
+    int64_t rs = L - recent;
+    if (rs < se)
+        rs = se;
+    *sink_end = se;
+    *rec_start = rs;
+}
+
+/* Block j is a scoring candidate iff it is full and none of its tokens is
+ * forced.  Reading: a partial tail block has no summary until it fills, and
+ * a block touching a forced range is attended (in part) anyway. */
+static int is_candidate(int64_t j, int32_t b, int64_t sink_end, int64_t rec_start)
+{
+    return j * b >= sink_end && (j + 1) * b <= rec_start;
+}
+
+/* ------------------------------------------------------------------ */
+/* Step: block summaries                                               */
+/* ------------------------------------------------------------------ */
+
+/* Mean of the b keys of (page p, head h), exact fp64 sum, one rounding. */
+static void summary_of(const orc_cache *c, int use_k8, int64_t p, int h, double *out)
+{
+    const int b = c->block_size;
+    for (int i = 0; i < c->dk; ++i) {
+        double sum = 0.0;
+        for (int t = 0; t < b; ++t)
+            sum += key_elem(c, use_k8, p, h, t, i);
+        out[i] = orc_bf16_to_f64(orc_f64_to_bf16(sum / (double)b));
+    }
+}
+
+/* Summaries of every full block referenced by the page tables.
+ * summ: [P, Hkv, dk] bf16 bits (untouched for pages with no full block);
+ * valid: [P] set to 1 for pages written (may be NULL). */
+int orc_summaries(const orc_cache *c, int use_k8, const int32_t *pt, const int32_t *lens,
+                  int32_t batch, int32_t max_blocks, uint16_t *summ, uint8_t *valid)
+{
+    double *tmp = (double *)malloc(sizeof(double) * (size_t)c->dk);
+    if (!tmp)
+        return ORC_NOMEM;
+    for (int r = 0; r < batch; ++r) {
+        int64_t nfull = lens[r] / c->block_size;
+        for (int64_t j = 0; j < nfull; ++j) {
+            int64_t p = pt[(int64_t)r * max_blocks + j];
+            if (p < 0 || p >= c->num_pages) {
+                free(tmp);
+                return ORC_BAD_PAGE;
+            }
+            for (int h = 0; h < c->num_kv_heads; ++h) {
+                summary_of(c, use_k8, p, h, tmp);
+                for (int i = 0; i < c->dk; ++i)
+                    summ[((int64_t)p * c->num_kv_heads + h) * c->dk + i] = orc_f64_to_bf16(tmp[i]);
+            }
+            if (valid)
+                valid[p] = 1;
+        }
+    }
+    free(tmp);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* Step: block scores                                                  */
+/* ------------------------------------------------------------------ */
+
+static void load_summary(const orc_cache *c, int use_k8, const uint16_t *summ,
+                         int64_t p, int h, double *out)
+{
+    if (summ) {
+        for (int i = 0; i < c->dk; ++i)
+            out[i] = orc_bf16_to_f64(summ[((int64_t)p * c->num_kv_heads + h) * c->dk + i]);
+    } else {
+        summary_of(c, use_k8, p, h, out);
+    }
+}
+
+/* s_j = sum over the group's query heads g of q_g . k_bar_j, for every
+ * candidate block j; -inf for every other j < max_blocks. */
+static int row_scores(const uint16_t *q, const orc_cache *c, int use_k8, const uint16_t *summ,
+                      const int32_t *pt, int64_t L, const orc_params *prm, int r, int h,
+                      double *scores)
+{
+    const int b = c->block_size, dk = c->dk;
+    const int G = prm->num_q_heads / c->num_kv_heads;
+    int64_t se, rs;
+    forced_ranges(L, prm->sink, prm->recent, &se, &rs);
+    double *sv = (double *)malloc(sizeof(double) * (size_t)dk);
+    if (!sv)
+        return ORC_NOMEM;
+    for (int64_t j = 0; j < prm->max_blocks; ++j) {
+        scores[j] = -INFINITY;
+        if (!is_candidate(j, b, se, rs))
+            continue;
+        int64_t p = pt[(int64_t)r * prm->max_blocks + j];
+        if (p < 0 || p >= c->num_pages) {
+            free(sv);
+            return ORC_BAD_PAGE;
+        }
+        load_summary(c, use_k8, summ, p, h, sv);
+        double s = 0.0;
+        for (int g = 0; g < G; ++g) {
+            const uint16_t *qg = q + ((int64_t)r * prm->num_q_heads + h * G + g) * dk;
+            for (int i = 0; i < dk; ++i)
+                s += orc_bf16_to_f64(qg[i]) * sv[i];
+        }
+        scores[j] = s;
+    }
+    free(sv);
+    return ORC_OK;
+}
+
+int orc_block_scores(const uint16_t *q, const orc_cache *c, int use_k8, const uint16_t *summ,
+                     const int32_t *pt, const int32_t *lens, const orc_params *prm,
+                     double *scores /* [B, Hkv, max_blocks] */)
+{
+    for (int r = 0; r < prm->batch; ++r)
+        for (int h = 0; h < c->num_kv_heads; ++h) {
+            int rc = row_scores(q, c, use_k8, summ, pt, lens[r], prm, r, h,
+                                scores + ((int64_t)r * c->num_kv_heads + h) * prm->max_blocks);
+            if (rc)
+                return rc;
+        }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* Step: top-k                                                         */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    double s;
+    int64_t j;
+} scored;
+
+/* Order: larger score first; equal scores -> lower index first. */
+static int by_score_then_index(const void *a, const void *b)
+{
+    const scored *x = (const scored *)a, *y = (const scored *)b;
+    if (x->s > y->s)
+        return -1;
+    if (x->s < y->s)
+        return 1;
+    return (x->j < y->j) ? -1 : (x->j > y->j);
+}
+
+static int by_index(const void *a, const void *b)
+{
+    int64_t x = *(const int64_t *)a, y = *(const int64_t *)b;
+    return (x < y) ? -1 : (x > y);
+}
+
+/* The k best of the n entries by (score desc, index asc).  Entries that are
+ * -inf or NaN are not candidates.  Output: the chosen indices in ascending
+ * order, then -1 padding up to k.  Returns the number chosen. */
+static int64_t select_topk(const double *s, const int64_t *ids, int64_t n, int64_t k, int64_t *out)
+{
+    scored *v = (scored *)malloc(sizeof(scored) * (size_t)(n > 0 ? n : 1));
+    int64_t m = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (isnan(s[i]) || s[i] == -INFINITY)
+            continue;
+        v[m].s = s[i];
+        v[m].j = ids ? ids[i] : i;
+        ++m;
+    }
+    qsort(v, (size_t)m, sizeof(scored), by_score_then_index);
+    int64_t take = m < k ? m : k;
+    for (int64_t i = 0; i < take; ++i)
+        out[i] = v[i].j;
+    qsort(out, (size_t)take, sizeof(int64_t), by_index);
+    for (int64_t i = take; i < k; ++i)
+        out[i] = -1;
+    free(v);
+    return take;
+}
+
+int orc_topk(const double *scores, int32_t n, int32_t k, int32_t *out)
+{
+    int64_t *tmp = (int64_t *)malloc(sizeof(int64_t) * (size_t)(k > 0 ? k : 1));
+    if (!tmp)
+        return ORC_NOMEM;
+    select_topk(scores, NULL, n, k, tmp);
+    for (int i = 0; i < k; ++i)
+        out[i] = (int32_t)tmp[i];
+    free(tmp);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* Step: attention over a token set                                    */
+/* ------------------------------------------------------------------ */
+
+/* o = softmax(scale * q K_T^T) V_T over the listed token positions of
+ * request r, KV head h; lse = log sum exp(scale * q K_T^T).  An empty set
+ * gives o = 0 and lse = -inf (reading: nothing to attend). */
+static int attend(const double *qd, const orc_cache *c, const int32_t *pt_row, int64_t ntok,
+                  const int64_t *tok, int h, double scale, double *o, double *lse)
+{
+    const int b = c->block_size, dk = c->dk, dv = c->dv;
+    for (int i = 0; i < dv; ++i)
+        o[i] = 0.0;
+    if (ntok == 0) {
+        *lse = -INFINITY;
+        return ORC_OK;
+    }
+    double *z = (double *)malloc(sizeof(double) * (size_t)ntok);
+    if (!z)
+        return ORC_NOMEM;
+    double zmax = -INFINITY;
+    for (int64_t n = 0; n < ntok; ++n) {
+        int64_t t = tok[n];
+        int64_t p = pt_row[t / b];
+        if (p < 0 || p >= c->num_pages) {
+            free(z);
+            return ORC_BAD_PAGE;
+        }
+        double d = 0.0;
+        for (int i = 0; i < dk; ++i)
+            d += qd[i] * key_elem(c, 0, p, h, (int)(t % b), i);
+        z[n] = scale * d;
+        if (z[n] > zmax)
+            zmax = z[n];
+    }
+    double denom = 0.0;
+    for (int64_t n = 0; n < ntok; ++n) {
+        int64_t t = tok[n];
+        int64_t p = pt_row[t / b];
+        double w = exp(z[n] - zmax);
+        denom += w;
+        for (int i = 0; i < dv; ++i)
+            o[i] += w * val_elem(c, p, h, (int)(t % b), i);
+    }
+    for (int i = 0; i < dv; ++i)
+        o[i] /= denom;
+    *lse = zmax + log(denom);
+    free(z);
+    return ORC_OK;
+}
+
+/* Attention of every query head of (r, h) over a given token list.
+ * out: [Hq, dv] doubles for this request (rows h*G .. h*G+G-1 written). */
+static int attend_group(const uint16_t *q, const orc_cache *c, const int32_t *pt_row,
+                        const orc_params *prm, int r, int h, int64_t ntok, const int64_t *tok,
+                        uint16_t *out, double *lse_out)
+{
+    const int G = prm->num_q_heads / c->num_kv_heads, dk = c->dk, dv = c->dv;
+    double *qd = (double *)malloc(sizeof(double) * (size_t)dk);
+    double *o = (double *)malloc(sizeof(double) * (size_t)dv);
+    if (!qd || !o) {
+        free(qd);
+        free(o);
+        return ORC_NOMEM;
+    }
+    int rc = ORC_OK;
+    for (int g = 0; g < G && rc == ORC_OK; ++g) {
+        int hq = h * G + g;
+        const uint16_t *qg = q + ((int64_t)r * prm->num_q_heads + hq) * dk;
+        for (int i = 0; i < dk; ++i)
+            qd[i] = orc_bf16_to_f64(qg[i]);
+        double lse;
+        rc = attend(qd, c, pt_row, ntok, tok, h, prm->scale, o, &lse);
+        for (int i = 0; i < dv; ++i)
+            out[((int64_t)r * prm->num_q_heads + hq) * dv + i] = orc_f64_to_bf16(o[i]);
+        lse_out[(int64_t)r * prm->num_q_heads + hq] = lse;
+    }
+    free(qd);
+    free(o);
+    return rc;
+}
+
+/* ------------------------------------------------------------------ */
+/* Step: coarse-to-fine token rescoring                                */
+/* ------------------------------------------------------------------ */
+
+/* f_t = scale_t * sum_g q_g . e4m3(k8_t) for every token of the given
+ * blocks (ascending), written to f / tok (n = nblocks * b entries). */
+static int fine_scores(const uint16_t *q, const orc_cache *c, const int32_t *pt_row,
+                       const orc_params *prm, int r, int h, int64_t nblocks, const int64_t *blocks,
+                       double *f, int64_t *tok)
+{
+    const int b = c->block_size, dk = c->dk;
+    const int G = prm->num_q_heads / c->num_kv_heads;
+    int64_t n = 0;
+    for (int64_t u = 0; u < nblocks; ++u) {
+        int64_t j = blocks[u];
+        int64_t p = pt_row[j];
+        if (p < 0 || p >= c->num_pages)
+            return ORC_BAD_PAGE;
+        for (int t = 0; t < b; ++t) {
+            int64_t base = ((int64_t)p * c->num_kv_heads + h) * b + t;
+            double s = 0.0;
+            for (int g = 0; g < G; ++g) {
+                const uint16_t *qg = q + ((int64_t)r * prm->num_q_heads + h * G + g) * dk;
+                for (int i = 0; i < dk; ++i)
+                    s += orc_bf16_to_f64(qg[i]) * orc_e4m3_to_f64(c->k8[base * dk + i]);
+            }
+            f[n] = (double)c->k8_scale[base] * s;
+            tok[n] = j * b + t;
+            ++n;
+        }
+    }
+    return ORC_OK;
+}
+
+int orc_fine_scores(const uint16_t *q, const orc_cache *idx, const int32_t *pt,
+                    const orc_params *prm, int r, int h, int64_t nblocks, const int64_t *blocks,
+                    double *f, int64_t *tok)
+{
+    return fine_scores(q, idx, pt + (int64_t)r * prm->max_blocks, prm, r, h, nblocks, blocks, f, tok);
+}
+
+/* ------------------------------------------------------------------ */
+/* The decode step                                                     */
+/* ------------------------------------------------------------------ */
+
+/* One (request, KV head) unit: forced ranges, candidates, scores,
+ * selection, token set, attention. */
+static int decode_unit(const uint16_t *q, const orc_cache *c, const uint16_t *summ,
+                       const orc_cache *ic, const uint16_t *isumm, const int32_t *pt,
+                       const int32_t *lens, const orc_params *prm, int r, int h,
+                       uint16_t *out, double *lse, int32_t *sel, int32_t *cand)
+{
+    const int b = c->block_size;
+    const int64_t L = lens[r];
+    const int32_t *pt_row = pt + (int64_t)r * prm->max_blocks;
+    const int c2f = prm->c2f_candidates > 0;
+    const int64_t ksel = c2f ? prm->c2f_tokens : prm->k_blocks;
+    int64_t se, rs;
+    forced_ranges(L, prm->sink, prm->recent, &se, &rs);
+
+    double *scores = (double *)malloc(sizeof(double) * (size_t)(prm->max_blocks > 0 ? prm->max_blocks : 1));
+    int64_t *chosen = (int64_t *)malloc(sizeof(int64_t) * (size_t)(ksel > 0 ? ksel : 1));
+    int64_t cap = se + (L - rs) + (c2f ? prm->c2f_tokens : (int64_t)prm->k_blocks * b);
+    int64_t *tok = (int64_t *)malloc(sizeof(int64_t) * (size_t)(cap > 0 ? cap : 1));
+    int rc = ORC_OK;
+    if (!scores || !chosen || !tok) {
+        rc = ORC_NOMEM;
+        goto done;
+    }
+
+    int64_t nchosen = 0;
+    if (!c2f) {
+        rc = row_scores(q, c, 0, summ, pt, L, prm, r, h, scores);
+        if (rc)
+            goto done;
+        nchosen = select_topk(scores, NULL, prm->max_blocks, ksel, chosen);
+    } else {
+        /* coarse: top-C blocks over summaries of the dequantised index keys */
+        int64_t C = prm->c2f_candidates;
+        int64_t *cb = (int64_t *)malloc(sizeof(int64_t) * (size_t)C);
+        if (!cb) {
+            rc = ORC_NOMEM;
+            goto done;
+        }
+        rc = row_scores(q, ic, 1, isumm, pt, L, prm, r, h, scores);
+        if (rc) {
+            free(cb);
+            goto done;
+        }
+        int64_t ncb = select_topk(scores, NULL, prm->max_blocks, C, cb);
+        if (cand)
+            for (int64_t i = 0; i < C; ++i)
+                cand[((int64_t)r * c->num_kv_heads + h) * C + i] = (int32_t)cb[i];
+        /* fine: exact FP8 rescoring of every token of the C blocks */
+        double *f = (double *)malloc(sizeof(double) * (size_t)(ncb * b > 0 ? ncb * b : 1));
+        int64_t *ft = (int64_t *)malloc(sizeof(int64_t) * (size_t)(ncb * b > 0 ? ncb * b : 1));
+        if (!f || !ft) {
+            free(cb);
+            free(f);
+            free(ft);
+            rc = ORC_NOMEM;
+            goto done;
+        }
+        rc = fine_scores(q, ic, pt_row, prm, r, h, ncb, cb, f, ft);
+        if (rc == ORC_OK)
+            nchosen = select_topk(f, ft, ncb * b, ksel, chosen);
+        free(cb);
+        free(f);
+        free(ft);
+        if (rc)
+            goto done;
+    }
+    if (sel)
+        for (int64_t i = 0; i < ksel; ++i)
+            sel[((int64_t)r * c->num_kv_heads + h) * ksel + i] = (int32_t)chosen[i];
+
+    /* token set T = F U selected, ascending */
+    int64_t ntok = 0;
+    for (int64_t t = 0; t < se; ++t)
+        tok[ntok++] = t;
+    for (int64_t i = 0; i < nchosen; ++i) {
+        if (c2f) {
+            tok[ntok++] = chosen[i];
+        } else {
+            for (int t = 0; t < b; ++t)
+                tok[ntok++] = chosen[i] * b + t;
+        }
+    }
+    for (int64_t t = rs; t < L; ++t)
+        tok[ntok++] = t;
+
+    rc = attend_group(q, c, pt_row, prm, r, h, ntok, tok, out, lse);
+done:
+    free(scores);
+    free(chosen);
+    free(tok);
+    return rc;
+}
+
+/* The whole decode step for every (request, KV head).
+ *   out  [B, Hq, dv] bf16 bits;  lse [B, Hq] double (natural log)
+ *   sel  [B, Hkv, ksel]: selected block indices (single stage, ksel =
+ *        k_blocks) or token positions (coarse-to-fine, ksel = c2f_tokens),
+ *        ascending, -1 padded.  May be NULL.
+ *   cand [B, Hkv, c2f_candidates] coarse blocks (coarse-to-fine only, may be NULL)
+ *   summ / isumm: precomputed summaries (bf16 bits, [P, Hkv, dk]) of the
+ *        attention keys / index keys, or NULL to compute them from the keys.
+ * nthreads > 1 runs units in parallel when built with OpenMP. */
+int orc_decode(const uint16_t *q, const orc_cache *c, const uint16_t *summ,
+               const orc_cache *ic, const uint16_t *isumm, const int32_t *pt,
+               const int32_t *lens, const orc_params *prm, int nthreads,
+               uint16_t *out, double *lse, int32_t *sel, int32_t *cand)
+{
+    if (prm->num_q_heads % c->num_kv_heads != 0)
+        return ORC_BAD_ARG;
+    if (prm->c2f_candidates > 0 && (!ic || !ic->k8 || !ic->k8_scale))
+        return ORC_BAD_ARG;
+    const int64_t units = (int64_t)prm->batch * c->num_kv_heads;
+    int rc = ORC_OK;
+    (void)nthreads;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads > 0 ? nthreads : 1)
+#endif
+    for (int64_t u = 0; u < units; ++u) {
+        int r = (int)(u / c->num_kv_heads), h = (int)(u % c->num_kv_heads);
+        int e = decode_unit(q, c, summ, ic, isumm, pt, lens, prm, r, h, out, lse, sel, cand);
+        if (e) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+            rc = e;
+        }
+    }
+    return rc;
+}
+
+/* Dense attention over [0, L) for every query head (tests only). */
+int orc_dense(const uint16_t *q, const orc_cache *c, const int32_t *pt, const int32_t *lens,
+              const orc_params *prm, uint16_t *out, double *lse)
+{
+    for (int r = 0; r < prm->batch; ++r) {
+        int64_t L = lens[r];
+        int64_t *tok = (int64_t *)malloc(sizeof(int64_t) * (size_t)(L > 0 ? L : 1));
+        if (!tok)
+            return ORC_NOMEM;
+        for (int64_t t = 0; t < L; ++t)
+            tok[t] = t;
+        for (int h = 0; h < c->num_kv_heads; ++h) {
+            int rc = attend_group(q, c, pt + (int64_t)r * prm->max_blocks, prm, r, h, L, tok, out, lse);
+            if (rc) {
+                free(tok);
+                return rc;
+            }
+        }
+        free(tok);
+    }
+    return ORC_OK;
+}
+
+/* Attention of one query head (fp64 query) over an explicit token list of
+ * request r, KV head h; o: [dv] doubles. */
+int orc_attend_tokens(const double *qd, const orc_cache *c, const int32_t *pt_row, int64_t ntok,
+                      const int64_t *tok, int h, double scale, double *o, double *lse)
+{
+    return attend(qd, c, pt_row, ntok, tok, h, scale, o, lse);
+}
+
+/* Log-sum-exp merge of partial results over a partition of the token set:
+ * part s has normalised output o_s and log-sum-exp lse_s; the union has
+ * weights exp(lse_s - M) with M the largest lse_s.  Empty parts (lse = -inf)
+ * contribute nothing; all parts empty gives o = 0, lse = -inf. */
+void orc_lse_merge(int nparts, int dv, const double *o, const double *lse,
+                   double *o_out, double *lse_out)
+{
+    double M = -INFINITY;
+    for (int s = 0; s < nparts; ++s)
+        if (lse[s] > M)
+            M = lse[s];
+    for (int i = 0; i < dv; ++i)
+        o_out[i] = 0.0;
+    if (M == -INFINITY) {
+        *lse_out = -INFINITY;
+        return;
+    }
+    double wsum = 0.0;
+    for (int s = 0; s < nparts; ++s) {
+        if (lse[s] == -INFINITY)
+            continue;
+        double w = exp(lse[s] - M);
+        wsum += w;
+        for (int i = 0; i < dv; ++i)
+            o_out[i] += w * o[(int64_t)s * dv + i];
+    }
+    for (int i = 0; i < dv; ++i)
+        o_out[i] /= wsum;
+    *lse_out = M + log(wsum);
+}

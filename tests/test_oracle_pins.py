@@ -1,0 +1,490 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics
+fix, independent of the oracle's own code.
+
+  * number formats: torch's IEEE conversions and hand-worked closed forms;
+  * the pages' worked examples (golden fixtures with citations);
+  * brute force on tiny inputs with numpy (dense softmax attention, full
+    argsort selection, einsum scores);
+  * invariants: top-k covering every block equals dense attention; the
+    selected set equals the first k of the stable argsort of the scores;
+    log-sum-exp merge over any partition equals one pass; page permutation
+    and page sharing do not change results; a constant V gives that V; the
+    coarse block score is the mean of the fine token scores (linearity).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import WORKLOADS, make_inputs, small_workloads
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def f64(bits):
+    return oracle.bf16_bits_to_f64(bits)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+# ---------------------------------------------------------------- formats
+
+def test_bf16_round_matches_torch_on_float_values():
+    g = torch.Generator().manual_seed(5)
+    x = torch.cat([
+        torch.randn(20000, generator=g),
+        torch.randn(2000, generator=g) * 1e-39,      # subnormal range
+        torch.randn(2000, generator=g) * 1e37,
+        torch.tensor([0.0, -0.0, 3.3895313892515355e38, -3.3895313892515355e38]),
+    ]).to(torch.float32)
+    want = bf16_bits(x.to(torch.bfloat16))
+    got = np.array([oracle.bf16_round(float(v)) for v in x.tolist()], dtype=np.uint16)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("x,bits", [
+    (1.0 + 2.0 ** -8, 0x3F80),                 # tie -> even (down)
+    (1.0 + 3 * 2.0 ** -8, 0x3F82),             # tie -> even (up)
+    (1.0 + 2.0 ** -8 + 2.0 ** -40, 0x3F81),    # above the tie: single rounding
+    (-(1.0 + 2.0 ** -8 + 2.0 ** -40), 0xBF81),
+    (2.0 ** -133, 0x0001),                     # smallest subnormal
+    (2.0 ** -134, 0x0000),                     # tie between 0 and 2^-133 -> even
+    (1.5 * 2.0 ** -133, 0x0002),               # tie -> even (up)
+    ((2.0 - 2.0 ** -8) * 2.0 ** 127, 0x7F80),  # tie above the largest finite -> inf
+    ((2.0 - 2.0 ** -7) * 2.0 ** 127, 0x7F7F),  # largest finite
+    (float("inf"), 0x7F80),
+    (-float("inf"), 0xFF80),
+])
+def test_bf16_round_closed_forms(x, bits):
+    assert oracle.bf16_round(x) == bits
+
+
+def test_e4m3_decode_matches_torch_all_codes():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float32).numpy().astype(np.float64)
+    got = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert np.array_equal(ref[~nan], got[~nan])
+    # OCP E4M3: max normal 448, min normal 2^-6, min subnormal 2^-9, one = 0x38
+    assert oracle.e4m3_decode(0x7E) == 448.0
+    assert oracle.e4m3_decode(0x08) == 2.0 ** -6
+    assert oracle.e4m3_decode(0x01) == 2.0 ** -9
+    assert oracle.e4m3_decode(0x38) == 1.0
+    assert oracle.e4m3_decode(0xB8) == -1.0
+    assert math.isnan(oracle.e4m3_decode(0x7F))
+
+
+# ---------------------------------------------------------------- helpers
+
+def tiny_inputs(**kw):
+    w = WORKLOADS["tiny"].replace(**kw) if kw else WORKLOADS["tiny"]
+    return w, make_inputs(w, "cpu")
+
+
+def cache_of(inp, w):
+    return oracle.Cache(inp["k_cache"], inp["v_cache"],
+                        k8=inp.get("idx_keys"), k8_scale=inp.get("idx_scale"))
+
+
+def np_dense(inp, w, r, hq, tokens=None):
+    """Brute-force softmax attention (numpy fp64) of query head hq of
+    request r over `tokens` (default: every token)."""
+    b = w.block_size
+    L = int(inp["lens"][r])
+    toks = np.arange(L) if tokens is None else np.asarray(tokens)
+    h = hq // w.group
+    pt = inp["page_table"][r].numpy()
+    K = f64(bf16_bits(inp["k_cache"][:, h]))      # [P, b, dk]
+    V = f64(bf16_bits(inp["v_cache"][:, h].contiguous()))
+    pages = pt[toks // b]
+    Kt = K[pages, toks % b]                        # [n, dk]
+    Vt = V[pages, toks % b]
+    q = f64(bf16_bits(inp["q"][r, hq]))
+    z = w.softmax_scale * (Kt @ q)
+    m = z.max()
+    p = np.exp(z - m)
+    return (p @ Vt) / p.sum(), m + math.log(p.sum())
+
+
+def assert_correctly_rounded(out_bits, exact):
+    """Every bf16 output is a correct rounding of the fp64 value: within
+    half a bf16 ulp (plus fp64 noise)."""
+    got = f64(out_bits)
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(exact), 2.0 ** -126))) - 7)
+    assert np.all(np.abs(got - exact) <= 0.5 * ulp * (1 + 1e-9) + 1e-300)
+
+
+# ---------------------------------------------------------------- summaries
+
+def test_summary_closed_forms():
+    # keys of one block: x + d_t with sum_t d_t = 0  ->  mean = x exactly
+    b, dk = 16, 8
+    x = torch.tensor([1.5, -2.25, 0.0078125, 3.0, -0.5, 7.0, 1.0, -1.0])
+    d = torch.linspace(-1, 1, b // 2).repeat_interleave(1)
+    d = torch.cat([d, -d])
+    k = (x[None, :] + d[:, None] * 0.25).to(torch.bfloat16).view(1, 1, b, dk)
+    # the perturbations are symmetric and exactly representable
+    assert torch.equal(k.float().mean(dim=2)[0, 0].to(torch.bfloat16).float(), x)
+    c = oracle.Cache(k, k)
+    s, valid = oracle.summaries(c, np.array([[0]], np.int32), np.array([16], np.int32))
+    assert valid[0]
+    assert np.array_equal(f64(s[0, 0]), x.numpy().astype(np.float64))
+
+
+def test_summaries_vs_torch_when_mean_is_float_exact():
+    # bf16 keys with one exponent (|x| in [1, 2)): the sum of 16 needs at
+    # most 12 significant bits, so torch's fp32 mean is exact and its bf16
+    # cast is a single correct rounding.
+    g = torch.Generator().manual_seed(3)
+    P, H, b, dk = 5, 2, 16, 32
+    mag = 1.0 + torch.rand((P, H, b, dk), generator=g)
+    sign = torch.where(torch.rand((P, H, b, dk), generator=g) < 0.5, -1.0, 1.0)
+    k = (mag * sign).to(torch.bfloat16)
+    c = oracle.Cache(k, k)
+    pt = np.array([[0, 1, 2], [3, 4, -1]], np.int32)
+    lens = np.array([48, 33], np.int32)
+    s, valid = oracle.summaries(c, pt, lens)
+    want = bf16_bits(k.float().mean(dim=2).to(torch.bfloat16))
+    assert valid.tolist() == [True, True, True, True, True]  # page 4 has a full block (33 >= 32)
+    assert np.array_equal(s, want)
+
+
+def test_summaries_correctly_rounded_random():
+    w, inp = tiny_inputs()
+    c = cache_of(inp, w)
+    s, valid = oracle.summaries(c, inp["page_table"], inp["seq_lens"])
+    K = f64(bf16_bits(inp["k_cache"]))                # [P, H, b, dk]
+    exact = K.mean(axis=2)                              # fp64, exact for 16 addends here
+    assert valid.all()
+    assert_correctly_rounded(s, exact)
+
+
+def test_summaries_only_full_blocks():
+    w, inp = tiny_inputs()
+    c = cache_of(inp, w)
+    lens = np.array([1000], np.int32)                   # 62 full blocks, tail of 8
+    s, valid = oracle.summaries(c, inp["page_table"], lens)
+    assert valid[:62].all() and not valid[62:].any()
+
+
+# ---------------------------------------------------------------- scores + top-k
+
+def test_topk_vortex_figure1_golden():
+    gold = json.load(open(os.path.join(GOLD, "vortex_fig1_block_topk.json")))
+    got = oracle.topk(np.array([gold["scores"]]), gold["k"])[0]
+    assert got.tolist() == gold["selected_ascending"]
+
+
+def test_topk_bruteforce_with_ties():
+    rng = np.random.default_rng(7)
+    for n, k in [(1, 1), (5, 3), (64, 8), (300, 62), (1000, 1), (10, 20)]:
+        s = rng.integers(-5, 5, size=n).astype(np.float64)     # many exact ties
+        s[rng.random(n) < 0.1] = -np.inf                       # non-candidates
+        order = np.lexsort((np.arange(n), -s))                 # score desc, index asc
+        fin = [j for j in order if np.isfinite(s[j])][:k]
+        want = sorted(fin) + [-1] * (k - len(fin))
+        assert oracle.topk(s[None], k)[0].tolist() == want
+
+
+def test_topk_negative_zero_ties_lower_index():
+    s = np.array([[-0.0, 0.0, -0.0, -1.0]])
+    assert oracle.topk(s, 2)[0].tolist() == [0, 1]
+
+
+def test_block_scores_bruteforce_and_candidates():
+    w, inp = tiny_inputs()
+    c = cache_of(inp, w)
+    summ, _ = oracle.summaries(c, inp["page_table"], inp["seq_lens"])
+    sc = oracle.block_scores(inp["q"], c, summ, inp["page_table"], inp["seq_lens"],
+                             w.num_q_heads, w.sink, w.recent)
+    S = f64(summ)[:, 0]                                  # [P, dk] (Hkv = 1)
+    qs = f64(bf16_bits(inp["q"][0])).sum(axis=0)        # sum over the 4-head group
+    want = S[inp["page_table"][0].numpy()] @ qs
+    # sink 16 + recent 16 tokens, block 16: blocks 0 and 63 are forced
+    assert np.isneginf(sc[0, 0, 0]) and np.isneginf(sc[0, 0, 63])
+    assert np.allclose(sc[0, 0, 1:63], want[1:63], rtol=1e-12, atol=1e-12)
+    # summaries computed from the keys on the fly give the same scores
+    sc2 = oracle.block_scores(inp["q"], c, None, inp["page_table"], inp["seq_lens"],
+                              w.num_q_heads, w.sink, w.recent)
+    assert np.array_equal(sc, sc2)
+
+
+def test_candidate_rule_ragged_forced_ranges():
+    # block 64, sink 4, recent 512 and L = 1000: blocks touching [0,4) or
+    # [488,1000) are forced; full blocks 1..6 are candidates (block 7 = 448..511
+    # touches the recent range, block 15 is the partial tail).
+    w = WORKLOADS["ragged"].replace(batch=1, seq_len_range=None, seq_lens=(1000,), name="x")
+    inp = make_inputs(w, "cpu")
+    c = cache_of(inp, w)
+    sc = oracle.block_scores(inp["q"], c, None, inp["page_table"], inp["seq_lens"],
+                             w.num_q_heads, w.sink, w.recent)
+    finite = np.isfinite(sc[0, 0])
+    assert np.flatnonzero(finite).tolist() == [1, 2, 3, 4, 5, 6]
+
+
+# ---------------------------------------------------------------- attention
+
+def test_decode_tiny_bruteforce_numpy():
+    w, inp = tiny_inputs()
+    c = cache_of(inp, w)
+    res = oracle.decode(inp["q"], c, inp["page_table"], inp["seq_lens"],
+                        num_q_heads=w.num_q_heads, k_blocks=w.k_blocks, sink=w.sink,
+                        recent=w.recent, scale=w.softmax_scale)
+    # selection = first k of the stable argsort of the scores
+    sc = oracle.block_scores(inp["q"], c, None, inp["page_table"], inp["seq_lens"],
+                             w.num_q_heads, w.sink, w.recent)[0, 0]
+    cand = np.flatnonzero(np.isfinite(sc))
+    order = cand[np.lexsort((cand, -sc[cand]))]
+    sel = sorted(order[: w.k_blocks].tolist())
+    assert res["sel"][0, 0].tolist() == sel
+    toks = list(range(16)) + [t for j in sel for t in range(j * 16, j * 16 + 16)] + \
+        list(range(1024 - 16, 1024))
+    for hq in range(w.num_q_heads):
+        o, lse = np_dense(inp, w, 0, hq, toks)
+        assert_correctly_rounded(res["out"][0, hq], o)
+        assert abs(res["lse"][0, hq] - lse) < 1e-10
+
+
+def test_dense_bruteforce_numpy():
+    w, inp = tiny_inputs()
+    c = cache_of(inp, w)
+    d = oracle.dense(inp["q"], c, inp["page_table"], inp["seq_lens"],
+                     num_q_heads=w.num_q_heads, scale=w.softmax_scale)
+    for hq in range(w.num_q_heads):
+        o, lse = np_dense(inp, w, 0, hq)
+        assert_correctly_rounded(d["out"][0, hq], o)
+        assert abs(d["lse"][0, hq] - lse) < 1e-10
+
+
+@pytest.mark.parametrize("name,lens", [
+    ("tiny", (1024,)), ("b16_small", (4105, 3001, 777)), ("ragged_small", (4100, 900, 68, 4996, 2500)),
+    ("mla_small", (3000, 1080))])
+def test_topk_covering_all_blocks_equals_dense(name, lens):
+    """With block-aligned forced ranges and k at least the number of
+    candidates, the token set is every token: sparse equals dense."""
+    w = small_workloads()[name]
+    b = w.block_size
+    resid = {L % b for L in lens}
+    assert len(resid) == 1
+    recent = resid.pop() + b          # L - recent is a block boundary for every request
+    w = w.replace(k_blocks=100000, seq_lens=lens, seq_len_range=None, batch=len(lens),
+                  sink=b, recent=recent)
+    inp = make_inputs(w, "cpu")
+    c = cache_of(inp, w)
+    res = oracle.decode(inp["q"], c, inp["page_table"], inp["seq_lens"],
+                        num_q_heads=w.num_q_heads, k_blocks=w.k_blocks, sink=w.sink,
+                        recent=w.recent, scale=w.softmax_scale)
+    d = oracle.dense(inp["q"], c, inp["page_table"], inp["seq_lens"],
+                     num_q_heads=w.num_q_heads, scale=w.softmax_scale)
+    # same token set, different summation order: fp64 results agree to
+    # ~1e-15, so the bf16 outputs are equal except at a rounding tie
+    diff = np.abs(f64(res["out"]) - f64(d["out"]))
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(f64(d["out"])), 2.0 ** -126))) - 7)
+    assert np.all(diff <= ulp)
+    assert np.mean(res["out"] == d["out"]) > 0.999
+    assert np.allclose(res["lse"], d["lse"], atol=1e-9)
+
+
+def test_constant_v_gives_v_and_single_token():
+    w, inp = tiny_inputs()
+    v = torch.zeros_like(inp["v_cache"])
+    vec = torch.randn(w.dv, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    v[:] = vec
+    c = oracle.Cache(inp["k_cache"], v)
+    res = oracle.decode(inp["q"], c, inp["page_table"], inp["seq_lens"],
+                        num_q_heads=w.num_q_heads, k_blocks=w.k_blocks, sink=w.sink,
+                        recent=w.recent, scale=w.softmax_scale)
+    assert np.array_equal(res["out"][0], np.tile(bf16_bits(vec), (w.num_q_heads, 1)))
+    # a single-token cache attends V_0 with lse = scale * q.K_0
+    c1 = cache_of(inp, w)
+    one = oracle.decode(inp["q"], c1, inp["page_table"], np.array([1], np.int32),
+                        num_q_heads=w.num_q_heads, k_blocks=w.k_blocks, sink=w.sink,
+                        recent=w.recent, scale=w.softmax_scale)
+    v0 = bf16_bits(inp["v_cache"][0, 0, 0])
+    assert np.array_equal(one["out"][0], np.tile(v0, (w.num_q_heads, 1)))
+    q = f64(bf16_bits(inp["q"][0]))
+    k0 = f64(bf16_bits(inp["k_cache"][0, 0, 0]))
+    assert np.allclose(one["lse"][0], w.softmax_scale * (q @ k0), atol=1e-12)
+
+
+def test_empty_request():
+    w, inp = tiny_inputs()
+    c = cache_of(inp, w)
+    res = oracle.decode(inp["q"], c, inp["page_table"], np.array([0], np.int32),
+                        num_q_heads=w.num_q_heads, k_blocks=w.k_blocks, sink=w.sink,
+                        recent=w.recent, scale=w.softmax_scale)
+    assert np.all(res["out"] == 0) and np.all(np.isneginf(res["lse"]))
+    assert np.all(res["sel"] == -1)
+
+
+def test_short_request_all_forced_equals_dense():
+    w, inp = tiny_inputs()
+    c = cache_of(inp, w)
+    lens = np.array([25], np.int32)      # L < sink + recent: every token forced
+    res = oracle.decode(inp["q"], c, inp["page_table"], lens, num_q_heads=w.num_q_heads,
+                        k_blocks=w.k_blocks, sink=w.sink, recent=w.recent, scale=w.softmax_scale)
+    d = oracle.dense(inp["q"], c, inp["page_table"], lens, num_q_heads=w.num_q_heads,
+                     scale=w.softmax_scale)
+    assert np.array_equal(res["out"], d["out"])
+    assert np.all(res["sel"] == -1)
+
+
+def test_lse_merge_any_partition_equals_one_pass():
+    w, inp = tiny_inputs()
+    c = cache_of(inp, w)
+    rng = np.random.default_rng(0)
+    q = f64(bf16_bits(inp["q"][0, 2]))
+    toks = np.sort(rng.choice(1024, size=300, replace=False))
+    ptr = inp["page_table"][0]
+    o_all, l_all = oracle.attend_tokens(q, c, ptr, toks, 0, w.softmax_scale)
+    for nparts in (1, 2, 5, 17):
+        cuts = np.sort(rng.choice(np.arange(1, 300), size=nparts - 1, replace=False))
+        parts = np.split(toks, cuts)
+        os_, ls_ = zip(*[oracle.attend_tokens(q, c, ptr, p, 0, w.softmax_scale) for p in parts])
+        o, l = oracle.lse_merge(np.stack(os_), np.array(ls_))
+        assert np.allclose(o, o_all, rtol=1e-12, atol=1e-14)
+        assert abs(l - l_all) < 1e-12
+    # an empty part changes nothing
+    o, l = oracle.lse_merge(np.stack([o_all, np.zeros_like(o_all)]), np.array([l_all, -np.inf]))
+    assert np.allclose(o, o_all) and abs(l - l_all) < 1e-14
+
+
+# ---------------------------------------------------------------- paging
+
+def test_page_permutation_invariance():
+    w = small_workloads()["b16_small"]
+    inp = make_inputs(w, "cpu")
+    c = cache_of(inp, w)
+    args = dict(num_q_heads=w.num_q_heads, k_blocks=w.k_blocks, sink=w.sink, recent=w.recent,
+                scale=w.softmax_scale)
+    a = oracle.decode(inp["q"], c, inp["page_table"], inp["seq_lens"], **args)
+    P = inp["num_pages"]
+    perm = torch.randperm(P, generator=torch.Generator().manual_seed(9))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(P)
+    k2 = inp["k_cache"][perm]               # new page i holds old page perm[i]
+    v2 = inp["v_cache"][perm]
+    pt2 = inp["page_table"].clone()
+    m = pt2 >= 0
+    pt2[m] = inv[pt2[m].long()].to(torch.int32)
+    b = oracle.decode(inp["q"], oracle.Cache(k2, v2), pt2, inp["seq_lens"], **args)
+    for key in ("out", "lse", "sel"):
+        assert np.array_equal(a[key], b[key])
+
+
+def test_vortex_figure2_shared_pages():
+    gold = json.load(open(os.path.join(GOLD, "vortex_fig2_paged_layout.json")))
+    P, H, b, d, Hq = gold["num_pages"], 2, 16, 32, 4
+    g = torch.Generator().manual_seed(21)
+    k = torch.randn((P, H, b, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((P, H, b, d), generator=g).to(torch.bfloat16)
+    q = torch.randn((3, Hq, d), generator=g).to(torch.bfloat16)
+    pt = np.array([gold["page_tables"][x] for x in ("x0", "x1", "x2")], np.int32)
+    lens = np.array([48, 40, 47], np.int32)
+    args = dict(num_q_heads=Hq, k_blocks=1, sink=1, recent=9, scale=0.2)
+    shared = oracle.decode(q, oracle.Cache(k, v), pt, lens, **args)
+    s_shared, _ = oracle.summaries(oracle.Cache(k, v), pt, lens)
+    for r in range(3):
+        # private copy of request r's pages
+        kp, vp = k[pt[r].tolist()], v[pt[r].tolist()]
+        one = oracle.decode(q[r:r + 1], oracle.Cache(kp, vp), np.arange(3, dtype=np.int32)[None],
+                            lens[r:r + 1], **args)
+        assert np.array_equal(shared["out"][r], one["out"][0])
+        assert np.array_equal(shared["sel"][r], one["sel"][0])
+    # a shared page's summary is one value whoever references it
+    s_priv, _ = oracle.summaries(oracle.Cache(k[[0, 3, 5]], v[[0, 3, 5]]),
+                                 np.array([[0, 1, 2]], np.int32), np.array([48], np.int32))
+    assert np.array_equal(s_shared[[0, 3, 5]], s_priv)
+
+
+# ---------------------------------------------------------------- coarse-to-fine
+
+def c2f_setup(**kw):
+    w = small_workloads()["c2f_small"].replace(**kw)
+    inp = make_inputs(w, "cpu")
+    ic = oracle.Cache(None, None, k8=inp["idx_keys"], k8_scale=inp["idx_scale"])
+    return w, inp, cache_of(inp, w), ic
+
+
+def test_c2f_coarse_score_is_mean_of_fine_scores():
+    w, inp, c, ic = c2f_setup()
+    isumm, _ = oracle.summaries(ic, inp["page_table"], inp["seq_lens"], use_index_keys=True)
+    sc = oracle.block_scores(inp["q"], ic, isumm, inp["page_table"], inp["seq_lens"],
+                             w.num_q_heads, w.sink, w.recent, use_index_keys=True)
+    qsum = f64(bf16_bits(inp["q"][0])).sum(axis=0)
+    blocks = np.flatnonzero(np.isfinite(sc[0, 0]))[:40]
+    f, t = oracle.fine_scores(inp["q"], ic, inp["page_table"], w.num_q_heads, 0, 0, blocks)
+    fm = f.reshape(len(blocks), w.block_size).mean(axis=1)
+    # difference only from rounding the mean key to bf16 (half an ulp per element)
+    S = f64(isumm[inp["page_table"][0].numpy()[blocks], 0])
+    bound = (np.abs(qsum)[None, :] * np.abs(S) * 2.0 ** -8).sum(axis=1) + 1e-9
+    assert np.all(np.abs(sc[0, 0, blocks] - fm) <= bound)
+    # and the fine scores are the dequantised dot products
+    k8 = inp["idx_keys"].view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    sca = inp["idx_scale"].numpy().astype(np.float64)
+    pg = inp["page_table"][0].numpy()[blocks]
+    want = (k8[pg, 0] * sca[pg, 0][..., None]) @ qsum
+    assert np.allclose(f, want.reshape(-1), rtol=1e-12, atol=1e-12)
+
+
+def test_c2f_fine_tokens_inside_coarse_candidates():
+    w, inp, c, ic = c2f_setup()
+    res = oracle.decode(inp["q"], c, inp["page_table"], inp["seq_lens"],
+                        num_q_heads=w.num_q_heads, k_blocks=0, sink=w.sink, recent=w.recent,
+                        scale=w.softmax_scale, index_cache=ic, c2f_candidates=w.c2f_candidates,
+                        c2f_tokens=w.c2f_tokens)
+    for r in range(w.batch):
+        cand = set(res["cand"][r, 0][res["cand"][r, 0] >= 0].tolist())
+        toks = res["sel"][r, 0][res["sel"][r, 0] >= 0]
+        assert len(toks) == min(w.c2f_tokens, len(cand) * w.block_size)
+        assert all((t // w.block_size) in cand for t in toks.tolist())
+        assert np.all(np.diff(toks) > 0)
+
+
+def test_c2f_all_blocks_is_exact_token_topk():
+    w, inp, c, ic = c2f_setup(seq_lens=(2000, 1500), recent=0, c2f_candidates=1000,
+                              c2f_tokens=300)
+    res = oracle.decode(inp["q"], c, inp["page_table"], inp["seq_lens"],
+                        num_q_heads=w.num_q_heads, k_blocks=0, sink=0, recent=0,
+                        scale=w.softmax_scale, index_cache=ic, c2f_candidates=w.c2f_candidates,
+                        c2f_tokens=w.c2f_tokens)
+    k8 = inp["idx_keys"].view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    sca = inp["idx_scale"].numpy().astype(np.float64)
+    b = w.block_size
+    for r in range(w.batch):
+        L = inp["lens"][r]
+        nfull = L // b
+        toks = np.arange(nfull * b)
+        pg = inp["page_table"][r].numpy()[toks // b]
+        qsum = f64(bf16_bits(inp["q"][r])).sum(axis=0)
+        f = (k8[pg, 0, toks % b] * sca[pg, 0, toks % b][:, None]) @ qsum
+        order = np.lexsort((toks, -f))
+        want = np.sort(toks[order[: w.c2f_tokens]])
+        assert np.array_equal(res["sel"][r, 0], want)
+        for hq in (0, 63):
+            o, lse = np_dense(inp, w, r, hq, want)
+            assert_correctly_rounded(res["out"][r, hq], o)
+
+
+# ---------------------------------------------------------------- latent cache
+
+def test_mla_aliased_v_equals_copied_v():
+    w = small_workloads()["mla_small"].replace(seq_lens=(3000, 1100))
+    inp = make_inputs(w, "cpu")
+    assert inp["v_cache"].data_ptr() == inp["k_cache"].data_ptr()
+    c_alias = oracle.Cache(inp["k_cache"], None, dv=w.dv)
+    c_copy = oracle.Cache(inp["k_cache"], inp["k_cache"][..., : w.dv].clone())
+    args = dict(num_q_heads=w.num_q_heads, k_blocks=w.k_blocks, sink=w.sink, recent=w.recent,
+                scale=w.softmax_scale)
+    a = oracle.decode(inp["q"], c_alias, inp["page_table"], inp["seq_lens"], **args)
+    b = oracle.decode(inp["q"], c_copy, inp["page_table"], inp["seq_lens"], **args)
+    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["sel"], b["sel"])
+    o, lse = np_dense(inp, w, 1, 5, tokens=None)  # spot-check the dense path shape
+    assert o.shape == (w.dv,)
