@@ -1,0 +1,437 @@
+#!/usr/bin/env python
+"""Benchmark of the block-sparse decode step (lsa_decode_step) on GB300.
+
+One step = one lsa_decode_step call over one batch of synthetic input: block
+scores against the mean-key summaries, per-(request, KV head) top-k with the
+sink / recent tokens forced, split-K attention over the selected blocks and
+the log-sum-exp merge.  The metric is decode-step calls/s on the B=16 x 32K
+workload (also reported: tokens/s = B x calls/s and achieved HBM GB/s of the
+algorithmic bytes: candidate summaries + forced/selected K/V + page table +
+q/out).
+
+Timing: W warm-up steps, an untimed soak under load, then exactly K steps
+replayed from CUDA graphs, bracketed by a barrier and a device synchronise,
+timed with CUDA events on the launching stream.  L2 stays cold: the steps
+rotate over R independent instances whose combined working set is several
+times the 129 MB L2 (config key "l2").  Under torchrun each rank runs an
+independent replica (the step has no cross-request exchange); the time is the
+max over ranks and the value counts every rank's steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import WORKLOADS, algorithmic_bytes, make_inputs  # noqa: E402
+
+METRIC = "sparse decode-step calls/s and achieved HBM GB/s vs GB300 peak (B=16, 32K)"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the GPU is loaded."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+class Instance:
+    def __init__(self, w, seed_offset, dev):
+        import sparse_attention_decode_block_gb300 as L
+        self.w = w.replace(seed=w.seed + 1000 * seed_offset) if seed_offset else w
+        self.g = make_inputs(self.w, dev)
+        g = self.g
+        B, Hkv = w.batch, w.num_kv_heads
+        self.cache = L.make_cache(g["k_cache"], g["v_cache"])
+        self.icache = None
+        self.summ = torch.zeros((g["num_pages"], Hkv, w.dk), dtype=torch.bfloat16, device=dev)
+        if w.c2f_candidates > 0:
+            self.icache = L.make_cache(g["idx_keys"], None, k_scale=g["idx_scale"])
+            L.lsa_build_summaries(self.icache, g["page_table"], g["seq_lens"], self.summ)
+            nsel = w.c2f_tokens
+        else:
+            L.lsa_build_summaries(self.cache, g["page_table"], g["seq_lens"], self.summ)
+            nsel = w.k_blocks
+        self.params = L.make_params(B, w.num_q_heads, g["max_blocks"], w.k_blocks, w.sink, w.recent,
+                                    w.softmax_scale, w.c2f_candidates, w.c2f_tokens)
+        self.ws = torch.empty(max(16, L.lsa_decode_step_workspace_size(self.cache, self.params)),
+                              dtype=torch.uint8, device=dev)
+        self.idx = torch.empty((B, Hkv, max(1, nsel)), dtype=torch.int32, device=dev)
+        self.out = torch.empty((B, w.num_q_heads, w.dv), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((B, w.num_q_heads), dtype=torch.float32, device=dev)
+        self.L = L
+
+    def step(self, q=None, pt=None, lens=None, stream=None):
+        g = self.g
+        self.L.lsa_decode_step(g["q"] if q is None else q, self.cache, self.summ, self.icache,
+                               g["page_table"] if pt is None else pt, g["seq_lens"] if lens is None else lens,
+                               self.params, self.idx, self.out, self.lse, self.ws, stream)
+
+
+
+def kernels_per_step(inst) -> int:
+    import ctypes
+    lib = inst.L.load_library()
+    # score + top-k (+ fine score + fine top-k) + attention (+ merge when split)
+    n = 2 + (2 if inst.w.c2f_candidates > 0 else 0) + 1
+    ws_attn = lib.lsa_sparse_decode_workspace_size(ctypes.byref(inst.cache), ctypes.byref(inst.params))
+    return n + (1 if ws_attn > 0 else 0)
+
+
+def stage_times(inst, reps: int, stream) -> dict:
+    """Average device time of each stage, timed with CUDA events around the
+    stage's entry-point call (score, top-k, attention+merge), cycling L2-cold
+    over the instances."""
+    L, g, w = inst.L, inst.g, inst.w
+    if w.c2f_candidates > 0:
+        return {}
+    B, Hkv = w.batch, w.num_kv_heads
+    scores = torch.empty((B * Hkv, g["max_blocks"]), dtype=torch.float32, device=g["q"].device)
+    idx = torch.empty((B * Hkv, max(1, w.k_blocks)), dtype=torch.int32, device=g["q"].device)
+    ws = torch.empty(max(16, L.lsa_sparse_decode_workspace_size(inst.cache, inst.params)), dtype=torch.uint8,
+                     device=g["q"].device)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=g["q"].device)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    acc = {"score": 0.0, "topk": 0.0, "attention": 0.0}
+    with torch.cuda.stream(stream):
+        for i in range(reps + 2):
+            flush.zero_()
+            ev[0].record(stream)
+            L.lsa_score(g["q"], inst.cache, inst.summ, g["page_table"], g["seq_lens"], inst.params, scores, stream)
+            ev[1].record(stream)
+            L.lsa_topk(scores, None, w.k_blocks, idx, stream)
+            ev[2].record(stream)
+            L.lsa_sparse_decode(g["q"], inst.cache, g["page_table"], g["seq_lens"], idx.view(B, Hkv, -1),
+                                inst.params, inst.out, inst.lse, ws, stream)
+            ev[3].record(stream)
+            stream.synchronize()
+            if i >= 2:
+                acc["score"] += ev[0].elapsed_time(ev[1])
+                acc["topk"] += ev[1].elapsed_time(ev[2])
+                acc["attention"] += ev[2].elapsed_time(ev[3])
+    return {k: v / reps for k, v in acc.items()}
+
+
+def run_gpu(args, rank, world, dev):
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.config]
+    import sparse_attention_decode_block_gb300 as L
+    L.load_library()
+    first = Instance(w, 0, dev)
+    step_bytes = algorithmic_bytes(w, first.g["lens"])["total"]
+    R = max(2, int(np.ceil(4 * L2_BYTES / max(step_bytes, 1))))
+    R = min(R, 8)
+    insts = [first] + [Instance(w, i, dev) for i in range(1, R)]
+    accs = [algorithmic_bytes(w, it.g["lens"]) for it in insts]
+    acc = {k: sum(a[k] for a in accs) // R for k in accs[0]}
+    step_bytes = acc["total"]
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    L.lsa_get_device_status(clear=True)
+
+    # warm-up (eager)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            insts[i % R].step(stream=stream)
+    stream.synchronize()
+    code, flags = L.lsa_get_device_status(clear=True)
+    if code != 0:
+        raise RuntimeError(f"device status after warm-up: {L.lsa_status_string(code)} ({flags:#x})")
+
+    # CUDA graphs of `chunk` steps cycling over the instances
+    chunk = R * max(1, 64 // R)
+
+    def capture(nsteps):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for i in range(nsteps):
+                insts[i % R].step(stream=stream)
+        return gr
+
+    K = args.steps
+    g_full = capture(chunk) if K >= chunk else None
+    rem = K % chunk
+    g_rem = capture(rem) if rem else None
+    n_full = K // chunk
+
+    def replay_k():
+        for _ in range(n_full):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    # soak: keep the GPU under load for ~1 s before the timed region so the
+    # clock samples describe the steady state
+    with torch.cuda.stream(stream):
+        t_end = time.time() + args.soak
+        while time.time() < t_end:
+            (g_full or g_rem).replay()
+            stream.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        replay_k()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    code, flags = L.lsa_get_device_status(clear=True)
+    if code != 0:
+        raise RuntimeError(f"device status after timing: {L.lsa_status_string(code)} ({flags:#x})")
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # per-stage split (separate untimed-for-value pass, L2 flushed before each)
+    st = stage_times(insts[0], 20, stream)
+
+    # end to end through the public call with host buffers: every step copies
+    # q, page table and lengths from pinned host memory and reads back out/lse
+    e2e = e2e_leg(insts, args, stream)
+
+    return dict(ms=ms, step_bytes=step_bytes, acc=acc, R=R, clocks=clocks, stages=st, e2e=e2e,
+                kernels=kernels_per_step(insts[0]), w=w)
+
+
+def e2e_leg(insts, args, stream):
+    inst = insts[0]
+    g = inst.g
+    hq = g["q"].cpu().pin_memory()
+    hpt = g["page_table"].cpu().pin_memory()
+    hl = g["seq_lens"].cpu().pin_memory()
+    hout = torch.empty(inst.out.shape, dtype=inst.out.dtype).pin_memory()
+    hlse = torch.empty(inst.lse.shape, dtype=inst.lse.dtype).pin_memory()
+    dq, dpt, dl = torch.empty_like(g["q"]), torch.empty_like(g["page_table"]), torch.empty_like(g["seq_lens"])
+    n = max(10, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            dq.copy_(hq, non_blocking=True)
+            dpt.copy_(hpt, non_blocking=True)
+            dl.copy_(hl, non_blocking=True)
+            inst.step(dq, dpt, dl, stream)
+            hout.copy_(inst.out, non_blocking=True)
+            hlse.copy_(inst.lse, non_blocking=True)
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            dq.copy_(hq, non_blocking=True)
+            dpt.copy_(hpt, non_blocking=True)
+            dl.copy_(hl, non_blocking=True)
+            inst.step(dq, dpt, dl, stream)
+            hout.copy_(inst.out, non_blocking=True)
+            hlse.copy_(inst.lse, non_blocking=True)
+        e1.record(stream)
+        stream.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    h2d = hq.numel() * hq.element_size() + hpt.numel() * hpt.element_size() + hl.numel() * hl.element_size()
+    d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+    return dict(ms_per_step=ms, h2d=h2d, d2h=d2h, steps=n)
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def cpu_baseline(w, budget_s: float = 15.0):
+    """The oracle as it stands on the host cores, on a bounded sample: whole
+    requests of the workload (all their KV heads), summaries precomputed by
+    the oracle (they are built once per block, outside the step)."""
+    import oracle
+    inp = make_inputs(w.replace(batch=1, seq_lens=None if w.seq_lens is None else w.seq_lens[:1]), "cpu")
+    c = oracle.Cache(inp["k_cache"], inp["v_cache"])
+    kw = dict(num_q_heads=w.num_q_heads, k_blocks=w.k_blocks, sink=w.sink, recent=w.recent,
+              scale=w.softmax_scale)
+    if w.c2f_candidates > 0:
+        ic = oracle.Cache(None, None, k8=inp["idx_keys"], k8_scale=inp["idx_scale"])
+        isumm, _ = oracle.summaries(ic, inp["page_table"], inp["seq_lens"], use_index_keys=True)
+        kw.update(index_cache=ic, index_summ=isumm, c2f_candidates=w.c2f_candidates, c2f_tokens=w.c2f_tokens)
+        summ = None
+    else:
+        summ, _ = oracle.summaries(c, inp["page_table"], inp["seq_lens"])
+    cores = os.cpu_count() or 1
+    n, t0 = 0, time.time()
+    while True:
+        oracle.decode(inp["q"], c, inp["page_table"], inp["seq_lens"], summ=summ, nthreads=cores, **kw)
+        n += 1
+        if time.time() - t0 > budget_s or n >= 5000:
+            break
+    per_req = (time.time() - t0) / n
+    calls = 1.0 / (per_req * w.batch)
+    return {"value": calls, "unit": "calls/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} run(s) of 1 of {w.batch} requests (all {w.num_kv_heads} KV heads), fp64 oracle, "
+                      f"summaries precomputed; calls/s = 1 / ({w.batch} x time per request)"}
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="b16_32k", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="lsa", choices=["lsa", "reference"])
+    ap.add_argument("--soak", type=float, default=1.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = WORKLOADS[args.config]
+
+    if args.impl == "reference":
+        # the reference arm is the CPU oracle; rank 0 alone runs it
+        if rank != 0:
+            return
+        t0 = time.time()
+        cb = cpu_baseline(w, budget_s=20.0)
+        line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "calls/s", "n_gpus": 0,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / cb["value"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": w.name, "description": w.description},
+                "cpu_baseline": cb,
+                "e2e": {"value": cb["value"], "unit": "calls/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "wall_s": round(time.time() - t0, 1)}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    res = run_gpu(args, rank, world, dev)
+    ms_step = res["ms"] / args.steps
+    calls = args.steps * world / (res["ms"] / 1e3)
+    peak, peak_kind = peaks()
+    gbs = res["step_bytes"] / (ms_step / 1e3) / 1e9
+    st = res["stages"]
+    dominant = max(st, key=st.get) if st else None
+    acc = res["acc"]
+    stage_bytes = {"score": acc["summaries"] + acc["page_table"] + acc["q_out"] // 2,
+                   "attention": acc["kv"] + acc["q_out"], "topk": 0}
+    if dominant:
+        ach = stage_bytes[dominant] / (st[dominant] / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "peak_kind": peak_kind, "traffic": None}
+    else:
+        roof = {"bound": "hbm", "kernel": "decode_step", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(gbs / peak, 4), "peak_kind": peak_kind, "traffic": None}
+    cb = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cb = cpu_baseline(res["w"])
+    e2e = res["e2e"]
+    w = res["w"]
+    line = {
+        "metric": METRIC, "value": round(calls, 1), "unit": "calls/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description, "batch": w.batch,
+                   "seq_len": w.seq_len or "ragged", "parallelism": f"replicas x{world}",
+                   "l2": f"cold: {res['R']} rotating instances, {res['R'] * res['step_bytes'] / 2**20:.0f} MiB "
+                         f"touched per rotation vs 129 MB L2"},
+        "tokens_per_s": round(calls * w.batch, 1),
+        "step": {"algorithmic_bytes": res["step_bytes"], "bytes_split": acc, "gbs": round(gbs, 1),
+                 "frac_of_peak": round(gbs / peak, 4), "frac_of_8tbs": round(gbs / 8000.0, 4)},
+        "stages_ms": {k: round(v, 5) for k, v in st.items()},
+        "roofline": roof,
+        "cpu_baseline": cb,
+        "e2e": {"value": round(1e3 / e2e["ms_per_step"] * world, 1), "unit": "calls/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "note": "eager public-API calls from Python, pinned host buffers copied in and out every step"},
+        "gpu_launches": res["kernels"] * args.steps,
+        "clocks": res["clocks"],
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

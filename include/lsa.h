@@ -1,0 +1,240 @@
+/*
+ * lsa.h -- block-sparse decode-step attention over a paged KV cache.
+ *
+ * C ABI of liblsa.so.  One decode step of block top-k sparse attention:
+ *
+ *   1. summaries  k_bar_j = mean key of the b tokens of block j, built once
+ *                 when the block fills and reused at every later step
+ *                 (Vortex blog post, "Block top-k attention", Figure 1 and
+ *                 the block top-k equation; forward_cache of the vFlow
+ *                 listing in "Writing an algorithm: vFlow").
+ *   2. scores     s_j = q . k_bar_j, summed over the query heads of one KV
+ *                 head's GQA group (same equation; the vFlow indexer reduces
+ *                 the GeMM of summaries and queries over the head dimension).
+ *   3. selection  I = top-k_j(s_j) per (request, KV head), ties to the lower
+ *                 block index, with sink tokens and a recent window always
+ *                 attended (ByteCross, Figure 1 caption and Appendix A
+ *                 "Scored selection"; Vortex cites StreamingLLM for this).
+ *   4. attention  o = softmax(q K_T^T * scale) V_T over the attended tokens
+ *                 T = forced U selected blocks, split into parts whose partial
+ *                 results are merged by log-sum-exp (ByteCross, Appendix A:
+ *                 the sink call and the window call are merged by
+ *                 log-sum-exp; split-K decode attention, Section 4.4).
+ *   Coarse-to-fine variant (LeanSparse, Section 5 "Coarse-to-fine decode
+ *   indexing", Figure 9): a coarse top-C over block summaries of FP8 index
+ *   keys, then exact rescoring of every token of those C blocks with its FP8
+ *   e4m3 key and fp32 scale (132 bytes per 128-d key), keeping the top tokens.
+ *
+ * Conventions for every call
+ *   - All pointers named as device pointers must be device memory of the
+ *     current CUDA device; host pointers are read during the call only.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream)
+ *     unless stated otherwise.  No call allocates device memory; scratch
+ *     comes from the caller's `workspace`.
+ *   - The caller owns every buffer; no pointer is retained after return.
+ *   - Host-side argument checks return a status immediately and launch
+ *     nothing.  Data errors found on the device (page ids out of range,
+ *     invalid selections, NaN scores, wait timeouts) are recorded in a
+ *     per-device status word and never fault: the offending access is
+ *     skipped.  Read it with lsa_get_device_status().
+ *   - Token positions and block indices are logical (per request); the page
+ *     table maps logical block j of request r to physical page
+ *     page_table[r * max_blocks + j].  Pages may be shared between requests
+ *     (prefix sharing); summaries are stored per physical page, so a shared
+ *     page has one summary (Vortex, Figure 2 and "Running it: vTensor": named
+ *     cache entries live in pages managed by the KV allocator).
+ *   - seq_lens[r] counts the tokens of request r in the cache, the current
+ *     step's token included (ByteCross, Appendix A: each step appends its own
+ *     key and value before reading).
+ */
+#ifndef LSA_H
+#define LSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *lsa_stream_t;
+
+typedef enum lsa_status {
+    LSA_OK = 0,
+    LSA_ERR_INVALID_ARG = 1,  /* bad pointer, size, stride or alignment        */
+    LSA_ERR_UNSUPPORTED = 2,  /* valid but not built (head dim, group size...)  */
+    LSA_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than required        */
+    LSA_ERR_BOUNDS = 4,       /* device: page id / index / length out of range  */
+    LSA_ERR_TIMEOUT = 5,      /* device: a bounded wait gave up                 */
+    LSA_ERR_CUDA = 6,         /* a CUDA runtime call failed                     */
+    LSA_ERR_NAN = 7           /* device: a NaN score was skipped                */
+} lsa_status;
+
+typedef enum lsa_key_format {
+    LSA_KEYS_BF16 = 0,        /* keys are bf16                                  */
+    LSA_KEYS_E4M3 = 1         /* keys are FP8 e4m3 bytes + one fp32 scale/token */
+} lsa_key_format;
+
+/* A paged cache.  Element (page p, KV head h, token slot t, dim i) of K is at
+ * k + p*k_page_stride + h*k_head_stride + t*k_token_stride + i, likewise V.
+ * Strides are in elements.  Requirements: the innermost dim is contiguous;
+ * pointers and every stride in bytes are multiples of 16; dk and dv in bytes
+ * are multiples of 16.
+ *   v == k with v strides equal to k strides and dv <= dk is a latent cache
+ *   whose values are the first dv dims of the keys (MLA-shaped; Vortex,
+ *   "Designing for a new architecture"); K bytes are then read once.
+ * An index cache (coarse-to-fine) has key_format = LSA_KEYS_E4M3, k = the
+ * e4m3 bytes, v = NULL, dv = 0, and k_scale[p*scale_page_stride +
+ * h*scale_head_stride + t] = the fp32 scale of that token's key: the key's
+ * value is scale * e4m3(byte). */
+typedef struct lsa_cache {
+    void *k;
+    void *v;
+    int64_t k_page_stride, k_head_stride, k_token_stride;
+    int64_t v_page_stride, v_head_stride, v_token_stride;
+    int32_t num_pages, block_size, num_kv_heads, dk, dv;
+    int32_t key_format;                 /* lsa_key_format                  */
+    const float *k_scale;               /* LSA_KEYS_E4M3 only              */
+    int64_t scale_page_stride, scale_head_stride;
+} lsa_cache;
+
+/* Per-step parameters.  Forced tokens: F = [0, min(sink, L)) U
+ * [max(L - recent, min(sink, L)), L).  Candidates: full blocks (j+1)*b <= L
+ * none of whose tokens is in F.  The token budget of a step is
+ * |F| + k_blocks * block_size (single stage) or |F| + c2f_tokens
+ * (coarse-to-fine). */
+typedef struct lsa_params {
+    int32_t batch;            /* B requests                                    */
+    int32_t num_q_heads;      /* Hq, a multiple of num_kv_heads; query head g
+                                 belongs to KV head g / (Hq / Hkv)              */
+    int32_t max_blocks;       /* page-table row length                         */
+    int32_t k_blocks;         /* scored blocks selected per (request, KV head) */
+    int32_t sink_tokens;
+    int32_t recent_tokens;
+    float softmax_scale;      /* <= 0 selects 1/sqrt(dk)                        */
+    int32_t c2f_candidates;   /* > 0: coarse-to-fine with C candidate blocks    */
+    int32_t c2f_tokens;       /* tokens kept by the fine pass                   */
+    int32_t num_splits;       /* split-K parts per (request, KV head); 0 = auto */
+} lsa_params;
+
+/* Status and errors ------------------------------------------------------ */
+
+const char *lsa_status_string(lsa_status s);
+
+/* Reads the current device's status word (synchronises the device), returns
+ * the most severe recorded code (LSA_OK if none) and, if clear != 0, resets
+ * it.  *flags (may be NULL) receives the raw bit set: bit n set means code n
+ * was recorded. */
+lsa_status lsa_get_device_status(uint32_t *flags, int clear);
+
+/* Step 1: summaries ------------------------------------------------------- */
+
+/* Writes the bf16 summary of every full block referenced by the page tables:
+ *   summaries[(p*Hkv + h)*dk + i] = bf16_rne( (1/b) * sum_t K[p,h,t,i] )
+ * with the sum taken in fp64 (exact for bf16 keys of moderate exponent
+ * spread), so the result does not depend on summation order.  For an e4m3
+ * index cache the summed values are scale_t * e4m3(k8).  Blocks j with
+ * (j+1)*b > seq_lens[r] (partial tails) are skipped.  A page referenced by
+ * several requests is written with identical bits by each.
+ *   page_table [batch, max_blocks] int32 device; seq_lens [batch] int32 device;
+ *   summaries  [num_pages, Hkv, dk] bf16 device, caller-allocated.
+ * Errors: LSA_ERR_INVALID_ARG for NULLs or batch < 0; device: LSA_ERR_BOUNDS
+ * for page ids outside [0, num_pages) or lengths beyond max_blocks*b. */
+lsa_status lsa_build_summaries(const lsa_cache *cache, const int32_t *page_table,
+                               const int32_t *seq_lens, int32_t batch, int32_t max_blocks,
+                               void *summaries, lsa_stream_t stream);
+
+/* Appends one token per request: writes k_new[r, h, :] and v_new[r, h, :]
+ * (bf16 [batch, Hkv, dk] / [batch, Hkv, dv], device) into slot L % b of page
+ * page_table[r, L / b] with L = seq_lens[r], then increments seq_lens[r].
+ * When the block becomes full, its summary is computed in the same kernel
+ * (the summary is built once, when the block fills: Vortex, "Block top-k
+ * attention").  v_new is ignored for a latent cache (v == k).
+ * Errors as lsa_build_summaries; LSA_ERR_UNSUPPORTED for e4m3 caches. */
+lsa_status lsa_append_block(const lsa_cache *cache, const void *k_new, const void *v_new,
+                            const int32_t *page_table, int32_t *seq_lens, int32_t batch,
+                            int32_t max_blocks, void *summaries, lsa_stream_t stream);
+
+/* Step 2: scores ---------------------------------------------------------- */
+
+/* scores[(r*Hkv + h)*max_blocks + j] = sum_{g in group(h)} q[r,g,:] .
+ * summaries[page_table[r,j], h, :] in fp32 for every candidate block j of
+ * request r; -inf for every other j < max_blocks.
+ *   q [batch, Hq, dk] bf16 device, contiguous;  scores fp32 device.
+ * `cache` supplies the geometry (num_kv_heads, block_size, dk, num_pages).
+ * Supported: dk in {64, 128, 256, 576} with Hkv*dk/8 lanes tiling a warp or
+ * Hkv == 1.  Otherwise LSA_ERR_UNSUPPORTED. */
+lsa_status lsa_score(const void *q, const lsa_cache *cache, const void *summaries,
+                     const int32_t *page_table, const int32_t *seq_lens, const lsa_params *params,
+                     float *scores, lsa_stream_t stream);
+
+/* Step 3: top-k ----------------------------------------------------------- */
+
+/* Row-wise exact top-k: for each of `rows` rows of `scores` ([rows, cols]
+ * fp32 device), among the first num_cols[row] entries (num_cols NULL: all
+ * cols), the k largest by (score descending, index ascending).  -inf entries
+ * are not candidates; NaN entries are skipped and flagged (LSA_ERR_NAN).
+ * -0.0 and +0.0 compare equal.  idx [rows, k] int32 device receives the
+ * chosen column indices in ascending order, padded with -1.
+ * Supported: cols <= 32768.  The result is bit-exact (no floating point). */
+lsa_status lsa_topk(const float *scores, const int32_t *num_cols, int32_t rows, int32_t cols,
+                    int32_t k, int32_t *idx, lsa_stream_t stream);
+
+/* Coarse-to-fine fine pass: for every token t of the candidate blocks
+ * cand[r, h, :] (ascending, -1 padded, c2f_candidates per row) of request r,
+ *   f_t = scale_t * sum_{g in group(h)} q[r,g,:] . e4m3(k8_t)
+ * in fp32; keeps the c2f_tokens best by (f descending, token ascending).
+ * tok_idx [batch, Hkv, c2f_tokens] int32 device: token positions, ascending,
+ * -1 padded.  index_cache: an LSA_KEYS_E4M3 cache with dk = 128. */
+lsa_status lsa_fine_topk(const void *q, const lsa_cache *index_cache, const int32_t *page_table,
+                         const int32_t *seq_lens, const int32_t *cand, const lsa_params *params,
+                         int32_t *tok_idx, void *workspace, size_t workspace_bytes,
+                         lsa_stream_t stream);
+
+/* Step 4: sparse attention ------------------------------------------------ */
+
+/* Bytes of workspace lsa_sparse_decode needs for these shapes (split-K
+ * partials). */
+size_t lsa_sparse_decode_workspace_size(const lsa_cache *cache, const lsa_params *params);
+
+/* Exact attention over T = F U selected for every query head:
+ *   out[r, g, :] = bf16_rne( softmax_t(scale * q[r,g,:] . K_t) V_t ),
+ *   lse[r, g]    = log sum_t exp(scale * q[r,g,:] . K_t)   (natural log),
+ * split into parts whose partial (o, m, l) are merged by log-sum-exp.
+ * idx [batch, Hkv, n] int32 device, ascending, -1 padded, where n = k_blocks
+ * and entries are block indices (single stage), or n = c2f_tokens and
+ * entries are token positions (c2f_candidates > 0).  Entries that are not
+ * candidates are skipped and flagged (LSA_ERR_BOUNDS).  A request with
+ * seq_lens[r] == 0 gets out = 0 and lse = -inf.
+ *   out [batch, Hq, dv] bf16 device; lse [batch, Hq] fp32 device or NULL.
+ * workspace: device, >= lsa_sparse_decode_workspace_size bytes (may be NULL
+ * when that size is 0). */
+lsa_status lsa_sparse_decode(const void *q, const lsa_cache *cache, const int32_t *page_table,
+                             const int32_t *seq_lens, const int32_t *idx, const lsa_params *params,
+                             void *out, float *lse, void *workspace, size_t workspace_bytes,
+                             lsa_stream_t stream);
+
+/* Fused decode step ------------------------------------------------------- */
+
+size_t lsa_decode_step_workspace_size(const lsa_cache *cache, const lsa_params *params);
+
+/* Steps 2-4 in one call: score every candidate block against the summaries,
+ * select top-k_blocks per (request, KV head), and attend F U selected.  With
+ * c2f_candidates > 0 and an index cache: coarse top-C blocks over
+ * `summaries` (built from the index keys), fine top-c2f_tokens tokens, then
+ * attention.  Block scores stay on chip (Vortex, "Making it fast": operators
+ * are fused so block scores never make a round trip through GPU memory).
+ *   idx_out [batch, Hkv, k_blocks or c2f_tokens] int32 device or NULL.
+ * Other arguments as in the calls above. */
+lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *summaries,
+                           const lsa_cache *index_cache, const int32_t *page_table,
+                           const int32_t *seq_lens, const lsa_params *params, int32_t *idx_out,
+                           void *out, float *lse, void *workspace, size_t workspace_bytes,
+                           lsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LSA_H */

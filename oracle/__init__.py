@@ -77,9 +77,10 @@ def _load():
             lib.orc_dense.argtypes = [P, P, P, P, P, P, P]
             lib.orc_attend_tokens.argtypes = [P, P, P, C.c_int64, P, C.c_int, C.c_double, P, P]
             lib.orc_lse_merge.argtypes = [C.c_int, C.c_int, P, P, P, P]
+            lib.orc_attend_selection.argtypes = [P, P, P, P, P, P, I, C.c_int, P, P]
             lib.orc_lse_merge.restype = None
             for f in ("orc_summaries", "orc_block_scores", "orc_topk", "orc_fine_scores",
-                      "orc_decode", "orc_dense", "orc_attend_tokens"):
+                      "orc_decode", "orc_dense", "orc_attend_tokens", "orc_attend_selection"):
                 getattr(lib, f).restype = C.c_int
             _lib = lib
     return _lib
@@ -282,6 +283,24 @@ def attend_tokens(q_head, cache: Cache, page_table_row, tokens, h: int, scale: f
     _check(lib.orc_attend_tokens(_p(qd), cache.ref, _p(ptr), tok.shape[0], _p(tok), int(h),
                                  float(scale), _p(o), _p(lse)))
     return o, float(lse[0])
+
+
+def attend_selection(q, cache: Cache, page_table, seq_lens, sel, *, num_q_heads, sink, recent, scale,
+                     token_mode: bool = False):
+    """Attention over forced tokens plus a given selection ([B, Hkv, n]
+    block indices, or token positions in token mode).  Returns dict(out, lse)."""
+    lib = _load()
+    qa = _np(q, np.uint16)
+    pt = _np(page_table, np.int32)
+    lens = _np(seq_lens, np.int32)
+    s = _np(sel, np.int32)
+    B, maxb = pt.shape
+    prm = _params(B, num_q_heads, maxb, s.shape[-1], sink, recent, scale)
+    out = np.zeros((B, num_q_heads, cache.dv), dtype=np.uint16)
+    lse = np.zeros((B, num_q_heads), dtype=np.float64)
+    _check(lib.orc_attend_selection(_p(qa), cache.ref, _p(pt), _p(lens), C.byref(prm), _p(s), s.shape[-1],
+                                    int(token_mode), _p(out), _p(lse)))
+    return dict(out=out, lse=lse)
 
 
 def lse_merge(o_parts, lse_parts):

@@ -646,3 +646,54 @@ void orc_lse_merge(int nparts, int dv, const double *o, const double *lse,
         o_out[i] /= wsum;
     *lse_out = M + log(wsum);
 }
+
+/* Attention over T = F U (given selection) for every (request, KV head):
+ * the definition behind a sparse decode call that receives its selection
+ * (block indices, or token positions when token_mode != 0; ascending, -1
+ * padded, nsel per row).  Entries that are not candidates, or that do not
+ * ascend, are skipped. */
+int orc_attend_selection(const uint16_t *q, const orc_cache *c, const int32_t *pt, const int32_t *lens,
+                         const orc_params *prm, const int32_t *sel, int32_t nsel, int token_mode,
+                         uint16_t *out, double *lse)
+{
+    const int b = c->block_size;
+    for (int r = 0; r < prm->batch; ++r) {
+        const int64_t L = lens[r];
+        int64_t se, rs;
+        forced_ranges(L, prm->sink, prm->recent, &se, &rs);
+        const int32_t *pt_row = pt + (int64_t)r * prm->max_blocks;
+        int64_t cap = se + (L - rs) + (int64_t)nsel * (token_mode ? 1 : b);
+        int64_t *tok = (int64_t *)malloc(sizeof(int64_t) * (size_t)(cap > 0 ? cap : 1));
+        if (!tok)
+            return ORC_NOMEM;
+        for (int h = 0; h < c->num_kv_heads; ++h) {
+            const int32_t *srow = sel + ((int64_t)r * c->num_kv_heads + h) * nsel;
+            int64_t ntok = 0, prev = -1;
+            for (int64_t t = 0; t < se; ++t)
+                tok[ntok++] = t;
+            for (int i = 0; i < nsel; ++i) {
+                int64_t e = srow[i];
+                if (e < 0 || e <= prev)
+                    continue;
+                int64_t j = token_mode ? e / b : e;
+                if (!is_candidate(j, b, se, rs))
+                    continue;
+                prev = e;
+                if (token_mode)
+                    tok[ntok++] = e;
+                else
+                    for (int t = 0; t < b; ++t)
+                        tok[ntok++] = e * b + t;
+            }
+            for (int64_t t = rs; t < L; ++t)
+                tok[ntok++] = t;
+            int rc = attend_group(q, c, pt_row, prm, r, h, ntok, tok, out, lse);
+            if (rc) {
+                free(tok);
+                return rc;
+            }
+        }
+        free(tok);
+    }
+    return ORC_OK;
+}

@@ -1,0 +1,554 @@
+// C-ABI entry points of liblsa.so: argument validation, work planning
+// (split-K sizing from the device's SM count), workspace layout and the
+// stream-ordered launch sequence of each call.  See include/lsa.h for the
+// contract of every function.
+#include <math.h>
+#include <mutex>
+#include <string.h>
+
+#include "lsa_internal.h"
+
+namespace lsa {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+__device__ uint32_t d_status_word;
+
+std::mutex g_mu;
+uint32_t *g_status_ptr[kMaxDevices];
+int g_sm_count[kMaxDevices];
+
+int current_device()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return (dev >= 0 && dev < kMaxDevices) ? dev : -1;
+}
+
+// Address of this device's status word (looked up once per device).
+uint32_t *status_word()
+{
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, d_status_word) == cudaSuccess) g_status_ptr[dev] = static_cast<uint32_t *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+int sm_count()
+{
+    const int dev = current_device();
+    if (dev < 0) return 148;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_sm_count[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool mult16(int64_t elems, int esz) { return ((elems * esz) & 15) == 0; }
+
+size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Validates a cache descriptor and converts it to the kernels' view.
+lsa_status make_view(const lsa_cache *c, bool need_values, CacheView *v)
+{
+    if (!c || !c->k) return LSA_ERR_INVALID_ARG;
+    if (c->num_pages <= 0 || c->block_size <= 0 || c->num_kv_heads <= 0 || c->dk <= 0) return LSA_ERR_INVALID_ARG;
+    const bool e4m3 = c->key_format == LSA_KEYS_E4M3;
+    if (!e4m3 && c->key_format != LSA_KEYS_BF16) return LSA_ERR_INVALID_ARG;
+    const int esz = e4m3 ? 1 : 2;
+    if (!aligned16(c->k) || !mult16(c->dk, esz) || !mult16(c->k_page_stride, esz) ||
+        !mult16(c->k_head_stride, esz) || !mult16(c->k_token_stride, esz))
+        return LSA_ERR_INVALID_ARG;
+    if (c->k_token_stride < c->dk) return LSA_ERR_INVALID_ARG;
+    memset(v, 0, sizeof *v);
+    v->k = static_cast<const uint8_t *>(c->k);
+    v->kps = c->k_page_stride;
+    v->khs = c->k_head_stride;
+    v->kts = c->k_token_stride;
+    v->num_pages = c->num_pages;
+    v->b = c->block_size;
+    v->hkv = c->num_kv_heads;
+    v->dk = c->dk;
+    v->e4m3 = e4m3;
+    if (e4m3) {
+        if (!c->k_scale) return LSA_ERR_INVALID_ARG;
+        v->kscale = c->k_scale;
+        v->sps = c->scale_page_stride;
+        v->shs = c->scale_head_stride;
+    }
+    if (need_values) {
+        if (e4m3 || !c->v || c->dv <= 0) return LSA_ERR_INVALID_ARG;
+        if (!aligned16(c->v) || !mult16(c->dv, 2) || !mult16(c->v_page_stride, 2) ||
+            !mult16(c->v_head_stride, 2) || !mult16(c->v_token_stride, 2) || c->v_token_stride < c->dv)
+            return LSA_ERR_INVALID_ARG;
+        v->v = static_cast<const uint8_t *>(c->v);
+        v->vps = c->v_page_stride;
+        v->vhs = c->v_head_stride;
+        v->vts = c->v_token_stride;
+        v->dv = c->dv;
+        v->v_alias = c->v == c->k && c->v_page_stride == c->k_page_stride &&
+                     c->v_head_stride == c->k_head_stride && c->v_token_stride == c->k_token_stride &&
+                     c->dv <= c->dk;
+    }
+    return LSA_OK;
+}
+
+lsa_status check_params(const lsa_params *p, const CacheView &v)
+{
+    if (!p) return LSA_ERR_INVALID_ARG;
+    if (p->batch < 0 || p->num_q_heads <= 0 || p->num_q_heads % v.hkv != 0) return LSA_ERR_INVALID_ARG;
+    if (p->batch > 0 && p->max_blocks <= 0) return LSA_ERR_INVALID_ARG;
+    if (p->k_blocks < 0 || p->sink_tokens < 0 || p->recent_tokens < 0) return LSA_ERR_INVALID_ARG;
+    if (p->c2f_candidates < 0 || p->c2f_tokens < 0 || p->num_splits < 0) return LSA_ERR_INVALID_ARG;
+    if (p->batch > 65535 || (int64_t)p->max_blocks * v.b > INT32_MAX) return LSA_ERR_INVALID_ARG;
+    return LSA_OK;
+}
+
+lsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LSA_OK : LSA_ERR_CUDA; }
+
+float scale_of(const lsa_params *p, int dk)
+{
+    return p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / sqrtf((float)dk);
+}
+
+// ---------------------------------------------------------------- planning
+
+struct AttnPlan {
+    int nsub, splits, items_per_split;
+    size_t ws_bytes;
+};
+
+lsa_status plan_attention(const CacheView &v, const lsa_params *p, bool token_mode, AttnPlan *pl)
+{
+    const int G = p->num_q_heads / v.hkv;
+    int gs = 0;
+    if (!attention_supported(v.dk, v.dv, G, v.v_alias != 0, &gs)) return LSA_ERR_UNSUPPORTED;
+    if (v.b % kChunk != 0) return LSA_ERR_UNSUPPORTED;
+    pl->nsub = G / gs;
+    const int nsel = token_mode ? p->c2f_tokens : p->k_blocks;
+    const int items = attention_items_max(p->sink_tokens, p->recent_tokens, v.b, nsel, token_mode);
+    const int64_t rows = (int64_t)p->batch * v.hkv * pl->nsub;
+    int s = p->num_splits;
+    if (s <= 0) {
+        const int64_t target = 2LL * sm_count();
+        s = rows > 0 ? (int)((target + rows - 1) / rows) : 1;
+    }
+    s = s < 1 ? 1 : (s > items ? items : s);
+    if (s > 65535) s = 65535;
+    pl->items_per_split = (items + s - 1) / s;
+    pl->splits = (items + pl->items_per_split - 1) / pl->items_per_split;
+    if (pl->splits < 1) pl->splits = 1;
+    pl->ws_bytes = 0;
+    if (pl->splits > 1) {
+        const size_t rowsq = (size_t)p->batch * p->num_q_heads * pl->splits;
+        pl->ws_bytes = round_up(rowsq * v.dv * sizeof(float)) + round_up(rowsq * sizeof(float));
+    }
+    return LSA_OK;
+}
+
+lsa_status run_attention(const void *q, const CacheView &v, const int32_t *pt, const int32_t *lens,
+                         const int32_t *idx, const lsa_params *p, bool token_mode, void *out, float *lse,
+                         uint8_t *ws, size_t ws_bytes, cudaStream_t st)
+{
+    AttnPlan pl;
+    lsa_status rc = plan_attention(v, p, token_mode, &pl);
+    if (rc != LSA_OK) return rc;
+    if (ws_bytes < pl.ws_bytes || (pl.ws_bytes && !ws)) return LSA_ERR_WORKSPACE;
+    AttnArgs a;
+    memset(&a, 0, sizeof a);
+    a.q = static_cast<const uint16_t *>(q);
+    a.c = v;
+    a.pt = pt;
+    a.lens = lens;
+    a.idx = idx;
+    a.batch = p->batch;
+    a.hq = p->num_q_heads;
+    a.max_blocks = p->max_blocks;
+    a.nsel = token_mode ? p->c2f_tokens : p->k_blocks;
+    a.token_mode = token_mode;
+    a.sink = p->sink_tokens;
+    a.recent = p->recent_tokens;
+    a.scale_log2 = scale_of(p, v.dk) * 1.4426950408889634f;
+    a.splits = pl.splits;
+    a.items_per_split = pl.items_per_split;
+    a.nsub = pl.nsub;
+    a.out = static_cast<uint16_t *>(out);
+    a.lse = lse;
+    a.status = status_word();
+    a.spin_budget = kSpinBudget;
+    const size_t rowsq = (size_t)p->batch * p->num_q_heads * pl.splits;
+    if (pl.splits > 1) {
+        a.o_part = reinterpret_cast<float *>(ws);
+        a.lse_part = reinterpret_cast<float *>(ws + round_up(rowsq * v.dv * sizeof(float)));
+    }
+    bool unsup = false;
+    cudaError_t e = launch_attention(a, st, &unsup);
+    if (unsup) return LSA_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return LSA_ERR_CUDA;
+    if (pl.splits > 1) {
+        MergeArgs m;
+        m.o_part = a.o_part;
+        m.lse_part = a.lse_part;
+        m.rows = p->batch * p->num_q_heads;
+        m.splits = pl.splits;
+        m.dv = v.dv;
+        m.out = a.out;
+        m.lse = lse;
+        e = launch_merge(m, st);
+        if (e != cudaSuccess) return LSA_ERR_CUDA;
+    }
+    return LSA_OK;
+}
+
+// Workspace of the fused step: [scores | selection | c2f extras | attention].
+struct StepLayout {
+    size_t scores, sel, cand, fine, attn, total;
+};
+
+lsa_status step_layout(const CacheView &v, const CacheView *iv, const lsa_params *p, StepLayout *L)
+{
+    const bool c2f = p->c2f_candidates > 0;
+    const CacheView &sv = c2f ? *iv : v;
+    AttnPlan pl;
+    lsa_status rc = plan_attention(v, p, c2f, &pl);
+    if (rc != LSA_OK) return rc;
+    const size_t rows = (size_t)p->batch * sv.hkv;
+    L->scores = round_up(rows * p->max_blocks * sizeof(float));
+    L->sel = round_up(rows * (size_t)(c2f ? p->c2f_tokens : p->k_blocks) * sizeof(int32_t));
+    L->cand = c2f ? round_up(rows * (size_t)p->c2f_candidates * sizeof(int32_t)) : 0;
+    L->fine = c2f ? round_up(rows * (size_t)p->c2f_candidates * sv.b * sizeof(float)) : 0;
+    L->attn = pl.ws_bytes;
+    L->total = L->scores + L->sel + L->cand + L->fine + L->attn;
+    return LSA_OK;
+}
+
+}  // namespace
+}  // namespace lsa
+
+using namespace lsa;
+
+extern "C" {
+
+const char *lsa_status_string(lsa_status s)
+{
+    switch (s) {
+    case LSA_OK: return "ok";
+    case LSA_ERR_INVALID_ARG: return "invalid argument";
+    case LSA_ERR_UNSUPPORTED: return "unsupported shape";
+    case LSA_ERR_WORKSPACE: return "workspace missing or too small";
+    case LSA_ERR_BOUNDS: return "index, page id or length out of range (device)";
+    case LSA_ERR_TIMEOUT: return "bounded wait timed out (device)";
+    case LSA_ERR_CUDA: return "CUDA runtime error";
+    case LSA_ERR_NAN: return "NaN score skipped (device)";
+    }
+    return "unknown status";
+}
+
+lsa_status lsa_get_device_status(uint32_t *flags, int clear)
+{
+    uint32_t *w = status_word();
+    if (!w) return LSA_ERR_CUDA;
+    uint32_t v = 0;
+    if (cudaMemcpyFromSymbol(&v, d_status_word, sizeof v) != cudaSuccess) return LSA_ERR_CUDA;
+    if (clear) {
+        const uint32_t z = 0;
+        if (cudaMemcpyToSymbol(d_status_word, &z, sizeof z) != cudaSuccess) return LSA_ERR_CUDA;
+    }
+    if (flags) *flags = v;
+    const lsa_status order[] = {LSA_ERR_TIMEOUT, LSA_ERR_BOUNDS, LSA_ERR_NAN, LSA_ERR_INVALID_ARG};
+    for (lsa_status s : order)
+        if (v & (1u << s)) return s;
+    return LSA_OK;
+}
+
+lsa_status lsa_build_summaries(const lsa_cache *cache, const int32_t *page_table, const int32_t *seq_lens,
+                               int32_t batch, int32_t max_blocks, void *summaries, lsa_stream_t stream)
+{
+    CacheView v;
+    lsa_status rc = make_view(cache, false, &v);
+    if (rc != LSA_OK) return rc;
+    if (batch < 0 || max_blocks < 0) return LSA_ERR_INVALID_ARG;
+    if (batch == 0 || max_blocks == 0) return LSA_OK;
+    if (!page_table || !seq_lens || !summaries || !aligned16(summaries)) return LSA_ERR_INVALID_ARG;
+    SummaryArgs a;
+    memset(&a, 0, sizeof a);
+    a.c = v;
+    a.pt = page_table;
+    a.lens = const_cast<int32_t *>(seq_lens);
+    a.batch = batch;
+    a.max_blocks = max_blocks;
+    a.summ = static_cast<uint16_t *>(summaries);
+    a.status = status_word();
+    return from_cuda(launch_build_summaries(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lsa_status lsa_append_block(const lsa_cache *cache, const void *k_new, const void *v_new,
+                            const int32_t *page_table, int32_t *seq_lens, int32_t batch, int32_t max_blocks,
+                            void *summaries, lsa_stream_t stream)
+{
+    CacheView v;
+    lsa_status rc = make_view(cache, cache && cache->key_format == LSA_KEYS_BF16, &v);
+    if (rc != LSA_OK) return rc;
+    if (v.e4m3) return LSA_ERR_UNSUPPORTED;
+    if (batch < 0 || max_blocks < 0) return LSA_ERR_INVALID_ARG;
+    if (batch == 0) return LSA_OK;
+    if (!k_new || !page_table || !seq_lens || !summaries || !aligned16(k_new) || !aligned16(summaries))
+        return LSA_ERR_INVALID_ARG;
+    if (!v.v_alias && (!v_new || !aligned16(v_new))) return LSA_ERR_INVALID_ARG;
+    SummaryArgs a;
+    memset(&a, 0, sizeof a);
+    a.c = v;
+    a.pt = page_table;
+    a.lens = seq_lens;
+    a.batch = batch;
+    a.max_blocks = max_blocks;
+    a.summ = static_cast<uint16_t *>(summaries);
+    a.k_new = static_cast<const uint16_t *>(k_new);
+    a.v_new = static_cast<const uint16_t *>(v_new);
+    a.status = status_word();
+    bool unsup = false;
+    cudaError_t e = launch_append(a, reinterpret_cast<cudaStream_t>(stream), &unsup);
+    if (unsup) return LSA_ERR_UNSUPPORTED;
+    return from_cuda(e);
+}
+
+lsa_status lsa_score(const void *q, const lsa_cache *cache, const void *summaries, const int32_t *page_table,
+                     const int32_t *seq_lens, const lsa_params *params, float *scores, lsa_stream_t stream)
+{
+    CacheView v;
+    lsa_status rc = make_view(cache, false, &v);
+    if (rc != LSA_OK) return rc;
+    if ((rc = check_params(params, v)) != LSA_OK) return rc;
+    if (params->batch == 0) return LSA_OK;
+    if (!q || !summaries || !page_table || !seq_lens || !scores || !aligned16(q) || !aligned16(summaries))
+        return LSA_ERR_INVALID_ARG;
+    if (!score_supported(v.dk, v.hkv)) return LSA_ERR_UNSUPPORTED;
+    ScoreArgs a;
+    a.q = static_cast<const uint16_t *>(q);
+    a.summ = static_cast<const uint16_t *>(summaries);
+    a.pt = page_table;
+    a.lens = seq_lens;
+    a.batch = params->batch;
+    a.hq = params->num_q_heads;
+    a.hkv = v.hkv;
+    a.dk = v.dk;
+    a.b = v.b;
+    a.num_pages = v.num_pages;
+    a.max_blocks = params->max_blocks;
+    a.sink = params->sink_tokens;
+    a.recent = params->recent_tokens;
+    a.scores = scores;
+    a.status = status_word();
+    bool unsup = false;
+    cudaError_t e = launch_score(a, reinterpret_cast<cudaStream_t>(stream), &unsup);
+    if (unsup) return LSA_ERR_UNSUPPORTED;
+    return from_cuda(e);
+}
+
+lsa_status lsa_topk(const float *scores, const int32_t *num_cols, int32_t rows, int32_t cols, int32_t k,
+                    int32_t *idx, lsa_stream_t stream)
+{
+    if (rows < 0 || cols < 0 || k < 0) return LSA_ERR_INVALID_ARG;
+    if (rows == 0 || k == 0) return LSA_OK;
+    if (!idx || (cols > 0 && !scores)) return LSA_ERR_INVALID_ARG;
+    TopkArgs a;
+    memset(&a, 0, sizeof a);
+    a.scores = scores;
+    a.num_cols = num_cols;
+    a.rows = rows;
+    a.cols = cols;
+    a.k = k;
+    a.idx = idx;
+    a.status = status_word();
+    bool unsup = false;
+    cudaError_t e = launch_topk(a, reinterpret_cast<cudaStream_t>(stream), &unsup);
+    if (unsup) return LSA_ERR_UNSUPPORTED;
+    return from_cuda(e);
+}
+
+lsa_status lsa_fine_topk(const void *q, const lsa_cache *index_cache, const int32_t *page_table,
+                         const int32_t *seq_lens, const int32_t *cand, const lsa_params *params, int32_t *tok_idx,
+                         void *workspace, size_t workspace_bytes, lsa_stream_t stream)
+{
+    CacheView iv;
+    lsa_status rc = make_view(index_cache, false, &iv);
+    if (rc != LSA_OK) return rc;
+    if ((rc = check_params(params, iv)) != LSA_OK) return rc;
+    if (!iv.e4m3 || params->c2f_candidates <= 0) return LSA_ERR_INVALID_ARG;
+    if (params->batch == 0 || params->c2f_tokens == 0) return LSA_OK;
+    if (!q || !page_table || !seq_lens || !cand || !tok_idx || !aligned16(q)) return LSA_ERR_INVALID_ARG;
+    const size_t rows = (size_t)params->batch * iv.hkv;
+    const int64_t cols = (int64_t)params->c2f_candidates * iv.b;
+    if (cols > topk_max_cols()) return LSA_ERR_UNSUPPORTED;
+    const size_t need = round_up(rows * cols * sizeof(float));
+    if (!workspace || workspace_bytes < need) return LSA_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    FineArgs f;
+    f.q = static_cast<const uint16_t *>(q);
+    f.ic = iv;
+    f.pt = page_table;
+    f.lens = seq_lens;
+    f.cand = cand;
+    f.batch = params->batch;
+    f.hq = params->num_q_heads;
+    f.max_blocks = params->max_blocks;
+    f.ncand = params->c2f_candidates;
+    f.fscores = static_cast<float *>(workspace);
+    f.status = status_word();
+    bool unsup = false;
+    cudaError_t e = launch_fine_scores(f, st, &unsup);
+    if (unsup) return LSA_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return LSA_ERR_CUDA;
+    TopkArgs t;
+    memset(&t, 0, sizeof t);
+    t.scores = f.fscores;
+    t.rows = (int32_t)rows;
+    t.cols = (int32_t)cols;
+    t.k = params->c2f_tokens;
+    t.idx = tok_idx;
+    t.cand = cand;
+    t.ncand = params->c2f_candidates;
+    t.b = iv.b;
+    t.status = f.status;
+    e = launch_topk(t, st, &unsup);
+    if (unsup) return LSA_ERR_UNSUPPORTED;
+    return from_cuda(e);
+}
+
+size_t lsa_sparse_decode_workspace_size(const lsa_cache *cache, const lsa_params *params)
+{
+    CacheView v;
+    if (make_view(cache, true, &v) != LSA_OK || check_params(params, v) != LSA_OK) return 0;
+    AttnPlan pl;
+    if (plan_attention(v, params, params->c2f_candidates > 0, &pl) != LSA_OK) return 0;
+    return pl.ws_bytes;
+}
+
+lsa_status lsa_sparse_decode(const void *q, const lsa_cache *cache, const int32_t *page_table,
+                             const int32_t *seq_lens, const int32_t *idx, const lsa_params *params, void *out,
+                             float *lse, void *workspace, size_t workspace_bytes, lsa_stream_t stream)
+{
+    CacheView v;
+    lsa_status rc = make_view(cache, true, &v);
+    if (rc != LSA_OK) return rc;
+    if ((rc = check_params(params, v)) != LSA_OK) return rc;
+    if (params->batch == 0) return LSA_OK;
+    const bool token_mode = params->c2f_candidates > 0;
+    const int nsel = token_mode ? params->c2f_tokens : params->k_blocks;
+    if (!q || !page_table || !seq_lens || !out || !aligned16(q) || (nsel > 0 && !idx)) return LSA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(out) & 7u) != 0) return LSA_ERR_INVALID_ARG;
+    return run_attention(q, v, page_table, seq_lens, nsel > 0 ? idx : nullptr, params, token_mode, out, lse,
+                         static_cast<uint8_t *>(workspace), workspace_bytes,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t lsa_decode_step_workspace_size(const lsa_cache *cache, const lsa_params *params)
+{
+    CacheView v;
+    if (make_view(cache, true, &v) != LSA_OK || check_params(params, v) != LSA_OK) return 0;
+    StepLayout L;
+    CacheView iv = v;
+    if (params->c2f_candidates > 0) {
+        // the index cache shares the paging; only its geometry matters here
+        iv.hkv = v.hkv;
+    }
+    if (step_layout(v, &iv, params, &L) != LSA_OK) return 0;
+    return L.total;
+}
+
+lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *summaries,
+                           const lsa_cache *index_cache, const int32_t *page_table, const int32_t *seq_lens,
+                           const lsa_params *params, int32_t *idx_out, void *out, float *lse, void *workspace,
+                           size_t workspace_bytes, lsa_stream_t stream)
+{
+    CacheView v;
+    lsa_status rc = make_view(cache, true, &v);
+    if (rc != LSA_OK) return rc;
+    if ((rc = check_params(params, v)) != LSA_OK) return rc;
+    const bool c2f = params->c2f_candidates > 0;
+    CacheView iv;
+    if (c2f) {
+        if ((rc = make_view(index_cache, false, &iv)) != LSA_OK) return rc;
+        if (!iv.e4m3 || iv.hkv != v.hkv || iv.b != v.b || iv.dk != v.dk) return LSA_ERR_INVALID_ARG;
+    } else {
+        iv = v;
+    }
+    if (params->batch == 0) return LSA_OK;
+    if (!q || !summaries || !page_table || !seq_lens || !out || !aligned16(q) || !aligned16(summaries))
+        return LSA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(out) & 7u) != 0) return LSA_ERR_INVALID_ARG;
+    StepLayout L;
+    if ((rc = step_layout(v, &iv, params, &L)) != LSA_OK) return rc;
+    if (L.total > 0 && (!workspace || workspace_bytes < L.total)) return LSA_ERR_WORKSPACE;
+    if (!score_supported(iv.dk, iv.hkv)) return LSA_ERR_UNSUPPORTED;
+    if ((int64_t)params->max_blocks > topk_max_cols()) return LSA_ERR_UNSUPPORTED;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *scores = reinterpret_cast<float *>(ws);
+    int32_t *sel = idx_out ? idx_out : reinterpret_cast<int32_t *>(ws + L.scores);
+    uint8_t *ws_attn = ws + L.scores + L.sel + L.cand + L.fine;
+    uint32_t *status = status_word();
+    const size_t rows = (size_t)params->batch * iv.hkv;
+
+    // coarse (or only) stage: block scores against the summaries
+    ScoreArgs s;
+    s.q = static_cast<const uint16_t *>(q);
+    s.summ = static_cast<const uint16_t *>(summaries);
+    s.pt = page_table;
+    s.lens = seq_lens;
+    s.batch = params->batch;
+    s.hq = params->num_q_heads;
+    s.hkv = iv.hkv;
+    s.dk = iv.dk;
+    s.b = iv.b;
+    s.num_pages = iv.num_pages;
+    s.max_blocks = params->max_blocks;
+    s.sink = params->sink_tokens;
+    s.recent = params->recent_tokens;
+    s.scores = scores;
+    s.status = status;
+    bool unsup = false;
+    cudaError_t e = launch_score(s, st, &unsup);
+    if (unsup) return LSA_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return LSA_ERR_CUDA;
+
+    TopkArgs t;
+    memset(&t, 0, sizeof t);
+    t.scores = scores;
+    t.rows = (int32_t)rows;
+    t.cols = params->max_blocks;
+    t.status = status;
+    if (!c2f) {
+        t.k = params->k_blocks;
+        t.idx = sel;
+        e = launch_topk(t, st, &unsup);
+        if (unsup) return LSA_ERR_UNSUPPORTED;
+        if (e != cudaSuccess) return LSA_ERR_CUDA;
+        return run_attention(q, v, page_table, seq_lens, params->k_blocks > 0 ? sel : nullptr, params, false,
+                             out, lse, ws_attn, L.attn, st);
+    }
+    // coarse-to-fine: top-C candidate blocks, exact FP8 rescoring, token top-k
+    int32_t *cand = reinterpret_cast<int32_t *>(ws + L.scores + L.sel);
+    t.k = params->c2f_candidates;
+    t.idx = cand;
+    e = launch_topk(t, st, &unsup);
+    if (unsup) return LSA_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return LSA_ERR_CUDA;
+    rc = lsa_fine_topk(q, index_cache, page_table, seq_lens, cand, params, sel, ws + L.scores + L.sel + L.cand,
+                       L.fine, stream);
+    if (rc != LSA_OK) return rc;
+    return run_attention(q, v, page_table, seq_lens, params->c2f_tokens > 0 ? sel : nullptr, params, true, out,
+                         lse, ws_attn, L.attn, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,534 @@
+// Exact attention over the attended token set T = F U selected, split-K,
+// with a log-sum-exp merge of the parts.
+//
+//   o = softmax(q K_T^T * scale) V_T      (Vortex blog post, block top-k
+//                                           equation)
+//   parts over a partition of T are merged by log-sum-exp (ByteCross,
+//   Appendix A: the sink call and the window call are merged by
+//   log-sum-exp; Section 4.4 / Appendix D: split-K decode attention).
+//
+// One CTA per (request, KV head, query-head subgroup, split).  The split's
+// token rows are staged into shared memory by the bulk-copy (TMA) engine in
+// items of 16 tokens, one item per slot of a ring: a producer warp issues
+// cp.async.bulk for the key and value rows of each item (one copy per
+// contiguous run of rows within a page) and arms the slot's mbarrier; four
+// consumer warps take items round-robin and run an online softmax.  Inside
+// a consumer warp, four groups of eight lanes each own every fourth token of
+// the item; a lane holds 8-dim chunks of the queries and of the output
+// accumulator, so q . K_t is 16-byte shared loads, packed f32x2 FMAs and a
+// three-step shuffle reduction, and P V needs no reduction at all.  The
+// lane groups, then the warps, are merged by log-sum-exp at the end.
+#include <math.h>
+
+#include "lsa_device.cuh"
+
+namespace lsa {
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
+constexpr float kLn2 = 0.693147180559945309f;
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float lg2(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <int DK, int DV, bool ALIAS>
+struct Layout {
+    static constexpr int KROW = DK * 2;
+    static constexpr int VROW = DV * 2;
+    static constexpr int VOFF = ALIAS ? 0 : kChunk * KROW;        // V rows within a slot
+    static constexpr int VSTRIDE = ALIAS ? KROW : VROW;            // bytes between V rows
+    static constexpr int SLOT = kChunk * (KROW + (ALIAS ? 0 : VROW));
+    static constexpr int NSLOT = SLOT <= 8192 ? 8 : 4;
+    static constexpr int BAR_OFF = NSLOT * SLOT;
+    static constexpr int SMEM = BAR_OFF + NSLOT * 16 + NSLOT * 4 + 16;
+};
+
+// Row plan of one (request): forced ranges and item counts.
+struct RowPlan {
+    int L, se, rs;
+    int nsc, nsel_items, nrc, n_items;
+};
+
+__device__ __forceinline__ RowPlan make_plan(const AttnArgs &a, int r, bool flag_bad)
+{
+    RowPlan pl;
+    int L = a.lens[r];
+    if (L < 0 || (int64_t)L > (int64_t)a.max_blocks * a.c.b) {
+        if (flag_bad) flag_error(a.status, LSA_ERR_BOUNDS);
+        L = 0;
+    }
+    pl.L = L;
+    pl.se = min(a.sink, L);
+    pl.rs = max(L - a.recent, pl.se);
+    pl.nsc = (pl.se + kChunk - 1) / kChunk;
+    pl.nsel_items = a.token_mode ? (a.nsel + kChunk - 1) / kChunk : a.nsel * (a.c.b / kChunk);
+    pl.nrc = L > pl.rs ? (L + kChunk - 1) / kChunk - pl.rs / kChunk : 0;
+    pl.n_items = pl.nsc + pl.nsel_items + pl.nrc;
+    return pl;
+}
+
+// Producer side: stage item i of row (r, h) into `dst`; returns the number
+// of token rows staged (0 = nothing to attend in this item).
+template <int DK, int DV, bool ALIAS>
+__device__ int stage_item(const AttnArgs &a, const RowPlan &pl, int r, int h, int i, uint8_t *dst,
+                          uint64_t *bar, int *nslot)
+{
+    using LY = Layout<DK, DV, ALIAS>;
+    const CacheView &c = a.c;
+    const int b = c.b;
+    const int32_t *ptr = a.pt + (int64_t)r * a.max_blocks;
+    const int64_t row = (int64_t)r * c.hkv + h;
+    const int32_t *irow = a.idx ? a.idx + row * a.nsel : nullptr;
+
+    int t0 = 0, n = 0;
+    bool list = false;
+    int toks[kChunk];
+    if (i < pl.nsc) {
+        t0 = i * kChunk;
+        n = min(kChunk, pl.se - t0);
+    } else if (i < pl.nsc + pl.nsel_items) {
+        const int k = i - pl.nsc;
+        if (!a.token_mode) {
+            const int cpb = b / kChunk;
+            const int ei = k / cpb, ck = k % cpb;
+            const int e = irow[ei];
+            const bool valid = e >= 0 && e < a.max_blocks && (int64_t)e * b >= pl.se &&
+                               (int64_t)(e + 1) * b <= pl.rs && (ei == 0 || irow[ei - 1] < e);
+            if (!valid && e != -1 && ck == 0) flag_error(a.status, LSA_ERR_BOUNDS);
+            if (valid) {
+                t0 = e * b + ck * kChunk;
+                n = kChunk;
+            }
+        } else {
+            list = true;
+            for (int u = 0; u < kChunk; ++u) {
+                const int ei = k * kChunk + u;
+                if (ei >= a.nsel) break;
+                const int t = irow[ei];
+                if (t == -1) continue;
+                const int j = t / b;
+                const bool valid = t >= 0 && (int64_t)j * b >= pl.se && (int64_t)(j + 1) * b <= pl.rs &&
+                                   (ei == 0 || irow[ei - 1] < t);
+                if (!valid) {
+                    flag_error(a.status, LSA_ERR_BOUNDS);
+                    continue;
+                }
+                toks[n++] = t;
+            }
+        }
+    } else {
+        const int k = i - pl.nsc - pl.nsel_items;
+        const int blk16 = pl.rs / kChunk + k;
+        t0 = max(pl.rs, blk16 * kChunk);
+        n = min(pl.L, blk16 * kChunk + kChunk) - t0;
+    }
+    if (n <= 0) return 0;
+
+    if (!list) {
+        const int p = ptr[t0 / b];
+        if (p < 0 || p >= c.num_pages) {
+            flag_error(a.status, LSA_ERR_BOUNDS);
+            return 0;
+        }
+        const uint32_t bytes = n * (LY::KROW + (ALIAS ? 0 : LY::VROW));
+        *nslot = n;   // visible to the consumer through the arrive's release
+        mbar_arrive_expect_tx(bar, bytes);
+        const int ts = t0 % b;
+        const uint8_t *ks = c.k + ((int64_t)p * c.kps + (int64_t)h * c.khs + (int64_t)ts * c.kts) * 2;
+        if (c.kts == DK) {
+            bulk_g2s(dst, ks, n * LY::KROW, bar);
+        } else {
+            for (int u = 0; u < n; ++u) bulk_g2s(dst + u * LY::KROW, ks + (int64_t)u * c.kts * 2, LY::KROW, bar);
+        }
+        if constexpr (!ALIAS) {
+            const uint8_t *vs = c.v + ((int64_t)p * c.vps + (int64_t)h * c.vhs + (int64_t)ts * c.vts) * 2;
+            if (c.vts == DV) {
+                bulk_g2s(dst + LY::VOFF, vs, n * LY::VROW, bar);
+            } else {
+                for (int u = 0; u < n; ++u)
+                    bulk_g2s(dst + LY::VOFF + u * LY::VROW, vs + (int64_t)u * c.vts * 2, LY::VROW, bar);
+            }
+        }
+        return n;
+    }
+    // token list: one row copy per token
+    int m = 0;
+    int pages[kChunk];
+    for (int u = 0; u < n; ++u) {
+        const int p = ptr[toks[u] / b];
+        if (p < 0 || p >= c.num_pages) {
+            flag_error(a.status, LSA_ERR_BOUNDS);
+            continue;
+        }
+        pages[m] = p;
+        toks[m] = toks[u];
+        ++m;
+    }
+    if (m == 0) return 0;
+    *nslot = m;
+    mbar_arrive_expect_tx(bar, m * (LY::KROW + (ALIAS ? 0 : LY::VROW)));
+    for (int u = 0; u < m; ++u) {
+        const int ts = toks[u] % b;
+        const uint8_t *ks = c.k + ((int64_t)pages[u] * c.kps + (int64_t)h * c.khs + (int64_t)ts * c.kts) * 2;
+        bulk_g2s(dst + u * LY::KROW, ks, LY::KROW, bar);
+        if constexpr (!ALIAS) {
+            const uint8_t *vs = c.v + ((int64_t)pages[u] * c.vps + (int64_t)h * c.vhs + (int64_t)ts * c.vts) * 2;
+            bulk_g2s(dst + LY::VOFF + u * LY::VROW, vs, LY::VROW, bar);
+        }
+    }
+    return m;
+}
+
+template <int DK, int DV, int GS, bool ALIAS>
+__global__ void __launch_bounds__(kAttnThreads, 2) k_sparse_attn(AttnArgs a)
+{
+    using LY = Layout<DK, DV, ALIAS>;
+    constexpr int NCK = DK / 64;   // 8-dim key chunks per lane
+    constexpr int NCV = DV / 64;   // 8-dim value chunks per lane
+    constexpr int NSLOT = LY::NSLOT;
+    static_assert(DK % 64 == 0 && DV % 64 == 0, "head dims must be multiples of 64");
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + LY::BAR_OFF);
+    uint64_t *empty = full + NSLOT;
+    int *item_n = reinterpret_cast<int *>(empty + NSLOT);
+
+    const int split = blockIdx.x;
+    const int h = blockIdx.y / a.nsub, sg = blockIdx.y % a.nsub;
+    const int r = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = a.hq / a.c.hkv;
+
+    const RowPlan pl = make_plan(a, r, threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0);
+    const int i_begin = split * a.items_per_split;
+    const int nloc = max(0, min(pl.n_items, i_begin + a.items_per_split) - i_begin);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSLOT; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    float m[GS], l[GS];
+    float2 o[GS][NCV][4];
+    const int grp = lane >> 3, sub = lane & 7;
+
+    if (warp == kConsumerWarps) {
+        // ---------------- producer
+        if (lane == 0) {
+            for (int k = 0; k < nloc; ++k) {
+                const int slot = k % NSLOT;
+                if (k >= NSLOT && !mbar_wait(&empty[slot], ((k / NSLOT) - 1) & 1, a.status, a.spin_budget)) break;
+                uint8_t *dst = smem + slot * LY::SLOT;
+                const int n = stage_item<DK, DV, ALIAS>(a, pl, r, h, i_begin + k, dst, &full[slot],
+                                                        &item_n[slot]);
+                if (n == 0) {
+                    item_n[slot] = 0;
+                    mbar_arrive(&full[slot]);
+                }
+            }
+        }
+    } else {
+        // ---------------- consumers
+        float2 qf[GS][NCK][4];
+#pragma unroll
+        for (int g = 0; g < GS; ++g) {
+            const int hq = h * G + sg * GS + g;
+            const uint16_t *qrow = a.q + ((int64_t)r * a.hq + hq) * DK;
+#pragma unroll
+            for (int kk = 0; kk < NCK; ++kk) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(qrow + (sub + 8 * kk) * 8);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float2 f = bf2_to_f2(w[e]);
+                    qf[g][kk][e] = make_float2(f.x * a.scale_log2, f.y * a.scale_log2);
+                }
+            }
+            m[g] = -INFINITY;
+            l[g] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < NCV; ++kk)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[g][kk][e] = make_float2(0.f, 0.f);
+        }
+
+        for (int k = warp; k < nloc; k += kConsumerWarps) {
+            const int slot = k % NSLOT;
+            if (!mbar_wait(&full[slot], (k / NSLOT) & 1, a.status, a.spin_budget)) break;
+            const int n = item_n[slot];
+            const uint8_t *Ks = smem + slot * LY::SLOT;
+            const uint8_t *Vs = Ks + LY::VOFF;
+            if (n > 0) {
+                float z[4][GS];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int t = grp + 4 * j;
+                    const uint8_t *krow = Ks + t * LY::KROW;
+                    float2 acc[GS];
+#pragma unroll
+                    for (int g = 0; g < GS; ++g) acc[g] = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int kk = 0; kk < NCK; ++kk) {
+                        const uint4 kv = *reinterpret_cast<const uint4 *>(krow + (sub + 8 * kk) * 16);
+                        const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 kf = bf2_to_f2(w[e]);
+#pragma unroll
+                            for (int g = 0; g < GS; ++g) acc[g] = __ffma2_rn(qf[g][kk][e], kf, acc[g]);
+                        }
+                    }
+#pragma unroll
+                    for (int g = 0; g < GS; ++g) {
+                        float zz = acc[g].x + acc[g].y;
+                        zz += __shfl_xor_sync(0xffffffffu, zz, 4);
+                        zz += __shfl_xor_sync(0xffffffffu, zz, 2);
+                        zz += __shfl_xor_sync(0xffffffffu, zz, 1);
+                        z[j][g] = t < n ? zz : -INFINITY;
+                    }
+                }
+                float p[4][GS];
+#pragma unroll
+                for (int g = 0; g < GS; ++g) {
+                    const float mx = fmaxf(fmaxf(z[0][g], z[1][g]), fmaxf(z[2][g], z[3][g]));
+                    const float mn = fmaxf(m[g], mx);
+                    if (mn == -INFINITY) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) p[j][g] = 0.f;
+                        continue;
+                    }
+                    const float alpha = ex2(m[g] - mn);
+                    float ps = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        p[j][g] = ex2(z[j][g] - mn);
+                        ps += p[j][g];
+                    }
+                    l[g] = l[g] * alpha + ps;
+                    m[g] = mn;
+                    const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+                    for (int kk = 0; kk < NCV; ++kk)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) o[g][kk][e] = __fmul2_rn(o[g][kk][e], a2);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int t = grp + 4 * j;
+                    if (t < n) {
+                        const uint8_t *vrow = Vs + t * LY::VSTRIDE;
+#pragma unroll
+                        for (int kk = 0; kk < NCV; ++kk) {
+                            const uint4 vv = *reinterpret_cast<const uint4 *>(vrow + (sub + 8 * kk) * 16);
+                            const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 vf = bf2_to_f2(w[e]);
+#pragma unroll
+                                for (int g = 0; g < GS; ++g)
+                                    o[g][kk][e] = __ffma2_rn(make_float2(p[j][g], p[j][g]), vf, o[g][kk][e]);
+                            }
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+
+        // merge the four lane groups of this warp (xor 8, 16)
+#pragma unroll
+        for (int off = 8; off <= 16; off <<= 1) {
+#pragma unroll
+            for (int g = 0; g < GS; ++g) {
+                const float m2 = __shfl_xor_sync(0xffffffffu, m[g], off);
+                const float l2 = __shfl_xor_sync(0xffffffffu, l[g], off);
+                const float mn = fmaxf(m[g], m2);
+                const float a1 = m[g] == -INFINITY ? 0.f : ex2(m[g] - mn);
+                const float b1 = m2 == -INFINITY ? 0.f : ex2(m2 - mn);
+                l[g] = l[g] * a1 + l2 * b1;
+                m[g] = mn;
+#pragma unroll
+                for (int kk = 0; kk < NCV; ++kk)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float2 ov;
+                        ov.x = __shfl_xor_sync(0xffffffffu, o[g][kk][e].x, off);
+                        ov.y = __shfl_xor_sync(0xffffffffu, o[g][kk][e].y, off);
+                        o[g][kk][e] = make_float2(o[g][kk][e].x * a1 + ov.x * b1, o[g][kk][e].y * a1 + ov.y * b1);
+                    }
+            }
+        }
+    }
+    __syncthreads();   // every slot consumed: the ring is reused for the merge
+
+    // merge the consumer warps through shared memory
+    float *mo = reinterpret_cast<float *>(smem);                    // [NW][GS][DV]
+    float *mm = mo + kConsumerWarps * GS * DV;                      // [NW][GS]
+    float *ml = mm + kConsumerWarps * GS;                           // [NW][GS]
+    if (warp < kConsumerWarps && grp == 0) {
+#pragma unroll
+        for (int g = 0; g < GS; ++g) {
+#pragma unroll
+            for (int kk = 0; kk < NCV; ++kk) {
+                float *dst = mo + (warp * GS + g) * DV + (sub + 8 * kk) * 8;
+                reinterpret_cast<float4 *>(dst)[0] = make_float4(o[g][kk][0].x, o[g][kk][0].y, o[g][kk][1].x, o[g][kk][1].y);
+                reinterpret_cast<float4 *>(dst)[1] = make_float4(o[g][kk][2].x, o[g][kk][2].y, o[g][kk][3].x, o[g][kk][3].y);
+            }
+            if (sub == 0) {
+                mm[warp * GS + g] = m[g];
+                ml[warp * GS + g] = l[g];
+            }
+        }
+    }
+    __syncthreads();
+
+    for (int t = threadIdx.x; t < GS * DV / 4; t += blockDim.x) {
+        const int g = t / (DV / 4), d = (t % (DV / 4)) * 4;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * GS + g]);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float wsum = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float mw = mm[w * GS + g];
+                if (mw == -INFINITY) continue;
+                const float f = ex2(mw - M);
+                wsum += f * ml[w * GS + g];
+                const float4 v = *reinterpret_cast<const float4 *>(mo + (w * GS + g) * DV + d);
+                acc.x += f * v.x;
+                acc.y += f * v.y;
+                acc.z += f * v.z;
+                acc.w += f * v.w;
+            }
+        }
+        const bool empty_set = !(wsum > 0.f);
+        const float inv = empty_set ? 0.f : 1.f / wsum;
+        acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        const float lse2 = empty_set ? -INFINITY : M + lg2(wsum);
+        const int hq = h * G + sg * GS + g;
+        const int64_t orow = (int64_t)r * a.hq + hq;
+        if (a.splits == 1) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 packed;
+            packed.x = *reinterpret_cast<uint32_t *>(&lo);
+            packed.y = *reinterpret_cast<uint32_t *>(&hi);
+            *reinterpret_cast<uint2 *>(a.out + orow * DV + d) = packed;
+            if (a.lse && d == 0) a.lse[orow] = empty_set ? -INFINITY : lse2 * kLn2;
+        } else {
+            *reinterpret_cast<float4 *>(a.o_part + (orow * a.splits + split) * DV + d) = acc;
+            if (d == 0) a.lse_part[orow * a.splits + split] = lse2;
+        }
+    }
+}
+
+// Log-sum-exp merge of the split partials: weights exp2(lse_s - max).
+__global__ void k_merge(MergeArgs a)
+{
+    const int row = blockIdx.x;
+    const int d = threadIdx.x * 4;
+    if (d >= a.dv) return;
+    const float *lp = a.lse_part + (int64_t)row * a.splits;
+    float M = -INFINITY;
+    for (int s = 0; s < a.splits; ++s) M = fmaxf(M, lp[s]);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < a.splits; ++s) {
+            if (lp[s] == -INFINITY) continue;
+            const float f = ex2(lp[s] - M);
+            wsum += f;
+            const float4 v = *reinterpret_cast<const float4 *>(a.o_part + ((int64_t)row * a.splits + s) * a.dv + d);
+            acc.x += f * v.x;
+            acc.y += f * v.y;
+            acc.z += f * v.z;
+            acc.w += f * v.w;
+        }
+    }
+    const bool empty_set = !(wsum > 0.f);
+    const float inv = empty_set ? 0.f : 1.f / wsum;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 packed;
+    packed.x = *reinterpret_cast<uint32_t *>(&lo);
+    packed.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(a.out + (int64_t)row * a.dv + d) = packed;
+    if (a.lse && d == 0) a.lse[row] = empty_set ? -INFINITY : (M + lg2(wsum)) * kLn2;
+}
+
+template <int DK, int DV, int GS, bool ALIAS>
+cudaError_t launch_attn_t(const AttnArgs &a, cudaStream_t s)
+{
+    using LY = Layout<DK, DV, ALIAS>;
+    static_assert(LY::NSLOT * LY::SLOT >= kConsumerWarps * GS * DV * 4 + 2 * kConsumerWarps * GS * 4,
+                  "merge buffers must fit in the slot ring");
+    auto kern = k_sparse_attn<DK, DV, GS, ALIAS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.splits, a.c.hkv * a.nsub, a.batch);
+    kern<<<grid, kAttnThreads, LY::SMEM, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attention_supported(int dk, int dv, int group, bool alias, int *sub_group)
+{
+    int gs = 0;
+    if (dk == 64 && dv == 64 && !alias) gs = group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1);
+    else if (dk == 128 && dv == 128 && !alias) gs = group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1);
+    else if (dk == 576 && dv == 512 && alias) gs = 1;
+    if (sub_group) *sub_group = gs;
+    return gs > 0;
+}
+
+int attention_items_max(int sink, int recent, int b, int nsel, int token_mode)
+{
+    const int sel_items = token_mode ? (nsel + kChunk - 1) / kChunk : nsel * (b / kChunk);
+    return (sink + kChunk - 1) / kChunk + sel_items + (recent + kChunk - 1) / kChunk + 1;
+}
+
+cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s, bool *unsupported)
+{
+    *unsupported = false;
+    if (a.batch == 0) return cudaSuccess;
+    const int G = a.hq / a.c.hkv;
+    const int gs = G / a.nsub;
+    const bool alias = a.c.v_alias != 0;
+#define LSA_ATTN_CASE(DK_, DV_, GS_, AL_) \
+    if (a.c.dk == DK_ && a.c.dv == DV_ && gs == GS_ && alias == AL_) return launch_attn_t<DK_, DV_, GS_, AL_>(a, s);
+    LSA_ATTN_CASE(64, 64, 4, false) LSA_ATTN_CASE(64, 64, 2, false) LSA_ATTN_CASE(64, 64, 1, false)
+    LSA_ATTN_CASE(128, 128, 4, false) LSA_ATTN_CASE(128, 128, 2, false) LSA_ATTN_CASE(128, 128, 1, false)
+    LSA_ATTN_CASE(576, 512, 1, true)
+#undef LSA_ATTN_CASE
+    *unsupported = true;
+    return cudaSuccess;
+}
+
+cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s)
+{
+    if (a.rows == 0) return cudaSuccess;
+    k_merge<<<a.rows, (a.dv + 3) / 4, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace lsa

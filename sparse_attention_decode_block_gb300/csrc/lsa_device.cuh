@@ -1,0 +1,157 @@
+// Device helpers shared by the kernels of liblsa: bulk-copy staging with
+// mbarriers (inline PTX for sm_103a), bf16 / e4m3 conversions, bounded waits
+// and the device status word.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lsa_internal.h"
+
+namespace lsa {
+
+// ---------------------------------------------------------------- status
+
+// Kernels record data errors by setting bit `code` of the per-device status
+// word (never by faulting): the offending access is skipped.
+__device__ __forceinline__ void flag_error(uint32_t *status, int code)
+{
+    if (status) atomicOr(status, 1u << code);
+}
+
+// ---------------------------------------------------------------- smem / mbarrier
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase.  Gives up after `budget` clock cycles
+// (records LSA_ERR_TIMEOUT) and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status,
+                                          long long budget)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > budget) {
+            flag_error(status, LSA_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// 1-D bulk copy (TMA engine) global -> shared; completion is counted in
+// bytes on `bar`.  Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// ---------------------------------------------------------------- conversions
+
+// Two packed bf16 (low half = element 0) -> two floats.  bf16 is the upper
+// half of a binary32, so this is exact.
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u)
+{
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+__device__ __forceinline__ float bf_to_f(uint16_t u)
+{
+    return __uint_as_float(static_cast<uint32_t>(u) << 16);
+}
+
+// fp64 -> bf16 with a single round-to-nearest-even: first round toward zero
+// to binary32 and make the result "sticky" (round to odd: set the last bit if
+// anything was discarded), then round binary32 -> bf16 to nearest even.
+// Rounding to odd with at least two extra bits and then to nearest gives the
+// correctly rounded result (Boldo & Melquiond, "Emulation of FMA and
+// correctly rounded sums: proved algorithms using rounding to odd", 2008).
+__device__ __forceinline__ uint16_t f64_to_bf16_rne(double x)
+{
+    float f = __double2float_rz(x);
+    if (static_cast<double>(f) != x && !isnan(x) && !isinf(f)) {
+        f = __uint_as_float(__float_as_uint(f) | 1u);
+    }
+    __nv_bfloat16 h = __float2bfloat16_rn(f);
+    return *reinterpret_cast<uint16_t *>(&h);
+}
+
+// Two e4m3 bytes (low byte = element 0) -> two floats; every e4m3 value is
+// exact in half precision.
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint16_t two)
+{
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+    __half2 hh = *reinterpret_cast<__half2 *>(&h2);
+    return __half22float2(hh);
+}
+
+// Order-preserving map from fp32 to uint32 for the radix select: larger
+// float -> larger key.  -0 is first made +0.  Keys of finite values and of
+// +inf are > 0x007fffff; the caller reserves 0 for "not a candidate".
+__device__ __forceinline__ uint32_t float_to_key(float s)
+{
+    uint32_t b = __float_as_uint(s);
+    if (b == 0x80000000u) b = 0u;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// ---------------------------------------------------------------- loads
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+}  // namespace lsa

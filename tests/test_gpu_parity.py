@@ -1,0 +1,381 @@
+"""GPU parity: every C-ABI entry point against the CPU oracle on the same
+seeded inputs (small workloads spanning several tiles with ragged tails,
+edge cases, and the full-size workloads on sampled requests)."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_attention_decode_block_gb300 as L
+from helpers import (GpuStep, assert_attention_close, assert_lse_close, bits, check_status_clean,
+                     compare_selection, f64, oracle_cache, oracle_decode, oracle_index, score_bound, subset,
+                     to_dev)
+from workloads import WORKLOADS, make_inputs, small_workloads
+
+pytestmark = pytest.mark.gpu
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+SMALL = ["tiny", "b16_small", "ragged_small", "mla_small"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    L.lsa_get_device_status(clear=True)
+    yield
+
+
+def small(name, **kw):
+    w = small_workloads()[name]
+    return w.replace(**kw) if kw else w
+
+
+# ---------------------------------------------------------------- summaries
+
+@pytest.mark.parametrize("name", SMALL + ["c2f_small"])
+def test_summaries_bit_exact(name):
+    w = small(name)
+    cpu = make_inputs(w, "cpu")
+    g = to_dev(cpu)
+    if w.c2f_candidates:
+        c = L.make_cache(g["idx_keys"], None, k_scale=g["idx_scale"])
+        oc, use8 = oracle_index(cpu), True
+    else:
+        c = L.make_cache(g["k_cache"], g["v_cache"])
+        oc, use8 = oracle_cache(cpu), False
+    summ = torch.zeros((cpu["num_pages"], w.num_kv_heads, w.dk), dtype=torch.bfloat16, device="cuda")
+    L.lsa_build_summaries(c, g["page_table"], g["seq_lens"], summ)
+    check_status_clean()
+    ref, valid = oracle.summaries(oc, cpu["page_table"], cpu["seq_lens"], use_index_keys=use8)
+    got = bits(summ)
+    assert valid.any()
+    assert np.array_equal(got[valid], ref[valid])
+    assert np.all(got[~valid] == 0)          # pages with no full block untouched
+
+
+def test_append_matches_bulk_build():
+    w = small("b16_small", seq_lens=(100, 33, 18))
+    cpu = make_inputs(w, "cpu", lens=[100 + 40, 33 + 40, 18 + 40])   # room for 40 appended tokens
+    g = to_dev(cpu)
+    L0 = torch.tensor([100, 33, 18], dtype=torch.int32, device="cuda")
+    k_full, v_full = g["k_cache"].clone(), g["v_cache"].clone()
+    k_cache = torch.zeros_like(k_full)
+    v_cache = torch.zeros_like(v_full)
+    # copy the first L0 tokens of every request, then append the rest one by one
+    pt = cpu["page_table"]
+    b = w.block_size
+    for r in range(w.batch):
+        for t in range(int(L0[r])):
+            p = int(pt[r, t // b])
+            k_cache[p, :, t % b] = k_full[p, :, t % b]
+            v_cache[p, :, t % b] = v_full[p, :, t % b]
+    cache = L.make_cache(k_cache, v_cache)
+    summ = torch.zeros((cpu["num_pages"], w.num_kv_heads, w.dk), dtype=torch.bfloat16, device="cuda")
+    lens = L0.clone()
+    L.lsa_build_summaries(cache, g["page_table"], lens, summ)
+    for step in range(40):
+        kn = torch.empty((w.batch, w.num_kv_heads, w.dk), dtype=torch.bfloat16, device="cuda")
+        vn = torch.empty_like(kn)
+        for r in range(w.batch):
+            t = int(L0[r]) + step
+            p = int(pt[r, t // b])
+            kn[r] = k_full[p, :, t % b]
+            vn[r] = v_full[p, :, t % b]
+        L.lsa_append_block(cache, kn, vn, g["page_table"], lens, summ)
+    check_status_clean()
+    assert lens.tolist() == [140, 73, 58]
+    ref = torch.zeros_like(summ)
+    L.lsa_build_summaries(L.make_cache(k_full, v_full), g["page_table"], lens, ref)
+    torch.cuda.synchronize()
+    assert torch.equal(summ.view(torch.int16), ref.view(torch.int16))
+    for r in range(w.batch):
+        for t in range(140 if r == 0 else (73 if r == 1 else 58)):
+            p = int(pt[r, t // b])
+            assert torch.equal(k_cache[p, :, t % b], k_full[p, :, t % b])
+            assert torch.equal(v_cache[p, :, t % b], v_full[p, :, t % b])
+
+
+# ---------------------------------------------------------------- scores / top-k
+
+@pytest.mark.parametrize("name", SMALL + ["c2f_small"])
+def test_scores_within_rounding_and_topk_bit_exact(name):
+    w = small(name)
+    cpu = make_inputs(w, "cpu")
+    g = to_dev(cpu)
+    use8 = w.c2f_candidates > 0
+    c = L.make_cache(g["idx_keys"], None, k_scale=g["idx_scale"]) if use8 else L.make_cache(g["k_cache"], g["v_cache"])
+    oc = oracle_index(cpu) if use8 else oracle_cache(cpu)
+    summ = torch.zeros((cpu["num_pages"], w.num_kv_heads, w.dk), dtype=torch.bfloat16, device="cuda")
+    L.lsa_build_summaries(c, g["page_table"], g["seq_lens"], summ)
+    prm = L.make_params(w.batch, w.num_q_heads, cpu["max_blocks"], w.k_blocks, w.sink, w.recent)
+    scores = torch.empty((w.batch, w.num_kv_heads, cpu["max_blocks"]), dtype=torch.float32, device="cuda")
+    L.lsa_score(g["q"], c, summ, g["page_table"], g["seq_lens"], prm, scores)
+    osumm, _ = oracle.summaries(oc, cpu["page_table"], cpu["seq_lens"], use_index_keys=use8)
+    ref = oracle.block_scores(cpu["q"], oc, osumm, cpu["page_table"], cpu["seq_lens"], w.num_q_heads, w.sink,
+                              w.recent, use_index_keys=use8)
+    got = scores.cpu().numpy().astype(np.float64)
+    assert np.array_equal(np.isneginf(got), np.isneginf(ref))
+    S = f64(osumm)
+    G = w.group
+    for r in range(w.batch):
+        for h in range(w.num_kv_heads):
+            pg = cpu["page_table"][r].numpy()
+            fin = np.isfinite(ref[r, h])
+            tau = score_bound(bits(cpu["q"][r, h * G:(h + 1) * G]), S[np.maximum(pg, 0), h], G, w.dk)
+            assert np.all(np.abs(got[r, h][fin] - ref[r, h][fin]) <= tau[fin] + 1e-30)
+    # top-k over the GPU's fp32 scores: bit-exact against the oracle's top-k of the same values
+    k = w.k_blocks if not use8 else w.c2f_candidates
+    idx = torch.empty((w.batch * w.num_kv_heads, k), dtype=torch.int32, device="cuda")
+    L.lsa_topk(scores.view(w.batch * w.num_kv_heads, -1), None, k, idx)
+    check_status_clean()
+    want = oracle.topk(got.reshape(w.batch * w.num_kv_heads, -1), k)
+    assert np.array_equal(idx.cpu().numpy(), want)
+
+
+def test_topk_vortex_figure1_golden_gpu():
+    gold = json.load(open(os.path.join(GOLD, "vortex_fig1_block_topk.json")))
+    s = torch.tensor([gold["scores"]], dtype=torch.float32, device="cuda")
+    idx = torch.empty((1, gold["k"]), dtype=torch.int32, device="cuda")
+    L.lsa_topk(s, None, gold["k"], idx)
+    assert idx.cpu().tolist()[0] == gold["selected_ascending"]
+
+
+@pytest.mark.parametrize("cols,k", [(1, 1), (7, 3), (64, 62), (2048, 62), (2048, 1), (5000, 256),
+                                    (16384, 2048), (16381, 29), (32768, 100), (100, 200)])
+def test_topk_random_rows_with_ties(cols, k):
+    gen = torch.Generator().manual_seed(cols * 7 + k)
+    rows = 6
+    s = torch.randint(-40, 40, (rows, cols), generator=gen).float() / 8     # many exact ties
+    s[1] = torch.randn(cols, generator=gen)                                  # distinct values
+    s[2] = 0.0
+    s[2, ::3] = -0.0                                                         # -0 and +0 tie
+    s[3, torch.rand(cols, generator=gen) < 0.5] = -math.inf                  # non-candidates
+    s[4] = -math.inf
+    s[5] = torch.randn(cols, generator=gen) * 1e30
+    ncols = torch.tensor([cols, cols, cols, cols, cols, max(0, cols - 3)], dtype=torch.int32)
+    idx = torch.empty((rows, k), dtype=torch.int32, device="cuda")
+    L.lsa_topk(s.cuda(), ncols.cuda(), k, idx)
+    check_status_clean()
+    want = np.stack([oracle.topk(s[i:i + 1, : int(ncols[i])].numpy(), k)[0] for i in range(rows)])
+    assert np.array_equal(idx.cpu().numpy(), want)
+
+
+def test_topk_nan_is_skipped_and_flagged():
+    s = torch.tensor([[0.5, float("nan"), 2.0, 1.0]], device="cuda")
+    idx = torch.empty((1, 2), dtype=torch.int32, device="cuda")
+    L.lsa_topk(s, None, 2, idx)
+    torch.cuda.synchronize()
+    code, flags = L.lsa_get_device_status(clear=True)
+    assert code == L.LSA_ERR_NAN
+    assert idx.cpu().tolist()[0] == [2, 3]
+
+
+# ---------------------------------------------------------------- attention
+
+@pytest.mark.parametrize("name", SMALL)
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_sparse_decode_with_oracle_selection(name, splits):
+    w = small(name)
+    cpu = make_inputs(w, "cpu")
+    g = to_dev(cpu)
+    ref = oracle_decode(w, cpu)
+    cache = L.make_cache(g["k_cache"], g["v_cache"])
+    prm = L.make_params(w.batch, w.num_q_heads, cpu["max_blocks"], w.k_blocks, w.sink, w.recent,
+                        w.softmax_scale, num_splits=splits)
+    ws = torch.empty(max(16, L.lsa_sparse_decode_workspace_size(cache, prm)), dtype=torch.uint8, device="cuda")
+    out = torch.empty((w.batch, w.num_q_heads, w.dv), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.batch, w.num_q_heads), dtype=torch.float32, device="cuda")
+    sel = torch.from_numpy(ref["sel"]).cuda()
+    L.lsa_sparse_decode(g["q"], cache, g["page_table"], g["seq_lens"], sel, prm, out, lse, ws)
+    check_status_clean()
+    assert_attention_close(out, ref["out"], name)
+    assert_lse_close(lse, ref["lse"], name)
+
+
+def run_and_compare_step(w, cpu, g, reqs=None, num_splits=0):
+    st = GpuStep(w, g, num_splits)
+    st.run()
+    check_status_clean()
+    reqs = list(range(w.batch)) if reqs is None else list(reqs)
+    sub = subset(cpu, reqs) if len(reqs) != w.batch else cpu
+    wr = w.replace(batch=len(reqs), seq_lens=tuple(sub["lens"]), seq_len_range=None)
+    ref = oracle_decode(wr, sub)
+    sel_gpu = st.idx.cpu().numpy()[reqs]
+    # oracle scores for the tie rule
+    use8 = w.c2f_candidates > 0
+    ties = 0
+    if not use8:
+        oc = oracle_cache(sub)
+        osumm, _ = oracle.summaries(oc, sub["page_table"], sub["seq_lens"])
+        sc = oracle.block_scores(sub["q"], oc, osumm, sub["page_table"], sub["seq_lens"], w.num_q_heads, w.sink,
+                                 w.recent)
+        S = f64(osumm)
+        G = w.group
+        for i in range(len(reqs)):
+            for h in range(w.num_kv_heads):
+                pg = np.maximum(sub["page_table"][i].numpy(), 0)
+                tau = score_bound(bits(sub["q"][i, h * G:(h + 1) * G]), S[pg, h], G, w.dk)
+                kind = compare_selection(sel_gpu[i, h], ref["sel"][i, h], sc[i, h], tau)
+                ties += kind == "tie"
+    else:
+        assert np.array_equal(sel_gpu, ref["sel"]), "fine token selection differs"
+    out = st.out[reqs]
+    lse = st.lse[reqs]
+    if ties:
+        # rows whose selection is an equally valid alternative (checked above):
+        # the expected output is the oracle's attention on that selection
+        ref = oracle.attend_selection(sub["q"], oracle_cache(sub), sub["page_table"], sub["seq_lens"], sel_gpu,
+                                      num_q_heads=w.num_q_heads, sink=w.sink, recent=w.recent,
+                                      scale=w.softmax_scale)
+        print(f"{w.name}: {ties} epsilon-tie rows")
+    err = assert_attention_close(out, ref["out"], w.name)
+    assert_lse_close(lse, ref["lse"], w.name)
+    return err
+
+
+@pytest.mark.parametrize("name", SMALL + ["c2f_small"])
+def test_decode_step_end_to_end(name):
+    w = small(name)
+    cpu = make_inputs(w, "cpu")
+    run_and_compare_step(w, cpu, to_dev(cpu))
+
+
+@pytest.mark.parametrize("splits", [1, 2, 5, 1000])
+def test_decode_step_split_count_does_not_change_result(splits):
+    w = small("ragged_small")
+    cpu = make_inputs(w, "cpu")
+    run_and_compare_step(w, cpu, to_dev(cpu), num_splits=splits)
+
+
+# ---------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("lens", [(0, 1, 5), (16, 17, 31), (33, 47, 1000)])
+def test_short_and_empty_requests(lens):
+    w = small("b16_small", seq_lens=lens)
+    cpu = make_inputs(w, "cpu")
+    g = to_dev(cpu)
+    st = GpuStep(w, g)
+    st.run()
+    check_status_clean()
+    ref = oracle_decode(w, cpu)
+    assert np.array_equal(st.idx.cpu().numpy(), ref["sel"])
+    assert_attention_close(st.out, ref["out"], "short")
+    assert_lse_close(st.lse, ref["lse"], "short")
+    for r, Lr in enumerate(lens):
+        if Lr == 0:
+            assert torch.all(st.out[r].float() == 0) and torch.all(torch.isneginf(st.lse[r]))
+
+
+def test_topk_covering_all_blocks_equals_dense():
+    lens = (4105, 3001, 777)
+    w = small("b16_small", seq_lens=lens, k_blocks=300, sink=16, recent=25)
+    cpu = make_inputs(w, "cpu")
+    g = to_dev(cpu)
+    st = GpuStep(w, g)
+    st.run()
+    check_status_clean()
+    d = oracle.dense(cpu["q"], oracle_cache(cpu), cpu["page_table"], cpu["seq_lens"], num_q_heads=w.num_q_heads,
+                     scale=w.softmax_scale)
+    assert_attention_close(st.out, d["out"], "dense")
+    assert_lse_close(st.lse, d["lse"], "dense")
+
+
+def test_only_forced_tokens_when_k_is_zero():
+    w = small("ragged_small", k_blocks=0)
+    cpu = make_inputs(w, "cpu")
+    g = to_dev(cpu)
+    st = GpuStep(w, g)
+    st.run()
+    check_status_clean()
+    ref = oracle_decode(w, cpu)
+    assert_attention_close(st.out, ref["out"], "k=0")
+
+
+def test_empty_batch_is_a_no_op():
+    w = small("tiny")
+    cpu = make_inputs(w, "cpu")
+    g = to_dev(cpu)
+    cache = L.make_cache(g["k_cache"], g["v_cache"])
+    prm = L.make_params(0, w.num_q_heads, cpu["max_blocks"], w.k_blocks, w.sink, w.recent)
+    out = torch.empty((1, 4, 64), dtype=torch.bfloat16, device="cuda")
+    L.lsa_decode_step(g["q"], cache, g["k_cache"], None, g["page_table"], g["seq_lens"], prm, None, out, None, None)
+    check_status_clean()
+
+
+def test_vortex_figure2_shared_pages_gpu():
+    gold = json.load(open(os.path.join(GOLD, "vortex_fig2_paged_layout.json")))
+    P, H, b, d, Hq = gold["num_pages"], 2, 16, 64, 8
+    gen = torch.Generator().manual_seed(21)
+    k = torch.randn((P, H, b, d), generator=gen).to(torch.bfloat16)
+    v = torch.randn((P, H, b, d), generator=gen).to(torch.bfloat16)
+    q = torch.randn((3, Hq, d), generator=gen).to(torch.bfloat16)
+    pt = torch.tensor([gold["page_tables"][x] for x in ("x0", "x1", "x2")], dtype=torch.int32)
+    lens = torch.tensor([48, 40, 47], dtype=torch.int32)
+    cache = L.make_cache(k.cuda(), v.cuda())
+    summ = torch.zeros((P, H, d), dtype=torch.bfloat16, device="cuda")
+    L.lsa_build_summaries(cache, pt.cuda(), lens.cuda(), summ)
+    prm = L.make_params(3, Hq, 3, 1, 16, 16, 0.2)
+    ws = torch.empty(max(16, L.lsa_decode_step_workspace_size(cache, prm)), dtype=torch.uint8, device="cuda")
+    out = torch.empty((3, Hq, d), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((3, H, 1), dtype=torch.int32, device="cuda")
+    L.lsa_decode_step(q.cuda(), cache, summ, None, pt.cuda(), lens.cuda(), prm, idx, out, None, ws)
+    check_status_clean()
+    ref = oracle.decode(q, oracle.Cache(k, v), pt, lens, num_q_heads=Hq, k_blocks=1, sink=16, recent=16, scale=0.2)
+    assert np.array_equal(idx.cpu().numpy(), ref["sel"])
+    assert_attention_close(out, ref["out"], "fig2")
+
+
+def test_bad_page_id_is_flagged_not_faulted():
+    w = small("tiny")
+    cpu = make_inputs(w, "cpu")
+    g = to_dev(cpu)
+    st = GpuStep(w, g)
+    bad = g["page_table"].clone()
+    bad[0, 5] = 10 ** 6          # out of range: the kernels check and skip it
+    bad[0, 9] = -3
+    g2 = dict(g, page_table=bad)
+    st.g = g2
+    st.run()
+    torch.cuda.synchronize()
+    code, flags = L.lsa_get_device_status(clear=True)
+    assert code == L.LSA_ERR_BOUNDS
+    assert torch.isfinite(st.out.float()).all()
+
+
+# ---------------------------------------------------------------- coarse-to-fine
+
+def test_fine_topk_matches_oracle():
+    w = small("c2f_small")
+    cpu = make_inputs(w, "cpu")
+    g = to_dev(cpu)
+    ref = oracle_decode(w, cpu)
+    ic = L.make_cache(g["idx_keys"], None, k_scale=g["idx_scale"])
+    prm = L.make_params(w.batch, w.num_q_heads, cpu["max_blocks"], 0, w.sink, w.recent, w.softmax_scale,
+                        w.c2f_candidates, w.c2f_tokens)
+    cand = torch.from_numpy(ref["cand"]).cuda()
+    tok = torch.empty((w.batch, 1, w.c2f_tokens), dtype=torch.int32, device="cuda")
+    ws = torch.empty(w.batch * w.c2f_candidates * w.block_size * 4 + 256, dtype=torch.uint8, device="cuda")
+    L.lsa_fine_topk(g["q"], ic, g["page_table"], g["seq_lens"], cand, prm, tok, ws)
+    check_status_clean()
+    assert np.array_equal(tok.cpu().numpy(), ref["sel"])
+    # fine tokens lie inside the coarse candidates
+    for r in range(w.batch):
+        cs = set(ref["cand"][r, 0].tolist())
+        assert all(t // w.block_size in cs for t in tok[r, 0].cpu().tolist() if t >= 0)
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+FULL = [("b16_32k", [0, 15]), ("ragged", [3, 40]), ("c2f", [1]), ("mla", [2])]
+
+
+@pytest.mark.parametrize("name,reqs", FULL)
+def test_full_size_sampled_requests(name, reqs):
+    w = WORKLOADS[name]
+    inp = make_inputs(w, "cuda")
+    run_and_compare_step(w, inp, inp, reqs=reqs)

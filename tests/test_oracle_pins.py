@@ -488,3 +488,24 @@ def test_mla_aliased_v_equals_copied_v():
     assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["sel"], b["sel"])
     o, lse = np_dense(inp, w, 1, 5, tokens=None)  # spot-check the dense path shape
     assert o.shape == (w.dv,)
+
+
+def test_attend_selection_reproduces_decode_and_dense():
+    w, inp = tiny_inputs()
+    c = cache_of(inp, w)
+    args = dict(num_q_heads=w.num_q_heads, sink=w.sink, recent=w.recent, scale=w.softmax_scale)
+    res = oracle.decode(inp["q"], c, inp["page_table"], inp["seq_lens"], k_blocks=w.k_blocks, **args)
+    a = oracle.attend_selection(inp["q"], c, inp["page_table"], inp["seq_lens"], res["sel"], **args)
+    assert np.array_equal(a["out"], res["out"]) and np.array_equal(a["lse"], res["lse"])
+    # every candidate block selected (block-aligned forced ranges) = dense
+    allc = np.arange(1, 63, dtype=np.int32)[None, None]
+    a = oracle.attend_selection(inp["q"], c, inp["page_table"], inp["seq_lens"], allc, **args)
+    d = oracle.dense(inp["q"], c, inp["page_table"], inp["seq_lens"], num_q_heads=w.num_q_heads,
+                     scale=w.softmax_scale)
+    assert np.allclose(a["lse"], d["lse"], atol=1e-12)
+    # invalid entries (forced block, out of range, repeated) are skipped
+    junk = np.array([[[0, 5, 5, 63, 200, -1]]], dtype=np.int32)
+    one = np.array([[[5]]], dtype=np.int32)
+    x = oracle.attend_selection(inp["q"], c, inp["page_table"], inp["seq_lens"], junk, **args)
+    y = oracle.attend_selection(inp["q"], c, inp["page_table"], inp["seq_lens"], one, **args)
+    assert np.array_equal(x["out"], y["out"])
