@@ -207,6 +207,8 @@ def topk(scores, k: int) -> np.ndarray:
     (an fp32 input converts exactly)."""
     lib = _load()
     s = np.ascontiguousarray(np.asarray(scores, dtype=np.float64))
+    if s.shape[-1] == 0:
+        return np.full(s.shape[:-1] + (k,), -1, dtype=np.int32)
     s2 = s.reshape(-1, s.shape[-1])
     out = np.empty((s2.shape[0], k), dtype=np.int32)
     for i in range(s2.shape[0]):
