@@ -131,7 +131,7 @@ class Instance:
             nsel = w.k_blocks
         self.params = L.make_params(B, w.num_q_heads, g["max_blocks"], w.k_blocks, w.sink, w.recent,
                                     w.softmax_scale, w.c2f_candidates, w.c2f_tokens)
-        self.ws = torch.empty(max(16, L.lsa_decode_step_workspace_size(self.cache, self.params)),
+        self.ws = torch.zeros(max(16, L.lsa_decode_step_workspace_size(self.cache, self.params)),
                               dtype=torch.uint8, device=dev)
         self.idx = torch.empty((B, Hkv, max(1, nsel)), dtype=torch.int32, device=dev)
         self.out = torch.empty((B, w.num_q_heads, w.dv), dtype=torch.bfloat16, device=dev)
@@ -155,38 +155,62 @@ def kernels_per_step(inst) -> int:
     return n + (1 if ws_attn > 0 else 0)
 
 
-def stage_times(inst, reps: int, stream) -> dict:
-    """Average device time of each stage, timed with CUDA events around the
-    stage's entry-point call (score, top-k, attention+merge), cycling L2-cold
-    over the instances."""
-    L, g, w = inst.L, inst.g, inst.w
+def stage_times(insts, reps: int, stream) -> dict:
+    """Average device time of each stage (score, top-k, attention + merge),
+    each captured in a CUDA graph of `reps` calls through the individual entry
+    points (the same kernels the fused call launches), rotating L2-cold over
+    the instances."""
+    w = insts[0].w
     if w.c2f_candidates > 0:
         return {}
+    L = insts[0].L
     B, Hkv = w.batch, w.num_kv_heads
-    scores = torch.empty((B * Hkv, g["max_blocks"]), dtype=torch.float32, device=g["q"].device)
-    idx = torch.empty((B * Hkv, max(1, w.k_blocks)), dtype=torch.int32, device=g["q"].device)
-    ws = torch.empty(max(16, L.lsa_sparse_decode_workspace_size(inst.cache, inst.params)), dtype=torch.uint8,
-                     device=g["q"].device)
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=g["q"].device)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-    acc = {"score": 0.0, "topk": 0.0, "attention": 0.0}
+    bufs = []
+    for it in insts:
+        g = it.g
+        dev = g["q"].device
+        bufs.append(dict(
+            scores=torch.empty((B * Hkv, g["max_blocks"]), dtype=torch.float32, device=dev),
+            idx=torch.empty((B * Hkv, max(1, w.k_blocks)), dtype=torch.int32, device=dev),
+            ws=torch.zeros(max(16, L.lsa_sparse_decode_workspace_size(it.cache, it.params)), dtype=torch.uint8,
+                           device=dev)))
+    R = len(insts)
+
+    def score(i):
+        it, b = insts[i % R], bufs[i % R]
+        L.lsa_score(it.g["q"], it.cache, it.summ, it.g["page_table"], it.g["seq_lens"], it.params, b["scores"],
+                    stream)
+
+    def topk(i):
+        b = bufs[i % R]
+        L.lsa_topk(b["scores"], None, w.k_blocks, b["idx"], stream)
+
+    def attn(i):
+        it, b = insts[i % R], bufs[i % R]
+        L.lsa_sparse_decode(it.g["q"], it.cache, it.g["page_table"], it.g["seq_lens"], b["idx"].view(B, Hkv, -1),
+                            it.params, it.out, it.lse, b["ws"], stream)
+
+    out = {}
     with torch.cuda.stream(stream):
-        for i in range(reps + 2):
-            flush.zero_()
-            ev[0].record(stream)
-            L.lsa_score(g["q"], inst.cache, inst.summ, g["page_table"], g["seq_lens"], inst.params, scores, stream)
-            ev[1].record(stream)
-            L.lsa_topk(scores, None, w.k_blocks, idx, stream)
-            ev[2].record(stream)
-            L.lsa_sparse_decode(g["q"], inst.cache, g["page_table"], g["seq_lens"], idx.view(B, Hkv, -1),
-                                inst.params, inst.out, inst.lse, ws, stream)
-            ev[3].record(stream)
+        for i in range(R):
+            score(i)
+            topk(i)
+            attn(i)
+        stream.synchronize()
+        for name, fn in (("score", score), ("topk", topk), ("attention", attn)):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                for i in range(reps):
+                    fn(i)
+            gr.replay()
             stream.synchronize()
-            if i >= 2:
-                acc["score"] += ev[0].elapsed_time(ev[1])
-                acc["topk"] += ev[1].elapsed_time(ev[2])
-                acc["attention"] += ev[2].elapsed_time(ev[3])
-    return {k: v / reps for k, v in acc.items()}
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gr.replay()
+            e1.record(stream)
+            stream.synchronize()
+            out[name] = e0.elapsed_time(e1) / reps
+    return out
 
 
 def run_gpu(args, rank, world, dev):
@@ -268,7 +292,7 @@ def run_gpu(args, rank, world, dev):
         ms = float(t.item())
 
     # per-stage split (separate untimed-for-value pass, L2 flushed before each)
-    st = stage_times(insts[0], 20, stream)
+    st = stage_times(insts, 8 * len(insts), stream)
 
     # end to end through the public call with host buffers: every step copies
     # q, page table and lengths from pinned host memory and reads back out/lse

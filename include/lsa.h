@@ -195,7 +195,9 @@ lsa_status lsa_fine_topk(const void *q, const lsa_cache *index_cache, const int3
 /* Step 4: sparse attention ------------------------------------------------ */
 
 /* Bytes of workspace lsa_sparse_decode needs for these shapes (split-K
- * partials). */
+ * partials and, for the persistent kernel, control counters).  The same
+ * rules as lsa_decode_step's workspace apply: zero-filled before first use,
+ * left zero-filled by every call that completes without a device error. */
 size_t lsa_sparse_decode_workspace_size(const lsa_cache *cache, const lsa_params *params);
 
 /* Exact attention over T = F U selected for every query head:
@@ -217,6 +219,14 @@ lsa_status lsa_sparse_decode(const void *q, const lsa_cache *cache, const int32_
 
 /* Fused decode step ------------------------------------------------------- */
 
+/* Bytes of workspace lsa_decode_step needs.  The workspace holds the
+ * block scores, the selection, split partials and (for the fused
+ * persistent kernel) a small block of control counters: it must be
+ * zero-filled once before its first use (e.g. cudaMemsetAsync after
+ * allocation).  Every call that completes without a device error leaves it
+ * zero-filled, so one workspace serves any number of calls and CUDA-graph
+ * replays on one stream; after a call that recorded LSA_ERR_TIMEOUT, zero it
+ * again.  Calls that share a workspace must not overlap in time. */
 size_t lsa_decode_step_workspace_size(const lsa_cache *cache, const lsa_params *params);
 
 /* Steps 2-4 in one call: score every candidate block against the summaries,

@@ -4,6 +4,7 @@
 // contract of every function.
 #include <math.h>
 #include <mutex>
+#include <stdlib.h>
 #include <string.h>
 
 #include "lsa_internal.h"
@@ -124,6 +125,7 @@ float scale_of(const lsa_params *p, int dk)
 
 struct AttnPlan {
     int nsub, splits, items_per_split;
+    int tc_group;          // > 0: tensor-core kernel with this many heads per CTA
     size_t ws_bytes;
 };
 
@@ -131,8 +133,15 @@ lsa_status plan_attention(const CacheView &v, const lsa_params *p, bool token_mo
 {
     const int G = p->num_q_heads / v.hkv;
     int gs = 0;
-    if (!attention_supported(v.dk, v.dv, G, v.v_alias != 0, &gs)) return LSA_ERR_UNSUPPORTED;
     if (v.b % kChunk != 0) return LSA_ERR_UNSUPPORTED;
+    const char *path = getenv("LSA_ATTENTION_PATH");
+    const bool allow_tc = !(path && strcmp(path, "cuda_core") == 0);
+    pl->tc_group = allow_tc ? attention_tc_group(v.dk, v.dv, G, v.v_alias != 0, token_mode, v) : 0;
+    if (pl->tc_group > 0) {
+        gs = pl->tc_group;
+    } else if (!attention_supported(v.dk, v.dv, G, v.v_alias != 0, &gs)) {
+        return LSA_ERR_UNSUPPORTED;
+    }
     pl->nsub = G / gs;
     const int nsel = token_mode ? p->c2f_tokens : p->k_blocks;
     const int items = attention_items_max(p->sink_tokens, p->recent_tokens, v.b, nsel, token_mode);
@@ -144,6 +153,12 @@ lsa_status plan_attention(const CacheView &v, const lsa_params *p, bool token_mo
     }
     s = s < 1 ? 1 : (s > items ? items : s);
     if (s > 65535) s = 65535;
+    // every split's item descriptors must fit in shared memory
+    const int max_ips = pl->tc_group > 0 ? attention_tc_max_items_per_split(v.dk)
+                                          : attention_max_items_per_split(v.dk, v.dv, v.v_alias != 0, token_mode);
+    if (max_ips < 1) return LSA_ERR_UNSUPPORTED;
+    const int min_s = (items + max_ips - 1) / max_ips;
+    if (s < min_s) s = min_s;
     pl->items_per_split = (items + s - 1) / s;
     pl->splits = (items + pl->items_per_split - 1) / pl->items_per_split;
     if (pl->splits < 1) pl->splits = 1;
@@ -191,7 +206,7 @@ lsa_status run_attention(const void *q, const CacheView &v, const int32_t *pt, c
         a.lse_part = reinterpret_cast<float *>(ws + round_up(rowsq * v.dv * sizeof(float)));
     }
     bool unsup = false;
-    cudaError_t e = launch_attention(a, st, &unsup);
+    cudaError_t e = pl.tc_group > 0 ? launch_attention_tc(a, pl.tc_group, st, &unsup) : launch_attention(a, st, &unsup);
     if (unsup) return LSA_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return LSA_ERR_CUDA;
     if (pl.splits > 1) {
@@ -229,6 +244,103 @@ lsa_status step_layout(const CacheView &v, const CacheView *iv, const lsa_params
     L->attn = pl.ws_bytes;
     L->total = L->scores + L->sel + L->cand + L->fine + L->attn;
     return LSA_OK;
+}
+
+// Workspace of the persistent kernel: [control counters | scores |
+// selection | page ids of the selection | part outputs | part lse].
+struct FusedLayout {
+    size_t ctrl, scores, sel, selpg, opart, lpart, total;
+    FusedPlan plan;
+};
+
+// Which implementation runs a step: LSA_DECODE_PATH=fused takes the
+// persistent kernel wherever it applies, =pipeline the stage-by-stage
+// kernels; unset, kFusedByDefault decides.
+constexpr bool kFusedByDefault = false;
+
+bool use_fused(const CacheView &v, const lsa_params *p)
+{
+    const char *e = getenv("LSA_DECODE_PATH");
+    const bool want = e ? strcmp(e, "fused") == 0 : kFusedByDefault;
+    if (!want) return false;
+    if (p->c2f_candidates > 0 || p->num_splits > 0) return false;
+    return fused_supported(v.dk, v.dv, v.hkv, p->num_q_heads / v.hkv, v.v_alias != 0, v.b, p->max_blocks,
+                           p->k_blocks);
+}
+
+void fused_layout(const CacheView &v, const lsa_params *p, bool scoring, FusedLayout *L)
+{
+    fused_plan(p->sink_tokens, p->recent_tokens, v.b, p->k_blocks, p->batch, v.hkv, p->max_blocks, scoring,
+               &L->plan);
+    const size_t rows = (size_t)p->batch * v.hkv;
+    const size_t rowsq = (size_t)p->batch * p->num_q_heads * L->plan.units_per_row;
+    // each counter on its own 256-byte line (64 words apart): the ticket, the
+    // leave counter, one per request and two per (request, KV head)
+    L->ctrl = round_up((2 + (size_t)p->batch + 2 * rows) * 64 * sizeof(uint32_t));
+    L->scores = scoring ? round_up(rows * p->max_blocks * sizeof(float)) : 0;
+    L->sel = scoring ? round_up(rows * p->k_blocks * sizeof(int32_t)) : 0;
+    L->selpg = 0;
+    L->opart = L->plan.units_per_row > 1 ? round_up(rowsq * v.dv * sizeof(float)) : 0;
+    L->lpart = L->plan.units_per_row > 1 ? round_up(rowsq * sizeof(float)) : 0;
+    L->total = L->ctrl + L->scores + L->sel + L->selpg + L->opart + L->lpart;
+}
+
+// scoring: the whole step (scores, top-k, attention); otherwise attention
+// only, over the caller's selection `sel`.
+lsa_status run_fused(const void *q, const CacheView &v, const void *summaries, const int32_t *pt,
+                     const int32_t *lens, const lsa_params *p, bool scoring, int32_t *sel, void *out, float *lse,
+                     uint8_t *ws, cudaStream_t st)
+{
+    FusedLayout L;
+    fused_layout(v, p, scoring, &L);
+    FusedArgs a;
+    memset(&a, 0, sizeof a);
+    a.q = static_cast<const uint16_t *>(q);
+    a.c = v;
+    a.summ = static_cast<const uint16_t *>(summaries);
+    a.pt = pt;
+    a.lens = lens;
+    a.batch = p->batch;
+    a.hq = p->num_q_heads;
+    a.max_blocks = p->max_blocks;
+    a.k_blocks = p->k_blocks;
+    a.sink = p->sink_tokens;
+    a.recent = p->recent_tokens;
+    a.scale_log2 = scale_of(p, v.dk) * 1.4426950408889634f;
+    a.score_blocks = L.plan.score_blocks;
+    a.score_chunks = L.plan.score_chunks;
+    a.score_units = L.plan.score_units;
+    a.attn_base = L.plan.attn_base;
+    a.total_units = L.plan.total_units;
+    a.units_per_row = L.plan.units_per_row;
+    a.chunks_per_unit = L.plan.chunks_per_unit;
+    a.wait_ready = scoring;
+    uint8_t *cur = ws;
+    a.ctrl = reinterpret_cast<uint32_t *>(cur);            // [0] ticket, [64] leave counter
+    a.score_done = a.ctrl + 2 * 64;
+    a.ready = a.score_done + (size_t)p->batch * 64;
+    a.split_done = a.ready + (size_t)p->batch * v.hkv * 64;
+    cur += L.ctrl;
+    a.scores = reinterpret_cast<float *>(cur);
+    cur += L.scores;
+    a.sel = sel ? sel : reinterpret_cast<int32_t *>(cur);
+    cur += L.sel;
+    a.sel_pg = nullptr;
+    cur += L.selpg;
+    a.o_part = reinterpret_cast<float *>(cur);
+    cur += L.opart;
+    a.lse_part = reinterpret_cast<float *>(cur);
+    a.out = static_cast<uint16_t *>(out);
+    a.lse = lse;
+    a.status = status_word();
+    a.spin_budget = kSpinBudget;
+#ifdef LSA_FUSED_TRACE
+    if (const char *tp = getenv("LSA_TRACE_PTR")) a.trace = reinterpret_cast<uint64_t *>(strtoull(tp, nullptr, 0));
+#endif
+    bool unsup = false;
+    cudaError_t e = launch_fused(a, st, sm_count(), &unsup);
+    if (unsup) return LSA_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? LSA_OK : LSA_ERR_CUDA;
 }
 
 }  // namespace
@@ -346,6 +458,7 @@ lsa_status lsa_score(const void *q, const lsa_cache *cache, const void *summarie
     a.max_blocks = params->max_blocks;
     a.sink = params->sink_tokens;
     a.recent = params->recent_tokens;
+    a.chunk = score_chunk(params->batch, params->max_blocks, sm_count());
     a.scores = scores;
     a.status = status_word();
     bool unsup = false;
@@ -430,7 +543,13 @@ size_t lsa_sparse_decode_workspace_size(const lsa_cache *cache, const lsa_params
     if (make_view(cache, true, &v) != LSA_OK || check_params(params, v) != LSA_OK) return 0;
     AttnPlan pl;
     if (plan_attention(v, params, params->c2f_candidates > 0, &pl) != LSA_OK) return 0;
-    return pl.ws_bytes;
+    size_t need = pl.ws_bytes;
+    if (use_fused(v, params)) {
+        FusedLayout F;
+        fused_layout(v, params, false, &F);
+        if (F.total > need) need = F.total;
+    }
+    return need;
 }
 
 lsa_status lsa_sparse_decode(const void *q, const lsa_cache *cache, const int32_t *page_table,
@@ -446,6 +565,13 @@ lsa_status lsa_sparse_decode(const void *q, const lsa_cache *cache, const int32_
     const int nsel = token_mode ? params->c2f_tokens : params->k_blocks;
     if (!q || !page_table || !seq_lens || !out || !aligned16(q) || (nsel > 0 && !idx)) return LSA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(out) & 7u) != 0) return LSA_ERR_INVALID_ARG;
+    if (use_fused(v, params)) {
+        FusedLayout F;
+        fused_layout(v, params, false, &F);
+        if (!workspace || workspace_bytes < F.total || !aligned16(workspace)) return LSA_ERR_WORKSPACE;
+        return run_fused(q, v, nullptr, page_table, seq_lens, params, false, const_cast<int32_t *>(idx), out, lse,
+                         static_cast<uint8_t *>(workspace), reinterpret_cast<cudaStream_t>(stream));
+    }
     return run_attention(q, v, page_table, seq_lens, nsel > 0 ? idx : nullptr, params, token_mode, out, lse,
                          static_cast<uint8_t *>(workspace), workspace_bytes,
                          reinterpret_cast<cudaStream_t>(stream));
@@ -456,13 +582,15 @@ size_t lsa_decode_step_workspace_size(const lsa_cache *cache, const lsa_params *
     CacheView v;
     if (make_view(cache, true, &v) != LSA_OK || check_params(params, v) != LSA_OK) return 0;
     StepLayout L;
-    CacheView iv = v;
-    if (params->c2f_candidates > 0) {
-        // the index cache shares the paging; only its geometry matters here
-        iv.hkv = v.hkv;
-    }
+    CacheView iv = v;   // the index cache shares paging and geometry with the attention cache
     if (step_layout(v, &iv, params, &L) != LSA_OK) return 0;
-    return L.total;
+    size_t need = L.total;
+    if (use_fused(v, params)) {
+        FusedLayout F;
+        fused_layout(v, params, true, &F);
+        if (F.total > need) need = F.total;
+    }
+    return need;
 }
 
 lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *summaries,
@@ -486,6 +614,14 @@ lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *su
     if (!q || !summaries || !page_table || !seq_lens || !out || !aligned16(q) || !aligned16(summaries))
         return LSA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(out) & 7u) != 0) return LSA_ERR_INVALID_ARG;
+    cudaStream_t st0 = reinterpret_cast<cudaStream_t>(stream);
+    if (use_fused(v, params)) {
+        FusedLayout F;
+        fused_layout(v, params, true, &F);
+        if (!workspace || workspace_bytes < F.total || !aligned16(workspace)) return LSA_ERR_WORKSPACE;
+        return run_fused(q, v, summaries, page_table, seq_lens, params, true, idx_out, out, lse,
+                         static_cast<uint8_t *>(workspace), st0);
+    }
     StepLayout L;
     if ((rc = step_layout(v, &iv, params, &L)) != LSA_OK) return rc;
     if (L.total > 0 && (!workspace || workspace_bytes < L.total)) return LSA_ERR_WORKSPACE;
@@ -515,6 +651,7 @@ lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *su
     s.max_blocks = params->max_blocks;
     s.sink = params->sink_tokens;
     s.recent = params->recent_tokens;
+    s.chunk = score_chunk(params->batch, params->max_blocks, sm_count());
     s.scores = scores;
     s.status = status;
     bool unsup = false;

@@ -20,6 +20,7 @@
 // lane groups, then the warps, are merged by log-sum-exp at the end.
 #include <math.h>
 
+#include "attn_items.cuh"
 #include "lsa_device.cuh"
 
 namespace lsa {
@@ -28,6 +29,7 @@ namespace {
 constexpr int kConsumerWarps = 4;
 constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
 constexpr float kLn2 = 0.693147180559945309f;
+constexpr int kAttnMaxSmem = 200 * 1024;
 
 __device__ __forceinline__ float ex2(float x)
 {
@@ -49,111 +51,37 @@ struct Layout {
     static constexpr int VROW = DV * 2;
     static constexpr int VOFF = ALIAS ? 0 : kChunk * KROW;        // V rows within a slot
     static constexpr int VSTRIDE = ALIAS ? KROW : VROW;            // bytes between V rows
-    static constexpr int SLOT = kChunk * (KROW + (ALIAS ? 0 : VROW));
+    static constexpr int ROWB = KROW + (ALIAS ? 0 : VROW);         // bytes staged per token
+    static constexpr int SLOT = kChunk * ROWB;
     static constexpr int NSLOT = SLOT <= 8192 ? 8 : 4;
     static constexpr int BAR_OFF = NSLOT * SLOT;
-    static constexpr int SMEM = BAR_OFF + NSLOT * 16 + NSLOT * 4 + 16;
-};
-
-// Row plan of one (request): forced ranges and item counts.
-struct RowPlan {
-    int L, se, rs;
-    int nsc, nsel_items, nrc, n_items;
-};
-
-__device__ __forceinline__ RowPlan make_plan(const AttnArgs &a, int r, bool flag_bad)
-{
-    RowPlan pl;
-    int L = a.lens[r];
-    if (L < 0 || (int64_t)L > (int64_t)a.max_blocks * a.c.b) {
-        if (flag_bad) flag_error(a.status, LSA_ERR_BOUNDS);
-        L = 0;
+    static constexpr int DESC_OFF = BAR_OFF + NSLOT * 16 + NSLOT * 4 + 16;   // 16-byte aligned
+    static int smem_bytes(int ips, int token_mode)
+    {
+        return DESC_OFF + ips * (int)sizeof(ItemDesc) + (token_mode ? ips * kChunk * (int)sizeof(int2) : 0);
     }
-    pl.L = L;
-    pl.se = min(a.sink, L);
-    pl.rs = max(L - a.recent, pl.se);
-    pl.nsc = (pl.se + kChunk - 1) / kChunk;
-    pl.nsel_items = a.token_mode ? (a.nsel + kChunk - 1) / kChunk : a.nsel * (a.c.b / kChunk);
-    pl.nrc = L > pl.rs ? (L + kChunk - 1) / kChunk - pl.rs / kChunk : 0;
-    pl.n_items = pl.nsc + pl.nsel_items + pl.nrc;
-    return pl;
-}
+};
 
-// Producer side: stage item i of row (r, h) into `dst`; returns the number
-// of token rows staged (0 = nothing to attend in this item).
+// Producer: issue the bulk copies of one described item into a slot;
+// returns the rows staged.  `nslot` is written before the barrier is armed.
 template <int DK, int DV, bool ALIAS>
-__device__ int stage_item(const AttnArgs &a, const RowPlan &pl, int r, int h, int i, uint8_t *dst,
+__device__ int issue_item(const AttnArgs &a, int h, const ItemDesc &d, const int2 *rows, uint8_t *dst,
                           uint64_t *bar, int *nslot)
 {
     using LY = Layout<DK, DV, ALIAS>;
     const CacheView &c = a.c;
-    const int b = c.b;
-    const int32_t *ptr = a.pt + (int64_t)r * a.max_blocks;
-    const int64_t row = (int64_t)r * c.hkv + h;
-    const int32_t *irow = a.idx ? a.idx + row * a.nsel : nullptr;
-
-    int t0 = 0, n = 0;
-    bool list = false;
-    int toks[kChunk];
-    if (i < pl.nsc) {
-        t0 = i * kChunk;
-        n = min(kChunk, pl.se - t0);
-    } else if (i < pl.nsc + pl.nsel_items) {
-        const int k = i - pl.nsc;
-        if (!a.token_mode) {
-            const int cpb = b / kChunk;
-            const int ei = k / cpb, ck = k % cpb;
-            const int e = irow[ei];
-            const bool valid = e >= 0 && e < a.max_blocks && (int64_t)e * b >= pl.se &&
-                               (int64_t)(e + 1) * b <= pl.rs && (ei == 0 || irow[ei - 1] < e);
-            if (!valid && e != -1 && ck == 0) flag_error(a.status, LSA_ERR_BOUNDS);
-            if (valid) {
-                t0 = e * b + ck * kChunk;
-                n = kChunk;
-            }
-        } else {
-            list = true;
-            for (int u = 0; u < kChunk; ++u) {
-                const int ei = k * kChunk + u;
-                if (ei >= a.nsel) break;
-                const int t = irow[ei];
-                if (t == -1) continue;
-                const int j = t / b;
-                const bool valid = t >= 0 && (int64_t)j * b >= pl.se && (int64_t)(j + 1) * b <= pl.rs &&
-                                   (ei == 0 || irow[ei - 1] < t);
-                if (!valid) {
-                    flag_error(a.status, LSA_ERR_BOUNDS);
-                    continue;
-                }
-                toks[n++] = t;
-            }
-        }
-    } else {
-        const int k = i - pl.nsc - pl.nsel_items;
-        const int blk16 = pl.rs / kChunk + k;
-        t0 = max(pl.rs, blk16 * kChunk);
-        n = min(pl.L, blk16 * kChunk + kChunk) - t0;
-    }
-    if (n <= 0) return 0;
-
-    if (!list) {
-        const int p = ptr[t0 / b];
-        if (p < 0 || p >= c.num_pages) {
-            flag_error(a.status, LSA_ERR_BOUNDS);
-            return 0;
-        }
-        const uint32_t bytes = n * (LY::KROW + (ALIAS ? 0 : LY::VROW));
+    if (d.n > 0) {
+        const int n = d.n;
         *nslot = n;   // visible to the consumer through the arrive's release
-        mbar_arrive_expect_tx(bar, bytes);
-        const int ts = t0 % b;
-        const uint8_t *ks = c.k + ((int64_t)p * c.kps + (int64_t)h * c.khs + (int64_t)ts * c.kts) * 2;
+        mbar_arrive_expect_tx(bar, n * LY::ROWB);
+        const uint8_t *ks = c.k + ((int64_t)d.page * c.kps + (int64_t)h * c.khs + (int64_t)d.ts * c.kts) * 2;
         if (c.kts == DK) {
             bulk_g2s(dst, ks, n * LY::KROW, bar);
         } else {
             for (int u = 0; u < n; ++u) bulk_g2s(dst + u * LY::KROW, ks + (int64_t)u * c.kts * 2, LY::KROW, bar);
         }
         if constexpr (!ALIAS) {
-            const uint8_t *vs = c.v + ((int64_t)p * c.vps + (int64_t)h * c.vhs + (int64_t)ts * c.vts) * 2;
+            const uint8_t *vs = c.v + ((int64_t)d.page * c.vps + (int64_t)h * c.vhs + (int64_t)d.ts * c.vts) * 2;
             if (c.vts == DV) {
                 bulk_g2s(dst + LY::VOFF, vs, n * LY::VROW, bar);
             } else {
@@ -163,32 +91,25 @@ __device__ int stage_item(const AttnArgs &a, const RowPlan &pl, int r, int h, in
         }
         return n;
     }
-    // token list: one row copy per token
+    if (d.n == 0) return 0;
+    int n = 0;
+    for (int u = 0; u < kChunk; ++u) n += rows[u].x >= 0;
+    if (n == 0) return 0;
+    *nslot = n;
+    mbar_arrive_expect_tx(bar, n * LY::ROWB);
     int m = 0;
-    int pages[kChunk];
-    for (int u = 0; u < n; ++u) {
-        const int p = ptr[toks[u] / b];
-        if (p < 0 || p >= c.num_pages) {
-            flag_error(a.status, LSA_ERR_BOUNDS);
-            continue;
+    for (int u = 0; u < kChunk; ++u) {
+        const int2 rw = rows[u];
+        if (rw.x < 0) continue;
+        const uint8_t *ks = c.k + ((int64_t)rw.x * c.kps + (int64_t)h * c.khs + (int64_t)rw.y * c.kts) * 2;
+        bulk_g2s(dst + m * LY::KROW, ks, LY::KROW, bar);
+        if constexpr (!ALIAS) {
+            const uint8_t *vs = c.v + ((int64_t)rw.x * c.vps + (int64_t)h * c.vhs + (int64_t)rw.y * c.vts) * 2;
+            bulk_g2s(dst + LY::VOFF + m * LY::VROW, vs, LY::VROW, bar);
         }
-        pages[m] = p;
-        toks[m] = toks[u];
         ++m;
     }
-    if (m == 0) return 0;
-    *nslot = m;
-    mbar_arrive_expect_tx(bar, m * (LY::KROW + (ALIAS ? 0 : LY::VROW)));
-    for (int u = 0; u < m; ++u) {
-        const int ts = toks[u] % b;
-        const uint8_t *ks = c.k + ((int64_t)pages[u] * c.kps + (int64_t)h * c.khs + (int64_t)ts * c.kts) * 2;
-        bulk_g2s(dst + u * LY::KROW, ks, LY::KROW, bar);
-        if constexpr (!ALIAS) {
-            const uint8_t *vs = c.v + ((int64_t)pages[u] * c.vps + (int64_t)h * c.vhs + (int64_t)ts * c.vts) * 2;
-            bulk_g2s(dst + LY::VOFF + u * LY::VROW, vs, LY::VROW, bar);
-        }
-    }
-    return m;
+    return n;
 }
 
 template <int DK, int DV, int GS, bool ALIAS>
@@ -204,6 +125,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_sparse_attn(AttnArgs a)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + LY::BAR_OFF);
     uint64_t *empty = full + NSLOT;
     int *item_n = reinterpret_cast<int *>(empty + NSLOT);
+    ItemDesc *descs = reinterpret_cast<ItemDesc *>(smem + LY::DESC_OFF);
+    int2 *rows = reinterpret_cast<int2 *>(descs + a.items_per_split);
 
     const int split = blockIdx.x;
     const int h = blockIdx.y / a.nsub, sg = blockIdx.y % a.nsub;
@@ -222,6 +145,17 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_sparse_attn(AttnArgs a)
         }
         fence_barrier_init();
     }
+    // resolve every item of this split (selection entries, page ids) in
+    // parallel, so the producer streams without dependent global loads
+    for (int it = threadIdx.x; it < nloc; it += blockDim.x) descs[it] = describe_item(a, pl, r, h, i_begin + it);
+    if (a.token_mode) {
+        for (int u = threadIdx.x; u < nloc * kChunk; u += blockDim.x) {
+            const int i = i_begin + u / kChunk;
+            int2 rw = make_int2(-1, 0);
+            if (i >= pl.nsc && i < pl.nsc + pl.nsel_items) rw = describe_token(a, pl, r, h, i, u % kChunk);
+            rows[u] = rw;
+        }
+    }
     __syncthreads();
 
     float m[GS], l[GS];
@@ -234,9 +168,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_sparse_attn(AttnArgs a)
             for (int k = 0; k < nloc; ++k) {
                 const int slot = k % NSLOT;
                 if (k >= NSLOT && !mbar_wait(&empty[slot], ((k / NSLOT) - 1) & 1, a.status, a.spin_budget)) break;
-                uint8_t *dst = smem + slot * LY::SLOT;
-                const int n = stage_item<DK, DV, ALIAS>(a, pl, r, h, i_begin + k, dst, &full[slot],
-                                                        &item_n[slot]);
+                const int n = issue_item<DK, DV, ALIAS>(a, h, descs[k], rows + k * kChunk, smem + slot * LY::SLOT,
+                                                        &full[slot], &item_n[slot]);
                 if (n == 0) {
                     item_n[slot] = 0;
                     mbar_arrive(&full[slot]);
@@ -482,10 +415,12 @@ cudaError_t launch_attn_t(const AttnArgs &a, cudaStream_t s)
     static_assert(LY::NSLOT * LY::SLOT >= kConsumerWarps * GS * DV * 4 + 2 * kConsumerWarps * GS * 4,
                   "merge buffers must fit in the slot ring");
     auto kern = k_sparse_attn<DK, DV, GS, ALIAS>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM);
+    const int smem = LY::smem_bytes(a.items_per_split, a.token_mode);
+    if (smem > kAttnMaxSmem) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnMaxSmem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.splits, a.c.hkv * a.nsub, a.batch);
-    kern<<<grid, kAttnThreads, LY::SMEM, s>>>(a);
+    kern<<<grid, kAttnThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -496,9 +431,19 @@ bool attention_supported(int dk, int dv, int group, bool alias, int *sub_group)
     int gs = 0;
     if (dk == 64 && dv == 64 && !alias) gs = group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1);
     else if (dk == 128 && dv == 128 && !alias) gs = group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1);
-    else if (dk == 576 && dv == 512 && alias) gs = 1;
+    else if (dk == 576 && dv == 512) gs = 1;
     if (sub_group) *sub_group = gs;
     return gs > 0;
+}
+
+int attention_max_items_per_split(int dk, int dv, bool alias, int token_mode)
+{
+    const int rowb = dk * 2 + (alias ? 0 : dv * 2);
+    const int slot = kChunk * rowb;
+    const int nslot = slot <= 8192 ? 8 : 4;
+    const int fixed = nslot * slot + nslot * 20 + 16;
+    const int per = (int)sizeof(ItemDesc) + (token_mode ? kChunk * (int)sizeof(int2) : 0);
+    return (kAttnMaxSmem - fixed) / per;
 }
 
 int attention_items_max(int sink, int recent, int b, int nsel, int token_mode)
@@ -518,7 +463,7 @@ cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s, bool *unsupporte
     if (a.c.dk == DK_ && a.c.dv == DV_ && gs == GS_ && alias == AL_) return launch_attn_t<DK_, DV_, GS_, AL_>(a, s);
     LSA_ATTN_CASE(64, 64, 4, false) LSA_ATTN_CASE(64, 64, 2, false) LSA_ATTN_CASE(64, 64, 1, false)
     LSA_ATTN_CASE(128, 128, 4, false) LSA_ATTN_CASE(128, 128, 2, false) LSA_ATTN_CASE(128, 128, 1, false)
-    LSA_ATTN_CASE(576, 512, 1, true)
+    LSA_ATTN_CASE(576, 512, 1, true) LSA_ATTN_CASE(576, 512, 1, false)
 #undef LSA_ATTN_CASE
     *unsupported = true;
     return cudaSuccess;

@@ -49,6 +49,7 @@ struct ScoreArgs {
     const int32_t *lens;
     int32_t batch, hq, hkv, dk, b, num_pages, max_blocks;
     int32_t sink, recent;
+    int32_t chunk;              // blocks per CTA (score_chunk)
     float *scores;              // [B, hkv, max_blocks]
     uint32_t *status;
 };
@@ -94,12 +95,63 @@ struct AttnArgs {
     long long spin_budget;
 };
 
+// A staged item: a run of token rows within one page (n > 0), nothing to
+// attend (n == 0), or a list of single tokens resolved per row (n == -1).
+struct ItemDesc {
+    int32_t page;
+    int16_t ts;
+    int16_t n;
+};
+
+// Row multipliers of the 2-D [rows, dim] views the tensor-core attention
+// kernel loads K and V tiles from: row = page*page_rows + head*head_rows + slot.
+struct TcRows {
+    int64_t k_page_rows, k_head_rows, v_page_rows, v_head_rows;
+};
+
 struct MergeArgs {
     const float *o_part;
     const float *lse_part;
     int32_t rows, splits, dv;
     uint16_t *out;
     float *lse;
+};
+
+// Persistent decode kernel (one worker per warp): score units, top-k units
+// and attention units in one launch, or attention units alone.  Control
+// counters live in the workspace and must be zero before the first call;
+// every call that completes leaves them zero.
+struct FusedArgs {
+    const uint16_t *q;          // [B, Hq, dk]
+    CacheView c;
+    const uint16_t *summ;       // [num_pages, hkv, dk]
+    const int32_t *pt;
+    const int32_t *lens;
+    int32_t batch, hq, max_blocks, k_blocks, sink, recent;
+    float scale_log2;
+    // work units: [0, score_units) scores, [score_units, attn_base) top-k,
+    // [attn_base, total_units) attention parts
+    int32_t score_blocks, score_chunks, score_units, attn_base, total_units, units_per_row, chunks_per_unit;
+    int32_t wait_ready;         // attention waits for the row's top-k
+    int32_t total_warps;
+    float *scores;              // [B*hkv, max_blocks]
+    int32_t *sel;               // [B*hkv, k_blocks] selected blocks (ascending, -1 pad)
+    int32_t *sel_pg;            // [B*hkv, k_blocks] their page ids, or NULL (look up)
+    float *o_part;              // [B*Hq, units_per_row, dv]
+    float *lse_part;            // [B*Hq, units_per_row] (log2 units)
+    uint32_t *ctrl;             // [0] ticket, [1] workers done
+    uint32_t *score_done;       // [B]
+    uint32_t *ready;            // [B*hkv]
+    uint32_t *split_done;       // [B*hkv]
+    uint16_t *out;
+    float *lse;
+    uint32_t *status;
+    long long spin_budget;
+    uint64_t *trace;            // per-unit timeline (trace builds only), or NULL
+};
+
+struct FusedPlan {
+    int32_t units_per_row, chunks_per_unit, score_blocks, score_chunks, score_units, attn_base, total_units;
 };
 
 // ---- launchers (return a cudaError_t from the launch; LSA_ERR_UNSUPPORTED
@@ -111,11 +163,21 @@ cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s, bool *unsupported);
 cudaError_t launch_fine_scores(const FineArgs &a, cudaStream_t s, bool *unsupported);
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s, bool *unsupported);
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);
+cudaError_t launch_attention_tc(const AttnArgs &a, int gs, cudaStream_t s, bool *unsupported);
+int attention_tc_group(int dk, int dv, int group, bool alias, bool token_mode, const CacheView &v);
+int attention_tc_max_items_per_split(int dk);
 
 // Shape support queries used by the planner.
 bool score_supported(int dk, int hkv);
 bool attention_supported(int dk, int dv, int group, bool alias, int *sub_group);
 int attention_items_max(int sink, int recent, int b, int nsel, int token_mode);
+int attention_max_items_per_split(int dk, int dv, bool alias, int token_mode);
 int topk_max_cols();
+int score_chunk(int batch, int max_blocks, int sms);
+bool fused_supported(int dk, int dv, int hkv, int group, bool alias, int b, int max_blocks, int k_blocks);
+void fused_plan(int sink, int recent, int b, int k_blocks, int batch, int hkv, int max_blocks, bool scoring,
+                FusedPlan *pl);
+int fused_smem_bytes();
+cudaError_t launch_fused(const FusedArgs &a, cudaStream_t s, int sms, bool *unsupported);
 
 }  // namespace lsa

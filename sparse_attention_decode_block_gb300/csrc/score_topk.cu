@@ -20,7 +20,8 @@ namespace {
 // ============================================================ scoring
 
 constexpr int kScoreWarps = 8;
-constexpr int kScoreChunk = 64;    // blocks per CTA
+constexpr int kScoreUnroll = 4;     // summary rows in flight per warp
+constexpr int kScoreMaxChunk = 1024;
 
 template <int DK, int HKV>
 __global__ void __launch_bounds__(kScoreWarps * 32) k_score(ScoreArgs a)
@@ -30,11 +31,37 @@ __global__ void __launch_bounds__(kScoreWarps * 32) k_score(ScoreArgs a)
     constexpr int CPH = DK / 8;            // chunks per head
     constexpr bool kGroupReduce = (CPH <= 32) && (32 % CPH == 0);
     static_assert(kGroupReduce || HKV == 1, "head rows must tile the warp");
+    __shared__ int s_page[kScoreMaxChunk];
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int r = blockIdx.y;
     const int G = a.hq / HKV;
 
+    const int L = a.lens[r];
+    const bool len_ok = L >= 0 && (int64_t)L <= (int64_t)a.max_blocks * a.b;
+    if (!len_ok && threadIdx.x == 0 && blockIdx.x == 0) flag_error(a.status, LSA_ERR_BOUNDS);
+    const int se = min(a.sink, max(L, 0));
+    const int rs = max(L - a.recent, se);
+    const int j0 = blockIdx.x * a.chunk;
+    const int j1 = min(j0 + a.chunk, a.max_blocks);
+
+    // page ids of the chunk's candidate blocks (-1: not a candidate); the
+    // other blocks get -inf right away
+    for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+        const bool cand = len_ok && (int64_t)j * a.b >= se && (int64_t)(j + 1) * a.b <= rs;
+        int p = cand ? a.pt[(int64_t)r * a.max_blocks + j] : -1;
+        if (cand && (p < 0 || p >= a.num_pages)) {
+            flag_error(a.status, LSA_ERR_BOUNDS);
+            p = -1;
+        }
+        s_page[j - j0] = p;
+        if (p < 0) {
+#pragma unroll
+            for (int h = 0; h < HKV; ++h) a.scores[((int64_t)r * HKV + h) * a.max_blocks + j] = -INFINITY;
+        }
+    }
+
+    // q_sum = sum of the group's queries, for this lane's chunks (fp32)
     float qs[NI][8];
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
@@ -55,33 +82,31 @@ __global__ void __launch_bounds__(kScoreWarps * 32) k_score(ScoreArgs a)
             }
         }
     }
+    __syncthreads();
 
-    const int L = a.lens[r];
-    const bool len_ok = L >= 0 && (int64_t)L <= (int64_t)a.max_blocks * a.b;
-    if (!len_ok && threadIdx.x == 0 && blockIdx.x == 0) flag_error(a.status, LSA_ERR_BOUNDS);
-    const int se = min(a.sink, max(L, 0));
-    const int rs = max(L - a.recent, se);
-
-    const int j0 = blockIdx.x * kScoreChunk;
-    const int j1 = min(j0 + kScoreChunk, a.max_blocks);
-    for (int j = j0 + warp; j < j1; j += kScoreWarps) {
-        const bool cand = len_ok && (int64_t)j * a.b >= se && (int64_t)(j + 1) * a.b <= rs;
-        int p = cand ? a.pt[(int64_t)r * a.max_blocks + j] : -1;
-        const bool ok = cand && p >= 0 && p < a.num_pages;
-        if (cand && !ok && lane == 0) flag_error(a.status, LSA_ERR_BOUNDS);
-        if (!ok) {
-            if (lane < HKV) a.scores[((int64_t)r * HKV + lane) * a.max_blocks + j] = -INFINITY;
-            continue;
-        }
-        const uint8_t *row = reinterpret_cast<const uint8_t *>(a.summ) + (int64_t)p * HKV * DK * 2;
-        float part[NI];
+    const uint8_t *summ = reinterpret_cast<const uint8_t *>(a.summ);
+    for (int jb = j0 + warp * kScoreUnroll; jb < j1; jb += kScoreWarps * kScoreUnroll) {
+        uint4 v[kScoreUnroll][NI];
+        int pg[kScoreUnroll];
 #pragma unroll
-        for (int i = 0; i < NI; ++i) {
-            const int ch = lane + 32 * i;
-            part[i] = 0.f;
-            if (ch < NCH) {
-                const uint4 v = ldg_nc_v4(row + ch * 16);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        for (int u = 0; u < kScoreUnroll; ++u) {
+            const int j = jb + u;
+            pg[u] = j < j1 ? s_page[j - j0] : -1;
+#pragma unroll
+            for (int i = 0; i < NI; ++i) {
+                const int ch = lane + 32 * i;
+                v[u][i] = make_uint4(0, 0, 0, 0);
+                if (pg[u] >= 0 && ch < NCH) v[u][i] = ldg_nc_v4(summ + (int64_t)pg[u] * HKV * DK * 2 + ch * 16);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kScoreUnroll; ++u) {
+            if (pg[u] < 0) continue;       // warp-uniform
+            const int j = jb + u;
+            float part[NI];
+#pragma unroll
+            for (int i = 0; i < NI; ++i) {
+                const uint32_t w[4] = {v[u][i].x, v[u][i].y, v[u][i].z, v[u][i].w};
                 float acc = 0.f;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -91,24 +116,24 @@ __global__ void __launch_bounds__(kScoreWarps * 32) k_score(ScoreArgs a)
                 }
                 part[i] = acc;
             }
-        }
-        if constexpr (kGroupReduce) {
+            if constexpr (kGroupReduce) {
 #pragma unroll
-            for (int i = 0; i < NI; ++i) {
+                for (int i = 0; i < NI; ++i) {
 #pragma unroll
-                for (int off = CPH / 2; off > 0; off >>= 1)
-                    part[i] += __shfl_xor_sync(0xffffffffu, part[i], off);
-                const int ch = lane + 32 * i;
-                if (ch < NCH && (lane % CPH) == 0)
-                    a.scores[((int64_t)r * HKV + ch / CPH) * a.max_blocks + j] = part[i];
+                    for (int off = CPH / 2; off > 0; off >>= 1)
+                        part[i] += __shfl_xor_sync(0xffffffffu, part[i], off);
+                    const int ch = lane + 32 * i;
+                    if (ch < NCH && (lane % CPH) == 0)
+                        a.scores[((int64_t)r * HKV + ch / CPH) * a.max_blocks + j] = part[i];
+                }
+            } else {
+                float tot = 0.f;
+#pragma unroll
+                for (int i = 0; i < NI; ++i) tot += part[i];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+                if (lane == 0) a.scores[(int64_t)r * a.max_blocks + j] = tot;
             }
-        } else {
-            float tot = 0.f;
-#pragma unroll
-            for (int i = 0; i < NI; ++i) tot += part[i];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
-            if (lane == 0) a.scores[(int64_t)r * a.max_blocks + j] = tot;
         }
     }
 }
@@ -352,7 +377,7 @@ __global__ void __launch_bounds__(kFineWarps * 32) k_fine_scores(FineArgs a)
 template <int DK, int HKV>
 cudaError_t launch_score_t(const ScoreArgs &a, cudaStream_t s)
 {
-    dim3 grid((a.max_blocks + kScoreChunk - 1) / kScoreChunk, a.batch);
+    dim3 grid((a.max_blocks + a.chunk - 1) / a.chunk, a.batch);
     k_score<DK, HKV><<<grid, kScoreWarps * 32, 0, s>>>(a);
     return cudaGetLastError();
 }
@@ -384,6 +409,18 @@ cudaError_t launch_score(const ScoreArgs &a, cudaStream_t s, bool *unsupported)
 }
 
 int topk_max_cols() { return kTopkMaxCols; }
+
+int score_chunk(int batch, int max_blocks, int sms)
+{
+    // one wave of CTAs (two per SM), chunk a multiple of the warps' stride
+    const int64_t target = 2LL * sms;
+    int64_t per = ((int64_t)batch * max_blocks + target - 1) / target;
+    const int step = kScoreWarps * kScoreUnroll;
+    per = ((per + step - 1) / step) * step;
+    if (per < step) per = step;
+    if (per > kScoreMaxChunk) per = kScoreMaxChunk;
+    return (int)per;
+}
 
 cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s, bool *unsupported)
 {

@@ -25,7 +25,12 @@ LSE_ATOL = 2e-3
 
 
 def to_dev(inp: dict, dev="cuda") -> dict:
-    return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    """Move an instance to the device, keeping a latent cache's V a view of K."""
+    out = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    k, v = inp["k_cache"], inp["v_cache"]
+    if v.data_ptr() == k.data_ptr():
+        out["v_cache"] = out["k_cache"][..., : v.shape[-1]]
+    return out
 
 
 def f64(bits) -> np.ndarray:
@@ -107,7 +112,7 @@ class GpuStep:
                                     w.softmax_scale, w.c2f_candidates, w.c2f_tokens, num_splits)
         ws = L.lsa_decode_step_workspace_size(self.cache, self.params)
         assert ws > 0 or w.batch == 0 or True
-        self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        self.ws = torch.zeros(max(ws, 16), dtype=torch.uint8, device=dev)
         self.idx = torch.full((B, Hkv, max(nsel, 1)), -7, dtype=torch.int32, device=dev)
         self.out = torch.empty((B, w.num_q_heads, w.dv), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((B, w.num_q_heads), dtype=torch.float32, device=dev)

@@ -177,9 +177,17 @@ def test_topk_nan_is_skipped_and_flagged():
 
 # ---------------------------------------------------------------- attention
 
+@pytest.mark.parametrize("engine", ["fused", "split_k", "cuda_core"])
 @pytest.mark.parametrize("name", SMALL)
 @pytest.mark.parametrize("splits", [0, 1, 3])
-def test_sparse_decode_with_oracle_selection(name, splits):
+def test_sparse_decode_with_oracle_selection(name, splits, engine, monkeypatch):
+    """Attention over the oracle's selection: the persistent kernel (where it
+    applies; an explicit split count takes the split-K kernels), the split-K
+    tensor-core kernel (GQA groups of 2..8 heads) and the split-K CUDA-core
+    kernel."""
+    monkeypatch.setenv("LSA_DECODE_PATH", "fused" if engine == "fused" else "pipeline")
+    if engine == "cuda_core":
+        monkeypatch.setenv("LSA_ATTENTION_PATH", "cuda_core")
     w = small(name)
     cpu = make_inputs(w, "cpu")
     g = to_dev(cpu)
@@ -187,7 +195,7 @@ def test_sparse_decode_with_oracle_selection(name, splits):
     cache = L.make_cache(g["k_cache"], g["v_cache"])
     prm = L.make_params(w.batch, w.num_q_heads, cpu["max_blocks"], w.k_blocks, w.sink, w.recent,
                         w.softmax_scale, num_splits=splits)
-    ws = torch.empty(max(16, L.lsa_sparse_decode_workspace_size(cache, prm)), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(16, L.lsa_sparse_decode_workspace_size(cache, prm)), dtype=torch.uint8, device="cuda")
     out = torch.empty((w.batch, w.num_q_heads, w.dv), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((w.batch, w.num_q_heads), dtype=torch.float32, device="cuda")
     sel = torch.from_numpy(ref["sel"]).cuda()
@@ -238,11 +246,39 @@ def run_and_compare_step(w, cpu, g, reqs=None, num_splits=0):
     return err
 
 
+@pytest.mark.parametrize("path", ["fused", "pipeline"])
 @pytest.mark.parametrize("name", SMALL + ["c2f_small"])
-def test_decode_step_end_to_end(name):
+def test_decode_step_end_to_end(name, path, monkeypatch):
+    """Both implementations of the step: the persistent kernel (where it
+    applies; the coarse-to-fine step always takes the pipeline) and the
+    stage-by-stage pipeline."""
+    monkeypatch.setenv("LSA_DECODE_PATH", path)
     w = small(name)
     cpu = make_inputs(w, "cpu")
     run_and_compare_step(w, cpu, to_dev(cpu))
+
+
+def test_fused_step_repeats_and_leaves_workspace_zeroed(monkeypatch):
+    monkeypatch.setenv("LSA_DECODE_PATH", "fused")
+    w = small("b16_small")
+    cpu = make_inputs(w, "cpu")
+    g = to_dev(cpu)
+    st = GpuStep(w, g)
+    outs = []
+    for _ in range(5):
+        st.run()
+        outs.append((st.idx.clone(), st.out.clone(), st.lse.clone()))
+    check_status_clean()
+    for o in outs[1:]:
+        assert torch.equal(o[0], outs[0][0])
+        assert torch.equal(o[1].view(torch.int16), outs[0][1].view(torch.int16))
+        assert torch.equal(o[2], outs[0][2])
+    # control counters at the head of the workspace (one per 256-byte line) are back to zero
+    ctrl_words = (2 + w.batch + 2 * w.batch * w.num_kv_heads) * 64
+    assert torch.all(st.ws[: 4 * ctrl_words] == 0)
+    ref = oracle_decode(w, cpu)
+    assert np.array_equal(outs[0][0].cpu().numpy(), ref["sel"])
+    assert_attention_close(outs[0][1], ref["out"], "repeat")
 
 
 @pytest.mark.parametrize("splits", [1, 2, 5, 1000])
@@ -316,14 +352,16 @@ def test_vortex_figure2_shared_pages_gpu():
     q = torch.randn((3, Hq, d), generator=gen).to(torch.bfloat16)
     pt = torch.tensor([gold["page_tables"][x] for x in ("x0", "x1", "x2")], dtype=torch.int32)
     lens = torch.tensor([48, 40, 47], dtype=torch.int32)
-    cache = L.make_cache(k.cuda(), v.cuda())
+    kd, vd = k.cuda(), v.cuda()          # keep the device copies alive while the descriptor is used
+    cache = L.make_cache(kd, vd)
     summ = torch.zeros((P, H, d), dtype=torch.bfloat16, device="cuda")
     L.lsa_build_summaries(cache, pt.cuda(), lens.cuda(), summ)
     prm = L.make_params(3, Hq, 3, 1, 16, 16, 0.2)
-    ws = torch.empty(max(16, L.lsa_decode_step_workspace_size(cache, prm)), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(16, L.lsa_decode_step_workspace_size(cache, prm)), dtype=torch.uint8, device="cuda")
     out = torch.empty((3, Hq, d), dtype=torch.bfloat16, device="cuda")
     idx = torch.empty((3, H, 1), dtype=torch.int32, device="cuda")
-    L.lsa_decode_step(q.cuda(), cache, summ, None, pt.cuda(), lens.cuda(), prm, idx, out, None, ws)
+    qd, ptd, ld = q.cuda(), pt.cuda(), lens.cuda()
+    L.lsa_decode_step(qd, cache, summ, None, ptd, ld, prm, idx, out, None, ws)
     check_status_clean()
     ref = oracle.decode(q, oracle.Cache(k, v), pt, lens, num_q_heads=Hq, k_blocks=1, sink=16, recent=16, scale=0.2)
     assert np.array_equal(idx.cpu().numpy(), ref["sel"])
@@ -345,6 +383,23 @@ def test_bad_page_id_is_flagged_not_faulted():
     code, flags = L.lsa_get_device_status(clear=True)
     assert code == L.LSA_ERR_BOUNDS
     assert torch.isfinite(st.out.float()).all()
+
+
+def test_latent_cache_aliased_and_copied_values_agree():
+    w = small("mla_small")
+    cpu = make_inputs(w, "cpu")
+    g = to_dev(cpu)
+    assert g["v_cache"].data_ptr() == g["k_cache"].data_ptr()
+    a = GpuStep(w, g)
+    a.run()
+    g2 = dict(g, v_cache=g["k_cache"][..., : w.dv].contiguous())
+    b = GpuStep(w, g2)
+    b.run()
+    check_status_clean()
+    assert torch.equal(a.idx, b.idx)
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+    ref = oracle_decode(w, cpu)
+    assert_attention_close(b.out, ref["out"], "copied V")
 
 
 # ---------------------------------------------------------------- coarse-to-fine
@@ -371,11 +426,15 @@ def test_fine_topk_matches_oracle():
 
 # ---------------------------------------------------------------- full-size workloads
 
-FULL = [("b16_32k", [0, 15]), ("ragged", [3, 40]), ("c2f", [1]), ("mla", [2])]
+FULL = [("b16_32k", [0, 15], "fused"), ("b16_32k", [0, 15], "pipeline"), ("ragged", [3, 40], "fused"),
+        ("ragged", [3, 40], "pipeline"), ("c2f", [1], "pipeline"), ("mla", [2], "pipeline")]
 
 
-@pytest.mark.parametrize("name,reqs", FULL)
-def test_full_size_sampled_requests(name, reqs):
+@pytest.mark.parametrize("name,reqs,path", FULL)
+def test_full_size_sampled_requests(name, reqs, path, monkeypatch):
+    """Sampled requests of the full-size workloads, checked against the
+    oracle one request at a time, on both implementations of the step."""
+    monkeypatch.setenv("LSA_DECODE_PATH", path)
     w = WORKLOADS[name]
     inp = make_inputs(w, "cuda")
     run_and_compare_step(w, inp, inp, reqs=reqs)
