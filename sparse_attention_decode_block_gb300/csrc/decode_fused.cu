@@ -340,7 +340,13 @@ __device__ bool score_compute(const FusedArgs &a, ScoreStream<DK, HKV> &S, Worke
             if (lane == 0) a.scores[(int64_t)r * a.max_blocks + j] = tot;
         }
     }
-    if (md.flags & 2) publish(&a.score_done[r * kCtr]);
+    if (md.flags & 2) {
+        publish(&a.score_done[r * kCtr]);
+#ifdef LSA_FUSED_TRACE
+        const int c = md.j[md.n - 1] / a.score_blocks;
+        LSA_TRACE(a, r == 0 ? c : a.score_chunks + (r - 1) * (a.score_chunks + a.c.hkv) + c, 1);
+#endif
+    }
     return true;
 }
 
@@ -380,8 +386,73 @@ __device__ uint32_t score_phase(const FusedArgs &a, uint32_t t, Worker &w)
 // threshold plus the first keys equal to it; each lane emits its own
 // columns in order at offsets given by two warp scans (ascending output,
 // -1 padded).
+// Bisection on the key value over the keys a warp holds (KPL per lane, 0 =
+// not a candidate).  On entry count(key >= lo) >= keff > count(key >= hi);
+// returns the largest such lo, or an earlier one with count(key >= lo) ==
+// keff exactly (either way the selection is every key > lo plus the first
+// keff - count(key > lo) keys == lo).
 template <int KPL>
-__device__ void warp_topk(const FusedArgs &a, int row)
+__device__ __forceinline__ uint32_t bisect_keys(const uint32_t (&keys)[KPL], uint64_t lo, uint64_t hi, int keff)
+{
+    while (hi - lo > 1) {
+        const uint32_t mid = (uint32_t)(lo + ((hi - lo) >> 1));
+        int c4[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int e = 0; e < KPL; ++e) c4[e & 3] += keys[e] >= mid;
+        const int c = (int)__reduce_add_sync(0xffffffffu, (uint32_t)((c4[0] + c4[1]) + (c4[2] + c4[3])));
+        if (c >= keff) lo = mid;
+        else hi = mid;
+        if (c == keff) break;
+    }
+    return (uint32_t)lo;
+}
+
+// Writes the selected columns of the keys a warp holds in column order (lane
+// l's keys precede lane l+1's, col(e) gives key e's column): every key >
+// thresh and the first take_eq keys == thresh.  Position of a taken key =
+// taken keys before it = (keys > thresh before it) + min(ties before it,
+// take_eq).
+template <int KPL, class Col>
+__device__ __forceinline__ void emit_selection(const uint32_t (&keys)[KPL], uint32_t thresh, int take_eq,
+                                               int32_t *sel, Col col)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t cnt = 0;   // keys > thresh in the low half, ties in the high half
+#pragma unroll
+    for (int e = 0; e < KPL; ++e)
+        cnt += (keys[e] > thresh ? 1u : 0u) + (keys[e] != 0 && keys[e] == thresh ? 0x10000u : 0u);
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    const uint32_t excl = incl - cnt;
+    int g = (int)(excl & 0xffffu), q = (int)(excl >> 16);
+    if (cnt == 0) return;
+#pragma unroll
+    for (int e = 0; e < KPL; ++e) {
+        const uint32_t key = keys[e];
+        const bool gt = key > thresh, eq = key != 0 && key == thresh;
+        if (gt || (eq && q < take_eq)) sel[g + min(q, take_eq)] = col(e);
+        g += gt;
+        q += eq;
+    }
+}
+
+constexpr int kCompactKeys = 512;   // candidates kept for the narrow bisection (16 per lane)
+static_assert(2 * kCompactKeys * 4 <= kStages * kStageBytes, "top-k scratch lives in the worker's ring");
+
+// Top-k of one score row by one warp, ties to the lower block index, output
+// ascending and padded with -1.  The row's keys stay in registers (KPL per
+// lane).  A lower bound on the threshold comes from the lanes' own top-2:
+// a lane holds at least j keys >= its j-th largest, so the smallest j-th
+// largest over n_j lanes has >= j n_j keys at or above it.  When at
+// most kCompactKeys keys reach the bound they are compacted (in column
+// order) into `scratch` (2 * kCompactKeys words of shared memory) and the
+// bisection runs over 8 keys per lane; otherwise over all of them.
+template <int KPL>
+__device__ void warp_topk(const FusedArgs &a, int row, uint32_t *scratch)
 {
     static_assert(KPL % 4 == 0, "keys per lane come in fours");
     const int lane = threadIdx.x & 31;
@@ -414,71 +485,82 @@ __device__ void warp_topk(const FusedArgs &a, int row)
         keys[e] = (isnan(v[e]) || v[e] == -INFINITY) ? 0u : float_to_key(v[e]);
     }
     if (nan) flag_error(a.status, LSA_ERR_NAN);
-    int nv4[4] = {0, 0, 0, 0};
-    uint32_t kmin4[4] = {~0u, ~0u, ~0u, ~0u}, kmax4[4] = {0u, 0u, 0u, 0u};
+    // valid count, smallest valid key, and the lane's two largest keys
+    // (two interleaved chains, merged)
+    int nv2[2] = {0, 0};
+    uint32_t kmin2[2] = {~0u, ~0u}, t1[2] = {0u, 0u}, t2[2] = {0u, 0u};
 #pragma unroll
     for (int e = 0; e < KPL; ++e) {
         const uint32_t key = keys[e];
-        nv4[e & 3] += key != 0;
-        kmax4[e & 3] = max(kmax4[e & 3], key);
-        kmin4[e & 3] = min(kmin4[e & 3], key ? key : ~0u);
+        nv2[e & 1] += key != 0;
+        kmin2[e & 1] = min(kmin2[e & 1], key ? key : ~0u);
+        t2[e & 1] = max(t2[e & 1], min(t1[e & 1], key));
+        t1[e & 1] = max(t1[e & 1], key);
     }
-    const int nv = (int)__reduce_add_sync(0xffffffffu, (uint32_t)((nv4[0] + nv4[1]) + (nv4[2] + nv4[3])));
-    const uint32_t kmin = __reduce_min_sync(0xffffffffu, min(min(kmin4[0], kmin4[1]), min(kmin4[2], kmin4[3])));
-    const uint32_t kmax = __reduce_max_sync(0xffffffffu, max(max(kmax4[0], kmax4[1]), max(kmax4[2], kmax4[3])));
+    const uint32_t m1 = max(t1[0], t1[1]);
+    const uint32_t m2 = max(min(t1[0], t1[1]), max(t2[0], t2[1]));
+    const int nv = (int)__reduce_add_sync(0xffffffffu, (uint32_t)(nv2[0] + nv2[1]));
+    const uint32_t kmin = __reduce_min_sync(0xffffffffu, min(kmin2[0], kmin2[1]));
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, m1);
     const int keff = min(k, nv);
-    // Selection: every key > thresh, then the first take_eq keys == thresh
-    // in column order (ties go to the lower block index).
-    uint32_t thresh = 0;
-    int take_eq = 0;
-    if (keff > 0 && keff < nv) {
-        // bisection on the key value; invariant count(key >= lo) >= keff >
-        // count(key >= hi).  Stops early once count(key >= lo) == keff.
-        uint64_t lo = kmin, hi = (uint64_t)kmax + 1;
-        while (hi - lo > 1) {
-            const uint32_t mid = (uint32_t)(lo + ((hi - lo) >> 1));
-            int c4[4] = {0, 0, 0, 0};
-#pragma unroll
-            for (int e = 0; e < KPL; ++e) c4[e & 3] += keys[e] >= mid;
-            const int c = (int)__reduce_add_sync(0xffffffffu, (uint32_t)((c4[0] + c4[1]) + (c4[2] + c4[3])));
-            if (c >= keff) lo = mid;
-            else hi = mid;
-            if (c == keff) break;
-        }
-        thresh = (uint32_t)lo;
-        int g4[4] = {0, 0, 0, 0};
-#pragma unroll
-        for (int e = 0; e < KPL; ++e) g4[e & 3] += keys[e] > thresh;
-        take_eq = keff - (int)__reduce_add_sync(0xffffffffu, (uint32_t)((g4[0] + g4[1]) + (g4[2] + g4[3])));
-    }
     int32_t *sel = a.sel + (int64_t)row * k;
-    if (keff > 0) {
-        // with keff == nv every valid key is taken (thresh = 0: key > 0).
-        // Output position of a taken key = taken keys in lower columns:
-        // (keys > thresh before it) + min(ties before it, take_eq).
-        uint32_t cnt = 0;   // gt count in the low half, tie count in the high half
+    uint32_t thresh = 0;   // with keff == nv every valid key is taken (key > 0)
+    int take_eq = 0;
+    bool done = false;
+    if (keff > 0 && keff < nv) {
+        // bound from the lanes holding >= j valid keys (j = 1, 2): their
+        // smallest j-th largest key has >= j * (such lanes) keys above it
+        uint32_t lo0 = kmin;
+        const int l1 = (int)__reduce_add_sync(0xffffffffu, m1 != 0 ? 1u : 0u);
+        const int l2 = (int)__reduce_add_sync(0xffffffffu, m2 != 0 ? 1u : 0u);
+        if (l1 >= keff) lo0 = max(lo0, __reduce_min_sync(0xffffffffu, m1 != 0 ? m1 : ~0u));
+        if (2 * l2 >= keff) lo0 = max(lo0, __reduce_min_sync(0xffffffffu, m2 != 0 ? m2 : ~0u));
+        int cl = 0;
 #pragma unroll
-        for (int e = 0; e < KPL; ++e)
-            cnt += (keys[e] > thresh ? 1u : 0u) + (keys[e] != 0 && keys[e] == thresh ? 0x10000u : 0u);
-        uint32_t incl = cnt;
+        for (int e = 0; e < KPL; ++e) cl += keys[e] >= lo0;
+        int incl = cl;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
             if (lane >= off) incl += y;
         }
-        const uint32_t excl = incl - cnt;
-        int g = (int)(excl & 0xffffu), q = (int)(excl >> 16);
-        if (cnt != 0) {
+        const int C = __shfl_sync(0xffffffffu, incl, 31);
+        if (C <= kCompactKeys) {
+            int pos = incl - cl;
 #pragma unroll
             for (int e = 0; e < KPL; ++e) {
-                const uint32_t key = keys[e];
-                const bool gt = key > thresh, eq = key != 0 && key == thresh;
-                if (gt || (eq && q < take_eq)) sel[g + min(q, take_eq)] = c0 + e;
-                g += gt;
-                q += eq;
+                if (keys[e] >= lo0) {
+                    scratch[pos] = keys[e];
+                    scratch[kCompactKeys + pos] = (uint32_t)(c0 + e);
+                    ++pos;
+                }
             }
+            __syncwarp();
+            constexpr int PL = kCompactKeys / 32;
+            uint32_t ck[PL];
+#pragma unroll
+            for (int i = 0; i < PL; ++i) {
+                const int idx = lane * PL + i;
+                ck[i] = idx < C ? scratch[idx] : 0u;
+            }
+            const uint32_t th = bisect_keys<PL>(ck, lo0, (uint64_t)kmax + 1, keff);
+            int g = 0;
+#pragma unroll
+            for (int i = 0; i < PL; ++i) g += ck[i] > th;
+            const int teq = keff - (int)__reduce_add_sync(0xffffffffu, (uint32_t)g);
+            emit_selection<PL>(ck, th, teq, sel,
+                               [&](int i) { return (int32_t)scratch[kCompactKeys + lane * PL + i]; });
+            __syncwarp();   // scratch is free again
+            done = true;
+        } else {
+            thresh = bisect_keys<KPL>(keys, lo0, (uint64_t)kmax + 1, keff);
+            int g4[4] = {0, 0, 0, 0};
+#pragma unroll
+            for (int e = 0; e < KPL; ++e) g4[e & 3] += keys[e] > thresh;
+            take_eq = keff - (int)__reduce_add_sync(0xffffffffu, (uint32_t)((g4[0] + g4[1]) + (g4[2] + g4[3])));
         }
     }
+    if (keff > 0 && !done) emit_selection<KPL>(keys, thresh, take_eq, sel, [&](int e) { return c0 + e; });
     for (int i = keff + lane; i < k; i += 32) sel[i] = -1;
 }
 
@@ -842,9 +924,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) k_decode_fused(FusedArgs a)
             LSA_TRACE(a, t, 0);
             if (wait_counter(&a.score_done[r * kCtr], (uint32_t)a.score_chunks, a.status, a.spin_budget)) {
                 LSA_TRACE(a, t, 2);
-                if (a.max_blocks <= 32 * 4) warp_topk<4>(a, row);
-                else if (a.max_blocks <= 32 * 16) warp_topk<16>(a, row);
-                else warp_topk<kMaxKpl>(a, row);
+                uint32_t *scratch = reinterpret_cast<uint32_t *>(w.ring);   // idle between streams
+                if (a.max_blocks <= 32 * 4) warp_topk<4>(a, row, scratch);
+                else if (a.max_blocks <= 32 * 16) warp_topk<16>(a, row, scratch);
+                else warp_topk<kMaxKpl>(a, row, scratch);
                 __syncwarp();
                 LSA_TRACE(a, t, 3);
             }

@@ -20,36 +20,96 @@ namespace {
 // ============================================================ scoring
 
 constexpr int kScoreWarps = 8;
-constexpr int kScoreUnroll = 4;     // summary rows in flight per warp
-constexpr int kScoreMaxChunk = 1024;
+constexpr int kScoreMaxChunk = 1024;   // blocks per CTA at most
+constexpr int kPtPerThread = kScoreMaxChunk / (kScoreWarps * 32);
 
+// One CTA scores a contiguous chunk of one request's blocks; each warp takes
+// a contiguous share of the chunk.  The prologue is one memory round trip:
+// the request length, the chunk's page ids and the group's queries are all
+// loaded before anything is stored; the group's query sum goes to shared
+// memory once per CTA.  The main loop keeps U summary rows in flight per
+// warp at all times: each row's registers are refilled with the row U ahead
+// as soon as its dot products are done.
 template <int DK, int HKV>
-__global__ void __launch_bounds__(kScoreWarps * 32) k_score(ScoreArgs a)
+__global__ void __launch_bounds__(kScoreWarps * 32, 2) k_score(ScoreArgs a)
 {
     constexpr int NCH = HKV * DK / 8;      // 16-byte chunks of one page's summary row
     constexpr int NI = (NCH + 31) / 32;    // chunks per lane
     constexpr int CPH = DK / 8;            // chunks per head
+    constexpr int U = NI <= 4 ? 4 : 2;     // rows in flight per warp
     constexpr bool kGroupReduce = (CPH <= 32) && (32 % CPH == 0);
     static_assert(kGroupReduce || HKV == 1, "head rows must tile the warp");
     __shared__ int s_page[kScoreMaxChunk];
+    __shared__ __align__(16) float s_qs[HKV * DK];
 
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = blockIdx.y;
     const int G = a.hq / HKV;
-
-    const int L = a.lens[r];
-    const bool len_ok = L >= 0 && (int64_t)L <= (int64_t)a.max_blocks * a.b;
-    if (!len_ok && threadIdx.x == 0 && blockIdx.x == 0) flag_error(a.status, LSA_ERR_BOUNDS);
-    const int se = min(a.sink, max(L, 0));
-    const int rs = max(L - a.recent, se);
     const int j0 = blockIdx.x * a.chunk;
     const int j1 = min(j0 + a.chunk, a.max_blocks);
 
-    // page ids of the chunk's candidate blocks (-1: not a candidate); the
-    // other blocks get -inf right away
-    for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+    // ---- prologue: every load first (one round trip), then the stores
+    const int L = a.lens[r];
+    int praw[kPtPerThread];
+#pragma unroll
+    for (int i = 0; i < kPtPerThread; ++i) {
+        const int j = j0 + tid + i * kScoreWarps * 32;
+        praw[i] = j < j1 ? a.pt[(int64_t)r * a.max_blocks + j] : -1;
+    }
+    float qacc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const bool qthread = tid < NCH;        // one 8-dim slice of one head per thread
+    const int qh = tid / CPH, qd = (tid % CPH) * 8;
+    if (qthread) {
+        const uint16_t *qp = a.q + ((int64_t)r * a.hq + qh * G) * DK + qd;
+        for (int g0 = 0; g0 < G; g0 += 4) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                v[u] = g0 + u < G ? *reinterpret_cast<const uint4 *>(qp + (int64_t)(g0 + u) * DK) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = bf2_to_f2(w[e]);
+                    qacc[2 * e] += f.x;
+                    qacc[2 * e + 1] += f.y;
+                }
+            }
+        }
+    }
+    for (int c = tid; c < NCH; c += kScoreWarps * 32) {   // NCH > threads only for wide rows
+        if (c != tid) {
+            const int h = c / CPH, d0 = (c % CPH) * 8;
+            float t8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int g = 0; g < G; ++g) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(a.q + ((int64_t)r * a.hq + h * G + g) * DK + d0);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = bf2_to_f2(w[e]);
+                    t8[2 * e] += f.x;
+                    t8[2 * e + 1] += f.y;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s_qs[h * DK + d0 + e] = t8[e];
+        }
+    }
+    if (qthread) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s_qs[qh * DK + qd + e] = qacc[e];
+    }
+    const bool len_ok = L >= 0 && (int64_t)L <= (int64_t)a.max_blocks * a.b;
+    if (!len_ok && tid == 0 && blockIdx.x == 0) flag_error(a.status, LSA_ERR_BOUNDS);
+    const int se = len_ok ? min(a.sink, L) : 0;
+    const int rs = len_ok ? max(L - a.recent, se) : 0;
+#pragma unroll
+    for (int i = 0; i < kPtPerThread; ++i) {
+        const int j = j0 + tid + i * kScoreWarps * 32;
+        if (j >= j1) continue;
         const bool cand = len_ok && (int64_t)j * a.b >= se && (int64_t)(j + 1) * a.b <= rs;
-        int p = cand ? a.pt[(int64_t)r * a.max_blocks + j] : -1;
+        int p = cand ? praw[i] : -1;
         if (cand && (p < 0 || p >= a.num_pages)) {
             flag_error(a.status, LSA_ERR_BOUNDS);
             p = -1;
@@ -60,80 +120,70 @@ __global__ void __launch_bounds__(kScoreWarps * 32) k_score(ScoreArgs a)
             for (int h = 0; h < HKV; ++h) a.scores[((int64_t)r * HKV + h) * a.max_blocks + j] = -INFINITY;
         }
     }
+    __syncthreads();
 
-    // q_sum = sum of the group's queries, for this lane's chunks (fp32)
+    // ---- this lane's slice of the query sum
     float qs[NI][8];
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
         const int ch = lane + 32 * i;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) qs[i][e] = 0.f;
-        if (ch < NCH) {
-            const int h = ch / CPH, d0 = (ch % CPH) * 8;
-            for (int g = 0; g < G; ++g) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(a.q + ((int64_t)r * a.hq + h * G + g) * DK + d0);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float2 f = bf2_to_f2(w[e]);
-                    qs[i][2 * e] += f.x;
-                    qs[i][2 * e + 1] += f.y;
-                }
-            }
-        }
+        for (int e = 0; e < 8; ++e) qs[i][e] = ch < NCH ? s_qs[(ch / CPH) * DK + (ch % CPH) * 8 + e] : 0.f;
     }
-    __syncthreads();
 
+    // ---- main loop over the warp's share [w0, w1) of the chunk
+    const int n = j1 - j0;
+    const int w0 = (int)((int64_t)n * warp / kScoreWarps), w1 = (int)((int64_t)n * (warp + 1) / kScoreWarps);
     const uint8_t *summ = reinterpret_cast<const uint8_t *>(a.summ);
-    for (int jb = j0 + warp * kScoreUnroll; jb < j1; jb += kScoreWarps * kScoreUnroll) {
-        uint4 v[kScoreUnroll][NI];
-        int pg[kScoreUnroll];
+    uint4 v[U][NI];
+    auto issue = [&](int i, uint4(&dst)[NI]) {
+        const int p = i < w1 ? s_page[i] : -1;
 #pragma unroll
-        for (int u = 0; u < kScoreUnroll; ++u) {
-            const int j = jb + u;
-            pg[u] = j < j1 ? s_page[j - j0] : -1;
-#pragma unroll
-            for (int i = 0; i < NI; ++i) {
-                const int ch = lane + 32 * i;
-                v[u][i] = make_uint4(0, 0, 0, 0);
-                if (pg[u] >= 0 && ch < NCH) v[u][i] = ldg_nc_v4(summ + (int64_t)pg[u] * HKV * DK * 2 + ch * 16);
-            }
+        for (int c = 0; c < NI; ++c) {
+            const int ch = lane + 32 * c;
+            dst[c] = (p >= 0 && ch < NCH) ? ldg_nc_v4(summ + (int64_t)p * HKV * DK * 2 + ch * 16)
+                                          : make_uint4(0, 0, 0, 0);
         }
+    };
 #pragma unroll
-        for (int u = 0; u < kScoreUnroll; ++u) {
-            if (pg[u] < 0) continue;       // warp-uniform
-            const int j = jb + u;
-            float part[NI];
+    for (int u = 0; u < U; ++u) issue(w0 + u, v[u]);
+    for (int base = w0; base < w1; base += U) {
 #pragma unroll
-            for (int i = 0; i < NI; ++i) {
-                const uint32_t w[4] = {v[u][i].x, v[u][i].y, v[u][i].z, v[u][i].w};
-                float acc = 0.f;
+        for (int u = 0; u < U; ++u) {
+            const int i = base + u;
+            const int p = i < w1 ? s_page[i] : -1;      // warp-uniform
+            if (p >= 0) {
+                const int j = j0 + i;
+                float part[NI];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float2 f = bf2_to_f2(w[e]);
-                    acc = fmaf(qs[i][2 * e], f.x, acc);
-                    acc = fmaf(qs[i][2 * e + 1], f.y, acc);
+                for (int c = 0; c < NI; ++c) {
+                    const uint32_t w[4] = {v[u][c].x, v[u][c].y, v[u][c].z, v[u][c].w};
+                    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        acc = __ffma2_rn(make_float2(qs[c][2 * e], qs[c][2 * e + 1]), bf2_to_f2(w[e]), acc);
+                    part[c] = acc.x + acc.y;
                 }
-                part[i] = acc;
-            }
-            if constexpr (kGroupReduce) {
+                if constexpr (kGroupReduce) {
 #pragma unroll
-                for (int i = 0; i < NI; ++i) {
+                    for (int c = 0; c < NI; ++c) {
 #pragma unroll
-                    for (int off = CPH / 2; off > 0; off >>= 1)
-                        part[i] += __shfl_xor_sync(0xffffffffu, part[i], off);
-                    const int ch = lane + 32 * i;
-                    if (ch < NCH && (lane % CPH) == 0)
-                        a.scores[((int64_t)r * HKV + ch / CPH) * a.max_blocks + j] = part[i];
+                        for (int off = CPH / 2; off > 0; off >>= 1)
+                            part[c] += __shfl_xor_sync(0xffffffffu, part[c], off);
+                        const int ch = lane + 32 * c;
+                        if (ch < NCH && (lane % CPH) == 0)
+                            a.scores[((int64_t)r * HKV + ch / CPH) * a.max_blocks + j] = part[c];
+                    }
+                } else {
+                    float tot = 0.f;
+#pragma unroll
+                    for (int c = 0; c < NI; ++c) tot += part[c];
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+                    if (lane == 0) a.scores[(int64_t)r * a.max_blocks + j] = tot;
                 }
-            } else {
-                float tot = 0.f;
-#pragma unroll
-                for (int i = 0; i < NI; ++i) tot += part[i];
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
-                if (lane == 0) a.scores[(int64_t)r * a.max_blocks + j] = tot;
             }
+            issue(i + U, v[u]);
         }
     }
 }
@@ -412,12 +462,11 @@ int topk_max_cols() { return kTopkMaxCols; }
 
 int score_chunk(int batch, int max_blocks, int sms)
 {
-    // one wave of CTAs (two per SM), chunk a multiple of the warps' stride
+    // one wave of two CTAs per SM with equal chunks (a multiple of 4 blocks)
     const int64_t target = 2LL * sms;
     int64_t per = ((int64_t)batch * max_blocks + target - 1) / target;
-    const int step = kScoreWarps * kScoreUnroll;
-    per = ((per + step - 1) / step) * step;
-    if (per < step) per = step;
+    per = ((per + 3) / 4) * 4;
+    if (per < 4) per = 4;
     if (per > kScoreMaxChunk) per = kScoreMaxChunk;
     return (int)per;
 }
