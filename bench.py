@@ -42,6 +42,13 @@ METRIC = "sparse decode-step calls/s and achieved HBM GB/s vs GB300 peak (B=16, 
 L2_BYTES = 129 * 1024 * 1024
 
 
+# DRAM bytes per launch from one ncu capture of each kernel as it stands
+# (read + write); a kernel changed since its capture has no entry.
+NCU_TRAFFIC = {
+    "attention": 67_441_152 + 831_232,   # k_sparse_attn_tc<128,4>, profiles/kernels_b16_32k_pipeline.md
+}
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -224,6 +231,20 @@ def stage_times(insts, reps: int, stream) -> dict:
     return out
 
 
+def max_over_ranks(ms: float, dev, world: int) -> float:
+    """The timed region's length as the slowest rank saw it (every rank gets it)."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_calls_per_s(steps: int, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank's replica ran `steps` calls within `ms`."""
+    return steps * world / (ms / 1e3)
+
+
 def run_gpu(args, rank, world, dev):
     torch.cuda.set_device(dev)
     w = WORKLOADS[args.config]
@@ -297,10 +318,7 @@ def run_gpu(args, rank, world, dev):
     code, flags = L.lsa_get_device_status(clear=True)
     if code != 0:
         raise RuntimeError(f"device status after timing: {L.lsa_status_string(code)} ({flags:#x})")
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev, world)
 
     # per-stage split (separate untimed-for-value pass, L2 flushed before each)
     st = stage_times(insts, 8 * len(insts), stream)
@@ -425,7 +443,7 @@ def main():
     dev = torch.device("cuda", local)
     res = run_gpu(args, rank, world, dev)
     ms_step = res["ms"] / args.steps
-    calls = args.steps * world / (res["ms"] / 1e3)
+    calls = job_calls_per_s(args.steps, world, res["ms"])
     peak, peak_kind = peaks()
     gbs = res["step_bytes"] / (ms_step / 1e3) / 1e9
     st = res["stages"]
@@ -436,7 +454,8 @@ def main():
     if dominant:
         ach = stage_bytes[dominant] / (st[dominant] / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(ach / peak, 4), "peak_kind": peak_kind, "traffic": None}
+                "frac": round(ach / peak, 4), "peak_kind": peak_kind,
+                "traffic": NCU_TRAFFIC.get(dominant) if w.name == "b16_32k" else None}
     else:
         # the persistent kernel is the whole step: its launch time is the step time
         roof = {"bound": "hbm", "kernel": "k_decode_fused", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
