@@ -217,6 +217,27 @@ lsa_status lsa_sparse_decode(const void *q, const lsa_cache *cache, const int32_
                              void *out, float *lse, void *workspace, size_t workspace_bytes,
                              lsa_stream_t stream);
 
+/* lsa_sparse_decode without a caller workspace.  The pages have no
+ * counterpart to this call: it exists for callers that cannot hand over
+ * device memory -- a plain C host with no device allocator of its own, or a
+ * serving loop whose memory plan is fixed before it starts and admits no
+ * allocation afterwards.  It allocates nothing: its scratch is one buffer of
+ * LSA_STATIC_SCRATCH_BYTES in the library's own static device memory, one
+ * per device, zero at load and left zero-filled by every call that completes
+ * without a device error.  Shapes whose lsa_sparse_decode_workspace_size
+ * exceeds LSA_STATIC_SCRATCH_BYTES are rejected with LSA_ERR_WORKSPACE
+ * before anything is launched.  The first call on a device looks up the
+ * buffer's address once; make that first call before any stream capture
+ * begins.  All calls on a device share the one buffer, so calls that may
+ * run at the same time (several streams, or host threads without an order
+ * between their calls) must not use this entry point.  Arguments and
+ * results otherwise as lsa_sparse_decode. */
+#define LSA_STATIC_SCRATCH_BYTES (8u << 20)
+lsa_status lsa_sparse_decode_static_scratch(const void *q, const lsa_cache *cache,
+                                            const int32_t *page_table, const int32_t *seq_lens,
+                                            const int32_t *idx, const lsa_params *params, void *out,
+                                            float *lse, lsa_stream_t stream);
+
 /* Fused decode step ------------------------------------------------------- */
 
 /* Bytes of workspace lsa_decode_step needs.  The workspace holds the

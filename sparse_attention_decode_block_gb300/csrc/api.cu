@@ -689,3 +689,54 @@ lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *su
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- no-allocation variant
+//
+// lsa_sparse_decode_static_scratch: the scratch that lsa_sparse_decode takes
+// from the caller lives here instead, in a file-scope static device array
+// (zero-initialised when the module loads).  Nothing is allocated per call;
+// the array's address is looked up once per device with that device current.
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = LSA_STATIC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mu;
+void *g_static_ptr[kMaxDevices] = {};
+
+lsa_status static_scratch_for_current_device(void **ptr)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LSA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return LSA_ERR_CUDA;
+        g_static_ptr[dev] = p;
+    }
+    *ptr = g_static_ptr[dev];
+    return LSA_OK;
+}
+
+}  // namespace
+
+extern "C" lsa_status lsa_sparse_decode_static_scratch(const void *q, const lsa_cache *cache,
+                                                       const int32_t *page_table, const int32_t *seq_lens,
+                                                       const int32_t *idx, const lsa_params *params, void *out,
+                                                       float *lse, lsa_stream_t stream)
+{
+    CacheView v;
+    lsa_status rc = make_view(cache, true, &v);
+    if (rc != LSA_OK) return rc;
+    if ((rc = check_params(params, v)) != LSA_OK) return rc;
+    if (lsa_sparse_decode_workspace_size(cache, params) > kStaticScratchBytes) return LSA_ERR_WORKSPACE;
+    if (params->batch == 0) return LSA_OK;
+    void *scratch = nullptr;
+    if ((rc = static_scratch_for_current_device(&scratch)) != LSA_OK) return rc;
+    return lsa_sparse_decode(q, cache, page_table, seq_lens, idx, params, out, lse, scratch, kStaticScratchBytes,
+                             stream);
+}
+

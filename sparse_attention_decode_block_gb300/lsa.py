@@ -32,7 +32,8 @@ LSA_KEYS_E4M3 = 1
 
 EXPORTED = ["lsa_status_string", "lsa_get_device_status", "lsa_build_summaries", "lsa_append_block",
             "lsa_score", "lsa_topk", "lsa_fine_topk", "lsa_sparse_decode_workspace_size",
-            "lsa_sparse_decode", "lsa_decode_step_workspace_size", "lsa_decode_step"]
+            "lsa_sparse_decode", "lsa_decode_step_workspace_size", "lsa_decode_step",
+            "lsa_sparse_decode_static_scratch"]
 
 
 class LsaError(RuntimeError):
@@ -84,6 +85,7 @@ def load_library(path: Optional[str] = None):
             "lsa_fine_topk": ([V, cache_p, V, V, V, params_p, V, V, S, V], C.c_int),
             "lsa_sparse_decode_workspace_size": ([cache_p, params_p], S),
             "lsa_sparse_decode": ([V, cache_p, V, V, V, params_p, V, V, V, S, V], C.c_int),
+            "lsa_sparse_decode_static_scratch": ([V, cache_p, V, V, V, params_p, V, V, V], C.c_int),
             "lsa_decode_step_workspace_size": ([cache_p, params_p], S),
             "lsa_decode_step": ([V, cache_p, V, cache_p, V, V, params_p, V, V, V, V, S, V], C.c_int),
         }
@@ -200,6 +202,14 @@ def lsa_sparse_decode(q, cache: lsa_cache, page_table, seq_lens, idx, params: ls
     _check(load_library().lsa_sparse_decode(_ptr(q), C.byref(cache), _ptr(page_table), _ptr(seq_lens), _ptr(idx),
                                             C.byref(params), _ptr(out), _ptr(lse), _ptr(workspace), nbytes,
                                             _stream(stream)), "lsa_sparse_decode")
+
+
+def lsa_sparse_decode_static_scratch(q, cache: lsa_cache, page_table, seq_lens, idx, params: lsa_params, out, lse,
+                                     stream=None):
+    _check(load_library().lsa_sparse_decode_static_scratch(_ptr(q), C.byref(cache), _ptr(page_table),
+                                                           _ptr(seq_lens), _ptr(idx), C.byref(params), _ptr(out),
+                                                           _ptr(lse), _stream(stream)),
+           "lsa_sparse_decode_static_scratch")
 
 
 def lsa_decode_step_workspace_size(cache: lsa_cache, params: lsa_params) -> int:
