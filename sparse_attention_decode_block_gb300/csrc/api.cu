@@ -3,6 +3,8 @@
 // stream-ordered launch sequence of each call.  See include/lsa.h for the
 // contract of every function.
 #include <math.h>
+
+#include <algorithm>
 #include <mutex>
 #include <stdlib.h>
 #include <string.h>
@@ -126,6 +128,9 @@ float scale_of(const lsa_params *p, int dk)
 struct AttnPlan {
     int nsub, splits, items_per_split;
     int tc_group;          // > 0: tensor-core kernel with this many heads per CTA
+    bool flat;             // even split of every row's items over the GPU (attention_flat.cu)
+    int fl_ns, fl_ctas, fl_parts;
+    int64_t fl_total;
     size_t ws_bytes;
 };
 
@@ -167,6 +172,26 @@ lsa_status plan_attention(const CacheView &v, const lsa_params *p, bool token_mo
         const size_t rowsq = (size_t)p->batch * p->num_q_heads * pl->splits;
         pl->ws_bytes = round_up(rowsq * v.dv * sizeof(float)) + round_up(rowsq * sizeof(float));
     }
+    // Without an explicit split count the tensor-core path splits all rows'
+    // items evenly over the GPU instead: at most two rows per CTA (a piece is
+    // no longer than a row) and at most the per-warp item limit per warp.
+    pl->flat = pl->tc_group > 0 && p->num_splits <= 0 && !token_mode && items > 0 && rows > 0;
+    if (pl->flat) {
+        const int64_t T = rows * items;
+        const int64_t per_cta = std::min<int64_t>(items, (int64_t)attention_flat_warps() *
+                                                              attention_flat_max_items_per_warp());
+        int64_t nc = std::max<int64_t>((int64_t)attention_flat_ctas_per_sm() * sm_count(), (T + per_cta - 1) / per_cta);
+        nc = std::min<int64_t>(nc, T);
+        if (nc > 0x7fffffff) return LSA_ERR_UNSUPPORTED;
+        pl->fl_ns = items;
+        pl->fl_total = T;
+        pl->fl_ctas = (int)nc;
+        const int64_t min_piece = T / nc;   // >= 1
+        pl->fl_parts = (int)((items + min_piece - 1) / min_piece + 1);
+        const size_t rowsq = (size_t)p->batch * p->num_q_heads * pl->fl_parts;
+        pl->ws_bytes = round_up(rowsq * v.dv * sizeof(float)) + round_up(rowsq * sizeof(float)) +
+                       round_up((size_t)rows * sizeof(uint32_t));
+    }
     return LSA_OK;
 }
 
@@ -200,6 +225,21 @@ lsa_status run_attention(const void *q, const CacheView &v, const int32_t *pt, c
     a.lse = lse;
     a.status = status_word();
     a.spin_budget = kSpinBudget;
+    if (pl.flat) {
+        a.fl_ns = pl.fl_ns;
+        a.fl_total = pl.fl_total;
+        a.fl_ctas = pl.fl_ctas;
+        a.fl_parts = pl.fl_parts;
+        const size_t rowsq = (size_t)p->batch * p->num_q_heads * pl.fl_parts;
+        a.o_part = reinterpret_cast<float *>(ws);
+        a.lse_part = reinterpret_cast<float *>(ws + round_up(rowsq * v.dv * sizeof(float)));
+        a.row_done = reinterpret_cast<uint32_t *>(ws + round_up(rowsq * v.dv * sizeof(float)) +
+                                                  round_up(rowsq * sizeof(float)));
+        bool unsup = false;
+        const cudaError_t e = launch_attention_flat(a, pl.tc_group, st, &unsup);
+        if (unsup) return LSA_ERR_UNSUPPORTED;
+        return e == cudaSuccess ? LSA_OK : LSA_ERR_CUDA;
+    }
     const size_t rowsq = (size_t)p->batch * p->num_q_heads * pl.splits;
     if (pl.splits > 1) {
         a.o_part = reinterpret_cast<float *>(ws);
@@ -247,9 +287,9 @@ lsa_status step_layout(const CacheView &v, const CacheView *iv, const lsa_params
 }
 
 // Workspace of the persistent kernel: [control counters | scores |
-// selection | page ids of the selection | part outputs | part lse].
+// selection | chunk table | part outputs | part lse].
 struct FusedLayout {
-    size_t ctrl, scores, sel, selpg, opart, lpart, total;
+    size_t ctrl, scores, sel, ctab, opart, lpart, total;
     FusedPlan plan;
 };
 
@@ -265,7 +305,7 @@ bool use_fused(const CacheView &v, const lsa_params *p)
     if (!want) return false;
     if (p->c2f_candidates > 0 || p->num_splits > 0) return false;
     return fused_supported(v.dk, v.dv, v.hkv, p->num_q_heads / v.hkv, v.v_alias != 0, v.b, p->max_blocks,
-                           p->k_blocks);
+                           p->k_blocks, p->batch, sm_count());
 }
 
 void fused_layout(const CacheView &v, const lsa_params *p, bool scoring, FusedLayout *L)
@@ -274,15 +314,16 @@ void fused_layout(const CacheView &v, const lsa_params *p, bool scoring, FusedLa
                &L->plan);
     const size_t rows = (size_t)p->batch * v.hkv;
     const size_t rowsq = (size_t)p->batch * p->num_q_heads * L->plan.units_per_row;
-    // each counter on its own 256-byte line (64 words apart): the ticket, the
-    // leave counter, one per request and two per (request, KV head)
-    L->ctrl = round_up((2 + (size_t)p->batch + 2 * rows) * 64 * sizeof(uint32_t));
+    // each counter on its own 256-byte line (64 words apart): the score
+    // tickets, the leave counter, the attention tickets, one per request
+    // (score units done) and one per (request, KV head) for the merge
+    L->ctrl = round_up((3 + (size_t)p->batch + rows) * 64 * sizeof(uint32_t));
     L->scores = scoring ? round_up(rows * p->max_blocks * sizeof(float)) : 0;
     L->sel = scoring ? round_up(rows * p->k_blocks * sizeof(int32_t)) : 0;
-    L->selpg = 0;
+    L->ctab = scoring ? round_up(rows * L->plan.units_per_row * L->plan.chunks_per_unit * sizeof(uint64_t)) : 0;
     L->opart = L->plan.units_per_row > 1 ? round_up(rowsq * v.dv * sizeof(float)) : 0;
     L->lpart = L->plan.units_per_row > 1 ? round_up(rowsq * sizeof(float)) : 0;
-    L->total = L->ctrl + L->scores + L->sel + L->selpg + L->opart + L->lpart;
+    L->total = L->ctrl + L->scores + L->sel + L->ctab + L->opart + L->lpart;
 }
 
 // scoring: the whole step (scores, top-k, attention); otherwise attention
@@ -314,19 +355,17 @@ lsa_status run_fused(const void *q, const CacheView &v, const void *summaries, c
     a.total_units = L.plan.total_units;
     a.units_per_row = L.plan.units_per_row;
     a.chunks_per_unit = L.plan.chunks_per_unit;
-    a.wait_ready = scoring;
     uint8_t *cur = ws;
-    a.ctrl = reinterpret_cast<uint32_t *>(cur);            // [0] ticket, [64] leave counter
-    a.score_done = a.ctrl + 2 * 64;
-    a.ready = a.score_done + (size_t)p->batch * 64;
-    a.split_done = a.ready + (size_t)p->batch * v.hkv * 64;
+    a.ctrl = reinterpret_cast<uint32_t *>(cur);            // [0] score, [64] leave, [128] attention tickets
+    a.score_hint = a.ctrl + 3 * 64;
+    a.split_done = a.score_hint + (size_t)p->batch * 64;
     cur += L.ctrl;
-    a.scores = reinterpret_cast<float *>(cur);
+    a.scores = reinterpret_cast<uint32_t *>(cur);
     cur += L.scores;
     a.sel = sel ? sel : reinterpret_cast<int32_t *>(cur);
     cur += L.sel;
-    a.sel_pg = nullptr;
-    cur += L.selpg;
+    a.ctab = scoring ? reinterpret_cast<uint64_t *>(cur) : nullptr;
+    cur += L.ctab;
     a.o_part = reinterpret_cast<float *>(cur);
     cur += L.opart;
     a.lse_part = reinterpret_cast<float *>(cur);

@@ -1,0 +1,406 @@
+// Sparse attention with an even split of the whole batch's work over the
+// GPU (tensor cores, GQA groups of 2..8 query heads, d = 64 or 128).
+//
+// The attended token set of every row (request, KV head, query subgroup) is
+// walked in 16-token items: forced sink tokens, the selected blocks, forced
+// recent tokens (Vortex blog post, block top-k equation; ByteCross, Appendix
+// A).  Every row gets the same number NS of item slots (empty slots stream
+// nothing), so item i belongs to row i / NS, and the flat list of all rows'
+// items is cut into equal contiguous pieces: CTA c takes the items i with
+// floor(i * NC / T) == c, and its warps take equal contiguous parts of
+// those.  Every SM thus streams the same number of bytes whatever the
+// lengths and the selection, and a piece touches at most two rows.
+//
+// Each warp resolves all its items' descriptors at once (request length and
+// selection in one round trip, page ids in a second), then streams K and V
+// through its own ring of cp.async stages into 128-byte XOR-swizzled tiles
+// for ldmatrix, and runs the group's S = Q K^T and O += P V as m16n8k16
+// MMAs (the G heads in rows 0..G-1) with an online softmax.  At the end the
+// CTA merges its warps' partial results per row in shared memory; a row
+// that several CTAs share is merged by log-sum-exp (ByteCross, Appendix A)
+// by the last of them to finish, found with a per-row counter that it
+// resets for the next call.
+#include <math.h>
+
+#include "attn_items.cuh"
+#include "lsa_device.cuh"
+
+namespace lsa {
+namespace {
+
+constexpr int kFlWarps = 4;
+constexpr int kFlCtasPerSm = 2;
+constexpr int kFlMaxRowsPerCta = 2;   // the host keeps a CTA's piece within two rows
+constexpr int kFlMaxItemsPerWarp = 32;
+constexpr float kFlLn2 = 0.693147180559945309f;
+
+template <int DK, int G>
+struct FlLayout {
+    static constexpr int STAGES = G <= 4 ? 3 : 2;   // two CTAs per SM
+    static constexpr int CPR = DK / 8;            // 16-byte chunks per token row
+    static constexpr int SUB = kChunk * 128;      // one swizzled 16-row x 128-byte sub-tile
+    static constexpr int KBYTES = (DK / 64) * SUB;
+    static constexpr int STAGE = 2 * KBYTES;      // K tile then V tile
+    static constexpr int WARP_RING = STAGES * STAGE;
+    static constexpr int RINGS = kFlWarps * WARP_RING;
+    static constexpr int SEG0 = RINGS + kFlWarps * 16;            // first-row results: [W][G][DK], m, l
+    static constexpr int LAST = SEG0 + kFlWarps * G * (DK + 2) * 4;   // per-row "last CTA" flags
+    static constexpr int SMEM = LAST + 16;
+    static_assert(RINGS >= kFlMaxRowsPerCta * kFlWarps * G * (DK + 2) * 4, "the CTA merge reuses the rings");
+    static_assert(SMEM * kFlCtasPerSm <= 227 * 1024, "two CTAs per SM");
+};
+
+// Row index -> (request, KV head, query subgroup).
+struct FlRow {
+    int r, h, sg;
+};
+
+__device__ __forceinline__ FlRow fl_row(const AttnArgs &a, int rho)
+{
+    FlRow x;
+    x.sg = rho % a.nsub;
+    x.h = (rho / a.nsub) % a.c.hkv;
+    x.r = rho / (a.nsub * a.c.hkv);
+    return x;
+}
+
+// First CTA whose piece holds item i.
+__device__ __forceinline__ int fl_cta_of(const AttnArgs &a, int64_t i)
+{
+    return (int)(i * a.fl_ctas / a.fl_total);
+}
+
+template <int DK, int G>
+__global__ void __launch_bounds__(kFlWarps * 32) k_attn_flat(AttnArgs a)
+{
+    using LY = FlLayout<DK, G>;
+    constexpr int NT = DK / 8;
+    constexpr int CPL = kChunk * LY::CPR / 32;
+    constexpr int kFlStages = LY::STAGES;
+    static_assert(G >= 2 && G <= 8, "heads of a group must fit rows 0..7 of the MMA tile");
+
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Gt = a.hq / a.c.hkv;
+    const CacheView &c = a.c;
+    if ((smem_addr(smem) & 1023u) != 0) {
+        if (threadIdx.x == 0) flag_error(a.status, LSA_ERR_INVALID_ARG);
+        return;
+    }
+    const int NS = a.fl_ns;
+    const int64_t T = a.fl_total;
+    const int cta = blockIdx.x;
+    const int64_t cs = ((int64_t)cta * T + a.fl_ctas - 1) / a.fl_ctas;         // this CTA's items [cs, ce)
+    const int64_t ce = ((int64_t)(cta + 1) * T + a.fl_ctas - 1) / a.fl_ctas;
+    const int64_t cn = ce - cs;
+    const int64_t ws = cs + cn * warp / kFlWarps, we = cs + cn * (warp + 1) / kFlWarps;
+    const int nmine = min((int)(we - ws), kFlMaxItemsPerWarp);   // the host keeps pieces within this
+    const int rho_first = (int)(cs / NS);
+
+    uint8_t *ring = smem + warp * LY::WARP_RING;
+    const uint32_t ring_s = smem_addr(ring);
+    int *stage_n = reinterpret_cast<int *>(smem + kFlWarps * LY::WARP_RING) + warp * 4;
+
+    // ---- descriptors of this warp's items, one per lane
+    ItemDesc my{-1, 0, 0};
+    int my_rho = -1;
+    if (lane < nmine) {
+        const int64_t i = ws + lane;
+        my_rho = (int)(i / NS);
+        const int k = (int)(i % NS);
+        const FlRow x = fl_row(a, my_rho);
+        const RowPlan pl = make_plan(a, x.r, k == 0 && x.h == 0 && x.sg == 0);
+        my = k < pl.n_items ? describe_item(a, pl, x.r, x.h, k) : ItemDesc{-1, 0, 0};
+    }
+
+    auto issue = [&](int j) {
+        if (j >= nmine) {
+            cp_async_commit();
+            return;
+        }
+        const int page = __shfl_sync(0xffffffffu, my.page, j);
+        const int ts = __shfl_sync(0xffffffffu, (int)my.ts, j);
+        const int n = __shfl_sync(0xffffffffu, (int)my.n, j);
+        const int rho = __shfl_sync(0xffffffffu, my_rho, j);
+        if (lane == 0) stage_n[j % kFlStages] = n;
+        if (n > 0) {
+            const int h = (rho / a.nsub) % c.hkv;
+            const uint32_t st = ring_s + (j % kFlStages) * LY::STAGE;
+            const uint8_t *kb = c.k + ((int64_t)page * c.kps + (int64_t)h * c.khs + (int64_t)ts * c.kts) * 2;
+            const uint8_t *vb = c.v + ((int64_t)page * c.vps + (int64_t)h * c.vhs + (int64_t)ts * c.vts) * 2;
+#pragma unroll
+            for (int u = 0; u < CPL; ++u) {
+                const int q = lane + 32 * u;
+                const int t = q / LY::CPR, ch = q % LY::CPR;
+                if (t < n) {
+                    cp_async16(st + swizzle_offset(t, ch), kb + (int64_t)t * c.kts * 2 + ch * 16);
+                    cp_async16(st + LY::KBYTES + swizzle_offset(t, ch), vb + (int64_t)t * c.vts * 2 + ch * 16);
+                }
+            }
+        }
+        cp_async_commit();
+    };
+
+    const int rr = lane >> 2, cc = lane & 3;
+    const int mi = lane >> 3, r8 = lane & 7;
+    const int tk = (mi >> 1) * 8 + r8, ck = mi & 1;
+    const int tv = (mi & 1) * 8 + r8, cv = mi >> 1;
+
+    // the current row segment's state lives in registers; a segment of the
+    // piece's first row that ends mid-stream is parked in shared memory
+    float m = -INFINITY, l = 0.f;
+    float o[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    float *s0o = reinterpret_cast<float *>(smem + LY::SEG0) + warp * G * DK;   // [G][DK]
+    float *s0m = reinterpret_cast<float *>(smem + LY::SEG0) + kFlWarps * G * DK + warp * 2 * G;   // m[G], l[G]
+    if (lane < G) {
+        s0m[lane] = -INFINITY;
+        s0m[G + lane] = 0.f;
+    }
+    uint32_t qa0[DK / 16], qa2[DK / 16];
+    int cur_rho = -1;
+
+    auto write_state = [&](float *dst_o, float *dst_ml) {
+        if (rr < G) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                *reinterpret_cast<float2 *>(dst_o + rr * DK + nt * 8 + 2 * cc) = make_float2(o[nt][0], o[nt][1]);
+            if (cc == 0) {
+                dst_ml[rr] = m;
+                dst_ml[G + rr] = l;
+            }
+        }
+    };
+    auto close_segment = [&]() {   // only the piece's first row can end mid-stream
+        if (cur_rho == rho_first) write_state(s0o, s0m);
+    };
+    auto open_segment = [&](int rho) {
+        cur_rho = rho;
+        m = -INFINITY;
+        l = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+        const FlRow x = fl_row(a, rho);
+        const bool qrow = rr < G;
+        const uint16_t *qp = a.q + ((int64_t)x.r * a.hq + x.h * Gt + x.sg * G + (qrow ? rr : 0)) * DK;
+#pragma unroll
+        for (int ks = 0; ks < DK / 16; ++ks) {
+            qa0[ks] = qrow ? *reinterpret_cast<const uint32_t *>(qp + 16 * ks + 2 * cc) : 0u;
+            qa2[ks] = qrow ? *reinterpret_cast<const uint32_t *>(qp + 16 * ks + 8 + 2 * cc) : 0u;
+        }
+    };
+
+#pragma unroll
+    for (int j = 0; j < kFlStages - 1; ++j) issue(j);
+    for (int j = 0; j < nmine; ++j) {
+        issue(j + kFlStages - 1);
+        const int rho = __shfl_sync(0xffffffffu, my_rho, j);
+        if (rho != cur_rho) {
+            close_segment();
+            open_segment(rho);
+        }
+        cp_async_wait<kFlStages - 1>();
+        __syncwarp();
+        const int n = stage_n[j % kFlStages];
+        if (n > 0) {
+            const uint32_t kbase = ring_s + (j % kFlStages) * LY::STAGE;
+            const uint32_t vbase = kbase + LY::KBYTES;
+            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < DK / 16; ++ks) {
+                uint32_t b[4];
+                ldsm_x4(b, kbase + swizzle_offset(tk, 2 * ks + ck));
+                mma_bf16_rows8(s0, qa0[ks], qa2[ks], b[0], b[1]);
+                mma_bf16_rows8(s1, qa0[ks], qa2[ks], b[2], b[3]);
+            }
+            const int t0 = 2 * cc;
+            const float z0 = t0 < n ? s0[0] * a.scale_log2 : -INFINITY;
+            const float z1 = t0 + 1 < n ? s0[1] * a.scale_log2 : -INFINITY;
+            const float z2 = t0 + 8 < n ? s1[0] * a.scale_log2 : -INFINITY;
+            const float z3 = t0 + 9 < n ? s1[1] * a.scale_log2 : -INFINITY;
+            float mx = fmaxf(fmaxf(z0, z1), fmaxf(z2, z3));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float mn = fmaxf(m, mx);
+            float alpha = 1.f;
+            uint32_t pa0 = 0u, pa2 = 0u;
+            if (mn != -INFINITY) {
+                alpha = fast_ex2(m - mn);
+                pa0 = pack_bf16x2(fast_ex2(z0 - mn), fast_ex2(z1 - mn));
+                pa2 = pack_bf16x2(fast_ex2(z2 - mn), fast_ex2(z3 - mn));
+                m = mn;
+            }
+            // the denominator sums the same bf16-rounded weights the MMA uses
+            const float2 p01 = bf2_to_f2(pa0), p23 = bf2_to_f2(pa2);
+            float ps = (p01.x + p01.y) + (p23.x + p23.y);
+            ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+            ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+            l = l * alpha + ps;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                o[nt][0] *= alpha;
+                o[nt][1] *= alpha;
+            }
+            if (n < kChunk) {   // stale V rows meet zero weights; 0 * NaN must not happen
+                for (int q = lane; q < (kChunk - n) * LY::CPR; q += 32) {
+                    const int t = n + q / LY::CPR, ch = q % LY::CPR;
+                    *reinterpret_cast<uint4 *>(ring + (j % kFlStages) * LY::STAGE + LY::KBYTES + swizzle_offset(t, ch)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
+            }
+#pragma unroll
+            for (int dt = 0; dt < DK / 16; ++dt) {
+                uint32_t b[4];
+                ldsm_x4_t(b, vbase + swizzle_offset(tv, 2 * dt + cv));
+                mma_bf16_rows8(o[2 * dt], pa0, pa2, b[0], b[1]);
+                mma_bf16_rows8(o[2 * dt + 1], pa0, pa2, b[2], b[3]);
+            }
+        }
+        __syncwarp();
+    }
+    cp_async_wait<0>();
+    __syncthreads();   // rings drained: reuse them for the CTA merge
+
+    // ---- CTA merge: per row of the piece, combine the warps' segments.
+    // Merge area (in the rings): o [rows][W][G][DK], then (m, l) [rows][W][2G].
+    float *mo = reinterpret_cast<float *>(smem);
+    float *mml = mo + kFlMaxRowsPerCta * kFlWarps * G * DK;
+    {
+        const int cur_s = cur_rho < 0 ? -1 : cur_rho - rho_first;   // 0 or 1 (host-guaranteed)
+        // slot 0: the parked first-row segment, or the current one; slot 1: the current one
+        for (int t = lane; t < G * DK; t += 32) {
+            mo[(0 * kFlWarps + warp) * G * DK + t] = s0o[t];
+        }
+        if (lane < 2 * G) {
+            mml[(0 * kFlWarps + warp) * 2 * G + lane] = s0m[lane];
+            mml[(1 * kFlWarps + warp) * 2 * G + lane] = lane < G ? -INFINITY : 0.f;
+        }
+        __syncwarp();
+        if (cur_s >= 0)
+            write_state(mo + (cur_s * kFlWarps + warp) * G * DK, mml + (cur_s * kFlWarps + warp) * 2 * G);
+    }
+    __syncthreads();
+
+    const int rho_last = cn > 0 ? (int)((ce - 1) / NS) : rho_first - 1;
+    int *s_last = reinterpret_cast<int *>(smem + LY::LAST);
+    for (int s = 0; s < kFlMaxRowsPerCta && rho_first + s <= rho_last; ++s) {
+        const int rho = rho_first + s;
+        const FlRow x = fl_row(a, rho);
+        const int fc = fl_cta_of(a, (int64_t)rho * NS);
+        const int lc = fl_cta_of(a, (int64_t)(rho + 1) * NS - 1);
+        const int parts = lc - fc + 1;
+        for (int t = threadIdx.x; t < G * DK / 4; t += blockDim.x) {
+            const int g = t / (DK / 4), d = (t % (DK / 4)) * 4;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kFlWarps; ++w) M = fmaxf(M, mml[(s * kFlWarps + w) * 2 * G + g]);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            float wsum = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < kFlWarps; ++w) {
+                    const float mw = mml[(s * kFlWarps + w) * 2 * G + g];
+                    if (mw == -INFINITY) continue;
+                    const float f = fast_ex2(mw - M);
+                    wsum += f * mml[(s * kFlWarps + w) * 2 * G + G + g];
+                    const float4 v = *reinterpret_cast<const float4 *>(mo + ((s * kFlWarps + w) * G + g) * DK + d);
+                    acc.x += f * v.x;
+                    acc.y += f * v.y;
+                    acc.z += f * v.z;
+                    acc.w += f * v.w;
+                }
+            }
+            const bool empty_set = !(wsum > 0.f);
+            const float inv = empty_set ? 0.f : 1.f / wsum;
+            acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            const float lse2 = empty_set ? -INFINITY : M + fast_lg2(wsum);
+            const int64_t orow = (int64_t)x.r * a.hq + x.h * Gt + x.sg * G + g;
+            if (parts == 1) {
+                uint2 pk;
+                pk.x = pack_bf16x2(acc.x, acc.y);
+                pk.y = pack_bf16x2(acc.z, acc.w);
+                *reinterpret_cast<uint2 *>(a.out + orow * DK + d) = pk;
+                if (a.lse && d == 0) a.lse[orow] = empty_set ? -INFINITY : lse2 * kFlLn2;
+            } else {
+                const int part = cta - fc;
+                *reinterpret_cast<float4 *>(a.o_part + (orow * a.fl_parts + part) * DK + d) = acc;
+                if (d == 0) a.lse_part[orow * a.fl_parts + part] = lse2;
+            }
+        }
+        if (parts == 1) continue;
+        // the last CTA of the row to finish merges its parts
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const uint32_t prev = atomicAdd(&a.row_done[rho], 1u);
+            s_last[s] = prev == (uint32_t)parts - 1;
+        }
+        __syncthreads();
+        if (!s_last[s]) continue;
+        __threadfence();
+        for (int t = threadIdx.x; t < G * DK / 4; t += blockDim.x) {
+            const int g = t / (DK / 4), d = (t % (DK / 4)) * 4;
+            const int64_t orow = (int64_t)x.r * a.hq + x.h * Gt + x.sg * G + g;
+            const float *lp = a.lse_part + orow * a.fl_parts;
+            float M = -INFINITY;
+            for (int p = 0; p < parts; ++p) M = fmaxf(M, __ldcg(lp + p));
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            float wsum = 0.f;
+            if (M != -INFINITY) {
+                for (int p = 0; p < parts; ++p) {
+                    const float ls = __ldcg(lp + p);
+                    if (ls == -INFINITY) continue;
+                    const float f = fast_ex2(ls - M);
+                    wsum += f;
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.o_part + (orow * a.fl_parts + p) * DK + d));
+                    acc.x += f * v.x;
+                    acc.y += f * v.y;
+                    acc.z += f * v.z;
+                    acc.w += f * v.w;
+                }
+            }
+            const bool empty_set = !(wsum > 0.f);
+            const float inv = empty_set ? 0.f : 1.f / wsum;
+            uint2 pk;
+            pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+            pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2 *>(a.out + orow * DK + d) = pk;
+            if (a.lse && d == 0) a.lse[orow] = empty_set ? -INFINITY : (M + fast_lg2(wsum)) * kFlLn2;
+        }
+        if (threadIdx.x == 0) a.row_done[rho] = 0u;   // ready for the next call
+    }
+}
+
+template <int DK, int G>
+cudaError_t launch_flat_t(const AttnArgs &a, cudaStream_t s)
+{
+    using LY = FlLayout<DK, G>;
+    auto kern = k_attn_flat<DK, G>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<a.fl_ctas, kFlWarps * 32, LY::SMEM, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int attention_flat_ctas_per_sm() { return kFlCtasPerSm; }
+int attention_flat_warps() { return kFlWarps; }
+int attention_flat_max_items_per_warp() { return kFlMaxItemsPerWarp; }
+
+cudaError_t launch_attention_flat(const AttnArgs &a, int gs, cudaStream_t s, bool *unsupported)
+{
+    *unsupported = false;
+    if (a.batch == 0 || a.fl_total == 0) return cudaSuccess;
+#define LSA_FL_CASE(D, G_) \
+    if (a.c.dk == D && gs == G_) return launch_flat_t<D, G_>(a, s);
+    LSA_FL_CASE(64, 2) LSA_FL_CASE(64, 4) LSA_FL_CASE(64, 8)
+    LSA_FL_CASE(128, 2) LSA_FL_CASE(128, 4) LSA_FL_CASE(128, 8)
+#undef LSA_FL_CASE
+    *unsupported = true;
+    return cudaSuccess;
+}
+
+}  // namespace lsa

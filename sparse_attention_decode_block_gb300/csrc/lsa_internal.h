@@ -87,8 +87,14 @@ struct AttnArgs {
     int32_t sink, recent;
     float scale_log2;           // softmax scale * log2(e)
     int32_t splits, items_per_split, nsub;
-    float *o_part;              // [B*Hq, splits, dv]   (splits > 1)
-    float *lse_part;            // [B*Hq, splits]       log2 domain
+    // even split of all rows' item slots over fl_ctas CTAs (attention_flat.cu):
+    // fl_ns item slots per row, fl_total = rows * fl_ns, at most fl_parts
+    // CTAs per row; row_done: one counter per row, zero between calls
+    int32_t fl_ns, fl_ctas, fl_parts;
+    int64_t fl_total;
+    uint32_t *row_done;
+    float *o_part;              // [B*Hq, splits or fl_parts, dv]
+    float *lse_part;            // [B*Hq, splits or fl_parts]   log2 domain
     uint16_t *out;              // [B, Hq, dv] bf16     (splits == 1)
     float *lse;                 // [B, Hq] natural log or NULL
     uint32_t *status;
@@ -132,16 +138,14 @@ struct FusedArgs {
     // work units: [0, score_units) scores, [score_units, attn_base) top-k,
     // [attn_base, total_units) attention parts
     int32_t score_blocks, score_chunks, score_units, attn_base, total_units, units_per_row, chunks_per_unit;
-    int32_t wait_ready;         // attention waits for the row's top-k
     int32_t total_warps;
-    float *scores;              // [B*hkv, max_blocks]
+    uint32_t *scores;           // [B*hkv, max_blocks] score keys, 0 = not yet written
     int32_t *sel;               // [B*hkv, k_blocks] selected blocks (ascending, -1 pad)
-    int32_t *sel_pg;            // [B*hkv, k_blocks] their page ids, or NULL (look up)
+    uint64_t *ctab;             // [B*hkv, units_per_row*chunks_per_unit] chunk table (whole step), or NULL
     float *o_part;              // [B*Hq, units_per_row, dv]
     float *lse_part;            // [B*Hq, units_per_row] (log2 units)
     uint32_t *ctrl;             // [0] ticket, [1] workers done
-    uint32_t *score_done;       // [B]
-    uint32_t *ready;            // [B*hkv]
+    uint32_t *score_hint;       // [B] score units done (relaxed count, a hint)
     uint32_t *split_done;       // [B*hkv]
     uint16_t *out;
     float *lse;
@@ -163,6 +167,10 @@ cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s, bool *unsupported);
 cudaError_t launch_fine_scores(const FineArgs &a, cudaStream_t s, bool *unsupported);
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s, bool *unsupported);
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);
+int attention_flat_ctas_per_sm();
+int attention_flat_warps();
+int attention_flat_max_items_per_warp();
+cudaError_t launch_attention_flat(const AttnArgs &a, int gs, cudaStream_t s, bool *unsupported);
 cudaError_t launch_attention_tc(const AttnArgs &a, int gs, cudaStream_t s, bool *unsupported);
 int attention_tc_group(int dk, int dv, int group, bool alias, bool token_mode, const CacheView &v);
 int attention_tc_max_items_per_split(int dk);
@@ -174,7 +182,8 @@ int attention_items_max(int sink, int recent, int b, int nsel, int token_mode);
 int attention_max_items_per_split(int dk, int dv, bool alias, int token_mode);
 int topk_max_cols();
 int score_chunk(int batch, int max_blocks, int sms);
-bool fused_supported(int dk, int dv, int hkv, int group, bool alias, int b, int max_blocks, int k_blocks);
+bool fused_supported(int dk, int dv, int hkv, int group, bool alias, int b, int max_blocks, int k_blocks, int batch,
+                     int sms);
 void fused_plan(int sink, int recent, int b, int k_blocks, int batch, int hkv, int max_blocks, bool scoring,
                 FusedPlan *pl);
 int fused_smem_bytes();

@@ -274,11 +274,35 @@ def test_fused_step_repeats_and_leaves_workspace_zeroed(monkeypatch):
         assert torch.equal(o[1].view(torch.int16), outs[0][1].view(torch.int16))
         assert torch.equal(o[2], outs[0][2])
     # control counters at the head of the workspace (one per 256-byte line) are back to zero
-    ctrl_words = (2 + w.batch + 2 * w.batch * w.num_kv_heads) * 64
+    ctrl_words = (3 + w.batch + w.batch * w.num_kv_heads) * 64
     assert torch.all(st.ws[: 4 * ctrl_words] == 0)
     ref = oracle_decode(w, cpu)
     assert np.array_equal(outs[0][0].cpu().numpy(), ref["sel"])
     assert_attention_close(outs[0][1], ref["out"], "repeat")
+
+
+@pytest.mark.parametrize("path", ["fused", "pipeline"])
+def test_one_workspace_serves_different_inputs(path, monkeypatch):
+    """Two calls with different inputs on one workspace: the second equals a
+    call on a fresh workspace (nothing of the first call is left behind)."""
+    monkeypatch.setenv("LSA_DECODE_PATH", path)
+    w = small("b16_small")
+    ga = to_dev(make_inputs(w, "cpu"))
+    gb = to_dev(make_inputs(w.replace(seed=w.seed + 7), "cpu"))
+    st = GpuStep(w, ga)
+    st.run()
+    shared_ws = st.ws
+    fresh = GpuStep(w, gb)
+    fresh.run()
+    again = GpuStep(w, gb)
+    again.ws = shared_ws
+    again.run()
+    check_status_clean()
+    assert torch.equal(again.idx, fresh.idx)
+    assert torch.equal(again.out.view(torch.int16), fresh.out.view(torch.int16))
+    assert torch.equal(again.lse, fresh.lse)
+    if path == "fused":   # control counters at the head of the workspace are back to zero
+        assert torch.count_nonzero(shared_ws[: 4 * (3 + w.batch + w.batch * w.num_kv_heads) * 64]) == 0
 
 
 @pytest.mark.parametrize("splits", [1, 2, 5, 1000])
