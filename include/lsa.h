@@ -194,10 +194,9 @@ lsa_status lsa_fine_topk(const void *q, const lsa_cache *index_cache, const int3
 
 /* Step 4: sparse attention ------------------------------------------------ */
 
-/* Bytes of workspace lsa_sparse_decode needs for these shapes (split-K
- * partials and, for the persistent kernel, control counters).  The same
- * rules as lsa_decode_step's workspace apply: zero-filled before first use,
- * left zero-filled by every call that completes without a device error. */
+/* Bytes of workspace lsa_sparse_decode needs for these shapes (partial
+ * results and per-row counters).  The same rules as lsa_decode_step's
+ * workspace apply. */
 size_t lsa_sparse_decode_workspace_size(const lsa_cache *cache, const lsa_params *params);
 
 /* Exact attention over T = F U selected for every query head:
@@ -223,8 +222,9 @@ lsa_status lsa_sparse_decode(const void *q, const lsa_cache *cache, const int32_
  * serving loop whose memory plan is fixed before it starts and admits no
  * allocation afterwards.  It allocates nothing: its scratch is one buffer of
  * LSA_STATIC_SCRATCH_BYTES in the library's own static device memory, one
- * per device, zero at load and left zero-filled by every call that completes
- * without a device error.  Shapes whose lsa_sparse_decode_workspace_size
+ * per device, zero at load.  A call whose shape (cache descriptor and
+ * parameters) or implementation differs from the previous call on that
+ * device first clears the bytes it needs, on its stream.  Shapes whose lsa_sparse_decode_workspace_size
  * exceeds LSA_STATIC_SCRATCH_BYTES are rejected with LSA_ERR_WORKSPACE
  * before anything is launched.  The first call on a device looks up the
  * buffer's address once; make that first call before any stream capture
@@ -241,13 +241,15 @@ lsa_status lsa_sparse_decode_static_scratch(const void *q, const lsa_cache *cach
 /* Fused decode step ------------------------------------------------------- */
 
 /* Bytes of workspace lsa_decode_step needs.  The workspace holds the
- * block scores, the selection, split partials and (for the fused
- * persistent kernel) a small block of control counters: it must be
- * zero-filled once before its first use (e.g. cudaMemsetAsync after
- * allocation).  Every call that completes without a device error leaves it
- * zero-filled, so one workspace serves any number of calls and CUDA-graph
- * replays on one stream; after a call that recorded LSA_ERR_TIMEOUT, zero it
- * again.  Calls that share a workspace must not overlap in time. */
+ * block scores, the selection, partial results and counters, some of which
+ * must be zero when a call starts: zero-fill it before its first use (e.g.
+ * cudaMemsetAsync after allocation).  Every call that completes without a
+ * device error leaves those parts at zero again, so one workspace serves any
+ * number of calls and CUDA-graph replays of the same shape (cache
+ * descriptor and parameters) and implementation; zero it again before
+ * using it for another shape or implementation, or after a call that
+ * recorded LSA_ERR_TIMEOUT.  Calls that share a workspace must not overlap
+ * in time. */
 size_t lsa_decode_step_workspace_size(const lsa_cache *cache, const lsa_params *params);
 
 /* Steps 2-4 in one call: score every candidate block against the summaries,

@@ -180,7 +180,16 @@ lsa_status plan_attention(const CacheView &v, const lsa_params *p, bool token_mo
         const int64_t T = rows * items;
         const int64_t per_cta = std::min<int64_t>(items, (int64_t)attention_flat_warps() *
                                                               attention_flat_max_items_per_warp());
-        int64_t nc = std::max<int64_t>((int64_t)attention_flat_ctas_per_sm() * sm_count(), (T + per_cta - 1) / per_cta);
+        const int64_t slots = (int64_t)attention_flat_ctas_per_sm() * sm_count();
+        int64_t nc;
+        if (rows <= slots && items <= per_cta) {
+            // every row has the same number of item slots: a whole number of
+            // CTAs per row keeps the GPU balanced, and one CTA per row needs
+            // no merge across CTAs
+            nc = rows * (slots / rows);
+        } else {
+            nc = std::max<int64_t>(slots, (T + per_cta - 1) / per_cta);
+        }
         nc = std::min<int64_t>(nc, T);
         if (nc > 0x7fffffff) return LSA_ERR_UNSUPPORTED;
         pl->fl_ns = items;
@@ -745,8 +754,22 @@ static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
 std::mutex g_static_mu;
 void *g_static_ptr[kMaxDevices] = {};
+// what the buffer of each device last served: the counters a call needs at
+// zero are left at zero for the next call of the same shape and path, but
+// another shape lays its counters over bytes the previous one used for data
+struct ScratchUse {
+    lsa_cache cache;
+    lsa_params params;
+    bool fused;
+    bool valid;
+};
+ScratchUse g_static_use[kMaxDevices] = {};
 
-lsa_status static_scratch_for_current_device(void **ptr)
+// The device's buffer; when the call's shape or path differs from the one
+// the buffer served last, the bytes it needs are cleared first (on the
+// call's stream: a memset, no allocation).
+lsa_status static_scratch_for_current_device(const lsa_cache *cache, const lsa_params *params, bool fused,
+                                             size_t need, cudaStream_t st, void **ptr)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LSA_ERR_CUDA;
@@ -755,6 +778,16 @@ lsa_status static_scratch_for_current_device(void **ptr)
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return LSA_ERR_CUDA;
         g_static_ptr[dev] = p;
+    }
+    ScratchUse &u = g_static_use[dev];
+    const bool same = u.valid && u.fused == fused && memcmp(&u.cache, cache, sizeof *cache) == 0 &&
+                      memcmp(&u.params, params, sizeof *params) == 0;
+    if (!same) {
+        if (need > 0 && cudaMemsetAsync(g_static_ptr[dev], 0, need, st) != cudaSuccess) return LSA_ERR_CUDA;
+        u.cache = *cache;
+        u.params = *params;
+        u.fused = fused;
+        u.valid = true;
     }
     *ptr = g_static_ptr[dev];
     return LSA_OK;
@@ -771,10 +804,13 @@ extern "C" lsa_status lsa_sparse_decode_static_scratch(const void *q, const lsa_
     lsa_status rc = make_view(cache, true, &v);
     if (rc != LSA_OK) return rc;
     if ((rc = check_params(params, v)) != LSA_OK) return rc;
-    if (lsa_sparse_decode_workspace_size(cache, params) > kStaticScratchBytes) return LSA_ERR_WORKSPACE;
+    const size_t need = lsa_sparse_decode_workspace_size(cache, params);
+    if (need > kStaticScratchBytes) return LSA_ERR_WORKSPACE;
     if (params->batch == 0) return LSA_OK;
     void *scratch = nullptr;
-    if ((rc = static_scratch_for_current_device(&scratch)) != LSA_OK) return rc;
+    if ((rc = static_scratch_for_current_device(cache, params, use_fused(v, params), need,
+                                                reinterpret_cast<cudaStream_t>(stream), &scratch)) != LSA_OK)
+        return rc;
     return lsa_sparse_decode(q, cache, page_table, seq_lens, idx, params, out, lse, scratch, kStaticScratchBytes,
                              stream);
 }

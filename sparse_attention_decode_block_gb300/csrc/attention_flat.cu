@@ -28,15 +28,15 @@
 namespace lsa {
 namespace {
 
-constexpr int kFlWarps = 4;
-constexpr int kFlCtasPerSm = 2;
+constexpr int kFlWarps = 8;
+constexpr int kFlCtasPerSm = 1;
 constexpr int kFlMaxRowsPerCta = 2;   // the host keeps a CTA's piece within two rows
 constexpr int kFlMaxItemsPerWarp = 32;
 constexpr float kFlLn2 = 0.693147180559945309f;
 
 template <int DK, int G>
 struct FlLayout {
-    static constexpr int STAGES = G <= 4 ? 3 : 2;   // two CTAs per SM
+    static constexpr int STAGES = G <= 4 ? 3 : 2;   // one CTA of eight warps per SM
     static constexpr int CPR = DK / 8;            // 16-byte chunks per token row
     static constexpr int SUB = kChunk * 128;      // one swizzled 16-row x 128-byte sub-tile
     static constexpr int KBYTES = (DK / 64) * SUB;
@@ -47,7 +47,7 @@ struct FlLayout {
     static constexpr int LAST = SEG0 + kFlWarps * G * (DK + 2) * 4;   // per-row "last CTA" flags
     static constexpr int SMEM = LAST + 16;
     static_assert(RINGS >= kFlMaxRowsPerCta * kFlWarps * G * (DK + 2) * 4, "the CTA merge reuses the rings");
-    static_assert(SMEM * kFlCtasPerSm <= 227 * 1024, "two CTAs per SM");
+    static_assert(SMEM * kFlCtasPerSm <= 227 * 1024, "the CTAs of one SM");
 };
 
 // Row index -> (request, KV head, query subgroup).
@@ -71,7 +71,7 @@ __device__ __forceinline__ int fl_cta_of(const AttnArgs &a, int64_t i)
 }
 
 template <int DK, int G>
-__global__ void __launch_bounds__(kFlWarps * 32) k_attn_flat(AttnArgs a)
+__global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
 {
     using LY = FlLayout<DK, G>;
     constexpr int NT = DK / 8;
@@ -101,16 +101,44 @@ __global__ void __launch_bounds__(kFlWarps * 32) k_attn_flat(AttnArgs a)
     const uint32_t ring_s = smem_addr(ring);
     int *stage_n = reinterpret_cast<int *>(smem + kFlWarps * LY::WARP_RING) + warp * 4;
 
-    // ---- descriptors of this warp's items, one per lane
+    const int rr = lane >> 2, cc = lane & 3;
+
+    // ---- descriptors of this warp's items, one per lane, in two round
+    // trips: the request length, the selection entries (read assuming the
+    // sink takes its full number of items, re-read in the rare case it does
+    // not) and the query fragments of the warp's rows, then the page ids
     ItemDesc my{-1, 0, 0};
-    int my_rho = -1;
+    int my_rho = -1, my_k = 0, my_L = 0;
+    int2 my_sel = make_int2(-1, -1);
+    const int nsc_full = (a.sink + kChunk - 1) / kChunk;
     if (lane < nmine) {
         const int64_t i = ws + lane;
         my_rho = (int)(i / NS);
-        const int k = (int)(i % NS);
+        my_k = (int)(i % NS);
         const FlRow x = fl_row(a, my_rho);
-        const RowPlan pl = make_plan(a, x.r, k == 0 && x.h == 0 && x.sg == 0);
-        my = k < pl.n_items ? describe_item(a, pl, x.r, x.h, k) : ItemDesc{-1, 0, 0};
+        my_L = a.lens[x.r];
+        my_sel = item_sel_entries(a, x.r, x.h, nsc_full, my_k);
+    }
+    const int rho_w0 = nmine > 0 ? (int)(ws / NS) : -1;
+    const int rho_w1 = nmine > 0 ? (int)((ws + nmine - 1) / NS) : -1;
+    uint32_t qa0[DK / 16], qa2[DK / 16], qb0[DK / 16], qb2[DK / 16];
+    auto load_q = [&](int rho, uint32_t (&q0)[DK / 16], uint32_t (&q2)[DK / 16]) {
+        const FlRow x = fl_row(a, rho < 0 ? 0 : rho);
+        const bool qrow = rr < G && rho >= 0;
+        const uint16_t *qp = a.q + ((int64_t)x.r * a.hq + x.h * Gt + x.sg * G + (qrow ? rr : 0)) * DK;
+#pragma unroll
+        for (int ks = 0; ks < DK / 16; ++ks) {
+            q0[ks] = qrow ? *reinterpret_cast<const uint32_t *>(qp + 16 * ks + 2 * cc) : 0u;
+            q2[ks] = qrow ? *reinterpret_cast<const uint32_t *>(qp + 16 * ks + 8 + 2 * cc) : 0u;
+        }
+    };
+    load_q(rho_w0, qa0, qa2);
+    load_q(rho_w1 != rho_w0 ? rho_w1 : -1, qb0, qb2);
+    if (lane < nmine) {
+        const FlRow x = fl_row(a, my_rho);
+        const RowPlan pl = plan_of_len(a, my_L, my_k == 0 && x.h == 0 && x.sg == 0);
+        if (pl.nsc != nsc_full) my_sel = item_sel_entries(a, x.r, x.h, pl.nsc, my_k);
+        my = my_k < pl.n_items ? describe_item_sel(a, pl, x.r, x.h, my_k, my_sel) : ItemDesc{-1, 0, 0};
     }
 
     auto issue = [&](int j) {
@@ -141,7 +169,6 @@ __global__ void __launch_bounds__(kFlWarps * 32) k_attn_flat(AttnArgs a)
         cp_async_commit();
     };
 
-    const int rr = lane >> 2, cc = lane & 3;
     const int mi = lane >> 3, r8 = lane & 7;
     const int tk = (mi >> 1) * 8 + r8, ck = mi & 1;
     const int tv = (mi & 1) * 8 + r8, cv = mi >> 1;
@@ -158,7 +185,6 @@ __global__ void __launch_bounds__(kFlWarps * 32) k_attn_flat(AttnArgs a)
         s0m[lane] = -INFINITY;
         s0m[G + lane] = 0.f;
     }
-    uint32_t qa0[DK / 16], qa2[DK / 16];
     int cur_rho = -1;
 
     auto write_state = [&](float *dst_o, float *dst_ml) {
@@ -181,13 +207,12 @@ __global__ void __launch_bounds__(kFlWarps * 32) k_attn_flat(AttnArgs a)
         l = 0.f;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-        const FlRow x = fl_row(a, rho);
-        const bool qrow = rr < G;
-        const uint16_t *qp = a.q + ((int64_t)x.r * a.hq + x.h * Gt + x.sg * G + (qrow ? rr : 0)) * DK;
+        if (rho != rho_w0) {   // the warp's second row: its query fragments were loaded up front
 #pragma unroll
-        for (int ks = 0; ks < DK / 16; ++ks) {
-            qa0[ks] = qrow ? *reinterpret_cast<const uint32_t *>(qp + 16 * ks + 2 * cc) : 0u;
-            qa2[ks] = qrow ? *reinterpret_cast<const uint32_t *>(qp + 16 * ks + 8 + 2 * cc) : 0u;
+            for (int ks = 0; ks < DK / 16; ++ks) {
+                qa0[ks] = qb0[ks];
+                qa2[ks] = qb2[ks];
+            }
         }
     };
 

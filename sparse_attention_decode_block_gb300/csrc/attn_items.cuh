@@ -16,10 +16,9 @@ struct RowPlan {
     int nsc, nsel_items, nrc, n_items;
 };
 
-__device__ __forceinline__ RowPlan make_plan(const AttnArgs &a, int r, bool flag_bad)
+__device__ __forceinline__ RowPlan plan_of_len(const AttnArgs &a, int L, bool flag_bad)
 {
     RowPlan pl;
-    int L = a.lens[r];
     if (L < 0 || (int64_t)L > (int64_t)a.max_blocks * a.c.b) {
         if (flag_bad) flag_error(a.status, LSA_ERR_BOUNDS);
         L = 0;
@@ -34,10 +33,38 @@ __device__ __forceinline__ RowPlan make_plan(const AttnArgs &a, int r, bool flag
     return pl;
 }
 
+__device__ __forceinline__ RowPlan make_plan(const AttnArgs &a, int r, bool flag_bad)
+{
+    return plan_of_len(a, a.lens[r], flag_bad);
+}
+
+// Selected-block item k of a row: the selection entry it reads and the one
+// before it (for the ascending check), or (-1, -1) when k is not a
+// selected-block item under a plan whose sink covers nsc items.
+__device__ __forceinline__ int2 item_sel_entries(const AttnArgs &a, int r, int h, int nsc, int i)
+{
+    const int k = i - nsc, cpb = a.c.b / kChunk;
+    if (a.token_mode || k < 0 || k >= a.nsel * cpb) return make_int2(-1, -1);
+    const int ei = k / cpb;
+    const int32_t *irow = a.idx + ((int64_t)r * a.c.hkv + h) * a.nsel;
+    return make_int2(irow[ei], ei > 0 ? irow[ei - 1] : -1);
+}
+
 // Resolves item i of row (r, h) to a run of token rows within one page:
 // d = {page, slot of the first token, rows}; rows = 0 for nothing to attend,
 // rows = -1 for a token-list item (rows resolved per token).
+__device__ ItemDesc describe_item_sel(const AttnArgs &a, const RowPlan &pl, int r, int h, int i, int2 sel);
+
 __device__ ItemDesc describe_item(const AttnArgs &a, const RowPlan &pl, int r, int h, int i)
+{
+    const int2 sel = (i >= pl.nsc && i < pl.nsc + pl.nsel_items) ? item_sel_entries(a, r, h, pl.nsc, i)
+                                                                  : make_int2(-1, -1);
+    return describe_item_sel(a, pl, r, h, i, sel);
+}
+
+// As describe_item, with the item's selection entries (item_sel_entries
+// under this plan) already loaded.
+__device__ ItemDesc describe_item_sel(const AttnArgs &a, const RowPlan &pl, int r, int h, int i, int2 sel)
 {
     const int b = a.c.b;
     ItemDesc d;
@@ -55,10 +82,8 @@ __device__ ItemDesc describe_item(const AttnArgs &a, const RowPlan &pl, int r, i
         }
         const int k = i - pl.nsc;
         const int cpb = b / kChunk;
-        const int ei = k / cpb, ck = k % cpb;
-        const int32_t *irow = a.idx + ((int64_t)r * a.c.hkv + h) * a.nsel;
-        const int e = irow[ei];
-        const int prev = ei > 0 ? irow[ei - 1] : -1;
+        const int ck = k % cpb;
+        const int e = sel.x, prev = sel.y;
         const bool valid = e >= 0 && e < a.max_blocks && (int64_t)e * b >= pl.se &&
                            (int64_t)(e + 1) * b <= pl.rs && prev < e;
         if (!valid && e != -1 && ck == 0) flag_error(a.status, LSA_ERR_BOUNDS);
