@@ -166,11 +166,19 @@ def kernels_per_step(inst) -> int:
     import ctypes
     if fused_path(inst.w):
         return 1
-    lib = inst.L.load_library()
-    # score + top-k (+ fine score + fine top-k) + attention (+ merge when split)
-    n = 2 + (2 if inst.w.c2f_candidates > 0 else 0) + 1
-    ws_attn = lib.lsa_sparse_decode_workspace_size(ctypes.byref(inst.cache), ctypes.byref(inst.params))
-    return n + (1 if ws_attn > 0 else 0)
+    w = inst.w
+    # score + top-k (+ fine score + fine top-k) + attention
+    n = 2 + (2 if w.c2f_candidates > 0 else 0) + 1
+    # the tensor-core attention (GQA groups of 2..8, dk = dv in {64, 128})
+    # merges its parts itself; the CUDA-core kernel adds a merge launch when split
+    group = w.num_q_heads // w.num_kv_heads
+    tc = (w.c2f_candidates == 0 and not w.v_aliased and w.dk == w.dv and w.dk in (64, 128)
+          and group % 2 == 0 and os.environ.get("LSA_ATTENTION_PATH") != "cuda_core")
+    if not tc:
+        lib = inst.L.load_library()
+        ws_attn = lib.lsa_sparse_decode_workspace_size(ctypes.byref(inst.cache), ctypes.byref(inst.params))
+        n += 1 if ws_attn > 0 else 0
+    return n
 
 
 def stage_times(insts, reps: int, stream) -> dict:

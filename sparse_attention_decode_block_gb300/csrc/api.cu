@@ -204,9 +204,13 @@ lsa_status plan_attention(const CacheView &v, const lsa_params *p, bool token_mo
     return LSA_OK;
 }
 
+// sel_scores: the attention kernel selects the blocks itself from these fp32
+// score rows (only with the even-split plan, see attention_flat_can_select)
+// and writes the selection to sel_write when that is not NULL.
 lsa_status run_attention(const void *q, const CacheView &v, const int32_t *pt, const int32_t *lens,
                          const int32_t *idx, const lsa_params *p, bool token_mode, void *out, float *lse,
-                         uint8_t *ws, size_t ws_bytes, cudaStream_t st)
+                         uint8_t *ws, size_t ws_bytes, cudaStream_t st, const float *sel_scores = nullptr,
+                         int32_t *sel_write = nullptr)
 {
     AttnPlan pl;
     lsa_status rc = plan_attention(v, p, token_mode, &pl);
@@ -234,7 +238,11 @@ lsa_status run_attention(const void *q, const CacheView &v, const int32_t *pt, c
     a.lse = lse;
     a.status = status_word();
     a.spin_budget = kSpinBudget;
+    if (sel_scores && !pl.flat) return LSA_ERR_UNSUPPORTED;
     if (pl.flat) {
+        a.sel_scores = sel_scores;
+        a.sel_cols = p->max_blocks;
+        a.sel_write = sel_write;
         a.fl_ns = pl.fl_ns;
         a.fl_total = pl.fl_total;
         a.fl_ctas = pl.fl_ctas;
@@ -714,6 +722,13 @@ lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *su
     t.cols = params->max_blocks;
     t.status = status;
     if (!c2f) {
+        // with the even-split attention the attention kernel selects the
+        // blocks itself (no top-k launch, the selection stays on chip)
+        AttnPlan apl;
+        if (plan_attention(v, params, false, &apl) == LSA_OK && apl.flat &&
+            attention_flat_can_select(params->max_blocks, params->k_blocks))
+            return run_attention(q, v, page_table, seq_lens, nullptr, params, false, out, lse, ws_attn, L.attn, st,
+                                 scores, idx_out);
         t.k = params->k_blocks;
         t.idx = sel;
         e = launch_topk(t, st, &unsup);

@@ -115,6 +115,7 @@ __device__ int issue_item(const AttnArgs &a, int h, const ItemDesc &d, const int
 template <int DK, int DV, int GS, bool ALIAS>
 __global__ void __launch_bounds__(kAttnThreads, 2) k_sparse_attn(AttnArgs a)
 {
+    pdl_enter();
     using LY = Layout<DK, DV, ALIAS>;
     constexpr int NCK = DK / 64;   // 8-dim key chunks per lane
     constexpr int NCV = DV / 64;   // 8-dim value chunks per lane
@@ -377,6 +378,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_sparse_attn(AttnArgs a)
 // Log-sum-exp merge of the split partials: weights exp2(lse_s - max).
 __global__ void k_merge(MergeArgs a)
 {
+    pdl_enter();
     const int row = blockIdx.x;
     const int d = threadIdx.x * 4;
     if (d >= a.dv) return;
@@ -420,7 +422,8 @@ cudaError_t launch_attn_t(const AttnArgs &a, cudaStream_t s)
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnMaxSmem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.splits, a.c.hkv * a.nsub, a.batch);
-    kern<<<grid, kAttnThreads, smem, s>>>(a);
+    cudaError_t le = launch_step_kernel(kern, grid, dim3(kAttnThreads), smem, s, a);
+    if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 
@@ -472,7 +475,8 @@ cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s, bool *unsupporte
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s)
 {
     if (a.rows == 0) return cudaSuccess;
-    k_merge<<<a.rows, (a.dv + 3) / 4, 0, s>>>(a);
+    cudaError_t le = launch_step_kernel(k_merge, dim3(a.rows), dim3((a.dv + 3) / 4), 0, s, a);
+    if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 

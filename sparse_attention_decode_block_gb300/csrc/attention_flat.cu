@@ -24,6 +24,7 @@
 
 #include "attn_items.cuh"
 #include "lsa_device.cuh"
+#include "topk_block.cuh"
 
 namespace lsa {
 namespace {
@@ -32,6 +33,7 @@ constexpr int kFlWarps = 8;
 constexpr int kFlCtasPerSm = 1;
 constexpr int kFlMaxRowsPerCta = 2;   // the host keeps a CTA's piece within two rows
 constexpr int kFlMaxItemsPerWarp = 32;
+constexpr int kFlMaxSel = 512;        // blocks a CTA selects per row when it selects them itself
 constexpr float kFlLn2 = 0.693147180559945309f;
 
 template <int DK, int G>
@@ -45,7 +47,9 @@ struct FlLayout {
     static constexpr int RINGS = kFlWarps * WARP_RING;
     static constexpr int SEG0 = RINGS + kFlWarps * 16;            // first-row results: [W][G][DK], m, l
     static constexpr int LAST = SEG0 + kFlWarps * G * (DK + 2) * 4;   // per-row "last CTA" flags
-    static constexpr int SMEM = LAST + 16;
+    static constexpr int SELBUF = LAST + 16;                          // top-k scratch, then [2][kFlMaxSel] selection
+    static constexpr int SELS = SELBUF + ((int)sizeof(TopkScratch) + 15) / 16 * 16;
+    static constexpr int SMEM = SELS + 2 * kFlMaxSel * 4;
     static_assert(RINGS >= kFlMaxRowsPerCta * kFlWarps * G * (DK + 2) * 4, "the CTA merge reuses the rings");
     static_assert(SMEM * kFlCtasPerSm <= 227 * 1024, "the CTAs of one SM");
 };
@@ -70,10 +74,14 @@ __device__ __forceinline__ int fl_cta_of(const AttnArgs &a, int64_t i)
     return (int)(i * a.fl_ctas / a.fl_total);
 }
 
-template <int DK, int G>
+// KSEL > 0: the CTA selects its rows' blocks itself from the score rows
+// (block_topk with KSEL keys per thread) instead of reading a selection.
+template <int DK, int G, int KSEL>
 __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
 {
+    pdl_enter();
     using LY = FlLayout<DK, G>;
+    static_assert(KSEL == 0 || kFlWarps * 32 == kTfThreads, "one CTA is one top-k block");
     constexpr int NT = DK / 8;
     constexpr int CPL = kChunk * LY::CPR / 32;
     constexpr int kFlStages = LY::STAGES;
@@ -103,6 +111,40 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
 
     const int rr = lane >> 2, cc = lane & 3;
 
+    // ---- the selection of the (request, KV head) rows of this piece (at
+    // most two), when this kernel makes it: exact top-k of each score row,
+    // written out by the CTA that holds the row's first item
+    int32_t *s_sel = reinterpret_cast<int32_t *>(smem + LY::SELS);   // [2][kFlMaxSel]
+    const int rh_first = rho_first / a.nsub;
+    if constexpr (KSEL > 0) {
+        TopkScratch &sm = *reinterpret_cast<TopkScratch *>(smem + LY::SELBUF);
+        const int rh_last = (int)((ce - 1) / NS) / a.nsub;
+        const bool aligned = (a.sel_cols & 3) == 0 && (reinterpret_cast<uintptr_t>(a.sel_scores) & 15) == 0;
+        for (int s = 0; s < 2 && rh_first + s <= rh_last; ++s) {
+            const int rh = rh_first + s;
+            int32_t *dst = s_sel + s * kFlMaxSel;
+            const int keff = block_topk<KSEL>(a.sel_scores + (int64_t)rh * a.sel_cols, a.sel_cols, aligned, a.nsel,
+                                              a.status, sm, [&](int pos, int col) { dst[pos] = col; });
+            for (int i = keff + (int)threadIdx.x; i < a.nsel; i += blockDim.x) dst[i] = -1;
+            __syncthreads();
+            if (a.sel_write && fl_cta_of(a, (int64_t)rh * a.nsub * NS) == cta)
+                for (int i = threadIdx.x; i < a.nsel; i += blockDim.x) a.sel_write[(int64_t)rh * a.nsel + i] = dst[i];
+        }
+    }
+    // selection entries (entry, the one before it) of item k of this lane's
+    // row under a plan whose sink takes nsc items
+    auto sel_entries = [&](int rho, int r, int h, int nsc, int k) -> int2 {
+        if constexpr (KSEL > 0) {
+            const int kk = k - nsc, cpb = a.c.b / kChunk;
+            if (kk < 0 || kk >= a.nsel * cpb) return make_int2(-1, -1);
+            const int ei = kk / cpb;
+            const int32_t *srow = s_sel + (rho / a.nsub - rh_first) * kFlMaxSel;
+            return make_int2(srow[ei], ei > 0 ? srow[ei - 1] : -1);
+        } else {
+            return item_sel_entries(a, r, h, nsc, k);
+        }
+    };
+
     // ---- descriptors of this warp's items, one per lane, in two round
     // trips: the request length, the selection entries (read assuming the
     // sink takes its full number of items, re-read in the rare case it does
@@ -117,7 +159,7 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
         my_k = (int)(i % NS);
         const FlRow x = fl_row(a, my_rho);
         my_L = a.lens[x.r];
-        my_sel = item_sel_entries(a, x.r, x.h, nsc_full, my_k);
+        my_sel = sel_entries(my_rho, x.r, x.h, nsc_full, my_k);
     }
     const int rho_w0 = nmine > 0 ? (int)(ws / NS) : -1;
     const int rho_w1 = nmine > 0 ? (int)((ws + nmine - 1) / NS) : -1;
@@ -137,7 +179,7 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
     if (lane < nmine) {
         const FlRow x = fl_row(a, my_rho);
         const RowPlan pl = plan_of_len(a, my_L, my_k == 0 && x.h == 0 && x.sg == 0);
-        if (pl.nsc != nsc_full) my_sel = item_sel_entries(a, x.r, x.h, pl.nsc, my_k);
+        if (pl.nsc != nsc_full) my_sel = sel_entries(my_rho, x.r, x.h, pl.nsc, my_k);
         my = my_k < pl.n_items ? describe_item_sel(a, pl, x.r, x.h, my_k, my_sel) : ItemDesc{-1, 0, 0};
     }
 
@@ -398,14 +440,15 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
     }
 }
 
-template <int DK, int G>
+template <int DK, int G, int KSEL>
 cudaError_t launch_flat_t(const AttnArgs &a, cudaStream_t s)
 {
     using LY = FlLayout<DK, G>;
-    auto kern = k_attn_flat<DK, G>;
+    auto kern = k_attn_flat<DK, G, KSEL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<a.fl_ctas, kFlWarps * 32, LY::SMEM, s>>>(a);
+    e = launch_step_kernel(kern, dim3(a.fl_ctas), dim3(kFlWarps * 32), LY::SMEM, s, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -414,13 +457,23 @@ cudaError_t launch_flat_t(const AttnArgs &a, cudaStream_t s)
 int attention_flat_ctas_per_sm() { return kFlCtasPerSm; }
 int attention_flat_warps() { return kFlWarps; }
 int attention_flat_max_items_per_warp() { return kFlMaxItemsPerWarp; }
+bool attention_flat_can_select(int cols, int k) { return cols <= kTfThreads * 32 && k > 0 && k <= kFlMaxSel; }
 
 cudaError_t launch_attention_flat(const AttnArgs &a, int gs, cudaStream_t s, bool *unsupported)
 {
     *unsupported = false;
     if (a.batch == 0 || a.fl_total == 0) return cudaSuccess;
-#define LSA_FL_CASE(D, G_) \
-    if (a.c.dk == D && gs == G_) return launch_flat_t<D, G_>(a, s);
+    const int ksel = !a.sel_scores ? 0 : (a.sel_cols <= kTfThreads * 8 ? 8 : 32);
+    if (a.sel_scores && (a.sel_cols > kTfThreads * 32 || a.nsel > kFlMaxSel || a.nsel <= 0)) {
+        *unsupported = true;
+        return cudaSuccess;
+    }
+#define LSA_FL_CASE(D, G_)                                                    \
+    if (a.c.dk == D && gs == G_) {                                            \
+        if (ksel == 8) return launch_flat_t<D, G_, 8>(a, s);                  \
+        if (ksel == 32) return launch_flat_t<D, G_, 32>(a, s);                \
+        return launch_flat_t<D, G_, 0>(a, s);                                 \
+    }
     LSA_FL_CASE(64, 2) LSA_FL_CASE(64, 4) LSA_FL_CASE(64, 8)
     LSA_FL_CASE(128, 2) LSA_FL_CASE(128, 4) LSA_FL_CASE(128, 8)
 #undef LSA_FL_CASE

@@ -47,6 +47,7 @@ struct TcLayout {
 template <int DK, int G>
 __global__ void __launch_bounds__(kTcWarps * 32) k_sparse_attn_tc(AttnArgs a)
 {
+    pdl_enter();
     using LY = TcLayout<DK>;
     constexpr int NT = DK / 8;        // n-tiles of the output (DV = DK)
     constexpr int CPL = kChunk * LY::CPR / 32;   // 16-byte chunks per lane per tile
@@ -265,7 +266,8 @@ cudaError_t launch_tc_t(const AttnArgs &a, cudaStream_t s)
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(a.splits, a.c.hkv * a.nsub, a.batch);
-    kern<<<grid, kTcWarps * 32, LY::SMEM, s>>>(a);
+    e = launch_step_kernel(kern, grid, dim3(kTcWarps * 32), LY::SMEM, s, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -93,6 +93,12 @@ struct AttnArgs {
     int32_t fl_ns, fl_ctas, fl_parts;
     int64_t fl_total;
     uint32_t *row_done;
+    // selection made by the attention kernel itself from fp32 score rows
+    // [B*hkv, sel_cols] (NULL: read idx); sel_write: where it writes the
+    // selection out [B*hkv, nsel], or NULL
+    const float *sel_scores;
+    int32_t sel_cols;
+    int32_t *sel_write;
     float *o_part;              // [B*Hq, splits or fl_parts, dv]
     float *lse_part;            // [B*Hq, splits or fl_parts]   log2 domain
     uint16_t *out;              // [B, Hq, dv] bf16     (splits == 1)
@@ -170,7 +176,9 @@ cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);
 int attention_flat_ctas_per_sm();
 int attention_flat_warps();
 int attention_flat_max_items_per_warp();
+bool attention_flat_can_select(int cols, int k);
 cudaError_t launch_attention_flat(const AttnArgs &a, int gs, cudaStream_t s, bool *unsupported);
+bool launch_topk_fast(const TopkArgs &a, cudaStream_t s, cudaError_t *err);
 cudaError_t launch_attention_tc(const AttnArgs &a, int gs, cudaStream_t s, bool *unsupported);
 int attention_tc_group(int dk, int dv, int group, bool alias, bool token_mode, const CacheView &v);
 int attention_tc_max_items_per_split(int dk);

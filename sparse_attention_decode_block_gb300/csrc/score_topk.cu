@@ -33,6 +33,7 @@ constexpr int kPtPerThread = kScoreMaxChunk / (kScoreWarps * 32);
 template <int DK, int HKV>
 __global__ void __launch_bounds__(kScoreWarps * 32, 2) k_score(ScoreArgs a)
 {
+    pdl_enter();
     constexpr int NCH = HKV * DK / 8;      // 16-byte chunks of one page's summary row
     constexpr int NI = (NCH + 31) / 32;    // chunks per lane
     constexpr int CPH = DK / 8;            // chunks per head
@@ -224,6 +225,7 @@ __device__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_sums)
 
 __global__ void __launch_bounds__(kTopkThreads) k_topk_rows(TopkArgs a)
 {
+    pdl_enter();
     extern __shared__ uint32_t keys[];
     __shared__ uint32_t hist[256];
     __shared__ uint32_t warp_sums[32];
@@ -359,6 +361,7 @@ constexpr int kFineBlocksPerCta = 4;
 // with their original FP8 indexer keys).  8 lanes per token, 16 dims each.
 __global__ void __launch_bounds__(kFineWarps * 32) k_fine_scores(FineArgs a)
 {
+    pdl_enter();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int row = blockIdx.y;                 // r * hkv + h
     const int hkv = a.ic.hkv;
@@ -428,7 +431,8 @@ template <int DK, int HKV>
 cudaError_t launch_score_t(const ScoreArgs &a, cudaStream_t s)
 {
     dim3 grid((a.max_blocks + a.chunk - 1) / a.chunk, a.batch);
-    k_score<DK, HKV><<<grid, kScoreWarps * 32, 0, s>>>(a);
+    cudaError_t le = launch_step_kernel(k_score<DK, HKV>, grid, dim3(kScoreWarps * 32), 0, s, a);
+    if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 
@@ -475,10 +479,13 @@ cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s, bool *unsupported)
 {
     *unsupported = a.cols > kTopkMaxCols;
     if (*unsupported || a.rows == 0 || a.k == 0) return cudaSuccess;
+    cudaError_t fe = cudaSuccess;
+    if (launch_topk_fast(a, s, &fe)) return fe;   // rows of up to 8192 columns
     const size_t smem = (size_t)max(a.cols, 1) * sizeof(uint32_t);
     cudaError_t e = cudaFuncSetAttribute(k_topk_rows, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_topk_rows<<<a.rows, kTopkThreads, smem, s>>>(a);
+    e = launch_step_kernel(k_topk_rows, dim3(a.rows), dim3(kTopkThreads), smem, s, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -487,7 +494,8 @@ cudaError_t launch_fine_scores(const FineArgs &a, cudaStream_t s, bool *unsuppor
     *unsupported = a.ic.dk != 128 || !a.ic.e4m3 || a.ic.b % 4 != 0;
     if (*unsupported || a.batch == 0 || a.ncand == 0) return cudaSuccess;
     dim3 grid((a.ncand + kFineBlocksPerCta - 1) / kFineBlocksPerCta, a.batch * a.ic.hkv);
-    k_fine_scores<<<grid, kFineWarps * 32, 0, s>>>(a);
+    cudaError_t le = launch_step_kernel(k_fine_scores, grid, dim3(kFineWarps * 32), 0, s, a);
+    if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 
