@@ -44,8 +44,9 @@ L2_BYTES = 129 * 1024 * 1024
 
 # DRAM bytes per launch from one ncu capture of each kernel as it stands
 # (read + write); a kernel changed since its capture has no entry.
-NCU_TRAFFIC = {
-    "attention": 67_441_152 + 831_232,   # k_sparse_attn_tc<128,4>, profiles/kernels_b16_32k_pipeline.md
+NCU_TRAFFIC = {   # profiles/kernels_b16_32k_pipeline.md
+    "k_attn_flat (selects)": 68_487_424 + 678_656,
+    "k_score": 67_334_656 + 302_080,
 }
 
 
@@ -162,11 +163,25 @@ def fused_path(w) -> bool:
             and w.dk in (64, 128) and group <= 8 and w.block_size in (16, 64) and not w.v_aliased)
 
 
+def selects_in_attention(w) -> bool:
+    """The library lets the attention kernel select the blocks (no top-k
+    launch) when the tensor-core attention with an even split applies:
+    GQA groups of 2..8 (even), dk = dv in {64, 128}, no coarse-to-fine pass,
+    rows of at most 8192 blocks, 0 < k <= 512."""
+    group = w.num_q_heads // w.num_kv_heads
+    max_blocks = -(-w.seq_len // w.block_size) if w.seq_len else None
+    return (not fused_path(w) and w.c2f_candidates == 0 and not w.v_aliased and w.dk == w.dv
+            and w.dk in (64, 128) and group % 2 == 0 and os.environ.get("LSA_ATTENTION_PATH") != "cuda_core"
+            and max_blocks is not None and max_blocks <= 8192 and 0 < w.k_blocks <= 512)
+
+
 def kernels_per_step(inst) -> int:
     import ctypes
     if fused_path(inst.w):
         return 1
     w = inst.w
+    if selects_in_attention(w):
+        return 2   # score, attention with the selection inside
     # score + top-k (+ fine score + fine top-k) + attention
     n = 2 + (2 if w.c2f_candidates > 0 else 0) + 1
     # the tensor-core attention (GQA groups of 2..8, dk = dv in {64, 128})
@@ -455,14 +470,26 @@ def main():
     peak, peak_kind = peaks()
     gbs = res["step_bytes"] / (ms_step / 1e3) / 1e9
     st = res["stages"]
-    dominant = None if fused_path(w) else (max(st, key=st.get) if st else None)
     acc = res["acc"]
     stage_bytes = {"score": acc["summaries"] + acc["page_table"] + acc["q_out"] // 2,
-                   "attention": acc["kv"] + acc["q_out"], "topk": 0}
+                   "attention": acc["kv"] + acc["q_out"] // 2 + acc["q_out"] // 2, "topk": 0}
+    kernel_ms = {}
+    if st and selects_in_attention(w):
+        # the step is two launches: the score kernel and the attention kernel
+        # that also selects the blocks; the latter's time is the step's time
+        # minus the score kernel's (both CUDA-event timings)
+        kernel_ms = {"k_score": st["score"], "k_attn_flat (selects)": max(ms_step - st["score"], 1e-9)}
+        kbytes = {"k_score": stage_bytes["score"], "k_attn_flat (selects)": stage_bytes["attention"]}
+    elif st:
+        kernel_ms = dict(st)
+        kbytes = stage_bytes
+    dominant = None if fused_path(w) or not kernel_ms else max(kernel_ms, key=kernel_ms.get)
     if dominant:
-        ach = stage_bytes[dominant] / (st[dominant] / 1e3) / 1e9
+        ach = kbytes[dominant] / (kernel_ms[dominant] / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4), "peak_kind": peak_kind,
+                "duration_us": round(kernel_ms[dominant] * 1e3, 2),
+                "timing": "step minus score kernel" if dominant.startswith("k_attn_flat") else "CUDA graph of the stage",
                 "traffic": NCU_TRAFFIC.get(dominant) if w.name == "b16_32k" else None}
     else:
         # the persistent kernel is the whole step: its launch time is the step time
@@ -487,6 +514,7 @@ def main():
         "step": {"algorithmic_bytes": res["step_bytes"], "bytes_split": acc, "gbs": round(gbs, 1),
                  "frac_of_peak": round(gbs / peak, 4), "frac_of_8tbs": round(gbs / 8000.0, 4)},
         "stages_ms": {k: round(v, 5) for k, v in st.items()},
+        "kernels_ms": {k: round(v, 5) for k, v in kernel_ms.items()},
         "roofline": roof,
         "cpu_baseline": cb,
         "e2e": {"value": round(1e3 / e2e["ms_per_step"] * world, 1), "unit": "calls/s",
