@@ -44,10 +44,9 @@ L2_BYTES = 129 * 1024 * 1024
 
 # DRAM bytes per launch from one ncu capture of each kernel as it stands
 # (read + write); a kernel changed since its capture has no entry.
-NCU_TRAFFIC = {   # profiles/kernels_b16_32k_pipeline.md
-    "k_attn_flat (selects)": 68_487_424 + 678_656,
-    "k_score": 67_334_656 + 302_080,
-}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch from the ncu capture
+# summarised in profiles/; emptied whenever a kernel changes after its capture.
+NCU_TRAFFIC = {}
 
 
 def peaks():

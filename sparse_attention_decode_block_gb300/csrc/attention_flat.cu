@@ -111,6 +111,37 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
 
     const int rr = lane >> 2, cc = lane & 3;
 
+    // ---- descriptors of this warp's items, one per lane: the request
+    // length and the query fragments of the warp's rows are loaded first
+    // (while the CTA selects, when it does), then the selection entries
+    // (read assuming the sink takes its full number of items, re-read in
+    // the rare case it does not), then the page ids
+    ItemDesc my{-1, 0, 0};
+    int my_rho = -1, my_k = 0, my_L = 0;
+    int2 my_sel = make_int2(-1, -1);
+    const int nsc_full = (a.sink + kChunk - 1) / kChunk;
+    if (lane < nmine) {
+        const int64_t i = ws + lane;
+        my_rho = (int)(i / NS);
+        my_k = (int)(i % NS);
+        my_L = a.lens[fl_row(a, my_rho).r];
+    }
+    const int rho_w0 = nmine > 0 ? (int)(ws / NS) : -1;
+    const int rho_w1 = nmine > 0 ? (int)((ws + nmine - 1) / NS) : -1;
+    uint32_t qa0[DK / 16], qa2[DK / 16], qb0[DK / 16], qb2[DK / 16];
+    auto load_q = [&](int rho, uint32_t (&q0)[DK / 16], uint32_t (&q2)[DK / 16]) {
+        const FlRow x = fl_row(a, rho < 0 ? 0 : rho);
+        const bool qrow = rr < G && rho >= 0;
+        const uint16_t *qp = a.q + ((int64_t)x.r * a.hq + x.h * Gt + x.sg * G + (qrow ? rr : 0)) * DK;
+#pragma unroll
+        for (int ks = 0; ks < DK / 16; ++ks) {
+            q0[ks] = qrow ? *reinterpret_cast<const uint32_t *>(qp + 16 * ks + 2 * cc) : 0u;
+            q2[ks] = qrow ? *reinterpret_cast<const uint32_t *>(qp + 16 * ks + 8 + 2 * cc) : 0u;
+        }
+    };
+    load_q(rho_w0, qa0, qa2);
+    load_q(rho_w1 != rho_w0 ? rho_w1 : -1, qb0, qb2);
+
     // ---- the selection of the (request, KV head) rows of this piece (at
     // most two), when this kernel makes it: exact top-k of each score row,
     // written out by the CTA that holds the row's first item
@@ -145,44 +176,15 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
         }
     };
 
-    // ---- descriptors of this warp's items, one per lane, in two round
-    // trips: the request length, the selection entries (read assuming the
-    // sink takes its full number of items, re-read in the rare case it does
-    // not) and the query fragments of the warp's rows, then the page ids
-    ItemDesc my{-1, 0, 0};
-    int my_rho = -1, my_k = 0, my_L = 0;
-    int2 my_sel = make_int2(-1, -1);
-    const int nsc_full = (a.sink + kChunk - 1) / kChunk;
     if (lane < nmine) {
-        const int64_t i = ws + lane;
-        my_rho = (int)(i / NS);
-        my_k = (int)(i % NS);
         const FlRow x = fl_row(a, my_rho);
-        my_L = a.lens[x.r];
         my_sel = sel_entries(my_rho, x.r, x.h, nsc_full, my_k);
-    }
-    const int rho_w0 = nmine > 0 ? (int)(ws / NS) : -1;
-    const int rho_w1 = nmine > 0 ? (int)((ws + nmine - 1) / NS) : -1;
-    uint32_t qa0[DK / 16], qa2[DK / 16], qb0[DK / 16], qb2[DK / 16];
-    auto load_q = [&](int rho, uint32_t (&q0)[DK / 16], uint32_t (&q2)[DK / 16]) {
-        const FlRow x = fl_row(a, rho < 0 ? 0 : rho);
-        const bool qrow = rr < G && rho >= 0;
-        const uint16_t *qp = a.q + ((int64_t)x.r * a.hq + x.h * Gt + x.sg * G + (qrow ? rr : 0)) * DK;
-#pragma unroll
-        for (int ks = 0; ks < DK / 16; ++ks) {
-            q0[ks] = qrow ? *reinterpret_cast<const uint32_t *>(qp + 16 * ks + 2 * cc) : 0u;
-            q2[ks] = qrow ? *reinterpret_cast<const uint32_t *>(qp + 16 * ks + 8 + 2 * cc) : 0u;
-        }
-    };
-    load_q(rho_w0, qa0, qa2);
-    load_q(rho_w1 != rho_w0 ? rho_w1 : -1, qb0, qb2);
-    if (lane < nmine) {
-        const FlRow x = fl_row(a, my_rho);
         const RowPlan pl = plan_of_len(a, my_L, my_k == 0 && x.h == 0 && x.sg == 0);
         if (pl.nsc != nsc_full) my_sel = sel_entries(my_rho, x.r, x.h, pl.nsc, my_k);
         my = my_k < pl.n_items ? describe_item_sel(a, pl, x.r, x.h, my_k, my_sel) : ItemDesc{-1, 0, 0};
     }
 
+    const uint64_t pol = l2_evict_first();
     auto issue = [&](int j) {
         if (j >= nmine) {
             cp_async_commit();
@@ -203,8 +205,9 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
                 const int q = lane + 32 * u;
                 const int t = q / LY::CPR, ch = q % LY::CPR;
                 if (t < n) {
-                    cp_async16(st + swizzle_offset(t, ch), kb + (int64_t)t * c.kts * 2 + ch * 16);
-                    cp_async16(st + LY::KBYTES + swizzle_offset(t, ch), vb + (int64_t)t * c.vts * 2 + ch * 16);
+                    cp_async16_policy(st + swizzle_offset(t, ch), kb + (int64_t)t * c.kts * 2 + ch * 16, pol);
+                    cp_async16_policy(st + LY::KBYTES + swizzle_offset(t, ch), vb + (int64_t)t * c.vts * 2 + ch * 16,
+                                      pol);
                 }
             }
         }

@@ -199,6 +199,27 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void *p)
     return r;
 }
 
+// ---------------------------------------------------------------- L2 policy for bulk streams
+
+// The summaries and the K/V a step streams are read once: loads of them
+// carry an L2 evict-first policy so that they do not push out what is read
+// again soon (page tables, lengths, the score rows, the kernels' code).
+__device__ __forceinline__ uint64_t l2_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint4 ldg_stream_v4(const void *p, uint64_t pol)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p), "l"(pol));
+    return r;
+}
+
 // ---------------------------------------------------------------- async copies
 
 // 16-byte cp.async (LSU path) into shared memory; completion by commit
@@ -207,6 +228,13 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void *p)
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// cp_async16 with an L2 cache policy (l2_evict_first for bulk streams).
+__device__ __forceinline__ void cp_async16_policy(uint32_t dst, const void *src, uint64_t pol)
+{
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)
+                 : "memory");
 }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }

@@ -136,13 +136,14 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 2) k_score(ScoreArgs a)
     const int n = j1 - j0;
     const int w0 = (int)((int64_t)n * warp / kScoreWarps), w1 = (int)((int64_t)n * (warp + 1) / kScoreWarps);
     const uint8_t *summ = reinterpret_cast<const uint8_t *>(a.summ);
+    const uint64_t pol = l2_evict_first();
     uint4 v[U][NI];
     auto issue = [&](int i, uint4(&dst)[NI]) {
         const int p = i < w1 ? s_page[i] : -1;
 #pragma unroll
         for (int c = 0; c < NI; ++c) {
             const int ch = lane + 32 * c;
-            dst[c] = (p >= 0 && ch < NCH) ? ldg_nc_v4(summ + (int64_t)p * HKV * DK * 2 + ch * 16)
+            dst[c] = (p >= 0 && ch < NCH) ? ldg_stream_v4(summ + (int64_t)p * HKV * DK * 2 + ch * 16, pol)
                                           : make_uint4(0, 0, 0, 0);
         }
     };

@@ -78,12 +78,71 @@ __device__ __forceinline__ uint32_t tf_block_scan(uint32_t v, uint32_t *red, uin
 }
 
 struct TopkScratch {
+    unsigned long long runs[kTfCand];   // sorted runs of 32 candidate sort keys
     uint32_t red[kTfWarps];
-    uint32_t tmax[kTfThreads];
+    uint32_t tmax[kTfThreads];          // sorted runs of 32 thread maxima
     uint32_t ck[kTfCand];
     int32_t cc[kTfCand];
     uint32_t lo;
 };
+
+// One value per lane, sorted across the warp in descending order (bitonic
+// network: lane 0 ends with the largest).
+__device__ __forceinline__ uint32_t warp_sort_desc(uint32_t v)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const uint32_t o = __shfl_xor_sync(0xffffffffu, v, j);
+            const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+            v = keep_max ? max(v, o) : min(v, o);
+        }
+    }
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long v)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, j);
+            const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+            v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
+        }
+    }
+    return v;
+}
+
+// Entries > x (GE: >= x) in R descending runs of 32 stored one after the
+// other.  Branch-free binary searches advanced in lockstep, so the R loads
+// of a step are independent.
+template <bool GE, int R, class T>
+__device__ __forceinline__ int runs_count(const T *runs, T x)
+{
+    int p[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const T y = runs[32 * r + 31];
+        p[r] = (GE ? y >= x : y > x) ? 32 : 0;
+    }
+#pragma unroll
+    for (int step = 16; step > 0; step >>= 1) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const T y = runs[32 * r + min(p[r] + step - 1, 31)];
+            p[r] += (p[r] < 32 && (GE ? y >= x : y > x)) ? step : 0;
+        }
+    }
+    int t = 0;
+#pragma unroll
+    for (int r = 0; r < R; ++r) t += p[r];
+    return t;
+}
 
 // Selects the top min(k, candidates) columns of the row srow[0, n) (fp32
 // scores; -inf = not a candidate; NaN = not a candidate, flagged) and calls
@@ -134,19 +193,18 @@ __device__ int block_topk(const float *srow, int n, bool row_aligned, int k, uin
     bool done = keff == 0;
     if (keff > 0 && keff < nv) {
         // lower bound: the keff-th largest thread maximum (1 when fewer than
-        // keff threads hold a candidate), found by ranking every thread's
-        // maximum against all the others (ties ranked by thread index)
+        // keff threads hold a candidate).  Each warp sorts its 32 maxima; a
+        // thread's maximum is the keff-th largest when fewer than keff
+        // maxima are above it and at least keff are at or above it, counted
+        // by binary search in the eight sorted runs.
         const int ntv = (int)tf_block_sum(m1 != 0u ? 1u : 0u, sm.red);
-        sm.tmax[tid] = m1;
+        sm.tmax[tid] = warp_sort_desc(m1);
         if (tid == 0) sm.lo = 1u;
         __syncthreads();
         if (keff <= ntv && m1 != 0u) {
-            int rank = 0;
-            for (int u = 0; u < kTfThreads; ++u) {
-                const uint32_t x = sm.tmax[u];
-                rank += (x > m1) | ((x == m1) & (u < tid));
-            }
-            if (rank == keff - 1) sm.lo = m1;
+            const int gt = runs_count<false, kTfWarps>(sm.tmax, m1);
+            const int ge = runs_count<true, kTfWarps>(sm.tmax, m1);
+            if (gt < keff && keff <= ge) sm.lo = m1;   // every thread that writes writes the same value
         }
         __syncthreads();
         const uint32_t lo0 = sm.lo;
@@ -166,17 +224,29 @@ __device__ int block_topk(const float *srow, int n, bool row_aligned, int k, uin
                 }
             }
             __syncthreads();
-            // exact rank of candidates tid and tid + 256 (larger key first,
-            // then lower column); the keff of rank < keff are the selection
+            // exact rank of candidates tid and tid + 256: sort key = (key,
+            // complement of the candidate index), unique and ordered like
+            // (larger key first, then lower column); each warp sorts its
+            // lanes' sort keys and a rank is a sum of binary searches in the
+            // sorted runs.  The keff of rank < keff are the selection.
             const int i0 = tid, i1 = tid + kTfThreads;
-            const uint32_t k0 = i0 < (int)C ? sm.ck[i0] : 0u, k1 = i1 < (int)C ? sm.ck[i1] : 0u;
-            int r0 = 0, r1 = 0;
-            for (int j = 0; j < (int)C; ++j) {
-                const uint32_t x = sm.ck[j];
-                r0 += (x > k0) | ((x == k0) & (j < i0));
-                r1 += (x > k1) | ((x == k1) & (j < i1));
+            const bool two = C > (uint32_t)kTfThreads;   // block-uniform
+            auto skey = [&](int i) -> unsigned long long {
+                return i < (int)C ? ((unsigned long long)sm.ck[i] << 32) | (0xffffffffu - (uint32_t)i) : 0ull;
+            };
+            const unsigned long long s0 = skey(i0), s1 = two ? skey(i1) : 0ull;
+            sm.runs[tid] = warp_sort_desc(s0);
+            if (two) sm.runs[kTfThreads + tid] = warp_sort_desc(s1);
+            __syncthreads();
+            int r0, r1 = 0;
+            if (two) {
+                r0 = runs_count<false, kTfCand / 32>(sm.runs, s0);
+                r1 = runs_count<false, kTfCand / 32>(sm.runs, s1);
+            } else {
+                r0 = runs_count<false, kTfThreads / 32>(sm.runs, s0);
             }
-            const uint32_t f0 = (i0 < (int)C && r0 < keff) ? 1u : 0u, f1 = (i1 < (int)C && r1 < keff) ? 1u : 0u;
+            const uint32_t f0 = (i0 < (int)C && r0 < keff) ? 1u : 0u;
+            const uint32_t f1 = (two && i1 < (int)C && r1 < keff) ? 1u : 0u;
             uint32_t tot = 0;
             const uint32_t ex = tf_block_scan(f0 | (f1 << 16), sm.red, &tot);
             if (f0) out((int)(ex & 0xffffu), sm.cc[i0]);
