@@ -8,12 +8,13 @@
 // lo0 is the k-th largest thread maximum, at least k threads hold a key
 // >= lo0, so at least k keys are >= lo0, and on typical rows only a little
 // more than k are.  Those keys are compacted in column order into shared
-// memory (one block scan); every thread then ranks one or two of them
-// against all (larger key first, then lower column), the k of rank < k are
-// the selection and a second scan gives their ascending output positions.
-// Rows where the bound leaves more than kTfCand keys (heavy ties) take a
-// block-wide bisection over all keys instead.  Either way the result is the
-// same exact, bit-reproducible selection.
+// memory (one block scan) and each is ranked against all of them (larger
+// key first, then lower column): by a linear count over broadcast reads
+// when there are few, else through warp-sorted runs and binary searches.
+// The k of rank < k are the selection and a second scan gives their
+// ascending output positions.  Rows where the bound leaves more than
+// kTfCand keys (heavy ties) take a block-wide bisection over all keys
+// instead.  Every way gives the same exact, bit-reproducible selection.
 #pragma once
 
 #include "lsa_device.cuh"
@@ -23,7 +24,8 @@ namespace {
 
 constexpr int kTfThreads = 256;
 constexpr int kTfWarps = kTfThreads / 32;
-constexpr int kTfCand = 512;   // candidates the final warp takes (16 per lane)
+constexpr int kTfCand = 512;     // candidates ranked through sorted runs at most
+constexpr int kTfLinear = 128;   // candidates ranked by a linear count at most
 
 // Block-wide sum / max of one value per thread; every thread gets the
 // result.  `red` holds kTfWarps words; two barriers.
@@ -81,7 +83,7 @@ struct TopkScratch {
     unsigned long long runs[kTfCand];   // sorted runs of 32 candidate sort keys
     uint32_t red[kTfWarps];
     uint32_t tmax[kTfThreads];          // sorted runs of 32 thread maxima
-    uint32_t ck[kTfCand];
+    alignas(16) uint32_t ck[kTfCand + 4];   // + 4: zero padding for 16-byte reads
     int32_t cc[kTfCand];
     uint32_t lo;
 };
@@ -144,6 +146,41 @@ __device__ __forceinline__ int runs_count(const T *runs, T x)
     return t;
 }
 
+// Entries > x and entries >= x in R descending runs of 32 stored one after
+// the other: both binary searches of every run advanced in lockstep.
+template <int R>
+__device__ __forceinline__ void runs_count_gt_ge(const uint32_t *runs, uint32_t x, int &gt, int &ge)
+{
+    int pg[R], pe[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uint32_t y = runs[32 * r + 31];
+        pg[r] = y > x ? 32 : 0;
+        pe[r] = y >= x ? 32 : 0;
+    }
+#pragma unroll
+    for (int step = 16; step > 0; step >>= 1) {
+        uint32_t yg[R], ye[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            yg[r] = runs[32 * r + min(pg[r] + step - 1, 31)];
+            ye[r] = runs[32 * r + min(pe[r] + step - 1, 31)];
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            pg[r] += (pg[r] < 32 && yg[r] > x) ? step : 0;
+            pe[r] += (pe[r] < 32 && ye[r] >= x) ? step : 0;
+        }
+    }
+    gt = 0;
+    ge = 0;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        gt += pg[r];
+        ge += pe[r];
+    }
+}
+
 // Selects the top min(k, candidates) columns of the row srow[0, n) (fp32
 // scores; -inf = not a candidate; NaN = not a candidate, flagged) and calls
 // out(position, column) for each; returns how many.  Every thread of the
@@ -184,8 +221,9 @@ __device__ int block_topk(const float *srow, int n, bool row_aligned, int k, uin
         m1 = max(m1, keys[e]);
     }
     if (nan) flag_error(status, LSA_ERR_NAN);
-    const int nv = (int)tf_block_sum(nvt, sm.red);
-    const uint32_t kmax = tf_block_max(m1, sm.red);
+    // candidate keys (low half) and threads holding one (high half)
+    const uint32_t both = tf_block_sum(nvt | (m1 != 0u ? 0x10000u : 0u), sm.red);
+    const int nv = (int)(both & 0xffffu), ntv = (int)(both >> 16);
     const int keff = min(k, nv);
 
     uint32_t thresh = 0;   // selection: keys > thresh, then the first take_eq keys == thresh
@@ -197,13 +235,12 @@ __device__ int block_topk(const float *srow, int n, bool row_aligned, int k, uin
         // thread's maximum is the keff-th largest when fewer than keff
         // maxima are above it and at least keff are at or above it, counted
         // by binary search in the eight sorted runs.
-        const int ntv = (int)tf_block_sum(m1 != 0u ? 1u : 0u, sm.red);
         sm.tmax[tid] = warp_sort_desc(m1);
         if (tid == 0) sm.lo = 1u;
         __syncthreads();
         if (keff <= ntv && m1 != 0u) {
-            const int gt = runs_count<false, kTfWarps>(sm.tmax, m1);
-            const int ge = runs_count<true, kTfWarps>(sm.tmax, m1);
+            int gt, ge;
+            runs_count_gt_ge<kTfWarps>(sm.tmax, m1, gt, ge);
             if (gt < keff && keff <= ge) sm.lo = m1;   // every thread that writes writes the same value
         }
         __syncthreads();
@@ -213,7 +250,42 @@ __device__ int block_topk(const float *srow, int n, bool row_aligned, int k, uin
         for (int e = 0; e < KPT; ++e) cnt += keys[e] >= lo0;
         uint32_t C = 0;
         uint32_t pos = tf_block_scan(cnt, sm.red, &C);
-        if (C <= (uint32_t)kTfCand) {
+        if (C <= (uint32_t)kTfLinear) {
+            // the candidates, in column order, to shared memory; candidate
+            // tid's rank (larger key first, then lower column) is counted
+            // against all of them with broadcast 16-byte reads
+#pragma unroll
+            for (int e = 0; e < KPT; ++e) {
+                if (keys[e] >= lo0) {
+                    sm.ck[pos] = keys[e];
+                    sm.cc[pos] = c0 + e;
+                    ++pos;
+                }
+            }
+            if (tid < 4) sm.ck[C + tid] = 0u;   // never above a candidate, never equal to one
+            __syncthreads();
+            uint32_t f = 0;
+            if (tid < (int)C) {
+                const uint32_t mine = sm.ck[tid];
+                const uint4 *ck4 = reinterpret_cast<const uint4 *>(sm.ck);
+                uint32_t rank = 0;
+                const int n4 = ((int)C + 3) >> 2;
+#pragma unroll 4
+                for (int j4 = 0; j4 < n4; ++j4) {
+                    const uint4 y = ck4[j4];
+                    const int j = 4 * j4;
+                    rank += (y.x > mine) | ((y.x == mine) & (j < tid));
+                    rank += (y.y > mine) | ((y.y == mine) & (j + 1 < tid));
+                    rank += (y.z > mine) | ((y.z == mine) & (j + 2 < tid));
+                    rank += (y.w > mine) | ((y.w == mine) & (j + 3 < tid));
+                }
+                f = rank < (uint32_t)keff ? 1u : 0u;
+            }
+            uint32_t tot = 0;
+            const uint32_t ex = tf_block_scan(f, sm.red, &tot);
+            if (f) out((int)ex, sm.cc[tid]);
+            done = true;
+        } else if (C <= (uint32_t)kTfCand) {
             // the candidates, in column order, to shared memory
 #pragma unroll
             for (int e = 0; e < KPT; ++e) {
@@ -254,6 +326,7 @@ __device__ int block_topk(const float *srow, int n, bool row_aligned, int k, uin
             done = true;
         } else {
             // heavy ties: bisection over all keys of the row
+            const uint32_t kmax = tf_block_max(m1, sm.red);
             uint64_t lo = lo0, hi = (uint64_t)kmax + 1;
             while (hi - lo > 1) {
                 const uint32_t mid = (uint32_t)(lo + ((hi - lo) >> 1));
