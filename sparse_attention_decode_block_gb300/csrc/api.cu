@@ -191,7 +191,12 @@ lsa_status plan_attention(const CacheView &v, const lsa_params *p, bool token_mo
             nc = std::max<int64_t>(slots, (T + per_cta - 1) / per_cta);
         }
         nc = std::min<int64_t>(nc, T);
-        if (nc > 0x7fffffff) return LSA_ERR_UNSUPPORTED;
+        // the kernel's index arithmetic is 32-bit; larger batches take the
+        // split-K plan above
+        if ((T + 1) * nc >= (int64_t(1) << 32)) {
+            pl->flat = false;
+            return LSA_OK;
+        }
         pl->fl_ns = items;
         pl->fl_total = T;
         pl->fl_ctas = (int)nc;

@@ -68,10 +68,10 @@ __device__ __forceinline__ FlRow fl_row(const AttnArgs &a, int rho)
     return x;
 }
 
-// First CTA whose piece holds item i.
-__device__ __forceinline__ int fl_cta_of(const AttnArgs &a, int64_t i)
+// First CTA whose piece holds item i (i * fl_ctas < 2^32: host-checked).
+__device__ __forceinline__ int fl_cta_of(const AttnArgs &a, uint32_t i)
 {
-    return (int)(i * a.fl_ctas / a.fl_total);
+    return (int)(i * (uint32_t)a.fl_ctas / (uint32_t)a.fl_total);
 }
 
 // KSEL > 0: the CTA selects its rows' blocks itself from the score rows
@@ -95,15 +95,27 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
         if (threadIdx.x == 0) flag_error(a.status, LSA_ERR_INVALID_ARG);
         return;
     }
-    const int NS = a.fl_ns;
-    const int64_t T = a.fl_total;
-    const int cta = blockIdx.x;
-    const int64_t cs = ((int64_t)cta * T + a.fl_ctas - 1) / a.fl_ctas;         // this CTA's items [cs, ce)
-    const int64_t ce = ((int64_t)(cta + 1) * T + a.fl_ctas - 1) / a.fl_ctas;
-    const int64_t cn = ce - cs;
-    const int64_t ws = cs + cn * warp / kFlWarps, we = cs + cn * (warp + 1) / kFlWarps;
+    // index arithmetic in 32 bits: the host keeps (T + 1) * fl_ctas < 2^32
+    const uint32_t NS = (uint32_t)a.fl_ns, NC = (uint32_t)a.fl_ctas;
+    const uint32_t T = (uint32_t)a.fl_total;
+    const uint32_t cta = blockIdx.x;
+    const uint32_t cs = (cta * T + NC - 1) / NC;   // this CTA's items [cs, ce)
+    const uint32_t ce = ((cta + 1) * T + NC - 1) / NC;
+    const uint32_t cn = ce - cs;
+    const uint32_t ws = cs + cn * warp / kFlWarps, we = cs + cn * (warp + 1) / kFlWarps;
     const int nmine = min((int)(we - ws), kFlMaxItemsPerWarp);   // the host keeps pieces within this
     const int rho_first = (int)(cs / NS);
+    const int rh_first = rho_first / a.nsub;
+    const int rh_last = cn > 0 ? (int)((ce - 1) / NS) / a.nsub : rh_first - 1;   // none when empty
+    // the first row's scores, when this kernel selects: loaded before
+    // anything else so that their latency hides behind the set-up below
+    constexpr int KV = KSEL > 0 ? KSEL : 4;
+    float sel_v[KV];
+    const bool sel_aligned = (a.sel_cols & 3) == 0 && (reinterpret_cast<uintptr_t>(a.sel_scores) & 15) == 0;
+    if constexpr (KSEL > 0) {
+        if (rh_first <= rh_last)
+            block_topk_load<KSEL>(a.sel_scores + (int64_t)rh_first * a.sel_cols, a.sel_cols, sel_aligned, sel_v);
+    }
 
     uint8_t *ring = smem + warp * LY::WARP_RING;
     const uint32_t ring_s = smem_addr(ring);
@@ -121,9 +133,9 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
     int2 my_sel = make_int2(-1, -1);
     const int nsc_full = (a.sink + kChunk - 1) / kChunk;
     if (lane < nmine) {
-        const int64_t i = ws + lane;
+        const uint32_t i = ws + lane;
         my_rho = (int)(i / NS);
-        my_k = (int)(i % NS);
+        my_k = (int)(i - (uint32_t)my_rho * NS);
         my_L = a.lens[fl_row(a, my_rho).r];
     }
     const int rho_w0 = nmine > 0 ? (int)(ws / NS) : -1;
@@ -146,19 +158,16 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
     // most two), when this kernel makes it: exact top-k of each score row,
     // written out by the CTA that holds the row's first item
     int32_t *s_sel = reinterpret_cast<int32_t *>(smem + LY::SELS);   // [2][kFlMaxSel]
-    const int rh_first = rho_first / a.nsub;
     if constexpr (KSEL > 0) {
         TopkScratch &sm = *reinterpret_cast<TopkScratch *>(smem + LY::SELBUF);
-        const int rh_last = (int)((ce - 1) / NS) / a.nsub;
-        const bool aligned = (a.sel_cols & 3) == 0 && (reinterpret_cast<uintptr_t>(a.sel_scores) & 15) == 0;
         for (int s = 0; s < 2 && rh_first + s <= rh_last; ++s) {
             const int rh = rh_first + s;
             int32_t *dst = s_sel + s * kFlMaxSel;
-            const int keff = block_topk<KSEL>(a.sel_scores + (int64_t)rh * a.sel_cols, a.sel_cols, aligned, a.nsel,
-                                              a.status, sm, [&](int pos, int col) { dst[pos] = col; });
+            if (s > 0) block_topk_load<KSEL>(a.sel_scores + (int64_t)rh * a.sel_cols, a.sel_cols, sel_aligned, sel_v);
+            const int keff = block_topk_scores<KSEL>(sel_v, a.nsel, a.status, sm, [&](int pos, int col) { dst[pos] = col; });
             for (int i = keff + (int)threadIdx.x; i < a.nsel; i += blockDim.x) dst[i] = -1;
             __syncthreads();
-            if (a.sel_write && fl_cta_of(a, (int64_t)rh * a.nsub * NS) == cta)
+            if (a.sel_write && fl_cta_of(a, (uint32_t)rh * a.nsub * NS) == (int)cta)
                 for (int i = threadIdx.x; i < a.nsel; i += blockDim.x) a.sel_write[(int64_t)rh * a.nsel + i] = dst[i];
         }
     }
@@ -358,8 +367,8 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
     for (int s = 0; s < kFlMaxRowsPerCta && rho_first + s <= rho_last; ++s) {
         const int rho = rho_first + s;
         const FlRow x = fl_row(a, rho);
-        const int fc = fl_cta_of(a, (int64_t)rho * NS);
-        const int lc = fl_cta_of(a, (int64_t)(rho + 1) * NS - 1);
+        const int fc = fl_cta_of(a, (uint32_t)rho * NS);
+        const int lc = fl_cta_of(a, (uint32_t)(rho + 1) * NS - 1);
         const int parts = lc - fc + 1;
         for (int t = threadIdx.x; t < G * DK / 4; t += blockDim.x) {
             const int g = t / (DK / 4), d = (t % (DK / 4)) * 4;

@@ -63,8 +63,11 @@ __device__ ItemDesc describe_item(const AttnArgs &a, const RowPlan &pl, int r, i
 }
 
 // As describe_item, with the item's selection entries (item_sel_entries
-// under this plan) already loaded.
-__device__ ItemDesc describe_item_sel(const AttnArgs &a, const RowPlan &pl, int r, int h, int i, int2 sel)
+// under this plan) already loaded and the page id of block j of request r
+// read by page_of(r, j).
+template <class PageOf>
+__device__ __forceinline__ ItemDesc describe_item_with(const AttnArgs &a, const RowPlan &pl, int r, int h, int i,
+                                                       int2 sel, PageOf page_of)
 {
     const int b = a.c.b;
     ItemDesc d;
@@ -98,7 +101,7 @@ __device__ ItemDesc describe_item_sel(const AttnArgs &a, const RowPlan &pl, int 
         n = min(pl.L, blk16 * kChunk + kChunk) - t0;
     }
     if (n <= 0) return d;
-    const int p = a.pt[(int64_t)r * a.max_blocks + t0 / b];
+    const int p = page_of(r, t0 / b);
     if (p < 0 || p >= a.c.num_pages) {
         flag_error(a.status, LSA_ERR_BOUNDS);
         return d;
@@ -107,6 +110,12 @@ __device__ ItemDesc describe_item_sel(const AttnArgs &a, const RowPlan &pl, int 
     d.ts = (int16_t)(t0 % b);
     d.n = (int16_t)n;
     return d;
+}
+
+__device__ ItemDesc describe_item_sel(const AttnArgs &a, const RowPlan &pl, int r, int h, int i, int2 sel)
+{
+    return describe_item_with(a, pl, r, h, i, sel,
+                              [&](int rq, int j) { return a.pt[(int64_t)rq * a.max_blocks + j]; });
 }
 
 // Token-list rows: entry u of token-list item i -> (page, slot) or page -1.

@@ -89,7 +89,9 @@ struct AttnArgs {
     int32_t splits, items_per_split, nsub;
     // even split of all rows' item slots over fl_ctas CTAs (attention_flat.cu):
     // fl_ns item slots per row, fl_total = rows * fl_ns, at most fl_parts
-    // CTAs per row; row_done: one counter per row, zero between calls
+    // CTAs per row; row_done: one counter per row, zero between calls.
+    // The host keeps (fl_total + 1) * fl_ctas below 2^32, so the split's
+    // index arithmetic fits 32 bits.
     int32_t fl_ns, fl_ctas, fl_parts;
     int64_t fl_total;
     uint32_t *row_done;

@@ -26,6 +26,7 @@ constexpr int kTfThreads = 256;
 constexpr int kTfWarps = kTfThreads / 32;
 constexpr int kTfCand = 512;     // candidates ranked through sorted runs at most
 constexpr int kTfLinear = 128;   // candidates ranked by a linear count at most
+constexpr int kTfTreeK = 64;     // k up to which the bound comes from the top-64 tree
 
 // Block-wide sum / max of one value per thread; every thread gets the
 // result.  `red` holds kTfWarps words; two barriers.
@@ -87,6 +88,7 @@ struct TopkScratch {
     int32_t cc[kTfCand];
     uint32_t lo;
 };
+static_assert(sizeof(((TopkScratch *)nullptr)->runs) >= 512 * 4, "the top-64 tree reuses the runs");
 
 // One value per lane, sorted across the warp in descending order (bitonic
 // network: lane 0 ends with the largest).
@@ -118,6 +120,64 @@ __device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long 
         }
     }
     return v;
+}
+
+// Sorts the 64-entry bitonic sequence (lane i holds entries i and 32 + i)
+// in descending order: hi = entry i, lo = entry 32 + i afterwards.
+__device__ __forceinline__ void warp_bitonic_merge64_desc(uint32_t &hi, uint32_t &lo)
+{
+    const int lane = threadIdx.x & 31;
+    const uint32_t a = max(hi, lo), b = min(hi, lo);
+    hi = a;
+    lo = b;
+#pragma unroll
+    for (int j = 16; j > 0; j >>= 1) {
+        const uint32_t oh = __shfl_xor_sync(0xffffffffu, hi, j);
+        const uint32_t ol = __shfl_xor_sync(0xffffffffu, lo, j);
+        const bool keep_max = (lane & j) == 0;
+        hi = keep_max ? max(hi, oh) : min(hi, oh);
+        lo = keep_max ? max(lo, ol) : min(lo, ol);
+    }
+}
+
+// The k-th largest (1 <= k <= 64) of the block's 256 values v, one per
+// thread; every thread gets it.  Each warp sorts its 32 values; sorted runs
+// are then merged pairwise keeping the 64 largest (the largest 64 of two
+// descending runs A, B are the bitonic sequence max(A[i], B[63 - i])).
+// tree: 384 words of scratch.
+__device__ __forceinline__ uint32_t block_kth_largest64(uint32_t v, int k, uint32_t *tree, uint32_t *out)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t *l0 = tree;          // 8 runs of 32, then (aliased) 2 runs of 64
+    uint32_t *l1 = tree + 256;    // 4 runs of 64 -> first half of the buffer reused
+    l0[warp * 32 + lane] = warp_sort_desc(v);
+    __syncthreads();
+    if (warp < 4) {   // runs 2w and 2w + 1 -> sorted 64
+        uint32_t hi = l0[(2 * warp) * 32 + lane];
+        uint32_t lo = l0[(2 * warp + 1) * 32 + 31 - lane];
+        warp_bitonic_merge64_desc(hi, lo);
+        l1[warp * 64 + lane] = hi;   // l1 spans tree[256, 512): 4 x 64 = 256 words
+        l1[warp * 64 + 32 + lane] = lo;
+    }
+    __syncthreads();
+    if (warp < 2) {   // sorted 64s 2w and 2w + 1 -> their top 64, sorted
+        const uint32_t *A = l1 + (2 * warp) * 64, *B = l1 + (2 * warp + 1) * 64;
+        uint32_t hi = max(A[lane], B[63 - lane]);
+        uint32_t lo = max(A[32 + lane], B[31 - lane]);
+        warp_bitonic_merge64_desc(hi, lo);
+        l0[warp * 64 + lane] = hi;
+        l0[warp * 64 + 32 + lane] = lo;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t *A = l0, *B = l0 + 64;
+        uint32_t hi = max(A[lane], B[63 - lane]);
+        uint32_t lo = max(A[32 + lane], B[31 - lane]);
+        warp_bitonic_merge64_desc(hi, lo);
+        if (lane == ((k - 1) & 31)) *out = k <= 32 ? hi : lo;
+    }
+    __syncthreads();
+    return *out;
 }
 
 // Entries > x (GE: >= x) in R descending runs of 32 stored one after the
@@ -186,16 +246,14 @@ __device__ __forceinline__ void runs_count_gt_ge(const uint32_t *runs, uint32_t 
 // out(position, column) for each; returns how many.  Every thread of the
 // block (kTfThreads) must call it; KPT * kTfThreads >= n.  row_aligned: srow
 // is 16-byte aligned (16-byte loads).
-template <int KPT, class Out>
-__device__ int block_topk(const float *srow, int n, bool row_aligned, int k, uint32_t *status, TopkScratch &sm,
-                          Out out)
+// This thread's scores of the row srow[0, n) for block_topk_scores: columns
+// [t*KPT, (t+1)*KPT), -inf past n (16-byte loads when the row is 16-byte
+// aligned).
+template <int KPT>
+__device__ __forceinline__ void block_topk_load(const float *srow, int n, bool row_aligned, float (&v)[KPT])
 {
     static_assert(KPT % 4 == 0, "keys per thread come in fours");
-    const int tid = threadIdx.x;
-    const int c0 = tid * KPT;
-
-    // keys (all loads first; 16-byte loads when the row is 16-byte aligned)
-    float v[KPT];
+    const int c0 = threadIdx.x * KPT;
     const bool vec = row_aligned && c0 + KPT <= n;
     if (vec) {
 #pragma unroll
@@ -210,6 +268,26 @@ __device__ int block_topk(const float *srow, int n, bool row_aligned, int k, uin
 #pragma unroll
         for (int e = 0; e < KPT; ++e) v[e] = c0 + e < n ? srow[c0 + e] : -INFINITY;
     }
+}
+
+template <int KPT, class Out>
+__device__ int block_topk_scores(const float (&v)[KPT], int k, uint32_t *status, TopkScratch &sm, Out out);
+
+template <int KPT, class Out>
+__device__ int block_topk(const float *srow, int n, bool row_aligned, int k, uint32_t *status, TopkScratch &sm,
+                          Out out)
+{
+    float v[KPT];
+    block_topk_load<KPT>(srow, n, row_aligned, v);
+    return block_topk_scores<KPT>(v, k, status, sm, out);
+}
+
+// block_topk on scores already loaded by block_topk_load.
+template <int KPT, class Out>
+__device__ int block_topk_scores(const float (&v)[KPT], int k, uint32_t *status, TopkScratch &sm, Out out)
+{
+    const int tid = threadIdx.x;
+    const int c0 = tid * KPT;
     uint32_t keys[KPT];
     bool nan = false;
     uint32_t nvt = 0, m1 = 0;
@@ -221,6 +299,57 @@ __device__ int block_topk(const float *srow, int n, bool row_aligned, int k, uin
         m1 = max(m1, keys[e]);
     }
     if (nan) flag_error(status, LSA_ERR_NAN);
+    if (k > 0 && k <= kTfTreeK) {
+        // lo0: the k-th largest thread maximum (1 when fewer than k threads
+        // hold a candidate: then every candidate is taken).  The C keys >=
+        // lo0 hold the selection; when C is small each is ranked by P
+        // threads (larger key first, then lower column), each counting over
+        // a P-th of the candidates with broadcast 16-byte reads.
+        const uint32_t lo0 = max(block_kth_largest64(m1, k, reinterpret_cast<uint32_t *>(sm.runs), &sm.lo), 1u);
+        uint32_t cnt = 0;
+#pragma unroll
+        for (int e = 0; e < KPT; ++e) cnt += keys[e] >= lo0;
+        uint32_t C = 0;
+        uint32_t pos = tf_block_scan(cnt, sm.red, &C);
+        if (C <= (uint32_t)kTfLinear) {
+#pragma unroll
+            for (int e = 0; e < KPT; ++e) {
+                if (keys[e] >= lo0) {
+                    sm.ck[pos] = keys[e];
+                    sm.cc[pos] = c0 + e;
+                    ++pos;
+                }
+            }
+            if (tid < 4) sm.ck[C + tid] = 0u;   // never above a candidate, never equal to one
+            __syncthreads();
+            const int lp = C <= (uint32_t)(kTfThreads / 4) ? 2 : 1;   // log2 P
+            const int i = tid >> lp, q = tid & ((1 << lp) - 1);
+            uint32_t rank = 0;
+            if (i < (int)C) {
+                const uint32_t mine = sm.ck[i];
+                const uint4 *ck4 = reinterpret_cast<const uint4 *>(sm.ck);
+                const int n4 = ((int)C + 3) >> 2;
+                const int per = (n4 + (1 << lp) - 1) >> lp;
+                const int j4e = min(n4, (q + 1) * per);
+#pragma unroll 4
+                for (int j4 = q * per; j4 < j4e; ++j4) {
+                    const uint4 y = ck4[j4];
+                    const int j = 4 * j4;
+                    rank += (y.x > mine) | ((y.x == mine) & (j < i));
+                    rank += (y.y > mine) | ((y.y == mine) & (j + 1 < i));
+                    rank += (y.z > mine) | ((y.z == mine) & (j + 2 < i));
+                    rank += (y.w > mine) | ((y.w == mine) & (j + 3 < i));
+                }
+            }
+            rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+            if (lp == 2) rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+            const uint32_t f = (i < (int)C && q == 0 && rank < (uint32_t)k) ? 1u : 0u;
+            uint32_t tot = 0;
+            const uint32_t ex = tf_block_scan(f, sm.red, &tot);
+            if (f) out((int)ex, sm.cc[i]);
+            return min(k, (int)C);
+        }
+    }
     // candidate keys (low half) and threads holding one (high half)
     const uint32_t both = tf_block_sum(nvt | (m1 != 0u ? 0x10000u : 0u), sm.red);
     const int nv = (int)(both & 0xffffu), ntv = (int)(both >> 16);
