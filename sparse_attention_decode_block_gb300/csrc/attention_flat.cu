@@ -79,7 +79,9 @@ __device__ __forceinline__ int fl_cta_of(const AttnArgs &a, uint32_t i)
 template <int DK, int G, int KSEL>
 __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
 {
-    pdl_enter();
+    const bool early = a.pdl_early != 0;
+    if (!early) pdl_wait();
+    pdl_launch_dependents();
     using LY = FlLayout<DK, G>;
     static_assert(KSEL == 0 || kFlWarps * 32 == kTfThreads, "one CTA is one top-k block");
     constexpr int NT = DK / 8;
@@ -107,15 +109,6 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
     const int rho_first = (int)(cs / NS);
     const int rh_first = rho_first / a.nsub;
     const int rh_last = cn > 0 ? (int)((ce - 1) / NS) / a.nsub : rh_first - 1;   // none when empty
-    // the first row's scores, when this kernel selects: loaded before
-    // anything else so that their latency hides behind the set-up below
-    constexpr int KV = KSEL > 0 ? KSEL : 4;
-    float sel_v[KV];
-    const bool sel_aligned = (a.sel_cols & 3) == 0 && (reinterpret_cast<uintptr_t>(a.sel_scores) & 15) == 0;
-    if constexpr (KSEL > 0) {
-        if (rh_first <= rh_last)
-            block_topk_load<KSEL>(a.sel_scores + (int64_t)rh_first * a.sel_cols, a.sel_cols, sel_aligned, sel_v);
-    }
 
     uint8_t *ring = smem + warp * LY::WARP_RING;
     const uint32_t ring_s = smem_addr(ring);
@@ -153,6 +146,17 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
     };
     load_q(rho_w0, qa0, qa2);
     load_q(rho_w1 != rho_w0 ? rho_w1 : -1, qb0, qb2);
+
+    // (early launch) the score rows come from the kernel before: wait for
+    // it here, then load the first row's scores
+    if (early) pdl_wait();
+    constexpr int KV = KSEL > 0 ? KSEL : 4;
+    float sel_v[KV];
+    const bool sel_aligned = (a.sel_cols & 3) == 0 && (reinterpret_cast<uintptr_t>(a.sel_scores) & 15) == 0;
+    if constexpr (KSEL > 0) {
+        if (rh_first <= rh_last)
+            block_topk_load<KSEL>(a.sel_scores + (int64_t)rh_first * a.sel_cols, a.sel_cols, sel_aligned, sel_v);
+    }
 
     // ---- the selection of the (request, KV head) rows of this piece (at
     // most two), when this kernel makes it: exact top-k of each score row,
@@ -459,7 +463,8 @@ cudaError_t launch_flat_t(const AttnArgs &a, cudaStream_t s)
     auto kern = k_attn_flat<DK, G, KSEL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM);
     if (e != cudaSuccess) return e;
-    e = launch_step_kernel(kern, dim3(a.fl_ctas), dim3(kFlWarps * 32), LY::SMEM, s, a);
+    e = launch_kernel_ex(a.pdl_early != 0 || pdl_enabled(), kern, dim3(a.fl_ctas), dim3(kFlWarps * 32), LY::SMEM, s,
+                         a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

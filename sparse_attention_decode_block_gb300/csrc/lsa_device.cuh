@@ -31,10 +31,17 @@ __device__ __forceinline__ void flag_error(uint32_t *status, int code)
 // visibility of its writes) before it reads anything.  The overlap hides the
 // launch latency between the kernels of a step; the order of their memory
 // effects is unchanged.  Outside such a launch the wait returns at once.
-__device__ __forceinline__ void pdl_enter()
+// The wait comes first: a kernel's dependents then launch only once
+// everything before that kernel in the stream has completed.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents()
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_enter()
+{
+    pdl_wait();
+    pdl_launch_dependents();
 }
 
 // Off unless LSA_PDL=1: measured on the B=16 x 32K step it saved nothing
@@ -49,9 +56,10 @@ inline bool pdl_enabled()
     return on;
 }
 
+// dependent: launch with programmatic stream serialization.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_step_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                               Args &&...args)
+cudaError_t launch_kernel_ex(bool dependent, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args &&...args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -62,8 +70,15 @@ cudaError_t launch_step_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, si
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cfg.numAttrs = dependent ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_step_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                               Args &&...args)
+{
+    return launch_kernel_ex(pdl_enabled(), kern, grid, block, smem, s, static_cast<Args &&>(args)...);
 }
 
 // ---------------------------------------------------------------- smem / mbarrier

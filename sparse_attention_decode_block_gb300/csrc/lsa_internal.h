@@ -100,6 +100,12 @@ struct AttnArgs {
     // selection out [B*hkv, nsel], or NULL
     const float *sel_scores;
     int32_t sel_cols;
+    // pdl_early: launched right after the score kernel of the same step on
+    // the same stream, as a programmatic dependent.  Everything before that
+    // score kernel had completed when it let this kernel launch, so q,
+    // lens and the page table are final and the kernel reads them (and
+    // sets up) before it waits for the score rows.
+    int32_t pdl_early;
     int32_t *sel_write;
     float *o_part;              // [B*Hq, splits or fl_parts, dv]
     float *lse_part;            // [B*Hq, splits or fl_parts]   log2 domain
