@@ -191,9 +191,9 @@ lsa_status plan_attention(const CacheView &v, const lsa_params *p, bool token_mo
             nc = std::max<int64_t>(slots, (T + per_cta - 1) / per_cta);
         }
         nc = std::min<int64_t>(nc, T);
-        // the kernel's index arithmetic is 32-bit; larger batches take the
-        // split-K plan above
-        if ((T + 1) * nc >= (int64_t(1) << 32)) {
+        // the kernel's index arithmetic is 32-bit (below 2^31: fdiv); larger
+        // batches take the split-K plan above
+        if ((T + 1) * nc >= (int64_t(1) << 31)) {
             pl->flat = false;
             return LSA_OK;
         }
@@ -236,9 +236,14 @@ lsa_status run_attention(const void *q, const CacheView &v, const int32_t *pt, c
     a.sink = p->sink_tokens;
     a.recent = p->recent_tokens;
     a.scale_log2 = scale_of(p, v.dk) * 1.4426950408889634f;
+    a.fd_b = make_fastdiv((uint32_t)v.b);
+    a.fd_cpb = make_fastdiv((uint32_t)(v.b / kChunk));
+    a.fd_hkv = make_fastdiv((uint32_t)v.hkv);
+    a.gsize = p->num_q_heads / v.hkv;
     a.splits = pl.splits;
     a.items_per_split = pl.items_per_split;
     a.nsub = pl.nsub;
+    a.fd_nsub = make_fastdiv((uint32_t)pl.nsub);
     a.out = static_cast<uint16_t *>(out);
     a.lse = lse;
     a.status = status_word();
@@ -253,6 +258,9 @@ lsa_status run_attention(const void *q, const CacheView &v, const int32_t *pt, c
         a.fl_total = pl.fl_total;
         a.fl_ctas = pl.fl_ctas;
         a.fl_parts = pl.fl_parts;
+        a.fd_ns = make_fastdiv((uint32_t)pl.fl_ns);
+        a.fd_nc = make_fastdiv((uint32_t)pl.fl_ctas);
+        a.fd_total = make_fastdiv((uint32_t)pl.fl_total);
         const size_t rowsq = (size_t)p->batch * p->num_q_heads * pl.fl_parts;
         a.o_part = reinterpret_cast<float *>(ws);
         a.lse_part = reinterpret_cast<float *>(ws + round_up(rowsq * v.dv * sizeof(float)));

@@ -50,7 +50,8 @@ struct FlLayout {
     static constexpr int SELBUF = LAST + 16;                          // top-k scratch, then [2][kFlMaxSel] selection
     static constexpr int SELS = SELBUF + ((int)sizeof(TopkScratch) + 15) / 16 * 16;
     static constexpr int SMEM = SELS + 2 * kFlMaxSel * 4;
-    static_assert(RINGS >= kFlMaxRowsPerCta * kFlWarps * G * (DK + 2) * 4, "the CTA merge reuses the rings");
+    static_assert(RINGS >= kFlMaxRowsPerCta * (kFlWarps * G * (DK + 2) + G * (kFlWarps + 1)) * 4,
+                  "the CTA merge reuses the rings");
     static_assert(SMEM * kFlCtasPerSm <= 227 * 1024, "the CTAs of one SM");
 };
 
@@ -62,16 +63,17 @@ struct FlRow {
 __device__ __forceinline__ FlRow fl_row(const AttnArgs &a, int rho)
 {
     FlRow x;
-    x.sg = rho % a.nsub;
-    x.h = (rho / a.nsub) % a.c.hkv;
-    x.r = rho / (a.nsub * a.c.hkv);
+    const uint32_t rh = fdiv((uint32_t)rho, a.fd_nsub);
+    x.sg = rho - (int)(rh * a.fd_nsub.d);
+    x.r = (int)fdiv(rh, a.fd_hkv);
+    x.h = (int)rh - x.r * (int)a.fd_hkv.d;
     return x;
 }
 
 // First CTA whose piece holds item i (i * fl_ctas < 2^32: host-checked).
 __device__ __forceinline__ int fl_cta_of(const AttnArgs &a, uint32_t i)
 {
-    return (int)(i * (uint32_t)a.fl_ctas / (uint32_t)a.fl_total);
+    return (int)fdiv(i * (uint32_t)a.fl_ctas, a.fd_total);
 }
 
 // KSEL > 0: the CTA selects its rows' blocks itself from the score rows
@@ -91,7 +93,7 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
 
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int Gt = a.hq / a.c.hkv;
+    const int Gt = a.gsize;
     const CacheView &c = a.c;
     if ((smem_addr(smem) & 1023u) != 0) {
         if (threadIdx.x == 0) flag_error(a.status, LSA_ERR_INVALID_ARG);
@@ -101,14 +103,14 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
     const uint32_t NS = (uint32_t)a.fl_ns, NC = (uint32_t)a.fl_ctas;
     const uint32_t T = (uint32_t)a.fl_total;
     const uint32_t cta = blockIdx.x;
-    const uint32_t cs = (cta * T + NC - 1) / NC;   // this CTA's items [cs, ce)
-    const uint32_t ce = ((cta + 1) * T + NC - 1) / NC;
+    const uint32_t cs = fdiv(cta * T + NC - 1, a.fd_nc);   // this CTA's items [cs, ce)
+    const uint32_t ce = fdiv((cta + 1) * T + NC - 1, a.fd_nc);
     const uint32_t cn = ce - cs;
     const uint32_t ws = cs + cn * warp / kFlWarps, we = cs + cn * (warp + 1) / kFlWarps;
     const int nmine = min((int)(we - ws), kFlMaxItemsPerWarp);   // the host keeps pieces within this
-    const int rho_first = (int)(cs / NS);
-    const int rh_first = rho_first / a.nsub;
-    const int rh_last = cn > 0 ? (int)((ce - 1) / NS) / a.nsub : rh_first - 1;   // none when empty
+    const int rho_first = (int)fdiv(cs, a.fd_ns);
+    const int rh_first = (int)fdiv((uint32_t)rho_first, a.fd_nsub);
+    const int rh_last = cn > 0 ? (int)fdiv(fdiv(ce - 1, a.fd_ns), a.fd_nsub) : rh_first - 1;   // none when empty
 
     uint8_t *ring = smem + warp * LY::WARP_RING;
     const uint32_t ring_s = smem_addr(ring);
@@ -127,12 +129,12 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
     const int nsc_full = (a.sink + kChunk - 1) / kChunk;
     if (lane < nmine) {
         const uint32_t i = ws + lane;
-        my_rho = (int)(i / NS);
+        my_rho = (int)fdiv(i, a.fd_ns);
         my_k = (int)(i - (uint32_t)my_rho * NS);
         my_L = a.lens[fl_row(a, my_rho).r];
     }
-    const int rho_w0 = nmine > 0 ? (int)(ws / NS) : -1;
-    const int rho_w1 = nmine > 0 ? (int)((ws + nmine - 1) / NS) : -1;
+    const int rho_w0 = nmine > 0 ? (int)fdiv(ws, a.fd_ns) : -1;
+    const int rho_w1 = nmine > 0 ? (int)fdiv(ws + nmine - 1, a.fd_ns) : -1;
     uint32_t qa0[DK / 16], qa2[DK / 16], qb0[DK / 16], qb2[DK / 16];
     auto load_q = [&](int rho, uint32_t (&q0)[DK / 16], uint32_t (&q2)[DK / 16]) {
         const FlRow x = fl_row(a, rho < 0 ? 0 : rho);
@@ -179,10 +181,10 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
     // row under a plan whose sink takes nsc items
     auto sel_entries = [&](int rho, int r, int h, int nsc, int k) -> int2 {
         if constexpr (KSEL > 0) {
-            const int kk = k - nsc, cpb = a.c.b / kChunk;
+            const int kk = k - nsc, cpb = (int)a.fd_cpb.d;
             if (kk < 0 || kk >= a.nsel * cpb) return make_int2(-1, -1);
-            const int ei = kk / cpb;
-            const int32_t *srow = s_sel + (rho / a.nsub - rh_first) * kFlMaxSel;
+            const int ei = (int)fdiv((uint32_t)kk, a.fd_cpb);
+            const int32_t *srow = s_sel + ((int)fdiv((uint32_t)rho, a.fd_nsub) - rh_first) * kFlMaxSel;
             return make_int2(srow[ei], ei > 0 ? srow[ei - 1] : -1);
         } else {
             return item_sel_entries(a, r, h, nsc, k);
@@ -209,7 +211,7 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
         const int rho = __shfl_sync(0xffffffffu, my_rho, j);
         if (lane == 0) stage_n[j % kFlStages] = n;
         if (n > 0) {
-            const int h = (rho / a.nsub) % c.hkv;
+            const int h = (int)fmodu(fdiv((uint32_t)rho, a.fd_nsub), a.fd_hkv);
             const uint32_t st = ring_s + (j % kFlStages) * LY::STAGE;
             const uint8_t *kb = c.k + ((int64_t)page * c.kps + (int64_t)h * c.khs + (int64_t)ts * c.kts) * 2;
             const uint8_t *vb = c.v + ((int64_t)page * c.vps + (int64_t)h * c.vhs + (int64_t)ts * c.vts) * 2;
@@ -347,26 +349,48 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
     __syncthreads();   // rings drained: reuse them for the CTA merge
 
     // ---- CTA merge: per row of the piece, combine the warps' segments.
-    // Merge area (in the rings): o [rows][W][G][DK], then (m, l) [rows][W][2G].
+    // Merge area (in the rings): o [rows][W][G][DK], (m, l) [rows][W][2G],
+    // then the warps' weights [rows][G][W] and the log2-sum-exp [rows][G].
     float *mo = reinterpret_cast<float *>(smem);
     float *mml = mo + kFlMaxRowsPerCta * kFlWarps * G * DK;
+    float *mcoef = mml + kFlMaxRowsPerCta * kFlWarps * 2 * G;
+    float *mlse = mcoef + kFlMaxRowsPerCta * G * kFlWarps;
     {
-        const int cur_s = cur_rho < 0 ? -1 : cur_rho - rho_first;   // 0 or 1 (host-guaranteed)
-        // slot 0: the parked first-row segment, or the current one; slot 1: the current one
-        for (int t = lane; t < G * DK; t += 32) {
-            mo[(0 * kFlWarps + warp) * G * DK + t] = s0o[t];
-        }
-        if (lane < 2 * G) {
-            mml[(0 * kFlWarps + warp) * 2 * G + lane] = s0m[lane];
+        // slot 0: the parked first-row segment when the warp went on to the
+        // second row, else the current one; slot 1: the current one then
+        const int cur_s = cur_rho < 0 ? -1 : cur_rho - rho_first;   // -1, 0 or 1 (host-guaranteed); warp-uniform
+        if (cur_s == 1) {
+            for (int t = lane; t < G * DK; t += 32) mo[(0 * kFlWarps + warp) * G * DK + t] = s0o[t];
+            if (lane < 2 * G) mml[(0 * kFlWarps + warp) * 2 * G + lane] = s0m[lane];
+        } else if (lane < 2 * G) {
             mml[(1 * kFlWarps + warp) * 2 * G + lane] = lane < G ? -INFINITY : 0.f;
+            if (cur_s < 0) mml[(0 * kFlWarps + warp) * 2 * G + lane] = lane < G ? -INFINITY : 0.f;
         }
         __syncwarp();
         if (cur_s >= 0)
             write_state(mo + (cur_s * kFlWarps + warp) * G * DK, mml + (cur_s * kFlWarps + warp) * 2 * G);
     }
     __syncthreads();
+    // per (row, head): the warps' weights exp2(m_w - M) / sum_w exp2(m_w - M)
+    // l_w and the log2-sum-exp, once, by kFlWarps consecutive lanes each
+    for (int t = threadIdx.x; t < kFlMaxRowsPerCta * G * kFlWarps; t += blockDim.x) {
+        const int sl = t / (G * kFlWarps), g = (t / kFlWarps) % G, w = t % kFlWarps;
+        const float mw = mml[(sl * kFlWarps + w) * 2 * G + g];
+        const float lw = mml[(sl * kFlWarps + w) * 2 * G + G + g];
+        float M = mw;
+#pragma unroll
+        for (int off = 1; off < kFlWarps; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float f = mw == -INFINITY ? 0.f : fast_ex2(mw - M);
+        float wsum = f * lw;
+#pragma unroll
+        for (int off = 1; off < kFlWarps; off <<= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+        const bool empty_set = !(wsum > 0.f);
+        mcoef[(sl * G + g) * kFlWarps + w] = empty_set ? 0.f : f / wsum;
+        if (w == 0) mlse[sl * G + g] = empty_set ? -INFINITY : M + fast_lg2(wsum);
+    }
+    __syncthreads();
 
-    const int rho_last = cn > 0 ? (int)((ce - 1) / NS) : rho_first - 1;
+    const int rho_last = cn > 0 ? (int)fdiv(ce - 1, a.fd_ns) : rho_first - 1;
     int *s_last = reinterpret_cast<int *>(smem + LY::LAST);
     for (int s = 0; s < kFlMaxRowsPerCta && rho_first + s <= rho_last; ++s) {
         const int rho = rho_first + s;
@@ -374,41 +398,25 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
         const int fc = fl_cta_of(a, (uint32_t)rho * NS);
         const int lc = fl_cta_of(a, (uint32_t)(rho + 1) * NS - 1);
         const int parts = lc - fc + 1;
-        for (int t = threadIdx.x; t < G * DK / 4; t += blockDim.x) {
-            const int g = t / (DK / 4), d = (t % (DK / 4)) * 4;
-            float M = -INFINITY;
+        for (int t = threadIdx.x; t < G * DK / 2; t += blockDim.x) {
+            const int g = t / (DK / 2), d = (t % (DK / 2)) * 2;
+            float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int w = 0; w < kFlWarps; ++w) M = fmaxf(M, mml[(s * kFlWarps + w) * 2 * G + g]);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            float wsum = 0.f;
-            if (M != -INFINITY) {
-#pragma unroll
-                for (int w = 0; w < kFlWarps; ++w) {
-                    const float mw = mml[(s * kFlWarps + w) * 2 * G + g];
-                    if (mw == -INFINITY) continue;
-                    const float f = fast_ex2(mw - M);
-                    wsum += f * mml[(s * kFlWarps + w) * 2 * G + G + g];
-                    const float4 v = *reinterpret_cast<const float4 *>(mo + ((s * kFlWarps + w) * G + g) * DK + d);
-                    acc.x += f * v.x;
-                    acc.y += f * v.y;
-                    acc.z += f * v.z;
-                    acc.w += f * v.w;
-                }
+            for (int w = 0; w < kFlWarps; ++w) {
+                // a warp with nothing in this row has weight 0 and an unwritten slot
+                const float cw = mcoef[(s * G + g) * kFlWarps + w];
+                const float2 v = *reinterpret_cast<const float2 *>(mo + ((s * kFlWarps + w) * G + g) * DK + d);
+                acc.x = cw != 0.f ? fmaf(cw, v.x, acc.x) : acc.x;
+                acc.y = cw != 0.f ? fmaf(cw, v.y, acc.y) : acc.y;
             }
-            const bool empty_set = !(wsum > 0.f);
-            const float inv = empty_set ? 0.f : 1.f / wsum;
-            acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-            const float lse2 = empty_set ? -INFINITY : M + fast_lg2(wsum);
+            const float lse2 = mlse[s * G + g];
             const int64_t orow = (int64_t)x.r * a.hq + x.h * Gt + x.sg * G + g;
             if (parts == 1) {
-                uint2 pk;
-                pk.x = pack_bf16x2(acc.x, acc.y);
-                pk.y = pack_bf16x2(acc.z, acc.w);
-                *reinterpret_cast<uint2 *>(a.out + orow * DK + d) = pk;
-                if (a.lse && d == 0) a.lse[orow] = empty_set ? -INFINITY : lse2 * kFlLn2;
+                *reinterpret_cast<uint32_t *>(a.out + orow * DK + d) = pack_bf16x2(acc.x, acc.y);
+                if (a.lse && d == 0) a.lse[orow] = lse2 == -INFINITY ? -INFINITY : lse2 * kFlLn2;
             } else {
                 const int part = cta - fc;
-                *reinterpret_cast<float4 *>(a.o_part + (orow * a.fl_parts + part) * DK + d) = acc;
+                *reinterpret_cast<float2 *>(a.o_part + (orow * a.fl_parts + part) * DK + d) = acc;
                 if (d == 0) a.lse_part[orow * a.fl_parts + part] = lse2;
             }
         }

@@ -43,9 +43,9 @@ __device__ __forceinline__ RowPlan make_plan(const AttnArgs &a, int r, bool flag
 // selected-block item under a plan whose sink covers nsc items.
 __device__ __forceinline__ int2 item_sel_entries(const AttnArgs &a, int r, int h, int nsc, int i)
 {
-    const int k = i - nsc, cpb = a.c.b / kChunk;
+    const int k = i - nsc, cpb = (int)a.fd_cpb.d;
     if (a.token_mode || k < 0 || k >= a.nsel * cpb) return make_int2(-1, -1);
-    const int ei = k / cpb;
+    const int ei = (int)fdiv((uint32_t)k, a.fd_cpb);
     const int32_t *irow = a.idx + ((int64_t)r * a.c.hkv + h) * a.nsel;
     return make_int2(irow[ei], ei > 0 ? irow[ei - 1] : -1);
 }
@@ -84,8 +84,7 @@ __device__ __forceinline__ ItemDesc describe_item_with(const AttnArgs &a, const 
             return d;
         }
         const int k = i - pl.nsc;
-        const int cpb = b / kChunk;
-        const int ck = k % cpb;
+        const int ck = (int)fmodu((uint32_t)k, a.fd_cpb);
         const int e = sel.x, prev = sel.y;
         const bool valid = e >= 0 && e < a.max_blocks && (int64_t)e * b >= pl.se &&
                            (int64_t)(e + 1) * b <= pl.rs && prev < e;
@@ -101,13 +100,14 @@ __device__ __forceinline__ ItemDesc describe_item_with(const AttnArgs &a, const 
         n = min(pl.L, blk16 * kChunk + kChunk) - t0;
     }
     if (n <= 0) return d;
-    const int p = page_of(r, t0 / b);
+    const uint32_t tb = fdiv((uint32_t)t0, a.fd_b);
+    const int p = page_of(r, (int)tb);
     if (p < 0 || p >= a.c.num_pages) {
         flag_error(a.status, LSA_ERR_BOUNDS);
         return d;
     }
     d.page = p;
-    d.ts = (int16_t)(t0 % b);
+    d.ts = (int16_t)(t0 - (int)tb * b);
     d.n = (int16_t)n;
     return d;
 }

@@ -19,6 +19,44 @@ constexpr int kChunk = 16;
 constexpr long long kSpinBudget = 2000000000LL;
 
 // A paged cache as the kernels see it: byte pointers, element strides.
+// x / d for 0 <= x < 2^31 as one multiply-high and a shift (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994).
+// With l = ceil(log2 d) and m = ceil(2^(31+l) / d): m < 2^32, and
+// x m / 2^(31+l) = x / d + x e / (d 2^(31+l)) with 0 <= e < d, where the
+// second term is below 2^-l <= 1/d, too small to carry floor(x / d) over
+// the next integer; so floor(x / d) = floor(x m / 2^(31+l)).  d = 1: s = -1.
+struct FastDiv {
+    uint32_t d, m;
+    int32_t s;   // l - 1
+};
+
+inline FastDiv make_fastdiv(uint32_t d)
+{
+    FastDiv f;
+    f.d = d < 1 ? 1 : d;
+    int l = 0;
+    while ((1ull << l) < f.d) ++l;
+    if (f.d == 1) {
+        f.m = 0;
+        f.s = -1;
+    } else {
+        f.m = (uint32_t)(((1ull << (31 + l)) + f.d - 1) / f.d);
+        f.s = l - 1;
+    }
+    return f;
+}
+
+__host__ __device__ __forceinline__ uint32_t fdiv(uint32_t x, const FastDiv &f)
+{
+#ifdef __CUDA_ARCH__
+    return f.s < 0 ? x : __umulhi(x, f.m) >> f.s;
+#else
+    return f.s < 0 ? x : (uint32_t)(((uint64_t)x * f.m) >> 32) >> f.s;
+#endif
+}
+
+__host__ __device__ __forceinline__ uint32_t fmodu(uint32_t x, const FastDiv &f) { return x - fdiv(x, f) * f.d; }
+
 struct CacheView {
     const uint8_t *k;
     const uint8_t *v;
@@ -100,6 +138,11 @@ struct AttnArgs {
     // selection out [B*hkv, nsel], or NULL
     const float *sel_scores;
     int32_t sel_cols;
+    // reciprocals of the run-time divisors: block size b, 16-token items per
+    // block, KV heads, query subgroups per KV head, and (even split) item
+    // slots per row, CTAs and items in all; gsize = hq / hkv
+    FastDiv fd_b, fd_cpb, fd_hkv, fd_nsub, fd_ns, fd_nc, fd_total;
+    int32_t gsize;
     // pdl_early: launched right after the score kernel of the same step on
     // the same stream, as a programmatic dependent.  Everything before that
     // score kernel had completed when it let this kernel launch, so q,
