@@ -252,7 +252,8 @@ lsa_status run_attention(const void *q, const CacheView &v, const int32_t *pt, c
     if (pl.flat) {
         a.sel_scores = sel_scores;
         a.sel_cols = p->max_blocks;
-        a.pdl_early = sel_scores ? 1 : 0;   // only the decode step passes score rows, right after scoring
+        // only the decode step passes score rows, right after scoring
+        a.pdl_early = sel_scores && pdl_step_dependent() ? 1 : 0;
         a.sel_write = sel_write;
         a.fl_ns = pl.fl_ns;
         a.fl_total = pl.fl_total;

@@ -149,6 +149,17 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
     load_q(rho_w0, qa0, qa2);
     load_q(rho_w1 != rho_w0 ? rho_w1 : -1, qb0, qb2);
 
+    // the page-table rows of the piece's requests (at most two, adjacent)
+    // into L1 while the CTA selects: the item descriptors read them after
+    // the selection.  One prefetch per 128-byte line, at most 32 KB.
+    if (KSEL > 0 && cn > 0) {
+        const int rq0 = (int)fdiv((uint32_t)rh_first, a.fd_hkv), rq1 = (int)fdiv((uint32_t)rh_last, a.fd_hkv);
+        const char *p0 = reinterpret_cast<const char *>(a.pt + (int64_t)rq0 * a.max_blocks);
+        const int64_t bytes = (int64_t)(rq1 - rq0 + 1) * a.max_blocks * 4;
+        const int lines = (bytes + 127) / 128 < 256 ? (int)((bytes + 127) / 128) : 256;
+        if ((int)threadIdx.x < lines) prefetch_l1(p0 + 128 * (int64_t)threadIdx.x);
+    }
+
     // (early launch) the score rows come from the kernel before: wait for
     // it here, then load the first row's scores
     if (early) pdl_wait();

@@ -44,17 +44,7 @@ __device__ __forceinline__ void pdl_enter()
     pdl_launch_dependents();
 }
 
-// Off unless LSA_PDL=1: measured on the B=16 x 32K step it saved nothing
-// (38.4 vs 38.4 us) and with some kernel mixes cost time (59.7 vs 38.7 us),
-// as early-launched CTAs wait on SMs the running kernel could use.
-inline bool pdl_enabled()
-{
-    static const bool on = [] {
-        const char *e = getenv("LSA_PDL");
-        return e && strcmp(e, "1") == 0;
-    }();
-    return on;
-}
+// pdl_mode / pdl_enabled: lsa_internal.h
 
 // dependent: launch with programmatic stream serialization.
 template <typename... KArgs, typename... Args>
@@ -251,6 +241,9 @@ __device__ __forceinline__ void cp_async16_policy(uint32_t dst, const void *src,
     asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)
                  : "memory");
 }
+
+// Pulls the 128-byte line holding p into L1 (no register result).
+__device__ __forceinline__ void prefetch_l1(const void *p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 

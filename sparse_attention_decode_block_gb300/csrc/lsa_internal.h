@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include "../../include/lsa.h"
 
@@ -56,6 +58,25 @@ __host__ __device__ __forceinline__ uint32_t fdiv(uint32_t x, const FastDiv &f)
 }
 
 __host__ __device__ __forceinline__ uint32_t fmodu(uint32_t x, const FastDiv &f) { return x - fdiv(x, f) * f.d; }
+
+// LSA_PDL=1: every kernel is launched as a programmatic dependent (off by
+// default: with the wait at the top of every kernel it saved nothing on the
+// B=16 x 32K step, 38.4 vs 38.4 us, and with some kernel mixes cost time,
+// 59.7 vs 38.7 us, as early-launched CTAs held SMs the running kernel could
+// use).  LSA_PDL=0: no kernel is, not even the decode step's attention
+// kernel, which by default is (it sets up before its wait).
+inline int pdl_mode()
+{
+    static const int m = [] {
+        const char *e = getenv("LSA_PDL");
+        if (!e) return 1;
+        if (strcmp(e, "0") == 0) return 0;
+        return strcmp(e, "1") == 0 ? 2 : 1;
+    }();
+    return m;
+}
+inline bool pdl_enabled() { return pdl_mode() == 2; }
+inline bool pdl_step_dependent() { return pdl_mode() >= 1; }
 
 struct CacheView {
     const uint8_t *k;

@@ -80,9 +80,39 @@ __device__ __forceinline__ uint32_t tf_block_scan(uint32_t v, uint32_t *red, uin
     return before + incl - v;
 }
 
+// Block-wide exclusive scan of one value per thread below 2^BITS: each bit
+// plane is counted with a warp ballot, and the warps' totals go through
+// `red`, read after one barrier.  No trailing barrier: a caller uses a given
+// `red` again only after at least one more barrier.
+template <int BITS>
+__device__ __forceinline__ uint32_t tf_block_scan_small(uint32_t v, uint32_t *red, uint32_t *total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t lt = (1u << lane) - 1u;
+    uint32_t ex = 0, wt = 0;
+#pragma unroll
+    for (int b = 0; b < BITS; ++b) {
+        const uint32_t m = __ballot_sync(0xffffffffu, (v >> b) & 1u);
+        ex += (uint32_t)__popc(m & lt) << b;
+        wt += (uint32_t)__popc(m) << b;
+    }
+    if (lane == 0) red[warp] = wt;
+    __syncthreads();
+    uint32_t before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < kTfWarps; ++w) {
+        const uint32_t x = red[w];
+        before += w < warp ? x : 0u;
+        all += x;
+    }
+    *total = all;
+    return before + ex;
+}
+
 struct TopkScratch {
     unsigned long long runs[kTfCand];   // sorted runs of 32 candidate sort keys
     uint32_t red[kTfWarps];
+    uint32_t red2[kTfWarps];            // the second scan of the small-k path
     uint32_t tmax[kTfThreads];          // sorted runs of 32 thread maxima
     alignas(16) uint32_t ck[kTfCand + 4];   // + 4: zero padding for 16-byte reads
     int32_t cc[kTfCand];
@@ -310,7 +340,8 @@ __device__ int block_topk_scores(const float (&v)[KPT], int k, uint32_t *status,
 #pragma unroll
         for (int e = 0; e < KPT; ++e) cnt += keys[e] >= lo0;
         uint32_t C = 0;
-        uint32_t pos = tf_block_scan(cnt, sm.red, &C);
+        constexpr int kCntBits = KPT <= 8 ? 4 : KPT <= 32 ? 6 : 16;
+        uint32_t pos = tf_block_scan_small<kCntBits>(cnt, sm.red, &C);
         if (C <= (uint32_t)kTfLinear) {
 #pragma unroll
             for (int e = 0; e < KPT; ++e) {
@@ -326,7 +357,10 @@ __device__ int block_topk_scores(const float (&v)[KPT], int k, uint32_t *status,
             const int i = tid >> lp, q = tid & ((1 << lp) - 1);
             uint32_t rank = 0;
             if (i < (int)C) {
-                const uint32_t mine = sm.ck[i];
+                // (key, complement of the candidate index): one 64-bit
+                // compare orders by larger key, then lower column
+                using u64 = unsigned long long;
+                const u64 me = ((u64)sm.ck[i] << 32) | (0xffffffffu - (uint32_t)i);
                 const uint4 *ck4 = reinterpret_cast<const uint4 *>(sm.ck);
                 const int n4 = ((int)C + 3) >> 2;
                 const int per = (n4 + (1 << lp) - 1) >> lp;
@@ -334,21 +368,22 @@ __device__ int block_topk_scores(const float (&v)[KPT], int k, uint32_t *status,
 #pragma unroll 4
                 for (int j4 = q * per; j4 < j4e; ++j4) {
                     const uint4 y = ck4[j4];
-                    const int j = 4 * j4;
-                    rank += (y.x > mine) | ((y.x == mine) & (j < i));
-                    rank += (y.y > mine) | ((y.y == mine) & (j + 1 < i));
-                    rank += (y.z > mine) | ((y.z == mine) & (j + 2 < i));
-                    rank += (y.w > mine) | ((y.w == mine) & (j + 3 < i));
+                    const uint32_t nj = 0xffffffffu - 4u * (uint32_t)j4;
+                    rank += (((u64)y.x << 32) | nj) > me;
+                    rank += (((u64)y.y << 32) | (nj - 1u)) > me;
+                    rank += (((u64)y.z << 32) | (nj - 2u)) > me;
+                    rank += (((u64)y.w << 32) | (nj - 3u)) > me;
                 }
             }
             rank += __shfl_xor_sync(0xffffffffu, rank, 1);
             if (lp == 2) rank += __shfl_xor_sync(0xffffffffu, rank, 2);
             const uint32_t f = (i < (int)C && q == 0 && rank < (uint32_t)k) ? 1u : 0u;
             uint32_t tot = 0;
-            const uint32_t ex = tf_block_scan(f, sm.red, &tot);
+            const uint32_t ex = tf_block_scan_small<1>(f, sm.red2, &tot);
             if (f) out((int)ex, sm.cc[i]);
             return min(k, (int)C);
         }
+        __syncthreads();   // every read of the scan's red done before the general path reuses it
     }
     // candidate keys (low half) and threads holding one (high half)
     const uint32_t both = tf_block_sum(nvt | (m1 != 0u ? 0x10000u : 0u), sm.red);
