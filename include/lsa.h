@@ -256,10 +256,25 @@ size_t lsa_decode_step_workspace_size(const lsa_cache *cache, const lsa_params *
  * select top-k_blocks per (request, KV head), and attend F U selected.  With
  * c2f_candidates > 0 and an index cache: coarse top-C blocks over
  * `summaries` (built from the index keys), fine top-c2f_tokens tokens, then
- * attention.  Block scores stay on chip (Vortex, "Making it fast": operators
- * are fused so block scores never make a round trip through GPU memory).
+ * attention.
  *   idx_out [batch, Hkv, k_blocks or c2f_tokens] int32 device or NULL.
- * Other arguments as in the calls above. */
+ * Other arguments as in the calls above.
+ *
+ * Implementations (Vortex, "Making it fast", fuses the operators so block
+ * scores never leave the chip; here they make one trip through L2):
+ *   default: two launches.  The score kernel writes fp32 block scores to the
+ *     workspace; the attention kernel selects each (request, KV head) row's
+ *     blocks itself (exact top-k in the CTA), writes idx_out, and attends.
+ *     It is launched as a programmatic dependent of the score kernel and
+ *     reads q, seq_lens and the page table before it waits for the scores,
+ *     which is safe because the score kernel starts only once all earlier
+ *     work on the stream is complete.  With c2f_candidates > 0, rows of more
+ *     than 8192 blocks, k_blocks > 512, an explicit split count or G outside
+ *     2..8, the stages run as separate launches (score, top-k, attention).
+ *   LSA_DECODE_PATH=fused (environment): one persistent launch where it
+ *     applies (no c2f, no explicit split count); slower at present.
+ *   LSA_PDL=0 (environment): no programmatic dependent launch anywhere;
+ *   LSA_PDL=1: every kernel of the library is launched as one. */
 lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *summaries,
                            const lsa_cache *index_cache, const int32_t *page_table,
                            const int32_t *seq_lens, const lsa_params *params, int32_t *idx_out,
