@@ -269,8 +269,10 @@ size_t lsa_decode_step_workspace_size(const lsa_cache *cache, const lsa_params *
  *     reads q, seq_lens and the page table before it waits for the scores,
  *     which is safe because the score kernel starts only once all earlier
  *     work on the stream is complete.  With c2f_candidates > 0, rows of more
- *     than 8192 blocks, k_blocks > 512, an explicit split count or G outside
- *     2..8, the stages run as separate launches (score, top-k, attention).
+ *     than 8192 blocks, k_blocks > 512, an explicit split count, an odd GQA
+ *     group, head dimensions other than dk = dv = 64 or 128, or a latent
+ *     (aliased K/V) cache, the stages run as separate launches (score,
+ *     top-k, attention).
  *   LSA_DECODE_PATH=fused (environment): one persistent launch where it
  *     applies (no c2f, no explicit split count); slower at present.
  *   LSA_PDL=0 (environment): no programmatic dependent launch anywhere;
