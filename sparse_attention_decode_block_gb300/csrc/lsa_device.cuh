@@ -25,14 +25,16 @@ __device__ __forceinline__ void flag_error(uint32_t *status, int code)
 
 // ---------------------------------------------------------------- dependent launch
 
-// The kernels of one step are launched with programmatic stream
-// serialization: a kernel lets the next one be launched as soon as all its
-// CTAs run, and waits for the previous kernel's completion (and the
-// visibility of its writes) before it reads anything.  The overlap hides the
-// launch latency between the kernels of a step; the order of their memory
-// effects is unchanged.  Outside such a launch the wait returns at once.
-// The wait comes first: a kernel's dependents then launch only once
-// everything before that kernel in the stream has completed.
+// A kernel launched with programmatic stream serialization (a dependent)
+// may start once every CTA of the kernel before it has signalled
+// launch_dependents; it must wait (griddepcontrol.wait: that kernel has
+// completed and its writes are visible) before it reads that kernel's
+// results.  Outside a dependent launch the wait returns at once.  Kernels
+// call pdl_enter at their top: the wait first, so that as dependents they
+// run nothing before their predecessor completes, then the signal, so that
+// their own dependents start only once everything before them on the
+// stream has completed.  The decode step's attention kernel signals first
+// and waits after its set-up (attention_flat.cu).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents()
 {
