@@ -165,6 +165,28 @@ def test_topk_random_rows_with_ties(cols, k):
     assert np.array_equal(idx.cpu().numpy(), want)
 
 
+@pytest.mark.parametrize("cols", [2048, 8192])
+@pytest.mark.parametrize("k", [32, 62, 64, 65, 128])
+def test_topk_clustered_rows_take_every_selection_path(cols, k):
+    """Rows whose largest keys sit in few threads' columns: the candidate
+    set at the k-th largest thread maximum grows past 128 (ranked through
+    sorted runs) and past 512 (bisection), on both sides of k = 64, where
+    the bound switches from the top-64 tree to the general search."""
+    gen = torch.Generator().manual_seed(cols * 131 + k)
+    rows = 5
+    s = torch.randn(rows, cols, generator=gen)
+    s[0, 500:700] += 20.0                                    # one contiguous cluster
+    s[1] = torch.arange(cols, dtype=torch.float32)           # increasing: the last columns win
+    s[2, ::16] += 10.0                                       # one high key every 16 columns
+    s[3, 100:100 + 3 * k] = 7.0                              # a tie run longer than k at the top
+    s[4, cols // 2:] = torch.randn(cols - cols // 2, generator=gen).abs() + 3.0   # upper half above the rest
+    idx = torch.empty((rows, k), dtype=torch.int32, device="cuda")
+    L.lsa_topk(s.cuda(), None, k, idx)
+    check_status_clean()
+    want = oracle.topk(s.numpy(), k)
+    assert np.array_equal(idx.cpu().numpy(), want)
+
+
 def test_topk_nan_is_skipped_and_flagged():
     s = torch.tensor([[0.5, float("nan"), 2.0, 1.0]], device="cuda")
     idx = torch.empty((1, 2), dtype=torch.int32, device="cuda")
