@@ -222,16 +222,25 @@ lsa_status lsa_sparse_decode(const void *q, const lsa_cache *cache, const int32_
  * serving loop whose memory plan is fixed before it starts and admits no
  * allocation afterwards.  It allocates nothing: its scratch is one buffer of
  * LSA_STATIC_SCRATCH_BYTES in the library's own static device memory, one
- * per device, zero at load.  A call whose shape (cache descriptor and
- * parameters) or implementation differs from the previous call on that
- * device first clears the bytes it needs, on its stream.  Shapes whose lsa_sparse_decode_workspace_size
- * exceeds LSA_STATIC_SCRATCH_BYTES are rejected with LSA_ERR_WORKSPACE
- * before anything is launched.  The first call on a device looks up the
- * buffer's address once; make that first call before any stream capture
- * begins.  All calls on a device share the one buffer, so calls that may
- * run at the same time (several streams, or host threads without an order
- * between their calls) must not use this entry point.  Arguments and
- * results otherwise as lsa_sparse_decode. */
+ * per device, zero at load, held until the process exits.
+ *   - Shapes whose lsa_sparse_decode_workspace_size exceeds
+ *     LSA_STATIC_SCRATCH_BYTES are rejected with LSA_ERR_WORKSPACE, and
+ *     invalid pointers with LSA_ERR_INVALID_ARG, before anything is
+ *     launched or cleared.
+ *   - Counters in the buffer must be zero when a call starts; a call that
+ *     completes leaves them zero for the next call with the same layout.  A
+ *     call whose cache descriptor, parameters or attention plan (which
+ *     LSA_ATTENTION_PATH can change) differs from the previous call's on
+ *     that device first clears the bytes it needs, on its stream.  So does
+ *     the first call after lsa_get_device_status reported a device error
+ *     (a call that recorded one may leave counters non-zero): read the
+ *     status after such a call before making the next one.
+ *   - The first call on a device looks up the buffer's address once; make
+ *     that first call before any stream capture begins.
+ *   - All calls on a device share the one buffer, so calls that may run at
+ *     the same time (several streams, or host threads without an order
+ *     between their calls) race on it and must not use this entry point.
+ * Arguments and results otherwise as lsa_sparse_decode. */
 #define LSA_STATIC_SCRATCH_BYTES (8u << 20)
 lsa_status lsa_sparse_decode_static_scratch(const void *q, const lsa_cache *cache,
                                             const int32_t *page_table, const int32_t *seq_lens,
@@ -273,8 +282,6 @@ size_t lsa_decode_step_workspace_size(const lsa_cache *cache, const lsa_params *
  *     group, head dimensions other than dk = dv = 64 or 128, or a latent
  *     (aliased K/V) cache, the stages run as separate launches (score,
  *     top-k, attention).
- *   LSA_DECODE_PATH=fused (environment): one persistent launch where it
- *     applies (no c2f, no explicit split count); slower at present.
  *   LSA_PDL=0 (environment): no programmatic dependent launch anywhere;
  *   LSA_PDL=1: every kernel of the library is launched as one. */
 lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *summaries,

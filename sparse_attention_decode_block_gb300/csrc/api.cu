@@ -123,6 +123,18 @@ float scale_of(const lsa_params *p, int dk)
     return p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / sqrtf((float)dk);
 }
 
+// Pointer checks of the attention call (lsa_sparse_decode and its
+// no-workspace variant), made before anything is launched or cleared.
+lsa_status check_decode_args(const void *q, const int32_t *page_table, const int32_t *seq_lens, const int32_t *idx,
+                             const lsa_params *p, const void *out)
+{
+    const bool token_mode = p->c2f_candidates > 0;
+    const int nsel = token_mode ? p->c2f_tokens : p->k_blocks;
+    if (!q || !page_table || !seq_lens || !out || !aligned16(q) || (nsel > 0 && !idx)) return LSA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(out) & 7u) != 0) return LSA_ERR_INVALID_ARG;
+    return LSA_OK;
+}
+
 // ---------------------------------------------------------------- planning
 
 struct AttnPlan {
@@ -296,7 +308,7 @@ lsa_status run_attention(const void *q, const CacheView &v, const int32_t *pt, c
     return LSA_OK;
 }
 
-// Workspace of the fused step: [scores | selection | c2f extras | attention].
+// Workspace of the decode step: [scores | selection | c2f extras | attention].
 struct StepLayout {
     size_t scores, sel, cand, fine, attn, total;
 };
@@ -318,104 +330,12 @@ lsa_status step_layout(const CacheView &v, const CacheView *iv, const lsa_params
     return LSA_OK;
 }
 
-// Workspace of the persistent kernel: [control counters | scores |
-// selection | chunk table | part outputs | part lse].
-struct FusedLayout {
-    size_t ctrl, scores, sel, ctab, opart, lpart, total;
-    FusedPlan plan;
-};
-
-// Which implementation runs a step: LSA_DECODE_PATH=fused takes the
-// persistent kernel wherever it applies, =pipeline the stage-by-stage
-// kernels; unset, kFusedByDefault decides.
-constexpr bool kFusedByDefault = false;
-
-bool use_fused(const CacheView &v, const lsa_params *p)
-{
-    const char *e = getenv("LSA_DECODE_PATH");
-    const bool want = e ? strcmp(e, "fused") == 0 : kFusedByDefault;
-    if (!want) return false;
-    if (p->c2f_candidates > 0 || p->num_splits > 0) return false;
-    return fused_supported(v.dk, v.dv, v.hkv, p->num_q_heads / v.hkv, v.v_alias != 0, v.b, p->max_blocks,
-                           p->k_blocks, p->batch, sm_count());
-}
-
-void fused_layout(const CacheView &v, const lsa_params *p, bool scoring, FusedLayout *L)
-{
-    fused_plan(p->sink_tokens, p->recent_tokens, v.b, p->k_blocks, p->batch, v.hkv, p->max_blocks, scoring,
-               &L->plan);
-    const size_t rows = (size_t)p->batch * v.hkv;
-    const size_t rowsq = (size_t)p->batch * p->num_q_heads * L->plan.units_per_row;
-    // each counter on its own 256-byte line (64 words apart): the score
-    // tickets, the leave counter, the attention tickets, one per request
-    // (score units done) and one per (request, KV head) for the merge
-    L->ctrl = round_up((3 + (size_t)p->batch + rows) * 64 * sizeof(uint32_t));
-    L->scores = scoring ? round_up(rows * p->max_blocks * sizeof(float)) : 0;
-    L->sel = scoring ? round_up(rows * p->k_blocks * sizeof(int32_t)) : 0;
-    L->ctab = scoring ? round_up(rows * L->plan.units_per_row * L->plan.chunks_per_unit * sizeof(uint64_t)) : 0;
-    L->opart = L->plan.units_per_row > 1 ? round_up(rowsq * v.dv * sizeof(float)) : 0;
-    L->lpart = L->plan.units_per_row > 1 ? round_up(rowsq * sizeof(float)) : 0;
-    L->total = L->ctrl + L->scores + L->sel + L->ctab + L->opart + L->lpart;
-}
-
-// scoring: the whole step (scores, top-k, attention); otherwise attention
-// only, over the caller's selection `sel`.
-lsa_status run_fused(const void *q, const CacheView &v, const void *summaries, const int32_t *pt,
-                     const int32_t *lens, const lsa_params *p, bool scoring, int32_t *sel, void *out, float *lse,
-                     uint8_t *ws, cudaStream_t st)
-{
-    FusedLayout L;
-    fused_layout(v, p, scoring, &L);
-    FusedArgs a;
-    memset(&a, 0, sizeof a);
-    a.q = static_cast<const uint16_t *>(q);
-    a.c = v;
-    a.summ = static_cast<const uint16_t *>(summaries);
-    a.pt = pt;
-    a.lens = lens;
-    a.batch = p->batch;
-    a.hq = p->num_q_heads;
-    a.max_blocks = p->max_blocks;
-    a.k_blocks = p->k_blocks;
-    a.sink = p->sink_tokens;
-    a.recent = p->recent_tokens;
-    a.scale_log2 = scale_of(p, v.dk) * 1.4426950408889634f;
-    a.score_blocks = L.plan.score_blocks;
-    a.score_chunks = L.plan.score_chunks;
-    a.score_units = L.plan.score_units;
-    a.attn_base = L.plan.attn_base;
-    a.total_units = L.plan.total_units;
-    a.units_per_row = L.plan.units_per_row;
-    a.chunks_per_unit = L.plan.chunks_per_unit;
-    uint8_t *cur = ws;
-    a.ctrl = reinterpret_cast<uint32_t *>(cur);            // [0] score, [64] leave, [128] attention tickets
-    a.score_hint = a.ctrl + 3 * 64;
-    a.split_done = a.score_hint + (size_t)p->batch * 64;
-    cur += L.ctrl;
-    a.scores = reinterpret_cast<uint32_t *>(cur);
-    cur += L.scores;
-    a.sel = sel ? sel : reinterpret_cast<int32_t *>(cur);
-    cur += L.sel;
-    a.ctab = scoring ? reinterpret_cast<uint64_t *>(cur) : nullptr;
-    cur += L.ctab;
-    a.o_part = reinterpret_cast<float *>(cur);
-    cur += L.opart;
-    a.lse_part = reinterpret_cast<float *>(cur);
-    a.out = static_cast<uint16_t *>(out);
-    a.lse = lse;
-    a.status = status_word();
-    a.spin_budget = kSpinBudget;
-#ifdef LSA_FUSED_TRACE
-    if (const char *tp = getenv("LSA_TRACE_PTR")) a.trace = reinterpret_cast<uint64_t *>(strtoull(tp, nullptr, 0));
-#endif
-    bool unsup = false;
-    cudaError_t e = launch_fused(a, st, sm_count(), &unsup);
-    if (unsup) return LSA_ERR_UNSUPPORTED;
-    return e == cudaSuccess ? LSA_OK : LSA_ERR_CUDA;
-}
-
 }  // namespace
 }  // namespace lsa
+
+namespace lsa {
+void static_scratch_forget(int dev);
+}
 
 using namespace lsa;
 
@@ -447,6 +367,9 @@ lsa_status lsa_get_device_status(uint32_t *flags, int clear)
         if (cudaMemcpyToSymbol(d_status_word, &z, sizeof z) != cudaSuccess) return LSA_ERR_CUDA;
     }
     if (flags) *flags = v;
+    // a call that recorded a device error may have left counters of the
+    // static scratch non-zero: the next no-workspace call clears it again
+    if (v != 0) static_scratch_forget(current_device());
     const lsa_status order[] = {LSA_ERR_TIMEOUT, LSA_ERR_BOUNDS, LSA_ERR_NAN, LSA_ERR_INVALID_ARG};
     for (lsa_status s : order)
         if (v & (1u << s)) return s;
@@ -614,13 +537,7 @@ size_t lsa_sparse_decode_workspace_size(const lsa_cache *cache, const lsa_params
     if (make_view(cache, true, &v) != LSA_OK || check_params(params, v) != LSA_OK) return 0;
     AttnPlan pl;
     if (plan_attention(v, params, params->c2f_candidates > 0, &pl) != LSA_OK) return 0;
-    size_t need = pl.ws_bytes;
-    if (use_fused(v, params)) {
-        FusedLayout F;
-        fused_layout(v, params, false, &F);
-        if (F.total > need) need = F.total;
-    }
-    return need;
+    return pl.ws_bytes;
 }
 
 lsa_status lsa_sparse_decode(const void *q, const lsa_cache *cache, const int32_t *page_table,
@@ -632,17 +549,9 @@ lsa_status lsa_sparse_decode(const void *q, const lsa_cache *cache, const int32_
     if (rc != LSA_OK) return rc;
     if ((rc = check_params(params, v)) != LSA_OK) return rc;
     if (params->batch == 0) return LSA_OK;
+    if ((rc = check_decode_args(q, page_table, seq_lens, idx, params, out)) != LSA_OK) return rc;
     const bool token_mode = params->c2f_candidates > 0;
     const int nsel = token_mode ? params->c2f_tokens : params->k_blocks;
-    if (!q || !page_table || !seq_lens || !out || !aligned16(q) || (nsel > 0 && !idx)) return LSA_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(out) & 7u) != 0) return LSA_ERR_INVALID_ARG;
-    if (use_fused(v, params)) {
-        FusedLayout F;
-        fused_layout(v, params, false, &F);
-        if (!workspace || workspace_bytes < F.total || !aligned16(workspace)) return LSA_ERR_WORKSPACE;
-        return run_fused(q, v, nullptr, page_table, seq_lens, params, false, const_cast<int32_t *>(idx), out, lse,
-                         static_cast<uint8_t *>(workspace), reinterpret_cast<cudaStream_t>(stream));
-    }
     return run_attention(q, v, page_table, seq_lens, nsel > 0 ? idx : nullptr, params, token_mode, out, lse,
                          static_cast<uint8_t *>(workspace), workspace_bytes,
                          reinterpret_cast<cudaStream_t>(stream));
@@ -655,13 +564,7 @@ size_t lsa_decode_step_workspace_size(const lsa_cache *cache, const lsa_params *
     StepLayout L;
     CacheView iv = v;   // the index cache shares paging and geometry with the attention cache
     if (step_layout(v, &iv, params, &L) != LSA_OK) return 0;
-    size_t need = L.total;
-    if (use_fused(v, params)) {
-        FusedLayout F;
-        fused_layout(v, params, true, &F);
-        if (F.total > need) need = F.total;
-    }
-    return need;
+    return L.total;
 }
 
 lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *summaries,
@@ -685,14 +588,6 @@ lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *su
     if (!q || !summaries || !page_table || !seq_lens || !out || !aligned16(q) || !aligned16(summaries))
         return LSA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(out) & 7u) != 0) return LSA_ERR_INVALID_ARG;
-    cudaStream_t st0 = reinterpret_cast<cudaStream_t>(stream);
-    if (use_fused(v, params)) {
-        FusedLayout F;
-        fused_layout(v, params, true, &F);
-        if (!workspace || workspace_bytes < F.total || !aligned16(workspace)) return LSA_ERR_WORKSPACE;
-        return run_fused(q, v, summaries, page_table, seq_lens, params, true, idx_out, out, lse,
-                         static_cast<uint8_t *>(workspace), st0);
-    }
     StepLayout L;
     if ((rc = step_layout(v, &iv, params, &L)) != LSA_OK) return rc;
     if (L.total > 0 && (!workspace || workspace_bytes < L.total)) return LSA_ERR_WORKSPACE;
@@ -775,34 +670,44 @@ lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *su
 // (zero-initialised when the module loads).  Nothing is allocated per call;
 // the array's address is looked up once per device with that device current.
 
+namespace lsa {
 namespace {
 
 constexpr size_t kStaticScratchBytes = LSA_STATIC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
 std::mutex g_static_mu;
 void *g_static_ptr[kMaxDevices] = {};
-// what the buffer of each device last served: the counters a call needs at
-// zero are left at zero for the next call of the same shape and path, but
-// another shape lays its counters over bytes the previous one used for data
+// What the buffer of each device last served.  A call leaves the counters
+// it needs at zero for the next call with the same layout, but another
+// shape, or another attention plan for the same shape (LSA_ATTENTION_PATH
+// picks the kernel per call), lays its counters over bytes the previous
+// one used for data.
 struct ScratchUse {
     lsa_cache cache;
     lsa_params params;
-    bool fused;
+    AttnPlan plan;
     bool valid;
 };
 ScratchUse g_static_use[kMaxDevices] = {};
 
-// The device's buffer; when the call's shape or path differs from the one
-// the buffer served last, the bytes it needs are cleared first (on the
-// call's stream: a memset, no allocation).
-lsa_status static_scratch_for_current_device(const lsa_cache *cache, const lsa_params *params, bool fused,
-                                             size_t need, cudaStream_t st, void **ptr)
+bool same_plan(const AttnPlan &a, const AttnPlan &b)
 {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LSA_ERR_CUDA;
+    return a.nsub == b.nsub && a.splits == b.splits && a.items_per_split == b.items_per_split &&
+           a.tc_group == b.tc_group && a.flat == b.flat && a.fl_ns == b.fl_ns && a.fl_ctas == b.fl_ctas &&
+           a.fl_parts == b.fl_parts && a.fl_total == b.fl_total && a.ws_bytes == b.ws_bytes;
+}
+
+// The device's buffer; when the call's shape or plan differs from the one
+// the buffer served last (or a device error was reported since), the bytes
+// it needs are cleared first (on the call's stream: a memset, no
+// allocation).
+lsa_status static_scratch_for_current_device(const lsa_cache *cache, const lsa_params *params, const AttnPlan &plan,
+                                             cudaStream_t st, void **ptr)
+{
+    const int dev = current_device();
+    if (dev < 0) return LSA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_static_mu);
     if (!g_static_ptr[dev]) {
         void *p = nullptr;
@@ -810,13 +715,15 @@ lsa_status static_scratch_for_current_device(const lsa_cache *cache, const lsa_p
         g_static_ptr[dev] = p;
     }
     ScratchUse &u = g_static_use[dev];
-    const bool same = u.valid && u.fused == fused && memcmp(&u.cache, cache, sizeof *cache) == 0 &&
+    const bool same = u.valid && same_plan(u.plan, plan) && memcmp(&u.cache, cache, sizeof *cache) == 0 &&
                       memcmp(&u.params, params, sizeof *params) == 0;
     if (!same) {
-        if (need > 0 && cudaMemsetAsync(g_static_ptr[dev], 0, need, st) != cudaSuccess) return LSA_ERR_CUDA;
+        u.valid = false;
+        if (plan.ws_bytes > 0 && cudaMemsetAsync(g_static_ptr[dev], 0, plan.ws_bytes, st) != cudaSuccess)
+            return LSA_ERR_CUDA;
         u.cache = *cache;
         u.params = *params;
-        u.fused = fused;
+        u.plan = plan;
         u.valid = true;
     }
     *ptr = g_static_ptr[dev];
@@ -824,6 +731,15 @@ lsa_status static_scratch_for_current_device(const lsa_cache *cache, const lsa_p
 }
 
 }  // namespace
+
+void static_scratch_forget(int dev)
+{
+    if (dev < 0 || dev >= kMaxDevices) return;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    g_static_use[dev].valid = false;
+}
+
+}  // namespace lsa
 
 extern "C" lsa_status lsa_sparse_decode_static_scratch(const void *q, const lsa_cache *cache,
                                                        const int32_t *page_table, const int32_t *seq_lens,
@@ -834,14 +750,15 @@ extern "C" lsa_status lsa_sparse_decode_static_scratch(const void *q, const lsa_
     lsa_status rc = make_view(cache, true, &v);
     if (rc != LSA_OK) return rc;
     if ((rc = check_params(params, v)) != LSA_OK) return rc;
-    const size_t need = lsa_sparse_decode_workspace_size(cache, params);
-    if (need > kStaticScratchBytes) return LSA_ERR_WORKSPACE;
+    AttnPlan plan;
+    if ((rc = plan_attention(v, params, params->c2f_candidates > 0, &plan)) != LSA_OK) return rc;
+    if (plan.ws_bytes > kStaticScratchBytes) return LSA_ERR_WORKSPACE;
     if (params->batch == 0) return LSA_OK;
+    if ((rc = check_decode_args(q, page_table, seq_lens, idx, params, out)) != LSA_OK) return rc;
     void *scratch = nullptr;
-    if ((rc = static_scratch_for_current_device(cache, params, use_fused(v, params), need,
-                                                reinterpret_cast<cudaStream_t>(stream), &scratch)) != LSA_OK)
+    if ((rc = static_scratch_for_current_device(cache, params, plan, reinterpret_cast<cudaStream_t>(stream),
+                                                &scratch)) != LSA_OK)
         return rc;
     return lsa_sparse_decode(q, cache, page_table, seq_lens, idx, params, out, lse, scratch, kStaticScratchBytes,
                              stream);
 }
-

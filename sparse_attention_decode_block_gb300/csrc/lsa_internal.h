@@ -201,41 +201,6 @@ struct MergeArgs {
     float *lse;
 };
 
-// Persistent decode kernel (one worker per warp): score units, top-k units
-// and attention units in one launch, or attention units alone.  Control
-// counters live in the workspace and must be zero before the first call;
-// every call that completes leaves them zero.
-struct FusedArgs {
-    const uint16_t *q;          // [B, Hq, dk]
-    CacheView c;
-    const uint16_t *summ;       // [num_pages, hkv, dk]
-    const int32_t *pt;
-    const int32_t *lens;
-    int32_t batch, hq, max_blocks, k_blocks, sink, recent;
-    float scale_log2;
-    // work units: [0, score_units) scores, [score_units, attn_base) top-k,
-    // [attn_base, total_units) attention parts
-    int32_t score_blocks, score_chunks, score_units, attn_base, total_units, units_per_row, chunks_per_unit;
-    int32_t total_warps;
-    uint32_t *scores;           // [B*hkv, max_blocks] score keys, 0 = not yet written
-    int32_t *sel;               // [B*hkv, k_blocks] selected blocks (ascending, -1 pad)
-    uint64_t *ctab;             // [B*hkv, units_per_row*chunks_per_unit] chunk table (whole step), or NULL
-    float *o_part;              // [B*Hq, units_per_row, dv]
-    float *lse_part;            // [B*Hq, units_per_row] (log2 units)
-    uint32_t *ctrl;             // [0] ticket, [1] workers done
-    uint32_t *score_hint;       // [B] score units done (relaxed count, a hint)
-    uint32_t *split_done;       // [B*hkv]
-    uint16_t *out;
-    float *lse;
-    uint32_t *status;
-    long long spin_budget;
-    uint64_t *trace;            // per-unit timeline (trace builds only), or NULL
-};
-
-struct FusedPlan {
-    int32_t units_per_row, chunks_per_unit, score_blocks, score_chunks, score_units, attn_base, total_units;
-};
-
 // ---- launchers (return a cudaError_t from the launch; LSA_ERR_UNSUPPORTED
 // is reported through *unsupported when no kernel instance fits the shape)
 cudaError_t launch_build_summaries(const SummaryArgs &a, cudaStream_t s);
@@ -262,11 +227,5 @@ int attention_items_max(int sink, int recent, int b, int nsel, int token_mode);
 int attention_max_items_per_split(int dk, int dv, bool alias, int token_mode);
 int topk_max_cols();
 int score_chunk(int batch, int max_blocks, int sms);
-bool fused_supported(int dk, int dv, int hkv, int group, bool alias, int b, int max_blocks, int k_blocks, int batch,
-                     int sms);
-void fused_plan(int sink, int recent, int b, int k_blocks, int batch, int hkv, int max_blocks, bool scoring,
-                FusedPlan *pl);
-int fused_smem_bytes();
-cudaError_t launch_fused(const FusedArgs &a, cudaStream_t s, int sms, bool *unsupported);
 
 }  // namespace lsa

@@ -36,7 +36,7 @@ __device__ void summarize_block(const CacheView &c, int64_t p, int h, uint16_t *
     const uint8_t *base = c.k + (p * c.kps + (int64_t)h * c.khs) * esz;
     const float *sbase = c.e4m3 ? c.kscale + p * c.sps + (int64_t)h * c.shs : nullptr;
     uint16_t *dst = summ + (p * c.hkv + h) * (int64_t)c.dk;
-    const double inv_b = 1.0 / (double)b;
+    const double db = (double)b;
 
     int phases = 1;
     if (nch < 32 && (32 % nch) == 0) phases = 32 / nch;
@@ -82,8 +82,11 @@ __device__ void summarize_block(const CacheView &c, int64_t p, int h, uint16_t *
             uint32_t packed[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                uint32_t lo = f64_to_bf16_rne(sum[2 * i] * inv_b);
-                uint32_t hi = f64_to_bf16_rne(sum[2 * i + 1] * inv_b);
+                // fp64 division is correctly rounded, as is the mean the
+                // definition asks for; a product with 1/b is not when b is
+                // not a power of two
+                uint32_t lo = f64_to_bf16_rne(sum[2 * i] / db);
+                uint32_t hi = f64_to_bf16_rne(sum[2 * i + 1] / db);
                 packed[i] = lo | (hi << 16);
             }
             uint4 *d = reinterpret_cast<uint4 *>(dst + (int64_t)ch * epc);

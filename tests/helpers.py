@@ -9,9 +9,11 @@ Tolerances
     checked to lie inside the tie band, and their attention is checked with
     the oracle run on that selection.
   attention: |o - o_ref| <= 2e-2 + 1e-2 * |o_ref| element-wise (bf16 inputs,
-    fp32 accumulation); lse within 2e-3 absolute.
+    fp32 accumulation); lse: |l - l_ref| <= 1e-3 + 1e-3 * |l_ref|.
 """
 from __future__ import annotations
+
+import os
 
 import numpy as np
 import torch
@@ -21,7 +23,7 @@ import sparse_attention_decode_block_gb300 as L
 from workloads import Workload
 
 ATOL, RTOL = 2e-2, 1e-2
-LSE_ATOL = 2e-3
+LSE_ATOL, LSE_RTOL = 1e-3, 1e-3
 
 
 def to_dev(inp: dict, dev="cuda") -> dict:
@@ -72,7 +74,7 @@ def oracle_index(inp: dict) -> oracle.Cache:
     return oracle.Cache(None, None, k8=inp["idx_keys"], k8_scale=inp["idx_scale"])
 
 
-def oracle_decode(w: Workload, cpu: dict, nthreads: int = 8, **over):
+def oracle_decode(w: Workload, cpu: dict, nthreads: int = os.cpu_count() or 1, **over):
     kw = dict(num_q_heads=w.num_q_heads, k_blocks=w.k_blocks, sink=w.sink, recent=w.recent,
               scale=w.softmax_scale, nthreads=nthreads)
     if w.c2f_candidates > 0:
@@ -149,7 +151,8 @@ def assert_lse_close(lse_gpu: torch.Tensor, lse_ref: np.ndarray, what: str = "")
     l = lse_gpu.detach().cpu().numpy().astype(np.float64)
     both_inf = np.isneginf(l) & np.isneginf(lse_ref)
     d = np.where(both_inf, 0.0, np.abs(l - lse_ref))
-    assert np.all(d <= LSE_ATOL), f"{what}: lse max err {np.nanmax(d):.3g}"
+    lim = LSE_ATOL + LSE_RTOL * np.where(both_inf, 0.0, np.abs(lse_ref))
+    assert np.all(d <= lim), f"{what}: lse max err {np.nanmax(d):.3g}"
 
 
 def score_bound(q_bits: np.ndarray, summ_f64: np.ndarray, G: int, dk: int) -> np.ndarray:

@@ -58,6 +58,24 @@ def test_summaries_bit_exact(name):
     assert np.all(got[~valid] == 0)          # pages with no full block untouched
 
 
+def test_summaries_bit_exact_block_48():
+    """A block size that is not a power of two: the mean is a correctly
+    rounded fp64 division on both sides, then one bf16 rounding."""
+    w = small("b16_small", block_size=48, seq_lens=(4096, 3001, 777), k_blocks=20)
+    cpu = make_inputs(w, "cpu")
+    g = to_dev(cpu)
+    c = L.make_cache(g["k_cache"], g["v_cache"])
+    summ = torch.zeros((cpu["num_pages"], w.num_kv_heads, w.dk), dtype=torch.bfloat16, device="cuda")
+    L.lsa_build_summaries(c, g["page_table"], g["seq_lens"], summ)
+    check_status_clean()
+    ref, valid = oracle.summaries(oracle_cache(cpu), cpu["page_table"], cpu["seq_lens"])
+    got = bits(summ)
+    assert valid.any()
+    assert np.array_equal(got[valid], ref[valid])
+    # and the whole step at b = 48 (three 16-token items per block)
+    run_and_compare_step(w, cpu, g)
+
+
 def test_append_matches_bulk_build():
     w = small("b16_small", seq_lens=(100, 33, 18))
     cpu = make_inputs(w, "cpu", lens=[100 + 40, 33 + 40, 18 + 40])   # room for 40 appended tokens
@@ -199,15 +217,13 @@ def test_topk_nan_is_skipped_and_flagged():
 
 # ---------------------------------------------------------------- attention
 
-@pytest.mark.parametrize("engine", ["fused", "split_k", "cuda_core"])
+@pytest.mark.parametrize("engine", ["tensor_core", "cuda_core"])
 @pytest.mark.parametrize("name", SMALL)
 @pytest.mark.parametrize("splits", [0, 1, 3])
 def test_sparse_decode_with_oracle_selection(name, splits, engine, monkeypatch):
-    """Attention over the oracle's selection: the persistent kernel (where it
-    applies; an explicit split count takes the split-K kernels), the split-K
-    tensor-core kernel (GQA groups of 2..8 heads) and the split-K CUDA-core
-    kernel."""
-    monkeypatch.setenv("LSA_DECODE_PATH", "fused" if engine == "fused" else "pipeline")
+    """Attention over the oracle's selection: the tensor-core kernels (GQA
+    groups of 2..8 heads: the even split over the GPU without a split count,
+    split-K with one) and the split-K CUDA-core kernel."""
     if engine == "cuda_core":
         monkeypatch.setenv("LSA_ATTENTION_PATH", "cuda_core")
     w = small(name)
@@ -227,11 +243,10 @@ def test_sparse_decode_with_oracle_selection(name, splits, engine, monkeypatch):
     assert_lse_close(lse, ref["lse"], name)
 
 
-def run_and_compare_step(w, cpu, g, reqs=None, num_splits=0):
-    st = GpuStep(w, g, num_splits)
-    st.run()
-    check_status_clean()
-    reqs = list(range(w.batch)) if reqs is None else list(reqs)
+def compare_step_rows(st, w, cpu, reqs):
+    """Checks requests `reqs` of a finished GpuStep against the oracle run on
+    those requests alone (selection, then attention and lse)."""
+    reqs = list(reqs)
     sub = subset(cpu, reqs) if len(reqs) != w.batch else cpu
     wr = w.replace(batch=len(reqs), seq_lens=tuple(sub["lens"]), seq_len_range=None)
     ref = oracle_decode(wr, sub)
@@ -248,7 +263,7 @@ def run_and_compare_step(w, cpu, g, reqs=None, num_splits=0):
         G = w.group
         for i in range(len(reqs)):
             for h in range(w.num_kv_heads):
-                pg = np.maximum(sub["page_table"][i].numpy(), 0)
+                pg = np.maximum(sub["page_table"][i].cpu().numpy(), 0)
                 tau = score_bound(bits(sub["q"][i, h * G:(h + 1) * G]), S[pg, h], G, w.dk)
                 kind = compare_selection(sel_gpu[i, h], ref["sel"][i, h], sc[i, h], tau)
                 ties += kind == "tie"
@@ -268,20 +283,23 @@ def run_and_compare_step(w, cpu, g, reqs=None, num_splits=0):
     return err
 
 
-@pytest.mark.parametrize("path", ["fused", "pipeline"])
+def run_and_compare_step(w, cpu, g, reqs=None, num_splits=0):
+    st = GpuStep(w, g, num_splits)
+    st.run()
+    check_status_clean()
+    return compare_step_rows(st, w, cpu, range(w.batch) if reqs is None else reqs)
+
+
 @pytest.mark.parametrize("name", SMALL + ["c2f_small"])
-def test_decode_step_end_to_end(name, path, monkeypatch):
-    """Both implementations of the step: the persistent kernel (where it
-    applies; the coarse-to-fine step always takes the pipeline) and the
-    stage-by-stage pipeline."""
-    monkeypatch.setenv("LSA_DECODE_PATH", path)
+def test_decode_step_end_to_end(name):
     w = small(name)
     cpu = make_inputs(w, "cpu")
     run_and_compare_step(w, cpu, to_dev(cpu))
 
 
-def test_fused_step_repeats_and_leaves_workspace_zeroed(monkeypatch):
-    monkeypatch.setenv("LSA_DECODE_PATH", "fused")
+def test_step_repeats_bit_identical():
+    """Five calls on one workspace give identical bits (the counters the
+    step needs at zero are left at zero by every call)."""
     w = small("b16_small")
     cpu = make_inputs(w, "cpu")
     g = to_dev(cpu)
@@ -295,19 +313,14 @@ def test_fused_step_repeats_and_leaves_workspace_zeroed(monkeypatch):
         assert torch.equal(o[0], outs[0][0])
         assert torch.equal(o[1].view(torch.int16), outs[0][1].view(torch.int16))
         assert torch.equal(o[2], outs[0][2])
-    # control counters at the head of the workspace (one per 256-byte line) are back to zero
-    ctrl_words = (3 + w.batch + w.batch * w.num_kv_heads) * 64
-    assert torch.all(st.ws[: 4 * ctrl_words] == 0)
     ref = oracle_decode(w, cpu)
     assert np.array_equal(outs[0][0].cpu().numpy(), ref["sel"])
     assert_attention_close(outs[0][1], ref["out"], "repeat")
 
 
-@pytest.mark.parametrize("path", ["fused", "pipeline"])
-def test_one_workspace_serves_different_inputs(path, monkeypatch):
+def test_one_workspace_serves_different_inputs():
     """Two calls with different inputs on one workspace: the second equals a
     call on a fresh workspace (nothing of the first call is left behind)."""
-    monkeypatch.setenv("LSA_DECODE_PATH", path)
     w = small("b16_small")
     ga = to_dev(make_inputs(w, "cpu"))
     gb = to_dev(make_inputs(w.replace(seed=w.seed + 7), "cpu"))
@@ -323,8 +336,6 @@ def test_one_workspace_serves_different_inputs(path, monkeypatch):
     assert torch.equal(again.idx, fresh.idx)
     assert torch.equal(again.out.view(torch.int16), fresh.out.view(torch.int16))
     assert torch.equal(again.lse, fresh.lse)
-    if path == "fused":   # control counters at the head of the workspace are back to zero
-        assert torch.count_nonzero(shared_ws[: 4 * (3 + w.batch + w.batch * w.num_kv_heads) * 64]) == 0
 
 
 @pytest.mark.parametrize("splits", [1, 2, 5, 1000])
@@ -472,15 +483,20 @@ def test_fine_topk_matches_oracle():
 
 # ---------------------------------------------------------------- full-size workloads
 
-FULL = [("b16_32k", [0, 15], "fused"), ("b16_32k", [0, 15], "pipeline"), ("ragged", [3, 40], "fused"),
-        ("ragged", [3, 40], "pipeline"), ("c2f", [1], "pipeline"), ("mla", [2], "pipeline")]
+FULL_CHUNK = {"b16_32k": 16, "ragged": 8, "c2f": 4, "mla": 2}
 
 
-@pytest.mark.parametrize("name,reqs,path", FULL)
-def test_full_size_sampled_requests(name, reqs, path, monkeypatch):
-    """Sampled requests of the full-size workloads, checked against the
-    oracle one request at a time, on both implementations of the step."""
-    monkeypatch.setenv("LSA_DECODE_PATH", path)
+@pytest.mark.parametrize("name", ["b16_32k", "ragged", "c2f", "mla"])
+def test_full_size_every_request(name):
+    """Every request of the full-size workloads, from one call over the whole
+    batch, checked against the oracle: the oracle runs on groups of requests
+    (their pages gathered into a compact cache) so that its host copy stays
+    small."""
     w = WORKLOADS[name]
     inp = make_inputs(w, "cuda")
-    run_and_compare_step(w, inp, inp, reqs=reqs)
+    st = GpuStep(w, inp)
+    st.run()
+    check_status_clean()
+    step = FULL_CHUNK[name]
+    for r0 in range(0, w.batch, step):
+        compare_step_rows(st, w, inp, list(range(r0, min(w.batch, r0 + step))))

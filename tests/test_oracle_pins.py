@@ -486,8 +486,43 @@ def test_mla_aliased_v_equals_copied_v():
     a = oracle.decode(inp["q"], c_alias, inp["page_table"], inp["seq_lens"], **args)
     b = oracle.decode(inp["q"], c_copy, inp["page_table"], inp["seq_lens"], **args)
     assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["sel"], b["sel"])
-    o, lse = np_dense(inp, w, 1, 5, tokens=None)  # spot-check the dense path shape
-    assert o.shape == (w.dv,)
+
+
+def test_mla_decode_bruteforce_numpy():
+    """The latent cache with dk = 576 keys and dv = 512 values (the first 512
+    key dims): the selection is the top-k of numpy scores over the candidate
+    blocks, and every output head is the correctly rounded brute-force
+    softmax over the forced tokens plus the selected blocks, with values read
+    from the first dv dims (a value read with the key's width, or at the
+    wrong offset, fails here)."""
+    w = small_workloads()["mla_small"].replace(seq_lens=(3000, 1100))
+    inp = make_inputs(w, "cpu")
+    c = oracle.Cache(inp["k_cache"], None, dv=w.dv)
+    res = oracle.decode(inp["q"], c, inp["page_table"], inp["seq_lens"], num_q_heads=w.num_q_heads,
+                        k_blocks=w.k_blocks, sink=w.sink, recent=w.recent, scale=w.softmax_scale)
+    assert res["out"].shape == (w.batch, w.num_q_heads, w.dv)
+    summ, _ = oracle.summaries(c, inp["page_table"], inp["seq_lens"])
+    S = f64(summ)[:, 0]                                   # [P, 576] (one latent head)
+    b = w.block_size
+    for r in range(w.batch):
+        L = int(inp["lens"][r])
+        se = min(w.sink, L)
+        rs = max(L - w.recent, se)
+        pt = inp["page_table"][r].numpy()
+        qs = f64(bf16_bits(inp["q"][r])).sum(axis=0)     # the 64 heads share one latent head
+        cand = np.array([j for j in range(L // b) if j * b >= se and (j + 1) * b <= rs])
+        sc = S[pt[cand]] @ qs
+        order = np.lexsort((cand, -sc))
+        want = np.sort(cand[order[: w.k_blocks]])
+        got = res["sel"][r, 0]
+        assert np.array_equal(got[got >= 0], want)
+        toks = sorted(set(range(se)) | set(range(rs, L)) |
+                      {t for j in want.tolist() for t in range(j * b, (j + 1) * b)})
+        for hq in (0, 17, 40, 63):
+            o, lse = np_dense(inp, w, r, hq, toks)
+            assert o.shape == (w.dv,)
+            assert_correctly_rounded(res["out"][r, hq], o)
+            assert abs(res["lse"][r, hq] - lse) <= 1e-10 * max(1.0, abs(lse))
 
 
 def test_attend_selection_reproduces_decode_and_dense():
