@@ -54,7 +54,7 @@ class _Params(C.Structure):
     _fields_ = [("batch", C.c_int32), ("num_q_heads", C.c_int32), ("max_blocks", C.c_int32),
                 ("k_blocks", C.c_int32), ("sink", C.c_int32), ("recent", C.c_int32),
                 ("scale", C.c_double), ("c2f_candidates", C.c_int32),
-                ("c2f_tokens", C.c_int32)]
+                ("c2f_tokens", C.c_int32), ("summary_kind", C.c_int32)]
 
 
 def _load():
@@ -70,6 +70,7 @@ def _load():
             lib.orc_e4m3_to_f64.argtypes = [C.c_uint8]
             lib.orc_e4m3_to_f64.restype = C.c_double
             lib.orc_summaries.argtypes = [P, C.c_int, P, P, I, I, P, P]
+            lib.orc_quest_summaries.argtypes = [P, P, P, I, I, P, P]
             lib.orc_block_scores.argtypes = [P, P, C.c_int, P, P, P, P, P]
             lib.orc_topk.argtypes = [P, I, I, P]
             lib.orc_fine_scores.argtypes = [P, P, P, P, C.c_int, C.c_int, C.c_int64, P, P, P]
@@ -79,7 +80,7 @@ def _load():
             lib.orc_lse_merge.argtypes = [C.c_int, C.c_int, P, P, P, P]
             lib.orc_attend_selection.argtypes = [P, P, P, P, P, P, I, C.c_int, P, P]
             lib.orc_lse_merge.restype = None
-            for f in ("orc_summaries", "orc_block_scores", "orc_topk", "orc_fine_scores",
+            for f in ("orc_summaries", "orc_quest_summaries", "orc_block_scores", "orc_topk", "orc_fine_scores",
                       "orc_decode", "orc_dense", "orc_attend_tokens", "orc_attend_selection"):
                 getattr(lib, f).restype = C.c_int
             _lib = lib
@@ -148,9 +149,9 @@ class Cache:
 
 
 def _params(batch, num_q_heads, max_blocks, k_blocks=0, sink=0, recent=0, scale=1.0,
-            c2f_candidates=0, c2f_tokens=0):
+            c2f_candidates=0, c2f_tokens=0, summary_kind=0):
     return _Params(batch, num_q_heads, max_blocks, k_blocks, sink, recent, float(scale),
-                   c2f_candidates, c2f_tokens)
+                   c2f_candidates, c2f_tokens, summary_kind)
 
 
 # ---------------------------------------------------------------- formats
@@ -184,17 +185,32 @@ def summaries(cache: Cache, page_table, seq_lens, use_index_keys: bool = False):
     return out, valid.astype(bool)
 
 
+def quest_summaries(cache: Cache, page_table, seq_lens):
+    """Quest summaries [P, Hkv, 2, dk] (uint16 bf16 bits): the element-wise
+    maximum then minimum of the keys of every full block the page tables
+    reference, and the [P] mask of pages written."""
+    lib = _load()
+    pt = _np(page_table, np.int32)
+    lens = _np(seq_lens, np.int32)
+    P, H, b, dk = cache.shape
+    out = np.zeros((P, H, 2, dk), dtype=np.uint16)
+    valid = np.zeros((P,), dtype=np.uint8)
+    _check(lib.orc_quest_summaries(cache.ref, _p(pt), _p(lens), pt.shape[0], pt.shape[1], _p(out), _p(valid)))
+    return out, valid.astype(bool)
+
+
 def block_scores(q, cache: Cache, summ, page_table, seq_lens, num_q_heads, sink, recent,
-                 use_index_keys: bool = False):
+                 use_index_keys: bool = False, summary_kind: int = 0):
     """fp64 block scores [B, Hkv, max_blocks]; -inf for non-candidates.
-    ``summ`` = oracle summaries (uint16 bits) or None to compute from keys."""
+    ``summ`` = oracle summaries (uint16 bits; Quest summaries when
+    summary_kind = 1) or None to compute from keys."""
     lib = _load()
     qa = _np(q, np.uint16)
     pt = _np(page_table, np.int32)
     lens = _np(seq_lens, np.int32)
     s = None if summ is None else _np(summ, np.uint16)
     B, maxb = pt.shape
-    prm = _params(B, num_q_heads, maxb, 0, sink, recent)
+    prm = _params(B, num_q_heads, maxb, 0, sink, recent, summary_kind=summary_kind)
     out = np.empty((B, cache.shape[1], maxb), dtype=np.float64)
     _check(lib.orc_block_scores(_p(qa), cache.ref, int(use_index_keys), _p(s), _p(pt), _p(lens),
                                 C.byref(prm), _p(out)))
@@ -237,7 +253,7 @@ def fine_scores(q, index_cache: Cache, page_table, num_q_heads, r: int, h: int, 
 
 def decode(q, cache: Cache, page_table, seq_lens, *, num_q_heads, k_blocks, sink, recent, scale,
            summ=None, index_cache: Optional[Cache] = None, index_summ=None,
-           c2f_candidates: int = 0, c2f_tokens: int = 0, nthreads: int = 1):
+           c2f_candidates: int = 0, c2f_tokens: int = 0, nthreads: int = 1, summary_kind: int = 0):
     """The whole decode step.  Returns dict(out [B,Hq,dv] uint16 bf16 bits,
     lse [B,Hq] fp64, sel [B,Hkv,ksel] int32, cand [B,Hkv,C] int32 or None)."""
     lib = _load()
@@ -248,7 +264,8 @@ def decode(q, cache: Cache, page_table, seq_lens, *, num_q_heads, k_blocks, sink
     isum = None if index_summ is None else _np(index_summ, np.uint16)
     B, maxb = pt.shape
     Hkv = cache.shape[1]
-    prm = _params(B, num_q_heads, maxb, k_blocks, sink, recent, scale, c2f_candidates, c2f_tokens)
+    prm = _params(B, num_q_heads, maxb, k_blocks, sink, recent, scale, c2f_candidates, c2f_tokens,
+                  summary_kind)
     ksel = c2f_tokens if c2f_candidates > 0 else k_blocks
     out = np.zeros((B, num_q_heads, cache.dv), dtype=np.uint16)
     lse = np.zeros((B, num_q_heads), dtype=np.float64)

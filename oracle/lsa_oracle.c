@@ -32,6 +32,14 @@
  *   merge     partial results over a partition of T combine by log-sum-exp
  *             (ByteCross, Appendix A: sink call and window call merged by
  *             log-sum-exp).
+ *   Quest     an alternative summary and score (Vortex blog post, end of
+ *             "Why Long Generations Are Expensive", and the Quest listing in
+ *             "Writing an algorithm: vFlow"): each block keeps the
+ *             element-wise maximum and minimum of its keys, and a block's
+ *             score for query head g is sum_i max(q_gi * max_i, q_gi * min_i),
+ *             an upper bound on q_g . k_t for every token t of the block;
+ *             the listing's Max over the query heads of the GQA group makes
+ *             the block score.
  *
  * Readings where the pages leave a step open are stated beside each step.
  */
@@ -114,6 +122,7 @@ typedef struct {
     double scale;              /* softmax scale                            */
     int32_t c2f_candidates;    /* 0: single stage                          */
     int32_t c2f_tokens;
+    int32_t summary_kind;      /* 0: mean keys; 1: Quest min/max keys      */
 } orc_params;
 
 enum { ORC_OK = 0, ORC_BAD_PAGE = 1, ORC_BAD_ARG = 2, ORC_NOMEM = 3 };
@@ -200,6 +209,59 @@ int orc_summaries(const orc_cache *c, int use_k8, const int32_t *pt, const int32
     return ORC_OK;
 }
 
+/* Quest summaries of (page p, head h): element-wise maximum and minimum of
+ * the b keys (exact: they are key values). */
+static void quest_summary_of(const orc_cache *c, int64_t p, int h, double *mx, double *mn)
+{
+    const int b = c->block_size;
+    for (int i = 0; i < c->dk; ++i) {
+        double hi = -INFINITY, lo = INFINITY;
+        for (int t = 0; t < b; ++t) {
+            double x = key_elem(c, 0, p, h, t, i);
+            if (x > hi)
+                hi = x;
+            if (x < lo)
+                lo = x;
+        }
+        mx[i] = hi;
+        mn[i] = lo;
+    }
+}
+
+/* Quest summaries of every full block referenced by the page tables:
+ * summ [P, Hkv, 2, dk] bf16 bits, the maximum keys then the minimum keys
+ * (untouched for pages with no full block); valid: [P] (may be NULL). */
+int orc_quest_summaries(const orc_cache *c, const int32_t *pt, const int32_t *lens, int32_t batch,
+                        int32_t max_blocks, uint16_t *summ, uint8_t *valid)
+{
+    double *mx = (double *)malloc(sizeof(double) * 2 * (size_t)c->dk);
+    if (!mx)
+        return ORC_NOMEM;
+    double *mn = mx + c->dk;
+    for (int r = 0; r < batch; ++r) {
+        int64_t nfull = lens[r] / c->block_size;
+        for (int64_t j = 0; j < nfull; ++j) {
+            int64_t p = pt[(int64_t)r * max_blocks + j];
+            if (p < 0 || p >= c->num_pages) {
+                free(mx);
+                return ORC_BAD_PAGE;
+            }
+            for (int h = 0; h < c->num_kv_heads; ++h) {
+                quest_summary_of(c, p, h, mx, mn);
+                uint16_t *dst = summ + ((int64_t)p * c->num_kv_heads + h) * 2 * c->dk;
+                for (int i = 0; i < c->dk; ++i) {
+                    dst[i] = orc_f64_to_bf16(mx[i]);
+                    dst[c->dk + i] = orc_f64_to_bf16(mn[i]);
+                }
+            }
+            if (valid)
+                valid[p] = 1;
+        }
+    }
+    free(mx);
+    return ORC_OK;
+}
+
 /* ------------------------------------------------------------------ */
 /* Step: block scores                                                  */
 /* ------------------------------------------------------------------ */
@@ -225,7 +287,7 @@ static int row_scores(const uint16_t *q, const orc_cache *c, int use_k8, const u
     const int G = prm->num_q_heads / c->num_kv_heads;
     int64_t se, rs;
     forced_ranges(L, prm->sink, prm->recent, &se, &rs);
-    double *sv = (double *)malloc(sizeof(double) * (size_t)dk);
+    double *sv = (double *)malloc(sizeof(double) * 2 * (size_t)dk);
     if (!sv)
         return ORC_NOMEM;
     for (int64_t j = 0; j < prm->max_blocks; ++j) {
@@ -236,6 +298,32 @@ static int row_scores(const uint16_t *q, const orc_cache *c, int use_k8, const u
         if (p < 0 || p >= c->num_pages) {
             free(sv);
             return ORC_BAD_PAGE;
+        }
+        if (prm->summary_kind == 1) {
+            /* Quest: max over the group's heads of sum_i max(q*max, q*min) */
+            double best = -INFINITY;
+            if (summ) {
+                const uint16_t *src = summ + ((int64_t)p * c->num_kv_heads + h) * 2 * dk;
+                for (int i = 0; i < dk; ++i) {
+                    sv[i] = orc_bf16_to_f64(src[i]);
+                    sv[dk + i] = orc_bf16_to_f64(src[dk + i]);
+                }
+            } else {
+                quest_summary_of(c, p, h, sv, sv + dk);
+            }
+            for (int g = 0; g < G; ++g) {
+                const uint16_t *qg = q + ((int64_t)r * prm->num_q_heads + h * G + g) * dk;
+                double s = 0.0;
+                for (int i = 0; i < dk; ++i) {
+                    double qi = orc_bf16_to_f64(qg[i]);
+                    double a = qi * sv[i], bb = qi * sv[dk + i];
+                    s += a > bb ? a : bb;
+                }
+                if (s > best)
+                    best = s;
+            }
+            scores[j] = best;
+            continue;
         }
         load_summary(c, use_k8, summ, p, h, sv);
         double s = 0.0;

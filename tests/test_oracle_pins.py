@@ -544,3 +544,108 @@ def test_attend_selection_reproduces_decode_and_dense():
     x = oracle.attend_selection(inp["q"], c, inp["page_table"], inp["seq_lens"], junk, **args)
     y = oracle.attend_selection(inp["q"], c, inp["page_table"], inp["seq_lens"], one, **args)
     assert np.array_equal(x["out"], y["out"])
+
+
+# ---------------------------------------------------------------- Quest min/max summaries
+
+def quest_setup(lens=(1000, 333)):
+    w = small_workloads()["b16_small"].replace(batch=len(lens), seq_lens=tuple(lens), name="quest")
+    inp = make_inputs(w, "cpu")
+    return w, inp, cache_of(inp, w)
+
+
+def test_quest_summaries_are_the_blocks_max_and_min():
+    """Quest keeps each block's element-wise maximum and minimum keys
+    (Vortex blog post, end of "Why Long Generations Are Expensive"): numpy's
+    max / min over the block's tokens, exactly, for full blocks only."""
+    w, inp, c = quest_setup()
+    qs, valid = oracle.quest_summaries(c, inp["page_table"], inp["seq_lens"])
+    K = f64(bf16_bits(inp["k_cache"]))                       # [P, H, b, dk]
+    full = set()
+    for r, L in enumerate(inp["lens"]):
+        full |= set(inp["page_table"][r, : L // w.block_size].tolist())
+    assert set(np.flatnonzero(valid).tolist()) == full
+    for p in sorted(full):
+        assert np.array_equal(f64(qs[p, :, 0]), K[p].max(axis=1))
+        assert np.array_equal(f64(qs[p, :, 1]), K[p].min(axis=1))
+    assert np.all(qs[~valid] == 0)
+
+
+def test_quest_score_bounds_every_token_of_the_block():
+    """The Quest score of a block is an upper bound on q_g . k_t for every
+    query head g of the group and every token t of the block (brute force),
+    and the maximum over heads is taken: lowering one head's bound below the
+    true maximum would fail here."""
+    w, inp, c = quest_setup()
+    qs, _ = oracle.quest_summaries(c, inp["page_table"], inp["seq_lens"])
+    sc = oracle.block_scores(inp["q"], c, qs, inp["page_table"], inp["seq_lens"], w.num_q_heads, w.sink,
+                             w.recent, summary_kind=1)
+    K = f64(bf16_bits(inp["k_cache"]))
+    G, b = w.group, w.block_size
+    checked = 0
+    for r in range(w.batch):
+        pt = inp["page_table"][r].numpy()
+        for h in range(w.num_kv_heads):
+            Q = f64(bf16_bits(inp["q"][r, h * G:(h + 1) * G]))   # [G, dk]
+            for j in np.flatnonzero(np.isfinite(sc[r, h])):
+                true_max = (Q @ K[pt[j], h].T).max()                 # over heads and tokens
+                assert sc[r, h, j] >= true_max - 1e-9 * abs(true_max)
+                checked += 1
+            # forced and tail blocks are not candidates
+            L = inp["lens"][r]
+            assert np.isneginf(sc[r, h, 0]) and np.isneginf(sc[r, h, (L - 1) // b])
+    assert checked > 100
+
+
+def test_quest_score_is_tight_on_a_block_of_equal_keys():
+    """A block whose tokens all hold the same key x has max = min = x, so its
+    bound is max_g q_g . x exactly; with a query whose coordinates are all
+    positive the bound is q . max (and q . min for all negative)."""
+    w, inp, _ = quest_setup(lens=(800,))
+    b = w.block_size
+    pt = inp["page_table"][0]
+    k = inp["k_cache"].clone()
+    k[pt[5], :, :] = k[pt[5], :, :1].expand(-1, b, -1)          # block 5: one key repeated
+    inp2 = dict(inp, k_cache=k)
+    c = cache_of(inp2, w)
+    sc = oracle.block_scores(inp["q"], c, None, inp["page_table"], inp["seq_lens"], w.num_q_heads, w.sink,
+                             w.recent, summary_kind=1)
+    G = w.group
+    K = f64(bf16_bits(k))
+    for h in range(w.num_kv_heads):
+        Q = f64(bf16_bits(inp["q"][0, h * G:(h + 1) * G]))
+        assert sc[0, h, 5] == pytest.approx((Q @ K[pt[5], h, 0]).max(), rel=1e-12, abs=1e-12)
+    # a positive query scores q . max; a negative one q . min
+    q = torch.full_like(inp["q"], 0.5)
+    qs, _ = oracle.quest_summaries(c, inp["page_table"], inp["seq_lens"])
+    sp = oracle.block_scores(q, c, qs, inp["page_table"], inp["seq_lens"], w.num_q_heads, w.sink, w.recent,
+                             summary_kind=1)
+    sn = oracle.block_scores(-q, c, qs, inp["page_table"], inp["seq_lens"], w.num_q_heads, w.sink, w.recent,
+                             summary_kind=1)
+    S = f64(qs)
+    for j in (2, 7, 30):
+        for h in range(w.num_kv_heads):
+            assert sp[0, h, j] == pytest.approx(0.5 * S[pt[j], h, 0].sum(), rel=1e-12)
+            assert sn[0, h, j] == pytest.approx(-0.5 * S[pt[j], h, 1].sum(), rel=1e-12)
+
+
+def test_quest_decode_selects_the_top_bounds_and_attends_them():
+    w, inp, c = quest_setup(lens=(4096, 3001))
+    qs, _ = oracle.quest_summaries(c, inp["page_table"], inp["seq_lens"])
+    args = dict(num_q_heads=w.num_q_heads, sink=w.sink, recent=w.recent, scale=w.softmax_scale)
+    res = oracle.decode(inp["q"], c, inp["page_table"], inp["seq_lens"], k_blocks=w.k_blocks, summ=qs,
+                        summary_kind=1, **args)
+    sc = oracle.block_scores(inp["q"], c, qs, inp["page_table"], inp["seq_lens"], w.num_q_heads, w.sink,
+                             w.recent, summary_kind=1)
+    for r in range(w.batch):
+        for h in range(w.num_kv_heads):
+            cand = np.flatnonzero(np.isfinite(sc[r, h]))
+            order = np.lexsort((cand, -sc[r, h, cand]))
+            want = np.sort(cand[order[: w.k_blocks]])
+            got = res["sel"][r, h]
+            assert np.array_equal(got[got >= 0], want)
+    a = oracle.attend_selection(inp["q"], c, inp["page_table"], inp["seq_lens"], res["sel"], **args)
+    assert np.array_equal(a["out"], res["out"])
+    # the mean-key selection differs on these inputs (the two scores rank differently)
+    m = oracle.decode(inp["q"], c, inp["page_table"], inp["seq_lens"], k_blocks=w.k_blocks, **args)
+    assert not np.array_equal(m["sel"], res["sel"])
