@@ -54,7 +54,7 @@ class _Params(C.Structure):
     _fields_ = [("batch", C.c_int32), ("num_q_heads", C.c_int32), ("max_blocks", C.c_int32),
                 ("k_blocks", C.c_int32), ("sink", C.c_int32), ("recent", C.c_int32),
                 ("scale", C.c_double), ("c2f_candidates", C.c_int32),
-                ("c2f_tokens", C.c_int32), ("summary_kind", C.c_int32)]
+                ("c2f_tokens", C.c_int32), ("summary_kind", C.c_int32), ("fine_weights", C.c_void_p)]
 
 
 def _load():
@@ -149,9 +149,12 @@ class Cache:
 
 
 def _params(batch, num_q_heads, max_blocks, k_blocks=0, sink=0, recent=0, scale=1.0,
-            c2f_candidates=0, c2f_tokens=0, summary_kind=0):
+            c2f_candidates=0, c2f_tokens=0, summary_kind=0, fine_weights=None):
+    """fine_weights: a C-contiguous float32 numpy array [batch, num_q_heads]
+    (kept alive by the caller) or None."""
     return _Params(batch, num_q_heads, max_blocks, k_blocks, sink, recent, float(scale),
-                   c2f_candidates, c2f_tokens, summary_kind)
+                   c2f_candidates, c2f_tokens, summary_kind,
+                   None if fine_weights is None else fine_weights.ctypes.data)
 
 
 # ---------------------------------------------------------------- formats
@@ -235,15 +238,17 @@ def topk(scores, k: int) -> np.ndarray:
     return out.reshape(s.shape[:-1] + (k,))
 
 
-def fine_scores(q, index_cache: Cache, page_table, num_q_heads, r: int, h: int, blocks):
+def fine_scores(q, index_cache: Cache, page_table, num_q_heads, r: int, h: int, blocks, fine_weights=None):
     """fp64 FP8 rescoring of every token of ``blocks`` (request r, KV head h):
-    returns (scores, token positions)."""
+    returns (scores, token positions).  fine_weights [B, Hq]: the weighted
+    ReLU head aggregation instead of the head sum."""
     lib = _load()
     qa = _np(q, np.uint16)
     pt = _np(page_table, np.int32)
     bl = np.ascontiguousarray(np.asarray(blocks, dtype=np.int64))
     b = index_cache.shape[2]
-    prm = _params(pt.shape[0], num_q_heads, pt.shape[1])
+    fw = None if fine_weights is None else _np(fine_weights, np.float32)
+    prm = _params(pt.shape[0], num_q_heads, pt.shape[1], fine_weights=fw)
     f = np.empty((bl.shape[0] * b,), dtype=np.float64)
     t = np.empty((bl.shape[0] * b,), dtype=np.int64)
     _check(lib.orc_fine_scores(_p(qa), index_cache.ref, _p(pt), C.byref(prm), r, h, bl.shape[0],
@@ -253,7 +258,8 @@ def fine_scores(q, index_cache: Cache, page_table, num_q_heads, r: int, h: int, 
 
 def decode(q, cache: Cache, page_table, seq_lens, *, num_q_heads, k_blocks, sink, recent, scale,
            summ=None, index_cache: Optional[Cache] = None, index_summ=None,
-           c2f_candidates: int = 0, c2f_tokens: int = 0, nthreads: int = 1, summary_kind: int = 0):
+           c2f_candidates: int = 0, c2f_tokens: int = 0, nthreads: int = 1, summary_kind: int = 0,
+           fine_weights=None):
     """The whole decode step.  Returns dict(out [B,Hq,dv] uint16 bf16 bits,
     lse [B,Hq] fp64, sel [B,Hkv,ksel] int32, cand [B,Hkv,C] int32 or None)."""
     lib = _load()
@@ -264,8 +270,9 @@ def decode(q, cache: Cache, page_table, seq_lens, *, num_q_heads, k_blocks, sink
     isum = None if index_summ is None else _np(index_summ, np.uint16)
     B, maxb = pt.shape
     Hkv = cache.shape[1]
+    fw = None if fine_weights is None else _np(fine_weights, np.float32)
     prm = _params(B, num_q_heads, maxb, k_blocks, sink, recent, scale, c2f_candidates, c2f_tokens,
-                  summary_kind)
+                  summary_kind, fw)
     ksel = c2f_tokens if c2f_candidates > 0 else k_blocks
     out = np.zeros((B, num_q_heads, cache.dv), dtype=np.uint16)
     lse = np.zeros((B, num_q_heads), dtype=np.float64)

@@ -123,6 +123,8 @@ typedef struct {
     int32_t c2f_candidates;    /* 0: single stage                          */
     int32_t c2f_tokens;
     int32_t summary_kind;      /* 0: mean keys; 1: Quest min/max keys      */
+    const float *fine_weights; /* NULL, or [batch, num_q_heads] indexer
+                                  head weights of the weighted-ReLU fine score */
 } orc_params;
 
 enum { ORC_OK = 0, ORC_BAD_PAGE = 1, ORC_BAD_ARG = 2, ORC_NOMEM = 3 };
@@ -502,7 +504,11 @@ static int attend_group(const uint16_t *q, const orc_cache *c, const int32_t *pt
 /* ------------------------------------------------------------------ */
 
 /* f_t = scale_t * sum_g q_g . e4m3(k8_t) for every token of the given
- * blocks (ascending), written to f / tok (n = nblocks * b entries). */
+ * blocks (ascending), written to f / tok (n = nblocks * b entries).
+ * With head weights w (prm->fine_weights), the indexer's weighted head
+ * aggregation instead (LeanSparse, Section 5, Eq. 6, applied to the exact
+ * FP8 keys rather than their PQ centroids):
+ *   f_t = sum_g w[r, g] * max(0, q_g . k_t),  k_t = scale_t * e4m3(k8_t). */
 static int fine_scores(const uint16_t *q, const orc_cache *c, const int32_t *pt_row,
                        const orc_params *prm, int r, int h, int64_t nblocks, const int64_t *blocks,
                        double *f, int64_t *tok)
@@ -517,6 +523,22 @@ static int fine_scores(const uint16_t *q, const orc_cache *c, const int32_t *pt_
             return ORC_BAD_PAGE;
         for (int t = 0; t < b; ++t) {
             int64_t base = ((int64_t)p * c->num_kv_heads + h) * b + t;
+            if (prm->fine_weights) {
+                const double sc = (double)c->k8_scale[base];
+                double f_t = 0.0;
+                for (int g = 0; g < G; ++g) {
+                    const uint16_t *qg = q + ((int64_t)r * prm->num_q_heads + h * G + g) * dk;
+                    double d = 0.0;
+                    for (int i = 0; i < dk; ++i)
+                        d += orc_bf16_to_f64(qg[i]) * (sc * orc_e4m3_to_f64(c->k8[base * dk + i]));
+                    const double w = (double)prm->fine_weights[(int64_t)r * prm->num_q_heads + h * G + g];
+                    f_t += w * (d > 0.0 ? d : 0.0);
+                }
+                f[n] = f_t;
+                tok[n] = j * b + t;
+                ++n;
+                continue;
+            }
             double s = 0.0;
             for (int g = 0; g < G; ++g) {
                 const uint16_t *qg = q + ((int64_t)r * prm->num_q_heads + h * G + g) * dk;

@@ -649,3 +649,81 @@ def test_quest_decode_selects_the_top_bounds_and_attends_them():
     # the mean-key selection differs on these inputs (the two scores rank differently)
     m = oracle.decode(inp["q"], c, inp["page_table"], inp["seq_lens"], k_blocks=w.k_blocks, **args)
     assert not np.array_equal(m["sel"], res["sel"])
+
+
+# ---------------------------------------------------------------- weighted-ReLU fine score
+
+def wrelu_setup(positive_q=False, positive_k=False):
+    w, inp, c, ic = c2f_setup(seq_lens=(2000, 1500), recent=0, c2f_candidates=6, c2f_tokens=100)
+    if positive_q:
+        inp["q"] = inp["q"].abs()
+    if positive_k:
+        k8 = inp["idx_keys"].view(torch.float8_e4m3fn).float().abs().to(torch.float8_e4m3fn)
+        inp["idx_keys"] = k8.view(torch.uint8)
+        ic = oracle.Cache(None, None, k8=inp["idx_keys"], k8_scale=inp["idx_scale"])
+    return w, inp, ic
+
+
+def test_weighted_relu_reduces_to_the_head_sum_when_every_dot_is_positive():
+    """LeanSparse Eq. 6's aggregation on exact keys, sum_g w_g ReLU(q_g . k_t):
+    with all-positive queries and keys every dot is positive, so with unit
+    weights it equals the plain head-sum fine score (scale_t sum_g q_g .
+    e4m3(k8_t)), which the coarse-score pin ties to the summaries."""
+    w, inp, ic = wrelu_setup(positive_q=True, positive_k=True)
+    ones = np.ones((w.batch, w.num_q_heads), dtype=np.float32)
+    blocks = np.array([3, 7, 11], dtype=np.int64)
+    for r in range(w.batch):
+        f1, t1 = oracle.fine_scores(inp["q"], ic, inp["page_table"], w.num_q_heads, r, 0, blocks, fine_weights=ones)
+        f0, t0 = oracle.fine_scores(inp["q"], ic, inp["page_table"], w.num_q_heads, r, 0, blocks)
+        assert np.array_equal(t1, t0)
+        assert np.all(f0 > 0)
+        assert np.allclose(f1, f0, rtol=1e-12, atol=0)
+
+
+def test_weighted_relu_negative_dots_contribute_nothing():
+    """All-negative queries against all-positive keys: every dot is below
+    zero, every head's ReLU is 0, so every fine score is 0 and the token
+    top-k (ties to the lower token) takes the first candidate tokens."""
+    w, inp, ic = wrelu_setup(positive_k=True)
+    inp["q"] = -inp["q"].abs()
+    wts = np.random.default_rng(3).uniform(0.1, 1.0, (w.batch, w.num_q_heads)).astype(np.float32)
+    f, t = oracle.fine_scores(inp["q"], ic, inp["page_table"], w.num_q_heads, 0, 0, np.array([2, 9], np.int64),
+                              fine_weights=wts)
+    assert np.all(f == 0.0)
+    res = oracle.decode(inp["q"], oracle.Cache(inp["k_cache"], inp["v_cache"]), inp["page_table"], inp["seq_lens"],
+                        num_q_heads=w.num_q_heads, k_blocks=0, sink=0, recent=0, scale=w.softmax_scale,
+                        index_cache=ic, c2f_candidates=w.c2f_candidates, c2f_tokens=w.c2f_tokens,
+                        fine_weights=wts)
+    for r in range(w.batch):
+        cand = np.sort(res["cand"][r, 0][res["cand"][r, 0] >= 0])
+        toks = np.concatenate([np.arange(j * w.block_size, (j + 1) * w.block_size) for j in cand])
+        assert np.array_equal(res["sel"][r, 0], np.sort(toks)[: w.c2f_tokens])
+
+
+def test_weighted_relu_is_linear_in_the_weights_and_each_weight_picks_its_head():
+    """f(a w1 + b w2) = a f(w1) + b f(w2); a weight on head g alone gives
+    w_g ReLU(q_g . k_t) (numpy over the decoded keys), so a weight applied
+    to the wrong head, or a ReLU taken after the sum, fails here."""
+    w, inp, ic = wrelu_setup()
+    rng = np.random.default_rng(5)
+    # weights on a 1/256 grid: 2 w1 + 3 w2 is then exact in float32
+    w1 = (rng.integers(0, 256, (w.batch, w.num_q_heads)) / 256.0).astype(np.float32)
+    w2 = (rng.integers(0, 256, (w.batch, w.num_q_heads)) / 256.0).astype(np.float32)
+    blocks = np.array([1, 4], dtype=np.int64)
+    args = (inp["q"], ic, inp["page_table"], w.num_q_heads, 1, 0, blocks)
+    fa, _ = oracle.fine_scores(*args, fine_weights=w1)
+    fb, _ = oracle.fine_scores(*args, fine_weights=w2)
+    fab, _ = oracle.fine_scores(*args, fine_weights=(2 * w1 + 3 * w2).astype(np.float32))
+    assert np.allclose(fab, 2 * fa + 3 * fb, rtol=1e-10, atol=1e-9)
+    K8 = inp["idx_keys"].view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    S = inp["idx_scale"].numpy().astype(np.float64)
+    b = w.block_size
+    pt = inp["page_table"][1].numpy()
+    toks = np.concatenate([np.arange(j * b, (j + 1) * b) for j in blocks])
+    kt = K8[pt[toks // b], 0, toks % b] * S[pt[toks // b], 0, toks % b][:, None]
+    for g in (0, 17, 63):
+        one = np.zeros((w.batch, w.num_q_heads), dtype=np.float32)
+        one[1, g] = 2.5
+        fg, _ = oracle.fine_scores(*args, fine_weights=one)
+        qg = f64(bf16_bits(inp["q"][1, g]))
+        assert np.allclose(fg, 2.5 * np.maximum(kt @ qg, 0.0), rtol=1e-12, atol=1e-12)
