@@ -127,16 +127,23 @@ class Instance:
         B, Hkv = w.batch, w.num_kv_heads
         self.cache = L.make_cache(g["k_cache"], g["v_cache"])
         self.icache = None
-        self.summ = torch.zeros((g["num_pages"], Hkv, w.dk), dtype=torch.bfloat16, device=dev)
+        if w.summary_kind == 1:
+            self.summ = torch.zeros((g["num_pages"], Hkv, 2, w.dk), dtype=torch.bfloat16, device=dev)
+        else:
+            self.summ = torch.zeros((g["num_pages"], Hkv, w.dk), dtype=torch.bfloat16, device=dev)
         if w.c2f_candidates > 0:
             self.icache = L.make_cache(g["idx_keys"], None, k_scale=g["idx_scale"])
             L.lsa_build_summaries(self.icache, g["page_table"], g["seq_lens"], self.summ)
             nsel = w.c2f_tokens
+        elif w.summary_kind == 1:
+            L.lsa_build_minmax_summaries(self.cache, g["page_table"], g["seq_lens"], self.summ)
+            nsel = w.k_blocks
         else:
             L.lsa_build_summaries(self.cache, g["page_table"], g["seq_lens"], self.summ)
             nsel = w.k_blocks
         self.params = L.make_params(B, w.num_q_heads, g["max_blocks"], w.k_blocks, w.sink, w.recent,
-                                    w.softmax_scale, w.c2f_candidates, w.c2f_tokens)
+                                    w.softmax_scale, w.c2f_candidates, w.c2f_tokens,
+                                    summary_kind=w.summary_kind, fine_head_weights=g.get("fine_weights"))
         self.ws = torch.zeros(max(16, L.lsa_decode_step_workspace_size(self.cache, self.params)),
                               dtype=torch.uint8, device=dev)
         self.idx = torch.empty((B, Hkv, max(1, nsel)), dtype=torch.int32, device=dev)
@@ -441,8 +448,12 @@ def cpu_baseline(w, budget_s: float = 12.0):
     if w.c2f_candidates > 0:
         ic = oracle.Cache(None, None, k8=inp["idx_keys"], k8_scale=inp["idx_scale"])
         isumm, _ = oracle.summaries(ic, inp["page_table"], inp["seq_lens"], use_index_keys=True)
-        kw.update(index_cache=ic, index_summ=isumm, c2f_candidates=w.c2f_candidates, c2f_tokens=w.c2f_tokens)
+        kw.update(index_cache=ic, index_summ=isumm, c2f_candidates=w.c2f_candidates, c2f_tokens=w.c2f_tokens,
+                  fine_weights=inp.get("fine_weights"))
         summ = None
+    elif w.summary_kind == 1:
+        summ, _ = oracle.quest_summaries(c, inp["page_table"], inp["seq_lens"])
+        kw.update(summary_kind=1)
     else:
         summ, _ = oracle.summaries(c, inp["page_table"], inp["seq_lens"])
 

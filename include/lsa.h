@@ -71,6 +71,11 @@ typedef enum lsa_status {
     LSA_ERR_NAN = 7           /* device: a NaN score was skipped                */
 } lsa_status;
 
+typedef enum lsa_summary_kind {
+    LSA_SUMMARY_MEAN = 0,     /* one mean key per block: [P, Hkv, dk]           */
+    LSA_SUMMARY_MINMAX = 1    /* Quest: max and min keys: [P, Hkv, 2, dk]       */
+} lsa_summary_kind;
+
 typedef enum lsa_key_format {
     LSA_KEYS_BF16 = 0,        /* keys are bf16                                  */
     LSA_KEYS_E4M3 = 1         /* keys are FP8 e4m3 bytes + one fp32 scale/token */
@@ -116,6 +121,14 @@ typedef struct lsa_params {
     int32_t c2f_candidates;   /* > 0: coarse-to-fine with C candidate blocks    */
     int32_t c2f_tokens;       /* tokens kept by the fine pass                   */
     int32_t num_splits;       /* split-K parts per (request, KV head); 0 = auto */
+    int32_t summary_kind;     /* lsa_summary_kind of the summaries passed in    */
+    /* Coarse-to-fine fine score.  NULL: the head sum of dot products (as for
+     * block scores).  Else device fp32 [batch, num_q_heads] indexer head
+     * weights w, and the fine score of token t is the indexer's weighted
+     * head aggregation sum_g w[r,g] * max(0, q[r,g,:] . k_t), k_t = scale_t
+     * * e4m3(k8_t) (LeanSparse, Section 5, Eq. 6, on the exact keys);
+     * needs 64 query heads per KV head. */
+    const float *fine_head_weights;
 } lsa_params;
 
 /* Status and errors ------------------------------------------------------ */
@@ -145,6 +158,20 @@ lsa_status lsa_build_summaries(const lsa_cache *cache, const int32_t *page_table
                                const int32_t *seq_lens, int32_t batch, int32_t max_blocks,
                                void *summaries, lsa_stream_t stream);
 
+/* Quest's block summaries (Vortex blog post, end of "Why Long Generations
+ * Are Expensive": each block keeps the element-wise maximum and minimum of
+ * its keys; the Quest listing in "Writing an algorithm: vFlow"):
+ *   summaries[((p*Hkv + h)*2 + 0)*dk + i] = max_t K[p,h,t,i]
+ *   summaries[((p*Hkv + h)*2 + 1)*dk + i] = min_t K[p,h,t,i]
+ * for every full block referenced by the page tables (exact: bf16 values).
+ *   summaries [num_pages, Hkv, 2, dk] bf16 device, caller-allocated.
+ * Scored with lsa_params.summary_kind = LSA_SUMMARY_MINMAX.  bf16 keys only
+ * (LSA_ERR_UNSUPPORTED for e4m3).  Other arguments and errors as
+ * lsa_build_summaries. */
+lsa_status lsa_build_minmax_summaries(const lsa_cache *cache, const int32_t *page_table,
+                                      const int32_t *seq_lens, int32_t batch, int32_t max_blocks,
+                                      void *summaries, lsa_stream_t stream);
+
 /* Appends one token per request: writes k_new[r, h, :] and v_new[r, h, :]
  * (bf16 [batch, Hkv, dk] / [batch, Hkv, dv], device) into slot L % b of page
  * page_table[r, L / b] with L = seq_lens[r], then increments seq_lens[r].
@@ -156,6 +183,13 @@ lsa_status lsa_append_block(const lsa_cache *cache, const void *k_new, const voi
                             const int32_t *page_table, int32_t *seq_lens, int32_t batch,
                             int32_t max_blocks, void *summaries, lsa_stream_t stream);
 
+/* lsa_append_block for Quest summaries: when a block fills, its maximum and
+ * minimum keys are written ([num_pages, Hkv, 2, dk], as
+ * lsa_build_minmax_summaries). */
+lsa_status lsa_append_block_minmax(const lsa_cache *cache, const void *k_new, const void *v_new,
+                                   const int32_t *page_table, int32_t *seq_lens, int32_t batch,
+                                   int32_t max_blocks, void *summaries, lsa_stream_t stream);
+
 /* Step 2: scores ---------------------------------------------------------- */
 
 /* scores[(r*Hkv + h)*max_blocks + j] = sum_{g in group(h)} q[r,g,:] .
@@ -164,7 +198,13 @@ lsa_status lsa_append_block(const lsa_cache *cache, const void *k_new, const voi
  *   q [batch, Hq, dk] bf16 device, contiguous;  scores fp32 device.
  * `cache` supplies the geometry (num_kv_heads, block_size, dk, num_pages).
  * Supported: dk in {64, 128, 256, 576} with Hkv*dk/8 lanes tiling a warp or
- * Hkv == 1.  Otherwise LSA_ERR_UNSUPPORTED. */
+ * Hkv == 1.  Otherwise LSA_ERR_UNSUPPORTED.
+ * With params->summary_kind = LSA_SUMMARY_MINMAX the summaries are Quest's
+ * ([num_pages, Hkv, 2, dk]) and the score of block j is the Quest bound
+ *   max_{g in group(h)} sum_i max(q[r,g,i]*max_ji, q[r,g,i]*min_ji),
+ * an upper bound on q_g . k_t for every token t of the block (the listing's
+ * Max over heads of Sum over dims); supported for dk in {64, 128}, Hkv and
+ * the group size in {1, 2, 4, 8}. */
 lsa_status lsa_score(const void *q, const lsa_cache *cache, const void *summaries,
                      const int32_t *page_table, const int32_t *seq_lens, const lsa_params *params,
                      float *scores, lsa_stream_t stream);
@@ -184,7 +224,8 @@ lsa_status lsa_topk(const float *scores, const int32_t *num_cols, int32_t rows, 
 /* Coarse-to-fine fine pass: for every token t of the candidate blocks
  * cand[r, h, :] (ascending, -1 padded, c2f_candidates per row) of request r,
  *   f_t = scale_t * sum_{g in group(h)} q[r,g,:] . e4m3(k8_t)
- * in fp32; keeps the c2f_tokens best by (f descending, token ascending).
+ * in fp32 (or the weighted-ReLU score when params->fine_head_weights is
+ * set); keeps the c2f_tokens best by (f descending, token ascending).
  * tok_idx [batch, Hkv, c2f_tokens] int32 device: token positions, ascending,
  * -1 padded.  index_cache: an LSA_KEYS_E4M3 cache with dk = 128. */
 lsa_status lsa_fine_topk(const void *q, const lsa_cache *index_cache, const int32_t *page_table,

@@ -60,6 +60,17 @@ bool mult16(int64_t elems, int esz) { return ((elems * esz) & 15) == 0; }
 
 size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
 
+// CTAs per SM of the tcgen05 attention kernel for a shape (cached; the
+// occupancy query is a host call).
+int umma_ctas_per_sm(int dk, int dv, bool alias)
+{
+    static int cache[3] = {-1, -1, -1};
+    const int idx = dk == 128 ? 0 : (alias ? 1 : 2);
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (cache[idx] < 0) cache[idx] = attention_umma_ctas_per_sm(dk, dv, alias);
+    return cache[idx];
+}
+
 // Validates a cache descriptor and converts it to the kernels' view.
 lsa_status make_view(const lsa_cache *c, bool need_values, CacheView *v)
 {
@@ -113,10 +124,24 @@ lsa_status check_params(const lsa_params *p, const CacheView &v)
     if (p->k_blocks < 0 || p->sink_tokens < 0 || p->recent_tokens < 0) return LSA_ERR_INVALID_ARG;
     if (p->c2f_candidates < 0 || p->c2f_tokens < 0 || p->num_splits < 0) return LSA_ERR_INVALID_ARG;
     if (p->batch > 65535 || (int64_t)p->max_blocks * v.b > INT32_MAX) return LSA_ERR_INVALID_ARG;
+    if (p->summary_kind != LSA_SUMMARY_MEAN && p->summary_kind != LSA_SUMMARY_MINMAX) return LSA_ERR_INVALID_ARG;
     return LSA_OK;
 }
 
 lsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LSA_OK : LSA_ERR_CUDA; }
+
+// Bounded waits give up after this many SM clock cycles (about a second
+// by default).  LSA_SPIN_BUDGET (environment, cycles) overrides it; tests set
+// a short budget to make a wait run out.
+long long spin_budget()
+{
+    const char *e = getenv("LSA_SPIN_BUDGET");
+    if (e && *e) {
+        const long long v = strtoll(e, nullptr, 10);
+        if (v > 0) return v;
+    }
+    return kSpinBudget;
+}
 
 float scale_of(const lsa_params *p, int dk)
 {
@@ -140,6 +165,8 @@ lsa_status check_decode_args(const void *q, const int32_t *page_table, const int
 struct AttnPlan {
     int nsub, splits, items_per_split;
     int tc_group;          // > 0: tensor-core kernel with this many heads per CTA
+    bool umma;             // tcgen05 kernel for groups of 64 heads, one tile of 128 tokens per CTA
+    bool umma_merge;       // ... merging the row's tiles itself (every CTA resident at once)
     bool flat;             // even split of every row's items over the GPU (attention_flat.cu)
     int fl_ns, fl_ctas, fl_parts;
     int64_t fl_total;
@@ -151,8 +178,38 @@ lsa_status plan_attention(const CacheView &v, const lsa_params *p, bool token_mo
     const int G = p->num_q_heads / v.hkv;
     int gs = 0;
     if (v.b % kChunk != 0) return LSA_ERR_UNSUPPORTED;
+    memset(pl, 0, sizeof *pl);
     const char *path = getenv("LSA_ATTENTION_PATH");
     const bool allow_tc = !(path && strcmp(path, "cuda_core") == 0);
+    pl->umma = allow_tc && attention_umma_supported(v.dk, v.dv, G, v.v_alias != 0);
+    if (pl->umma) {
+        // one CTA per 128-token tile of a row: the tiles are the split-K
+        // parts (an explicit split count does not change them)
+        const int nsel = token_mode ? p->c2f_tokens : p->k_blocks;
+        const int items = attention_items_max(p->sink_tokens, p->recent_tokens, v.b, nsel, token_mode);
+        const int ipt = attention_umma_items_per_tile();
+        pl->tc_group = 0;
+        pl->flat = false;
+        pl->nsub = 1;
+        pl->fl_ns = pl->fl_ctas = pl->fl_parts = 0;
+        pl->fl_total = 0;
+        pl->items_per_split = ipt;
+        pl->splits = std::max(1, (items + ipt - 1) / ipt);
+        pl->ws_bytes = 0;
+        pl->umma_merge = false;
+        const int64_t rows = (int64_t)p->batch * v.hkv;
+        if (pl->splits > 1) {
+            const size_t rowsq = (size_t)p->batch * p->num_q_heads * pl->splits;
+            pl->ws_bytes = round_up(rowsq * v.dv * sizeof(float)) + round_up(rowsq * sizeof(float));
+            // the tiles merge their row themselves when the whole grid is
+            // resident at once (their wait for the row's other tiles then
+            // always ends); otherwise the merge kernel does it
+            const int per_sm = umma_ctas_per_sm(v.dk, v.dv, v.v_alias != 0);
+            pl->umma_merge = per_sm > 0 && (int64_t)pl->splits * rows <= (int64_t)per_sm * sm_count();
+            if (pl->umma_merge) pl->ws_bytes += round_up(2 * (size_t)rows * sizeof(uint32_t));
+        }
+        return rows > 65535 ? LSA_ERR_UNSUPPORTED : LSA_OK;
+    }
     pl->tc_group = allow_tc ? attention_tc_group(v.dk, v.dv, G, v.v_alias != 0, token_mode, v) : 0;
     if (pl->tc_group > 0) {
         gs = pl->tc_group;
@@ -259,7 +316,7 @@ lsa_status run_attention(const void *q, const CacheView &v, const int32_t *pt, c
     a.out = static_cast<uint16_t *>(out);
     a.lse = lse;
     a.status = status_word();
-    a.spin_budget = kSpinBudget;
+    a.spin_budget = spin_budget();
     if (sel_scores && !pl.flat) return LSA_ERR_UNSUPPORTED;
     if (pl.flat) {
         a.sel_scores = sel_scores;
@@ -289,11 +346,19 @@ lsa_status run_attention(const void *q, const CacheView &v, const int32_t *pt, c
         a.o_part = reinterpret_cast<float *>(ws);
         a.lse_part = reinterpret_cast<float *>(ws + round_up(rowsq * v.dv * sizeof(float)));
     }
+    if (pl.umma_merge) {
+        a.merge_in_kernel = 1;
+        a.mrg_arrive = reinterpret_cast<uint32_t *>(ws + round_up(rowsq * v.dv * sizeof(float)) +
+                                                    round_up(rowsq * sizeof(float)));
+        a.mrg_done = a.mrg_arrive + (size_t)p->batch * v.hkv;
+    }
     bool unsup = false;
-    cudaError_t e = pl.tc_group > 0 ? launch_attention_tc(a, pl.tc_group, st, &unsup) : launch_attention(a, st, &unsup);
+    cudaError_t e = pl.umma           ? launch_attention_umma(a, st, &unsup)
+                    : pl.tc_group > 0 ? launch_attention_tc(a, pl.tc_group, st, &unsup)
+                                      : launch_attention(a, st, &unsup);
     if (unsup) return LSA_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return LSA_ERR_CUDA;
-    if (pl.splits > 1) {
+    if (pl.splits > 1 && !pl.umma_merge) {
         MergeArgs m;
         m.o_part = a.o_part;
         m.lse_part = a.lse_part;
@@ -310,8 +375,16 @@ lsa_status run_attention(const void *q, const CacheView &v, const int32_t *pt, c
 
 // Workspace of the decode step: [scores | selection | c2f extras | attention].
 struct StepLayout {
-    size_t scores, sel, cand, fine, attn, total;
+    size_t scores, sel, cand, fine, ctrl, attn, total;
 };
+
+// The coarse-to-fine step as three launches: the coarse kernel's last CTA
+// per request selects the candidates, the fine kernel's the tokens.
+bool c2f_fused(const CacheView &iv, const lsa_params *p)
+{
+    return iv.dk == 128 && iv.hkv == 1 && iv.b <= 64 && p->max_blocks <= 8192 && p->c2f_tokens > 0 &&
+           (int64_t)p->c2f_candidates * iv.b <= 16384;
+}
 
 lsa_status step_layout(const CacheView &v, const CacheView *iv, const lsa_params *p, StepLayout *L)
 {
@@ -325,8 +398,10 @@ lsa_status step_layout(const CacheView &v, const CacheView *iv, const lsa_params
     L->sel = round_up(rows * (size_t)(c2f ? p->c2f_tokens : p->k_blocks) * sizeof(int32_t));
     L->cand = c2f ? round_up(rows * (size_t)p->c2f_candidates * sizeof(int32_t)) : 0;
     L->fine = c2f ? round_up(rows * (size_t)p->c2f_candidates * sv.b * sizeof(float)) : 0;
+    // per request: coarse CTAs done, candidates ready, fine CTAs done
+    L->ctrl = c2f ? round_up(3 * (size_t)p->batch * sizeof(uint32_t)) : 0;
     L->attn = pl.ws_bytes;
-    L->total = L->scores + L->sel + L->cand + L->fine + L->attn;
+    L->total = L->scores + L->sel + L->cand + L->fine + L->ctrl + L->attn;
     return LSA_OK;
 }
 
@@ -376,12 +451,18 @@ lsa_status lsa_get_device_status(uint32_t *flags, int clear)
     return LSA_OK;
 }
 
-lsa_status lsa_build_summaries(const lsa_cache *cache, const int32_t *page_table, const int32_t *seq_lens,
-                               int32_t batch, int32_t max_blocks, void *summaries, lsa_stream_t stream)
+}  // extern "C"
+
+namespace lsa {
+namespace {
+
+lsa_status build_summaries(const lsa_cache *cache, const int32_t *page_table, const int32_t *seq_lens,
+                           int32_t batch, int32_t max_blocks, void *summaries, lsa_stream_t stream, bool quest)
 {
     CacheView v;
     lsa_status rc = make_view(cache, false, &v);
     if (rc != LSA_OK) return rc;
+    if (quest && v.e4m3) return LSA_ERR_UNSUPPORTED;
     if (batch < 0 || max_blocks < 0) return LSA_ERR_INVALID_ARG;
     if (batch == 0 || max_blocks == 0) return LSA_OK;
     if (!page_table || !seq_lens || !summaries || !aligned16(summaries)) return LSA_ERR_INVALID_ARG;
@@ -394,12 +475,12 @@ lsa_status lsa_build_summaries(const lsa_cache *cache, const int32_t *page_table
     a.max_blocks = max_blocks;
     a.summ = static_cast<uint16_t *>(summaries);
     a.status = status_word();
-    return from_cuda(launch_build_summaries(a, reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_build_summaries(a, reinterpret_cast<cudaStream_t>(stream), quest));
 }
 
-lsa_status lsa_append_block(const lsa_cache *cache, const void *k_new, const void *v_new,
-                            const int32_t *page_table, int32_t *seq_lens, int32_t batch, int32_t max_blocks,
-                            void *summaries, lsa_stream_t stream)
+lsa_status append_block(const lsa_cache *cache, const void *k_new, const void *v_new, const int32_t *page_table,
+                        int32_t *seq_lens, int32_t batch, int32_t max_blocks, void *summaries, lsa_stream_t stream,
+                        bool quest)
 {
     CacheView v;
     lsa_status rc = make_view(cache, cache && cache->key_format == LSA_KEYS_BF16, &v);
@@ -422,9 +503,52 @@ lsa_status lsa_append_block(const lsa_cache *cache, const void *k_new, const voi
     a.v_new = static_cast<const uint16_t *>(v_new);
     a.status = status_word();
     bool unsup = false;
-    cudaError_t e = launch_append(a, reinterpret_cast<cudaStream_t>(stream), &unsup);
+    cudaError_t e = launch_append(a, reinterpret_cast<cudaStream_t>(stream), quest, &unsup);
     if (unsup) return LSA_ERR_UNSUPPORTED;
     return from_cuda(e);
+}
+
+// Block scores with the kernel the summaries call for.
+cudaError_t launch_scores(const ScoreArgs &s, int summary_kind, cudaStream_t st, bool *unsup)
+{
+    return summary_kind == LSA_SUMMARY_MINMAX ? launch_score_quest(s, st, unsup) : launch_score(s, st, unsup);
+}
+
+bool scores_supported(const CacheView &v, const lsa_params *p)
+{
+    return p->summary_kind == LSA_SUMMARY_MINMAX ? score_quest_supported(v.dk, v.hkv, p->num_q_heads / v.hkv)
+                                                 : score_supported(v.dk, v.hkv);
+}
+
+}  // namespace
+}  // namespace lsa
+
+extern "C" {
+
+lsa_status lsa_build_summaries(const lsa_cache *cache, const int32_t *page_table, const int32_t *seq_lens,
+                               int32_t batch, int32_t max_blocks, void *summaries, lsa_stream_t stream)
+{
+    return build_summaries(cache, page_table, seq_lens, batch, max_blocks, summaries, stream, false);
+}
+
+lsa_status lsa_build_minmax_summaries(const lsa_cache *cache, const int32_t *page_table, const int32_t *seq_lens,
+                                      int32_t batch, int32_t max_blocks, void *summaries, lsa_stream_t stream)
+{
+    return build_summaries(cache, page_table, seq_lens, batch, max_blocks, summaries, stream, true);
+}
+
+lsa_status lsa_append_block(const lsa_cache *cache, const void *k_new, const void *v_new,
+                            const int32_t *page_table, int32_t *seq_lens, int32_t batch, int32_t max_blocks,
+                            void *summaries, lsa_stream_t stream)
+{
+    return append_block(cache, k_new, v_new, page_table, seq_lens, batch, max_blocks, summaries, stream, false);
+}
+
+lsa_status lsa_append_block_minmax(const lsa_cache *cache, const void *k_new, const void *v_new,
+                                   const int32_t *page_table, int32_t *seq_lens, int32_t batch, int32_t max_blocks,
+                                   void *summaries, lsa_stream_t stream)
+{
+    return append_block(cache, k_new, v_new, page_table, seq_lens, batch, max_blocks, summaries, stream, true);
 }
 
 lsa_status lsa_score(const void *q, const lsa_cache *cache, const void *summaries, const int32_t *page_table,
@@ -437,8 +561,10 @@ lsa_status lsa_score(const void *q, const lsa_cache *cache, const void *summarie
     if (params->batch == 0) return LSA_OK;
     if (!q || !summaries || !page_table || !seq_lens || !scores || !aligned16(q) || !aligned16(summaries))
         return LSA_ERR_INVALID_ARG;
-    if (!score_supported(v.dk, v.hkv)) return LSA_ERR_UNSUPPORTED;
+    if (!scores_supported(v, params)) return LSA_ERR_UNSUPPORTED;
+    if (params->summary_kind == LSA_SUMMARY_MINMAX && v.e4m3) return LSA_ERR_UNSUPPORTED;
     ScoreArgs a;
+    memset(&a, 0, sizeof a);
     a.q = static_cast<const uint16_t *>(q);
     a.summ = static_cast<const uint16_t *>(summaries);
     a.pt = page_table;
@@ -456,7 +582,7 @@ lsa_status lsa_score(const void *q, const lsa_cache *cache, const void *summarie
     a.scores = scores;
     a.status = status_word();
     bool unsup = false;
-    cudaError_t e = launch_score(a, reinterpret_cast<cudaStream_t>(stream), &unsup);
+    cudaError_t e = launch_scores(a, params->summary_kind, reinterpret_cast<cudaStream_t>(stream), &unsup);
     if (unsup) return LSA_ERR_UNSUPPORTED;
     return from_cuda(e);
 }
@@ -500,6 +626,7 @@ lsa_status lsa_fine_topk(const void *q, const lsa_cache *index_cache, const int3
     if (!workspace || workspace_bytes < need) return LSA_ERR_WORKSPACE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     FineArgs f;
+    memset(&f, 0, sizeof f);
     f.q = static_cast<const uint16_t *>(q);
     f.ic = iv;
     f.pt = page_table;
@@ -511,6 +638,7 @@ lsa_status lsa_fine_topk(const void *q, const lsa_cache *index_cache, const int3
     f.ncand = params->c2f_candidates;
     f.fscores = static_cast<float *>(workspace);
     f.status = status_word();
+    f.weights = params->fine_head_weights;
     bool unsup = false;
     cudaError_t e = launch_fine_scores(f, st, &unsup);
     if (unsup) return LSA_ERR_UNSUPPORTED;
@@ -591,19 +719,21 @@ lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *su
     StepLayout L;
     if ((rc = step_layout(v, &iv, params, &L)) != LSA_OK) return rc;
     if (L.total > 0 && (!workspace || workspace_bytes < L.total)) return LSA_ERR_WORKSPACE;
-    if (!score_supported(iv.dk, iv.hkv)) return LSA_ERR_UNSUPPORTED;
+    if (!scores_supported(iv, params)) return LSA_ERR_UNSUPPORTED;
+    if (c2f && params->summary_kind != LSA_SUMMARY_MEAN) return LSA_ERR_UNSUPPORTED;
     if ((int64_t)params->max_blocks > topk_max_cols()) return LSA_ERR_UNSUPPORTED;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     float *scores = reinterpret_cast<float *>(ws);
     int32_t *sel = idx_out ? idx_out : reinterpret_cast<int32_t *>(ws + L.scores);
-    uint8_t *ws_attn = ws + L.scores + L.sel + L.cand + L.fine;
+    uint8_t *ws_attn = ws + L.scores + L.sel + L.cand + L.fine + L.ctrl;
     uint32_t *status = status_word();
     const size_t rows = (size_t)params->batch * iv.hkv;
 
     // coarse (or only) stage: block scores against the summaries
     ScoreArgs s;
+    memset(&s, 0, sizeof s);
     s.q = static_cast<const uint16_t *>(q);
     s.summ = static_cast<const uint16_t *>(summaries);
     s.pt = page_table;
@@ -620,8 +750,17 @@ lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *su
     s.chunk = score_chunk(params->batch, params->max_blocks, sm_count());
     s.scores = scores;
     s.status = status;
+    int32_t *cand = reinterpret_cast<int32_t *>(ws + L.scores + L.sel);
+    uint32_t *ctrl = reinterpret_cast<uint32_t *>(ws + L.scores + L.sel + L.cand + L.fine);
+    const bool fused = c2f && c2f_fused(iv, params);
+    if (fused) {
+        s.sel_k = params->c2f_candidates;
+        s.sel_idx = cand;
+        s.cnt = ctrl;
+        s.ready = ctrl + params->batch;
+    }
     bool unsup = false;
-    cudaError_t e = launch_score(s, st, &unsup);
+    cudaError_t e = launch_scores(s, params->summary_kind, st, &unsup);
     if (unsup) return LSA_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return LSA_ERR_CUDA;
 
@@ -647,8 +786,38 @@ lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *su
         return run_attention(q, v, page_table, seq_lens, params->k_blocks > 0 ? sel : nullptr, params, false,
                              out, lse, ws_attn, L.attn, st);
     }
-    // coarse-to-fine: top-C candidate blocks, exact FP8 rescoring, token top-k
-    int32_t *cand = reinterpret_cast<int32_t *>(ws + L.scores + L.sel);
+    if (fused) {
+        // the fine kernel waits for each request's candidates and selects
+        // its tokens; then attention over them
+        FineArgs f;
+        memset(&f, 0, sizeof f);
+        f.q = static_cast<const uint16_t *>(q);
+        f.ic = iv;
+        f.pt = page_table;
+        f.lens = seq_lens;
+        f.cand = cand;
+        f.batch = params->batch;
+        f.hq = params->num_q_heads;
+        f.max_blocks = params->max_blocks;
+        f.ncand = params->c2f_candidates;
+        f.fscores = reinterpret_cast<float *>(ws + L.scores + L.sel + L.cand);
+        f.status = status;
+        f.tok_k = params->c2f_tokens;
+        f.tok_idx = sel;
+        f.cnt = ctrl + 2 * params->batch;
+        f.ready = ctrl + params->batch;
+        f.spin_budget = spin_budget();
+        f.weights = params->fine_head_weights;
+        if (f.tok_k > 0) {
+            e = launch_fine_scores(f, st, &unsup);
+            if (unsup) return LSA_ERR_UNSUPPORTED;
+            if (e != cudaSuccess) return LSA_ERR_CUDA;
+        }
+        return run_attention(q, v, page_table, seq_lens, params->c2f_tokens > 0 ? sel : nullptr, params, true, out,
+                             lse, ws_attn, L.attn, st);
+    }
+    // coarse-to-fine in separate stages: top-C candidate blocks, exact FP8
+    // rescoring, token top-k
     t.k = params->c2f_candidates;
     t.idx = cand;
     e = launch_topk(t, st, &unsup);
@@ -695,7 +864,7 @@ ScratchUse g_static_use[kMaxDevices] = {};
 bool same_plan(const AttnPlan &a, const AttnPlan &b)
 {
     return a.nsub == b.nsub && a.splits == b.splits && a.items_per_split == b.items_per_split &&
-           a.tc_group == b.tc_group && a.flat == b.flat && a.fl_ns == b.fl_ns && a.fl_ctas == b.fl_ctas &&
+           a.tc_group == b.tc_group && a.umma == b.umma && a.umma_merge == b.umma_merge && a.flat == b.flat && a.fl_ns == b.fl_ns && a.fl_ctas == b.fl_ctas &&
            a.fl_parts == b.fl_parts && a.fl_total == b.fl_total && a.ws_bytes == b.ws_bytes;
 }
 

@@ -375,28 +375,48 @@ __global__ void __launch_bounds__(kAttnThreads, 2) k_sparse_attn(AttnArgs a)
     }
 }
 
-// Log-sum-exp merge of the split partials: weights exp2(lse_s - max).
+// Log-sum-exp merge of the split partials: weights exp2(lse_s - max).  The
+// partials of eight splits are loaded at once (one round trip per eight
+// splits instead of one per split).
 __global__ void k_merge(MergeArgs a)
 {
     pdl_enter();
+    constexpr int kB = 8;
     const int row = blockIdx.x;
     const int d = threadIdx.x * 4;
     if (d >= a.dv) return;
     const float *lp = a.lse_part + (int64_t)row * a.splits;
     float M = -INFINITY;
-    for (int s = 0; s < a.splits; ++s) M = fmaxf(M, lp[s]);
+    for (int s0 = 0; s0 < a.splits; s0 += kB) {
+        float l8[kB];
+#pragma unroll
+        for (int e = 0; e < kB; ++e) l8[e] = s0 + e < a.splits ? lp[s0 + e] : -INFINITY;
+#pragma unroll
+        for (int e = 0; e < kB; ++e) M = fmaxf(M, l8[e]);
+    }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float wsum = 0.f;
     if (M != -INFINITY) {
-        for (int s = 0; s < a.splits; ++s) {
-            if (lp[s] == -INFINITY) continue;
-            const float f = ex2(lp[s] - M);
-            wsum += f;
-            const float4 v = *reinterpret_cast<const float4 *>(a.o_part + ((int64_t)row * a.splits + s) * a.dv + d);
-            acc.x += f * v.x;
-            acc.y += f * v.y;
-            acc.z += f * v.z;
-            acc.w += f * v.w;
+        for (int s0 = 0; s0 < a.splits; s0 += kB) {
+            float l8[kB];
+            float4 v8[kB];
+#pragma unroll
+            for (int e = 0; e < kB; ++e) {
+                const int sp = s0 + e;
+                l8[e] = sp < a.splits ? lp[sp] : -INFINITY;
+                v8[e] = sp < a.splits ? *reinterpret_cast<const float4 *>(a.o_part + ((int64_t)row * a.splits + sp) * a.dv + d)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int e = 0; e < kB; ++e) {
+                if (l8[e] == -INFINITY) continue;   // an empty part adds nothing (its output is not read)
+                const float f = ex2(l8[e] - M);
+                wsum += f;
+                acc.x += f * v8[e].x;
+                acc.y += f * v8[e].y;
+                acc.z += f * v8[e].z;
+                acc.w += f * v8[e].w;
+            }
         }
     }
     const bool empty_set = !(wsum > 0.f);

@@ -25,6 +25,7 @@
 #include "attn_items.cuh"
 #include "lsa_device.cuh"
 #include "topk_block.cuh"
+#include "topk_bucket.cuh"
 
 namespace lsa {
 namespace {
@@ -52,6 +53,7 @@ struct FlLayout {
     static constexpr int SMEM = SELS + 2 * kFlMaxSel * 4;
     static_assert(RINGS >= kFlMaxRowsPerCta * (kFlWarps * G * (DK + 2) + G * (kFlWarps + 1)) * 4,
                   "the CTA merge reuses the rings");
+    static_assert(RINGS >= (int)sizeof(BucketScratch<kFlWarps * 32>), "the selection's scratch reuses the rings");
     static_assert(SMEM * kFlCtasPerSm <= 227 * 1024, "the CTAs of one SM");
 };
 
@@ -181,7 +183,24 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
             const int rh = rh_first + s;
             int32_t *dst = s_sel + s * kFlMaxSel;
             if (s > 0) block_topk_load<KSEL>(a.sel_scores + (int64_t)rh * a.sel_cols, a.sel_cols, sel_aligned, sel_v);
-            const int keff = block_topk_scores<KSEL>(sel_v, a.nsel, a.status, sm, [&](int pos, int col) { dst[pos] = col; });
+            int keff;
+            if constexpr (KSEL == 8) {
+                // rows of up to 2048 blocks: the bucketed exact top-k
+                // (topk_bucket.cuh), its scratch in the K / V rings, which
+                // are not in use before the selection is made
+                BucketScratch<kFlWarps * 32> &bsm = *reinterpret_cast<BucketScratch<kFlWarps * 32> *>(smem);
+                uint32_t keys[KSEL];
+                bool nan = false;
+#pragma unroll
+                for (int e = 0; e < KSEL; ++e) {
+                    nan |= isnan(sel_v[e]);
+                    keys[e] = (isnan(sel_v[e]) || sel_v[e] == -INFINITY) ? 0u : float_to_key(sel_v[e]);
+                }
+                if (nan) flag_error(a.status, LSA_ERR_NAN);
+                keff = block_bucket_topk<kFlWarps * 32, KSEL>(keys, a.nsel, bsm, [&](int pos, int col) { dst[pos] = col; });
+            } else {
+                keff = block_topk_scores<KSEL>(sel_v, a.nsel, a.status, sm, [&](int pos, int col) { dst[pos] = col; });
+            }
             for (int i = keff + (int)threadIdx.x; i < a.nsel; i += blockDim.x) dst[i] = -1;
             __syncthreads();
             if (a.sel_write && fl_cta_of(a, (uint32_t)rh * a.nsub * NS) == (int)cta)

@@ -23,6 +23,56 @@ __device__ __forceinline__ void flag_error(uint32_t *status, int code)
     if (status) atomicOr(status, 1u << code);
 }
 
+// ---------------------------------------------------------------- counters between CTAs
+
+// red.release / ld.acquire of a GPU-scope counter.
+__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Waits until *p == want (acquire).  Gives up after `budget` SM clock
+// cycles, records LSA_ERR_TIMEOUT and returns false: a wait never hangs.
+// The counters it waits on only ever reach `want` once per call and stay
+// there until every waiter has passed, so an exact comparison cannot miss.
+__device__ __forceinline__ bool wait_counter_eq(const uint32_t *p, uint32_t want, uint32_t *status, long long budget)
+{
+    if (ld_acquire(p) == want) return true;
+    const long long t0 = clock64();
+    while (ld_acquire(p) != want) {
+        if (clock64() - t0 > budget) {
+            flag_error(status, LSA_ERR_TIMEOUT);
+            return false;
+        }
+        __nanosleep(100);
+    }
+    return true;
+}
+
+// Every thread of the CTA calls this once its results are written; it
+// returns true in every thread of the group's last CTA to arrive (`members`
+// CTAs share the counter), which may then read what the others wrote.  The
+// caller resets the counter.
+__device__ __forceinline__ bool last_cta_arrival(uint32_t *counter, uint32_t members, uint32_t *s_flag)
+{
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t prev = atomicAdd(counter, 1u);
+        *s_flag = prev == members - 1 ? 1u : 0u;
+    }
+    __syncthreads();
+    const bool last = *s_flag != 0u;
+    if (last) __threadfence();
+    return last;
+}
+
 // ---------------------------------------------------------------- dependent launch
 
 // A kernel launched with programmatic stream serialization (a dependent)
@@ -309,6 +359,102 @@ __device__ __forceinline__ float fast_lg2(float x)
 __device__ __forceinline__ uint32_t swizzle_offset(int t, int ch)
 {
     return (uint32_t)((ch >> 3) * (16 * 128) + t * 128 + (((ch & 7) ^ (t & 7)) << 4));
+}
+
+// ---------------------------------------------------------------- tcgen05 (fifth-generation tensor cores)
+
+// Tensor memory (TMEM) is 128 lanes x 512 columns of 32-bit cells per SM.
+// An address is (lane << 16) | column.  Allocation is by a whole warp, in
+// power-of-two column counts >= 32; the base address is written to shared
+// memory.  Every allocation must be freed by the same CTA before it exits.
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Ordering of tcgen05 operations across a thread barrier.
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Makes this thread's generic-proxy writes to shared memory (st.shared,
+// cp.async) visible to the async proxy that tcgen05.mma reads through.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Shared-memory matrix descriptor with the 128-byte swizzle: atoms of 8
+// rows x 128 bytes (1024-byte aligned), the 16-byte chunk index of each row
+// XORed with the row index (swizzle_offset above lays tiles out this way).
+// lbo / sbo: byte offsets between atoms along the leading and the strided
+// dimension; bits 46-47 hold the descriptor version (1), bits 61-63 the
+// layout (2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulation:
+// D format bits 4-5, A and B formats bits 7-9 / 10-12, A and B major-ness
+// bits 15 / 16 (0 = K-major, 1 = MN-major), N / 8 in bits 17-22, M / 16 in
+// bits 24-28.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool a_mn, bool b_mn)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]; issued by one thread.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          bool accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
+// One arrive on `bar` once every tcgen05.mma this thread issued before it
+// has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+// 32 consecutive columns of this thread's TMEM lane (the warp reads the 32
+// lanes of its quadrant: taddr's lane field is 32 * (warp % 4)).  The wait
+// for the load is part of the same statement, so no use of the registers
+// can be scheduled before the data has arrived.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 }  // namespace lsa

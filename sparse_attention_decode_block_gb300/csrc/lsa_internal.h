@@ -111,6 +111,13 @@ struct ScoreArgs {
     int32_t chunk;              // blocks per CTA (score_chunk)
     float *scores;              // [B, hkv, max_blocks]
     uint32_t *status;
+    // coarse-to-fine step (sel_k > 0): the last CTA of each request selects
+    // the top sel_k blocks of the request's rows into sel_idx [B*hkv, sel_k]
+    // (ascending, -1 padded), then adds 1 to ready[r]; cnt[r] counts the
+    // request's CTAs (zero between calls; the selecting CTA resets it)
+    int32_t sel_k;
+    int32_t *sel_idx;
+    uint32_t *cnt, *ready;
 };
 
 struct TopkArgs {
@@ -134,6 +141,18 @@ struct FineArgs {
     int32_t batch, hq, max_blocks, ncand;
     float *fscores;             // [B*hkv, ncand*b]
     uint32_t *status;
+    // coarse-to-fine step (tok_k > 0): every CTA first waits (bounded) for
+    // ready[r] == 1, set once the request's candidates are final; the last
+    // CTA of each request (cnt[r]) selects the top tok_k tokens of each of
+    // its rows into tok_idx [B*hkv, tok_k] (token positions, ascending, -1
+    // padded) and resets cnt[r] and ready[r]
+    int32_t tok_k;
+    int32_t *tok_idx;
+    uint32_t *cnt, *ready;
+    long long spin_budget;
+    // indexer head weights [B, Hq] (NULL: the head-sum score): the fine
+    // score is then sum_g w[r,g] ReLU(q_g . k_t) (weighted-ReLU kernel)
+    const float *weights;
 };
 
 struct AttnArgs {
@@ -177,6 +196,12 @@ struct AttnArgs {
     float *lse;                 // [B, Hq] natural log or NULL
     uint32_t *status;
     long long spin_budget;
+    // tcgen05 kernel: merge the row's tiles inside the kernel (every CTA of
+    // the grid resident at once): each tile CTA adds 1 to mrg_arrive[row],
+    // waits (bounded) for it to reach the tile count, merges a slice of the
+    // row's outputs, then adds 1 to mrg_done[row]; the last resets both
+    int32_t merge_in_kernel;
+    uint32_t *mrg_arrive, *mrg_done;
 };
 
 // A staged item: a run of token rows within one page (n > 0), nothing to
@@ -203,9 +228,11 @@ struct MergeArgs {
 
 // ---- launchers (return a cudaError_t from the launch; LSA_ERR_UNSUPPORTED
 // is reported through *unsupported when no kernel instance fits the shape)
-cudaError_t launch_build_summaries(const SummaryArgs &a, cudaStream_t s);
-cudaError_t launch_append(const SummaryArgs &a, cudaStream_t s, bool *unsupported);
+cudaError_t launch_build_summaries(const SummaryArgs &a, cudaStream_t s, bool quest);
+cudaError_t launch_append(const SummaryArgs &a, cudaStream_t s, bool quest, bool *unsupported);
 cudaError_t launch_score(const ScoreArgs &a, cudaStream_t s, bool *unsupported);
+cudaError_t launch_score_quest(const ScoreArgs &a, cudaStream_t s, bool *unsupported);
+bool score_quest_supported(int dk, int hkv, int group);
 cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s, bool *unsupported);
 cudaError_t launch_fine_scores(const FineArgs &a, cudaStream_t s, bool *unsupported);
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s, bool *unsupported);
@@ -219,6 +246,10 @@ bool launch_topk_fast(const TopkArgs &a, cudaStream_t s, cudaError_t *err);
 cudaError_t launch_attention_tc(const AttnArgs &a, int gs, cudaStream_t s, bool *unsupported);
 int attention_tc_group(int dk, int dv, int group, bool alias, bool token_mode, const CacheView &v);
 int attention_tc_max_items_per_split(int dk);
+bool attention_umma_supported(int dk, int dv, int group, bool alias);
+int attention_umma_items_per_tile();
+int attention_umma_ctas_per_sm(int dk, int dv, bool alias);
+cudaError_t launch_attention_umma(const AttnArgs &a, cudaStream_t s, bool *unsupported);
 
 // Shape support queries used by the planner.
 bool score_supported(int dk, int hkv);

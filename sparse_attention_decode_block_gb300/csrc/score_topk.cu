@@ -6,13 +6,16 @@
 // linear in q, the group's queries are summed once (q_sum = sum_g q_g, fp32)
 // and each summary row is read once with 16-byte loads and dotted with q_sum.
 //
-// Top-k: exact radix select on order-preserving 32-bit keys, 8 bits per
-// pass, one CTA per row with the keys in shared memory (Vortex, "Making it
-// fast": radix-based top-k buckets values by their digits).  Ties go to the
-// lower index and the output is ascending, so the result is bit-exact.
+// Top-k of wide rows or large k: one CTA per row buckets the scores by a
+// monotone remap of their values and ranks the boundary bucket exactly
+// (topk_bucket.cuh; Vortex, "Making it fast").  Ties go to the lower index
+// and the output is ascending, so the result is bit-exact.
 #include <math.h>
 
+#include <type_traits>
+
 #include "lsa_device.cuh"
+#include "topk_bucket.cuh"
 
 namespace lsa {
 namespace {
@@ -30,7 +33,9 @@ constexpr int kPtPerThread = kScoreMaxChunk / (kScoreWarps * 32);
 // memory once per CTA.  The main loop keeps U summary rows in flight per
 // warp at all times: each row's registers are refilled with the row U ahead
 // as soon as its dot products are done.
-template <int DK, int HKV>
+constexpr int kSelMaxCols = kScoreWarps * 32 * 32;   // rows the select-at-end epilogue handles
+
+template <int DK, int HKV, bool SEL>
 __global__ void __launch_bounds__(kScoreWarps * 32, 2) k_score(ScoreArgs a)
 {
     pdl_enter();
@@ -57,10 +62,18 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 2) k_score(ScoreArgs a)
         const int j = j0 + tid + i * kScoreWarps * 32;
         praw[i] = j < j1 ? a.pt[(int64_t)r * a.max_blocks + j] : -1;
     }
+    // the group's query sum, one 8-dim slice of one head per thread (NCH <=
+    // threads for every supported shape).  Up to 8 heads a thread adds them
+    // in head order; larger groups are cut into QSL slices of heads whose
+    // loads are all issued at once, and the slices are added in slice order
+    constexpr int QSL = (kScoreWarps * 32) / NCH;
+    static_assert(QSL >= 1, "one thread per 16-byte chunk of the summary row");
+    __shared__ __align__(16) float s_qpart[QSL > 1 ? QSL * NCH * 8 : 1];
     float qacc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    const bool qthread = tid < NCH;        // one 8-dim slice of one head per thread
-    const int qh = tid / CPH, qd = (tid % CPH) * 8;
-    if (qthread) {
+    const int qc = tid % NCH, qsl = tid / NCH;   // chunk, slice
+    const int qh = qc / CPH, qd = (qc % CPH) * 8;
+    const bool sliced = G > 8 && QSL > 1;
+    if (!sliced && tid < NCH) {
         const uint16_t *qp = a.q + ((int64_t)r * a.hq + qh * G) * DK + qd;
         for (int g0 = 0; g0 < G; g0 += 4) {
             uint4 v[4];
@@ -78,28 +91,31 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 2) k_score(ScoreArgs a)
                 }
             }
         }
-    }
-    for (int c = tid; c < NCH; c += kScoreWarps * 32) {   // NCH > threads only for wide rows
-        if (c != tid) {
-            const int h = c / CPH, d0 = (c % CPH) * 8;
-            float t8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int g = 0; g < G; ++g) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(a.q + ((int64_t)r * a.hq + h * G + g) * DK + d0);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    } else if (sliced && qsl < QSL) {
+        // heads qsl, qsl + QSL, ...: at most 32 per thread (G <= 32 * QSL)
+        const uint16_t *qp = a.q + ((int64_t)r * a.hq + qh * G) * DK + qd;
+        for (int g0 = qsl; g0 < G; g0 += 8 * QSL) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int g = g0 + u * QSL;
+                v[u] = g < G ? *reinterpret_cast<const uint4 *>(qp + (int64_t)g * DK) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 f = bf2_to_f2(w[e]);
-                    t8[2 * e] += f.x;
-                    t8[2 * e + 1] += f.y;
+                    qacc[2 * e] += f.x;
+                    qacc[2 * e + 1] += f.y;
                 }
             }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) s_qs[h * DK + d0 + e] = t8[e];
         }
-    }
-    if (qthread) {
+        if constexpr (QSL > 1) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) s_qs[qh * DK + qd + e] = qacc[e];
+            for (int e = 0; e < 8; ++e) s_qpart[(qsl * NCH + qc) * 8 + e] = qacc[e];
+        }
     }
     const bool len_ok = L >= 0 && (int64_t)L <= (int64_t)a.max_blocks * a.b;
     if (!len_ok && tid == 0 && blockIdx.x == 0) flag_error(a.status, LSA_ERR_BOUNDS);
@@ -121,13 +137,36 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 2) k_score(ScoreArgs a)
             for (int h = 0; h < HKV; ++h) a.scores[((int64_t)r * HKV + h) * a.max_blocks + j] = -INFINITY;
         }
     }
+    if (!sliced && tid < NCH) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s_qs[qh * DK + qd + e] = qacc[e];
+    }
+    if constexpr (QSL > 1) {
+        if (sliced) {
+            __syncthreads();
+            if (tid < NCH) {
+                float t8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                for (int sl = 0; sl < QSL; ++sl)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) t8[e] += s_qpart[(sl * NCH + tid) * 8 + e];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s_qs[qh * DK + qd + e] = t8[e];
+            }
+        }
+    }
     __syncthreads();
 
-    // ---- this lane's slice of the query sum
+    // ---- this lane's slice of the query sum.  Rows narrower than a warp
+    // (NCH < 32 chunks) are taken R at a time, NCH lanes each.
+    constexpr int R = NCH < 32 ? 32 / NCH : 1;
+    static_assert(R == 1 || (NI == 1 && 32 % NCH == 0), "narrow rows tile the warp");
+    constexpr int UR = (NI == 1 ? 8 : U);   // row groups in flight per warp
+    const int sr = R > 1 ? lane / NCH : 0;  // this lane's row within a group
+    const int lc = R > 1 ? lane % NCH : lane;
     float qs[NI][8];
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
-        const int ch = lane + 32 * i;
+        const int ch = lc + 32 * i;
 #pragma unroll
         for (int e = 0; e < 8; ++e) qs[i][e] = ch < NCH ? s_qs[(ch / CPH) * DK + (ch % CPH) * 8 + e] : 0.f;
     }
@@ -137,24 +176,26 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 2) k_score(ScoreArgs a)
     const int w0 = (int)((int64_t)n * warp / kScoreWarps), w1 = (int)((int64_t)n * (warp + 1) / kScoreWarps);
     const uint8_t *summ = reinterpret_cast<const uint8_t *>(a.summ);
     const uint64_t pol = l2_evict_first();
-    uint4 v[U][NI];
+    uint4 v[UR][NI];
+    // row group gi covers rows w0 + gi * R + [0, R)
     auto issue = [&](int i, uint4(&dst)[NI]) {
         const int p = i < w1 ? s_page[i] : -1;
 #pragma unroll
         for (int c = 0; c < NI; ++c) {
-            const int ch = lane + 32 * c;
+            const int ch = lc + 32 * c;
             dst[c] = (p >= 0 && ch < NCH) ? ldg_stream_v4(summ + (int64_t)p * HKV * DK * 2 + ch * 16, pol)
                                           : make_uint4(0, 0, 0, 0);
         }
     };
 #pragma unroll
-    for (int u = 0; u < U; ++u) issue(w0 + u, v[u]);
-    for (int base = w0; base < w1; base += U) {
+    for (int u = 0; u < UR; ++u) issue(w0 + u * R + sr, v[u]);
+    for (int base = w0; base < w1; base += UR * R) {
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = base + u;
-            const int p = i < w1 ? s_page[i] : -1;      // warp-uniform
-            if (p >= 0) {
+        for (int u = 0; u < UR; ++u) {
+            const int i = base + u * R + sr;
+            const int p = i < w1 ? s_page[i] : -1;      // warp-uniform when R == 1
+            const bool any = R > 1 ? __any_sync(0xffffffffu, p >= 0) : p >= 0;
+            if (any) {
                 const int j = j0 + i;
                 float part[NI];
 #pragma unroll
@@ -172,8 +213,8 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 2) k_score(ScoreArgs a)
 #pragma unroll
                         for (int off = CPH / 2; off > 0; off >>= 1)
                             part[c] += __shfl_xor_sync(0xffffffffu, part[c], off);
-                        const int ch = lane + 32 * c;
-                        if (ch < NCH && (lane % CPH) == 0)
+                        const int ch = lc + 32 * c;
+                        if (p >= 0 && ch < NCH && (lane % CPH) == 0)
                             a.scores[((int64_t)r * HKV + ch / CPH) * a.max_blocks + j] = part[c];
                     }
                 } else {
@@ -185,9 +226,249 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 2) k_score(ScoreArgs a)
                     if (lane == 0) a.scores[(int64_t)r * a.max_blocks + j] = tot;
                 }
             }
-            issue(i + U, v[u]);
+            issue(i + UR * R, v[u]);
         }
     }
+
+    if constexpr (SEL) {
+        // coarse-to-fine step: the request's last CTA selects the top sel_k
+        // blocks of each of its rows (LeanSparse, Section 5: the coarse pass
+        // keeps the candidates the exact pass rescores)
+        __shared__ uint32_t s_last;
+        __shared__ BucketScratch<kScoreWarps * 32> bsm;
+        if (last_cta_arrival(a.cnt + r, gridDim.x, &s_last)) {
+            constexpr int KPT = kSelMaxCols / (kScoreWarps * 32);
+            for (int h = 0; h < HKV; ++h) {
+                const float *srow = a.scores + ((int64_t)r * HKV + h) * a.max_blocks;
+                uint32_t keys[KPT];
+                bool nan = false;
+#pragma unroll
+                for (int e = 0; e < KPT; ++e) {
+                    const int col = tid * KPT + e;
+                    const float x = col < a.max_blocks ? __ldcg(srow + col) : -INFINITY;
+                    nan |= isnan(x);
+                    keys[e] = (isnan(x) || x == -INFINITY) ? 0u : float_to_key(x);
+                }
+                if (nan) flag_error(a.status, LSA_ERR_NAN);
+                int32_t *orow = a.sel_idx + ((int64_t)r * HKV + h) * a.sel_k;
+                const int keff = block_bucket_topk<kScoreWarps * 32, KPT>(keys, a.sel_k, bsm,
+                                                                           [&](int pos, int col) { orow[pos] = col; });
+                for (int i = keff + tid; i < a.sel_k; i += kScoreWarps * 32) orow[i] = -1;
+            }
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) {
+                a.cnt[r] = 0u;
+                red_release_add(a.ready + r, 1u);
+            }
+        }
+    }
+}
+
+// ============================================================ Quest scores
+
+// Halves per-lane partials across the lane pair that differs in `bit`:
+// the lane with the bit clear keeps the lower half of the entries (summed
+// with its partner's), the other lane the upper half.
+template <int N>
+__device__ __forceinline__ void halve_sum(const float (&v)[N], float (&out)[N / 2], int bit)
+{
+    const bool up = (threadIdx.x & bit) != 0;
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+        const float send = up ? v[i] : v[N / 2 + i];
+        out[i] = (up ? v[N / 2 + i] : v[i]) + __shfl_xor_sync(0xffffffffu, send, bit);
+    }
+}
+
+// The maximum over G heads of each head's sum over the warp's 32 lanes:
+// log2 G reduce-scatter steps leave each lane one head's partial, the
+// remaining lane bits finish the sums, and a max across the scatter bits
+// combines the heads.  Every lane gets the result.
+template <int G>
+__device__ __forceinline__ float warp_heads_sum_max(const float (&v)[G])
+{
+    float s;
+    int sbits;   // lane bits used by the scatter
+    if constexpr (G == 1) {
+        s = v[0];
+        sbits = 0;
+    } else if constexpr (G == 2) {
+        float a1[1];
+        halve_sum<2>(v, a1, 16);
+        s = a1[0];
+        sbits = 16;
+    } else if constexpr (G == 4) {
+        float a2[2], a1[1];
+        halve_sum<4>(v, a2, 16);
+        halve_sum<2>(a2, a1, 8);
+        s = a1[0];
+        sbits = 16 | 8;
+    } else {
+        static_assert(G == 8, "groups of 1, 2, 4 or 8 query heads");
+        float a4[4], a2[2], a1[1];
+        halve_sum<8>(v, a4, 16);
+        halve_sum<4>(a4, a2, 8);
+        halve_sum<2>(a2, a1, 4);
+        s = a1[0];
+        sbits = 16 | 8 | 4;
+    }
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1)
+        if (!(sbits & off)) s += __shfl_xor_sync(0xffffffffu, s, off);
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1)
+        if (sbits & off) s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, off));
+    return s;
+}
+
+// s_j = max over the group's query heads g of sum_i max(q_gi * max_ji,
+// q_gi * min_ji) for every candidate block j: the Quest bound on q_g . k_t
+// over the block's tokens t (Vortex blog post, end of "Why Long
+// Generations Are Expensive"; the Quest listing in "Writing an algorithm:
+// vFlow" takes Max over heads of Sum over dims of Maximum(q * max, q * min)).
+// It is not linear in q, so every head's query is kept: a warp owns one KV
+// head of a share of the chunk's blocks, each lane DK / 32 dims, with the G
+// query heads' slices in registers; per block it reads the head's maximum
+// and minimum keys (DK / 16 bytes per lane each) and keeps U blocks in
+// flight.  Summaries: [num_pages, HKV, 2, DK] bf16, maximum then minimum.
+template <int DK, int HKV, int G>
+__global__ void __launch_bounds__(kScoreWarps * 32, 2) k_score_quest(ScoreArgs a)
+{
+    pdl_enter();
+    constexpr int DPL = DK / 32;                 // dims per lane
+    constexpr int PARTS = kScoreWarps / HKV;     // warps per KV head
+    constexpr int U = 8;                         // blocks in flight per warp
+    static_assert(DPL == 2 || DPL == 4, "64- or 128-dim heads");
+    static_assert(kScoreWarps % HKV == 0, "KV heads divide the warps");
+    using VT = typename std::conditional<DPL == 4, uint2, uint32_t>::type;
+    __shared__ int s_page[kScoreMaxChunk];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r = blockIdx.y;
+    const int h = warp % HKV, part = warp / HKV;
+    const int j0 = blockIdx.x * a.chunk;
+    const int j1 = min(j0 + a.chunk, a.max_blocks);
+
+    const int L = a.lens[r];
+    int praw[kPtPerThread];
+#pragma unroll
+    for (int i = 0; i < kPtPerThread; ++i) {
+        const int j = j0 + tid + i * kScoreWarps * 32;
+        praw[i] = j < j1 ? a.pt[(int64_t)r * a.max_blocks + j] : -1;
+    }
+    // this lane's dims of the G query heads of KV head h
+    float qv[G][DPL];
+    {
+        const uint16_t *qp = a.q + ((int64_t)r * a.hq + h * G) * DK + lane * DPL;
+        VT raw[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) raw[g] = *reinterpret_cast<const VT *>(qp + (int64_t)g * DK);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            if constexpr (DPL == 4) {
+                const float2 lo = bf2_to_f2(raw[g].x), hi = bf2_to_f2(raw[g].y);
+                qv[g][0] = lo.x;
+                qv[g][1] = lo.y;
+                qv[g][2] = hi.x;
+                qv[g][3] = hi.y;
+            } else {
+                const float2 f = bf2_to_f2(raw[g]);
+                qv[g][0] = f.x;
+                qv[g][1] = f.y;
+            }
+        }
+    }
+    const bool len_ok = L >= 0 && (int64_t)L <= (int64_t)a.max_blocks * a.b;
+    if (!len_ok && tid == 0 && blockIdx.x == 0) flag_error(a.status, LSA_ERR_BOUNDS);
+    const int se = len_ok ? min(a.sink, L) : 0;
+    const int rs = len_ok ? max(L - a.recent, se) : 0;
+#pragma unroll
+    for (int i = 0; i < kPtPerThread; ++i) {
+        const int j = j0 + tid + i * kScoreWarps * 32;
+        if (j >= j1) continue;
+        const bool cand = len_ok && (int64_t)j * a.b >= se && (int64_t)(j + 1) * a.b <= rs;
+        int p = cand ? praw[i] : -1;
+        if (cand && (p < 0 || p >= a.num_pages)) {
+            flag_error(a.status, LSA_ERR_BOUNDS);
+            p = -1;
+        }
+        s_page[j - j0] = p;
+        if (p < 0) {
+#pragma unroll
+            for (int hh = 0; hh < HKV; ++hh) a.scores[((int64_t)r * HKV + hh) * a.max_blocks + j] = -INFINITY;
+        }
+    }
+    __syncthreads();
+
+    const int n = j1 - j0;
+    const int w0 = n * part / PARTS, w1 = n * (part + 1) / PARTS;
+    const uint8_t *summ = reinterpret_cast<const uint8_t *>(a.summ) + ((int64_t)h * 2 * DK + lane * DPL) * 2;
+    constexpr int64_t kPageBytes = (int64_t)HKV * 2 * DK * 2;
+    const uint64_t pol = l2_evict_first();
+    VT vmax[U], vmin[U];
+    auto issue = [&](int i, VT &mx, VT &mn) {
+        const int p = i < w1 ? s_page[i] : -1;
+        if (p >= 0) {
+            const uint8_t *src = summ + (int64_t)p * kPageBytes;
+            if constexpr (DPL == 4) {
+                uint4 both;   // two 8-byte loads (maximum, minimum)
+                asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;"
+                             : "=r"(both.x), "=r"(both.y) : "l"(src), "l"(pol));
+                asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;"
+                             : "=r"(both.z), "=r"(both.w) : "l"(src + DK * 2), "l"(pol));
+                mx = make_uint2(both.x, both.y);
+                mn = make_uint2(both.z, both.w);
+            } else {
+                asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;"
+                             : "=r"(mx) : "l"(src), "l"(pol));
+                asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;"
+                             : "=r"(mn) : "l"(src + DK * 2), "l"(pol));
+            }
+        }
+    };
+#pragma unroll
+    for (int u = 0; u < U; ++u) issue(w0 + u, vmax[u], vmin[u]);
+    for (int base = w0; base < w1; base += U) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + u;
+            const int p = i < w1 ? s_page[i] : -1;   // warp-uniform
+            if (p >= 0) {
+                float M[DPL], m[DPL];
+                if constexpr (DPL == 4) {
+                    const float2 a0 = bf2_to_f2(vmax[u].x), a1 = bf2_to_f2(vmax[u].y);
+                    const float2 b0 = bf2_to_f2(vmin[u].x), b1 = bf2_to_f2(vmin[u].y);
+                    M[0] = a0.x; M[1] = a0.y; M[2] = a1.x; M[3] = a1.y;
+                    m[0] = b0.x; m[1] = b0.y; m[2] = b1.x; m[3] = b1.y;
+                } else {
+                    const float2 a0 = bf2_to_f2(vmax[u]), b0 = bf2_to_f2(vmin[u]);
+                    M[0] = a0.x; M[1] = a0.y;
+                    m[0] = b0.x; m[1] = b0.y;
+                }
+                float part_g[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int d = 0; d < DPL; ++d) acc += fmaxf(qv[g][d] * M[d], qv[g][d] * m[d]);
+                    part_g[g] = acc;
+                }
+                const float sc = warp_heads_sum_max<G>(part_g);
+                if (lane == 0) a.scores[((int64_t)r * HKV + h) * a.max_blocks + j0 + i] = sc;
+            }
+            issue(i + U, vmax[u], vmin[u]);
+        }
+    }
+}
+
+template <int DK, int HKV, int G>
+cudaError_t launch_score_quest_t(const ScoreArgs &a, cudaStream_t s)
+{
+    dim3 grid((a.max_blocks + a.chunk - 1) / a.chunk, a.batch);
+    cudaError_t le = launch_step_kernel(k_score_quest<DK, HKV, G>, grid, dim3(kScoreWarps * 32), 0, s, a);
+    if (le != cudaSuccess) return le;
+    return cudaGetLastError();
 }
 
 // ============================================================ top-k
@@ -195,174 +476,121 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 2) k_score(ScoreArgs a)
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkMaxCols = 32768;
 
-// Block-wide exclusive scan of one uint32 per thread.
-__device__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_sums)
+// Output index of column `col` of row `row`: the column, or for the fine
+// pass of coarse-to-fine the token position it stands for.
+__device__ __forceinline__ int32_t topk_out(const TopkArgs &a, int row, int col)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t x = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
-        if (lane >= off) x += y;
-    }
-    if (lane == 31) warp_sums[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        const int nw = blockDim.x >> 5;
-        uint32_t s = lane < nw ? warp_sums[lane] : 0u;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            uint32_t y = __shfl_up_sync(0xffffffffu, s, off);
-            if (lane >= off) s += y;
-        }
-        if (lane < nw) warp_sums[lane] = s;   // inclusive
-    }
-    __syncthreads();
-    const uint32_t before_warp = warp ? warp_sums[warp - 1] : 0u;
-    const uint32_t r = before_warp + x - v;
-    __syncthreads();
-    return r;
+    if (!a.cand) return col;
+    const int cb = a.cand[(int64_t)row * a.ncand + col / a.b];
+    return cb * a.b + col % a.b;
 }
 
+// One block of 1024 threads per row, KPT columns per thread: the exact
+// bucketed top-k of topk_bucket.cuh.
+template <int KPT>
 __global__ void __launch_bounds__(kTopkThreads) k_topk_rows(TopkArgs a)
 {
     pdl_enter();
-    extern __shared__ uint32_t keys[];
-    __shared__ uint32_t hist[256];
-    __shared__ uint32_t warp_sums[32];
-    __shared__ uint32_t s_nvalid, s_digit, s_gt;
-
-    const int row = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31;
+    __shared__ BucketScratch<kTopkThreads> sm;
+    const int row = blockIdx.x, tid = threadIdx.x;
     int n = a.num_cols ? a.num_cols[row] : a.cols;
     n = max(0, min(n, a.cols));
-    if (tid == 0) s_nvalid = 0;
-    __syncthreads();
-
-    uint32_t cnt = 0;
     const float *srow = a.scores + (int64_t)row * a.cols;
-    for (int i = tid; i < n; i += kTopkThreads) {
-        const float s = srow[i];
-        uint32_t key = 0;
-        if (isnan(s)) {
-            flag_error(a.status, LSA_ERR_NAN);
-        } else if (s != -INFINITY) {
-            key = float_to_key(s);
-            ++cnt;
+    const int c0 = tid * KPT;
+    float v[KPT];
+    const bool vec = (a.cols & 3) == 0 && (reinterpret_cast<uintptr_t>(a.scores) & 15) == 0 && c0 + KPT <= n;
+    if (vec) {
+#pragma unroll
+        for (int e = 0; e < KPT; e += 4) {
+            const float4 f = *reinterpret_cast<const float4 *>(srow + c0 + e);
+            v[e] = f.x;
+            v[e + 1] = f.y;
+            v[e + 2] = f.z;
+            v[e + 3] = f.w;
         }
-        keys[i] = key;
+    } else {
+#pragma unroll
+        for (int e = 0; e < KPT; ++e) v[e] = c0 + e < n ? srow[c0 + e] : -INFINITY;
     }
+    uint32_t keys[KPT];
+    bool nan = false;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
-    if (lane == 0 && cnt) atomicAdd(&s_nvalid, cnt);
-    __syncthreads();
-    const uint32_t nvalid = s_nvalid;
-    const uint32_t keff = min((uint32_t)max(a.k, 0), nvalid);
-
-    uint32_t thresh = 0, take_eq = 0;   // select key > thresh, and the first take_eq with key == thresh
-    if (keff > 0 && keff < nvalid) {
-        uint32_t prefix = 0, mask = 0, remaining = keff;
-        for (int shift = 24; shift >= 0; shift -= 8) {
-            if (tid < 256) hist[tid] = 0;
-            __syncthreads();
-            for (int base = 0; base < n; base += kTopkThreads) {
-                const int i = base + tid;
-                const uint32_t key = i < n ? keys[i] : 0u;
-                const bool in = key != 0 && (key & mask) == prefix;
-                const uint32_t digit = (key >> shift) & 0xffu;
-                const uint32_t act = __ballot_sync(0xffffffffu, in);
-                if (in) {
-                    const uint32_t peers = __match_any_sync(act, digit);
-                    if ((__ffs(peers) - 1) == lane) atomicAdd(&hist[digit], __popc(peers));
-                }
-            }
-            __syncthreads();
-            if (tid < 32) {
-                // lane l owns digits 8l .. 8l+7; find the digit whose bucket
-                // holds the remaining-th largest key
-                uint32_t c[8], tot = 0;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    c[e] = hist[8 * lane + e];
-                    tot += c[e];
-                }
-                // above = sum of the totals of lanes > lane
-                uint32_t incl = tot;   // inclusive suffix scan over lanes
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    uint32_t y = __shfl_down_sync(0xffffffffu, incl, off);
-                    if (lane + off < 32) incl += y;
-                }
-                uint32_t gt = incl - tot;
-#pragma unroll
-                for (int e = 7; e >= 0; --e) {
-                    if (gt < remaining && remaining <= gt + c[e]) {
-                        s_digit = 8 * lane + e;
-                        s_gt = gt;
-                    }
-                    gt += c[e];
-                }
-            }
-            __syncthreads();
-            prefix |= s_digit << shift;
-            mask |= 0xffu << shift;
-            remaining -= s_gt;
-            __syncthreads();
-        }
-        thresh = prefix;
-        take_eq = remaining;
+    for (int e = 0; e < KPT; ++e) {
+        nan |= isnan(v[e]);
+        keys[e] = (isnan(v[e]) || v[e] == -INFINITY) ? 0u : float_to_key(v[e]);
     }
-
-    // compact the selected columns in index order
-    const int per = (n + kTopkThreads - 1) / kTopkThreads;
-    const int lo = min(n, tid * per), hi = min(n, lo + per);
-    uint32_t ngt = 0, neq = 0;
-    if (keff > 0) {
-        for (int i = lo; i < hi; ++i) {
-            const uint32_t key = keys[i];
-            ngt += key != 0 && key > thresh;
-            neq += key != 0 && key == thresh;
-        }
-    }
-    const uint32_t packed = block_excl_scan((ngt << 16) | neq, warp_sums);
-    uint32_t gt_before = packed >> 16, eq_before = packed & 0xffffu;
+    if (nan) flag_error(a.status, LSA_ERR_NAN);
     int32_t *orow = a.idx + (int64_t)row * a.k;
-    if (keff > 0) {
-        for (int i = lo; i < hi; ++i) {
-            const uint32_t key = keys[i];
-            if (key == 0) continue;
-            int pos = -1;
-            if (key > thresh) {
-                pos = (int)(gt_before + min(eq_before, take_eq));
-                ++gt_before;
-            } else if (key == thresh) {
-                if (eq_before < take_eq) pos = (int)(gt_before + eq_before);
-                ++eq_before;
-            }
-            if (pos >= 0) {
-                int out = i;
-                if (a.cand) {
-                    const int cb = a.cand[(int64_t)row * a.ncand + i / a.b];
-                    out = cb * a.b + i % a.b;
-                }
-                orow[pos] = out;
-            }
-        }
-    }
-    for (int i = (int)keff + tid; i < a.k; i += kTopkThreads) orow[i] = -1;
+    const int keff = block_bucket_topk<kTopkThreads, KPT>(keys, a.k, sm,
+                                                          [&](int pos, int col) { orow[pos] = topk_out(a, row, col); });
+    for (int i = keff + tid; i < a.k; i += kTopkThreads) orow[i] = -1;
 }
 
 // ============================================================ fine pass
 
 constexpr int kFineWarps = 8;
 constexpr int kFineBlocksPerCta = 4;
+constexpr int kFineMaxCols = 16384;   // fine-score columns the selecting CTA handles (64 per thread)
 
 // f_t = scale_t * q_sum . e4m3(k8_t) for every token of the candidate
 // blocks (LeanSparse, Section 5: exact rescoring of the retained candidates
 // with their original FP8 indexer keys).  8 lanes per token, 16 dims each.
+// The coarse-to-fine step's last fine CTA of request r: the exact top tok_k
+// of each of the request's rows of fine scores (LeanSparse, Section 5: the
+// exact pass keeps the final tokens), written as token positions; then the
+// request's counters are reset.  Every thread of the CTA calls it.
+__device__ void fine_select_tokens(const FineArgs &a, int r, int hkv, int64_t ntok_row, int b)
+{
+    __shared__ uint32_t s_last;
+    __shared__ BucketScratch<kFineWarps * 32> bsm;
+    if (!last_cta_arrival(a.cnt + r, gridDim.x * hkv, &s_last)) return;
+    constexpr int KPT = kFineMaxCols / (kFineWarps * 32);
+    const int cols = (int)ntok_row;
+    for (int hh = 0; hh < hkv; ++hh) {
+        const int rw = r * hkv + hh;
+        const float *srow = a.fscores + (int64_t)rw * ntok_row;
+        uint32_t keys[KPT];
+        bool nan = false;
+#pragma unroll
+        for (int e = 0; e < KPT; e += 4) {
+            const int col = threadIdx.x * KPT + e;
+            float4 x4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (col + 3 < cols) x4 = __ldcg(reinterpret_cast<const float4 *>(srow + col));
+            else {
+                if (col < cols) x4.x = __ldcg(srow + col);
+                if (col + 1 < cols) x4.y = __ldcg(srow + col + 1);
+                if (col + 2 < cols) x4.z = __ldcg(srow + col + 2);
+            }
+            const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                nan |= isnan(xs[u]);
+                keys[e + u] = (isnan(xs[u]) || xs[u] == -INFINITY) ? 0u : float_to_key(xs[u]);
+            }
+        }
+        if (nan) flag_error(a.status, LSA_ERR_NAN);
+        const int32_t *crow = a.cand + (int64_t)rw * a.ncand;
+        int32_t *orow = a.tok_idx + (int64_t)rw * a.tok_k;
+        const int keff = block_bucket_topk<kFineWarps * 32, KPT>(
+            keys, a.tok_k, bsm, [&](int pos, int col) { orow[pos] = __ldcg(crow + col / b) * b + col % b; });
+        for (int i = keff + (int)threadIdx.x; i < a.tok_k; i += kFineWarps * 32) orow[i] = -1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {   // every CTA of the request has passed its wait
+        a.cnt[r] = 0u;
+        a.ready[r] = 0u;
+    }
+}
+
+// SEL: the fine pass of the coarse-to-fine step, launched as a programmatic
+// dependent of the coarse kernel: it does not wait for that kernel to
+// complete, but for each request's candidates (ready[r]), and its last CTA
+// per request selects the request's tokens.
+template <bool SEL>
 __global__ void __launch_bounds__(kFineWarps * 32) k_fine_scores(FineArgs a)
 {
-    pdl_enter();
+    if constexpr (SEL) pdl_launch_dependents();
+    else pdl_enter();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int row = blockIdx.y;                 // r * hkv + h
     const int hkv = a.ic.hkv;
@@ -371,68 +599,281 @@ __global__ void __launch_bounds__(kFineWarps * 32) k_fine_scores(FineArgs a)
     const int b = a.ic.b;
     const int sub = lane & 7, tq = lane >> 3;   // 16 dims per lane, 4 tokens per warp
 
+    // the group's query sum over all 256 threads: thread (slice sl, 8-dim
+    // chunk c) adds heads sl, sl + 16, ... of its chunk, all loads issued at
+    // once; the 16 slices are then added in slice order
+    __shared__ float s_part[16][128];
+    __shared__ float s_qsum[128];
+    {
+        const int c = threadIdx.x & 15, sl = threadIdx.x >> 4;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const uint16_t *qb = a.q + ((int64_t)r * a.hq + h * G) * 128 + c * 8;
+        for (int g0 = sl; g0 < G; g0 += 4 * 16) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int g = g0 + 16 * u;
+                v[u] = g < G ? *reinterpret_cast<const uint4 *>(qb + (int64_t)g * 128) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = bf2_to_f2(w[e]);
+                    acc[2 * e] += f.x;
+                    acc[2 * e + 1] += f.y;
+                }
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s_part[sl][c * 8 + e] = acc[e];
+        __syncthreads();
+        if (threadIdx.x < 128) {
+            float t = 0.f;
+            for (int k = 0; k < 16; ++k) t += s_part[k][threadIdx.x];
+            s_qsum[threadIdx.x] = t;
+        }
+        __syncthreads();
+    }
     float qs[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) qs[e] = 0.f;
-    for (int g = 0; g < G; ++g) {
-        const uint16_t *qg = a.q + ((int64_t)r * a.hq + h * G + g) * 128 + sub * 16;
-        const uint4 v0 = *reinterpret_cast<const uint4 *>(qg);
-        const uint4 v1 = *reinterpret_cast<const uint4 *>(qg + 8);
-        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float2 f = bf2_to_f2(w[e]);
-            qs[2 * e] += f.x;
-            qs[2 * e + 1] += f.y;
-        }
-    }
+    for (int e = 0; e < 16; ++e) qs[e] = s_qsum[sub * 16 + e];
 
     const int L = a.lens[r];
     const int nfull = (L >= 0 && (int64_t)L <= (int64_t)a.max_blocks * b) ? L / b : 0;
     const int64_t ntok_row = (int64_t)a.ncand * b;
     float *frow = a.fscores + (int64_t)row * ntok_row;
     const int c0 = blockIdx.x * kFineBlocksPerCta;
-    const int c1 = min(c0 + kFineBlocksPerCta, a.ncand);
-    for (int ci = c0; ci < c1; ++ci) {
-        const int j = a.cand[(int64_t)row * a.ncand + ci];
+    const int nb = min(kFineBlocksPerCta, a.ncand - c0);
+    bool cand_ok = true;
+    if constexpr (SEL) {
+        // the request's candidates are final once ready[r] == 1 (a wait
+        // that gives up records LSA_ERR_TIMEOUT; the CTA then scores nothing)
+        __shared__ uint32_t s_ok;
+        if (threadIdx.x == 0) s_ok = wait_counter_eq(a.ready + r, 1u, a.status, a.spin_budget) ? 1u : 0u;
+        __syncthreads();
+        cand_ok = s_ok != 0u;
+    }
+    // the CTA's candidate blocks -> page ids (two dependent round trips,
+    // once for all of them); -1 for padding and invalid entries
+    __shared__ int s_pg[kFineBlocksPerCta];
+    if (threadIdx.x < nb) {
+        const int j = cand_ok ? __ldcg(a.cand + (int64_t)row * a.ncand + c0 + threadIdx.x) : -1;
         int p = -1;
         if (j >= 0 && j < nfull) p = a.pt[(int64_t)r * a.max_blocks + j];
         const bool ok = p >= 0 && p < a.ic.num_pages;
-        if (!ok) {
-            if (j != -1 && warp == 0 && lane == 0) flag_error(a.status, LSA_ERR_BOUNDS);
-            for (int t = threadIdx.x; t < b; t += blockDim.x) frow[(int64_t)ci * b + t] = -INFINITY;
-            continue;
-        }
-        const uint8_t *kb = a.ic.k + (int64_t)p * a.ic.kps + (int64_t)h * a.ic.khs;
-        const float *sb = a.ic.kscale + (int64_t)p * a.ic.sps + (int64_t)h * a.ic.shs;
-        for (int t0 = warp * 4; t0 < b; t0 += kFineWarps * 4) {
-            const int t = t0 + tq;
-            float acc = 0.f;
-            if (t < b) {
-                const uint4 v = ldg_nc_v4(kb + (int64_t)t * a.ic.kts + sub * 16);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        if (!ok && j != -1) flag_error(a.status, LSA_ERR_BOUNDS);
+        s_pg[threadIdx.x] = ok ? p : -1;
+    }
+    __syncthreads();
+    // every (block, token) of the CTA: 8 lanes per token, 16 dims each; a
+    // warp takes 4 tokens per step and all its steps' loads go out at once
+    constexpr int kSteps = kFineBlocksPerCta * 64 / (kFineWarps * 4);
+    static_assert(kSteps <= 16, "loads in flight per lane");
+    const int ntok = nb * b;
+    uint4 kv[kSteps];
+    float sc[kSteps];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float2 lo = e4m3x2_to_f2((uint16_t)(w[e] & 0xffffu));
-                    float2 hi = e4m3x2_to_f2((uint16_t)(w[e] >> 16));
-                    acc = fmaf(qs[4 * e + 0], lo.x, acc);
-                    acc = fmaf(qs[4 * e + 1], lo.y, acc);
-                    acc = fmaf(qs[4 * e + 2], hi.x, acc);
-                    acc = fmaf(qs[4 * e + 3], hi.y, acc);
-                }
-            }
-#pragma unroll
-            for (int off = 4; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            if (t < b && sub == 0) frow[(int64_t)ci * b + t] = sb[t] * acc;
+    for (int it = 0; it < kSteps; ++it) {
+        const int t = (it * kFineWarps + warp) * 4 + tq;   // token of the CTA, block-major
+        const int bi = t / b, slot = t - bi * b;
+        const int p = t < ntok ? s_pg[bi] : -1;
+        kv[it] = make_uint4(0, 0, 0, 0);
+        sc[it] = 0.f;
+        if (p >= 0) {
+            kv[it] = ldg_nc_v4(a.ic.k + (int64_t)p * a.ic.kps + (int64_t)h * a.ic.khs + (int64_t)slot * a.ic.kts +
+                               sub * 16);
+            sc[it] = a.ic.kscale[(int64_t)p * a.ic.sps + (int64_t)h * a.ic.shs + slot];
         }
     }
+#pragma unroll
+    for (int it = 0; it < kSteps; ++it) {
+        const int t = (it * kFineWarps + warp) * 4 + tq;
+        const int bi = t / b;
+        const bool have = t < ntok && s_pg[bi] >= 0;
+        float acc = 0.f;
+        const uint32_t w[4] = {kv[it].x, kv[it].y, kv[it].z, kv[it].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float2 lo = e4m3x2_to_f2((uint16_t)(w[e] & 0xffffu));
+            float2 hi = e4m3x2_to_f2((uint16_t)(w[e] >> 16));
+            acc = fmaf(qs[4 * e + 0], lo.x, acc);
+            acc = fmaf(qs[4 * e + 1], lo.y, acc);
+            acc = fmaf(qs[4 * e + 2], hi.x, acc);
+            acc = fmaf(qs[4 * e + 3], hi.y, acc);
+        }
+#pragma unroll
+        for (int off = 4; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (t < ntok && sub == 0) frow[(int64_t)c0 * b + t] = have ? sc[it] * acc : -INFINITY;
+    }
+
+    if constexpr (SEL) fine_select_tokens(a, r, hkv, ntok_row, b);
 }
 
-template <int DK, int HKV>
+// The weighted-ReLU indexer score of the fine pass: f_t = sum_g w[r, g] *
+// ReLU(q_g . k_t), k_t = scale_t * e4m3(k8_t) (LeanSparse, Section 5: Eq. 6's
+// weighted head aggregation, applied to the exact keys).  The ReLU acts per
+// head, so the queries cannot be summed first: for the CTA's tokens the dots
+// of all 64 heads are a dense [64 x 128] x [128 x tokens] product, run as
+// m16n8k16 MMAs (bf16 queries; the e4m3 keys widened to bf16, exactly, in
+// shared memory).  Warp w takes the 16 heads of M-tile w % 4 over half of
+// the tokens; per token the weighted ReLUs of its heads are summed across
+// lanes and then across the four M-tiles in shared memory, and scaled by
+// scale_t (>= 0, so scale_t ReLU(x) = ReLU(scale_t x)).
+constexpr int kWrTok = kFineBlocksPerCta * 64;        // tokens per CTA at most
+constexpr int kWrSmem = kWrTok * 128 * 2;              // the widened key tile
+
+template <bool SEL>
+__global__ void __launch_bounds__(kFineWarps * 32) k_fine_scores_wrelu(FineArgs a)
+{
+    if constexpr (SEL) pdl_launch_dependents();
+    else pdl_enter();
+    extern __shared__ __align__(1024) uint8_t wsm[];   // [kWrTok / 16] tiles of 16 tokens x 128 dims, swizzled
+    __shared__ float s_part[4][kWrTok];
+    __shared__ int s_pg[kFineBlocksPerCta];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int row = blockIdx.y;
+    const int hkv = a.ic.hkv;
+    const int r = row / hkv, h = row % hkv;
+    const int G = a.hq / hkv;   // 64 (host-checked)
+    const int b = a.ic.b;
+    const int mt = warp & 3, th = warp >> 2;
+    const int rr = lane >> 2, cc = lane & 3;
+
+    // this warp's A fragments: heads 16 mt .. 16 mt + 15, all 128 dims
+    uint32_t qa[8][4];
+    {
+        const uint16_t *q0 = a.q + ((int64_t)r * a.hq + h * G + 16 * mt + rr) * 128;
+        const uint16_t *q8 = q0 + 8 * 128;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            qa[ks][0] = *reinterpret_cast<const uint32_t *>(q0 + 16 * ks + 2 * cc);
+            qa[ks][1] = *reinterpret_cast<const uint32_t *>(q8 + 16 * ks + 2 * cc);
+            qa[ks][2] = *reinterpret_cast<const uint32_t *>(q0 + 16 * ks + 8 + 2 * cc);
+            qa[ks][3] = *reinterpret_cast<const uint32_t *>(q8 + 16 * ks + 8 + 2 * cc);
+        }
+    }
+    const float w_lo = a.weights[(int64_t)r * a.hq + h * G + 16 * mt + rr];
+    const float w_hi = a.weights[(int64_t)r * a.hq + h * G + 16 * mt + rr + 8];
+
+    const int L = a.lens[r];
+    const int nfull = (L >= 0 && (int64_t)L <= (int64_t)a.max_blocks * b) ? L / b : 0;
+    const int64_t ntok_row = (int64_t)a.ncand * b;
+    float *frow = a.fscores + (int64_t)row * ntok_row;
+    const int c0 = blockIdx.x * kFineBlocksPerCta;
+    const int nb = min(kFineBlocksPerCta, a.ncand - c0);
+    bool cand_ok = true;
+    if constexpr (SEL) {
+        __shared__ uint32_t s_ok;
+        if (threadIdx.x == 0) s_ok = wait_counter_eq(a.ready + r, 1u, a.status, a.spin_budget) ? 1u : 0u;
+        __syncthreads();
+        cand_ok = s_ok != 0u;
+    }
+    if (threadIdx.x < nb) {
+        const int j = cand_ok ? __ldcg(a.cand + (int64_t)row * a.ncand + c0 + threadIdx.x) : -1;
+        int p = -1;
+        if (j >= 0 && j < nfull) p = a.pt[(int64_t)r * a.max_blocks + j];
+        const bool ok = p >= 0 && p < a.ic.num_pages;
+        if (!ok && j != -1) flag_error(a.status, LSA_ERR_BOUNDS);
+        s_pg[threadIdx.x] = ok ? p : -1;
+    }
+    __syncthreads();
+    const int ntok = nb * b;
+
+    // ---- the keys, widened: task (token t, 16-dim chunk u) -> two swizzled
+    // 16-byte chunks of bf16; tokens with nothing to score become zeros
+    {
+        constexpr int kTasks = kWrTok * 8;
+        for (int task = threadIdx.x; task < kTasks; task += kFineWarps * 32) {
+            const int t = task >> 3, u = task & 7;
+            const int bi = t / b, slot = t - bi * b;
+            const int p = t < ntok ? s_pg[bi] : -1;
+            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+            if (p >= 0) {
+                const uint4 v = ldg_nc_v4(a.ic.k + (int64_t)p * a.ic.kps + (int64_t)h * a.ic.khs +
+                                          (int64_t)slot * a.ic.kts + u * 16);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                uint32_t o[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f0 = e4m3x2_to_f2((uint16_t)(w[e] & 0xffffu));
+                    const float2 f1 = e4m3x2_to_f2((uint16_t)(w[e] >> 16));
+                    o[2 * e] = pack_bf16x2(f0.x, f0.y);       // exact: e4m3 values are bf16 values
+                    o[2 * e + 1] = pack_bf16x2(f1.x, f1.y);
+                }
+                lo = make_uint4(o[0], o[1], o[2], o[3]);
+                hi = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            uint8_t *tile = wsm + (t >> 4) * (16 * 256);
+            *reinterpret_cast<uint4 *>(tile + swizzle_offset(t & 15, 2 * u)) = lo;
+            *reinterpret_cast<uint4 *>(tile + swizzle_offset(t & 15, 2 * u + 1)) = hi;
+        }
+    }
+    __syncthreads();
+
+    // ---- dots of the warp's 16 heads with its half of the tokens
+    const int mi = lane >> 3, r8 = lane & 7;
+    const int tk = (mi >> 1) * 8 + r8, ck = mi & 1;
+    const uint32_t wbase = smem_addr(wsm);
+    for (int gi = 8 * th; gi < min(8 * th + 8, (ntok + 15) / 16); ++gi) {
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t tb = wbase + gi * (16 * 256);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t bb[4];
+            ldsm_x4(bb, tb + swizzle_offset(tk, 2 * ks + ck));
+            asm volatile(
+                "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                "{%0,%1,%2,%3};"
+                : "+f"(s0[0]), "+f"(s0[1]), "+f"(s0[2]), "+f"(s0[3])
+                : "r"(qa[ks][0]), "r"(qa[ks][1]), "r"(qa[ks][2]), "r"(qa[ks][3]), "r"(bb[0]), "r"(bb[1]));
+            asm volatile(
+                "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                "{%0,%1,%2,%3};"
+                : "+f"(s1[0]), "+f"(s1[1]), "+f"(s1[2]), "+f"(s1[3])
+                : "r"(qa[ks][0]), "r"(qa[ks][1]), "r"(qa[ks][2]), "r"(qa[ks][3]), "r"(bb[2]), "r"(bb[3]));
+        }
+        // lane holds heads rr (s[0], s[1]) and rr + 8 (s[2], s[3]) of tokens
+        // 2 cc, 2 cc + 1 of each 8-token n-tile: weight, ReLU, then the sum
+        // over the 8 lanes sharing cc
+        float t0 = w_lo * fmaxf(s0[0], 0.f) + w_hi * fmaxf(s0[2], 0.f);
+        float t1 = w_lo * fmaxf(s0[1], 0.f) + w_hi * fmaxf(s0[3], 0.f);
+        float t2 = w_lo * fmaxf(s1[0], 0.f) + w_hi * fmaxf(s1[2], 0.f);
+        float t3 = w_lo * fmaxf(s1[1], 0.f) + w_hi * fmaxf(s1[3], 0.f);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            t0 += __shfl_xor_sync(0xffffffffu, t0, off);
+            t1 += __shfl_xor_sync(0xffffffffu, t1, off);
+            t2 += __shfl_xor_sync(0xffffffffu, t2, off);
+            t3 += __shfl_xor_sync(0xffffffffu, t3, off);
+        }
+        if (rr == 0) {
+            s_part[mt][gi * 16 + 2 * cc] = t0;
+            s_part[mt][gi * 16 + 2 * cc + 1] = t1;
+            s_part[mt][gi * 16 + 8 + 2 * cc] = t2;
+            s_part[mt][gi * 16 + 8 + 2 * cc + 1] = t3;
+        }
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < ntok; t += kFineWarps * 32) {
+        const int bi = t / b, slot = t - bi * b;
+        const int p = s_pg[bi];
+        float f = -INFINITY;
+        if (p >= 0) {
+            const float sc = a.ic.kscale[(int64_t)p * a.ic.sps + (int64_t)h * a.ic.shs + slot];
+            f = sc * ((s_part[0][t] + s_part[1][t]) + (s_part[2][t] + s_part[3][t]));
+        }
+        frow[(int64_t)c0 * b + t] = f;
+    }
+    if constexpr (SEL) fine_select_tokens(a, r, hkv, ntok_row, b);
+}
+
+template <int DK, int HKV, bool SEL = false>
 cudaError_t launch_score_t(const ScoreArgs &a, cudaStream_t s)
 {
     dim3 grid((a.max_blocks + a.chunk - 1) / a.chunk, a.batch);
-    cudaError_t le = launch_step_kernel(k_score<DK, HKV>, grid, dim3(kScoreWarps * 32), 0, s, a);
+    cudaError_t le = launch_step_kernel(k_score<DK, HKV, SEL>, grid, dim3(kScoreWarps * 32), 0, s, a);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
@@ -452,6 +893,12 @@ cudaError_t launch_score(const ScoreArgs &a, cudaStream_t s, bool *unsupported)
 {
     *unsupported = false;
     if (a.batch == 0 || a.max_blocks == 0) return cudaSuccess;
+    if (a.sel_k > 0) {
+        // the coarse pass of the coarse-to-fine step (FP8 index summaries,
+        // one 128-dim index head)
+        *unsupported = !(a.dk == 128 && a.hkv == 1 && a.max_blocks <= kSelMaxCols);
+        return *unsupported ? cudaSuccess : launch_score_t<128, 1, true>(a, s);
+    }
 #define LSA_SCORE_CASE(D, H) \
     if (a.dk == D && a.hkv == H) return launch_score_t<D, H>(a, s);
     LSA_SCORE_CASE(64, 1) LSA_SCORE_CASE(64, 2) LSA_SCORE_CASE(64, 4) LSA_SCORE_CASE(64, 8)
@@ -459,6 +906,31 @@ cudaError_t launch_score(const ScoreArgs &a, cudaStream_t s, bool *unsupported)
     LSA_SCORE_CASE(256, 1) LSA_SCORE_CASE(256, 2) LSA_SCORE_CASE(256, 4) LSA_SCORE_CASE(256, 8)
     LSA_SCORE_CASE(576, 1)
 #undef LSA_SCORE_CASE
+    *unsupported = true;
+    return cudaSuccess;
+}
+
+bool score_quest_supported(int dk, int hkv, int group)
+{
+    return (dk == 64 || dk == 128) && (hkv == 1 || hkv == 2 || hkv == 4 || hkv == 8) &&
+           (group == 1 || group == 2 || group == 4 || group == 8);
+}
+
+cudaError_t launch_score_quest(const ScoreArgs &a, cudaStream_t s, bool *unsupported)
+{
+    *unsupported = false;
+    if (a.batch == 0 || a.max_blocks == 0) return cudaSuccess;
+    const int G = a.hq / a.hkv;
+#define LSA_QUEST_G(D, H)                                                    \
+    if (a.dk == D && a.hkv == H) {                                           \
+        if (G == 1) return launch_score_quest_t<D, H, 1>(a, s);               \
+        if (G == 2) return launch_score_quest_t<D, H, 2>(a, s);               \
+        if (G == 4) return launch_score_quest_t<D, H, 4>(a, s);               \
+        if (G == 8) return launch_score_quest_t<D, H, 8>(a, s);               \
+    }
+    LSA_QUEST_G(64, 1) LSA_QUEST_G(64, 2) LSA_QUEST_G(64, 4) LSA_QUEST_G(64, 8)
+    LSA_QUEST_G(128, 1) LSA_QUEST_G(128, 2) LSA_QUEST_G(128, 4) LSA_QUEST_G(128, 8)
+#undef LSA_QUEST_G
     *unsupported = true;
     return cudaSuccess;
 }
@@ -481,21 +953,38 @@ cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s, bool *unsupported)
     *unsupported = a.cols > kTopkMaxCols;
     if (*unsupported || a.rows == 0 || a.k == 0) return cudaSuccess;
     cudaError_t fe = cudaSuccess;
-    if (launch_topk_fast(a, s, &fe)) return fe;   // rows of up to 8192 columns
-    const size_t smem = (size_t)max(a.cols, 1) * sizeof(uint32_t);
-    cudaError_t e = cudaFuncSetAttribute(k_topk_rows, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    e = launch_step_kernel(k_topk_rows, dim3(a.rows), dim3(kTopkThreads), smem, s, a);
+    // rows of up to 8192 columns with k <= 64: the block top-k (a bound from
+    // the threads' maxima, then an exact rank of the few keys above it);
+    // wider rows and larger k: the radix select
+    if (a.k <= 64 && launch_topk_fast(a, s, &fe)) return fe;
+    cudaError_t e;
+    if (a.cols <= kTopkThreads * 8) e = launch_step_kernel(k_topk_rows<8>, dim3(a.rows), dim3(kTopkThreads), 0, s, a);
+    else if (a.cols <= kTopkThreads * 16) e = launch_step_kernel(k_topk_rows<16>, dim3(a.rows), dim3(kTopkThreads), 0, s, a);
+    else e = launch_step_kernel(k_topk_rows<32>, dim3(a.rows), dim3(kTopkThreads), 0, s, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 cudaError_t launch_fine_scores(const FineArgs &a, cudaStream_t s, bool *unsupported)
 {
-    *unsupported = a.ic.dk != 128 || !a.ic.e4m3 || a.ic.b % 4 != 0;
+    // a CTA scores kFineBlocksPerCta blocks of at most 64 tokens each
+    *unsupported = a.ic.dk != 128 || !a.ic.e4m3 || a.ic.b > 64 || a.ic.b % 16 != 0 ||
+                   (a.tok_k > 0 && (int64_t)a.ncand * a.ic.b > kFineMaxCols) ||
+                   (a.weights && a.hq / a.ic.hkv != 64);
     if (*unsupported || a.batch == 0 || a.ncand == 0) return cudaSuccess;
     dim3 grid((a.ncand + kFineBlocksPerCta - 1) / kFineBlocksPerCta, a.batch * a.ic.hkv);
-    cudaError_t le = launch_step_kernel(k_fine_scores, grid, dim3(kFineWarps * 32), 0, s, a);
+    cudaError_t le;
+    if (a.weights) {
+        auto kern = a.tok_k > 0 ? k_fine_scores_wrelu<true> : k_fine_scores_wrelu<false>;
+        le = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kWrSmem);
+        if (le != cudaSuccess) return le;
+        le = a.tok_k > 0 ? launch_kernel_ex(pdl_step_dependent(), kern, grid, dim3(kFineWarps * 32), kWrSmem, s, a)
+                         : launch_step_kernel(kern, grid, dim3(kFineWarps * 32), kWrSmem, s, a);
+    } else if (a.tok_k > 0) {
+        le = launch_kernel_ex(pdl_step_dependent(), k_fine_scores<true>, grid, dim3(kFineWarps * 32), 0, s, a);
+    } else {
+        le = launch_step_kernel(k_fine_scores<false>, grid, dim3(kFineWarps * 32), 0, s, a);
+    }
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }

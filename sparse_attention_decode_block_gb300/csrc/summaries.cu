@@ -1,5 +1,7 @@
 // Block summaries: the bf16 mean key of every full block, one warp per
-// (page, KV head) block.  The mean is summed in fp64 and rounded to bf16
+// (page, KV head) block; or Quest's element-wise maximum and minimum keys
+// of the block (Vortex blog post, end of "Why Long Generations Are
+// Expensive", and the Quest listing in "Writing an algorithm: vFlow").  The mean is summed in fp64 and rounded to bf16
 // once, so it does not depend on the order of the reduction (Vortex blog
 // post, "Block top-k attention": each block is summarized by its mean key,
 // computed once when the block fills; forward_cache of the vFlow listing).
@@ -96,6 +98,49 @@ __device__ void summarize_block(const CacheView &c, int64_t p, int h, uint16_t *
     }
 }
 
+// Quest summaries of one block (page p, head h): the element-wise maximum
+// and minimum of its b keys, written as [max (dk), min (dk)] bf16 (exact:
+// they are key values).  Lanes own 8-dim chunks; rows wider than a warp take
+// several chunks per lane.
+template <bool kNonCoherent>
+__device__ void minmax_block(const CacheView &c, int64_t p, int h, uint16_t *summ)
+{
+    const int lane = threadIdx.x & 31;
+    const int nch = c.dk / 8;
+    const uint8_t *base = c.k + (p * c.kps + (int64_t)h * c.khs) * 2;
+    uint16_t *dst = summ + (p * c.hkv + h) * (int64_t)2 * c.dk;
+    for (int ch = lane; ch < nch; ch += 32) {
+        float mx[8], mn[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            mx[i] = -INFINITY;
+            mn[i] = INFINITY;
+        }
+        for (int t = 0; t < c.b; ++t) {
+            const uint4 v = load16<kNonCoherent>(base + (int64_t)t * c.kts * 2 + ch * 16);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = bf2_to_f2(w[i]);
+                mx[2 * i] = fmaxf(mx[2 * i], f.x);
+                mx[2 * i + 1] = fmaxf(mx[2 * i + 1], f.y);
+                mn[2 * i] = fminf(mn[2 * i], f.x);
+                mn[2 * i + 1] = fminf(mn[2 * i + 1], f.y);
+            }
+        }
+        uint32_t px[4], pn[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            // bf16 values held as floats: the upper halves are the bits
+            px[i] = (__float_as_uint(mx[2 * i]) >> 16) | (__float_as_uint(mx[2 * i + 1]) & 0xffff0000u);
+            pn[i] = (__float_as_uint(mn[2 * i]) >> 16) | (__float_as_uint(mn[2 * i + 1]) & 0xffff0000u);
+        }
+        *reinterpret_cast<uint4 *>(dst + ch * 8) = make_uint4(px[0], px[1], px[2], px[3]);
+        *reinterpret_cast<uint4 *>(dst + c.dk + ch * 8) = make_uint4(pn[0], pn[1], pn[2], pn[3]);
+    }
+}
+
+template <bool QUEST>
 __global__ void __launch_bounds__(kWarpsPerCta * 32) k_build_summaries(SummaryArgs a)
 {
     const int64_t item = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
@@ -116,11 +161,13 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) k_build_summaries(SummaryAr
         if ((threadIdx.x & 31) == 0) flag_error(a.status, LSA_ERR_BOUNDS);
         return;
     }
-    summarize_block<true>(a.c, p, h, a.summ);
+    if constexpr (QUEST) minmax_block<true>(a.c, p, h, a.summ);
+    else summarize_block<true>(a.c, p, h, a.summ);
 }
 
 // One CTA per request, one warp per KV head: write the new token's key and
 // value into its slot, and when that fills the block, summarize it.
+template <bool QUEST>
 __global__ void k_append(SummaryArgs a)
 {
     const int r = blockIdx.x;
@@ -150,7 +197,8 @@ __global__ void k_append(SummaryArgs a)
         __syncwarp();
         if (t == c.b - 1) {
             __threadfence_block();
-            summarize_block<false>(c, p, h, a.summ);
+            if constexpr (QUEST) minmax_block<false>(c, p, h, a.summ);
+            else summarize_block<false>(c, p, h, a.summ);
         }
     }
     __syncthreads();
@@ -159,20 +207,22 @@ __global__ void k_append(SummaryArgs a)
 
 }  // namespace
 
-cudaError_t launch_build_summaries(const SummaryArgs &a, cudaStream_t s)
+cudaError_t launch_build_summaries(const SummaryArgs &a, cudaStream_t s, bool quest)
 {
     const int64_t items = (int64_t)a.batch * a.max_blocks * a.c.hkv;
     if (items == 0) return cudaSuccess;
     const int64_t grid = (items + kWarpsPerCta - 1) / kWarpsPerCta;
-    k_build_summaries<<<(unsigned)grid, kWarpsPerCta * 32, 0, s>>>(a);
+    if (quest) k_build_summaries<true><<<(unsigned)grid, kWarpsPerCta * 32, 0, s>>>(a);
+    else k_build_summaries<false><<<(unsigned)grid, kWarpsPerCta * 32, 0, s>>>(a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_append(const SummaryArgs &a, cudaStream_t s, bool *unsupported)
+cudaError_t launch_append(const SummaryArgs &a, cudaStream_t s, bool quest, bool *unsupported)
 {
-    *unsupported = a.c.e4m3 != 0 || a.c.hkv > 32;
+    *unsupported = a.c.e4m3 != 0 || a.c.hkv > 32 || (quest && a.c.dk % 8 != 0);
     if (*unsupported || a.batch == 0) return cudaSuccess;
-    k_append<<<a.batch, 32 * a.c.hkv, 0, s>>>(a);
+    if (quest) k_append<true><<<a.batch, 32 * a.c.hkv, 0, s>>>(a);
+    else k_append<false><<<a.batch, 32 * a.c.hkv, 0, s>>>(a);
     return cudaGetLastError();
 }
 

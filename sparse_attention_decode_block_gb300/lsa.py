@@ -29,8 +29,11 @@ LSA_ERR_CUDA = 6
 LSA_ERR_NAN = 7
 LSA_KEYS_BF16 = 0
 LSA_KEYS_E4M3 = 1
+LSA_SUMMARY_MEAN = 0
+LSA_SUMMARY_MINMAX = 1
 
 EXPORTED = ["lsa_status_string", "lsa_get_device_status", "lsa_build_summaries", "lsa_append_block",
+            "lsa_build_minmax_summaries", "lsa_append_block_minmax",
             "lsa_score", "lsa_topk", "lsa_fine_topk", "lsa_sparse_decode_workspace_size",
             "lsa_sparse_decode", "lsa_decode_step_workspace_size", "lsa_decode_step",
             "lsa_sparse_decode_static_scratch"]
@@ -55,7 +58,8 @@ class lsa_params(C.Structure):
     _fields_ = [("batch", C.c_int32), ("num_q_heads", C.c_int32), ("max_blocks", C.c_int32),
                 ("k_blocks", C.c_int32), ("sink_tokens", C.c_int32), ("recent_tokens", C.c_int32),
                 ("softmax_scale", C.c_float), ("c2f_candidates", C.c_int32), ("c2f_tokens", C.c_int32),
-                ("num_splits", C.c_int32)]
+                ("num_splits", C.c_int32), ("summary_kind", C.c_int32),
+                ("fine_head_weights", C.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -80,6 +84,8 @@ def load_library(path: Optional[str] = None):
             "lsa_get_device_status": ([P(C.c_uint32), C.c_int], C.c_int),
             "lsa_build_summaries": ([cache_p, V, V, I, I, V, V], C.c_int),
             "lsa_append_block": ([cache_p, V, V, V, V, I, I, V, V], C.c_int),
+            "lsa_build_minmax_summaries": ([cache_p, V, V, I, I, V, V], C.c_int),
+            "lsa_append_block_minmax": ([cache_p, V, V, V, V, I, I, V, V], C.c_int),
             "lsa_score": ([V, cache_p, V, V, V, params_p, V, V], C.c_int),
             "lsa_topk": ([V, V, I, I, I, V, V], C.c_int),
             "lsa_fine_topk": ([V, cache_p, V, V, V, params_p, V, V, S, V], C.c_int),
@@ -147,10 +153,13 @@ def make_cache(k: torch.Tensor, v: Optional[torch.Tensor] = None, *, k_scale: Op
 
 
 def make_params(batch, num_q_heads, max_blocks, k_blocks=0, sink_tokens=0, recent_tokens=0,
-                softmax_scale=0.0, c2f_candidates=0, c2f_tokens=0, num_splits=0) -> lsa_params:
+                softmax_scale=0.0, c2f_candidates=0, c2f_tokens=0, num_splits=0, summary_kind=0,
+                fine_head_weights: Optional[torch.Tensor] = None) -> lsa_params:
+    """fine_head_weights: device fp32 [batch, num_q_heads]; the caller keeps
+    the tensor alive while the parameters are in use."""
     return lsa_params(int(batch), int(num_q_heads), int(max_blocks), int(k_blocks), int(sink_tokens),
                       int(recent_tokens), float(softmax_scale), int(c2f_candidates), int(c2f_tokens),
-                      int(num_splits))
+                      int(num_splits), int(summary_kind), _ptr(fine_head_weights))
 
 
 def lsa_get_device_status(clear: bool = True):
@@ -164,6 +173,19 @@ def lsa_build_summaries(cache: lsa_cache, page_table, seq_lens, summaries, strea
     B, maxb = page_table.shape
     _check(load_library().lsa_build_summaries(C.byref(cache), _ptr(page_table), _ptr(seq_lens), B, maxb,
                                               _ptr(summaries), _stream(stream)), "lsa_build_summaries")
+
+
+def lsa_build_minmax_summaries(cache: lsa_cache, page_table, seq_lens, summaries, stream=None):
+    B, maxb = page_table.shape
+    _check(load_library().lsa_build_minmax_summaries(C.byref(cache), _ptr(page_table), _ptr(seq_lens), B, maxb,
+                                                     _ptr(summaries), _stream(stream)), "lsa_build_minmax_summaries")
+
+
+def lsa_append_block_minmax(cache: lsa_cache, k_new, v_new, page_table, seq_lens, summaries, stream=None):
+    B, maxb = page_table.shape
+    _check(load_library().lsa_append_block_minmax(C.byref(cache), _ptr(k_new), _ptr(v_new), _ptr(page_table),
+                                                  _ptr(seq_lens), B, maxb, _ptr(summaries), _stream(stream)),
+           "lsa_append_block_minmax")
 
 
 def lsa_append_block(cache: lsa_cache, k_new, v_new, page_table, seq_lens, summaries, stream=None):

@@ -63,6 +63,8 @@ def subset(inp: dict, reqs) -> dict:
     if "idx_keys" in inp:
         out["idx_keys"] = inp["idx_keys"][uniq.to(inp["idx_keys"].device)].cpu()
         out["idx_scale"] = inp["idx_scale"][uniq.to(inp["idx_scale"].device)].cpu()
+    if "fine_weights" in inp:
+        out["fine_weights"] = inp["fine_weights"][list(reqs)].cpu()
     return out
 
 
@@ -81,12 +83,16 @@ def oracle_decode(w: Workload, cpu: dict, nthreads: int = os.cpu_count() or 1, *
         ic = oracle_index(cpu)
         isumm, _ = oracle.summaries(ic, cpu["page_table"], cpu["seq_lens"], use_index_keys=True)
         kw.update(index_cache=ic, index_summ=isumm, c2f_candidates=w.c2f_candidates,
-                  c2f_tokens=w.c2f_tokens)
+                  c2f_tokens=w.c2f_tokens, fine_weights=cpu.get("fine_weights"))
     kw.update(over)
     c = oracle_cache(cpu)
     summ = None
     if w.c2f_candidates == 0:
-        summ, _ = oracle.summaries(c, cpu["page_table"], cpu["seq_lens"])
+        if w.summary_kind == 1:
+            summ, _ = oracle.quest_summaries(c, cpu["page_table"], cpu["seq_lens"])
+            kw["summary_kind"] = 1
+        else:
+            summ, _ = oracle.summaries(c, cpu["page_table"], cpu["seq_lens"])
     return oracle.decode(cpu["q"], c, cpu["page_table"], cpu["seq_lens"], summ=summ, **kw)
 
 
@@ -106,12 +112,17 @@ class GpuStep:
             self.summ = torch.zeros((g["num_pages"], Hkv, w.dk), dtype=torch.bfloat16, device=dev)
             L.lsa_build_summaries(self.icache, g["page_table"], g["seq_lens"], self.summ)
             nsel = w.c2f_tokens
+        elif w.summary_kind == 1:
+            self.summ = torch.zeros((g["num_pages"], Hkv, 2, w.dk), dtype=torch.bfloat16, device=dev)
+            L.lsa_build_minmax_summaries(self.cache, g["page_table"], g["seq_lens"], self.summ)
+            nsel = w.k_blocks
         else:
             self.summ = torch.zeros((g["num_pages"], Hkv, w.dk), dtype=torch.bfloat16, device=dev)
             L.lsa_build_summaries(self.cache, g["page_table"], g["seq_lens"], self.summ)
             nsel = w.k_blocks
         self.params = L.make_params(B, w.num_q_heads, g["max_blocks"], w.k_blocks, w.sink, w.recent,
-                                    w.softmax_scale, w.c2f_candidates, w.c2f_tokens, num_splits)
+                                    w.softmax_scale, w.c2f_candidates, w.c2f_tokens, num_splits,
+                                    summary_kind=w.summary_kind, fine_head_weights=g.get("fine_weights"))
         ws = L.lsa_decode_step_workspace_size(self.cache, self.params)
         assert ws > 0 or w.batch == 0 or True
         self.ws = torch.zeros(max(ws, 16), dtype=torch.uint8, device=dev)
@@ -153,6 +164,16 @@ def assert_lse_close(lse_gpu: torch.Tensor, lse_ref: np.ndarray, what: str = "")
     d = np.where(both_inf, 0.0, np.abs(l - lse_ref))
     lim = LSE_ATOL + LSE_RTOL * np.where(both_inf, 0.0, np.abs(lse_ref))
     assert np.all(d <= lim), f"{what}: lse max err {np.nanmax(d):.3g}"
+
+
+def quest_score_bound(q_bits: np.ndarray, mx_f64: np.ndarray, mn_f64: np.ndarray, dk: int) -> np.ndarray:
+    """Upper bound on |fp32 GPU Quest score - exact score| per block: each
+    head's sum of dk rounded products (each max(q M, q m) exact up to one
+    product rounding) is off by at most 2 dk 2^-24 sum_i |q_i| max(|M_i|,
+    |m_i|); the maximum over heads is exact.  Twice that, for safety."""
+    q = np.abs(f64(q_bits))                        # [G, dk]
+    a = np.maximum(np.abs(mx_f64), np.abs(mn_f64))   # [nblocks, dk]
+    return 4 * dk * 2.0 ** -24 * (a @ q.T).max(axis=1)
 
 
 def score_bound(q_bits: np.ndarray, summ_f64: np.ndarray, G: int, dk: int) -> np.ndarray:

@@ -12,13 +12,14 @@ import torch
 import oracle
 import sparse_attention_decode_block_gb300 as L
 from helpers import (GpuStep, assert_attention_close, assert_lse_close, bits, check_status_clean,
-                     compare_selection, f64, oracle_cache, oracle_decode, oracle_index, score_bound, subset,
-                     to_dev)
+                     compare_selection, f64, oracle_cache, oracle_decode, oracle_index, quest_score_bound,
+                     score_bound, subset, to_dev)
 from workloads import WORKLOADS, make_inputs, small_workloads
 
 pytestmark = pytest.mark.gpu
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
 SMALL = ["tiny", "b16_small", "ragged_small", "mla_small"]
+QUEST = ["quest_small"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -74,6 +75,78 @@ def test_summaries_bit_exact_block_48():
     assert np.array_equal(got[valid], ref[valid])
     # and the whole step at b = 48 (three 16-token items per block)
     run_and_compare_step(w, cpu, g)
+
+
+def test_quest_summaries_bit_exact_and_append_matches_bulk():
+    """Quest's max / min key summaries: bit-exact against the oracle, and
+    appending tokens one by one builds the same summaries as the bulk call."""
+    w = small("quest_small")
+    cpu = make_inputs(w, "cpu")
+    g = to_dev(cpu)
+    c = L.make_cache(g["k_cache"], g["v_cache"])
+    summ = torch.zeros((cpu["num_pages"], w.num_kv_heads, 2, w.dk), dtype=torch.bfloat16, device="cuda")
+    L.lsa_build_minmax_summaries(c, g["page_table"], g["seq_lens"], summ)
+    check_status_clean()
+    ref, valid = oracle.quest_summaries(oracle_cache(cpu), cpu["page_table"], cpu["seq_lens"])
+    got = bits(summ)
+    assert valid.any()
+    assert np.array_equal(got[valid], ref[valid])
+    assert np.all(got[~valid] == 0)
+    # append: the last 40 tokens of each request one at a time
+    lens0 = [L_ - 40 for L_ in cpu["lens"]]
+    kc = g["k_cache"].clone()
+    vc = g["v_cache"].clone()
+    cache2 = L.make_cache(kc, vc)
+    lens = torch.tensor(lens0, dtype=torch.int32, device="cuda")
+    summ2 = torch.zeros_like(summ)
+    L.lsa_build_minmax_summaries(cache2, g["page_table"], lens, summ2)
+    pt = cpu["page_table"]
+    b = w.block_size
+    for step in range(40):
+        kn = torch.empty((w.batch, w.num_kv_heads, w.dk), dtype=torch.bfloat16, device="cuda")
+        vn = torch.empty_like(kn)
+        for r in range(w.batch):
+            t = lens0[r] + step
+            p = int(pt[r, t // b])
+            kn[r] = g["k_cache"][p, :, t % b]
+            vn[r] = g["v_cache"][p, :, t % b]
+        L.lsa_append_block_minmax(cache2, kn, vn, g["page_table"], lens, summ2)
+    check_status_clean()
+    assert lens.tolist() == list(cpu["lens"])
+    assert torch.equal(summ2.view(torch.int16), summ.view(torch.int16))
+
+
+def test_quest_scores_within_rounding_and_topk_bit_exact():
+    w = small("quest_small")
+    cpu = make_inputs(w, "cpu")
+    g = to_dev(cpu)
+    c = L.make_cache(g["k_cache"], g["v_cache"])
+    summ = torch.zeros((cpu["num_pages"], w.num_kv_heads, 2, w.dk), dtype=torch.bfloat16, device="cuda")
+    L.lsa_build_minmax_summaries(c, g["page_table"], g["seq_lens"], summ)
+    prm = L.make_params(w.batch, w.num_q_heads, cpu["max_blocks"], w.k_blocks, w.sink, w.recent,
+                        summary_kind=L.LSA_SUMMARY_MINMAX)
+    scores = torch.empty((w.batch, w.num_kv_heads, cpu["max_blocks"]), dtype=torch.float32, device="cuda")
+    L.lsa_score(g["q"], c, summ, g["page_table"], g["seq_lens"], prm, scores)
+    check_status_clean()
+    oc = oracle_cache(cpu)
+    osumm, _ = oracle.quest_summaries(oc, cpu["page_table"], cpu["seq_lens"])
+    ref = oracle.block_scores(cpu["q"], oc, osumm, cpu["page_table"], cpu["seq_lens"], w.num_q_heads, w.sink,
+                              w.recent, summary_kind=1)
+    got = scores.cpu().numpy().astype(np.float64)
+    assert np.array_equal(np.isneginf(got), np.isneginf(ref))
+    S = f64(osumm)
+    G = w.group
+    for r in range(w.batch):
+        pg = np.maximum(cpu["page_table"][r].numpy(), 0)
+        for h in range(w.num_kv_heads):
+            fin = np.isfinite(ref[r, h])
+            tau = quest_score_bound(bits(cpu["q"][r, h * G:(h + 1) * G]), S[pg, h, 0], S[pg, h, 1], w.dk)
+            assert np.all(np.abs(got[r, h][fin] - ref[r, h][fin]) <= tau[fin] + 1e-30)
+    idx = torch.empty((w.batch * w.num_kv_heads, w.k_blocks), dtype=torch.int32, device="cuda")
+    L.lsa_topk(scores.view(w.batch * w.num_kv_heads, -1), None, w.k_blocks, idx)
+    check_status_clean()
+    want = oracle.topk(got.reshape(w.batch * w.num_kv_heads, -1), w.k_blocks)
+    assert np.array_equal(idx.cpu().numpy(), want)
 
 
 def test_append_matches_bulk_build():
@@ -256,15 +329,18 @@ def compare_step_rows(st, w, cpu, reqs):
     ties = 0
     if not use8:
         oc = oracle_cache(sub)
-        osumm, _ = oracle.summaries(oc, sub["page_table"], sub["seq_lens"])
+        quest = w.summary_kind == 1
+        osumm, _ = (oracle.quest_summaries if quest else oracle.summaries)(oc, sub["page_table"], sub["seq_lens"])
         sc = oracle.block_scores(sub["q"], oc, osumm, sub["page_table"], sub["seq_lens"], w.num_q_heads, w.sink,
-                                 w.recent)
+                                 w.recent, summary_kind=w.summary_kind)
         S = f64(osumm)
         G = w.group
         for i in range(len(reqs)):
             for h in range(w.num_kv_heads):
                 pg = np.maximum(sub["page_table"][i].cpu().numpy(), 0)
-                tau = score_bound(bits(sub["q"][i, h * G:(h + 1) * G]), S[pg, h], G, w.dk)
+                qb = bits(sub["q"][i, h * G:(h + 1) * G])
+                tau = (quest_score_bound(qb, S[pg, h, 0], S[pg, h, 1], w.dk) if quest
+                       else score_bound(qb, S[pg, h], G, w.dk))
                 kind = compare_selection(sel_gpu[i, h], ref["sel"][i, h], sc[i, h], tau)
                 ties += kind == "tie"
     else:
@@ -290,7 +366,7 @@ def run_and_compare_step(w, cpu, g, reqs=None, num_splits=0):
     return compare_step_rows(st, w, cpu, range(w.batch) if reqs is None else reqs)
 
 
-@pytest.mark.parametrize("name", SMALL + ["c2f_small"])
+@pytest.mark.parametrize("name", SMALL + ["c2f_small", "c2f_wrelu_small"] + QUEST)
 def test_decode_step_end_to_end(name):
     w = small(name)
     cpu = make_inputs(w, "cpu")
@@ -461,14 +537,17 @@ def test_latent_cache_aliased_and_copied_values_agree():
 
 # ---------------------------------------------------------------- coarse-to-fine
 
-def test_fine_topk_matches_oracle():
-    w = small("c2f_small")
+@pytest.mark.parametrize("name", ["c2f_small", "c2f_wrelu_small"])
+def test_fine_topk_matches_oracle(name):
+    """The fine pass alone (lsa_fine_topk) over the oracle's candidates: the
+    head-sum score, and the weighted-ReLU indexer score on tensor cores."""
+    w = small(name)
     cpu = make_inputs(w, "cpu")
     g = to_dev(cpu)
     ref = oracle_decode(w, cpu)
     ic = L.make_cache(g["idx_keys"], None, k_scale=g["idx_scale"])
     prm = L.make_params(w.batch, w.num_q_heads, cpu["max_blocks"], 0, w.sink, w.recent, w.softmax_scale,
-                        w.c2f_candidates, w.c2f_tokens)
+                        w.c2f_candidates, w.c2f_tokens, fine_head_weights=g.get("fine_weights"))
     cand = torch.from_numpy(ref["cand"]).cuda()
     tok = torch.empty((w.batch, 1, w.c2f_tokens), dtype=torch.int32, device="cuda")
     ws = torch.empty(w.batch * w.c2f_candidates * w.block_size * 4 + 256, dtype=torch.uint8, device="cuda")
@@ -483,10 +562,10 @@ def test_fine_topk_matches_oracle():
 
 # ---------------------------------------------------------------- full-size workloads
 
-FULL_CHUNK = {"b16_32k": 16, "ragged": 8, "c2f": 4, "mla": 2}
+FULL_CHUNK = {"b16_32k": 16, "b16_32k_quest": 16, "ragged": 8, "c2f": 4, "c2f_wrelu": 4, "mla": 2}
 
 
-@pytest.mark.parametrize("name", ["b16_32k", "ragged", "c2f", "mla"])
+@pytest.mark.parametrize("name", ["b16_32k", "b16_32k_quest", "ragged", "c2f", "c2f_wrelu", "mla"])
 def test_full_size_every_request(name):
     """Every request of the full-size workloads, from one call over the whole
     batch, checked against the oracle: the oracle runs on groups of requests

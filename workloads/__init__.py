@@ -17,7 +17,7 @@ Workload shapes follow the pages' workloads:
 
 Draw order for every workload, from one ``torch.Generator`` seeded with the
 workload's seed: lengths -> page permutation -> q -> K -> V -> per-(request,
-KV head) shifted blocks -> FP8 index keys.
+KV head) shifted blocks -> FP8 index keys -> indexer head weights.
 """
 from __future__ import annotations
 
@@ -56,6 +56,8 @@ class Workload:
     v_aliased: bool = False     # V = K[..., :dv] (latent cache)
     c2f_candidates: int = 0
     c2f_tokens: int = 0
+    summary_kind: int = 0       # 0: mean keys; 1: Quest's max and min keys
+    fine_weighted: bool = False  # coarse-to-fine: weighted-ReLU fine score with drawn head weights
     extra_pages: int = 0        # unused pages appended to the pool
     description: str = ""
 
@@ -83,6 +85,11 @@ WORKLOADS = {
         shift_frac=0.05, shift_sigma=2.0,
         description="B=16, 32q/8kv, d=128, L=32768, block 16, top-64 blocks incl. first and "
                     "last, 5% of blocks shifted +2 sigma along the group's mean query"),
+    "b16_32k_quest": Workload(
+        name="b16_32k_quest", seed=1, batch=16, num_q_heads=32, num_kv_heads=8, dk=128, dv=128,
+        block_size=16, seq_len=32768, sink=16, recent=16, k_blocks=62,
+        shift_frac=0.05, shift_sigma=2.0, summary_kind=1,
+        description="the B=16 x 32K workload with Quest's min/max key summaries and bound scores"),
     "ragged": Workload(
         name="ragged", seed=2, batch=64, num_q_heads=32, num_kv_heads=8, dk=128, dv=128,
         block_size=64, seq_len_range=(4096, 131072), sink=4, recent=512, k_blocks=23,
@@ -94,6 +101,12 @@ WORKLOADS = {
         c2f_candidates=256, c2f_tokens=2048,
         description="B=4, L=512K, block 64, coarse top-256 blocks, fine FP8 top-2048 tokens, "
                     "64q/1kv, d=128"),
+    "c2f_wrelu": Workload(
+        name="c2f_wrelu", seed=3, batch=4, num_q_heads=64, num_kv_heads=1, dk=128, dv=128,
+        block_size=64, seq_len=524288, sink=0, recent=0, k_blocks=0,
+        c2f_candidates=256, c2f_tokens=2048, fine_weighted=True,
+        description="the coarse-to-fine workload with the weighted-ReLU indexer fine score "
+                    "(head weights ~ U[0, 1))"),
     "mla": Workload(
         name="mla", seed=4, batch=4, num_q_heads=64, num_kv_heads=1, dk=576, dv=512,
         block_size=64, seq_len=1048576, sink=4, recent=128, k_blocks=29, v_aliased=True,
@@ -119,6 +132,11 @@ def small_workloads() -> dict:
             c2f_candidates=32, c2f_tokens=512, recent=37),
         "mla_small": W["mla"].replace(
             name="mla_small", seed=14, batch=2, seq_len=0, seq_lens=(20000, 6001)),
+        "c2f_wrelu_small": W["c2f_wrelu"].replace(
+            name="c2f_wrelu_small", seed=16, batch=2, seq_len=0, seq_lens=(16384 + 37, 9000),
+            c2f_candidates=32, c2f_tokens=512, recent=37),
+        "quest_small": W["b16_32k_quest"].replace(
+            name="quest_small", seed=15, batch=3, seq_len=0, seq_lens=(4096, 3001, 777)),
     }
 
 
@@ -215,6 +233,9 @@ def make_inputs(w: Workload, device: str = "cpu", lens: Optional[Sequence[int]] 
         k8 = (kk / scale.unsqueeze(-1)).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
         out["idx_keys"] = k8.view(torch.uint8)
         out["idx_scale"] = scale.contiguous()
+        if w.fine_weighted:
+            # indexer head weights of the weighted-ReLU fine score
+            out["fine_weights"] = torch.rand((B, Hq), generator=g, device=dev, dtype=torch.float32)
     return out
 
 
@@ -240,7 +261,7 @@ def algorithmic_bytes(w: Workload, lens: Sequence[int]) -> dict:
                 ncand += 1
         nblk = (L + b - 1) // b
         pt += nblk * 4
-        summ += ncand * Hkv * w.dk * 2
+        summ += ncand * Hkv * w.dk * 2 * (2 if w.summary_kind == 1 else 1)
         if w.c2f_candidates > 0:
             ncb = min(w.c2f_candidates, ncand)
             fine += ncb * b * Hkv * (w.dk * 1 + 4)
