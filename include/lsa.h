@@ -221,6 +221,30 @@ lsa_status lsa_score(const void *q, const lsa_cache *cache, const void *summarie
 lsa_status lsa_topk(const float *scores, const int32_t *num_cols, int32_t rows, int32_t cols,
                     int32_t k, int32_t *idx, lsa_stream_t stream);
 
+/* Row-wise APPROXIMATE top-k, the stochastic early exit (Vortex blog post,
+ * "Making it fast": a monotone remap spreads the scores over the buckets of
+ * a radix-style select, and the select stops once it has enough confident
+ * winners, sampling the rest from the boundary bucket).  Opt-in; it trades
+ * recall of the exact top-k for speed.  Per row, over the candidates
+ * (entries as for lsa_topk), keff = min(k, candidates):
+ *   1. bucket(x) = floor((x - vmin) * (2048 / (vmax - vmin))), clamped to
+ *      2047, in fp32 over the candidates' smallest and largest value (one
+ *      bucket when they are equal or the span is not finite);
+ *   2. the candidates in buckets above the one holding the keff-th largest
+ *      value (the boundary bucket, cnt candidates) are all taken;
+ *   3. the remaining `take` are the boundary bucket's candidates numbered,
+ *      in column order, within `take` steps after off circularly:
+ *      number n is taken iff (n - off) mod cnt < take, with
+ *      off = splitmix64(seed, row + 1) mod cnt, where splitmix64(s, n) is
+ *      output n of SplitMix64 (Steele, Lea and Flood, OOPSLA 2014) seeded
+ *      with s.
+ * Every candidate above the boundary bucket is kept, and every one in it is
+ * kept with probability take / cnt over the seed.  The result is a
+ * deterministic function of (scores, k, seed, row).  idx as lsa_topk.
+ * Supported: cols <= 32768.  Errors as lsa_topk. */
+lsa_status lsa_topk_approx(const float *scores, const int32_t *num_cols, int32_t rows, int32_t cols,
+                           int32_t k, uint64_t seed, int32_t *idx, lsa_stream_t stream);
+
 /* Coarse-to-fine fine pass: for every token t of the candidate blocks
  * cand[r, h, :] (ascending, -1 padded, c2f_candidates per row) of request r,
  *   f_t = scale_t * sum_{g in group(h)} q[r,g,:] . e4m3(k8_t)

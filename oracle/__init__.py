@@ -73,6 +73,10 @@ def _load():
             lib.orc_quest_summaries.argtypes = [P, P, P, I, I, P, P]
             lib.orc_block_scores.argtypes = [P, P, C.c_int, P, P, P, P, P]
             lib.orc_topk.argtypes = [P, I, I, P]
+            lib.orc_splitmix64.argtypes = [C.c_uint64, C.c_uint64]
+            lib.orc_splitmix64.restype = C.c_uint64
+            lib.orc_topk_approx.argtypes = [P, I, I, I, C.c_uint64, C.c_int64, P]
+            lib.orc_topk_approx.restype = C.c_int
             lib.orc_fine_scores.argtypes = [P, P, P, P, C.c_int, C.c_int, C.c_int64, P, P, P]
             lib.orc_decode.argtypes = [P, P, P, P, P, P, P, P, C.c_int, P, P, P, P]
             lib.orc_dense.argtypes = [P, P, P, P, P, P, P]
@@ -235,6 +239,27 @@ def topk(scores, k: int) -> np.ndarray:
         o = np.empty((k,), dtype=np.int32)
         _check(lib.orc_topk(_p(row), row.shape[0], k, _p(o)))
         out[i] = o
+    return out.reshape(s.shape[:-1] + (k,))
+
+
+def splitmix64(seed: int, n: int) -> int:
+    """Output n (n >= 1) of SplitMix64 seeded with ``seed``."""
+    return int(_load().orc_splitmix64(seed & (2**64 - 1), n & (2**64 - 1)))
+
+
+def topk_approx(scores, k: int, seed: int, nbins: int = 2048, row0: int = 0) -> np.ndarray:
+    """Row-wise approximate top-k with the stochastic early exit (the
+    boundary bucket sampled): rows of fp32 scores, row i drawing
+    splitmix64(seed, row0 + i + 1).  Indices ascending, -1 padded."""
+    lib = _load()
+    s = np.ascontiguousarray(np.asarray(scores, dtype=np.float32))
+    s2 = s.reshape(-1, s.shape[-1])
+    out = np.empty((s2.shape[0], k), dtype=np.int32)
+    for i in range(s2.shape[0]):
+        row = np.ascontiguousarray(s2[i])
+        o = np.empty((max(k, 1),), dtype=np.int32)
+        _check(lib.orc_topk_approx(_p(row), row.shape[0], k, nbins, seed & (2**64 - 1), row0 + i, _p(o)))
+        out[i] = o[:k]
     return out.reshape(s.shape[:-1] + (k,))
 
 

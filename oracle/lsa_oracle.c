@@ -417,6 +417,109 @@ int orc_topk(const double *scores, int32_t n, int32_t k, int32_t *out)
     return ORC_OK;
 }
 
+/* SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+ * generators", OOPSLA 2014): the state advances by the golden-ratio
+ * increment 0x9e3779b97f4a7c15 and each output is the state passed through
+ * the variant-13 finaliser (xor-shift 30, multiply, xor-shift 27, multiply,
+ * xor-shift 31).  Used counter-style: output n (n >= 1) of the generator
+ * seeded with `seed` is mix(seed + n * increment). */
+uint64_t orc_splitmix64(uint64_t seed, uint64_t n)
+{
+    uint64_t z = seed + n * 0x9e3779b97f4a7c15ULL;
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ULL;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebULL;
+    return z ^ (z >> 31);
+}
+
+/* Approximate top-k with a stochastic early exit (Vortex blog post, "Making
+ * it fast": a monotone remap spreads the scores over the buckets, and the
+ * selection stops once it has enough confident winners, sampling the rest
+ * from the boundary bucket).  The steps, in that order, for one row of n
+ * fp32 scores (-inf and NaN are not candidates; keff = min(k, candidates)):
+ *   1. remap: bucket(x) = floor((x - vmin) * (nbins / (vmax - vmin))),
+ *      clamped to nbins - 1, over the candidates' smallest and largest
+ *      value, in fp32 (one bucket when vmax == vmin or the span is not
+ *      finite); larger values never fall in lower buckets;
+ *   2. the boundary bucket B holds the keff-th largest value: the G
+ *      candidates in buckets above B are the confident winners (G < keff);
+ *   3. the remaining keff - G are sampled from the cnt candidates of B: in
+ *      column order they are numbered 0 .. cnt-1, and those whose number is
+ *      within keff - G steps after off = splitmix64(seed, row + 1) mod cnt,
+ *      circularly, are taken (every one of them is taken with probability
+ *      (keff - G) / cnt over the seed).
+ * Output: the chosen columns ascending, -1 padded to k. */
+int orc_topk_approx(const float *scores, int32_t n, int32_t k, int32_t nbins, uint64_t seed, int64_t row,
+                    int32_t *out)
+{
+    if (nbins < 1)
+        return ORC_BAD_ARG;
+    int32_t m = 0;
+    float vmin = INFINITY, vmax = -INFINITY;
+    for (int32_t i = 0; i < n; ++i) {
+        const float x = scores[i];
+        if (isnan(x) || x == -INFINITY)
+            continue;
+        ++m;
+        if (x < vmin)
+            vmin = x;
+        if (x > vmax)
+            vmax = x;
+    }
+    const int32_t keff = k < m ? (k > 0 ? k : 0) : m;
+    int32_t nout = 0;
+    if (keff == m) {
+        for (int32_t i = 0; i < n; ++i)
+            if (!(isnan(scores[i]) || scores[i] == -INFINITY))
+                out[nout++] = i;
+    } else if (keff > 0) {
+        const float span = vmax - vmin;
+        const float scale = (span > 0.0f && span < INFINITY) ? (float)nbins / span : 0.0f;
+        int32_t *bucket = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
+        int64_t *count = (int64_t *)calloc((size_t)nbins, sizeof(int64_t));
+        if (!bucket || !count) {
+            free(bucket);
+            free(count);
+            return ORC_NOMEM;
+        }
+        for (int32_t i = 0; i < n; ++i) {
+            const float x = scores[i];
+            bucket[i] = -1;
+            if (isnan(x) || x == -INFINITY)
+                continue;
+            int32_t bk = 0;
+            if (scale != 0.0f) {
+                const float y = (x - vmin) * scale;
+                bk = y >= (float)(nbins - 1) ? nbins - 1 : (int32_t)y;
+            }
+            bucket[i] = bk;
+            count[bk]++;
+        }
+        int64_t above = 0;
+        int32_t B = nbins - 1;
+        while (above + count[B] < keff) {
+            above += count[B];
+            --B;
+        }
+        const int64_t cnt = count[B], take = keff - above;
+        const int64_t off = (int64_t)(orc_splitmix64(seed, (uint64_t)row + 1) % (uint64_t)cnt);
+        int64_t rank = 0;
+        for (int32_t i = 0; i < n; ++i) {
+            if (bucket[i] > B) {
+                out[nout++] = i;
+            } else if (bucket[i] == B) {
+                if ((rank - off + cnt) % cnt < take)
+                    out[nout++] = i;
+                ++rank;
+            }
+        }
+        free(bucket);
+        free(count);
+    }
+    for (int32_t i = nout; i < k; ++i)
+        out[i] = -1;
+    return ORC_OK;
+}
+
 /* ------------------------------------------------------------------ */
 /* Step: attention over a token set                                    */
 /* ------------------------------------------------------------------ */

@@ -375,16 +375,8 @@ lsa_status run_attention(const void *q, const CacheView &v, const int32_t *pt, c
 
 // Workspace of the decode step: [scores | selection | c2f extras | attention].
 struct StepLayout {
-    size_t scores, sel, cand, fine, ctrl, attn, total;
+    size_t scores, sel, cand, fine, attn, total;
 };
-
-// The coarse-to-fine step as three launches: the coarse kernel's last CTA
-// per request selects the candidates, the fine kernel's the tokens.
-bool c2f_fused(const CacheView &iv, const lsa_params *p)
-{
-    return iv.dk == 128 && iv.hkv == 1 && iv.b <= 64 && p->max_blocks <= 8192 && p->c2f_tokens > 0 &&
-           (int64_t)p->c2f_candidates * iv.b <= 16384;
-}
 
 lsa_status step_layout(const CacheView &v, const CacheView *iv, const lsa_params *p, StepLayout *L)
 {
@@ -398,10 +390,8 @@ lsa_status step_layout(const CacheView &v, const CacheView *iv, const lsa_params
     L->sel = round_up(rows * (size_t)(c2f ? p->c2f_tokens : p->k_blocks) * sizeof(int32_t));
     L->cand = c2f ? round_up(rows * (size_t)p->c2f_candidates * sizeof(int32_t)) : 0;
     L->fine = c2f ? round_up(rows * (size_t)p->c2f_candidates * sv.b * sizeof(float)) : 0;
-    // per request: coarse CTAs done, candidates ready, fine CTAs done
-    L->ctrl = c2f ? round_up(3 * (size_t)p->batch * sizeof(uint32_t)) : 0;
     L->attn = pl.ws_bytes;
-    L->total = L->scores + L->sel + L->cand + L->fine + L->ctrl + L->attn;
+    L->total = L->scores + L->sel + L->cand + L->fine + L->attn;
     return LSA_OK;
 }
 
@@ -608,6 +598,29 @@ lsa_status lsa_topk(const float *scores, const int32_t *num_cols, int32_t rows, 
     return from_cuda(e);
 }
 
+lsa_status lsa_topk_approx(const float *scores, const int32_t *num_cols, int32_t rows, int32_t cols, int32_t k,
+                           uint64_t seed, int32_t *idx, lsa_stream_t stream)
+{
+    if (rows < 0 || cols < 0 || k < 0) return LSA_ERR_INVALID_ARG;
+    if (rows == 0 || k == 0) return LSA_OK;
+    if (!idx || (cols > 0 && !scores)) return LSA_ERR_INVALID_ARG;
+    TopkArgs a;
+    memset(&a, 0, sizeof a);
+    a.scores = scores;
+    a.num_cols = num_cols;
+    a.rows = rows;
+    a.cols = cols;
+    a.k = k;
+    a.idx = idx;
+    a.status = status_word();
+    a.approx = 1;
+    a.seed = seed;
+    bool unsup = false;
+    cudaError_t e = launch_topk(a, reinterpret_cast<cudaStream_t>(stream), &unsup);
+    if (unsup) return LSA_ERR_UNSUPPORTED;
+    return from_cuda(e);
+}
+
 lsa_status lsa_fine_topk(const void *q, const lsa_cache *index_cache, const int32_t *page_table,
                          const int32_t *seq_lens, const int32_t *cand, const lsa_params *params, int32_t *tok_idx,
                          void *workspace, size_t workspace_bytes, lsa_stream_t stream)
@@ -727,7 +740,7 @@ lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *su
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     float *scores = reinterpret_cast<float *>(ws);
     int32_t *sel = idx_out ? idx_out : reinterpret_cast<int32_t *>(ws + L.scores);
-    uint8_t *ws_attn = ws + L.scores + L.sel + L.cand + L.fine + L.ctrl;
+    uint8_t *ws_attn = ws + L.scores + L.sel + L.cand + L.fine;
     uint32_t *status = status_word();
     const size_t rows = (size_t)params->batch * iv.hkv;
 
@@ -751,14 +764,9 @@ lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *su
     s.scores = scores;
     s.status = status;
     int32_t *cand = reinterpret_cast<int32_t *>(ws + L.scores + L.sel);
-    uint32_t *ctrl = reinterpret_cast<uint32_t *>(ws + L.scores + L.sel + L.cand + L.fine);
-    const bool fused = c2f && c2f_fused(iv, params);
-    if (fused) {
-        s.sel_k = params->c2f_candidates;
-        s.sel_idx = cand;
-        s.cnt = ctrl;
-        s.ready = ctrl + params->batch;
-    }
+    const bool fused = c2f && params->c2f_tokens > 0 &&
+                       c2f_fine_supported(iv, params->num_q_heads, params->max_blocks, params->c2f_candidates,
+                                          params->c2f_tokens, params->fine_head_weights != nullptr);
     bool unsup = false;
     cudaError_t e = launch_scores(s, params->summary_kind, st, &unsup);
     if (unsup) return LSA_ERR_UNSUPPORTED;
@@ -787,34 +795,28 @@ lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *su
                              out, lse, ws_attn, L.attn, st);
     }
     if (fused) {
-        // the fine kernel waits for each request's candidates and selects
-        // its tokens; then attention over them
+        // one cluster per request selects the candidates, rescores their
+        // tokens and selects the tokens; then attention over them
         FineArgs f;
         memset(&f, 0, sizeof f);
         f.q = static_cast<const uint16_t *>(q);
         f.ic = iv;
         f.pt = page_table;
         f.lens = seq_lens;
-        f.cand = cand;
         f.batch = params->batch;
         f.hq = params->num_q_heads;
         f.max_blocks = params->max_blocks;
         f.ncand = params->c2f_candidates;
-        f.fscores = reinterpret_cast<float *>(ws + L.scores + L.sel + L.cand);
         f.status = status;
+        f.weights = params->fine_head_weights;
+        f.coarse = scores;
+        f.cand_out = cand;
         f.tok_k = params->c2f_tokens;
         f.tok_idx = sel;
-        f.cnt = ctrl + 2 * params->batch;
-        f.ready = ctrl + params->batch;
-        f.spin_budget = spin_budget();
-        f.weights = params->fine_head_weights;
-        if (f.tok_k > 0) {
-            e = launch_fine_scores(f, st, &unsup);
-            if (unsup) return LSA_ERR_UNSUPPORTED;
-            if (e != cudaSuccess) return LSA_ERR_CUDA;
-        }
-        return run_attention(q, v, page_table, seq_lens, params->c2f_tokens > 0 ? sel : nullptr, params, true, out,
-                             lse, ws_attn, L.attn, st);
+        e = launch_c2f_fine(f, st, &unsup);
+        if (unsup) return LSA_ERR_UNSUPPORTED;
+        if (e != cudaSuccess) return LSA_ERR_CUDA;
+        return run_attention(q, v, page_table, seq_lens, sel, params, true, out, lse, ws_attn, L.attn, st);
     }
     // coarse-to-fine in separate stages: top-C candidate blocks, exact FP8
     // rescoring, token top-k

@@ -111,13 +111,6 @@ struct ScoreArgs {
     int32_t chunk;              // blocks per CTA (score_chunk)
     float *scores;              // [B, hkv, max_blocks]
     uint32_t *status;
-    // coarse-to-fine step (sel_k > 0): the last CTA of each request selects
-    // the top sel_k blocks of the request's rows into sel_idx [B*hkv, sel_k]
-    // (ascending, -1 padded), then adds 1 to ready[r]; cnt[r] counts the
-    // request's CTAs (zero between calls; the selecting CTA resets it)
-    int32_t sel_k;
-    int32_t *sel_idx;
-    uint32_t *cnt, *ready;
 };
 
 struct TopkArgs {
@@ -130,6 +123,10 @@ struct TopkArgs {
     const int32_t *cand;
     int32_t ncand, b;
     uint32_t *status;
+    // approx != 0: the stochastic early exit (the boundary bucket sampled
+    // with splitmix64(seed, row + 1) instead of ranked)
+    int32_t approx;
+    uint64_t seed;
 };
 
 struct FineArgs {
@@ -141,15 +138,15 @@ struct FineArgs {
     int32_t batch, hq, max_blocks, ncand;
     float *fscores;             // [B*hkv, ncand*b]
     uint32_t *status;
-    // coarse-to-fine step (tok_k > 0): every CTA first waits (bounded) for
-    // ready[r] == 1, set once the request's candidates are final; the last
-    // CTA of each request (cnt[r]) selects the top tok_k tokens of each of
-    // its rows into tok_idx [B*hkv, tok_k] (token positions, ascending, -1
-    // padded) and resets cnt[r] and ready[r]
+    // the coarse-to-fine step's cluster kernel (c2f_fine.cu): it selects
+    // the top ncand blocks of the coarse score rows coarse [B, max_blocks]
+    // itself (written to cand_out [B, ncand] if not NULL), rescores their
+    // tokens and writes the top tok_k into tok_idx [B, tok_k] (token
+    // positions, ascending, -1 padded)
+    const float *coarse;
+    int32_t *cand_out;
     int32_t tok_k;
     int32_t *tok_idx;
-    uint32_t *cnt, *ready;
-    long long spin_budget;
     // indexer head weights [B, Hq] (NULL: the head-sum score): the fine
     // score is then sum_g w[r,g] ReLU(q_g . k_t) (weighted-ReLU kernel)
     const float *weights;
@@ -235,6 +232,8 @@ cudaError_t launch_score_quest(const ScoreArgs &a, cudaStream_t s, bool *unsuppo
 bool score_quest_supported(int dk, int hkv, int group);
 cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s, bool *unsupported);
 cudaError_t launch_fine_scores(const FineArgs &a, cudaStream_t s, bool *unsupported);
+bool c2f_fine_supported(const CacheView &iv, int hq, int max_blocks, int ncand, int tok_k, bool weighted);
+cudaError_t launch_c2f_fine(const FineArgs &a, cudaStream_t s, bool *unsupported);
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s, bool *unsupported);
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);
 int attention_flat_ctas_per_sm();

@@ -12,10 +12,12 @@
 // and the output is ascending, so the result is bit-exact.
 #include <math.h>
 
+#include <mutex>
 #include <type_traits>
 
 #include "lsa_device.cuh"
 #include "topk_bucket.cuh"
+#include "topk_cluster.cuh"
 
 namespace lsa {
 namespace {
@@ -33,9 +35,7 @@ constexpr int kPtPerThread = kScoreMaxChunk / (kScoreWarps * 32);
 // memory once per CTA.  The main loop keeps U summary rows in flight per
 // warp at all times: each row's registers are refilled with the row U ahead
 // as soon as its dot products are done.
-constexpr int kSelMaxCols = kScoreWarps * 32 * 32;   // rows the select-at-end epilogue handles
-
-template <int DK, int HKV, bool SEL>
+template <int DK, int HKV>
 __global__ void __launch_bounds__(kScoreWarps * 32, 2) k_score(ScoreArgs a)
 {
     pdl_enter();
@@ -229,40 +229,6 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 2) k_score(ScoreArgs a)
             issue(i + UR * R, v[u]);
         }
     }
-
-    if constexpr (SEL) {
-        // coarse-to-fine step: the request's last CTA selects the top sel_k
-        // blocks of each of its rows (LeanSparse, Section 5: the coarse pass
-        // keeps the candidates the exact pass rescores)
-        __shared__ uint32_t s_last;
-        __shared__ BucketScratch<kScoreWarps * 32> bsm;
-        if (last_cta_arrival(a.cnt + r, gridDim.x, &s_last)) {
-            constexpr int KPT = kSelMaxCols / (kScoreWarps * 32);
-            for (int h = 0; h < HKV; ++h) {
-                const float *srow = a.scores + ((int64_t)r * HKV + h) * a.max_blocks;
-                uint32_t keys[KPT];
-                bool nan = false;
-#pragma unroll
-                for (int e = 0; e < KPT; ++e) {
-                    const int col = tid * KPT + e;
-                    const float x = col < a.max_blocks ? __ldcg(srow + col) : -INFINITY;
-                    nan |= isnan(x);
-                    keys[e] = (isnan(x) || x == -INFINITY) ? 0u : float_to_key(x);
-                }
-                if (nan) flag_error(a.status, LSA_ERR_NAN);
-                int32_t *orow = a.sel_idx + ((int64_t)r * HKV + h) * a.sel_k;
-                const int keff = block_bucket_topk<kScoreWarps * 32, KPT>(keys, a.sel_k, bsm,
-                                                                           [&](int pos, int col) { orow[pos] = col; });
-                for (int i = keff + tid; i < a.sel_k; i += kScoreWarps * 32) orow[i] = -1;
-            }
-            __threadfence();
-            __syncthreads();
-            if (tid == 0) {
-                a.cnt[r] = 0u;
-                red_release_add(a.ready + r, 1u);
-            }
-        }
-    }
 }
 
 // ============================================================ Quest scores
@@ -281,13 +247,15 @@ __device__ __forceinline__ void halve_sum(const float (&v)[N], float (&out)[N / 
     }
 }
 
-// The maximum over G heads of each head's sum over the warp's 32 lanes:
-// log2 G reduce-scatter steps leave each lane one head's partial, the
-// remaining lane bits finish the sums, and a max across the scatter bits
-// combines the heads.  Every lane gets the result.
-template <int G>
-__device__ __forceinline__ float warp_heads_sum_max(const float (&v)[G])
+// The maximum over G heads of each head's sum over an aligned group of T
+// lanes (T a power of two, G <= T): log2 G reduce-scatter steps on the
+// group's top lane bits leave each lane one head's partial, the remaining
+// bits finish the sums, and a max across the scatter bits combines the
+// heads.  Every lane of the group gets the result.
+template <int G, int T>
+__device__ __forceinline__ float group_heads_sum_max(const float (&v)[G])
 {
+    static_assert(G <= T && (T & (T - 1)) == 0 && T <= 32, "head groups");
     float s;
     int sbits;   // lane bits used by the scatter
     if constexpr (G == 1) {
@@ -295,29 +263,29 @@ __device__ __forceinline__ float warp_heads_sum_max(const float (&v)[G])
         sbits = 0;
     } else if constexpr (G == 2) {
         float a1[1];
-        halve_sum<2>(v, a1, 16);
+        halve_sum<2>(v, a1, T / 2);
         s = a1[0];
-        sbits = 16;
+        sbits = T / 2;
     } else if constexpr (G == 4) {
         float a2[2], a1[1];
-        halve_sum<4>(v, a2, 16);
-        halve_sum<2>(a2, a1, 8);
+        halve_sum<4>(v, a2, T / 2);
+        halve_sum<2>(a2, a1, T / 4);
         s = a1[0];
-        sbits = 16 | 8;
+        sbits = T / 2 | T / 4;
     } else {
         static_assert(G == 8, "groups of 1, 2, 4 or 8 query heads");
         float a4[4], a2[2], a1[1];
-        halve_sum<8>(v, a4, 16);
-        halve_sum<4>(a4, a2, 8);
-        halve_sum<2>(a2, a1, 4);
+        halve_sum<8>(v, a4, T / 2);
+        halve_sum<4>(a4, a2, T / 4);
+        halve_sum<2>(a2, a1, T / 8);
         s = a1[0];
-        sbits = 16 | 8 | 4;
+        sbits = T / 2 | T / 4 | T / 8;
     }
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1)
+    for (int off = 1; off < T; off <<= 1)
         if (!(sbits & off)) s += __shfl_xor_sync(0xffffffffu, s, off);
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1)
+    for (int off = 1; off < T; off <<= 1)
         if (sbits & off) s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, off));
     return s;
 }
@@ -327,55 +295,75 @@ __device__ __forceinline__ float warp_heads_sum_max(const float (&v)[G])
 // over the block's tokens t (Vortex blog post, end of "Why Long
 // Generations Are Expensive"; the Quest listing in "Writing an algorithm:
 // vFlow" takes Max over heads of Sum over dims of Maximum(q * max, q * min)).
-// It is not linear in q, so every head's query is kept: a warp owns one KV
-// head of a share of the chunk's blocks, each lane DK / 32 dims, with the G
-// query heads' slices in registers; per block it reads the head's maximum
-// and minimum keys (DK / 16 bytes per lane each) and keeps U blocks in
-// flight.  Summaries: [num_pages, HKV, 2, DK] bf16, maximum then minimum.
-template <int DK, int HKV, int G>
-__global__ void __launch_bounds__(kScoreWarps * 32, 2) k_score_quest(ScoreArgs a)
-{
-    pdl_enter();
-    constexpr int DPL = DK / 32;                 // dims per lane
-    constexpr int PARTS = kScoreWarps / HKV;     // warps per KV head
-    constexpr int U = 8;                         // blocks in flight per warp
-    static_assert(DPL == 2 || DPL == 4, "64- or 128-dim heads");
-    static_assert(kScoreWarps % HKV == 0, "KV heads divide the warps");
-    using VT = typename std::conditional<DPL == 4, uint2, uint32_t>::type;
-    __shared__ int s_page[kScoreMaxChunk];
+// Since max_ji >= min_ji, max(q * max, q * min) is q * max where q >= 0 and
+// q * min where q < 0, so the head's bound is the exact identity
+//   sum_i max(q_gi max_ji, q_gi min_ji) = q+_g . max_j + q-_g . min_j,
+// q+ = max(q, 0), q- = min(q, 0): two multiply-adds per dim and head, with
+// q+ and q- (fixed over the blocks) in registers.
+//
+// A CTA scores a contiguous chunk of one request's blocks.  The blocks'
+// summary rows ([num_pages, HKV, 2, DK] bf16, maximum then minimum; ROW
+// bytes a page) are staged in shared memory by 16-byte cp.async, NB pages a
+// tile, kQsStages tiles in flight.  A thread owns DPT dims of one KV head's
+// rows (TPB threads a row) and scores BPP blocks per pass.
+constexpr int kQsThreads = 256;
+constexpr int kQsStages = 3;
+constexpr int kQsTileBytes = 32 * 1024;
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+template <int DK, int HKV, int G>
+struct QsCfg {
+    static constexpr int DPT = G <= 4 ? 8 : 4;              // dims per thread
+    static constexpr int TPB = DK / DPT;                     // threads per (block, KV head)
+    static constexpr int BPP = kQsThreads / (TPB * HKV);     // blocks per pass
+    static constexpr int ROW = HKV * 2 * DK * 2;             // summary bytes of one page
+    static constexpr int NB = kQsTileBytes / ROW;            // pages per tile
+    static constexpr int PASSES = NB / BPP;
+    static constexpr int SMEM = kQsStages * kQsTileBytes;
+    static_assert(BPP >= 1 && PASSES >= 1 && NB % BPP == 0, "tile layout");
+};
+
+template <int DK, int HKV, int G>
+__global__ void __launch_bounds__(kQsThreads, 2) k_score_quest(ScoreArgs a)
+{
+    using C = QsCfg<DK, HKV, G>;
+    constexpr int DPT = C::DPT, TPB = C::TPB, BPP = C::BPP, ROW = C::ROW, NB = C::NB;
+    extern __shared__ __align__(128) uint8_t qsm[];
+    __shared__ int s_page[kScoreMaxChunk];
+    pdl_enter();
+    const int tid = threadIdx.x;
     const int r = blockIdx.y;
-    const int h = warp % HKV, part = warp / HKV;
+    const int sl = tid % TPB, h = (tid / TPB) % HKV, bp = tid / (TPB * HKV);
     const int j0 = blockIdx.x * a.chunk;
     const int j1 = min(j0 + a.chunk, a.max_blocks);
 
+    // ---- prologue: lengths, page ids and the query, all loaded first
     const int L = a.lens[r];
     int praw[kPtPerThread];
 #pragma unroll
     for (int i = 0; i < kPtPerThread; ++i) {
-        const int j = j0 + tid + i * kScoreWarps * 32;
+        const int j = j0 + tid + i * kQsThreads;
         praw[i] = j < j1 ? a.pt[(int64_t)r * a.max_blocks + j] : -1;
     }
-    // this lane's dims of the G query heads of KV head h
-    float qv[G][DPL];
+    float qp[G][DPT], qn[G][DPT];
     {
-        const uint16_t *qp = a.q + ((int64_t)r * a.hq + h * G) * DK + lane * DPL;
-        VT raw[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) raw[g] = *reinterpret_cast<const VT *>(qp + (int64_t)g * DK);
+        const uint16_t *q0 = a.q + ((int64_t)r * a.hq + h * G) * DK + sl * DPT;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            if constexpr (DPL == 4) {
-                const float2 lo = bf2_to_f2(raw[g].x), hi = bf2_to_f2(raw[g].y);
-                qv[g][0] = lo.x;
-                qv[g][1] = lo.y;
-                qv[g][2] = hi.x;
-                qv[g][3] = hi.y;
+            uint32_t w[DPT / 2];
+            if constexpr (DPT == 8) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(q0 + (int64_t)g * DK);
+                w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
             } else {
-                const float2 f = bf2_to_f2(raw[g]);
-                qv[g][0] = f.x;
-                qv[g][1] = f.y;
+                const uint2 v = *reinterpret_cast<const uint2 *>(q0 + (int64_t)g * DK);
+                w[0] = v.x; w[1] = v.y;
+            }
+#pragma unroll
+            for (int e = 0; e < DPT / 2; ++e) {
+                const float2 f = bf2_to_f2(w[e]);
+                qp[g][2 * e] = fmaxf(f.x, 0.f);
+                qn[g][2 * e] = fminf(f.x, 0.f);
+                qp[g][2 * e + 1] = fmaxf(f.y, 0.f);
+                qn[g][2 * e + 1] = fminf(f.y, 0.f);
             }
         }
     }
@@ -385,7 +373,7 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 2) k_score_quest(ScoreArgs a
     const int rs = len_ok ? max(L - a.recent, se) : 0;
 #pragma unroll
     for (int i = 0; i < kPtPerThread; ++i) {
-        const int j = j0 + tid + i * kScoreWarps * 32;
+        const int j = j0 + tid + i * kQsThreads;
         if (j >= j1) continue;
         const bool cand = len_ok && (int64_t)j * a.b >= se && (int64_t)(j + 1) * a.b <= rs;
         int p = cand ? praw[i] : -1;
@@ -401,72 +389,85 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 2) k_score_quest(ScoreArgs a
     }
     __syncthreads();
 
+    // ---- the chunk's tiles through a kQsStages-deep cp.async ring
     const int n = j1 - j0;
-    const int w0 = n * part / PARTS, w1 = n * (part + 1) / PARTS;
-    const uint8_t *summ = reinterpret_cast<const uint8_t *>(a.summ) + ((int64_t)h * 2 * DK + lane * DPL) * 2;
-    constexpr int64_t kPageBytes = (int64_t)HKV * 2 * DK * 2;
+    const int ntiles = (n + NB - 1) / NB;
+    const uint8_t *summ = reinterpret_cast<const uint8_t *>(a.summ);
     const uint64_t pol = l2_evict_first();
-    VT vmax[U], vmin[U];
-    auto issue = [&](int i, VT &mx, VT &mn) {
-        const int p = i < w1 ? s_page[i] : -1;
-        if (p >= 0) {
-            const uint8_t *src = summ + (int64_t)p * kPageBytes;
-            if constexpr (DPL == 4) {
-                uint4 both;   // two 8-byte loads (maximum, minimum)
-                asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;"
-                             : "=r"(both.x), "=r"(both.y) : "l"(src), "l"(pol));
-                asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;"
-                             : "=r"(both.z), "=r"(both.w) : "l"(src + DK * 2), "l"(pol));
-                mx = make_uint2(both.x, both.y);
-                mn = make_uint2(both.z, both.w);
-            } else {
-                asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;"
-                             : "=r"(mx) : "l"(src), "l"(pol));
-                asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;"
-                             : "=r"(mn) : "l"(src + DK * 2), "l"(pol));
+    const uint32_t sbase = smem_addr(qsm);
+    auto issue = [&](int t) {
+        if (t < ntiles) {
+            const uint32_t dst = sbase + (uint32_t)((t % kQsStages) * kQsTileBytes);
+            constexpr int CPR = ROW / 16;   // 16-byte chunks per page row
+            for (int c = tid; c < NB * CPR; c += kQsThreads) {
+                const int bi = c / CPR, off = c - bi * CPR;
+                const int i = t * NB + bi;
+                const int p = i < n ? s_page[i] : -1;
+                if (p >= 0) cp_async16_policy(dst + (uint32_t)(bi * ROW + off * 16), summ + (int64_t)p * ROW + off * 16, pol);
             }
         }
+        cp_async_commit();
     };
 #pragma unroll
-    for (int u = 0; u < U; ++u) issue(w0 + u, vmax[u], vmin[u]);
-    for (int base = w0; base < w1; base += U) {
+    for (int t = 0; t < kQsStages - 1; ++t) issue(t);
+    for (int t = 0; t < ntiles; ++t) {
+        cp_async_wait<kQsStages - 2>();
+        __syncthreads();                      // tile t is in; tile t - 1's stage is free
+        issue(t + kQsStages - 1);
+        const uint8_t *tile = qsm + (t % kQsStages) * kQsTileBytes;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = base + u;
-            const int p = i < w1 ? s_page[i] : -1;   // warp-uniform
-            if (p >= 0) {
-                float M[DPL], m[DPL];
-                if constexpr (DPL == 4) {
-                    const float2 a0 = bf2_to_f2(vmax[u].x), a1 = bf2_to_f2(vmax[u].y);
-                    const float2 b0 = bf2_to_f2(vmin[u].x), b1 = bf2_to_f2(vmin[u].y);
-                    M[0] = a0.x; M[1] = a0.y; M[2] = a1.x; M[3] = a1.y;
-                    m[0] = b0.x; m[1] = b0.y; m[2] = b1.x; m[3] = b1.y;
-                } else {
-                    const float2 a0 = bf2_to_f2(vmax[u]), b0 = bf2_to_f2(vmin[u]);
-                    M[0] = a0.x; M[1] = a0.y;
-                    m[0] = b0.x; m[1] = b0.y;
-                }
-                float part_g[G];
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int d = 0; d < DPL; ++d) acc += fmaxf(qv[g][d] * M[d], qv[g][d] * m[d]);
-                    part_g[g] = acc;
-                }
-                const float sc = warp_heads_sum_max<G>(part_g);
-                if (lane == 0) a.scores[((int64_t)r * HKV + h) * a.max_blocks + j0 + i] = sc;
+        for (int ps = 0; ps < C::PASSES; ++ps) {
+            const int bi = ps * BPP + bp;
+            const int i = t * NB + bi;
+            const bool have = i < n && s_page[i] >= 0;
+            const uint8_t *row = tile + bi * ROW + h * (2 * DK * 2) + sl * DPT * 2;
+            uint32_t wM[DPT / 2], wm[DPT / 2];
+            if constexpr (DPT == 8) {
+                const uint4 x = *reinterpret_cast<const uint4 *>(row);
+                const uint4 y = *reinterpret_cast<const uint4 *>(row + DK * 2);
+                wM[0] = x.x; wM[1] = x.y; wM[2] = x.z; wM[3] = x.w;
+                wm[0] = y.x; wm[1] = y.y; wm[2] = y.z; wm[3] = y.w;
+            } else {
+                const uint2 x = *reinterpret_cast<const uint2 *>(row);
+                const uint2 y = *reinterpret_cast<const uint2 *>(row + DK * 2);
+                wM[0] = x.x; wM[1] = x.y;
+                wm[0] = y.x; wm[1] = y.y;
             }
-            issue(i + U, vmax[u], vmin[u]);
+            float M[DPT], m[DPT];
+#pragma unroll
+            for (int e = 0; e < DPT / 2; ++e) {
+                const float2 fM = bf2_to_f2(wM[e]), fm = bf2_to_f2(wm[e]);
+                M[2 * e] = fM.x;
+                M[2 * e + 1] = fM.y;
+                m[2 * e] = fm.x;
+                m[2 * e + 1] = fm.y;
+            }
+            float part[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float acc = 0.f;
+#pragma unroll
+                for (int d = 0; d < DPT; ++d) {
+                    acc = fmaf(qp[g][d], M[d], acc);
+                    acc = fmaf(qn[g][d], m[d], acc);
+                }
+                part[g] = acc;
+            }
+            const float sc = group_heads_sum_max<G, TPB>(part);
+            if (have && sl == 0) a.scores[((int64_t)r * HKV + h) * a.max_blocks + j0 + i] = sc;
         }
     }
+    cp_async_wait<0>();
 }
 
 template <int DK, int HKV, int G>
 cudaError_t launch_score_quest_t(const ScoreArgs &a, cudaStream_t s)
 {
+    auto kern = k_score_quest<DK, HKV, G>;
+    cudaError_t le = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, QsCfg<DK, HKV, G>::SMEM);
+    if (le != cudaSuccess) return le;
     dim3 grid((a.max_blocks + a.chunk - 1) / a.chunk, a.batch);
-    cudaError_t le = launch_step_kernel(k_score_quest<DK, HKV, G>, grid, dim3(kScoreWarps * 32), 0, s, a);
+    le = launch_step_kernel(kern, grid, dim3(kQsThreads), QsCfg<DK, HKV, G>::SMEM, s, a);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
@@ -487,7 +488,7 @@ __device__ __forceinline__ int32_t topk_out(const TopkArgs &a, int row, int col)
 
 // One block of 1024 threads per row, KPT columns per thread: the exact
 // bucketed top-k of topk_bucket.cuh.
-template <int KPT>
+template <int KPT, bool APPROX = false>
 __global__ void __launch_bounds__(kTopkThreads) k_topk_rows(TopkArgs a)
 {
     pdl_enter();
@@ -521,76 +522,149 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_rows(TopkArgs a)
     }
     if (nan) flag_error(a.status, LSA_ERR_NAN);
     int32_t *orow = a.idx + (int64_t)row * a.k;
-    const int keff = block_bucket_topk<kTopkThreads, KPT>(keys, a.k, sm,
-                                                          [&](int pos, int col) { orow[pos] = topk_out(a, row, col); });
+    const int keff = block_bucket_topk<kTopkThreads, KPT, APPROX>(
+        keys, a.k, sm, [&](int pos, int col) { orow[pos] = topk_out(a, row, col); },
+        APPROX ? splitmix64(a.seed, (uint64_t)row + 1) : 0ull);
     for (int i = keff + tid; i < a.k; i += kTopkThreads) orow[i] = -1;
+}
+
+// Few long rows: a cluster of CS CTAs of kClThreads threads per row, KPT
+// columns per thread (topk_cluster.cuh), so that a handful of rows still
+// spread over many SMs.  CTA c of the row's cluster holds columns
+// [c * kClThreads * KPT, (c + 1) * kClThreads * KPT).
+constexpr int kClThreads = 512;
+
+template <int CS, int KPT, bool APPROX = false>
+__global__ void __launch_bounds__(kClThreads, 1) k_topk_cluster(TopkArgs a)
+{
+    pdl_enter();
+    __shared__ ClusterTopkScratch<kClThreads, CS> sm;
+    const int rank = (int)cluster_rank();
+    const int row = blockIdx.y, tid = threadIdx.x;
+    int n = a.num_cols ? a.num_cols[row] : a.cols;
+    n = max(0, min(n, a.cols));
+    const float *srow = a.scores + (int64_t)row * a.cols;
+    const int c0 = (rank * kClThreads + tid) * KPT;
+    float v[KPT];
+    const bool vec = KPT >= 2 && (a.cols % KPT) == 0 && (reinterpret_cast<uintptr_t>(a.scores) % (4 * KPT)) == 0 &&
+                     c0 + KPT <= n;
+    if constexpr (KPT == 2) {
+        if (vec) {
+            const float2 f = *reinterpret_cast<const float2 *>(srow + c0);
+            v[0] = f.x;
+            v[1] = f.y;
+        }
+    } else if constexpr (KPT >= 4) {
+        if (vec) {
+#pragma unroll
+            for (int e = 0; e < KPT; e += 4) {
+                const float4 f = *reinterpret_cast<const float4 *>(srow + c0 + e);
+                v[e] = f.x;
+                v[e + 1] = f.y;
+                v[e + 2] = f.z;
+                v[e + 3] = f.w;
+            }
+        }
+    }
+    if (!vec) {
+#pragma unroll
+        for (int e = 0; e < KPT; ++e) v[e] = c0 + e < n ? srow[c0 + e] : -INFINITY;
+    }
+    uint32_t keys[KPT];
+    bool nan = false;
+#pragma unroll
+    for (int e = 0; e < KPT; ++e) {
+        nan |= isnan(v[e]);
+        keys[e] = (isnan(v[e]) || v[e] == -INFINITY) ? 0u : float_to_key(v[e]);
+    }
+    if (nan) flag_error(a.status, LSA_ERR_NAN);
+    int32_t *orow = a.idx + (int64_t)row * a.k;
+    const int keff = cluster_bucket_topk<kClThreads, KPT, CS, APPROX>(
+        keys, a.k, c0, sm, [&](int pos, int col) { orow[pos] = topk_out(a, row, col); },
+        APPROX ? splitmix64(a.seed, (uint64_t)row + 1) : 0ull);
+    if (rank == 0)
+        for (int i = keff + tid; i < a.k; i += kClThreads) orow[i] = -1;
+}
+
+// Cluster size the cluster top-k runs with on this device: 16 CTAs where a
+// cluster of 16 can be resident, else 8 (0: neither).
+int topk_cluster_size()
+{
+    static std::mutex mu;
+    static int cs[64] = {};
+    static bool done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!done[dev]) {
+        int c = 0;
+        if (max_active_clusters(k_topk_cluster<16, 1>, 16, dim3(kClThreads), 0) > 0 &&
+            max_active_clusters(k_topk_cluster<16, 2>, 16, dim3(kClThreads), 0) > 0 &&
+            max_active_clusters(k_topk_cluster<16, 4>, 16, dim3(kClThreads), 0) > 0)
+            c = 16;
+        else if (max_active_clusters(k_topk_cluster<8, 8>, 8, dim3(kClThreads), 0) > 0)
+            c = 8;
+        cs[dev] = c;
+        done[dev] = true;
+    }
+    return cs[dev];
+}
+
+template <int CS, int KPT>
+cudaError_t launch_topk_cluster_t(const TopkArgs &a, cudaStream_t s)
+{
+    if (a.approx && CS > 8) {
+        cudaError_t e = cudaFuncSetAttribute(k_topk_cluster<CS, KPT, true>,
+                                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    return a.approx ? launch_cluster_kernel(pdl_enabled(), CS, k_topk_cluster<CS, KPT, true>, dim3(CS, a.rows),
+                                            dim3(kClThreads), 0, s, a)
+                    : launch_cluster_kernel(pdl_enabled(), CS, k_topk_cluster<CS, KPT>, dim3(CS, a.rows),
+                                            dim3(kClThreads), 0, s, a);
+}
+
+// The cluster top-k when the rows are few and long enough for it to pay
+// (LSA_TOPK_PATH=rows / cluster forces one or the other); false: not taken.
+bool launch_topk_cluster(const TopkArgs &a, cudaStream_t s, cudaError_t *err)
+{
+    const char *env = getenv("LSA_TOPK_PATH");
+    const int mode = !env ? 0 : strcmp(env, "rows") == 0 ? 1 : strcmp(env, "cluster") == 0 ? 2 : 0;
+    if (mode == 1) return false;
+    const int cs = topk_cluster_size();
+    if (cs == 0) return false;
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (mode == 0 && !(a.cols > 4096 && (int64_t)a.rows * cs <= sms)) return false;
+    const int per = cs * kClThreads;
+    const int kpt = a.cols <= per ? 1 : a.cols <= 2 * per ? 2 : a.cols <= 4 * per ? 4 : 8;
+    cudaError_t e;
+    if (cs == 16) {
+        if (kpt > 4) return false;
+        e = kpt == 1 ? launch_topk_cluster_t<16, 1>(a, s)
+          : kpt == 2 ? launch_topk_cluster_t<16, 2>(a, s)
+                     : launch_topk_cluster_t<16, 4>(a, s);
+    } else {
+        e = kpt == 1 ? launch_topk_cluster_t<8, 1>(a, s)
+          : kpt == 2 ? launch_topk_cluster_t<8, 2>(a, s)
+          : kpt == 4 ? launch_topk_cluster_t<8, 4>(a, s)
+                     : launch_topk_cluster_t<8, 8>(a, s);
+    }
+    *err = e != cudaSuccess ? e : cudaGetLastError();
+    return true;
 }
 
 // ============================================================ fine pass
 
 constexpr int kFineWarps = 8;
 constexpr int kFineBlocksPerCta = 4;
-constexpr int kFineMaxCols = 16384;   // fine-score columns the selecting CTA handles (64 per thread)
 
 // f_t = scale_t * q_sum . e4m3(k8_t) for every token of the candidate
 // blocks (LeanSparse, Section 5: exact rescoring of the retained candidates
 // with their original FP8 indexer keys).  8 lanes per token, 16 dims each.
-// The coarse-to-fine step's last fine CTA of request r: the exact top tok_k
-// of each of the request's rows of fine scores (LeanSparse, Section 5: the
-// exact pass keeps the final tokens), written as token positions; then the
-// request's counters are reset.  Every thread of the CTA calls it.
-__device__ void fine_select_tokens(const FineArgs &a, int r, int hkv, int64_t ntok_row, int b)
-{
-    __shared__ uint32_t s_last;
-    __shared__ BucketScratch<kFineWarps * 32> bsm;
-    if (!last_cta_arrival(a.cnt + r, gridDim.x * hkv, &s_last)) return;
-    constexpr int KPT = kFineMaxCols / (kFineWarps * 32);
-    const int cols = (int)ntok_row;
-    for (int hh = 0; hh < hkv; ++hh) {
-        const int rw = r * hkv + hh;
-        const float *srow = a.fscores + (int64_t)rw * ntok_row;
-        uint32_t keys[KPT];
-        bool nan = false;
-#pragma unroll
-        for (int e = 0; e < KPT; e += 4) {
-            const int col = threadIdx.x * KPT + e;
-            float4 x4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            if (col + 3 < cols) x4 = __ldcg(reinterpret_cast<const float4 *>(srow + col));
-            else {
-                if (col < cols) x4.x = __ldcg(srow + col);
-                if (col + 1 < cols) x4.y = __ldcg(srow + col + 1);
-                if (col + 2 < cols) x4.z = __ldcg(srow + col + 2);
-            }
-            const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                nan |= isnan(xs[u]);
-                keys[e + u] = (isnan(xs[u]) || xs[u] == -INFINITY) ? 0u : float_to_key(xs[u]);
-            }
-        }
-        if (nan) flag_error(a.status, LSA_ERR_NAN);
-        const int32_t *crow = a.cand + (int64_t)rw * a.ncand;
-        int32_t *orow = a.tok_idx + (int64_t)rw * a.tok_k;
-        const int keff = block_bucket_topk<kFineWarps * 32, KPT>(
-            keys, a.tok_k, bsm, [&](int pos, int col) { orow[pos] = __ldcg(crow + col / b) * b + col % b; });
-        for (int i = keff + (int)threadIdx.x; i < a.tok_k; i += kFineWarps * 32) orow[i] = -1;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {   // every CTA of the request has passed its wait
-        a.cnt[r] = 0u;
-        a.ready[r] = 0u;
-    }
-}
-
-// SEL: the fine pass of the coarse-to-fine step, launched as a programmatic
-// dependent of the coarse kernel: it does not wait for that kernel to
-// complete, but for each request's candidates (ready[r]), and its last CTA
-// per request selects the request's tokens.
-template <bool SEL>
 __global__ void __launch_bounds__(kFineWarps * 32) k_fine_scores(FineArgs a)
 {
-    if constexpr (SEL) pdl_launch_dependents();
-    else pdl_enter();
+    pdl_enter();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int row = blockIdx.y;                 // r * hkv + h
     const int hkv = a.ic.hkv;
@@ -646,20 +720,11 @@ __global__ void __launch_bounds__(kFineWarps * 32) k_fine_scores(FineArgs a)
     float *frow = a.fscores + (int64_t)row * ntok_row;
     const int c0 = blockIdx.x * kFineBlocksPerCta;
     const int nb = min(kFineBlocksPerCta, a.ncand - c0);
-    bool cand_ok = true;
-    if constexpr (SEL) {
-        // the request's candidates are final once ready[r] == 1 (a wait
-        // that gives up records LSA_ERR_TIMEOUT; the CTA then scores nothing)
-        __shared__ uint32_t s_ok;
-        if (threadIdx.x == 0) s_ok = wait_counter_eq(a.ready + r, 1u, a.status, a.spin_budget) ? 1u : 0u;
-        __syncthreads();
-        cand_ok = s_ok != 0u;
-    }
     // the CTA's candidate blocks -> page ids (two dependent round trips,
     // once for all of them); -1 for padding and invalid entries
     __shared__ int s_pg[kFineBlocksPerCta];
     if (threadIdx.x < nb) {
-        const int j = cand_ok ? __ldcg(a.cand + (int64_t)row * a.ncand + c0 + threadIdx.x) : -1;
+        const int j = a.cand[(int64_t)row * a.ncand + c0 + threadIdx.x];
         int p = -1;
         if (j >= 0 && j < nfull) p = a.pt[(int64_t)r * a.max_blocks + j];
         const bool ok = p >= 0 && p < a.ic.num_pages;
@@ -708,7 +773,6 @@ __global__ void __launch_bounds__(kFineWarps * 32) k_fine_scores(FineArgs a)
         if (t < ntok && sub == 0) frow[(int64_t)c0 * b + t] = have ? sc[it] * acc : -INFINITY;
     }
 
-    if constexpr (SEL) fine_select_tokens(a, r, hkv, ntok_row, b);
 }
 
 // The weighted-ReLU indexer score of the fine pass: f_t = sum_g w[r, g] *
@@ -724,11 +788,9 @@ __global__ void __launch_bounds__(kFineWarps * 32) k_fine_scores(FineArgs a)
 constexpr int kWrTok = kFineBlocksPerCta * 64;        // tokens per CTA at most
 constexpr int kWrSmem = kWrTok * 128 * 2;              // the widened key tile
 
-template <bool SEL>
 __global__ void __launch_bounds__(kFineWarps * 32) k_fine_scores_wrelu(FineArgs a)
 {
-    if constexpr (SEL) pdl_launch_dependents();
-    else pdl_enter();
+    pdl_enter();
     extern __shared__ __align__(1024) uint8_t wsm[];   // [kWrTok / 16] tiles of 16 tokens x 128 dims, swizzled
     __shared__ float s_part[4][kWrTok];
     __shared__ int s_pg[kFineBlocksPerCta];
@@ -763,15 +825,8 @@ __global__ void __launch_bounds__(kFineWarps * 32) k_fine_scores_wrelu(FineArgs 
     float *frow = a.fscores + (int64_t)row * ntok_row;
     const int c0 = blockIdx.x * kFineBlocksPerCta;
     const int nb = min(kFineBlocksPerCta, a.ncand - c0);
-    bool cand_ok = true;
-    if constexpr (SEL) {
-        __shared__ uint32_t s_ok;
-        if (threadIdx.x == 0) s_ok = wait_counter_eq(a.ready + r, 1u, a.status, a.spin_budget) ? 1u : 0u;
-        __syncthreads();
-        cand_ok = s_ok != 0u;
-    }
     if (threadIdx.x < nb) {
-        const int j = cand_ok ? __ldcg(a.cand + (int64_t)row * a.ncand + c0 + threadIdx.x) : -1;
+        const int j = a.cand[(int64_t)row * a.ncand + c0 + threadIdx.x];
         int p = -1;
         if (j >= 0 && j < nfull) p = a.pt[(int64_t)r * a.max_blocks + j];
         const bool ok = p >= 0 && p < a.ic.num_pages;
@@ -866,14 +921,13 @@ __global__ void __launch_bounds__(kFineWarps * 32) k_fine_scores_wrelu(FineArgs 
         }
         frow[(int64_t)c0 * b + t] = f;
     }
-    if constexpr (SEL) fine_select_tokens(a, r, hkv, ntok_row, b);
 }
 
-template <int DK, int HKV, bool SEL = false>
+template <int DK, int HKV>
 cudaError_t launch_score_t(const ScoreArgs &a, cudaStream_t s)
 {
     dim3 grid((a.max_blocks + a.chunk - 1) / a.chunk, a.batch);
-    cudaError_t le = launch_step_kernel(k_score<DK, HKV, SEL>, grid, dim3(kScoreWarps * 32), 0, s, a);
+    cudaError_t le = launch_step_kernel(k_score<DK, HKV>, grid, dim3(kScoreWarps * 32), 0, s, a);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
@@ -893,12 +947,6 @@ cudaError_t launch_score(const ScoreArgs &a, cudaStream_t s, bool *unsupported)
 {
     *unsupported = false;
     if (a.batch == 0 || a.max_blocks == 0) return cudaSuccess;
-    if (a.sel_k > 0) {
-        // the coarse pass of the coarse-to-fine step (FP8 index summaries,
-        // one 128-dim index head)
-        *unsupported = !(a.dk == 128 && a.hkv == 1 && a.max_blocks <= kSelMaxCols);
-        return *unsupported ? cudaSuccess : launch_score_t<128, 1, true>(a, s);
-    }
 #define LSA_SCORE_CASE(D, H) \
     if (a.dk == D && a.hkv == H) return launch_score_t<D, H>(a, s);
     LSA_SCORE_CASE(64, 1) LSA_SCORE_CASE(64, 2) LSA_SCORE_CASE(64, 4) LSA_SCORE_CASE(64, 8)
@@ -956,11 +1004,19 @@ cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s, bool *unsupported)
     // rows of up to 8192 columns with k <= 64: the block top-k (a bound from
     // the threads' maxima, then an exact rank of the few keys above it);
     // wider rows and larger k: the radix select
-    if (a.k <= 64 && launch_topk_fast(a, s, &fe)) return fe;
+    if (!a.approx && a.k <= 64 && launch_topk_fast(a, s, &fe)) return fe;
+    if (launch_topk_cluster(a, s, &fe)) return fe;
     cudaError_t e;
-    if (a.cols <= kTopkThreads * 8) e = launch_step_kernel(k_topk_rows<8>, dim3(a.rows), dim3(kTopkThreads), 0, s, a);
-    else if (a.cols <= kTopkThreads * 16) e = launch_step_kernel(k_topk_rows<16>, dim3(a.rows), dim3(kTopkThreads), 0, s, a);
-    else e = launch_step_kernel(k_topk_rows<32>, dim3(a.rows), dim3(kTopkThreads), 0, s, a);
+    const dim3 g(a.rows), blk(kTopkThreads);
+    if (a.approx) {
+        if (a.cols <= kTopkThreads * 8) e = launch_step_kernel(k_topk_rows<8, true>, g, blk, 0, s, a);
+        else if (a.cols <= kTopkThreads * 16) e = launch_step_kernel(k_topk_rows<16, true>, g, blk, 0, s, a);
+        else e = launch_step_kernel(k_topk_rows<32, true>, g, blk, 0, s, a);
+    } else {
+        if (a.cols <= kTopkThreads * 8) e = launch_step_kernel(k_topk_rows<8>, g, blk, 0, s, a);
+        else if (a.cols <= kTopkThreads * 16) e = launch_step_kernel(k_topk_rows<16>, g, blk, 0, s, a);
+        else e = launch_step_kernel(k_topk_rows<32>, g, blk, 0, s, a);
+    }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -969,21 +1025,16 @@ cudaError_t launch_fine_scores(const FineArgs &a, cudaStream_t s, bool *unsuppor
 {
     // a CTA scores kFineBlocksPerCta blocks of at most 64 tokens each
     *unsupported = a.ic.dk != 128 || !a.ic.e4m3 || a.ic.b > 64 || a.ic.b % 16 != 0 ||
-                   (a.tok_k > 0 && (int64_t)a.ncand * a.ic.b > kFineMaxCols) ||
                    (a.weights && a.hq / a.ic.hkv != 64);
     if (*unsupported || a.batch == 0 || a.ncand == 0) return cudaSuccess;
     dim3 grid((a.ncand + kFineBlocksPerCta - 1) / kFineBlocksPerCta, a.batch * a.ic.hkv);
     cudaError_t le;
     if (a.weights) {
-        auto kern = a.tok_k > 0 ? k_fine_scores_wrelu<true> : k_fine_scores_wrelu<false>;
-        le = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kWrSmem);
+        le = cudaFuncSetAttribute(k_fine_scores_wrelu, cudaFuncAttributeMaxDynamicSharedMemorySize, kWrSmem);
         if (le != cudaSuccess) return le;
-        le = a.tok_k > 0 ? launch_kernel_ex(pdl_step_dependent(), kern, grid, dim3(kFineWarps * 32), kWrSmem, s, a)
-                         : launch_step_kernel(kern, grid, dim3(kFineWarps * 32), kWrSmem, s, a);
-    } else if (a.tok_k > 0) {
-        le = launch_kernel_ex(pdl_step_dependent(), k_fine_scores<true>, grid, dim3(kFineWarps * 32), 0, s, a);
+        le = launch_step_kernel(k_fine_scores_wrelu, grid, dim3(kFineWarps * 32), kWrSmem, s, a);
     } else {
-        le = launch_step_kernel(k_fine_scores<false>, grid, dim3(kFineWarps * 32), 0, s, a);
+        le = launch_step_kernel(k_fine_scores, grid, dim3(kFineWarps * 32), 0, s, a);
     }
     if (le != cudaSuccess) return le;
     return cudaGetLastError();

@@ -11,10 +11,10 @@
 // bucket that holds the k-th largest score is then resolved exactly: its
 // few keys are ranked by (larger key, lower column).  Because the remap is
 // monotone, every key in a higher bucket is at least every key in a lower
-// one, so the selection is the exact top-k (there is no stochastic early
-// exit: that approximate mode is a separate, opt-in kernel).  When the
-// boundary bucket holds more than kBkCap keys (heavy ties or extreme skew)
-// a bisection over the keys finds the threshold instead.
+// one, so the selection is the exact top-k.  When the boundary bucket holds
+// more than kBkCap keys (heavy ties or extreme skew) a bisection over the
+// keys finds the threshold instead.  The stochastic early exit (approximate,
+// opt-in) is the APPROX variant below.
 #pragma once
 
 #include "lsa_device.cuh"
@@ -99,13 +99,31 @@ __device__ __forceinline__ uint32_t bk_sum(uint32_t v, uint32_t (*red)[3])
     return bk_sum_min_max<NT>(v, 0u, 0u, red).x;
 }
 
+// SplitMix64 (Steele, Lea and Flood, OOPSLA 2014), counter style: output n
+// (n >= 1) of the generator seeded with `seed` is the variant-13 finaliser
+// of seed + n * 0x9e3779b97f4a7c15.
+__host__ __device__ __forceinline__ uint64_t splitmix64(uint64_t seed, uint64_t n)
+{
+    uint64_t z = seed + n * 0x9e3779b97f4a7c15ULL;
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ULL;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebULL;
+    return z ^ (z >> 31);
+}
+
 // Selects the top min(k, candidates) of the keys (order-preserving, 0 = not a
 // candidate) held KPT per thread, thread t holding columns [t*KPT, (t+1)*KPT),
 // and calls out(position, column) for each selected column, positions in
 // ascending column order; returns how many.  Every thread of the block must
 // call it.
-template <int NT, int KPT, class Out>
-__device__ int block_bucket_topk(const uint32_t (&keys)[KPT], int k, BucketScratch<NT> &sm, Out out)
+//
+// APPROX: the stochastic early exit (Vortex, "Making it fast"): the keys in
+// buckets above the boundary bucket are the confident winners, and the rest
+// are sampled from the boundary bucket instead of ranked: numbered in column
+// order 0 .. cnt-1, those within (k - winners) steps after sample mod cnt,
+// circularly, are taken (sample: a SplitMix64 output drawn by the caller).
+template <int NT, int KPT, bool APPROX = false, class Out>
+__device__ int block_bucket_topk(const uint32_t (&keys)[KPT], int k, BucketScratch<NT> &sm, Out out,
+                                 uint64_t sample = 0)
 {
     static_assert(KPT <= 64, "selection mask of 64 bits");
     const int tid = threadIdx.x;
@@ -184,7 +202,19 @@ __device__ int block_bucket_topk(const uint32_t (&keys)[KPT], int k, BucketScrat
             inb |= (uint64_t)(bk[e] == B) << e;
             nb += bk[e] == B;
         }
-        if (cnt <= kBkCap) {
+        if (APPROX) {
+            uint32_t dummy = 0;
+            const uint32_t base = bk_scan<NT>(nb, sm.red, &dummy);
+            const uint32_t off = (uint32_t)(sample % (uint64_t)cnt);
+            uint32_t pos = base;
+#pragma unroll
+            for (int e = 0; e < KPT; ++e) {
+                if ((inb >> e) & 1ull) {
+                    if ((pos + (uint32_t)cnt - off) % (uint32_t)cnt < (uint32_t)take) sel |= (uint64_t)1 << e;
+                    ++pos;
+                }
+            }
+        } else if (cnt <= kBkCap) {
             // the boundary bucket's keys, in column order, then each ranked
             // against all of them (larger key first, then lower column)
             uint32_t dummy = 0;

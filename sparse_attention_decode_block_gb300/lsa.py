@@ -34,7 +34,7 @@ LSA_SUMMARY_MINMAX = 1
 
 EXPORTED = ["lsa_status_string", "lsa_get_device_status", "lsa_build_summaries", "lsa_append_block",
             "lsa_build_minmax_summaries", "lsa_append_block_minmax",
-            "lsa_score", "lsa_topk", "lsa_fine_topk", "lsa_sparse_decode_workspace_size",
+            "lsa_score", "lsa_topk", "lsa_topk_approx", "lsa_fine_topk", "lsa_sparse_decode_workspace_size",
             "lsa_sparse_decode", "lsa_decode_step_workspace_size", "lsa_decode_step",
             "lsa_sparse_decode_static_scratch"]
 
@@ -88,6 +88,7 @@ def load_library(path: Optional[str] = None):
             "lsa_append_block_minmax": ([cache_p, V, V, V, V, I, I, V, V], C.c_int),
             "lsa_score": ([V, cache_p, V, V, V, params_p, V, V], C.c_int),
             "lsa_topk": ([V, V, I, I, I, V, V], C.c_int),
+            "lsa_topk_approx": ([V, V, I, I, I, C.c_uint64, V, V], C.c_int),
             "lsa_fine_topk": ([V, cache_p, V, V, V, params_p, V, V, S, V], C.c_int),
             "lsa_sparse_decode_workspace_size": ([cache_p, params_p], S),
             "lsa_sparse_decode": ([V, cache_p, V, V, V, params_p, V, V, V, S, V], C.c_int),
@@ -204,6 +205,13 @@ def lsa_topk(scores, num_cols, k: int, idx, stream=None):
     rows, cols = scores.shape
     _check(load_library().lsa_topk(_ptr(scores), _ptr(num_cols), rows, cols, int(k), _ptr(idx), _stream(stream)),
            "lsa_topk")
+
+
+def lsa_topk_approx(scores, num_cols, k: int, seed: int, idx, stream=None):
+    rows, cols = scores.shape
+    _check(load_library().lsa_topk_approx(_ptr(scores), _ptr(num_cols), rows, cols, int(k),
+                                          int(seed) & (2**64 - 1), _ptr(idx), _stream(stream)),
+           "lsa_topk_approx")
 
 
 def lsa_fine_topk(q, index_cache: lsa_cache, page_table, seq_lens, cand, params: lsa_params, tok_idx,

@@ -88,6 +88,8 @@ def test_host_validation_rejects_bad_arguments(lib):
                                  s) == L.LSA_ERR_INVALID_ARG
     assert lib.lsa_topk(fake, None, -1, 4, 2, fake, s) == L.LSA_ERR_INVALID_ARG
     assert lib.lsa_topk(fake, None, 3, 4, 2, None, s) == L.LSA_ERR_INVALID_ARG
+    assert lib.lsa_topk_approx(fake, None, 3, 4, -2, 1, fake, s) == L.LSA_ERR_INVALID_ARG
+    assert lib.lsa_topk_approx(fake, None, 3, 4, 2, 1, None, s) == L.LSA_ERR_INVALID_ARG
 
 
 def test_empty_work_is_ok_without_launching(lib):
@@ -97,6 +99,7 @@ def test_empty_work_is_ok_without_launching(lib):
     assert lib.lsa_score(None, C.byref(c), None, None, None, C.byref(prm), None, s) == L.LSA_OK
     assert lib.lsa_topk(None, None, 0, 10, 3, None, s) == L.LSA_OK
     assert lib.lsa_topk(None, None, 5, 10, 0, None, s) == L.LSA_OK
+    assert lib.lsa_topk_approx(None, None, 0, 10, 3, 7, None, s) == L.LSA_OK
     assert lib.lsa_build_summaries(C.byref(c), None, None, 0, 4, None, s) == L.LSA_OK
 
 

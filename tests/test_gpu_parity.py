@@ -278,6 +278,50 @@ def test_topk_clustered_rows_take_every_selection_path(cols, k):
     assert np.array_equal(idx.cpu().numpy(), want)
 
 
+@pytest.mark.parametrize("path", ["rows", "cluster"])
+@pytest.mark.parametrize("cols,k", [(4097, 1), (8192, 256), (16381, 29), (16384, 2048), (32768, 100),
+                                    (32768, 4000)])
+def test_topk_row_and_cluster_kernels(cols, k, path, monkeypatch):
+    """Few long rows: one CTA per row, or one cluster of CTAs per row
+    sharing counts through distributed shared memory; both bit-exact,
+    through the boundary-bucket ranking and the bisection for heavy ties."""
+    monkeypatch.setenv("LSA_TOPK_PATH", path)
+    gen = torch.Generator().manual_seed(cols * 3 + k)
+    rows = 4
+    s = torch.randn(rows, cols, generator=gen)
+    s[1] = torch.randint(-6, 6, (cols,), generator=gen).float()       # ties far past the boundary cap
+    s[2, : cols // 3] = -math.inf
+    s[3, 100:100 + 2 * k] = 9.0                                       # a tie run longer than k at the top
+    idx = torch.empty((rows, k), dtype=torch.int32, device="cuda")
+    L.lsa_topk(s.cuda(), None, k, idx)
+    check_status_clean()
+    assert np.array_equal(idx.cpu().numpy(), oracle.topk(s.numpy(), k))
+
+
+@pytest.mark.parametrize("path", ["rows", "cluster"])
+@pytest.mark.parametrize("cols,k", [(7, 3), (2048, 62), (5000, 256), (16381, 29), (16384, 2048), (32768, 100)])
+def test_topk_approx_matches_oracle(cols, k, path, monkeypatch):
+    """The stochastic early exit equals the oracle's, bit for bit, for the
+    same seed and row numbers: exact winners above the boundary bucket and
+    the same circular sample of it (fp32 bucket decisions on both sides)."""
+    monkeypatch.setenv("LSA_TOPK_PATH", path)
+    gen = torch.Generator().manual_seed(cols * 5 + k)
+    rows = 5
+    s = torch.randn(rows, cols, generator=gen)
+    s[1] = torch.randint(-20, 20, (cols,), generator=gen).float() / 4     # crowded buckets
+    s[2, torch.rand(cols, generator=gen) < 0.5] = -math.inf
+    s[3] = 0.0
+    s[4] = torch.randn(cols, generator=gen) * 1e30
+    ncols = torch.tensor([cols, cols, cols, max(0, cols - 5), cols], dtype=torch.int32)
+    for seed in (0, 12345, 2**64 - 1):
+        idx = torch.empty((rows, k), dtype=torch.int32, device="cuda")
+        L.lsa_topk_approx(s.cuda(), ncols.cuda(), k, seed, idx)
+        check_status_clean()
+        want = np.stack([oracle.topk_approx(s[i:i + 1, : int(ncols[i])].numpy(), k, seed, row0=i)[0]
+                         for i in range(rows)])
+        assert np.array_equal(idx.cpu().numpy(), want), seed
+
+
 def test_topk_nan_is_skipped_and_flagged():
     s = torch.tensor([[0.5, float("nan"), 2.0, 1.0]], device="cuda")
     idx = torch.empty((1, 2), dtype=torch.int32, device="cuda")
@@ -438,6 +482,19 @@ def test_short_and_empty_requests(lens):
     for r, Lr in enumerate(lens):
         if Lr == 0:
             assert torch.all(st.out[r].float() == 0) and torch.all(torch.isneginf(st.lse[r]))
+
+
+@pytest.mark.parametrize("name", ["c2f_small", "c2f_wrelu_small"])
+@pytest.mark.parametrize("lens,ncand,ntok", [((0, 30, 64 * 5, 64 * 20 + 5), 32, 512),
+                                             ((64 * 40, 64 * 3 + 1, 64 * 9), 5, 100),
+                                             ((64 * 70, 64 * 66), 64, 4096), ((64 * 300, 64 * 260), 256, 2048)])
+def test_coarse_to_fine_short_requests_and_few_candidates(name, lens, ncand, ntok):
+    """Requests with fewer full blocks than candidates or fewer tokens than
+    the token budget, and candidate counts that leave most of a cluster's
+    CTAs without a block (or give each the most it takes)."""
+    w = small(name, seq_lens=lens, batch=len(lens), c2f_candidates=ncand, c2f_tokens=ntok)
+    cpu = make_inputs(w, "cpu")
+    run_and_compare_step(w, cpu, to_dev(cpu))
 
 
 def test_topk_covering_all_blocks_equals_dense():

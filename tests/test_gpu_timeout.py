@@ -1,13 +1,13 @@
 """Bounded device waits run out instead of hanging.
 
-The coarse-to-fine step's fine kernel waits for each request's candidates,
-and the tensor-core attention's tiles wait for the rest of their row before
-merging it.  Each wait gives up after a budget of SM clock cycles, records
-LSA_ERR_TIMEOUT in the device status word and lets the kernel finish.  Here
-every counter those waits read starts at a value they never reach (the
-workspace is filled with 0xff bytes instead of zeros) and the budget is cut
-to a few microseconds: the call must return promptly with LSA_ERR_TIMEOUT,
-and the same call on a zeroed workspace must then match the oracle.
+The tensor-core attention's tiles (the 64-head groups of the coarse-to-fine
+and latent-cache steps) wait for the rest of their row before merging it.
+The wait gives up after a budget of SM clock cycles, records LSA_ERR_TIMEOUT
+in the device status word and lets the kernel finish.  Here every counter
+the wait reads starts at a value it never reaches (the workspace is filled
+with 0xff bytes instead of zeros) and the budget is cut to a few
+microseconds: the call must return promptly with LSA_ERR_TIMEOUT, and the
+same call on a zeroed workspace must then match the oracle.
 """
 import time
 

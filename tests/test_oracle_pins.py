@@ -727,3 +727,102 @@ def test_weighted_relu_is_linear_in_the_weights_and_each_weight_picks_its_head()
         fg, _ = oracle.fine_scores(*args, fine_weights=one)
         qg = f64(bf16_bits(inp["q"][1, g]))
         assert np.allclose(fg, 2.5 * np.maximum(kt @ qg, 0.0), rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- approximate top-k (stochastic early exit)
+
+def test_splitmix64_published_vectors():
+    gold = json.load(open(os.path.join(GOLD, "splitmix64_vectors.json")))
+    for v in gold["vectors"]:
+        for n, want in enumerate(v["outputs"], start=1):
+            assert oracle.splitmix64(v["seed"], n) == int(want, 0)
+
+
+def _approx_invariants(s, k, sel):
+    """What any approximate selection of this kind must satisfy: keff
+    entries, ascending, candidates only, and no unselected candidate above a
+    selected one by more than one bucket width (plus the remap's rounding)."""
+    cand = ~np.isnan(s) & (s != -np.inf)
+    m = int(cand.sum())
+    keff = min(k, m)
+    chosen = sel[sel >= 0]
+    assert len(chosen) == keff and np.all(sel[keff:] == -1)
+    assert np.all(np.diff(chosen) > 0) and np.all(cand[chosen])
+    if 0 < keff < m:
+        vals = s[cand].astype(np.float64)
+        width = (vals.max() - vals.min()) / 2048
+        rest = np.setdiff1d(np.flatnonzero(cand), chosen)
+        assert s[rest].max() <= s[chosen].min() + width * (1 + 1e-4) + 1e-30
+
+
+@pytest.mark.parametrize("seed", [0, 1, 99, 2**63 + 5])
+def test_topk_approx_equals_exact_when_every_bucket_holds_one_key(seed):
+    """Distinct values spread one per bucket: the boundary bucket holds one
+    key, which the sample must take, so the result is the exact top-k."""
+    n = 2048
+    gen = np.random.default_rng(3)
+    s = gen.permutation(n).astype(np.float32)
+    for k in (1, 62, 300, 2047):
+        got = oracle.topk_approx(s[None], k, seed)[0]
+        assert np.array_equal(got, oracle.topk(s[None], k)[0])
+
+
+def test_topk_approx_invariants_random_and_clustered_rows():
+    gen = np.random.default_rng(11)
+    rows = [gen.standard_normal(5000).astype(np.float32),
+            (gen.integers(-30, 30, 4096) / 4).astype(np.float32),                   # heavy ties
+            np.concatenate([gen.standard_normal(3000), 50 + gen.standard_normal(40)]).astype(np.float32),
+            np.where(gen.random(3000) < 0.4, -np.inf, gen.standard_normal(3000)).astype(np.float32)]
+    for s in rows:
+        for k in (1, 30, 256, 2000):
+            for seed in (0, 7):
+                _approx_invariants(s, k, oracle.topk_approx(s[None], k, seed)[0])
+
+
+def test_topk_approx_all_candidates_empty_and_nan():
+    s = np.array([[1.0, np.nan, -np.inf, 3.0, 2.0]], dtype=np.float32)
+    assert oracle.topk_approx(s, 5, 1).tolist() == [[0, 3, 4, -1, -1]]
+    assert oracle.topk_approx(s, 3, 1).tolist() == [[0, 3, 4]]
+    assert oracle.topk_approx(s, 0, 1).shape == (1, 0)
+    assert oracle.topk_approx(np.full((1, 4), -np.inf, np.float32), 2, 1).tolist() == [[-1, -1]]
+
+
+def test_topk_approx_confident_winners_are_kept_and_the_rest_is_a_circular_window():
+    """h well-separated high values above a run of equal values: the high
+    ones are always taken, and the k - h others form a circular run of the
+    equal ones in column order, whose start moves with the seed."""
+    n, h, k = 1000, 7, 50
+    s = np.zeros(n, np.float32)
+    hi = np.array([13, 200, 201, 555, 700, 901, 999])
+    s[hi] = 1000 + np.arange(h) * 100
+    starts = set()
+    low = np.setdiff1d(np.arange(n), hi)
+    for seed in range(40):
+        got = oracle.topk_approx(s[None], k, seed)[0]
+        assert set(hi) <= set(got.tolist())
+        rest = np.setdiff1d(got, hi)
+        pos = np.searchsorted(low, rest)          # numbers 0 .. len(low)-1 in column order
+        assert len(pos) == k - h
+        gaps = np.diff(np.concatenate([pos, [pos[0] + len(low)]]))
+        assert np.sum(gaps != 1) == 1             # one circular run
+        starts.add(int(pos[(int(np.argmax(gaps != 1)) + 1) % len(pos)]))
+    assert len(starts) > 30
+
+
+def test_topk_approx_samples_the_boundary_bucket_uniformly():
+    """Over many seeds every key of the crowded boundary bucket is taken
+    with probability take / cnt (a binomial bound), and nothing below it."""
+    n, k = 400, 100
+    s = np.zeros(n, np.float32)
+    s[:60] = 10 + np.arange(60, dtype=np.float32)      # 60 confident winners
+    s[60:160] = 5.0                                    # boundary bucket: 100 equal keys, 40 taken
+    s[160:] = -5.0 - np.arange(n - 160, dtype=np.float32) / 1000
+    trials = 2000
+    freq = np.zeros(n)
+    for seed in range(trials):
+        got = oracle.topk_approx(s[None], k, seed * 7919 + 1)[0]
+        freq[got] += 1
+    assert np.all(freq[:60] == trials) and np.all(freq[160:] == 0)
+    p = 40 / 100
+    sd = math.sqrt(trials * p * (1 - p))
+    assert np.all(np.abs(freq[60:160] - trials * p) < 5 * sd)
