@@ -54,7 +54,9 @@ class _Params(C.Structure):
     _fields_ = [("batch", C.c_int32), ("num_q_heads", C.c_int32), ("max_blocks", C.c_int32),
                 ("k_blocks", C.c_int32), ("sink", C.c_int32), ("recent", C.c_int32),
                 ("scale", C.c_double), ("c2f_candidates", C.c_int32),
-                ("c2f_tokens", C.c_int32), ("summary_kind", C.c_int32), ("fine_weights", C.c_void_p)]
+                ("c2f_tokens", C.c_int32), ("summary_kind", C.c_int32), ("fine_weights", C.c_void_p),
+                ("pq_candidates", C.c_int32), ("pq_codes", C.c_void_p), ("pq_codebook", C.c_void_p),
+                ("pq_hit", C.c_void_p)]
 
 
 def _load():
@@ -73,6 +75,14 @@ def _load():
             lib.orc_quest_summaries.argtypes = [P, P, P, I, I, P, P]
             lib.orc_block_scores.argtypes = [P, P, C.c_int, P, P, P, P, P]
             lib.orc_topk.argtypes = [P, I, I, P]
+            lib.orc_pq_scores.argtypes = [P, P, P, P, C.c_int, C.c_int, C.c_int64, C.c_int64, P]
+            lib.orc_pq_scores.restype = C.c_int
+            lib.orc_pq_encode.argtypes = [P, P, C.c_int64, P, P]
+            lib.orc_pq_encode.restype = C.c_int
+            lib.orc_miss_filter.argtypes = [P, P, C.c_int64, C.c_int64, P, P]
+            lib.orc_miss_filter.restype = C.c_int
+            lib.orc_pq_select.argtypes = [P, P, P, P, P, C.c_int, C.c_int, P, P, P, P]
+            lib.orc_pq_select.restype = C.c_int
             lib.orc_splitmix64.argtypes = [C.c_uint64, C.c_uint64]
             lib.orc_splitmix64.restype = C.c_uint64
             lib.orc_topk_approx.argtypes = [P, I, I, I, C.c_uint64, C.c_int64, P]
@@ -153,12 +163,14 @@ class Cache:
 
 
 def _params(batch, num_q_heads, max_blocks, k_blocks=0, sink=0, recent=0, scale=1.0,
-            c2f_candidates=0, c2f_tokens=0, summary_kind=0, fine_weights=None):
-    """fine_weights: a C-contiguous float32 numpy array [batch, num_q_heads]
+            c2f_candidates=0, c2f_tokens=0, summary_kind=0, fine_weights=None,
+            pq_candidates=0, pq_codes=None, pq_codebook=None, pq_hit=None):
+    """fine_weights, pq_codes, pq_codebook, pq_hit: C-contiguous numpy arrays
     (kept alive by the caller) or None."""
+    ptr = lambda a: None if a is None else a.ctypes.data
     return _Params(batch, num_q_heads, max_blocks, k_blocks, sink, recent, float(scale),
-                   c2f_candidates, c2f_tokens, summary_kind,
-                   None if fine_weights is None else fine_weights.ctypes.data)
+                   c2f_candidates, c2f_tokens, summary_kind, ptr(fine_weights),
+                   pq_candidates, ptr(pq_codes), ptr(pq_codebook), ptr(pq_hit))
 
 
 # ---------------------------------------------------------------- formats
@@ -281,12 +293,77 @@ def fine_scores(q, index_cache: Cache, page_table, num_q_heads, r: int, h: int, 
     return f, t
 
 
+def pq_scores(q, index_cache: Cache, page_table, num_q_heads, fine_weights, pq_codes, pq_codebook,
+              r: int, h: int, t0: int, n: int):
+    """fp64 PQ32 coarse scores (LeanSparse Eq. 6) of tokens [t0, t0+n) of
+    request r, KV head h."""
+    lib = _load()
+    qa = _np(q, np.uint16)
+    pt = _np(page_table, np.int32)
+    fw = _np(fine_weights, np.float32)
+    codes = _np(pq_codes, np.uint8)
+    cbk = _np(pq_codebook, np.uint16)
+    prm = _params(pt.shape[0], num_q_heads, pt.shape[1], fine_weights=fw, pq_candidates=1,
+                  pq_codes=codes, pq_codebook=cbk)
+    out = np.empty((n,), dtype=np.float64)
+    _check(lib.orc_pq_scores(_p(qa), index_cache.ref, _p(pt), C.byref(prm), r, h, int(t0), int(n), _p(out)))
+    return out
+
+
+def pq_encode(index_cache: Cache, pq_codebook, slots):
+    """PQ32 codes [n, 32] of the index keys at flattened slots p * b + t
+    (one KV head): nearest centroid per 4-dim subvector, fp32 distances."""
+    lib = _load()
+    sl = np.ascontiguousarray(np.asarray(slots, dtype=np.int64))
+    cbk = _np(pq_codebook, np.uint16)
+    codes = np.empty((sl.shape[0], 32), dtype=np.uint8)
+    _check(lib.orc_pq_encode(index_cache.ref, _p(cbk), sl.shape[0], _p(sl), _p(codes)))
+    return codes
+
+
+def miss_filter(scores, hit, k: int):
+    """LeanSparse's miss filter over candidate coarse scores: (keep mask, tau)."""
+    lib = _load()
+    s = np.ascontiguousarray(np.asarray(scores, dtype=np.float64))
+    hh = np.ascontiguousarray(np.asarray(hit, dtype=np.uint8))
+    keep = np.empty((s.shape[0],), dtype=np.uint8)
+    tau = np.empty((1,), dtype=np.float64)
+    _check(lib.orc_miss_filter(_p(s), _p(hh), s.shape[0], int(k), _p(keep), _p(tau)))
+    return keep.astype(bool), float(tau[0])
+
+
+def pq_select(q, index_cache: Cache, page_table, seq_lens, *, num_q_heads, sink, recent, fine_weights,
+              pq_codes, pq_codebook, pq_hit, pq_candidates: int, tokens: int, r: int, h: int):
+    """The PQ coarse-to-fine selection of (r, h): dict(sel [tokens], cand
+    [C], kept [C] bool, tau)."""
+    lib = _load()
+    qa = _np(q, np.uint16)
+    pt = _np(page_table, np.int32)
+    lens = _np(seq_lens, np.int32)
+    fw = _np(fine_weights, np.float32)
+    codes = _np(pq_codes, np.uint8)
+    cbk = _np(pq_codebook, np.uint16)
+    hit = None if pq_hit is None else _np(pq_hit, np.uint8)
+    prm = _params(pt.shape[0], num_q_heads, pt.shape[1], 0, sink, recent, 1.0, 0, tokens, 0, fw,
+                  pq_candidates, codes, cbk, hit)
+    sel = np.empty((max(tokens, 1),), dtype=np.int32)
+    cand = np.empty((max(pq_candidates, 1),), dtype=np.int32)
+    kept = np.empty((max(pq_candidates, 1),), dtype=np.uint8)
+    tau = np.empty((1,), dtype=np.float64)
+    _check(lib.orc_pq_select(_p(qa), index_cache.ref, _p(pt), _p(lens), C.byref(prm), int(r), int(h),
+                             _p(sel), _p(cand), _p(kept), _p(tau)))
+    return dict(sel=sel[:tokens], cand=cand[:pq_candidates], kept=kept[:pq_candidates].astype(bool),
+                tau=float(tau[0]))
+
+
 def decode(q, cache: Cache, page_table, seq_lens, *, num_q_heads, k_blocks, sink, recent, scale,
            summ=None, index_cache: Optional[Cache] = None, index_summ=None,
            c2f_candidates: int = 0, c2f_tokens: int = 0, nthreads: int = 1, summary_kind: int = 0,
-           fine_weights=None):
+           fine_weights=None, pq_candidates: int = 0, pq_codes=None, pq_codebook=None, pq_hit=None):
     """The whole decode step.  Returns dict(out [B,Hq,dv] uint16 bf16 bits,
-    lse [B,Hq] fp64, sel [B,Hkv,ksel] int32, cand [B,Hkv,C] int32 or None)."""
+    lse [B,Hq] fp64, sel [B,Hkv,ksel] int32, cand [B,Hkv,C] int32 or None)
+    (C: the coarse block candidates, or with pq_candidates the PQ coarse
+    token candidates)."""
     lib = _load()
     qa = _np(q, np.uint16)
     pt = _np(page_table, np.int32)
@@ -296,13 +373,17 @@ def decode(q, cache: Cache, page_table, seq_lens, *, num_q_heads, k_blocks, sink
     B, maxb = pt.shape
     Hkv = cache.shape[1]
     fw = None if fine_weights is None else _np(fine_weights, np.float32)
+    codes = None if pq_codes is None else _np(pq_codes, np.uint8)
+    cbk = None if pq_codebook is None else _np(pq_codebook, np.uint16)
+    hit = None if pq_hit is None else _np(pq_hit, np.uint8)
     prm = _params(B, num_q_heads, maxb, k_blocks, sink, recent, scale, c2f_candidates, c2f_tokens,
-                  summary_kind, fw)
-    ksel = c2f_tokens if c2f_candidates > 0 else k_blocks
+                  summary_kind, fw, pq_candidates, codes, cbk, hit)
+    ksel = c2f_tokens if (c2f_candidates > 0 or pq_candidates > 0) else k_blocks
+    ncand = pq_candidates if pq_candidates > 0 else c2f_candidates
     out = np.zeros((B, num_q_heads, cache.dv), dtype=np.uint16)
     lse = np.zeros((B, num_q_heads), dtype=np.float64)
     sel = np.zeros((B, Hkv, max(ksel, 0)), dtype=np.int32)
-    cand = np.zeros((B, Hkv, c2f_candidates), dtype=np.int32) if c2f_candidates > 0 else None
+    cand = np.zeros((B, Hkv, ncand), dtype=np.int32) if ncand > 0 else None
     _check(lib.orc_decode(_p(qa), cache.ref, _p(s), index_cache.ref if index_cache else None,
                           _p(isum), _p(pt), _p(lens), C.byref(prm), int(nthreads), _p(out),
                           _p(lse), _p(sel), _p(cand)))

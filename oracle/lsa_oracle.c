@@ -125,6 +125,14 @@ typedef struct {
     int32_t summary_kind;      /* 0: mean keys; 1: Quest min/max keys      */
     const float *fine_weights; /* NULL, or [batch, num_q_heads] indexer
                                   head weights of the weighted-ReLU fine score */
+    /* PQ32 coarse-to-fine (pq_candidates > 0): token-level coarse scores
+     * from product-quantised index keys, a miss filter, then the exact
+     * weighted-ReLU rescoring (fine_weights required) */
+    int32_t pq_candidates;     /* C: token candidates of the coarse pass    */
+    const uint8_t *pq_codes;   /* [P, Hkv, b, 32] one byte per 4-dim subvector */
+    const uint16_t *pq_codebook; /* [32, 256, 4] bf16 centroids            */
+    const uint8_t *pq_hit;     /* [P, Hkv, b] 1: the token's original index
+                                  key is cached (NULL: every token is)      */
 } orc_params;
 
 enum { ORC_OK = 0, ORC_BAD_PAGE = 1, ORC_BAD_ARG = 2, ORC_NOMEM = 3 };
@@ -664,6 +672,297 @@ int orc_fine_scores(const uint16_t *q, const orc_cache *idx, const int32_t *pt,
 }
 
 /* ------------------------------------------------------------------ */
+/* Step: PQ32 coarse scores and the miss filter                        */
+/* ------------------------------------------------------------------ */
+
+/* PQ32 (LeanSparse, Section 5, "Approximate scoring with PQ"): a 128-dim
+ * index key is split into 32 four-dim subvectors, each stored as a one-byte
+ * index c_j into a codebook C_j of 256 centroids.  The coarse score of
+ * token t (Eq. 6) substitutes the centroids for the subvectors inside the
+ * indexer's weighted head aggregation:
+ *   s~_t = sum_g w_g * max(0, sum_j q_{g,j} . C_j[c_{t,j}])
+ * over the query heads g of the KV head's group (q_{g,j}: dims 4j .. 4j+3
+ * of head g's query). */
+static double pq_score(const uint16_t *q, const float *w, const uint8_t *codes, const uint16_t *codebook,
+                       int G, int dk)
+{
+    double s = 0.0;
+    for (int g = 0; g < G; ++g) {
+        const uint16_t *qg = q + (int64_t)g * dk;
+        double d = 0.0;
+        for (int j = 0; j < dk / 4; ++j) {
+            const uint16_t *cj = codebook + ((int64_t)j * 256 + codes[j]) * 4;
+            for (int e = 0; e < 4; ++e)
+                d += orc_bf16_to_f64(qg[4 * j + e]) * orc_bf16_to_f64(cj[e]);
+        }
+        s += (double)w[g] * (d > 0.0 ? d : 0.0);
+    }
+    return s;
+}
+
+/* s~ of the tokens [t0, t0 + n) of request r, KV head h (full blocks). */
+int orc_pq_scores(const uint16_t *q, const orc_cache *c, const int32_t *pt, const orc_params *prm,
+                  int r, int h, int64_t t0, int64_t n, double *out)
+{
+    const int b = c->block_size, dk = c->dk, G = prm->num_q_heads / c->num_kv_heads;
+    if (dk != 128 || !prm->pq_codes || !prm->pq_codebook || !prm->fine_weights)
+        return ORC_BAD_ARG;
+    const uint16_t *qr = q + ((int64_t)r * prm->num_q_heads + h * G) * dk;
+    const float *wr = prm->fine_weights + (int64_t)r * prm->num_q_heads + h * G;
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t t = t0 + i;
+        const int64_t p = pt[(int64_t)r * prm->max_blocks + t / b];
+        if (p < 0 || p >= c->num_pages)
+            return ORC_BAD_PAGE;
+        const uint8_t *codes = prm->pq_codes + (((int64_t)p * c->num_kv_heads + h) * b + t % b) * 32;
+        out[i] = pq_score(qr, wr, codes, prm->pq_codebook, G, dk);
+    }
+    return ORC_OK;
+}
+
+/* PQ32 encoding of index keys: per subvector, the nearest centroid by
+ * squared Euclidean distance to the dequantised key scale_t * e4m3(k8_t),
+ * ties to the lower centroid.  The distance decides an integer, so it is
+ * evaluated in fp32 in a fixed order: k = scale * e4m3 (one rounding),
+ * diff_e = k_e - C_e, dist = ((diff_0^2 + diff_1^2) + diff_2^2) + diff_3^2,
+ * each operation rounded to fp32 (no fused multiply-add).  tokens: n
+ * positions (page p, slot t) pairs flattened as p * b + t. */
+int orc_pq_encode(const orc_cache *c, const uint16_t *codebook, int64_t n, const int64_t *slots, uint8_t *codes)
+{
+    if (c->dk != 128 || !c->k8 || !c->k8_scale || c->num_kv_heads != 1)
+        return ORC_BAD_ARG;
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t base = slots[i];   /* (p * Hkv + h) * b + t with Hkv = 1 */
+        const float sc = c->k8_scale[base];
+        for (int j = 0; j < 32; ++j) {
+            volatile float kk[4];
+            for (int e = 0; e < 4; ++e)
+                kk[e] = sc * (float)orc_e4m3_to_f64(c->k8[base * 128 + 4 * j + e]);
+            int best = 0;
+            float bd = INFINITY;
+            for (int cc = 0; cc < 256; ++cc) {
+                const uint16_t *cj = codebook + ((int64_t)j * 256 + cc) * 4;
+                volatile float d0 = kk[0] - (float)orc_bf16_to_f64(cj[0]);
+                volatile float d1 = kk[1] - (float)orc_bf16_to_f64(cj[1]);
+                volatile float d2 = kk[2] - (float)orc_bf16_to_f64(cj[2]);
+                volatile float d3 = kk[3] - (float)orc_bf16_to_f64(cj[3]);
+                volatile float s0 = d0 * d0, s1 = d1 * d1, s2 = d2 * d2, s3 = d3 * d3;
+                volatile float a = s0 + s1;
+                volatile float b2 = a + s2;
+                volatile float dist = b2 + s3;
+                if (dist < bd) {
+                    bd = dist;
+                    best = cc;
+                }
+            }
+            codes[i * 32 + j] = (uint8_t)best;
+        }
+    }
+    return ORC_OK;
+}
+
+static int by_value_desc(const void *a, const void *b)
+{
+    const double x = *(const double *)a, y = *(const double *)b;
+    return (x > y) ? -1 : (x < y);
+}
+
+/* The miss filter (LeanSparse, Section 5, "Retrieving and refining
+ * candidates"): candidates whose original index key is cached (hits) are
+ * kept; a miss is dropped when its coarse score is below the candidates'
+ * k-th largest coarse score minus one sample standard deviation of the
+ * candidates' coarse scores.  With at most k candidates every one is kept
+ * (there is no k-th largest to compare with).  keep[i] = 1 / 0; returns
+ * the number kept.  The threshold is written to *tau (-inf when every
+ * candidate is kept). */
+static int64_t miss_filter(const double *s, const uint8_t *hit, int64_t n, int64_t k, uint8_t *keep, double *tau)
+{
+    *tau = -INFINITY;
+    if (n <= k) {
+        for (int64_t i = 0; i < n; ++i)
+            keep[i] = 1;
+        return n;
+    }
+    double *srt = (double *)malloc(sizeof(double) * (size_t)n);
+    if (!srt)
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        srt[i] = s[i];
+    qsort(srt, (size_t)n, sizeof(double), by_value_desc);   /* k-th largest */
+    const double sk = srt[k - 1];
+    free(srt);
+    double mean = 0.0;
+    for (int64_t i = 0; i < n; ++i)
+        mean += s[i];
+    mean /= (double)n;
+    double var = 0.0;
+    for (int64_t i = 0; i < n; ++i)
+        var += (s[i] - mean) * (s[i] - mean);
+    var /= (double)(n - 1);
+    *tau = sk - sqrt(var);
+    int64_t m = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        keep[i] = (hit[i] || s[i] >= *tau) ? 1 : 0;
+        m += keep[i];
+    }
+    return m;
+}
+
+int orc_miss_filter(const double *s, const uint8_t *hit, int64_t n, int64_t k, uint8_t *keep, double *tau)
+{
+    return miss_filter(s, hit, n, k, keep, tau) < 0 ? ORC_NOMEM : ORC_OK;
+}
+
+/* Exact weighted-ReLU index scores of explicit tokens of request r, KV
+ * head h: f_t = sum_g w_g max(0, q_g . scale_t e4m3(k8_t)). */
+static int token_scores_wrelu(const uint16_t *q, const orc_cache *c, const int32_t *pt_row, const orc_params *prm,
+                              int r, int h, int64_t n, const int64_t *tok, double *f)
+{
+    const int b = c->block_size, dk = c->dk, G = prm->num_q_heads / c->num_kv_heads;
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t t = tok[i];
+        const int64_t p = pt_row[t / b];
+        if (p < 0 || p >= c->num_pages)
+            return ORC_BAD_PAGE;
+        const int64_t base = ((int64_t)p * c->num_kv_heads + h) * b + t % b;
+        const double sc = (double)c->k8_scale[base];
+        double s = 0.0;
+        for (int g = 0; g < G; ++g) {
+            const uint16_t *qg = q + ((int64_t)r * prm->num_q_heads + h * G + g) * dk;
+            double d = 0.0;
+            for (int e = 0; e < dk; ++e)
+                d += orc_bf16_to_f64(qg[e]) * (sc * orc_e4m3_to_f64(c->k8[base * dk + e]));
+            s += (double)prm->fine_weights[(int64_t)r * prm->num_q_heads + h * G + g] * (d > 0.0 ? d : 0.0);
+        }
+        f[i] = s;
+    }
+    return ORC_OK;
+}
+
+/* The PQ coarse-to-fine selection of one (request, KV head), in the order
+ * of LeanSparse Section 5 and Figure 9:
+ *   1. coarse: s~_t for every token of the full candidate blocks (the
+ *      encoded history), top-C tokens (pq_candidates) by s~;
+ *   2. miss filter over the C candidates (hits kept, misses below the
+ *      k-th largest s~ minus one sample standard deviation dropped);
+ *   3. fine: exact weighted-ReLU scores of the kept candidates and of the
+ *      tokens of the partial last block (the unencoded tail, always scored
+ *      from its original keys), top-k (c2f_tokens) by f.
+ * chosen: the k tokens, ascending, -1 padded; cand (may be NULL): the C
+ * coarse candidates ascending, -1 padded; kept (may be NULL): 1 / 0 per
+ * cand entry.  Returns the number chosen through *nchosen. */
+static int pq_select(const uint16_t *q, const orc_cache *ic, const int32_t *pt, int64_t L, const orc_params *prm,
+                     int r, int h, int64_t *chosen, int64_t *nchosen, int32_t *cand, uint8_t *kept_out, double *tau_out)
+{
+    const int b = ic->block_size;
+    const int32_t *pt_row = pt + (int64_t)r * prm->max_blocks;
+    int64_t se, rs;
+    forced_ranges(L, prm->sink, prm->recent, &se, &rs);
+    const int64_t nfull = L / b;
+    const int64_t C = prm->pq_candidates, k = prm->c2f_tokens;
+    /* 1. coarse over the encoded history */
+    int64_t ntok = 0;
+    for (int64_t j = 0; j < nfull; ++j)
+        if (is_candidate(j, b, se, rs))
+            ntok += b;
+    int64_t cap = ntok + b + 1;
+    double *s = (double *)malloc(sizeof(double) * (size_t)cap);
+    int64_t *ids = (int64_t *)malloc(sizeof(int64_t) * (size_t)cap);
+    int64_t *cb = (int64_t *)malloc(sizeof(int64_t) * (size_t)(C > 0 ? C : 1));
+    double *cs = (double *)malloc(sizeof(double) * (size_t)(C > 0 ? C : 1));
+    uint8_t *hit = (uint8_t *)malloc((size_t)(C > 0 ? C : 1));
+    uint8_t *keep = (uint8_t *)malloc((size_t)(C > 0 ? C : 1));
+    int64_t *ft = (int64_t *)malloc(sizeof(int64_t) * (size_t)(C + b + 1));
+    double *f = (double *)malloc(sizeof(double) * (size_t)(C + b + 1));
+    int rc = ORC_OK;
+    if (!s || !ids || !cb || !cs || !hit || !keep || !ft || !f) {
+        rc = ORC_NOMEM;
+        goto out;
+    }
+    {
+        int64_t n = 0;
+        for (int64_t j = 0; j < nfull && rc == ORC_OK; ++j) {
+            if (!is_candidate(j, b, se, rs))
+                continue;
+            rc = orc_pq_scores(q, ic, pt, prm, r, h, j * b, b, s + n);
+            for (int t = 0; t < b; ++t)
+                ids[n + t] = j * b + t;
+            n += b;
+        }
+        if (rc)
+            goto out;
+        const int64_t ncb = select_topk(s, ids, n, C, cb);
+        if (cand)
+            for (int64_t i = 0; i < C; ++i)
+                cand[i] = (int32_t)cb[i];
+        /* coarse scores and hits of the candidates */
+        for (int64_t i = 0; i < ncb; ++i) {
+            const int64_t t = cb[i];
+            int64_t lo = 0, hi = n - 1;   /* ids ascend: binary search */
+            while (lo < hi) {
+                const int64_t mid = (lo + hi) / 2;
+                if (ids[mid] < t)
+                    lo = mid + 1;
+                else
+                    hi = mid;
+            }
+            cs[i] = s[lo];
+            const int64_t p = pt_row[t / b];
+            hit[i] = prm->pq_hit ? prm->pq_hit[((int64_t)p * ic->num_kv_heads + h) * b + t % b] : 1;
+        }
+        /* 2. miss filter */
+        double tau;
+        if (miss_filter(cs, hit, ncb, k, keep, &tau) < 0) {
+            rc = ORC_NOMEM;
+            goto out;
+        }
+        if (tau_out)
+            *tau_out = tau;
+        if (kept_out)
+            for (int64_t i = 0; i < C; ++i)
+                kept_out[i] = i < ncb ? keep[i] : 0;
+        /* 3. fine over the kept candidates and the tail */
+        int64_t m = 0;
+        for (int64_t i = 0; i < ncb; ++i)
+            if (keep[i])
+                ft[m++] = cb[i];
+        for (int64_t t = nfull * b; t < L; ++t)
+            if (t >= se && t < rs)
+                ft[m++] = t;
+        rc = token_scores_wrelu(q, ic, pt_row, prm, r, h, m, ft, f);
+        if (rc)
+            goto out;
+        *nchosen = select_topk(f, ft, m, k, chosen);
+    }
+out:
+    free(s);
+    free(ids);
+    free(cb);
+    free(cs);
+    free(hit);
+    free(keep);
+    free(ft);
+    free(f);
+    return rc;
+}
+
+int orc_pq_select(const uint16_t *q, const orc_cache *ic, const int32_t *pt, const int32_t *lens,
+                  const orc_params *prm, int r, int h, int32_t *chosen, int32_t *cand, uint8_t *kept, double *tau)
+{
+    if (prm->pq_candidates <= 0 || !prm->fine_weights)
+        return ORC_BAD_ARG;
+    int64_t *ch = (int64_t *)malloc(sizeof(int64_t) * (size_t)(prm->c2f_tokens > 0 ? prm->c2f_tokens : 1));
+    if (!ch)
+        return ORC_NOMEM;
+    int64_t nch = 0;
+    int rc = pq_select(q, ic, pt, lens[r], prm, r, h, ch, &nch, cand, kept, tau);
+    for (int64_t i = 0; i < prm->c2f_tokens; ++i)
+        chosen[i] = (int32_t)ch[i];
+    free(ch);
+    return rc;
+}
+
+/* ------------------------------------------------------------------ */
 /* The decode step                                                     */
 /* ------------------------------------------------------------------ */
 
@@ -677,7 +976,7 @@ static int decode_unit(const uint16_t *q, const orc_cache *c, const uint16_t *su
     const int b = c->block_size;
     const int64_t L = lens[r];
     const int32_t *pt_row = pt + (int64_t)r * prm->max_blocks;
-    const int c2f = prm->c2f_candidates > 0;
+    const int c2f = prm->c2f_candidates > 0 || prm->pq_candidates > 0;
     const int64_t ksel = c2f ? prm->c2f_tokens : prm->k_blocks;
     int64_t se, rs;
     forced_ranges(L, prm->sink, prm->recent, &se, &rs);
@@ -693,7 +992,12 @@ static int decode_unit(const uint16_t *q, const orc_cache *c, const uint16_t *su
     }
 
     int64_t nchosen = 0;
-    if (!c2f) {
+    if (prm->pq_candidates > 0) {
+        rc = pq_select(q, ic, pt, L, prm, r, h, chosen, &nchosen,
+                       cand ? cand + ((int64_t)r * c->num_kv_heads + h) * prm->pq_candidates : NULL, NULL, NULL);
+        if (rc)
+            goto done;
+    } else if (!c2f) {
         rc = row_scores(q, c, 0, summ, pt, L, prm, r, h, scores);
         if (rc)
             goto done;
@@ -777,7 +1081,9 @@ int orc_decode(const uint16_t *q, const orc_cache *c, const uint16_t *summ,
 {
     if (prm->num_q_heads % c->num_kv_heads != 0)
         return ORC_BAD_ARG;
-    if (prm->c2f_candidates > 0 && (!ic || !ic->k8 || !ic->k8_scale))
+    if ((prm->c2f_candidates > 0 || prm->pq_candidates > 0) && (!ic || !ic->k8 || !ic->k8_scale))
+        return ORC_BAD_ARG;
+    if (prm->pq_candidates > 0 && (!prm->pq_codes || !prm->pq_codebook || !prm->fine_weights))
         return ORC_BAD_ARG;
     const int64_t units = (int64_t)prm->batch * c->num_kv_heads;
     int rc = ORC_OK;

@@ -826,3 +826,199 @@ def test_topk_approx_samples_the_boundary_bucket_uniformly():
     p = 40 / 100
     sd = math.sqrt(trials * p * (1 - p))
     assert np.all(np.abs(freq[60:160] - trials * p) < 5 * sd)
+
+
+# ---------------------------------------------------------------- PQ32 coarse scores and the miss filter
+
+def pq_setup(**kw):
+    w = small_workloads()["c2f_pq_small"].replace(**kw)
+    inp = make_inputs(w, "cpu")
+    ic = oracle.Cache(None, None, k8=inp["idx_keys"], k8_scale=inp["idx_scale"])
+    return w, inp, ic
+
+
+def lossless_pq(inp, seed=0):
+    """Rewrites the index keys as their codes' centroids exactly: centroids
+    drawn from values exact in e4m3 and bf16, keys = e4m3(centroid), scale 1."""
+    rng = np.random.default_rng(seed)
+    vals = np.array([-4, -3, -2, -1.5, -1, -0.5, 0, 0.5, 1, 1.5, 2, 3, 4], dtype=np.float32)
+    cb = torch.from_numpy(rng.choice(vals, (32, 256, 4))).to(torch.bfloat16)
+    codes = inp["pq_codes"].long()
+    P, H, b, _ = codes.shape
+    keys = cb.float()[torch.arange(32), codes].reshape(P, H, b, 128)
+    inp["pq_codebook"] = cb
+    inp["idx_keys"] = keys.to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+    inp["idx_scale"] = torch.ones((P, H, b), dtype=torch.float32)
+    return oracle.Cache(None, None, k8=inp["idx_keys"], k8_scale=inp["idx_scale"])
+
+
+def test_pq_score_with_lossless_codes_is_the_exact_indexer_score():
+    """When every key's subvectors are exactly its codes' centroids, Eq. 6's
+    PQ score equals the exact weighted-ReLU score of the FP8 key (the fine
+    score, a separate function pinned above): a wrong subspace offset,
+    centroid index, weight or a ReLU outside the head sum fails here."""
+    w, inp, ic = pq_setup(seq_lens=(640, 300))
+    ic = lossless_pq(inp)
+    b = w.block_size
+    for r in (0, 1):
+        for blk in (0, 3):
+            f, _ = oracle.fine_scores(inp["q"], ic, inp["page_table"], w.num_q_heads, r, 0,
+                                      np.array([blk]), fine_weights=inp["fine_weights"])
+            s = oracle.pq_scores(inp["q"], ic, inp["page_table"], w.num_q_heads, inp["fine_weights"],
+                                 inp["pq_codes"], inp["pq_codebook"], r, 0, blk * b, b)
+            assert np.allclose(s, f, rtol=1e-12, atol=1e-9)
+
+
+def test_pq_score_relu_and_weights():
+    """All-positive queries against all-negative centroids: every head's dot
+    is negative, so the score is 0; flipping the centroids' sign gives the
+    weighted sum of the heads' dots (linear in the weights)."""
+    w, inp, ic = pq_setup(seq_lens=(640, 300))
+    inp["q"] = inp["q"].abs()
+    cb = inp["pq_codebook"].float().abs().to(torch.bfloat16)
+    b = w.block_size
+    args = (inp["q"], ic, inp["page_table"], w.num_q_heads)
+    neg = oracle.pq_scores(*args, inp["fine_weights"], inp["pq_codes"], (-cb.float()).to(torch.bfloat16), 0, 0, 0, b)
+    assert np.all(neg == 0.0)
+    pos = oracle.pq_scores(*args, inp["fine_weights"], inp["pq_codes"], cb, 0, 0, 0, b)
+    w2 = (inp["fine_weights"] * 2.0).contiguous()
+    pos2 = oracle.pq_scores(*args, w2, inp["pq_codes"], cb, 0, 0, 0, b)
+    assert np.all(pos > 0) and np.allclose(pos2, 2 * pos, rtol=1e-12)
+
+
+def test_pq_encode_picks_the_nearest_centroid():
+    """Keys equal to a centroid get it back (the lowest index among equal
+    centroids); random keys get a centroid at the smallest fp64 distance up
+    to fp32 rounding."""
+    w, inp, ic = pq_setup(seq_lens=(640, 300))
+    b = w.block_size
+    slots = np.arange(0, 40, dtype=np.int64)     # tokens of page 0 (one KV head)
+    got = oracle.pq_encode(ic, inp["pq_codebook"], slots)
+    K8 = inp["idx_keys"].view(torch.float8_e4m3fn).float().numpy().astype(np.float64).reshape(-1, 128)
+    S = inp["idx_scale"].numpy().astype(np.float64).reshape(-1)
+    cb = inp["pq_codebook"].float().numpy().astype(np.float64)
+    for i, s in enumerate(slots):
+        k = (K8[s] * S[s]).reshape(32, 4)
+        d = ((cb - k[:, None, :]) ** 2).sum(-1)          # [32, 256]
+        dmin = d.min(axis=1)
+        chosen = d[np.arange(32), got[i]]
+        assert np.all(chosen <= dmin * (1 + 1e-5) + 1e-6)
+    ic2 = lossless_pq(inp, seed=3)
+    cbl = inp["pq_codebook"].float().numpy()
+    got2 = oracle.pq_encode(ic2, inp["pq_codebook"], slots)
+    codes = inp["pq_codes"].numpy().reshape(-1, 32)
+    for i, s in enumerate(slots):
+        for j in range(32):
+            same = np.flatnonzero((cbl[j] == cbl[j, codes[s, j]]).all(axis=1))
+            assert got2[i, j] == same[0]
+
+
+def test_miss_filter_closed_form():
+    """Hits stay; a miss stays only at or above the k-th largest coarse score
+    minus one sample standard deviation (numpy's, ddof=1)."""
+    s = np.array([10.0, 9.0, 8.0, 1.0, 0.0, 4.0])
+    hit = np.array([0, 0, 0, 0, 1, 0])
+    keep, tau = oracle.miss_filter(s, hit, 2)
+    assert tau == pytest.approx(9.0 - np.std(s, ddof=1), rel=1e-14)
+    assert keep.tolist() == [True, True, True, False, True, False]
+    keep, tau = oracle.miss_filter(s, np.zeros(6), 6)      # no k-th largest: everything kept
+    assert keep.all() and tau == -math.inf
+    keep, _ = oracle.miss_filter(s, np.ones(6), 1)         # all hits
+    assert keep.all()
+
+
+def _pq_args(w, inp, ic, **kw):
+    a = dict(num_q_heads=w.num_q_heads, sink=w.sink, recent=w.recent, fine_weights=inp["fine_weights"],
+             pq_codes=inp["pq_codes"], pq_codebook=inp["pq_codebook"], pq_hit=inp["pq_hit"],
+             pq_candidates=w.pq_candidates, tokens=w.c2f_tokens)
+    a.update(kw)
+    return a
+
+
+def _exact_topk_all_tokens(w, inp, ic, r, k):
+    """Brute force: the exact weighted-ReLU top-k over every full block's
+    tokens and the partial last block's tokens (no forced ranges)."""
+    b = w.block_size
+    L = int(inp["seq_lens"][r])
+    nblk = (L + b - 1) // b
+    f, t = oracle.fine_scores(inp["q"], ic, inp["page_table"], w.num_q_heads, r, 0,
+                              np.arange(nblk), fine_weights=inp["fine_weights"])
+    f = np.where(t < L, f, -np.inf)
+    return oracle.topk(f[None], k)[0]
+
+
+def test_pq_select_every_token_a_cached_candidate_is_the_exact_topk():
+    """With C at least every encoded token and every key cached, the coarse
+    pass keeps everything and the selection is the exact top-k over all
+    tokens (the coarse-to-fine claim with no approximation left)."""
+    w, inp, ic = pq_setup(seq_lens=(640 + 21, 300), recent=0)
+    for r in (0, 1):
+        got = oracle.pq_select(inp["q"], ic, inp["page_table"], inp["seq_lens"],
+                               **_pq_args(w, inp, ic, pq_hit=None, pq_candidates=700, tokens=50), r=r, h=0)
+        assert np.array_equal(got["sel"], _exact_topk_all_tokens(w, inp, ic, r, 50))
+        assert got["kept"][got["cand"] >= 0].all()
+
+
+def test_pq_select_lossless_codes_coarse_is_exact():
+    """Lossless codes make the coarse score exact: the C candidates are the
+    exact top-C of the encoded tokens, and with C = k and every key cached
+    the selection is the exact top-k over the candidates and the tail."""
+    w, inp, ic = pq_setup(seq_lens=(640 + 21, 300), recent=0)
+    ic = lossless_pq(inp, seed=1)
+    b = w.block_size
+    for r in (0, 1):
+        L = int(inp["seq_lens"][r])
+        nfull = L // b
+        f, t = oracle.fine_scores(inp["q"], ic, inp["page_table"], w.num_q_heads, r, 0, np.arange(nfull),
+                                  fine_weights=inp["fine_weights"])
+        got = oracle.pq_select(inp["q"], ic, inp["page_table"], inp["seq_lens"],
+                               **_pq_args(w, inp, ic, pq_hit=None, pq_candidates=60, tokens=60), r=r, h=0)
+        assert np.array_equal(got["cand"], oracle.topk(f[None], 60)[0])
+        tail = np.arange(nfull * b, L)
+        ft, tt = oracle.fine_scores(inp["q"], ic, inp["page_table"], w.num_q_heads, r, 0,
+                                    np.array([nfull]) if L % b else np.zeros(0, np.int64),
+                                    fine_weights=inp["fine_weights"])
+        pool = np.concatenate([got["cand"], tail])
+        fpool = np.concatenate([f[got["cand"]], ft[: len(tail)]])
+        order = sorted(range(len(pool)), key=lambda i: (-fpool[i], pool[i]))[:60]
+        assert np.array_equal(got["sel"], np.sort(pool[order]))
+
+
+def test_pq_select_filter_and_final_tokens():
+    """The kept candidates are exactly the hits and the misses at or above
+    the threshold; the final tokens are kept candidates or tail tokens."""
+    w, inp, ic = pq_setup()
+    b = w.block_size
+    for r in (0, 1):
+        L = int(inp["seq_lens"][r])
+        got = oracle.pq_select(inp["q"], ic, inp["page_table"], inp["seq_lens"], **_pq_args(w, inp, ic), r=r, h=0)
+        cand = got["cand"][got["cand"] >= 0]
+        pt = inp["page_table"][r].numpy()
+        hit = inp["pq_hit"].numpy()[pt[cand // b], 0, cand % b].astype(bool)
+        s = np.concatenate([oracle.pq_scores(inp["q"], ic, inp["page_table"], w.num_q_heads, inp["fine_weights"],
+                                             inp["pq_codes"], inp["pq_codebook"], r, 0, int(t), 1) for t in cand])
+        keep, tau = oracle.miss_filter(s, hit, w.c2f_tokens)
+        assert got["tau"] == pytest.approx(tau, rel=1e-12)
+        assert np.array_equal(got["kept"][: len(cand)], keep)
+        assert 0 < keep.sum() < len(cand)
+        sel = got["sel"][got["sel"] >= 0]
+        tail = set(range((L // b) * b, L))
+        allowed = set(cand[keep].tolist()) | tail
+        assert set(sel.tolist()) <= allowed
+
+
+def test_pq_decode_attends_its_selection():
+    w, inp, ic = pq_setup()
+    c = oracle.Cache(inp["k_cache"], inp["v_cache"])
+    d = oracle.decode(inp["q"], c, inp["page_table"], inp["seq_lens"], num_q_heads=w.num_q_heads, k_blocks=0,
+                      sink=w.sink, recent=w.recent, scale=w.softmax_scale, index_cache=ic,
+                      c2f_tokens=w.c2f_tokens, fine_weights=inp["fine_weights"], pq_candidates=w.pq_candidates,
+                      pq_codes=inp["pq_codes"], pq_codebook=inp["pq_codebook"], pq_hit=inp["pq_hit"])
+    for r in (0, 1):
+        got = oracle.pq_select(inp["q"], ic, inp["page_table"], inp["seq_lens"], **_pq_args(w, inp, ic), r=r, h=0)
+        assert np.array_equal(d["sel"][r, 0], got["sel"])
+        assert np.array_equal(d["cand"][r, 0], got["cand"])
+    a = oracle.attend_selection(inp["q"], c, inp["page_table"], inp["seq_lens"], d["sel"],
+                                num_q_heads=w.num_q_heads, sink=w.sink, recent=w.recent, scale=w.softmax_scale,
+                                token_mode=True)
+    assert np.array_equal(a["out"], d["out"])

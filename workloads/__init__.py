@@ -58,6 +58,9 @@ class Workload:
     c2f_tokens: int = 0
     summary_kind: int = 0       # 0: mean keys; 1: Quest's max and min keys
     fine_weighted: bool = False  # coarse-to-fine: weighted-ReLU fine score with drawn head weights
+    pq_candidates: int = 0      # PQ32 coarse-to-fine: token candidates of the coarse pass
+    pq_hit_frac: float = 0.5    # ... fraction of tokens whose original index key is cached
+    pq_noise: float = 0.35      # ... key = its codes' centroids + N(0, pq_noise^2) per dim
     extra_pages: int = 0        # unused pages appended to the pool
     description: str = ""
 
@@ -107,6 +110,13 @@ WORKLOADS = {
         c2f_candidates=256, c2f_tokens=2048, fine_weighted=True,
         description="the coarse-to-fine workload with the weighted-ReLU indexer fine score "
                     "(head weights ~ U[0, 1))"),
+    "c2f_pq": Workload(
+        name="c2f_pq", seed=5, batch=4, num_q_heads=64, num_kv_heads=1, dk=128, dv=128,
+        block_size=64, seq_len=524288, sink=0, recent=0, k_blocks=0,
+        c2f_tokens=2048, pq_candidates=8192,
+        description="B=4, L=512K, 64-head FP8 indexer with PQ32 codes: coarse top-8192 tokens by the "
+                    "PQ weighted-ReLU score, miss filter (half the tokens' keys cached), exact "
+                    "weighted-ReLU top-2048 tokens, 64q/1kv d=128"),
     "mla": Workload(
         name="mla", seed=4, batch=4, num_q_heads=64, num_kv_heads=1, dk=576, dv=512,
         block_size=64, seq_len=1048576, sink=4, recent=128, k_blocks=29, v_aliased=True,
@@ -135,6 +145,9 @@ def small_workloads() -> dict:
         "c2f_wrelu_small": W["c2f_wrelu"].replace(
             name="c2f_wrelu_small", seed=16, batch=2, seq_len=0, seq_lens=(16384 + 37, 9000),
             c2f_candidates=32, c2f_tokens=512, recent=37),
+        "c2f_pq_small": W["c2f_pq"].replace(
+            name="c2f_pq_small", seed=17, batch=2, seq_len=0, seq_lens=(16384 + 37, 9000),
+            pq_candidates=1024, c2f_tokens=256, recent=37),
         "quest_small": W["b16_32k_quest"].replace(
             name="quest_small", seed=15, batch=3, seq_len=0, seq_lens=(4096, 3001, 777)),
     }
@@ -226,16 +239,28 @@ def make_inputs(w: Workload, device: str = "cpu", lens: Optional[Sequence[int]] 
                seq_lens=torch.tensor(lens, dtype=torch.int32, device=dev),
                lens=lens, num_pages=num_pages, max_blocks=max_blocks)
 
-    if w.c2f_candidates > 0:
+    if w.pq_candidates > 0:
+        # PQ32 index keys: a codebook of 256 centroids per 4-dim subspace,
+        # a code per (token, subspace), the key its centroids plus noise
+        cbk = torch.randn((32, 256, 4), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        codes = torch.randint(0, 256, (num_pages, Hkv, b, 32), generator=g, device=dev, dtype=torch.int64)
+        kk = cbk.float()[torch.arange(32, device=dev), codes].reshape(num_pages, Hkv, b, w.dk)
+        kk += w.pq_noise * torch.randn((num_pages, Hkv, b, w.dk), generator=g, device=dev, dtype=torch.float32)
+        out["pq_codebook"] = cbk.contiguous()
+        out["pq_codes"] = codes.to(torch.uint8).contiguous()
+    elif w.c2f_candidates > 0:
         kk = torch.randn((num_pages, Hkv, b, w.dk), generator=g, device=dev, dtype=torch.float32)
+    if w.c2f_candidates > 0 or w.pq_candidates > 0:
         amax = kk.abs().amax(dim=-1).clamp_min(1e-30)
         scale = (amax / 448.0).to(torch.float32)
         k8 = (kk / scale.unsqueeze(-1)).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
         out["idx_keys"] = k8.view(torch.uint8)
         out["idx_scale"] = scale.contiguous()
-        if w.fine_weighted:
+        if w.fine_weighted or w.pq_candidates > 0:
             # indexer head weights of the weighted-ReLU fine score
             out["fine_weights"] = torch.rand((B, Hq), generator=g, device=dev, dtype=torch.float32)
+        if w.pq_candidates > 0:
+            out["pq_hit"] = (torch.rand((num_pages, Hkv, b), generator=g, device=dev) < w.pq_hit_frac).to(torch.uint8)
     return out
 
 
@@ -261,12 +286,22 @@ def algorithmic_bytes(w: Workload, lens: Sequence[int]) -> dict:
                 ncand += 1
         nblk = (L + b - 1) // b
         pt += nblk * 4
-        summ += ncand * Hkv * w.dk * 2 * (2 if w.summary_kind == 1 else 1)
-        if w.c2f_candidates > 0:
+        if w.pq_candidates > 0:
+            # the PQ32 codes of every candidate token (32 bytes), the FP8
+            # keys and scales of at most C candidates plus the tail, their
+            # hit flags
+            summ += ncand * b * Hkv * 32
+            ntail = L - nb_full * b
+            nfine = min(w.pq_candidates, ncand * b)
+            fine += (nfine + ntail) * Hkv * (w.dk * 1 + 4) + nfine * Hkv
+            ntok = forced + min(w.c2f_tokens, nfine + ntail)
+        elif w.c2f_candidates > 0:
+            summ += ncand * Hkv * w.dk * 2
             ncb = min(w.c2f_candidates, ncand)
             fine += ncb * b * Hkv * (w.dk * 1 + 4)
             ntok = forced + min(w.c2f_tokens, ncb * b)
         else:
+            summ += ncand * Hkv * w.dk * 2 * (2 if w.summary_kind == 1 else 1)
             ntok = forced + min(w.k_blocks, ncand) * b
         kv_row = w.dk * 2 + (0 if w.v_aliased else w.dv * 2)
         sel += ntok * Hkv * kv_row
