@@ -276,26 +276,67 @@ def stage_times(insts, reps: int, stream) -> dict:
         e1.record(stream)
         stream.synchronize()
         approx_ms = e0.elapsed_time(e1) / reps
-        hit = tot = 0
-        for i in range(R):
-            b = bufs[i]
-            topk(i)
-            exact = b["idx"].clone()
-            topk_approx(i)
-            stream.synchronize()
-            ex, ap = exact.cpu().numpy(), b["idx"].cpu().numpy()
-            for r in range(ex.shape[0]):
-                e = set(ex[r][ex[r] >= 0].tolist())
-                hit += len(e & set(ap[r][ap[r] >= 0].tolist()))
-                tot += len(e)
+        recall, mass = topk_recall(bufs, topk, topk_approx, stream)
+        # tie-heavy rows (the scores' signs: two values, the boundary bucket
+        # crowded), where the exact selection needs its bisection
+        for b in bufs:
+            sc = b["scores"]
+            b["scores"] = torch.where(torch.isneginf(sc), sc, torch.sign(sc))
+        tie_exact = graph_ms(topk, reps, stream)
+        tie_approx = graph_ms(topk_approx, reps, stream)
+        tie_recall, tie_mass = topk_recall(bufs, topk, topk_approx, stream)
     out["_topk_approx"] = {"rows": int(bufs[0]["scores"].shape[0]), "cols": int(bufs[0]["scores"].shape[1]),
                            "k": int(bufs[0]["idx"].shape[1]), "exact_us": round(out["topk"] * 1e3, 2),
                            "approx_us": round(approx_ms * 1e3, 2),
                            "speedup": round(out["topk"] / max(approx_ms, 1e-9), 3),
-                           "recall": round(hit / max(tot, 1), 5),
+                           "recall": round(recall, 5), "score_mass": round(mass, 6),
+                           "tie_heavy": {"exact_us": round(tie_exact * 1e3, 2), "approx_us": round(tie_approx * 1e3, 2),
+                                         "speedup": round(tie_exact / max(tie_approx, 1e-9), 3),
+                                         "recall": round(tie_recall, 5), "score_mass": round(tie_mass, 6),
+                                         "rows": "sign of the step's scores (-inf kept)"},
                            "note": "lsa_topk vs lsa_topk_approx on the step's score rows, each a CUDA graph "
                                    "rotating over the instances; recall = exact selections kept"}
     return out
+
+
+def graph_ms(fn, reps: int, stream) -> float:
+    """Device time of one call of fn(i), from a CUDA graph of reps calls."""
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        for i in range(reps):
+            fn(i)
+    gr.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    gr.replay()
+    e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def topk_recall(bufs, topk, topk_approx, stream):
+    """(fraction of the exact top-k selections the approximate one keeps,
+    the approximate selection's score mass over the exact one's): equal
+    scores make the first low and leave the second at 1."""
+    hit = tot = 0
+    mass_a = mass_e = 0.0
+    for i in range(len(bufs)):
+        b = bufs[i]
+        topk(i)
+        exact = b["idx"].clone()
+        topk_approx(i)
+        stream.synchronize()
+        ex, ap = exact.cpu().numpy(), b["idx"].cpu().numpy()
+        sc = b["scores"].double().cpu().numpy()
+        for r in range(ex.shape[0]):
+            er, ar = ex[r][ex[r] >= 0], ap[r][ap[r] >= 0]
+            hit += len(set(er.tolist()) & set(ar.tolist()))
+            tot += len(er)
+            base = sc[r][er].min() if len(er) else 0.0     # shift so the masses compare positive parts
+            mass_e += float((sc[r][er] - base).sum())
+            mass_a += float((sc[r][ar] - base).sum())
+    return hit / max(tot, 1), (mass_a / mass_e if mass_e > 0 else 1.0)
 
 
 def max_over_ranks(ms: float, dev, world: int) -> float:

@@ -486,13 +486,13 @@ __device__ __forceinline__ int32_t topk_out(const TopkArgs &a, int row, int col)
     return cb * a.b + col % a.b;
 }
 
-// One block of 1024 threads per row, KPT columns per thread: the exact
-// bucketed top-k of topk_bucket.cuh.
-template <int KPT, bool APPROX = false>
-__global__ void __launch_bounds__(kTopkThreads) k_topk_rows(TopkArgs a)
+// One block of NT threads per row (256 for rows of up to 2048 columns, else
+// 1024), KPT columns per thread: the bucketed top-k of topk_bucket.cuh.
+template <int KPT, bool APPROX = false, int NT = kTopkThreads>
+__global__ void __launch_bounds__(NT) k_topk_rows(TopkArgs a)
 {
     pdl_enter();
-    __shared__ BucketScratch<kTopkThreads> sm;
+    __shared__ BucketScratch<NT> sm;
     const int row = blockIdx.x, tid = threadIdx.x;
     int n = a.num_cols ? a.num_cols[row] : a.cols;
     n = max(0, min(n, a.cols));
@@ -522,10 +522,10 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_rows(TopkArgs a)
     }
     if (nan) flag_error(a.status, LSA_ERR_NAN);
     int32_t *orow = a.idx + (int64_t)row * a.k;
-    const int keff = block_bucket_topk<kTopkThreads, KPT, APPROX>(
+    const int keff = block_bucket_topk<NT, KPT, APPROX>(
         keys, a.k, sm, [&](int pos, int col) { orow[pos] = topk_out(a, row, col); },
         APPROX ? splitmix64(a.seed, (uint64_t)row + 1) : 0ull);
-    for (int i = keff + tid; i < a.k; i += kTopkThreads) orow[i] = -1;
+    for (int i = keff + tid; i < a.k; i += NT) orow[i] = -1;
 }
 
 // Few long rows: a cluster of CS CTAs of kClThreads threads per row, KPT
@@ -1009,11 +1009,13 @@ cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s, bool *unsupported)
     cudaError_t e;
     const dim3 g(a.rows), blk(kTopkThreads);
     if (a.approx) {
-        if (a.cols <= kTopkThreads * 8) e = launch_step_kernel(k_topk_rows<8, true>, g, blk, 0, s, a);
+        if (a.cols <= 256 * 8) e = launch_step_kernel(k_topk_rows<8, true, 256>, g, dim3(256), 0, s, a);
+        else if (a.cols <= kTopkThreads * 8) e = launch_step_kernel(k_topk_rows<8, true>, g, blk, 0, s, a);
         else if (a.cols <= kTopkThreads * 16) e = launch_step_kernel(k_topk_rows<16, true>, g, blk, 0, s, a);
         else e = launch_step_kernel(k_topk_rows<32, true>, g, blk, 0, s, a);
     } else {
-        if (a.cols <= kTopkThreads * 8) e = launch_step_kernel(k_topk_rows<8>, g, blk, 0, s, a);
+        if (a.cols <= 256 * 8) e = launch_step_kernel(k_topk_rows<8, false, 256>, g, dim3(256), 0, s, a);
+        else if (a.cols <= kTopkThreads * 8) e = launch_step_kernel(k_topk_rows<8>, g, blk, 0, s, a);
         else if (a.cols <= kTopkThreads * 16) e = launch_step_kernel(k_topk_rows<16>, g, blk, 0, s, a);
         else e = launch_step_kernel(k_topk_rows<32>, g, blk, 0, s, a);
     }
