@@ -48,13 +48,16 @@ L2_BYTES = 129 * 1024 * 1024
 NCU_TRAFFIC = {}
 
 
-def peaks():
+def peaks(kind: str = "hbm"):
+    """(peak, "measured" | "fallback"): HBM GB/s, or dense bf16 TFLOP/s
+    (the burst figure: the kernel is timed on its own)."""
+    key, fallback = ("hbm_gbs", 6800.0) if kind == "hbm" else ("bf16_tflops", 1900.0)
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
+        return float(p[key]), "measured"
     except Exception:
-        return 6800.0, "fallback"
+        return fallback, "fallback"
 
 
 # ---------------------------------------------------------------- clocks
@@ -131,7 +134,10 @@ class Instance:
             self.summ = torch.zeros((g["num_pages"], Hkv, 2, w.dk), dtype=torch.bfloat16, device=dev)
         else:
             self.summ = torch.zeros((g["num_pages"], Hkv, w.dk), dtype=torch.bfloat16, device=dev)
-        if w.c2f_candidates > 0:
+        if w.pq_candidates > 0:
+            self.icache = L.make_cache(g["idx_keys"], None, k_scale=g["idx_scale"])
+            nsel = w.c2f_tokens
+        elif w.c2f_candidates > 0:
             self.icache = L.make_cache(g["idx_keys"], None, k_scale=g["idx_scale"])
             L.lsa_build_summaries(self.icache, g["page_table"], g["seq_lens"], self.summ)
             nsel = w.c2f_tokens
@@ -143,7 +149,9 @@ class Instance:
             nsel = w.k_blocks
         self.params = L.make_params(B, w.num_q_heads, g["max_blocks"], w.k_blocks, w.sink, w.recent,
                                     w.softmax_scale, w.c2f_candidates, w.c2f_tokens,
-                                    summary_kind=w.summary_kind, fine_head_weights=g.get("fine_weights"))
+                                    summary_kind=w.summary_kind, fine_head_weights=g.get("fine_weights"),
+                                    pq_candidates=w.pq_candidates, pq_codes=g.get("pq_codes"),
+                                    pq_codebook=g.get("pq_codebook"), pq_hit=g.get("pq_hit"))
         self.ws = torch.zeros(max(16, L.lsa_decode_step_workspace_size(self.cache, self.params)),
                               dtype=torch.uint8, device=dev)
         self.idx = torch.empty((B, Hkv, max(1, nsel)), dtype=torch.int32, device=dev)
@@ -173,22 +181,49 @@ def selects_in_attention(w) -> bool:
 
 
 def kernels_per_step(inst) -> int:
-    import ctypes
-    w = inst.w
-    if selects_in_attention(w):
-        return 2   # score, attention with the selection inside
-    # score + top-k (+ fine score + fine top-k) + attention
-    n = 2 + (2 if w.c2f_candidates > 0 else 0) + 1
-    # the tensor-core attention (GQA groups of 2..8, dk = dv in {64, 128})
-    # merges its parts itself; the CUDA-core kernel adds a merge launch when split
-    group = w.num_q_heads // w.num_kv_heads
-    tc = (w.c2f_candidates == 0 and not w.v_aliased and w.dk == w.dv and w.dk in (64, 128)
-          and 2 <= group <= 8 and group % 2 == 0 and os.environ.get("LSA_ATTENTION_PATH") != "cuda_core")
-    if not tc:
-        lib = inst.L.load_library()
-        ws_attn = lib.lsa_sparse_decode_workspace_size(ctypes.byref(inst.cache), ctypes.byref(inst.params))
-        n += 1 if ws_attn > 0 else 0
+    """Kernel launches of one step, as the library's planner makes them."""
+    n = inst.L.lsa_decode_step_launches(inst.cache, inst.icache, inst.params)
+    assert n > 0, "invalid step shapes"
     return n
+
+
+def pq_stage_times(insts, reps: int, stream) -> dict:
+    """The PQ32 coarse-to-fine step's stages through their entry points:
+    the coarse scores (lsa_pq_scores) and attention over each instance's
+    own selection (lsa_sparse_decode); the selection kernels are the step's
+    time minus these."""
+    w = insts[0].w
+    L = insts[0].L
+    R = len(insts)
+    bufs = []
+    with torch.cuda.stream(stream):
+        for it in insts:
+            it.step(stream=stream)   # each instance's own selection
+        stream.synchronize()
+    for it in insts:
+        T = it.g["max_blocks"] * w.block_size
+        bufs.append(dict(coarse=torch.empty((w.batch, T), dtype=torch.float32, device=it.g["q"].device),
+                         ws=torch.zeros(max(16, L.lsa_sparse_decode_workspace_size(it.cache, it.params)),
+                                        dtype=torch.uint8, device=it.g["q"].device)))
+
+    def pq_scores(i):
+        it, b = insts[i % R], bufs[i % R]
+        L.lsa_pq_scores(it.g["q"], it.icache, it.g["page_table"], it.g["seq_lens"], it.params, b["coarse"], stream)
+
+    def attn(i):
+        it, b = insts[i % R], bufs[i % R]
+        L.lsa_sparse_decode(it.g["q"], it.cache, it.g["page_table"], it.g["seq_lens"], it.idx, it.params, it.out,
+                            it.lse, b["ws"], stream)
+
+    out = {}
+    with torch.cuda.stream(stream):
+        for fn in (pq_scores, attn):
+            for i in range(R):
+                fn(i)
+        stream.synchronize()
+        out["pq_scores"] = graph_ms(pq_scores, reps, stream)
+        out["attention"] = graph_ms(attn, reps, stream)
+    return out
 
 
 def stage_times(insts, reps: int, stream) -> dict:
@@ -198,6 +233,8 @@ def stage_times(insts, reps: int, stream) -> dict:
     (lsa_topk), the coarse-to-fine fine pass (lsa_fine_topk) and attention
     with its merge (lsa_sparse_decode over the stage's own selection)."""
     w = insts[0].w
+    if w.pq_candidates > 0:
+        return pq_stage_times(insts, reps, stream)
     L = insts[0].L
     B, Hkv = w.batch, w.num_kv_heads
     c2f = w.c2f_candidates > 0
@@ -439,8 +476,16 @@ def run_gpu(args, rank, world, dev):
     # q, page table and lengths from pinned host memory and reads back out/lse
     e2e = e2e_leg(insts, args, stream)
 
+    pq_tokens = 0
+    if w.pq_candidates > 0:
+        # encoded candidate tokens of the first instance (every instance has the same lengths)
+        for Lr in first.g["lens"]:
+            se = min(w.sink, Lr)
+            rs = max(Lr - w.recent, se)
+            pq_tokens += sum(w.block_size for j in range(Lr // w.block_size)
+                             if j * w.block_size >= se and (j + 1) * w.block_size <= rs)
     return dict(ms=ms, step_bytes=step_bytes, acc=acc, R=R, clocks=clocks, stages=st, e2e=e2e,
-                kernels=kernels_per_step(insts[0]), w=w)
+                kernels=kernels_per_step(insts[0]), w=w, pq_tokens=pq_tokens)
 
 
 def e2e_leg(insts, args, stream):
@@ -527,7 +572,13 @@ def cpu_baseline(w, budget_s: float = 12.0):
     c = oracle.Cache(inp["k_cache"], None if w.v_aliased else inp["v_cache"], dv=w.dv if w.v_aliased else None)
     kw = dict(num_q_heads=w.num_q_heads, k_blocks=w.k_blocks, sink=w.sink, recent=w.recent,
               scale=w.softmax_scale)
-    if w.c2f_candidates > 0:
+    if w.pq_candidates > 0:
+        ic = oracle.Cache(None, None, k8=inp["idx_keys"], k8_scale=inp["idx_scale"])
+        kw.update(index_cache=ic, c2f_tokens=w.c2f_tokens, fine_weights=inp["fine_weights"],
+                  pq_candidates=w.pq_candidates, pq_codes=inp["pq_codes"], pq_codebook=inp["pq_codebook"],
+                  pq_hit=inp["pq_hit"])
+        summ = None
+    elif w.c2f_candidates > 0:
         ic = oracle.Cache(None, None, k8=inp["idx_keys"], k8_scale=inp["idx_scale"])
         isumm, _ = oracle.summaries(ic, inp["page_table"], inp["seq_lens"], use_index_keys=True)
         kw.update(index_cache=ic, index_summ=isumm, c2f_candidates=w.c2f_candidates, c2f_tokens=w.c2f_tokens,
@@ -617,7 +668,15 @@ def main():
     # moves no algorithmic bytes (its input and output are intermediates)
     stage_bytes = {"score": acc["summaries"] + acc["page_table"] + acc["q_out"] // 2, "topk": 0,
                    "fine": acc["fine"], "attention": acc["kv"] + acc["q_out"]}
-    if st and selects_in_attention(w):
+    if st and w.pq_candidates > 0:
+        # four launches: coarse scores and bucket counts, the selection
+        # cluster kernel, attention; the selection's time is the step's
+        # minus the coarse scores' and attention's
+        kernel_ms = {"k_pq_scores": st["pq_scores"], "attention": st["attention"],
+                     "k_pq_hist + k_pq_select": max(ms_step - st["pq_scores"] - st["attention"], 1e-9)}
+        kbytes = {"k_pq_scores": stage_bytes["score"], "attention": stage_bytes["attention"],
+                  "k_pq_hist + k_pq_select": acc["fine"]}
+    elif st and selects_in_attention(w):
         # the step is two launches: the score kernel and the attention kernel
         # that also selects the blocks; the latter's time is the step's time
         # minus the score kernel's (both CUDA-event timings)
@@ -629,14 +688,27 @@ def main():
     # the dominant kernel: the longest stage that moves algorithmic bytes
     moving = {k: v for k, v in kernel_ms.items() if kbytes.get(k, 0) > 0}
     dominant = max(moving, key=moving.get)
-    ach = kbytes[dominant] / (kernel_ms[dominant] / 1e3) / 1e9
-    roof = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(ach / peak, 4), "peak_kind": peak_kind,
-            "duration_us": round(kernel_ms[dominant] * 1e3, 2),
-            "algorithmic_bytes": kbytes[dominant],
-            "timing": ("step minus score kernel" if dominant.startswith("k_attn_flat")
-                       else "CUDA graph of the stage's entry point"),
-            "traffic": NCU_TRAFFIC.get((w.name, dominant))}
+    if dominant == "k_pq_scores":
+        # a dense contraction: every encoded candidate token's 64 x 128 dots
+        flops = 2.0 * w.num_q_heads * w.dk * res["pq_tokens"]
+        tpeak, tkind = peaks("tensor")
+        ach = flops / (kernel_ms[dominant] / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": dominant, "achieved": round(ach, 1), "peak": tpeak, "unit": "TFLOP/s",
+                "frac": round(ach / tpeak, 4), "peak_kind": tkind, "duration_us": round(kernel_ms[dominant] * 1e3, 2),
+                "algorithmic_flops": flops, "algorithmic_bytes": kbytes[dominant],
+                "hbm_frac": round(kbytes[dominant] / (kernel_ms[dominant] / 1e3) / 1e9 / peak, 4),
+                "timing": "CUDA graph of the stage's entry point",
+                "traffic": NCU_TRAFFIC.get((w.name, dominant))}
+    else:
+        ach = kbytes[dominant] / (kernel_ms[dominant] / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dominant, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "peak_kind": peak_kind,
+                "duration_us": round(kernel_ms[dominant] * 1e3, 2),
+                "algorithmic_bytes": kbytes[dominant],
+                "timing": ("step minus score kernel" if dominant.startswith("k_attn_flat")
+                           else "step minus the other kernels" if dominant.startswith("k_pq_hist")
+                           else "CUDA graph of the stage's entry point"),
+                "traffic": NCU_TRAFFIC.get((w.name, dominant))}
     cb = None
     if rank == 0 and not args.no_cpu_baseline:
         cb = cpu_baseline(res["w"])

@@ -129,6 +129,34 @@ typedef struct lsa_params {
      * * e4m3(k8_t) (LeanSparse, Section 5, Eq. 6, on the exact keys);
      * needs 64 query heads per KV head. */
     const float *fine_head_weights;
+    /* PQ32 coarse-to-fine (LeanSparse, Section 5: "Approximate scoring with
+     * PQ" and "Retrieving and refining candidates"); pq_candidates > 0
+     * selects it (c2f_candidates must then be 0).  Each token of a full block
+     * carries a PQ32 code: 32 bytes, byte j the index of the centroid of
+     * dims 4j .. 4j+3 of its index key among the 256 of codebook j.  A step
+     *   1. scores every token of every full candidate block with Eq. 6,
+     *        s~_t = sum_g w[r,g] max(0, sum_j q[r,g,4j:4j+4] . C_j[c_{t,j}])
+     *      (w = fine_head_weights, required),
+     *   2. keeps the pq_candidates tokens of largest s~ (ties to the lower
+     *      token),
+     *   3. drops a kept token whose original index key is not cached (a
+     *      miss: pq_hit 0) when its s~ is below the candidates' c2f_tokens-th
+     *      largest s~ minus the sample standard deviation (n - 1) of the
+     *      candidates' s~ (no drop with at most c2f_tokens candidates),
+     *   4. scores the remaining candidates and the tokens of the partial
+     *      last block with their FP8 index keys (the weighted-ReLU score
+     *      above, with the exact keys) and keeps the c2f_tokens best, whose
+     *      positions are the selection.
+     * pq_codes [num_pages, 1, block_size, 32] uint8 device (the index
+     * cache's geometry, one KV head); pq_codebook [32, 256, 4] bf16 device;
+     * pq_hit [num_pages, 1, block_size] uint8 device, 1 = the token's index
+     * key is cached, or NULL (every key cached).  Needs 64 query heads over
+     * one KV head, dk = 128.  The miss filter's threshold is computed in
+     * fp64 from fp32 coarse scores. */
+    int32_t pq_candidates;
+    const uint8_t *pq_codes;
+    const void *pq_codebook;
+    const uint8_t *pq_hit;
 } lsa_params;
 
 /* Status and errors ------------------------------------------------------ */
@@ -257,6 +285,35 @@ lsa_status lsa_fine_topk(const void *q, const lsa_cache *index_cache, const int3
                          int32_t *tok_idx, void *workspace, size_t workspace_bytes,
                          lsa_stream_t stream);
 
+/* Kernel launches one lsa_decode_step call with these shapes makes (the
+ * selection and attention kernels the planner picks for them), or -1 when
+ * the shapes are invalid.  index_cache: as for lsa_decode_step (NULL unless
+ * coarse-to-fine).  No device work. */
+int32_t lsa_decode_step_launches(const lsa_cache *cache, const lsa_cache *index_cache, const lsa_params *params);
+
+/* PQ32 codes of the index keys of every full block of each request (the
+ * encoded history): byte j of token t is the centroid of codebook j nearest
+ * to dims 4j .. 4j+3 of scale_t * e4m3(k8_t) in squared Euclidean distance,
+ * ties to the lower centroid (LeanSparse, Section 5: each completed page is
+ * encoded when it is written).  The distance is evaluated in fp32 in one
+ * fixed order (k = scale * e4m3; d_e = k_e - C_e; ((d0^2 + d1^2) + d2^2) +
+ * d3^2, each step rounded, no fused multiply-add), so the codes are
+ * reproducible bit for bit.  index_cache: LSA_KEYS_E4M3, one KV head, dk =
+ * 128.  codebook [32, 256, 4] bf16 device; codes [num_pages, 1, block_size,
+ * 32] uint8 device (pages of partial blocks are not written).  Errors as
+ * lsa_build_summaries. */
+lsa_status lsa_pq_encode(const lsa_cache *index_cache, const void *codebook, const int32_t *page_table,
+                         const int32_t *seq_lens, int32_t batch, int32_t max_blocks, uint8_t *codes,
+                         lsa_stream_t stream);
+
+/* The PQ32 coarse scores s~_t (step 1 of the PQ32 coarse-to-fine in
+ * lsa_params) of every token position t < max_blocks * block_size:
+ * scores [batch, max_blocks * block_size] fp32 device, -inf for tokens that
+ * are not in a full candidate block.  params: pq_codes, pq_codebook and
+ * fine_head_weights are used; fp32 accumulation of exact bf16 products. */
+lsa_status lsa_pq_scores(const void *q, const lsa_cache *index_cache, const int32_t *page_table,
+                         const int32_t *seq_lens, const lsa_params *params, float *scores, lsa_stream_t stream);
+
 /* Step 4: sparse attention ------------------------------------------------ */
 
 /* Bytes of workspace lsa_sparse_decode needs for these shapes (partial
@@ -270,8 +327,10 @@ size_t lsa_sparse_decode_workspace_size(const lsa_cache *cache, const lsa_params
  * split into parts whose partial (o, m, l) are merged by log-sum-exp.
  * idx [batch, Hkv, n] int32 device, ascending, -1 padded, where n = k_blocks
  * and entries are block indices (single stage), or n = c2f_tokens and
- * entries are token positions (c2f_candidates > 0).  Entries that are not
- * candidates are skipped and flagged (LSA_ERR_BOUNDS).  A request with
+ * entries are token positions (c2f_candidates > 0 or pq_candidates > 0).
+ * A selected block must be a candidate; a selected token must lie outside
+ * the forced ranges (it may be in the partial last block).  Other entries
+ * are skipped and flagged (LSA_ERR_BOUNDS).  A request with
  * seq_lens[r] == 0 gets out = 0 and lse = -inf.
  *   out [batch, Hq, dv] bf16 device; lse [batch, Hq] fp32 device or NULL.
  * workspace: device, >= lsa_sparse_decode_workspace_size bytes (may be NULL

@@ -79,6 +79,8 @@ def _load():
             lib.orc_pq_scores.restype = C.c_int
             lib.orc_pq_encode.argtypes = [P, P, C.c_int64, P, P]
             lib.orc_pq_encode.restype = C.c_int
+            lib.orc_token_scores_wrelu.argtypes = [P, P, P, P, C.c_int, C.c_int, C.c_int64, P, P]
+            lib.orc_token_scores_wrelu.restype = C.c_int
             lib.orc_miss_filter.argtypes = [P, P, C.c_int64, C.c_int64, P, P]
             lib.orc_miss_filter.restype = C.c_int
             lib.orc_pq_select.argtypes = [P, P, P, P, P, C.c_int, C.c_int, P, P, P, P]
@@ -319,6 +321,20 @@ def pq_encode(index_cache: Cache, pq_codebook, slots):
     codes = np.empty((sl.shape[0], 32), dtype=np.uint8)
     _check(lib.orc_pq_encode(index_cache.ref, _p(cbk), sl.shape[0], _p(sl), _p(codes)))
     return codes
+
+
+def token_scores_wrelu(q, index_cache: Cache, page_table, num_q_heads, fine_weights, r: int, h: int, tokens):
+    """fp64 weighted-ReLU index scores (the exact keys) of explicit tokens."""
+    lib = _load()
+    qa = _np(q, np.uint16)
+    pt = _np(page_table, np.int32)
+    fw = _np(fine_weights, np.float32)
+    tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
+    prm = _params(pt.shape[0], num_q_heads, pt.shape[1], fine_weights=fw)
+    out = np.empty((tok.shape[0],), dtype=np.float64)
+    _check(lib.orc_token_scores_wrelu(_p(qa), index_cache.ref, _p(pt), C.byref(prm), int(r), int(h), tok.shape[0],
+                                      _p(tok), _p(out)))
+    return out
 
 
 def miss_filter(scores, hit, k: int):

@@ -839,6 +839,14 @@ static int token_scores_wrelu(const uint16_t *q, const orc_cache *c, const int32
     return ORC_OK;
 }
 
+int orc_token_scores_wrelu(const uint16_t *q, const orc_cache *c, const int32_t *pt, const orc_params *prm,
+                           int r, int h, int64_t n, const int64_t *tok, double *f)
+{
+    if (!prm->fine_weights || !c->k8 || !c->k8_scale)
+        return ORC_BAD_ARG;
+    return token_scores_wrelu(q, c, pt + (int64_t)r * prm->max_blocks, prm, r, h, n, tok, f);
+}
+
 /* The PQ coarse-to-fine selection of one (request, KV head), in the order
  * of LeanSparse Section 5 and Figure 9:
  *   1. coarse: s~_t for every token of the full candidate blocks (the
@@ -1169,8 +1177,8 @@ void orc_lse_merge(int nparts, int dv, const double *o, const double *lse,
 /* Attention over T = F U (given selection) for every (request, KV head):
  * the definition behind a sparse decode call that receives its selection
  * (block indices, or token positions when token_mode != 0; ascending, -1
- * padded, nsel per row).  Entries that are not candidates, or that do not
- * ascend, are skipped. */
+ * padded, nsel per row).  Blocks that are not candidates, tokens inside the
+ * forced ranges, and entries that do not ascend are skipped. */
 int orc_attend_selection(const uint16_t *q, const orc_cache *c, const int32_t *pt, const int32_t *lens,
                          const orc_params *prm, const int32_t *sel, int32_t nsel, int token_mode,
                          uint16_t *out, double *lse)
@@ -1194,8 +1202,10 @@ int orc_attend_selection(const uint16_t *q, const orc_cache *c, const int32_t *p
                 int64_t e = srow[i];
                 if (e < 0 || e <= prev)
                     continue;
-                int64_t j = token_mode ? e / b : e;
-                if (!is_candidate(j, b, se, rs))
+                /* a selected block must be a candidate; a selected token
+                 * need only lie outside the forced ranges (the PQ32
+                 * selection rescores the unencoded tail and may keep it) */
+                if (token_mode ? !(e >= se && e < rs) : !is_candidate(e, b, se, rs))
                     continue;
                 prev = e;
                 if (token_mode)

@@ -125,10 +125,15 @@ lsa_status check_params(const lsa_params *p, const CacheView &v)
     if (p->c2f_candidates < 0 || p->c2f_tokens < 0 || p->num_splits < 0) return LSA_ERR_INVALID_ARG;
     if (p->batch > 65535 || (int64_t)p->max_blocks * v.b > INT32_MAX) return LSA_ERR_INVALID_ARG;
     if (p->summary_kind != LSA_SUMMARY_MEAN && p->summary_kind != LSA_SUMMARY_MINMAX) return LSA_ERR_INVALID_ARG;
+    if (p->pq_candidates < 0 || (p->pq_candidates > 0 && p->c2f_candidates > 0)) return LSA_ERR_INVALID_ARG;
     return LSA_OK;
 }
 
 lsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LSA_OK : LSA_ERR_CUDA; }
+
+// Whether the selection is of tokens (the two coarse-to-fine variants)
+// rather than of blocks.
+bool token_mode_of(const lsa_params *p) { return p->c2f_candidates > 0 || p->pq_candidates > 0; }
 
 // Bounded waits give up after this many SM clock cycles (about a second
 // by default).  LSA_SPIN_BUDGET (environment, cycles) overrides it; tests set
@@ -153,7 +158,7 @@ float scale_of(const lsa_params *p, int dk)
 lsa_status check_decode_args(const void *q, const int32_t *page_table, const int32_t *seq_lens, const int32_t *idx,
                              const lsa_params *p, const void *out)
 {
-    const bool token_mode = p->c2f_candidates > 0;
+    const bool token_mode = token_mode_of(p);
     const int nsel = token_mode ? p->c2f_tokens : p->k_blocks;
     if (!q || !page_table || !seq_lens || !out || !aligned16(q) || (nsel > 0 && !idx)) return LSA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(out) & 7u) != 0) return LSA_ERR_INVALID_ARG;
@@ -374,25 +379,66 @@ lsa_status run_attention(const void *q, const CacheView &v, const int32_t *pt, c
 }
 
 // Workspace of the decode step: [scores | selection | c2f extras | attention].
+// PQ32 coarse-to-fine: [coarse scores of every token | selection |
+// candidates | row extremes + bucket counts | attention].
 struct StepLayout {
     size_t scores, sel, cand, fine, attn, total;
 };
 
 lsa_status step_layout(const CacheView &v, const CacheView *iv, const lsa_params *p, StepLayout *L)
 {
-    const bool c2f = p->c2f_candidates > 0;
-    const CacheView &sv = c2f ? *iv : v;
+    const bool c2f = p->c2f_candidates > 0, pq = p->pq_candidates > 0;
+    const CacheView &sv = (c2f || pq) ? *iv : v;
     AttnPlan pl;
-    lsa_status rc = plan_attention(v, p, c2f, &pl);
+    lsa_status rc = plan_attention(v, p, c2f || pq, &pl);
     if (rc != LSA_OK) return rc;
     const size_t rows = (size_t)p->batch * sv.hkv;
-    L->scores = round_up(rows * p->max_blocks * sizeof(float));
-    L->sel = round_up(rows * (size_t)(c2f ? p->c2f_tokens : p->k_blocks) * sizeof(int32_t));
-    L->cand = c2f ? round_up(rows * (size_t)p->c2f_candidates * sizeof(int32_t)) : 0;
-    L->fine = c2f ? round_up(rows * (size_t)p->c2f_candidates * sv.b * sizeof(float)) : 0;
+    if (pq) {
+        L->scores = round_up(rows * p->max_blocks * (size_t)sv.b * sizeof(float));
+        L->sel = round_up(rows * (size_t)p->c2f_tokens * sizeof(int32_t));
+        L->cand = round_up(rows * (size_t)p->pq_candidates * sizeof(int32_t));
+        L->fine = round_up(rows * 2 * sizeof(uint32_t)) + round_up(rows * (size_t)kPqBins * sizeof(uint32_t));
+    } else {
+        L->scores = round_up(rows * p->max_blocks * sizeof(float));
+        L->sel = round_up(rows * (size_t)(c2f ? p->c2f_tokens : p->k_blocks) * sizeof(int32_t));
+        L->cand = c2f ? round_up(rows * (size_t)p->c2f_candidates * sizeof(int32_t)) : 0;
+        L->fine = c2f ? round_up(rows * (size_t)p->c2f_candidates * sv.b * sizeof(float)) : 0;
+    }
     L->attn = pl.ws_bytes;
     L->total = L->scores + L->sel + L->cand + L->fine + L->attn;
     return LSA_OK;
+}
+
+// The PQ arguments of a step or a scoring call (pointers the caller checked).
+PqArgs pq_args(const void *q, const CacheView &iv, const int32_t *page_table, const int32_t *seq_lens,
+               const lsa_params *p)
+{
+    PqArgs a;
+    memset(&a, 0, sizeof a);
+    a.q = static_cast<const uint16_t *>(q);
+    a.weights = p->fine_head_weights;
+    a.ic = iv;
+    a.codes = p->pq_codes;
+    a.codebook = static_cast<const uint16_t *>(p->pq_codebook);
+    a.hit = p->pq_hit;
+    a.pt = page_table;
+    a.lens = seq_lens;
+    a.batch = p->batch;
+    a.hq = p->num_q_heads;
+    a.max_blocks = p->max_blocks;
+    a.sink = p->sink_tokens;
+    a.recent = p->recent_tokens;
+    a.ncand = p->pq_candidates;
+    a.tok_k = p->c2f_tokens;
+    a.status = status_word();
+    a.spin_budget = spin_budget();
+    return a;
+}
+
+bool pq_inputs_ok(const void *q, const lsa_params *p)
+{
+    return q && aligned16(q) && p->fine_head_weights && p->pq_codes && aligned16(p->pq_codes) && p->pq_codebook &&
+           aligned16(p->pq_codebook);
 }
 
 }  // namespace
@@ -672,12 +718,77 @@ lsa_status lsa_fine_topk(const void *q, const lsa_cache *index_cache, const int3
     return from_cuda(e);
 }
 
+int32_t lsa_decode_step_launches(const lsa_cache *cache, const lsa_cache *index_cache, const lsa_params *params)
+{
+    CacheView v;
+    if (make_view(cache, true, &v) != LSA_OK || check_params(params, v) != LSA_OK) return -1;
+    if (params->batch == 0) return 0;
+    AttnPlan pl;
+    if (plan_attention(v, params, token_mode_of(params), &pl) != LSA_OK) return -1;
+    const int32_t attn = pl.flat ? 1 : 1 + ((pl.splits > 1 && !pl.umma_merge) ? 1 : 0);
+    if (params->pq_candidates > 0) return 3 + attn;   // coarse scores, bucket counts, selection
+    if (params->c2f_candidates > 0) {
+        CacheView iv;
+        if (make_view(index_cache, false, &iv) != LSA_OK) return -1;
+        const bool fused = params->c2f_tokens > 0 &&
+                           c2f_fine_supported(iv, params->num_q_heads, params->max_blocks, params->c2f_candidates,
+                                              params->c2f_tokens, params->fine_head_weights != nullptr);
+        if (fused) return 2 + attn;   // coarse scores, the cluster kernel
+        return 2 + (params->c2f_tokens > 0 ? 2 : 0) + attn;
+    }
+    if (pl.flat && attention_flat_can_select(params->max_blocks, params->k_blocks)) return 2;
+    return 1 + (params->k_blocks > 0 ? 1 : 0) + attn;
+}
+
+lsa_status lsa_pq_encode(const lsa_cache *index_cache, const void *codebook, const int32_t *page_table,
+                         const int32_t *seq_lens, int32_t batch, int32_t max_blocks, uint8_t *codes,
+                         lsa_stream_t stream)
+{
+    CacheView iv;
+    lsa_status rc = make_view(index_cache, false, &iv);
+    if (rc != LSA_OK) return rc;
+    if (batch < 0 || (batch > 0 && max_blocks <= 0) || batch > 65535) return LSA_ERR_INVALID_ARG;
+    if (!iv.e4m3 || iv.dk != 128 || iv.hkv != 1) return LSA_ERR_UNSUPPORTED;
+    if (batch == 0) return LSA_OK;
+    if (!codebook || !aligned16(codebook) || !page_table || !seq_lens || !codes) return LSA_ERR_INVALID_ARG;
+    if ((iv.kts & 3) || (iv.kps & 3) || (reinterpret_cast<uintptr_t>(iv.k) & 3)) return LSA_ERR_INVALID_ARG;
+    PqArgs a;
+    memset(&a, 0, sizeof a);
+    a.ic = iv;
+    a.codebook = static_cast<const uint16_t *>(codebook);
+    a.pt = page_table;
+    a.lens = seq_lens;
+    a.batch = batch;
+    a.max_blocks = max_blocks;
+    a.codes_out = codes;
+    a.status = status_word();
+    return from_cuda(launch_pq_encode(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lsa_status lsa_pq_scores(const void *q, const lsa_cache *index_cache, const int32_t *page_table,
+                         const int32_t *seq_lens, const lsa_params *params, float *scores, lsa_stream_t stream)
+{
+    CacheView iv;
+    lsa_status rc = make_view(index_cache, false, &iv);
+    if (rc != LSA_OK) return rc;
+    if ((rc = check_params(params, iv)) != LSA_OK) return rc;
+    if (!iv.e4m3 || iv.dk != 128 || iv.hkv != 1 || params->num_q_heads != 64) return LSA_ERR_UNSUPPORTED;
+    if (params->batch == 0) return LSA_OK;
+    if (!pq_inputs_ok(q, params) || !page_table || !seq_lens || !scores) return LSA_ERR_INVALID_ARG;
+    PqArgs a = pq_args(q, iv, page_table, seq_lens, params);
+    a.coarse = scores;   // no row extremes or counts: scores only
+    bool unsup = false;
+    cudaError_t e = launch_pq_scores(a, reinterpret_cast<cudaStream_t>(stream), &unsup);
+    if (unsup) return LSA_ERR_UNSUPPORTED;
+    return from_cuda(e);
+}
+
 size_t lsa_sparse_decode_workspace_size(const lsa_cache *cache, const lsa_params *params)
 {
     CacheView v;
     if (make_view(cache, true, &v) != LSA_OK || check_params(params, v) != LSA_OK) return 0;
     AttnPlan pl;
-    if (plan_attention(v, params, params->c2f_candidates > 0, &pl) != LSA_OK) return 0;
+    if (plan_attention(v, params, token_mode_of(params), &pl) != LSA_OK) return 0;
     return pl.ws_bytes;
 }
 
@@ -691,7 +802,7 @@ lsa_status lsa_sparse_decode(const void *q, const lsa_cache *cache, const int32_
     if ((rc = check_params(params, v)) != LSA_OK) return rc;
     if (params->batch == 0) return LSA_OK;
     if ((rc = check_decode_args(q, page_table, seq_lens, idx, params, out)) != LSA_OK) return rc;
-    const bool token_mode = params->c2f_candidates > 0;
+    const bool token_mode = token_mode_of(params);
     const int nsel = token_mode ? params->c2f_tokens : params->k_blocks;
     return run_attention(q, v, page_table, seq_lens, nsel > 0 ? idx : nullptr, params, token_mode, out, lse,
                          static_cast<uint8_t *>(workspace), workspace_bytes,
@@ -717,15 +828,46 @@ lsa_status lsa_decode_step(const void *q, const lsa_cache *cache, const void *su
     lsa_status rc = make_view(cache, true, &v);
     if (rc != LSA_OK) return rc;
     if ((rc = check_params(params, v)) != LSA_OK) return rc;
-    const bool c2f = params->c2f_candidates > 0;
+    const bool c2f = params->c2f_candidates > 0, pq = params->pq_candidates > 0;
     CacheView iv;
-    if (c2f) {
+    if (c2f || pq) {
         if ((rc = make_view(index_cache, false, &iv)) != LSA_OK) return rc;
         if (!iv.e4m3 || iv.hkv != v.hkv || iv.b != v.b || iv.dk != v.dk) return LSA_ERR_INVALID_ARG;
     } else {
         iv = v;
     }
     if (params->batch == 0) return LSA_OK;
+    if (pq) {
+        // PQ32 coarse-to-fine: coarse scores of every encoded token and the
+        // rows' bucket counts, one cluster per request for the candidates,
+        // the miss filter, the exact rescoring and the token selection, then
+        // attention over the selected tokens
+        if (!pq_inputs_ok(q, params) || !page_table || !seq_lens || !out) return LSA_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(out) & 7u) != 0) return LSA_ERR_INVALID_ARG;
+        if (!pq_supported(iv, params->num_q_heads, params->max_blocks, params->pq_candidates, params->c2f_tokens))
+            return LSA_ERR_UNSUPPORTED;
+        StepLayout L;
+        if ((rc = step_layout(v, &iv, params, &L)) != LSA_OK) return rc;
+        if (L.total > 0 && (!workspace || workspace_bytes < L.total)) return LSA_ERR_WORKSPACE;
+        cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+        uint8_t *ws = static_cast<uint8_t *>(workspace);
+        const size_t rows = (size_t)params->batch;
+        PqArgs a = pq_args(q, iv, page_table, seq_lens, params);
+        a.coarse = reinterpret_cast<float *>(ws);
+        a.tok_idx = idx_out ? idx_out : reinterpret_cast<int32_t *>(ws + L.scores);
+        a.cand_out = reinterpret_cast<int32_t *>(ws + L.scores + L.sel);
+        a.row_ext = reinterpret_cast<uint32_t *>(ws + L.scores + L.sel + L.cand);
+        a.hist = reinterpret_cast<uint32_t *>(ws + L.scores + L.sel + L.cand + round_up(rows * 2 * sizeof(uint32_t)));
+        bool unsup = false;
+        cudaError_t e = launch_pq_scores(a, st, &unsup);
+        if (unsup) return LSA_ERR_UNSUPPORTED;
+        if (e != cudaSuccess) return LSA_ERR_CUDA;
+        e = launch_pq_select(a, st, &unsup);
+        if (unsup) return LSA_ERR_UNSUPPORTED;
+        if (e != cudaSuccess) return LSA_ERR_CUDA;
+        return run_attention(q, v, page_table, seq_lens, a.tok_idx, params, true, out, lse,
+                             ws + L.scores + L.sel + L.cand + L.fine, L.attn, st);
+    }
     if (!q || !summaries || !page_table || !seq_lens || !out || !aligned16(q) || !aligned16(summaries))
         return LSA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(out) & 7u) != 0) return LSA_ERR_INVALID_ARG;
@@ -922,7 +1064,7 @@ extern "C" lsa_status lsa_sparse_decode_static_scratch(const void *q, const lsa_
     if (rc != LSA_OK) return rc;
     if ((rc = check_params(params, v)) != LSA_OK) return rc;
     AttnPlan plan;
-    if ((rc = plan_attention(v, params, params->c2f_candidates > 0, &plan)) != LSA_OK) return rc;
+    if ((rc = plan_attention(v, params, token_mode_of(params), &plan)) != LSA_OK) return rc;
     if (plan.ws_bytes > kStaticScratchBytes) return LSA_ERR_WORKSPACE;
     if (params->batch == 0) return LSA_OK;
     if ((rc = check_decode_args(q, page_table, seq_lens, idx, params, out)) != LSA_OK) return rc;

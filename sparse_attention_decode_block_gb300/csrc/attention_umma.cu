@@ -73,13 +73,6 @@ struct UmLayout {
     static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
 };
 
-// Byte offset of 16-byte chunk j (0..7) of row t inside an atom column of
-// 8-row x 128-byte atoms with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t atom_offset(int t, int j)
-{
-    return (uint32_t)((t >> 3) * 1024 + (t & 7) * 128 + ((j ^ (t & 7)) << 4));
-}
-
 // Reduces 32 per-thread values over the warp's 32 lanes column by column
 // (a reduce-scatter: each step hands half of the columns to the partner
 // lane); lane L ends with column L.

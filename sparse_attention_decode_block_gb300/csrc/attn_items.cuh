@@ -130,7 +130,9 @@ __device__ int2 describe_token(const AttnArgs &a, const RowPlan &pl, int r, int 
     const int prev = ei > 0 ? irow[ei - 1] : -1;
     if (t == -1) return row;
     const int j = t / b;
-    const bool valid = t >= 0 && (int64_t)j * b >= pl.se && (int64_t)(j + 1) * b <= pl.rs && prev < t;
+    // a selected token is any token outside the forced ranges (it may lie in
+    // the partial last block: the PQ32 selection rescores that tail)
+    const bool valid = t >= 0 && (int64_t)t >= pl.se && (int64_t)t < pl.rs && prev < t;
     if (!valid) {
         flag_error(a.status, LSA_ERR_BOUNDS);
         return row;

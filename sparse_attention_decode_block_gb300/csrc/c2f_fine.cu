@@ -17,14 +17,15 @@
 #include <mutex>
 
 #include "lsa_device.cuh"
+#include "fine_tile.cuh"
 #include "topk_cluster.cuh"
 
 namespace lsa {
 namespace {
 
-constexpr int kCfThreads = 512;
-constexpr int kCfWarps = kCfThreads / 32;
-constexpr int kCfTok = 1024;                 // tokens one CTA rescores at most
+constexpr int kCfThreads = kFtThreads;
+constexpr int kCfWarps = kFtWarps;
+constexpr int kCfTok = kFtTok;               // tokens one CTA rescores at most
 constexpr int kCfMaxCand = 64;               // candidate blocks one CTA takes at most
 constexpr int kCfKpt = kCfTok / kCfThreads;  // fine-score columns per thread
 
@@ -40,25 +41,6 @@ struct CfLayout {
     static constexpr int SMEM = PG + kCfMaxCand * 4;
 };
 static_assert(CfLayout::SMEM + sizeof(ClusterTopkScratch<kCfThreads, 8>) <= 227 * 1024, "shared memory");
-
-// Byte offset of 16-byte chunk u of token t's 128-byte key row: the chunk
-// index is XORed with t mod 8, so that 8 consecutive tokens' same chunk
-// fall in different banks.
-__device__ __forceinline__ uint32_t cf_key_off(int t, int u) { return (uint32_t)(t * 128 + ((u ^ (t & 7)) << 4)); }
-
-// Two floats -> f16x2 (low half = lo).
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
-{
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two)
-{
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
-    return h2;
-}
 
 template <int CS, int KPT1, bool WRELU>
 __global__ void __launch_bounds__(kCfThreads, 1) k_c2f_fine(FineArgs a)
@@ -81,43 +63,14 @@ __global__ void __launch_bounds__(kCfThreads, 1) k_c2f_fine(FineArgs a)
     int *s_pg = reinterpret_cast<int *>(smem + LY::PG);
 
     // ---- prologue, before the coarse scores are final: the query side
-    uint32_t qa[8][4];      // WRELU: this warp's A fragments (16 heads x 128 dims, f16)
-    float w_lo = 0.f, w_hi = 0.f;
+    WreluQ Q;               // WRELU: this warp's A fragments and weights (fine_tile.cuh)
     float qs[16];           // head sum: this lane's 16 dims of the query sum
-    const int mt = warp & 3;
-    const int rr = lane >> 2, cc = lane & 3;
     if constexpr (WRELU) {
-        // A fragment of m16n8k16 with the k index permuted within each
-        // 16-dim slice (logical k 2cc, 2cc+1, 2cc+8, 2cc+9 = dims 4cc ..
-        // 4cc+3), the same permutation as the B fragments below.  The bf16
-        // queries are exact in f16 for 2^-17 <= |q| < 2^16; a larger one is
-        // flagged (LSA_ERR_BOUNDS) and the request scores nothing.
-        const uint16_t *q0 = a.q + ((int64_t)r * a.hq + 16 * mt + rr) * 128;
-        const uint16_t *q8 = q0 + 8 * 128;
-        bool big = false;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint2 x0 = *reinterpret_cast<const uint2 *>(q0 + 16 * ks + 4 * cc);
-            const uint2 x8 = *reinterpret_cast<const uint2 *>(q8 + 16 * ks + 4 * cc);
-            const float2 f00 = bf2_to_f2(x0.x), f01 = bf2_to_f2(x0.y);
-            const float2 f80 = bf2_to_f2(x8.x), f81 = bf2_to_f2(x8.y);
-            big |= fabsf(f00.x) >= 65536.f || fabsf(f00.y) >= 65536.f || fabsf(f01.x) >= 65536.f ||
-                   fabsf(f01.y) >= 65536.f || fabsf(f80.x) >= 65536.f || fabsf(f80.y) >= 65536.f ||
-                   fabsf(f81.x) >= 65536.f || fabsf(f81.y) >= 65536.f;
-            qa[ks][0] = pack_f16x2(f00.x, f00.y);
-            qa[ks][1] = pack_f16x2(f80.x, f80.y);
-            qa[ks][2] = pack_f16x2(f01.x, f01.y);
-            qa[ks][3] = pack_f16x2(f81.x, f81.y);
-        }
+        // a query element outside f16's exact range is flagged
+        // (LSA_ERR_BOUNDS) and the request scores nothing
+        const bool big = wrelu_load_q(a.q + (int64_t)r * a.hq * 128, a.weights + (int64_t)r * a.hq, Q);
         if (big) flag_error(a.status, LSA_ERR_BOUNDS);
-        w_lo = a.weights[(int64_t)r * a.hq + 16 * mt + rr];
-        w_hi = a.weights[(int64_t)r * a.hq + 16 * mt + rr + 8];
-        if (__syncthreads_or(big ? 1 : 0)) {
-            // nothing is scored: the selections still run (on empty rows)
-            w_lo = w_hi = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) qa[ks][0] = qa[ks][1] = qa[ks][2] = qa[ks][3] = 0u;
-        }
+        if (__syncthreads_or(big ? 1 : 0)) wrelu_zero(Q);   // the selections still run (on empty rows)
     } else {
         // the group's query sum: thread (slice sl, 8-dim chunk c) adds heads
         // sl, sl + 32, ... of its chunk; the slices are then added in order
@@ -218,85 +171,17 @@ __global__ void __launch_bounds__(kCfThreads, 1) k_c2f_fine(FineArgs a)
         __syncthreads();
     }
     if constexpr (WRELU) {
-        // f_t = scale_t * sum_g w_g ReLU(q_g . e4m3(k8_t)) (scale_t >= 0):
-        // the dots of all heads as f16 m16n8k16 MMAs with fp32 accumulation
-        // (e4m3 values are exact in f16).  Warp w takes the 16 heads of
-        // M-tile w % 4 over a quarter of the tokens, 16 at a time.
-        const int th = warp >> 2;
-        const uint32_t kb = smem_addr(smem + LY::KEYS);
-        const int ng = (ntok + 15) / 16;
-        for (int gi = th; gi < ng; gi += 4) {
-            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-            const int t0 = gi * 16 + rr, t1 = t0 + 8;
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                uint32_t k0, k1;
-                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(k0) : "r"(kb + cf_key_off(t0, ks) + 4 * cc));
-                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(k1) : "r"(kb + cf_key_off(t1, ks) + 4 * cc));
-                const uint32_t b00 = e4m3x2_to_f16x2((uint16_t)(k0 & 0xffffu));
-                const uint32_t b01 = e4m3x2_to_f16x2((uint16_t)(k0 >> 16));
-                const uint32_t b10 = e4m3x2_to_f16x2((uint16_t)(k1 & 0xffffu));
-                const uint32_t b11 = e4m3x2_to_f16x2((uint16_t)(k1 >> 16));
-                asm volatile(
-                    "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-                    "{%0,%1,%2,%3};"
-                    : "+f"(s0[0]), "+f"(s0[1]), "+f"(s0[2]), "+f"(s0[3])
-                    : "r"(qa[ks][0]), "r"(qa[ks][1]), "r"(qa[ks][2]), "r"(qa[ks][3]), "r"(b00), "r"(b01));
-                asm volatile(
-                    "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-                    "{%0,%1,%2,%3};"
-                    : "+f"(s1[0]), "+f"(s1[1]), "+f"(s1[2]), "+f"(s1[3])
-                    : "r"(qa[ks][0]), "r"(qa[ks][1]), "r"(qa[ks][2]), "r"(qa[ks][3]), "r"(b10), "r"(b11));
-            }
-            // lane holds heads rr (s[0], s[1]) and rr + 8 (s[2], s[3]) of
-            // tokens 2cc, 2cc + 1 of each 8-token n-tile: weight, ReLU, then
-            // the sum over the 8 lanes sharing cc
-            float u0 = w_lo * fmaxf(s0[0], 0.f) + w_hi * fmaxf(s0[2], 0.f);
-            float u1 = w_lo * fmaxf(s0[1], 0.f) + w_hi * fmaxf(s0[3], 0.f);
-            float u2 = w_lo * fmaxf(s1[0], 0.f) + w_hi * fmaxf(s1[2], 0.f);
-            float u3 = w_lo * fmaxf(s1[1], 0.f) + w_hi * fmaxf(s1[3], 0.f);
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                u0 += __shfl_xor_sync(0xffffffffu, u0, off);
-                u1 += __shfl_xor_sync(0xffffffffu, u1, off);
-                u2 += __shfl_xor_sync(0xffffffffu, u2, off);
-                u3 += __shfl_xor_sync(0xffffffffu, u3, off);
-            }
-            if (rr == 0) {
-                s_part[mt * kCfTok + gi * 16 + 2 * cc] = u0;
-                s_part[mt * kCfTok + gi * 16 + 2 * cc + 1] = u1;
-                s_part[mt * kCfTok + gi * 16 + 8 + 2 * cc] = u2;
-                s_part[mt * kCfTok + gi * 16 + 8 + 2 * cc + 1] = u3;
-            }
-        }
+        wrelu_tile_partials(smem_addr(smem + LY::KEYS), ntok, Q, s_part);
         __syncthreads();
-        for (int t = tid; t < ntok; t += kCfThreads) {
-            const bool have = s_pg[t / b] >= 0;
-            s_fs[t] = have ? s_sc[t] * ((s_part[t] + s_part[kCfTok + t]) + (s_part[2 * kCfTok + t] + s_part[3 * kCfTok + t]))
-                           : -INFINITY;
-        }
+        for (int t = tid; t < ntok; t += kCfThreads)
+            s_fs[t] = s_pg[t / b] >= 0 ? s_sc[t] * wrelu_combine(s_part, t) : -INFINITY;
     } else {
-        // f_t = scale_t * q_sum . e4m3(k8_t): 8 lanes per token, 16 dims each
+        // 8 lanes per token, 16 dims each
         const int sub = lane & 7, tq = lane >> 3;
         for (int t0 = warp * 4; t0 < ntok; t0 += kCfWarps * 4) {
-            const int t = t0 + tq;
-            float acc = 0.f;
-            if (t < ntok) {
-                const uint4 kv = *reinterpret_cast<const uint4 *>(smem + LY::KEYS + cf_key_off(t, sub));
-                const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 lo = e4m3x2_to_f2((uint16_t)(w[e] & 0xffffu));
-                    const float2 hi = e4m3x2_to_f2((uint16_t)(w[e] >> 16));
-                    acc = fmaf(qs[4 * e + 0], lo.x, acc);
-                    acc = fmaf(qs[4 * e + 1], lo.y, acc);
-                    acc = fmaf(qs[4 * e + 2], hi.x, acc);
-                    acc = fmaf(qs[4 * e + 3], hi.y, acc);
-                }
-            }
-#pragma unroll
-            for (int off = 4; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            if (t < ntok && sub == 0) s_fs[t] = s_pg[t / b] >= 0 ? s_sc[t] * acc : -INFINITY;
+            const int t = min(t0 + tq, ntok - 1);
+            const float acc = headsum_dot(smem + LY::KEYS, t, qs);
+            if (t0 + tq < ntok && sub == 0) s_fs[t] = s_pg[t / b] >= 0 ? s_sc[t] * acc : -INFINITY;
         }
     }
     __syncthreads();

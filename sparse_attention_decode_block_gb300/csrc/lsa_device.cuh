@@ -226,6 +226,13 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t a, uint32_t v)
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ double ld_cluster_f64(uint32_t a)
+{
+    double v;
+    asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(a) : "memory");
+    return v;
+}
+
 // ---------------------------------------------------------------- smem / mbarrier
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
@@ -492,6 +499,13 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 // Makes this thread's generic-proxy writes to shared memory (st.shared,
 // cp.async) visible to the async proxy that tcgen05.mma reads through.
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Byte offset of 16-byte chunk j (0..7) of row t inside an atom column of
+// 8-row x 128-byte atoms with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t atom_offset(int t, int j)
+{
+    return (uint32_t)((t >> 3) * 1024 + (t & 7) * 128 + ((j ^ (t & 7)) << 4));
+}
 
 // Shared-memory matrix descriptor with the 128-byte swizzle: atoms of 8
 // rows x 128 bytes (1024-byte aligned), the 16-byte chunk index of each row

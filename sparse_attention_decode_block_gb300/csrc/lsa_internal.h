@@ -152,6 +152,32 @@ struct FineArgs {
     const float *weights;
 };
 
+// PQ32 coarse-to-fine (pq.cu): PQ32 codes of the index keys, their
+// coarse scores (LeanSparse Eq. 6 with the codebook centroids), the top-C
+// coarse candidates, the miss filter and the exact rescoring.
+struct PqArgs {
+    const uint16_t *q;          // [B, Hq, 128] bf16
+    const float *weights;       // [B, Hq] indexer head weights
+    CacheView ic;               // e4m3 index cache, one KV head, dk = 128
+    const uint8_t *codes;       // [num_pages, 1, b, 32]
+    const uint16_t *codebook;   // [32, 256, 4] bf16
+    const uint8_t *hit;         // [num_pages, 1, b] 1 = key cached, or NULL (all cached)
+    const int32_t *pt;
+    const int32_t *lens;
+    int32_t batch, hq, max_blocks, sink, recent;
+    int32_t ncand, tok_k;       // C coarse candidates, k final tokens
+    float *coarse;              // [B, max_blocks * b] coarse scores (-inf: not a candidate)
+    uint32_t *row_ext;          // [B][2] largest score key, complemented smallest (zero between calls)
+    uint32_t *hist;             // [B][kPqBins] bucket counts of the coarse scores (zero between calls)
+    int32_t *cand_out;          // [B, ncand] coarse candidates, ascending, -1 padded (or NULL)
+    int32_t *tok_idx;           // [B, tok_k] selected token positions, ascending, -1 padded
+    uint32_t *status;
+    long long spin_budget;
+    uint8_t *codes_out;         // encoding: [num_pages, 1, b, 32]
+};
+
+constexpr int kPqBins = 2048;
+
 struct AttnArgs {
     const uint16_t *q;          // [B, Hq, dk]
     CacheView c;
@@ -233,6 +259,10 @@ bool score_quest_supported(int dk, int hkv, int group);
 cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s, bool *unsupported);
 cudaError_t launch_fine_scores(const FineArgs &a, cudaStream_t s, bool *unsupported);
 bool c2f_fine_supported(const CacheView &iv, int hq, int max_blocks, int ncand, int tok_k, bool weighted);
+bool pq_supported(const CacheView &iv, int hq, int max_blocks, int ncand, int tok_k);
+cudaError_t launch_pq_encode(const PqArgs &a, cudaStream_t s);
+cudaError_t launch_pq_scores(const PqArgs &a, cudaStream_t s, bool *unsupported);
+cudaError_t launch_pq_select(const PqArgs &a, cudaStream_t s, bool *unsupported);
 cudaError_t launch_c2f_fine(const FineArgs &a, cudaStream_t s, bool *unsupported);
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t s, bool *unsupported);
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t s);

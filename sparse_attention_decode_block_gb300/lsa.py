@@ -34,7 +34,8 @@ LSA_SUMMARY_MINMAX = 1
 
 EXPORTED = ["lsa_status_string", "lsa_get_device_status", "lsa_build_summaries", "lsa_append_block",
             "lsa_build_minmax_summaries", "lsa_append_block_minmax",
-            "lsa_score", "lsa_topk", "lsa_topk_approx", "lsa_fine_topk", "lsa_sparse_decode_workspace_size",
+            "lsa_score", "lsa_topk", "lsa_topk_approx", "lsa_fine_topk", "lsa_pq_encode", "lsa_pq_scores",
+            "lsa_decode_step_launches", "lsa_sparse_decode_workspace_size",
             "lsa_sparse_decode", "lsa_decode_step_workspace_size", "lsa_decode_step",
             "lsa_sparse_decode_static_scratch"]
 
@@ -59,7 +60,8 @@ class lsa_params(C.Structure):
                 ("k_blocks", C.c_int32), ("sink_tokens", C.c_int32), ("recent_tokens", C.c_int32),
                 ("softmax_scale", C.c_float), ("c2f_candidates", C.c_int32), ("c2f_tokens", C.c_int32),
                 ("num_splits", C.c_int32), ("summary_kind", C.c_int32),
-                ("fine_head_weights", C.c_void_p)]
+                ("fine_head_weights", C.c_void_p), ("pq_candidates", C.c_int32),
+                ("pq_codes", C.c_void_p), ("pq_codebook", C.c_void_p), ("pq_hit", C.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -89,6 +91,9 @@ def load_library(path: Optional[str] = None):
             "lsa_score": ([V, cache_p, V, V, V, params_p, V, V], C.c_int),
             "lsa_topk": ([V, V, I, I, I, V, V], C.c_int),
             "lsa_topk_approx": ([V, V, I, I, I, C.c_uint64, V, V], C.c_int),
+            "lsa_pq_encode": ([cache_p, V, V, V, I, I, V, V], C.c_int),
+            "lsa_decode_step_launches": ([cache_p, cache_p, params_p], C.c_int32),
+            "lsa_pq_scores": ([V, cache_p, V, V, params_p, V, V], C.c_int),
             "lsa_fine_topk": ([V, cache_p, V, V, V, params_p, V, V, S, V], C.c_int),
             "lsa_sparse_decode_workspace_size": ([cache_p, params_p], S),
             "lsa_sparse_decode": ([V, cache_p, V, V, V, params_p, V, V, V, S, V], C.c_int),
@@ -155,12 +160,17 @@ def make_cache(k: torch.Tensor, v: Optional[torch.Tensor] = None, *, k_scale: Op
 
 def make_params(batch, num_q_heads, max_blocks, k_blocks=0, sink_tokens=0, recent_tokens=0,
                 softmax_scale=0.0, c2f_candidates=0, c2f_tokens=0, num_splits=0, summary_kind=0,
-                fine_head_weights: Optional[torch.Tensor] = None) -> lsa_params:
-    """fine_head_weights: device fp32 [batch, num_q_heads]; the caller keeps
-    the tensor alive while the parameters are in use."""
+                fine_head_weights: Optional[torch.Tensor] = None, pq_candidates=0,
+                pq_codes: Optional[torch.Tensor] = None, pq_codebook: Optional[torch.Tensor] = None,
+                pq_hit: Optional[torch.Tensor] = None) -> lsa_params:
+    """fine_head_weights: device fp32 [batch, num_q_heads]; pq_codes uint8
+    [num_pages, 1, b, 32], pq_codebook bf16 [32, 256, 4], pq_hit uint8
+    [num_pages, 1, b] (device).  The caller keeps the tensors alive while the
+    parameters are in use."""
     return lsa_params(int(batch), int(num_q_heads), int(max_blocks), int(k_blocks), int(sink_tokens),
                       int(recent_tokens), float(softmax_scale), int(c2f_candidates), int(c2f_tokens),
-                      int(num_splits), int(summary_kind), _ptr(fine_head_weights))
+                      int(num_splits), int(summary_kind), _ptr(fine_head_weights), int(pq_candidates),
+                      _ptr(pq_codes), _ptr(pq_codebook), _ptr(pq_hit))
 
 
 def lsa_get_device_status(clear: bool = True):
@@ -212,6 +222,22 @@ def lsa_topk_approx(scores, num_cols, k: int, seed: int, idx, stream=None):
     _check(load_library().lsa_topk_approx(_ptr(scores), _ptr(num_cols), rows, cols, int(k),
                                           int(seed) & (2**64 - 1), _ptr(idx), _stream(stream)),
            "lsa_topk_approx")
+
+
+def lsa_decode_step_launches(cache: lsa_cache, index_cache: Optional[lsa_cache], params: lsa_params) -> int:
+    return int(load_library().lsa_decode_step_launches(C.byref(cache), C.byref(index_cache) if index_cache else None,
+                                                       C.byref(params)))
+
+
+def lsa_pq_encode(index_cache: lsa_cache, codebook, page_table, seq_lens, codes, stream=None):
+    B, maxb = page_table.shape
+    _check(load_library().lsa_pq_encode(C.byref(index_cache), _ptr(codebook), _ptr(page_table), _ptr(seq_lens), B,
+                                        maxb, _ptr(codes), _stream(stream)), "lsa_pq_encode")
+
+
+def lsa_pq_scores(q, index_cache: lsa_cache, page_table, seq_lens, params: lsa_params, scores, stream=None):
+    _check(load_library().lsa_pq_scores(_ptr(q), C.byref(index_cache), _ptr(page_table), _ptr(seq_lens),
+                                        C.byref(params), _ptr(scores), _stream(stream)), "lsa_pq_scores")
 
 
 def lsa_fine_topk(q, index_cache: lsa_cache, page_table, seq_lens, cand, params: lsa_params, tok_idx,

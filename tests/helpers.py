@@ -107,7 +107,11 @@ class GpuStep:
         self.cache = L.make_cache(g["k_cache"], g["v_cache"])
         self.icache = None
         B, Hkv = w.batch, w.num_kv_heads
-        if w.c2f_candidates > 0:
+        if w.pq_candidates > 0:
+            self.icache = L.make_cache(g["idx_keys"], None, k_scale=g["idx_scale"])
+            self.summ = torch.zeros((1, 1, w.dk), dtype=torch.bfloat16, device=dev)   # not read
+            nsel = w.c2f_tokens
+        elif w.c2f_candidates > 0:
             self.icache = L.make_cache(g["idx_keys"], None, k_scale=g["idx_scale"])
             self.summ = torch.zeros((g["num_pages"], Hkv, w.dk), dtype=torch.bfloat16, device=dev)
             L.lsa_build_summaries(self.icache, g["page_table"], g["seq_lens"], self.summ)
@@ -122,7 +126,9 @@ class GpuStep:
             nsel = w.k_blocks
         self.params = L.make_params(B, w.num_q_heads, g["max_blocks"], w.k_blocks, w.sink, w.recent,
                                     w.softmax_scale, w.c2f_candidates, w.c2f_tokens, num_splits,
-                                    summary_kind=w.summary_kind, fine_head_weights=g.get("fine_weights"))
+                                    summary_kind=w.summary_kind, fine_head_weights=g.get("fine_weights"),
+                                    pq_candidates=w.pq_candidates, pq_codes=g.get("pq_codes"),
+                                    pq_codebook=g.get("pq_codebook"), pq_hit=g.get("pq_hit"))
         ws = L.lsa_decode_step_workspace_size(self.cache, self.params)
         assert ws > 0 or w.batch == 0 or True
         self.ws = torch.zeros(max(ws, 16), dtype=torch.uint8, device=dev)

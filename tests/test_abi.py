@@ -44,7 +44,8 @@ def test_every_declared_symbol_is_exported(lib):
 def test_struct_layouts_match_header():
     # lsa_cache: 2 pointers, 6 int64 strides, 6 int32, 1 pointer, 2 int64
     assert C.sizeof(L.lsa_cache) == 8 * 2 + 8 * 6 + 4 * 6 + 8 + 8 * 2
-    assert C.sizeof(L.lsa_params) == 4 * 12 + 8   # 11 int32 / float fields, padding, one pointer
+    # 11 int32 / float fields, padding, a pointer, an int32, padding, 3 pointers
+    assert C.sizeof(L.lsa_params) == 4 * 12 + 8 + 8 + 8 * 3
 
 
 def test_status_strings(lib):

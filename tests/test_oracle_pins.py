@@ -1022,3 +1022,31 @@ def test_pq_decode_attends_its_selection():
                                 num_q_heads=w.num_q_heads, sink=w.sink, recent=w.recent, scale=w.softmax_scale,
                                 token_mode=True)
     assert np.array_equal(a["out"], d["out"])
+
+
+def test_token_scores_wrelu_equal_the_block_fine_scores():
+    w, inp, ic = pq_setup()
+    blocks = np.array([2, 7])
+    f, t = oracle.fine_scores(inp["q"], ic, inp["page_table"], w.num_q_heads, 1, 0, blocks,
+                              fine_weights=inp["fine_weights"])
+    g = oracle.token_scores_wrelu(inp["q"], ic, inp["page_table"], w.num_q_heads, inp["fine_weights"], 1, 0, t[::-1])
+    assert np.array_equal(g, f[::-1])
+
+
+def test_attend_selection_token_rule():
+    """A token selection attends any token outside the forced ranges, the
+    partial last block's included (the PQ32 selection may keep that tail),
+    and skips a token inside a forced range (it is attended as forced)."""
+    w, inp, ic = pq_setup(seq_lens=(64 * 5 + 20, 64 * 3), recent=8)
+    c = oracle.Cache(inp["k_cache"], inp["v_cache"])
+    L0 = 64 * 5 + 20
+    rs = L0 - 8
+    sel = np.full((2, 1, 4), -1, dtype=np.int32)
+    sel[0, 0, :3] = [7, 64 * 5 + 3, rs + 1]        # a full-block token, a tail token, a forced one
+    a = oracle.attend_selection(inp["q"], c, inp["page_table"], inp["seq_lens"], sel, num_q_heads=w.num_q_heads,
+                                sink=0, recent=8, scale=w.softmax_scale, token_mode=True)
+    toks = [7, 64 * 5 + 3] + list(range(rs, L0))
+    qd = f64(bf16_bits(inp["q"][0, 5]))
+    o, lse = oracle.attend_tokens(qd, c, inp["page_table"][0], toks, 0, w.softmax_scale)
+    assert a["lse"][0, 5] == pytest.approx(lse, rel=1e-14)
+    assert np.array_equal(a["out"][0, 5], np.array([oracle.bf16_round(x) for x in o], dtype=np.uint16))
