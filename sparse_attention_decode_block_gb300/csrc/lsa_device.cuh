@@ -226,6 +226,11 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t a, uint32_t v)
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ void red_cluster_add_u32(uint32_t a, uint32_t v)
+{
+    asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ double ld_cluster_f64(uint32_t a)
 {
     double v;

@@ -106,32 +106,43 @@ __global__ void __launch_bounds__(kPeThreads) k_pq_encode(PqArgs a)
 
 // ---------------------------------------------------------------- coarse scores
 
-constexpr int kPsThreads = 128;   // four warps: warp w reads TMEM lane quadrant w
-constexpr int kPsTok = 128;       // tokens per tile (the MMA's M)
-constexpr int kPsHeads = 64;      // query heads (the MMA's N)
+// One CTA per SM, two roles: warps 4-7 produce (load the codes of a tile's
+// 128 tokens, a tile ahead, and decode them into a free key buffer), warps
+// 0-3 consume (thread 0 issues the tile's product, the four warps read its
+// accumulator, one TMEM lane quadrant each, and apply the weighted ReLU).
+// Key tiles and accumulators are double-buffered: the product of tile i+1
+// runs while tile i's scores are read and tile i+2 is decoded.  full[b]
+// (128 producer arrivals) says key buffer b holds a decoded tile; mma[b]
+// (the product's commit) says the product of buffer b is done, so that
+// the buffer may be decoded into again and its accumulator read.
+constexpr int kPsConsumers = 128;   // warps 0-3
+constexpr int kPsThreads = 256;     // and warps 4-7, the producers
+constexpr int kPsTok = 128;         // tokens per tile (the MMA's M)
+constexpr int kPsHeads = 64;        // query heads (the MMA's N)
 
 struct PsLayout {
     static constexpr int CB = 0;                          // codebook, bf16 [32][256][4]
-    static constexpr int COL = (kPsTok / 8) * 1024;       // one 64-dim atom column of the key tile
+    static constexpr int COL = (kPsTok / 8) * 1024;       // one 64-dim atom column of a key tile
     static constexpr int QCOL = (kPsHeads / 8) * 1024;    // one atom column of the query tile
-    static constexpr int KS = 32 * 256 * 8;               // key tile: 2 atom columns
-    static constexpr int QS = KS + 2 * COL;               // query tile: 2 atom columns
+    static constexpr int KS = 32 * 256 * 8;               // key tiles: 2 buffers x 2 atom columns
+    static constexpr int QS = KS + 4 * COL;               // query tile: 2 atom columns
     static constexpr int W = QS + 2 * QCOL;               // [64] fp32 head weights
-    static constexpr int BAR = W + kPsHeads * 4;          // mbarrier, TMEM base address
-    static constexpr int SMEM = BAR + 16;
-    static constexpr int TCOLS = 64;
+    static constexpr int VAL = W + kPsHeads * 4;          // [2][128] token of each key row (-1: not scored)
+    static constexpr int BAR = VAL + 2 * kPsTok * 4;      // full[2], mma[2], TMEM base address
+    static constexpr int SMEM = BAR + 48;
+    static constexpr int TCOLS = 128;                     // two accumulators of 64 columns
     static_assert(KS % 1024 == 0 && QS % 1024 == 0, "swizzled atoms are 1024-byte aligned");
+    static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
 };
 
-// Whether block j of a request of L tokens is a candidate: full and outside
-// the forced sink [0, se) and recent [rs, L) ranges.
+// Whether block j of a request is a candidate: full and outside the forced
+// sink [0, se) and recent [rs, L) ranges.
 __device__ __forceinline__ bool pq_block_candidate(int64_t j, int b, int64_t se, int64_t rs)
 {
     return j * b >= se && (j + 1) * b <= rs;
 }
 
-// Adds this CTA's extremes of request r's scores to the row's (warp
-// reduction, then one atomic per warp).
+// Adds a warp's extremes of request r's scores to the row's.
 __device__ __forceinline__ void pq_flush_ext(uint32_t *row_ext, int r, uint32_t kmax, uint32_t kmin)
 {
     kmax = __reduce_max_sync(0xffffffffu, kmax);
@@ -140,6 +151,25 @@ __device__ __forceinline__ void pq_flush_ext(uint32_t *row_ext, int r, uint32_t 
         atomicMax(row_ext + 2 * r, kmax);
         atomicMax(row_ext + 2 * r + 1, ~kmin);
     }
+}
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Barrier over the consumer warps that returns whether `ok` holds in all
+// of them (a wait that gave up in one thread ends the loop in every one, so
+// no consumer is left at a barrier the others never reach).
+__device__ __forceinline__ bool consumer_all(bool ok)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(ok ? 1u : 0u)
+        : "memory");
+    return r != 0;
 }
 
 __global__ void __launch_bounds__(kPsThreads, 1) k_pq_scores(PqArgs a)
@@ -153,130 +183,207 @@ __global__ void __launch_bounds__(kPsThreads, 1) k_pq_scores(PqArgs a)
         if (tid == 0) flag_error(a.status, LSA_ERR_INVALID_ARG);
         return;
     }
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + LY::BAR);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + LY::BAR + 8);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + LY::BAR);
+    uint64_t *mma = full + 2;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + LY::BAR + 32);
     const float *w_s = reinterpret_cast<const float *>(smem + LY::W);
+    int *vtok = reinterpret_cast<int *>(smem + LY::VAL);
     const uint32_t sbase = smem_addr(smem);
     if (warp == 0) {
         tmem_alloc(tslot, LY::TCOLS);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(bar, 1);
+        mbar_init(&full[0], 128);
+        mbar_init(&full[1], 128);
+        mbar_init(&mma[0], 1);
+        mbar_init(&mma[1], 1);
         fence_barrier_init();
     }
     // the codebook, once per CTA
     for (int i = tid; i < 32 * 256 * 8 / 16; i += kPsThreads)
         cp_async16(sbase + LY::CB + i * 16, reinterpret_cast<const uint8_t *>(a.codebook) + i * 16);
     cp_async_commit();
+    cp_async_wait<0>();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
 
     const int b = a.ic.b;
     const int T = a.max_blocks * b;
     const int tpr = (T + kPsTok - 1) / kPsTok;
     const int total = a.batch * tpr;
-    int cur = -1;
-    uint32_t kmax = 0u, kmin = 0xffffffffu;
-    uint32_t phase = 0;
+    const int ntiles = (int)blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    auto tile_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-        const int r = tile / tpr;
-        const int i0 = (tile - r * tpr) * kPsTok;
-        if (r != cur) {
-            if (cur >= 0) pq_flush_ext(a.row_ext, cur, kmax, kmin);
-            kmax = 0u;
-            kmin = 0xffffffffu;
-            // the request's 64 query rows and head weights (the previous
-            // tile's product, the last reader of the query tile, is done)
+
+    if (warp >= 4) {
+        // ---------------- producers: thread p decodes key row p
+        const int p = tid - kPsConsumers;
+        // this thread's token of tile i, whether it is scored, its codes
+        auto fetch = [&](int i, int &tok, uint4 &c0, uint4 &c1) -> bool {
+            const int tile = tile_of(i);
+            const int r = tile / tpr;
+            tok = (tile - r * tpr) * kPsTok + p;
+            const int L = a.lens[r];
+            const bool len_ok = L >= 0 && (int64_t)L <= (int64_t)T;
+            if (!len_ok && p == 0 && tok == 0) flag_error(a.status, LSA_ERR_BOUNDS);
+            const int64_t se = len_ok ? min(a.sink, L) : 0;
+            const int64_t rs = len_ok ? max((int64_t)L - a.recent, se) : 0;
+            const int nfull_tok = len_ok ? (L / b) * b : 0;
+            if (!(tok < nfull_tok && pq_block_candidate(tok / b, b, se, rs))) return false;
+            const int pg = a.pt[(int64_t)r * a.max_blocks + tok / b];
+            if (pg < 0 || pg >= a.ic.num_pages) {
+                flag_error(a.status, LSA_ERR_BOUNDS);
+                return false;
+            }
+            const uint4 *cp = reinterpret_cast<const uint4 *>(a.codes + ((int64_t)pg * b + tok % b) * 32);
+            c0 = cp[0];
+            c1 = cp[1];
+            return true;
+        };
+        int tok = 0, tok_n = 0;
+        uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0, n0 = c0, n1 = c0;
+        bool v = ntiles > 0 && fetch(0, tok, c0, c1);
+        for (int i = 0; i < ntiles && ok; ++i) {
+            // the next tile's codes load while this one decodes
+            const bool vn = i + 1 < ntiles && fetch(i + 1, tok_n, n0, n1);
+            const int buf = i & 1;
+            if (i >= 2) {
+                // buffer b's previous product (tile i - 2) is done
+                ok = mbar_wait(&mma[buf], ((i - 2) >> 1) & 1, a.status, a.spin_budget);
+                if (!ok) break;
+            }
+            if (v) {
+                const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                uint8_t *kt = smem + LY::KS + buf * 2 * LY::COL;
+#pragma unroll
+                for (int jj = 0; jj < 32; jj += 2) {
+                    const uint32_t ca = (cw[jj >> 2] >> (8 * (jj & 3))) & 0xffu;
+                    const uint32_t cb = (cw[(jj + 1) >> 2] >> (8 * ((jj + 1) & 3))) & 0xffu;
+                    const uint2 ea = *reinterpret_cast<const uint2 *>(smem + LY::CB + (jj * 256 + ca) * 8);
+                    const uint2 eb = *reinterpret_cast<const uint2 *>(smem + LY::CB + ((jj + 1) * 256 + cb) * 8);
+                    *reinterpret_cast<uint4 *>(kt + (jj >> 4) * LY::COL + atom_offset(p, (jj & 15) >> 1)) =
+                        make_uint4(ea.x, ea.y, eb.x, eb.y);
+                }
+            }
+            vtok[buf * kPsTok + p] = v ? tok : -1;
+            fence_proxy_async_smem();
+            mbar_arrive(&full[buf]);
+            v = vn;
+            tok = tok_n;
+            c0 = n0;
+            c1 = n1;
+        }
+    } else {
+        // ---------------- consumers: warp w reads TMEM lane quadrant w
+        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        int cur = -1;
+        uint32_t kmax = 0u, kmin = 0xffffffffu;
+        // the query tile and head weights of request r (every product that
+        // reads the previous ones is done when this is called)
+        auto load_q = [&](int r) {
             const uint8_t *qg = reinterpret_cast<const uint8_t *>(a.q + (int64_t)r * a.hq * 128);
             const int j = tid & 7;
-            for (int task = tid >> 3; task < 2 * kPsHeads; task += kPsThreads / 8) {
+            for (int task = tid >> 3; task < 2 * kPsHeads; task += kPsConsumers / 8) {
                 const int cc = task >> 6, g = task & (kPsHeads - 1);
                 cp_async16(sbase + LY::QS + cc * LY::QCOL + atom_offset(g, j), qg + (int64_t)g * 256 + cc * 128 + j * 16);
             }
             cp_async_commit();
             if (tid < kPsHeads) reinterpret_cast<float *>(smem + LY::W)[tid] = a.weights[(int64_t)r * a.hq + tid];
-            cur = r;
-        }
-        const int L = a.lens[r];
-        const bool len_ok = L >= 0 && (int64_t)L <= (int64_t)T;
-        if (!len_ok && tid == 0 && i0 == 0) flag_error(a.status, LSA_ERR_BOUNDS);
-        const int64_t se = len_ok ? min(a.sink, L) : 0;
-        const int64_t rs = len_ok ? max((int64_t)L - a.recent, se) : 0;
-        const int nfull_tok = len_ok ? (L / b) * b : 0;
-        // ---- this thread's token: its codes, decoded into key-tile row tid
-        const int tok = i0 + tid;
-        bool valid = tok < nfull_tok && pq_block_candidate(tok / b, b, se, rs);
-        if (valid) {
-            const int p = a.pt[(int64_t)r * a.max_blocks + tok / b];
-            if (p < 0 || p >= a.ic.num_pages) {
-                flag_error(a.status, LSA_ERR_BOUNDS);
-                valid = false;
-            } else {
-                const uint4 *cp = reinterpret_cast<const uint4 *>(a.codes + ((int64_t)p * b + tok % b) * 32);
-                const uint4 c0 = cp[0], c1 = cp[1];
-                const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const uint32_t code = (cw[jj >> 2] >> (8 * (jj & 3))) & 0xffu;
-                    const uint2 cent = *reinterpret_cast<const uint2 *>(smem + LY::CB + (jj * 256 + code) * 8);
-                    *reinterpret_cast<uint2 *>(smem + LY::KS + (jj >> 4) * LY::COL + atom_offset(tid, (jj & 15) >> 1) +
-                                               (jj & 1) * 8) = cent;
-                }
-            }
-        }
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        tc_fence_before();
-        const bool any = __syncthreads_or(valid ? 1 : 0) != 0;
-        float sc = -INFINITY;
-        if (any) {
+            cp_async_wait<0>();
+            fence_proxy_async_smem();
+            consumer_sync();
+        };
+        // product of tile i into accumulator i & 1, once its keys are in;
+        // each thread takes its key row's token first (the producers write
+        // the next tile's over it once this product is done)
+        int issued[2] = {-1, -1};
+        int tok_of[2] = {-1, -1};
+        auto issue = [&](int i) -> bool {
+            const int buf = i & 1;
+            if (!consumer_all(mbar_wait(&full[buf], (i >> 1) & 1, a.status, a.spin_budget))) return false;
+            tok_of[buf] = vtok[buf * kPsTok + tid];
+            consumer_sync();
+            tc_fence_after();
+            issued[buf] = i;
             if (tid == 0) {
-                tc_fence_after();
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
-                        const uint64_t ad = umma_desc_sw128(sbase + LY::KS + cc * LY::COL + s * 32, 16, 1024);
+                        const uint64_t ad =
+                            umma_desc_sw128(sbase + LY::KS + (2 * buf + cc) * LY::COL + s * 32, 16, 1024);
                         const uint64_t bd = umma_desc_sw128(sbase + LY::QS + cc * LY::QCOL + s * 32, 16, 1024);
-                        umma_bf16(tmem, ad, bd, IDESC, cc > 0 || s > 0);
+                        umma_bf16(tmem + 64 * buf, ad, bd, IDESC, cc > 0 || s > 0);
                     }
                 }
-                umma_commit(bar);
+                umma_commit(&mma[buf]);
             }
-            ok = mbar_wait(bar, phase, a.status, a.spin_budget);
-            ok = __syncthreads_and(ok) != 0;
-            phase ^= 1u;
+            return true;
+        };
+        if (ntiles > 0) {
+            cur = tile_of(0) / tpr;
+            load_q(cur);
+            ok = issue(0);
+        }
+        for (int i = 0; i < ntiles && ok; ++i) {
+            const int buf = i & 1;
+            const int r = tile_of(i) / tpr;
+            // the next tile's product: the request's query tile stays until
+            // this tile's product is done
+            if (i + 1 < ntiles) {
+                const int rn = tile_of(i + 1) / tpr;
+                if (rn != r) {
+                    ok = consumer_all(mbar_wait(&mma[buf], (i >> 1) & 1, a.status, a.spin_budget));
+                    if (!ok) break;
+                    load_q(rn);
+                }
+                tc_fence_before();
+                consumer_sync();   // accumulator (i + 1) & 1 was read (tile i - 1) before it is written
+                ok = issue(i + 1);
+                if (!ok) break;
+            }
+            ok = consumer_all(mbar_wait(&mma[buf], (i >> 1) & 1, a.status, a.spin_budget));
             if (!ok) break;
             tc_fence_after();
+            // ---- this thread's token: the weighted ReLU of its 64 dots
+            const int tok = tok_of[buf];
             float d[32];
             float s = 0.f;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                tmem_ld32(tmem + lane_base + 32 * half, d);
+                tmem_ld32(tmem + lane_base + 64 * buf + 32 * half, d);
 #pragma unroll
                 for (int g = 0; g < 32; ++g) s = fmaf(w_s[32 * half + g], fmaxf(d[g], 0.f), s);
             }
+            if (r != cur) {
+                pq_flush_ext(a.row_ext, cur, kmax, kmin);
+                kmax = 0u;
+                kmin = 0xffffffffu;
+                cur = r;
+            }
+            const bool valid = tok >= 0;
             if (valid) {
-                sc = s;
-                const uint32_t key = isnan(s) ? 0u : float_to_key(s);
                 if (isnan(s)) flag_error(a.status, LSA_ERR_NAN);
                 else {
+                    const uint32_t key = float_to_key(s);
                     kmax = max(kmax, key);
                     kmin = min(kmin, key);
                 }
             }
+            const int tok_row = (tile_of(i) - r * tpr) * kPsTok + tid;
+            if (tok_row < T) a.coarse[(int64_t)r * T + tok_row] = valid && !isnan(s) ? s : -INFINITY;
         }
-        if (tok < T) a.coarse[(int64_t)r * T + tok] = valid && !isnan(sc) ? sc : -INFINITY;
-        tc_fence_before();
-        __syncthreads();   // the tensor memory is read and the tiles are free
+        if (cur >= 0) pq_flush_ext(a.row_ext, cur, kmax, kmin);
+        if (!ok) {
+            // a wait gave up: wait (bounded) for the products issued before
+            // the tensor memory is freed
+            for (int bb = 0; bb < 2; ++bb)
+                if (issued[bb] >= 0) mbar_wait(&mma[bb], (issued[bb] >> 1) & 1, nullptr, a.spin_budget);
+        }
     }
-    if (cur >= 0) pq_flush_ext(a.row_ext, cur, kmax, kmin);
-    if (!ok) mbar_wait(bar, phase ^ 1u, nullptr, a.spin_budget);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, LY::TCOLS);
@@ -317,11 +424,24 @@ __global__ void __launch_bounds__(kPhThreads) k_pq_hist(PqArgs a)
     float vmin, scale;
     pq_remap(a.row_ext, r, &vmin, &scale);
     __syncthreads();
-    const float *row = a.coarse + (int64_t)r * T;
-    for (int i = t0 + threadIdx.x; i < t1; i += kPhThreads) {
-        const float x = __ldcg(row + i);
-        if (x == -INFINITY || isnan(x)) continue;
-        atomicAdd(&h[pq_bucket(key_to_float(float_to_key(x)), vmin, scale)], 1u);
+    // this thread's chunks of four scores, all loads in flight at once (T
+    // and t0 are multiples of four: block sizes are multiples of 16)
+    const float4 *row4 = reinterpret_cast<const float4 *>(a.coarse + (int64_t)r * T);
+    constexpr int kPer = kPhTok / 4 / kPhThreads;
+    float4 v[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int i4 = t0 / 4 + threadIdx.x + u * kPhThreads;
+        v[u] = 4 * i4 < t1 ? __ldcg(row4 + i4) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const float xs[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (xs[e] == -INFINITY || isnan(xs[e])) continue;
+            atomicAdd(&h[pq_bucket(key_to_float(float_to_key(xs[e])), vmin, scale)], 1u);
+        }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < kPqBins; i += kPhThreads)
@@ -350,6 +470,13 @@ struct PqSelLayout {
     static constexpr int SMEM = DX + (2 + kFtWarps) * 8;
 };
 static_assert(PqSelLayout::SMEM + sizeof(ClusterTopkScratch<kFtThreads, 8>) <= 227 * 1024, "shared memory");
+
+// The coarse scores each CTA of a request's cluster reads: ceil(T / CS)
+// rounded up to whole chunks of four tokens for every thread.
+__host__ __device__ __forceinline__ int pq_slice(int T, int cs)
+{
+    return ((T + cs - 1) / cs + 4 * kFtThreads - 1) / (4 * kFtThreads) * (4 * kFtThreads);
+}
 
 // Sum over the CTA of every thread's fp64 value, in a fixed order (lanes,
 // then warps), returned to every thread.  ws: kFtWarps doubles.
@@ -432,10 +559,31 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
     pdl_wait();
     pdl_launch_dependents();
 
-    // ---- A. the bucket of the C-th largest coarse score, from the row's counts
+    // ---- A. the CTA's slice of the coarse scores into shared memory (the
+    // key region, free until the rescoring): thread t's PT tokens as NCH
+    // 16-byte chunks, the chunk index XORed with t mod 8 when NCH allows,
+    // so that 8 threads reading their c-th chunks hit distinct banks
+    {
+        const int S = pq_slice(T, CS), NCH = S / NT / 4;
+        const uint32_t sk = smem_addr(smem + LY::KEYS);
+        const float *src = a.coarse + (int64_t)r * T + (int64_t)me * S;
+        const int valid_chunks = max(0, min(S, T - (int)me * S)) / 4;
+        for (int gch = tid; gch < S / 4; gch += NT) {
+            const int t = gch / NCH, c = gch - t * NCH;
+            const uint32_t sw = (NCH & 7) == 0 ? (uint32_t)(t & 7) : 0u;
+            const uint32_t dst = sk + (uint32_t)(((size_t)t * NCH + ((uint32_t)c ^ sw)) * 16);
+            if (gch < valid_chunks) cp_async16(dst, src + 4 * gch);
+            else
+                *reinterpret_cast<float4 *>(smem + (dst - sk) + LY::KEYS) =
+                    make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+        cp_async_commit();
+    }
+    // ---- the bucket of the C-th largest coarse score, from the row's counts
     for (int i = tid; i < kPqBins; i += NT) hist[i] = __ldcg(a.hist + (int64_t)r * kPqBins + i);
     float vmin, scale;
     pq_remap(a.row_ext, r, &vmin, &scale);
+    cp_async_wait<0>();
     __syncthreads();
     constexpr int BPT = kPqBins / NT;
     const int top = kPqBins - 1 - tid * BPT;
@@ -469,16 +617,18 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
     const int cnt1 = (int)s_u[2];
     const bool crowded = B1 >= 0 && cnt1 > kBkCap;
 
-    // ---- B. this thread's tokens of this CTA's slice
-    const int S = ((T + CS - 1) / CS + 4 * NT - 1) / (4 * NT) * (4 * NT);
-    const int PT = S / NT;
+    // ---- B. this thread's tokens of this CTA's slice, from shared memory
+    // (staged above; thread t owns PT consecutive tokens, NCH chunks of 4)
+    const int S = pq_slice(T, CS);
+    const int PT = S / NT, NCH = PT / 4;
     const int t_lo = min((int)me * S + tid * PT, T), t_hi = min(t_lo + PT, T);
-    const float *row = a.coarse + (int64_t)r * T;
-    auto key_at = [&](int i) -> uint32_t {
-        const float x = __ldcg(row + i);
-        return (x == -INFINITY || isnan(x)) ? 0u : float_to_key(x);
+    const uint32_t swz = (NCH & 7) == 0 ? (uint32_t)(tid & 7) : 0u;
+    auto chunk_at = [&](int c) -> float4 {
+        return *reinterpret_cast<const float4 *>(smem + LY::KEYS + ((size_t)tid * NCH + ((uint32_t)c ^ swz)) * 16);
     };
+    auto key_of = [](float x) -> uint32_t { return (x == -INFINITY || isnan(x)) ? 0u : float_to_key(x); };
     auto bucket_of = [&](uint32_t k) -> int { return pq_bucket(key_to_float(k), vmin, scale); };
+    const int nch = (t_hi - t_lo + 3) / 4;   // this thread's chunks inside the row
 
     // the candidate rule, exact in both cases: by bucket (winners above the
     // boundary bucket, the boundary bucket's keys ranked), or, with a
@@ -488,12 +638,17 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
     int take_eq = 0;
     uint32_t n_a = 0, n_b = 0;   // this thread's winners / boundary keys (or > Tk / == Tk)
     if (!crowded) {
-        for (int i = t_lo; i < t_hi; ++i) {
-            const uint32_t k = key_at(i);
-            if (k == 0u) continue;
-            const int bk = bucket_of(k);
-            n_a += bk > B1;
-            n_b += bk == B1;
+        for (int c = 0; c < nch; ++c) {
+            const float4 v = chunk_at(c);
+            const float xs[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t k = key_of(xs[e]);
+                if (k == 0u) continue;
+                const int bk = bucket_of(k);
+                n_a += bk > B1;
+                n_b += bk == B1;
+            }
         }
     } else {
         // the threshold by bisection over the key space, counts summed over
@@ -503,10 +658,13 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
         while (hi - lo > 1) {
             const uint32_t mid = (uint32_t)(lo + ((hi - lo) >> 1));
             uint32_t c = 0;
-            for (int i = t_lo; i < t_hi; ++i) c += key_at(i) >= mid;
-            const uint32_t cc = bk_sum<NT>(c, tsm.red);
+            for (int cc = 0; cc < nch; ++cc) {
+                const float4 v = chunk_at(cc);
+                c += (key_of(v.x) >= mid) + (key_of(v.y) >= mid) + (key_of(v.z) >= mid) + (key_of(v.w) >= mid);
+            }
+            const uint32_t csum = bk_sum<NT>(c, tsm.red);
             const int slot = 3 + (it & 1);
-            if (tid == 0) tsm.xch[slot][0] = cc;
+            if (tid == 0) tsm.xch[slot][0] = csum;
             cluster_sync();
             const int cs = (int)cl_gather_sum<NT, CS>(tsm, slot, 0, nullptr);
             if (cs >= keff1) lo = mid;
@@ -515,10 +673,15 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
             if (cs == keff1) break;
         }
         Tk = (uint32_t)lo;
-        for (int i = t_lo; i < t_hi; ++i) {
-            const uint32_t k = key_at(i);
-            n_a += k > Tk;
-            n_b += k != 0u && k == Tk;
+        for (int c = 0; c < nch; ++c) {
+            const float4 v = chunk_at(c);
+            const float xs[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t k = key_of(xs[e]);
+                n_a += k > Tk;
+                n_b += k != 0u && k == Tk;
+            }
         }
     }
     // per-CTA totals, in thread order
@@ -529,12 +692,17 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
     if (!crowded && B1 >= 0 && n_b > 0) {
         // this CTA's boundary keys, in token order
         uint32_t pos = b_base;
-        for (int i = t_lo; i < t_hi; ++i) {
-            const uint32_t k = key_at(i);
-            if (k != 0u && bucket_of(k) == B1) {
-                tsm.ck[pos] = k;
-                ckt[pos] = i;
-                ++pos;
+        for (int c = 0; c < nch; ++c) {
+            const float4 v = chunk_at(c);
+            const float xs[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t k = key_of(xs[e]);
+                if (k != 0u && bucket_of(k) == B1) {
+                    tsm.ck[pos] = k;
+                    ckt[pos] = t_lo + 4 * c + e;
+                    ++pos;
+                }
             }
         }
     }
@@ -645,30 +813,36 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
         __syncthreads();
         uint32_t pos = cbase + bk_scan<NT>(mine, tsm.red, &dummy);
         int32_t *cout = a.cand_out ? a.cand_out + (int64_t)r * C : nullptr;
-        for (int i = t_lo; i < t_hi && (n_a + n_b) > 0; ++i) {
-            const uint32_t k = key_at(i);
-            if (k == 0u) continue;
-            bool take;
-            if (crowded) {
-                if (k > Tk) take = true;
-                else if (k == Tk) {
-                    take = (int)bpos < take_eq;
-                    ++bpos;
-                } else take = false;
-            } else {
-                const int bk = bucket_of(k);
-                if (bk > B1) take = true;
-                else if (bk == B1) {
-                    take = tsm.pick[bpos] != 0;
-                    ++bpos;
-                } else take = false;
+        for (int c = 0; c < nch && (n_a + n_b) > 0; ++c) {
+            const float4 v = chunk_at(c);
+            const float xs[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t k = key_of(xs[e]);
+                if (k == 0u) continue;
+                bool take;
+                if (crowded) {
+                    if (k > Tk) take = true;
+                    else if (k == Tk) {
+                        take = (int)bpos < take_eq;
+                        ++bpos;
+                    } else take = false;
+                } else {
+                    const int bk = bucket_of(k);
+                    if (bk > B1) take = true;
+                    else if (bk == B1) {
+                        take = tsm.pick[bpos] != 0;
+                        ++bpos;
+                    } else take = false;
+                }
+                if (!take) continue;
+                const int i = t_lo + 4 * c + e;
+                const int owner = (int)pos / CB, slot = (int)pos - owner * CB;
+                st_cluster_u32(cluster_map(smem_addr(&ctok[slot]), (uint32_t)owner), (uint32_t)i);
+                st_cluster_u32(cluster_map(smem_addr(&csc[slot]), (uint32_t)owner), __float_as_uint(key_to_float(k)));
+                if (cout) cout[pos] = i;
+                ++pos;
             }
-            if (!take) continue;
-            const int owner = (int)pos / CB, slot = (int)pos - owner * CB;
-            st_cluster_u32(cluster_map(smem_addr(&ctok[slot]), (uint32_t)owner), (uint32_t)i);
-            st_cluster_u32(cluster_map(smem_addr(&csc[slot]), (uint32_t)owner), __float_as_uint(key_to_float(k)));
-            if (cout) cout[pos] = i;
-            ++pos;
         }
         if (cout && me == 0)
             for (int i = keff1 + tid; i < C; i += NT) cout[i] = -1;
@@ -852,7 +1026,10 @@ bool pq_supported(const CacheView &iv, int hq, int max_blocks, int ncand, int to
     const int cs = pq_cluster_size();
     if (cs == 0) return false;
     const int cb = (ncand + cs - 1) / cs;
-    return cb + iv.b <= kFtTok && tok_k <= cs * kFtTok && (int64_t)max_blocks * iv.b <= (1 << 26);
+    // a CTA's slice of the coarse scores fits the key region (128 KB)
+    return cb + iv.b <= kFtTok && tok_k <= cs * kFtTok && iv.b % 4 == 0 &&
+           (int64_t)max_blocks * iv.b <= (int64_t)cs * kFtTok * 32 &&
+           pq_slice(max_blocks * iv.b, cs) * 4 <= kFtTok * 128;
 }
 
 cudaError_t launch_pq_encode(const PqArgs &a, cudaStream_t s)
@@ -874,7 +1051,7 @@ cudaError_t launch_pq_scores(const PqArgs &a, cudaStream_t s, bool *unsupported)
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t tiles = (int64_t)a.batch * ((a.max_blocks * a.ic.b + kPsTok - 1) / kPsTok);
-    const int grid = (int)std::min<int64_t>(tiles, 2LL * sms);
+    const int grid = (int)std::min<int64_t>(tiles, (int64_t)sms);
     e = launch_step_kernel(k_pq_scores, dim3(grid), dim3(kPsThreads), (size_t)PsLayout::SMEM, s, a);
     if (e != cudaSuccess) return e;
     if (!a.hist) return cudaGetLastError();   // scores only

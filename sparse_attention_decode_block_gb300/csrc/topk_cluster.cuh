@@ -10,11 +10,14 @@
 // each other's memory as they can:
 //   - per-CTA scalars (counts, smallest and largest key) are read by one
 //     warp, one lane per CTA;
-//   - the bucket counts are reduce-scattered: CTA c sums bucket slice c
-//     over the cluster, and every CTA then reads the slice totals and the
-//     one slice that holds the boundary;
+//   - the bucket counts are summed by remote atomic adds into the CTA that
+//     owns each slice of the buckets, and every CTA then reads all the sums
+//     (one 16-byte load a thread) and finds the boundary itself;
 //   - the boundary bucket's keys stay where they are counted; each CTA
-//     gathers the cluster's list (at most kBkCap keys) to rank its own.
+//     gathers the cluster's list (at most kBkCap keys), ranks all of it, and
+//     so knows every CTA's output count without another exchange.
+// Four cluster barriers in the common case: extremes, counts, boundary
+// lists, and the last one before any CTA may leave.
 // No CTA waits on a flag; the barriers are the hardware's, and the
 // cluster's CTAs are co-scheduled by construction.  The APPROX variant
 // samples the boundary bucket instead (the stochastic early exit of
@@ -38,7 +41,8 @@ struct ClusterTopkScratch {
     uint32_t red[NT / 32][3];
     __align__(16) uint32_t xch[8][4];         // this CTA's values of each exchange
     uint32_t off[CS + 1];                     // per-CTA offsets of the current exchange
-    uint32_t bc[4];                           // boundary bucket, keys above it, keys in it
+    uint32_t bc[4];                           // the cluster's candidate count, extremes, this CTA's offset
+    uint32_t bucket, gt, cnt, pad;            // boundary bucket, keys above it, keys in it
 };
 
 // Sum over the cluster of word w of exchange slot s (written before the
@@ -89,11 +93,15 @@ __device__ int cluster_bucket_topk(const uint32_t (&keys)[KPT], int k, int col0,
 {
     static_assert(KPT <= 64, "selection mask of 64 bits");
     constexpr int SL = ClusterTopkScratch<NT, CS>::SL;
-    static_assert(SL % 32 == 0 && NT % SL == 0 && CS % (NT / SL) == 0, "slice layout");
+    constexpr int BPT = kBkBins / NT;
+    static_assert(SL % 4 == 0 && BPT % 4 == 0 && SL % BPT == 0, "slice layout");
     const int tid = threadIdx.x, lane = tid & 31;
     const uint32_t me = cluster_rank();
 
-    // ---- candidates, smallest and largest key over the cluster
+    // ---- candidates, smallest and largest key over the cluster (the slice
+    // sums this CTA owns are cleared before the barrier that precedes every
+    // remote add to them)
+    for (int i = tid; i < SL; i += NT) sm.ssum[i] = 0u;
     uint32_t nv = 0, kmn = 0xffffffffu, kmx = 0u;
 #pragma unroll
     for (int e = 0; e < KPT; ++e) {
@@ -109,21 +117,29 @@ __device__ int cluster_bucket_topk(const uint32_t (&keys)[KPT], int k, int col0,
         sm.xch[0][1] = loc.y;
         sm.xch[0][2] = loc.z;
     }
-    cluster_sync();
+    cluster_sync();   // (1)
     if (tid < 32) {
         uint4 x = make_uint4(0u, 0xffffffffu, 0u, 0u);
         if (lane < CS) x = ld_cluster_v4(cluster_map(smem_addr(&sm.xch[0][0]), (uint32_t)lane));
         const uint32_t n = __reduce_add_sync(0xffffffffu, x.x);
         const uint32_t mn = __reduce_min_sync(0xffffffffu, x.y);
         const uint32_t mx = __reduce_max_sync(0xffffffffu, x.z);
+        uint32_t incl = x.x;   // valid keys of the CTAs before each lane's
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const uint32_t below = __shfl_sync(0xffffffffu, incl - x.x, (int)me);
         if (lane == 0) {
             sm.bc[0] = n;
             sm.bc[1] = mn;
             sm.bc[2] = mx;
+            sm.bc[3] = below;
         }
     }
     __syncthreads();
-    const uint32_t nvalid = sm.bc[0], gmn = sm.bc[1], gmx = sm.bc[2];
+    const uint32_t nvalid = sm.bc[0], gmn = sm.bc[1], gmx = sm.bc[2], nv_below = sm.bc[3];
     const int keff = min(max(k, 0), (int)nvalid);
     if (keff == 0) {
         cluster_sync();
@@ -131,9 +147,12 @@ __device__ int cluster_bucket_topk(const uint32_t (&keys)[KPT], int k, int col0,
     }
 
     uint64_t sel = 0;
+    uint32_t base = 0;   // selected keys of the CTAs before this one
+    bool need_exchange = false;
     if (keff == (int)nvalid) {
 #pragma unroll
         for (int e = 0; e < KPT; ++e) sel |= (uint64_t)(keys[e] != 0u) << e;
+        base = nv_below;
     } else {
         const float vmin = key_to_float(gmn), vmax = key_to_float(gmx);
         const float span = vmax - vmin;
@@ -151,137 +170,107 @@ __device__ int cluster_bucket_topk(const uint32_t (&keys)[KPT], int k, int col0,
             }
             bk[e] = bb;
         }
-        __syncthreads();   // every thread has read bc before it is rewritten below
         for (int i = tid; i < kBkBins; i += NT) sm.hist[i] = 0u;
         __syncthreads();
 #pragma unroll
         for (int e = 0; e < KPT; ++e)
             if (bk[e] >= 0) atomicAdd(&sm.hist[bk[e]], 1u);
-        cluster_sync();   // every CTA's counts are complete
-        // reduce-scatter: this CTA sums slice `me` (buckets me*SL ..) over
-        // the cluster; thread (group g, bucket j) adds CS / NG ranks
-        {
-            constexpr int NG = NT / SL, RPG = CS / NG;
-            const int j = tid % SL, g = tid / SL;
-            const uint32_t a = smem_addr(&sm.hist[me * SL + j]);
-            uint32_t v[RPG];
-#pragma unroll
-            for (int i = 0; i < RPG; ++i) v[i] = ld_cluster_u32(cluster_map(a, (uint32_t)(g * RPG + i)));
-            uint32_t s = 0;
-#pragma unroll
-            for (int i = 0; i < RPG; ++i) s += v[i];
-            sm.part[g][j] = s;
-            __syncthreads();
-            uint32_t t = 0;
-            if (tid < SL) {
-#pragma unroll
-                for (int i = 0; i < NG; ++i) t += sm.part[i][tid];
-                sm.ssum[tid] = t;
-            }
-            const uint32_t tot = bk_sum<NT>(t, sm.red);
-            if (tid == 0) sm.xch[1][0] = tot;
+        __syncthreads();
+        // this CTA's counts into the owners' slice sums
+        for (int i = tid; i < kBkBins; i += NT) {
+            const uint32_t h = sm.hist[i];
+            if (h) red_cluster_add_u32(cluster_map(smem_addr(&sm.ssum[i % SL]), (uint32_t)(i / SL)), h);
         }
-        cluster_sync();   // every slice sum is complete
-        // every CTA finds the boundary: the slice that holds the keff-th
-        // largest key (slice totals, one lane per CTA), then the bucket
-        // within that slice (its SL sums, SL / 32 per lane)
-        if (tid < 32) {
-            const uint32_t tot =
-                lane < CS ? ld_cluster_u32(cluster_map(smem_addr(&sm.xch[1][0]), (uint32_t)lane)) : 0u;
-            // keys in this lane's slice and the ones above it
-            uint32_t suf = tot;
+        cluster_sync();   // (2) every slice sum is complete
+        // thread t reads the cluster's counts of its BPT buckets below
+        // kBkBins - t * BPT (16 bytes at a time) and an exclusive scan in
+        // thread order counts the keys in higher buckets
+        const int top = kBkBins - 1 - tid * BPT;
+        uint32_t cb[BPT];
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_down_sync(0xffffffffu, suf, o);
-                if (lane + o < 32) suf += y;
+        for (int q = 0; q < BPT / 4; ++q) {
+            const int lo = top - 4 * q - 3;   // 4 buckets lo .. lo + 3, one owner
+            const uint4 v = ld_cluster_v4(cluster_map(smem_addr(&sm.ssum[lo % SL]), (uint32_t)(lo / SL)));
+            cb[4 * q] = v.w;
+            cb[4 * q + 1] = v.z;
+            cb[4 * q + 2] = v.y;
+            cb[4 * q + 3] = v.x;
+        }
+        uint32_t cown = 0;
+#pragma unroll
+        for (int e = 0; e < BPT; ++e) cown += cb[e];
+        uint32_t tot = 0;
+        uint32_t g = bk_scan<NT>(cown, sm.red, &tot);
+#pragma unroll
+        for (int e = 0; e < BPT; ++e) {
+            if (g < (uint32_t)keff && (uint32_t)keff <= g + cb[e]) {
+                sm.bucket = (uint32_t)(top - e);
+                sm.gt = g;
+                sm.cnt = cb[e];
             }
-            const uint32_t above_s = suf - tot;
-            const unsigned hit =
-                __ballot_sync(0xffffffffu, lane < CS && above_s < (uint32_t)keff && (uint32_t)keff <= suf);
-            // exactly one slice holds it; were none found, no bucket is
-            // either, and the crowded-boundary count below sends the
-            // selection to the bisection, which needs no boundary
-            const int cs_ = hit ? __ffs(hit) - 1 : 0;
-            if (lane == 0) sm.bc[2] = 0x7fffffffu;
-            __syncwarp();
-            const uint32_t above = __shfl_sync(0xffffffffu, above_s, cs_);
-            constexpr int SPL = SL / 32;
-            uint32_t c[SPL];
-            const uint32_t a = cluster_map(smem_addr(&sm.ssum[lane * SPL]), (uint32_t)cs_);
-#pragma unroll
-            for (int i = 0; i < SPL; ++i) c[i] = ld_cluster_u32(a + 4 * i);
-            uint32_t ls = 0;
-#pragma unroll
-            for (int i = 0; i < SPL; ++i) ls += c[i];
-            uint32_t lsuf = ls;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_down_sync(0xffffffffu, lsuf, o);
-                if (lane + o < 32) lsuf += y;
-            }
-            uint32_t g = above + lsuf - ls;   // keys above this lane's buckets
-#pragma unroll
-            for (int i = SPL - 1; i >= 0; --i) {
-                if (g < (uint32_t)keff && (uint32_t)keff <= g + c[i]) {
-                    sm.bc[0] = (uint32_t)(cs_ * SL + lane * SPL + i);
-                    sm.bc[1] = g;
-                    sm.bc[2] = c[i];
-                }
-                g += c[i];
-            }
+            g += cb[e];
         }
         __syncthreads();
-        const int B = (int)sm.bc[0];
-        const int take = keff - (int)sm.bc[1];   // 1 .. cnt
-        const int cnt = (int)sm.bc[2];
+        const int B = (int)sm.bucket;
+        const int take = keff - (int)sm.gt;   // 1 .. cnt
+        const int cnt = (int)sm.cnt;
         uint64_t inb = 0;
-        uint32_t nb = 0;
+        uint32_t nb = 0, nw = 0;
 #pragma unroll
         for (int e = 0; e < KPT; ++e) {
             sel |= (uint64_t)(bk[e] > B) << e;
             inb |= (uint64_t)(bk[e] == B) << e;
             nb += bk[e] == B;
+            nw += bk[e] > B;
         }
         if (APPROX || cnt <= kBkCap) {
             // the boundary bucket's keys in column order over the cluster:
-            // this CTA's after those of lower ranks
-            uint32_t nbc = 0;
+            // this CTA's after those of lower ranks; with them every CTA's
+            // winners, so that each CTA knows every CTA's output count
+            uint32_t nbc = 0, nwc = 0;
             const uint32_t lbase = bk_scan<NT>(nb, sm.red, &nbc);
+            __syncthreads();   // the scan's reads of red are done before it is reused
+            nwc = bk_sum<NT>(nw, sm.red);
             if (!APPROX) {
                 uint32_t pos = lbase;
 #pragma unroll
                 for (int e = 0; e < KPT; ++e)
                     if ((inb >> e) & 1ull) sm.ck[pos++] = keys[e];
             }
-            if (tid == 0) sm.xch[2][0] = nbc;
-            cluster_sync();
+            if (tid == 0) {
+                sm.xch[1][0] = nbc;
+                sm.xch[1][1] = nwc;
+            }
+            cluster_sync();   // (3)
             if (tid < 32) {
-                const uint32_t v =
-                    lane < CS ? ld_cluster_u32(cluster_map(smem_addr(&sm.xch[2][0]), (uint32_t)lane)) : 0u;
-                uint32_t incl = v;
+                uint32_t vb = 0, vw = 0;
+                if (lane < CS) {
+                    vb = ld_cluster_u32(cluster_map(smem_addr(&sm.xch[1][0]), (uint32_t)lane));
+                    vw = ld_cluster_u32(cluster_map(smem_addr(&sm.xch[1][1]), (uint32_t)lane));
+                }
+                uint32_t incl = vb;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
                     if (lane >= o) incl += y;
                 }
-                const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);   // every lane takes part
-                if (lane < CS) sm.off[lane] = incl - v;
+                const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+                if (lane < CS) sm.off[lane] = incl - vb;
                 if (lane == 0) sm.off[CS] = total;
+                // winners of the CTAs before this one
+                uint32_t iw = vw;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, iw, o);
+                    if (lane >= o) iw += y;
+                }
+                const uint32_t wb = __shfl_sync(0xffffffffu, iw - vw, (int)me);
+                if (lane == 0) sm.bc[3] = wb;
             }
             __syncthreads();
             const uint32_t cbase = sm.off[me];
-            if (APPROX) {
-                const uint32_t off = (uint32_t)(sample % (uint64_t)cnt);
-                uint32_t pos = cbase + lbase;
-#pragma unroll
-                for (int e = 0; e < KPT; ++e) {
-                    if ((inb >> e) & 1ull) {
-                        if ((pos + (uint32_t)cnt - off) % (uint32_t)cnt < (uint32_t)take) sel |= (uint64_t)1 << e;
-                        ++pos;
-                    }
-                }
-            } else {
-                // gather the cluster's boundary keys, then rank this CTA's
+            if (!APPROX) {
+                // gather the cluster's boundary keys and rank all of them
                 for (int gi = tid; gi < cnt; gi += NT) {
                     int owner = 0;
 #pragma unroll
@@ -290,24 +279,32 @@ __device__ int cluster_bucket_topk(const uint32_t (&keys)[KPT], int k, int col0,
                         cluster_map(smem_addr(&sm.ck[gi - (int)sm.off[owner]]), (uint32_t)owner));
                 }
                 __syncthreads();
-                for (int i = tid; i < (int)nbc; i += NT) {
-                    const int gi = (int)cbase + i;
+                for (int gi = tid; gi < cnt; gi += NT) {
                     const uint32_t mine = sm.ckall[gi];
                     int rank = 0;
                     for (int j = 0; j < cnt; ++j) {
                         const uint32_t y = sm.ckall[j];
                         rank += (y > mine) || (y == mine && j < gi);
                     }
-                    sm.pick[i] = rank < take ? 1 : 0;
+                    sm.pick[gi] = rank < take ? 1 : 0;
                 }
                 __syncthreads();
-                uint32_t pos = lbase;
+            }
+            // boundary keys taken by the CTAs before this one
+            const uint32_t off = APPROX ? (uint32_t)(sample % (uint64_t)cnt) : 0u;
+            auto taken = [&](uint32_t gi) -> bool {
+                return APPROX ? (gi + (uint32_t)cnt - off) % (uint32_t)cnt < (uint32_t)take : sm.pick[gi] != 0;
+            };
+            uint32_t tb = 0;
+            for (uint32_t gi = (uint32_t)tid; gi < cbase; gi += NT) tb += taken(gi) ? 1u : 0u;
+            tb = bk_sum<NT>(tb, sm.red);
+            base = sm.bc[3] + tb;
+            uint32_t pos = cbase + lbase;
 #pragma unroll
-                for (int e = 0; e < KPT; ++e) {
-                    if ((inb >> e) & 1ull) {
-                        if (sm.pick[pos]) sel |= (uint64_t)1 << e;
-                        ++pos;
-                    }
+            for (int e = 0; e < KPT; ++e) {
+                if ((inb >> e) & 1ull) {
+                    if (taken(pos)) sel |= (uint64_t)1 << e;
+                    ++pos;
                 }
             }
         } else {
@@ -361,22 +358,25 @@ __device__ int cluster_bucket_topk(const uint32_t (&keys)[KPT], int k, int col0,
                     ++eqr;
                 }
             }
+            need_exchange = true;
         }
     }
     // ---- output positions in column order over the cluster
     __syncthreads();
     uint32_t tot = 0;
     uint32_t lpos = bk_scan<NT>((uint32_t)__popcll(sel), sm.red, &tot);
-    if (tid == 0) sm.xch[6][0] = tot;
-    cluster_sync();
-    __syncthreads();   // bk_scan's reads of red are done before it is reused
-    uint32_t below = 0;
-    cl_gather_sum<NT, CS>(sm, 6, 0, &below);
-    uint32_t pos = below + lpos;
+    if (need_exchange) {
+        // (the bisection path) every CTA's output count
+        if (tid == 0) sm.xch[6][0] = tot;
+        cluster_sync();
+        __syncthreads();
+        cl_gather_sum<NT, CS>(sm, 6, 0, &base);
+    }
+    uint32_t pos = base + lpos;
 #pragma unroll
     for (int e = 0; e < KPT; ++e)
         if ((sel >> e) & 1ull) out((int)pos++, col0 + e);
-    cluster_sync();   // no CTA leaves, or reuses the scratch, while another reads it
+    cluster_sync();   // (4) no CTA leaves, or reuses the scratch, while another reads it
     return keff;
 }
 
