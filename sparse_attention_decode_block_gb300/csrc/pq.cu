@@ -126,8 +126,9 @@ struct PsLayout {
     static constexpr int QCOL = (kPsHeads / 8) * 1024;    // one atom column of the query tile
     static constexpr int KS = 32 * 256 * 8;               // key tiles: 2 buffers x 2 atom columns
     static constexpr int QS = KS + 4 * COL;               // query tile: 2 atom columns
-    static constexpr int W = QS + 2 * QCOL;               // [64] fp32 head weights
-    static constexpr int VAL = W + kPsHeads * 4;          // [2][128] token of each key row (-1: not scored)
+    static constexpr int W = QS + 2 * QCOL;               // [2][64] fp32 head weights (the request of
+                                                          // a tile being read, and the next one's)
+    static constexpr int VAL = W + 2 * kPsHeads * 4;      // [2][128] token of each key row (-1: not scored)
     static constexpr int BAR = VAL + 2 * kPsTok * 4;      // full[2], mma[2], TMEM base address
     static constexpr int SMEM = BAR + 48;
     static constexpr int TCOLS = 128;                     // two accumulators of 64 columns
@@ -221,34 +222,55 @@ __global__ void __launch_bounds__(kPsThreads, 1) k_pq_scores(PqArgs a)
     if (warp >= 4) {
         // ---------------- producers: thread p decodes key row p
         const int p = tid - kPsConsumers;
-        // this thread's token of tile i, whether it is scored, its codes
-        auto fetch = [&](int i, int &tok, uint4 &c0, uint4 &c1) -> bool {
+        // this thread's token of tile i and whether it is scored (the
+        // request's length is read once per request)
+        int len_r = -1, len_v = 0;
+        auto token_of = [&](int i, int &r, int &tok) -> bool {
             const int tile = tile_of(i);
-            const int r = tile / tpr;
+            r = tile / tpr;
             tok = (tile - r * tpr) * kPsTok + p;
-            const int L = a.lens[r];
+            if (r != len_r) {
+                len_r = r;
+                len_v = a.lens[r];
+                if (!(len_v >= 0 && (int64_t)len_v <= (int64_t)T) && p == 0) flag_error(a.status, LSA_ERR_BOUNDS);
+            }
+            const int L = len_v;
             const bool len_ok = L >= 0 && (int64_t)L <= (int64_t)T;
-            if (!len_ok && p == 0 && tok == 0) flag_error(a.status, LSA_ERR_BOUNDS);
             const int64_t se = len_ok ? min(a.sink, L) : 0;
             const int64_t rs = len_ok ? max((int64_t)L - a.recent, se) : 0;
             const int nfull_tok = len_ok ? (L / b) * b : 0;
-            if (!(tok < nfull_tok && pq_block_candidate(tok / b, b, se, rs))) return false;
-            const int pg = a.pt[(int64_t)r * a.max_blocks + tok / b];
-            if (pg < 0 || pg >= a.ic.num_pages) {
-                flag_error(a.status, LSA_ERR_BOUNDS);
-                return false;
-            }
-            const uint4 *cp = reinterpret_cast<const uint4 *>(a.codes + ((int64_t)pg * b + tok % b) * 32);
-            c0 = cp[0];
-            c1 = cp[1];
-            return true;
+            return tok < nfull_tok && pq_block_candidate(tok / b, b, se, rs);
         };
-        int tok = 0, tok_n = 0;
-        uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0, n0 = c0, n1 = c0;
-        bool v = ntiles > 0 && fetch(0, tok, c0, c1);
+        auto codes_ptr = [&](int pg, int tok) {
+            return reinterpret_cast<const uint4 *>(a.codes + ((int64_t)pg * b + tok % b) * 32);
+        };
+        // a two-stage prefetch: while tile i decodes, the codes of tile i + 1
+        // (its page id is here) and the page id of tile i + 2 load
+        int r0 = 0, tok = 0, r1 = 0, tok1 = 0, r2 = 0, tok2 = 0;
+        uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
+        bool v = ntiles > 0 && token_of(0, r0, tok);
+        if (v) {
+            const int pg = a.pt[(int64_t)r0 * a.max_blocks + tok / b];
+            v = pg >= 0 && pg < a.ic.num_pages;
+            if (!v) flag_error(a.status, LSA_ERR_BOUNDS);
+            else {
+                c0 = codes_ptr(pg, tok)[0];
+                c1 = codes_ptr(pg, tok)[1];
+            }
+        }
+        bool v1 = ntiles > 1 && token_of(1, r1, tok1);
+        int pg1 = v1 ? a.pt[(int64_t)r1 * a.max_blocks + tok1 / b] : -1;
         for (int i = 0; i < ntiles && ok; ++i) {
-            // the next tile's codes load while this one decodes
-            const bool vn = i + 1 < ntiles && fetch(i + 1, tok_n, n0, n1);
+            // codes of tile i + 1, page id of tile i + 2: issued now, used later
+            uint4 n0 = make_uint4(0u, 0u, 0u, 0u), n1 = n0;
+            const bool v1ok = v1 && pg1 >= 0 && pg1 < a.ic.num_pages;
+            if (v1 && !v1ok) flag_error(a.status, LSA_ERR_BOUNDS);
+            if (v1ok) {
+                n0 = codes_ptr(pg1, tok1)[0];
+                n1 = codes_ptr(pg1, tok1)[1];
+            }
+            const bool v2 = i + 2 < ntiles && token_of(i + 2, r2, tok2);
+            const int pg2 = v2 ? a.pt[(int64_t)r2 * a.max_blocks + tok2 / b] : -1;
             const int buf = i & 1;
             if (i >= 2) {
                 // buffer b's previous product (tile i - 2) is done
@@ -271,10 +293,14 @@ __global__ void __launch_bounds__(kPsThreads, 1) k_pq_scores(PqArgs a)
             vtok[buf * kPsTok + p] = v ? tok : -1;
             fence_proxy_async_smem();
             mbar_arrive(&full[buf]);
-            v = vn;
-            tok = tok_n;
+            v = v1ok;
+            tok = tok1;
             c0 = n0;
             c1 = n1;
+            v1 = v2;
+            r1 = r2;
+            tok1 = tok2;
+            pg1 = pg2;
         }
     } else {
         // ---------------- consumers: warp w reads TMEM lane quadrant w
@@ -283,7 +309,7 @@ __global__ void __launch_bounds__(kPsThreads, 1) k_pq_scores(PqArgs a)
         uint32_t kmax = 0u, kmin = 0xffffffffu;
         // the query tile and head weights of request r (every product that
         // reads the previous ones is done when this is called)
-        auto load_q = [&](int r) {
+        auto load_q = [&](int r, int slot) {
             const uint8_t *qg = reinterpret_cast<const uint8_t *>(a.q + (int64_t)r * a.hq * 128);
             const int j = tid & 7;
             for (int task = tid >> 3; task < 2 * kPsHeads; task += kPsConsumers / 8) {
@@ -291,7 +317,8 @@ __global__ void __launch_bounds__(kPsThreads, 1) k_pq_scores(PqArgs a)
                 cp_async16(sbase + LY::QS + cc * LY::QCOL + atom_offset(g, j), qg + (int64_t)g * 256 + cc * 128 + j * 16);
             }
             cp_async_commit();
-            if (tid < kPsHeads) reinterpret_cast<float *>(smem + LY::W)[tid] = a.weights[(int64_t)r * a.hq + tid];
+            if (tid < kPsHeads)
+                reinterpret_cast<float *>(smem + LY::W)[slot * kPsHeads + tid] = a.weights[(int64_t)r * a.hq + tid];
             cp_async_wait<0>();
             fence_proxy_async_smem();
             consumer_sync();
@@ -323,9 +350,11 @@ __global__ void __launch_bounds__(kPsThreads, 1) k_pq_scores(PqArgs a)
             }
             return true;
         };
+        int wslot = 0;      // weights of tile i's request
+        int wslot_n = 0;    // and of tile i + 1's
         if (ntiles > 0) {
             cur = tile_of(0) / tpr;
-            load_q(cur);
+            load_q(cur, 0);
             ok = issue(0);
         }
         for (int i = 0; i < ntiles && ok; ++i) {
@@ -335,10 +364,12 @@ __global__ void __launch_bounds__(kPsThreads, 1) k_pq_scores(PqArgs a)
             // this tile's product is done
             if (i + 1 < ntiles) {
                 const int rn = tile_of(i + 1) / tpr;
+                wslot_n = wslot;
                 if (rn != r) {
                     ok = consumer_all(mbar_wait(&mma[buf], (i >> 1) & 1, a.status, a.spin_budget));
                     if (!ok) break;
-                    load_q(rn);
+                    wslot_n = wslot ^ 1;   // tile i's weights stay for its scores below
+                    load_q(rn, wslot_n);
                 }
                 tc_fence_before();
                 consumer_sync();   // accumulator (i + 1) & 1 was read (tile i - 1) before it is written
@@ -356,8 +387,9 @@ __global__ void __launch_bounds__(kPsThreads, 1) k_pq_scores(PqArgs a)
             for (int half = 0; half < 2; ++half) {
                 tmem_ld32(tmem + lane_base + 64 * buf + 32 * half, d);
 #pragma unroll
-                for (int g = 0; g < 32; ++g) s = fmaf(w_s[32 * half + g], fmaxf(d[g], 0.f), s);
+                for (int g = 0; g < 32; ++g) s = fmaf(w_s[wslot * kPsHeads + 32 * half + g], fmaxf(d[g], 0.f), s);
             }
+            wslot = wslot_n;
             if (r != cur) {
                 pq_flush_ext(a.row_ext, cur, kmax, kmin);
                 kmax = 0u;
