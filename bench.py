@@ -544,15 +544,26 @@ def e2e_leg(insts, args, stream):
 # ---------------------------------------------------------------- CPU oracle
 
 def cpu_model() -> str:
+    """The host CPU's model name; on Arm, the implementer and part numbers
+    from /proc/cpuinfo with the name of the few known parts."""
     try:
         with open("/proc/cpuinfo") as f:
             txt = f.read()
     except OSError:
         return "unknown"
-    for key in ("model name", "Model", "CPU part"):
-        for ln in txt.splitlines():
-            if ln.startswith(key):
-                return ln.split(":", 1)[1].strip()
+    for ln in txt.splitlines():
+        if ln.startswith("model name"):
+            return ln.split(":", 1)[1].strip()
+    fields = {}
+    for ln in txt.splitlines():
+        if ":" in ln:
+            k, v = ln.split(":", 1)
+            fields.setdefault(k.strip(), v.strip())
+    parts = {("0x41", "0xd4f"): "Arm Neoverse V2", ("0x41", "0xd40"): "Arm Neoverse V1",
+             ("0x41", "0xd0c"): "Arm Neoverse N1", ("0x41", "0xd49"): "Arm Neoverse N2"}
+    imp, part = fields.get("CPU implementer"), fields.get("CPU part")
+    if part:
+        return parts.get((imp, part), f"implementer {imp} part {part}")
     return "unknown"
 
 
