@@ -19,7 +19,7 @@ NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2"
                      "-I" + os.path.join(HERE, "..", "include")]
 SOURCES = ["summaries.cu", "score_topk.cu", "topk_fast.cu", "attention.cu", "attention_tc.cu", "attention_flat.cu", "attention_umma.cu",
            "c2f_fine.cu", "pq.cu", "api.cu"]
-DEPS = ["lsa_device.cuh", "lsa_internal.h", "attn_items.cuh", "topk_block.cuh", "topk_bucket.cuh", "topk_cluster.cuh", "fine_tile.cuh", os.path.join("..", "..", "include", "lsa.h")]
+DEPS = ["lsa_device.cuh", "lsa_internal.h", "attn_items.cuh", "attn_stage.cuh", "topk_block.cuh", "topk_bucket.cuh", "topk_cluster.cuh", "fine_tile.cuh", os.path.join("..", "..", "include", "lsa.h")]
 
 
 def _nvcc() -> str:

@@ -23,6 +23,7 @@
 #include <math.h>
 
 #include "attn_items.cuh"
+#include "attn_stage.cuh"
 #include "lsa_device.cuh"
 #include "topk_block.cuh"
 #include "topk_bucket.cuh"
@@ -40,7 +41,6 @@ constexpr float kFlLn2 = 0.693147180559945309f;
 template <int DK, int G>
 struct FlLayout {
     static constexpr int STAGES = G <= 4 ? 3 : 2;   // one CTA of eight warps per SM
-    static constexpr int CPR = DK / 8;            // 16-byte chunks per token row
     static constexpr int SUB = kChunk * 128;      // one swizzled 16-row x 128-byte sub-tile
     static constexpr int KBYTES = (DK / 64) * SUB;
     static constexpr int STAGE = 2 * KBYTES;      // K tile then V tile
@@ -89,7 +89,6 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
     using LY = FlLayout<DK, G>;
     static_assert(KSEL == 0 || kFlWarps * 32 == kTfThreads, "one CTA is one top-k block");
     constexpr int NT = DK / 8;
-    constexpr int CPL = kChunk * LY::CPR / 32;
     constexpr int kFlStages = LY::STAGES;
     static_assert(G >= 2 && G <= 8, "heads of a group must fit rows 0..7 of the MMA tile");
 
@@ -242,33 +241,17 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
         if (lane == 0) stage_n[j % kFlStages] = n;
         if (n > 0) {
             const int h = (int)fmodu(fdiv((uint32_t)rho, a.fd_nsub), a.fd_hkv);
-            const uint32_t st = ring_s + (j % kFlStages) * LY::STAGE;
             const uint8_t *kb = c.k + ((int64_t)page * c.kps + (int64_t)h * c.khs + (int64_t)ts * c.kts) * 2;
             const uint8_t *vb = c.v + ((int64_t)page * c.vps + (int64_t)h * c.vhs + (int64_t)ts * c.vts) * 2;
-#pragma unroll
-            for (int u = 0; u < CPL; ++u) {
-                const int q = lane + 32 * u;
-                const int t = q / LY::CPR, ch = q % LY::CPR;
-                if (t < n) {
-                    cp_async16_policy(st + swizzle_offset(t, ch), kb + (int64_t)t * c.kts * 2 + ch * 16, pol);
-                    cp_async16_policy(st + LY::KBYTES + swizzle_offset(t, ch), vb + (int64_t)t * c.vts * 2 + ch * 16,
-                                      pol);
-                }
-            }
+            stage_item_kv<DK>(ring_s + (j % kFlStages) * LY::STAGE, kb, vb, c.kts, c.vts, n, pol);
         }
         cp_async_commit();
     };
 
-    const int mi = lane >> 3, r8 = lane & 7;
-    const int tk = (mi >> 1) * 8 + r8, ck = mi & 1;
-    const int tv = (mi & 1) * 8 + r8, cv = mi >> 1;
-
     // the current row segment's state lives in registers; a segment of the
     // piece's first row that ends mid-stream is parked in shared memory
-    float m = -INFINITY, l = 0.f;
-    float o[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    GroupState<DK> gs;
+    group_state_reset(gs);
     float *s0o = reinterpret_cast<float *>(smem + LY::SEG0) + warp * G * DK;   // [G][DK]
     float *s0m = reinterpret_cast<float *>(smem + LY::SEG0) + kFlWarps * G * DK + warp * 2 * G;   // m[G], l[G]
     if (lane < G) {
@@ -281,10 +264,10 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
         if (rr < G) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
-                *reinterpret_cast<float2 *>(dst_o + rr * DK + nt * 8 + 2 * cc) = make_float2(o[nt][0], o[nt][1]);
+                *reinterpret_cast<float2 *>(dst_o + rr * DK + nt * 8 + 2 * cc) = make_float2(gs.o[nt][0], gs.o[nt][1]);
             if (cc == 0) {
-                dst_ml[rr] = m;
-                dst_ml[G + rr] = l;
+                dst_ml[rr] = gs.m;
+                dst_ml[G + rr] = gs.l;
             }
         }
     };
@@ -293,10 +276,7 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
     };
     auto open_segment = [&](int rho) {
         cur_rho = rho;
-        m = -INFINITY;
-        l = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+        group_state_reset(gs);
         if (rho != rho_w0) {   // the warp's second row: its query fragments were loaded up front
 #pragma unroll
             for (int ks = 0; ks < DK / 16; ++ks) {
@@ -318,61 +298,9 @@ __global__ void __launch_bounds__(kFlWarps * 32, 1) k_attn_flat(AttnArgs a)
         cp_async_wait<kFlStages - 1>();
         __syncwarp();
         const int n = stage_n[j % kFlStages];
-        if (n > 0) {
-            const uint32_t kbase = ring_s + (j % kFlStages) * LY::STAGE;
-            const uint32_t vbase = kbase + LY::KBYTES;
-            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int ks = 0; ks < DK / 16; ++ks) {
-                uint32_t b[4];
-                ldsm_x4(b, kbase + swizzle_offset(tk, 2 * ks + ck));
-                mma_bf16_rows8(s0, qa0[ks], qa2[ks], b[0], b[1]);
-                mma_bf16_rows8(s1, qa0[ks], qa2[ks], b[2], b[3]);
-            }
-            const int t0 = 2 * cc;
-            const float z0 = t0 < n ? s0[0] * a.scale_log2 : -INFINITY;
-            const float z1 = t0 + 1 < n ? s0[1] * a.scale_log2 : -INFINITY;
-            const float z2 = t0 + 8 < n ? s1[0] * a.scale_log2 : -INFINITY;
-            const float z3 = t0 + 9 < n ? s1[1] * a.scale_log2 : -INFINITY;
-            float mx = fmaxf(fmaxf(z0, z1), fmaxf(z2, z3));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float mn = fmaxf(m, mx);
-            float alpha = 1.f;
-            uint32_t pa0 = 0u, pa2 = 0u;
-            if (mn != -INFINITY) {
-                alpha = fast_ex2(m - mn);
-                pa0 = pack_bf16x2(fast_ex2(z0 - mn), fast_ex2(z1 - mn));
-                pa2 = pack_bf16x2(fast_ex2(z2 - mn), fast_ex2(z3 - mn));
-                m = mn;
-            }
-            // the denominator sums the same bf16-rounded weights the MMA uses
-            const float2 p01 = bf2_to_f2(pa0), p23 = bf2_to_f2(pa2);
-            float ps = (p01.x + p01.y) + (p23.x + p23.y);
-            ps += __shfl_xor_sync(0xffffffffu, ps, 1);
-            ps += __shfl_xor_sync(0xffffffffu, ps, 2);
-            l = l * alpha + ps;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                o[nt][0] *= alpha;
-                o[nt][1] *= alpha;
-            }
-            if (n < kChunk) {   // stale V rows meet zero weights; 0 * NaN must not happen
-                for (int q = lane; q < (kChunk - n) * LY::CPR; q += 32) {
-                    const int t = n + q / LY::CPR, ch = q % LY::CPR;
-                    *reinterpret_cast<uint4 *>(ring + (j % kFlStages) * LY::STAGE + LY::KBYTES + swizzle_offset(t, ch)) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-                __syncwarp();
-            }
-#pragma unroll
-            for (int dt = 0; dt < DK / 16; ++dt) {
-                uint32_t b[4];
-                ldsm_x4_t(b, vbase + swizzle_offset(tv, 2 * dt + cv));
-                mma_bf16_rows8(o[2 * dt], pa0, pa2, b[0], b[1]);
-                mma_bf16_rows8(o[2 * dt + 1], pa0, pa2, b[2], b[3]);
-            }
-        }
+        if (n > 0)
+            attend_staged_item<DK>(ring_s + (j % kFlStages) * LY::STAGE, ring + (j % kFlStages) * LY::STAGE, n, qa0,
+                                   qa2, a.scale_log2, gs);
         __syncwarp();
     }
     cp_async_wait<0>();

@@ -360,6 +360,12 @@ __device__ __forceinline__ uint32_t float_to_key(float s)
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// Inverse of float_to_key on the keys it produces.
+__device__ __forceinline__ float key_to_float(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 // ---------------------------------------------------------------- loads
 
 __device__ __forceinline__ uint4 ldg_nc_v4(const void *p)

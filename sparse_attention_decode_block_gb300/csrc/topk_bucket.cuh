@@ -34,12 +34,6 @@ struct BucketScratch {
     uint32_t bucket, gt, cnt;     // boundary bucket, keys in higher buckets, keys in it
 };
 
-// Inverse of float_to_key (lsa_device.cuh) on the keys it produces.
-__device__ __forceinline__ float key_to_float(uint32_t k)
-{
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
 // Block-wide exclusive scan of one value per thread; *total gets the sum.
 // One barrier; the caller separates two uses of `red` by another barrier.
 template <int NT>
