@@ -45,7 +45,19 @@ L2_BYTES = 129 * 1024 * 1024
 # (workload, kernel) -> dram__bytes_read.sum + dram__bytes_write.sum per
 # launch from the ncu capture summarised in profiles/; an entry is removed
 # whenever its kernel changes after the capture.
-NCU_TRAFFIC = {}
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
+# each kernel the roofline may name, from one ncu capture of
+# `python bench.py --config NAME --steps 8 --warmup 3 --soak 0
+# --no-cpu-baseline --instances 1` (summaries in profiles/); an entry goes
+# when its kernel changes until it is captured again.
+NCU_TRAFFIC = {
+    ("b16_32k", "k_attn_flat (selects)"): 68554837, ("b16_32k", "k_score"): 67405483,
+    ("ragged", "k_attn_flat (selects)"): 526917717, ("ragged", "k_score"): 139504299,
+    ("b16_32k_quest", "k_attn_flat (selects)"): 68547755, ("b16_32k_quest", "k_score_quest"): 135514197,
+    ("c2f", "k_c2f_fine"): 9007488, ("c2f", "k_score"): 8614912, ("c2f_wrelu", "k_c2f_fine"): 9009067,
+    ("mla", "k_score"): 76397312, ("mla", "k_topk"): 303104,
+    ("c2f_pq", "k_pq_scores"): 67777792, ("c2f_pq", "k_pq_hist + k_pq_select"): 25298688,
+}
 
 
 def peaks(kind: str = "hbm"):
@@ -691,11 +703,25 @@ def main():
         # the step is two launches: the score kernel and the attention kernel
         # that also selects the blocks; the latter's time is the step's time
         # minus the score kernel's (both CUDA-event timings)
-        kernel_ms = {"k_score": st["score"], "k_attn_flat (selects)": max(ms_step - st["score"], 1e-9)}
-        kbytes = {"k_score": stage_bytes["score"], "k_attn_flat (selects)": stage_bytes["attention"]}
+        sk = "k_score_quest" if w.summary_kind == 1 else "k_score"
+        kernel_ms = {sk: st["score"], "k_attn_flat (selects)": max(ms_step - st["score"], 1e-9)}
+        kbytes = {sk: stage_bytes["score"], "k_attn_flat (selects)": stage_bytes["attention"]}
+    elif st and w.c2f_candidates > 0 and res["kernels"] == 3:
+        # coarse scores, the cluster kernel (coarse top-C, FP8 rescoring,
+        # token top-k), attention; the cluster kernel's time is the step's
+        # minus the other two
+        kernel_ms = {"k_score": st["score"], "k_c2f_fine": max(ms_step - st["score"] - st["attention"], 1e-9),
+                     "k_sparse_attn_umma": st["attention"]}
+        kbytes = {"k_score": stage_bytes["score"], "k_c2f_fine": stage_bytes["fine"],
+                  "k_sparse_attn_umma": stage_bytes["attention"]}
     else:
-        kernel_ms = dict(st)
-        kbytes = stage_bytes
+        # one kernel per stage (scores, top-k, attention): each stage's
+        # entry point launches the step's own kernel for it
+        names = {"score": "k_score_quest" if w.summary_kind == 1 else "k_score",
+                 "topk": "k_topk", "attention": "k_sparse_attn_umma" if w.num_q_heads // w.num_kv_heads == 64
+                 else "attention"}
+        kernel_ms = {names.get(k, k): v for k, v in st.items()}
+        kbytes = {names.get(k, k): v for k, v in stage_bytes.items()}
     # the dominant kernel: the longest stage that moves algorithmic bytes
     moving = {k: v for k, v in kernel_ms.items() if kbytes.get(k, 0) > 0}
     dominant = max(moving, key=moving.get)
@@ -717,7 +743,7 @@ def main():
                 "duration_us": round(kernel_ms[dominant] * 1e3, 2),
                 "algorithmic_bytes": kbytes[dominant],
                 "timing": ("step minus score kernel" if dominant.startswith("k_attn_flat")
-                           else "step minus the other kernels" if dominant.startswith("k_pq_hist")
+                           else "step minus the other kernels" if dominant.startswith(("k_pq_hist", "k_c2f_fine"))
                            else "CUDA graph of the stage's entry point"),
                 "traffic": NCU_TRAFFIC.get((w.name, dominant))}
     cb = None
