@@ -29,6 +29,7 @@
 // product.  Every tile writes
 // its normalised output and log-sum-exp; the tiles of a row are merged by
 // log-sum-exp (ByteCross, Appendix A) in the merge kernel.
+#include <cuda.h>   // CUtensorMap (the encoder is taken from the driver at run time)
 #include <math.h>
 
 #include "attn_items.cuh"
@@ -61,8 +62,8 @@ struct UmLayout {
     static constexpr int ROFF = ROWS + kUmTok * 8;       // int64 byte offset of each K / V row (-1: none)
     static constexpr int RED = ROFF + 2 * kUmTok * 8;    // [4 quadrants][64] per-head partials
     static constexpr int STAT = RED + 4 * kUmHeads * 4;  // per-head max, 1 / sum
-    static constexpr int BAR = STAT + 2 * kUmHeads * 4;  // mbarrier, TMEM base address, merge flag
-    static constexpr int SMEM = BAR + 16;
+    static constexpr int BAR = STAT + 2 * kUmHeads * 4;  // mbarrier, TMEM base address, merge flag, query mbarrier
+    static constexpr int SMEM = BAR + 24;
     static constexpr int TCOLS_USED = kUmHeads + kUmHeads * (DV / 128);   // S^T, then O^T per 128 dims
     static constexpr int TCOLS = TCOLS_USED <= 128 ? 128 : (TCOLS_USED <= 256 ? 256 : 512);
     static_assert(DK % 64 == 0 && DV % 128 == 0, "tile shapes");
@@ -139,8 +140,11 @@ __device__ __forceinline__ void gather_rows(uint32_t dst, uint8_t *dst_generic, 
     }
 }
 
+// tmq: a 2-D tensor map of the queries [B * Hq rows, DK] (bf16, 64 x 64
+// boxes, 128-byte swizzle): the group's 64 x DK query tile comes in with one
+// tensor copy per 64-dim atom column, already in the MMA's atom layout.
 template <int DK, int DV, bool ALIAS>
-__global__ void __launch_bounds__(kUmThreads, 1) k_sparse_attn_umma(AttnArgs a)
+__global__ void __launch_bounds__(kUmThreads, 1) k_sparse_attn_umma(AttnArgs a, const __grid_constant__ CUtensorMap tmq)
 {
     pdl_enter();
     using LY = UmLayout<DK, DV, ALIAS>;
@@ -158,6 +162,7 @@ __global__ void __launch_bounds__(kUmThreads, 1) k_sparse_attn_umma(AttnArgs a)
     const int r = (int)fdiv((uint32_t)rh, a.fd_hkv), h = rh - r * c.hkv;
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + LY::BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + LY::BAR + 8);
+    uint64_t *qbar = reinterpret_cast<uint64_t *>(smem + LY::BAR + 16);
     int2 *rows = reinterpret_cast<int2 *>(smem + LY::ROWS);
     int64_t *koff = reinterpret_cast<int64_t *>(smem + LY::ROFF);   // [128] K rows, then [128] V rows
     int64_t *voff = koff + kUmTok;
@@ -174,6 +179,7 @@ __global__ void __launch_bounds__(kUmThreads, 1) k_sparse_attn_umma(AttnArgs a)
     }
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(qbar, 1);
         fence_barrier_init();
     }
 
@@ -207,14 +213,12 @@ __global__ void __launch_bounds__(kUmThreads, 1) k_sparse_attn_umma(AttnArgs a)
     const uint64_t pol = l2_evict_first();
     gather_rows<LY::KC>(sbase + LY::KS, smem + LY::KS, c.k, koff, LY::COL, pol);
     if constexpr (LY::VSEP) gather_rows<LY::VC>(sbase + LY::VS, smem + LY::VS, c.v, voff, LY::COL, pol);
-    {
-        // queries: a task is one (atom column, head) pair, 8 lanes of 16 bytes
-        const uint8_t *qg = reinterpret_cast<const uint8_t *>(a.q + ((int64_t)r * a.hq + (int64_t)h * a.gsize) * DK);
-        const int j = lane & 7;
-        for (int task = tid >> 3; task < LY::KC * kUmHeads; task += kUmThreads / 8) {
-            const int cc = task >> 6, g = task & (kUmHeads - 1);
-            cp_async16(sbase + LY::QS + cc * LY::QCOL + atom_offset(g, j), qg + (int64_t)g * DK * 2 + cc * 128 + j * 16);
-        }
+    if (tid == 0) {
+        // the group's queries: one tensor copy per 64-dim atom column
+        mbar_arrive_expect_tx(qbar, (uint32_t)(LY::KC * kUmHeads * 128));
+#pragma unroll 1
+        for (int cc = 0; cc < LY::KC; ++cc)
+            tma_load_2d(sbase + LY::QS + cc * LY::QCOL, &tmq, cc * 64, r * a.hq + h * a.gsize, qbar);
     }
     cp_async_commit();
     cp_async_wait<0>();
@@ -222,8 +226,13 @@ __global__ void __launch_bounds__(kUmThreads, 1) k_sparse_attn_umma(AttnArgs a)
     tc_fence_before();
     __syncthreads();
 
-    // ---- S^T = K_tile Q^T: one 64-dim atom column (four K = 16 steps) at a time
-    if (tid == 0) {
+    // ---- S^T = K_tile Q^T: one 64-dim atom column (four K = 16 steps) at a
+    // time, once the queries have landed (a wait that gives up issues
+    // nothing; the product's wait below then gives up too)
+    bool q_ok = true;
+    if (tid == 0) q_ok = mbar_wait(qbar, 0, a.status, a.spin_budget);
+    q_ok = __syncthreads_and(q_ok) != 0;
+    if (tid == 0 && q_ok) {
         tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < LY::KC; ++cc) {
@@ -240,7 +249,7 @@ __global__ void __launch_bounds__(kUmThreads, 1) k_sparse_attn_umma(AttnArgs a)
     // for are then waited for once more (bounded) before the tensor memory
     // they write is freed
     uint32_t phase = 0;
-    bool ok = mbar_wait(bar, phase, a.status, a.spin_budget);
+    bool ok = q_ok && mbar_wait(bar, phase, a.status, a.spin_budget);
     ok = __syncthreads_and(ok) != 0;
     if (ok) {
         tc_fence_after();
@@ -366,7 +375,10 @@ __global__ void __launch_bounds__(kUmThreads, 1) k_sparse_attn_umma(AttnArgs a)
             }
         }
     }
-    if (!ok) mbar_wait(bar, phase, nullptr, a.spin_budget);
+    if (!ok) {
+        if (q_ok) mbar_wait(bar, phase, nullptr, a.spin_budget);   // products in flight
+        else if (tid == 0) mbar_wait(qbar, 0, nullptr, a.spin_budget);   // query copies in flight
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, LY::TCOLS);
@@ -448,6 +460,41 @@ __global__ void __launch_bounds__(kUmThreads, 1) k_sparse_attn_umma(AttnArgs a)
     }
 }
 
+// cuTensorMapEncodeTiled from the driver (the runtime is linked statically;
+// the driver library is not linked).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled()
+{
+    static const EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (EncodeTiledFn) nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// The queries [rows, dk] bf16 (rows = batch * Hq, row stride dk) as 64 x 64
+// boxes with the 128-byte swizzle.
+bool encode_query_map(CUtensorMap *m, const void *q, int64_t rows, int dk)
+{
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t gdim[2] = {(cuuint64_t)dk, (cuuint64_t)rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)dk * 2};
+    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t estride[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(q), gdim, gstride, box, estride,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int DK, int DV, bool ALIAS>
 cudaError_t launch_umma_t(const AttnArgs &a, cudaStream_t s)
 {
@@ -455,7 +502,9 @@ cudaError_t launch_umma_t(const AttnArgs &a, cudaStream_t s)
     auto kern = k_sparse_attn_umma<DK, DV, ALIAS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM);
     if (e != cudaSuccess) return e;
-    e = launch_step_kernel(kern, dim3(a.splits, a.batch * a.c.hkv), dim3(kUmThreads), LY::SMEM, s, a);
+    CUtensorMap tmq;
+    if (!encode_query_map(&tmq, a.q, (int64_t)a.batch * a.hq, DK)) return cudaErrorNotSupported;
+    e = launch_step_kernel(kern, dim3(a.splits, a.batch * a.c.hkv), dim3(kUmThreads), LY::SMEM, s, a, tmq);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -299,6 +299,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
     return true;
 }
 
+// Tiled 2-D tensor copy (TMA) global -> shared: the tensor map's box at
+// element coordinates (x, y) into dst (shared address), with the map's
+// swizzle; completion is counted in bytes on the mbarrier at bar.  tmap:
+// the generic address of a __grid_constant__ CUtensorMap parameter.  x times
+// the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // 1-D bulk copy (TMA engine) global -> shared; completion is counted in
 // bytes on `bar`.  Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
