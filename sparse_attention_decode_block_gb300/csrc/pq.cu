@@ -106,34 +106,38 @@ __global__ void __launch_bounds__(kPeThreads) k_pq_encode(PqArgs a)
 
 // ---------------------------------------------------------------- coarse scores
 
-// One CTA per SM, two roles: warps 4-7 produce (load the codes of a tile's
-// 128 tokens, a tile ahead, and decode them into a free key buffer), warps
-// 0-3 consume (thread 0 issues the tile's product, the four warps read its
-// accumulator, one TMEM lane quadrant each, and apply the weighted ReLU).
-// Key tiles and accumulators are double-buffered: the product of tile i+1
-// runs while tile i's scores are read and tile i+2 is decoded.  full[b]
-// (128 producer arrivals) says key buffer b holds a decoded tile; mma[b]
-// (the product's commit) says the product of buffer b is done, so that
-// the buffer may be decoded into again and its accumulator read.
-constexpr int kPsConsumers = 128;   // warps 0-3
-constexpr int kPsThreads = 256;     // and warps 4-7, the producers
+// Four warps a CTA, two CTAs an SM, tiles of 128 tokens strided over the
+// grid.  Thread p owns token row p of a tile, which is TMEM lane p (warp w
+// writes and reads lane quadrant w).  For tile i it decodes its token's 32
+// centroids into 64 registers (two bf16 a 32-bit word, dims in order) and
+// writes them into its lane of the A buffer i & 1 (tcgen05.st), once the
+// product that last read that buffer has completed; thread 0 then issues
+// the tile's product with A from tensor memory,
+//   S^T [128 tokens x 64 heads] = K~ [128 x 128] . Q^T [128 x 64],
+// Q^T the request's query tile in shared memory, into accumulator i & 1,
+// and while it runs every thread reads the accumulator of tile i - 1 and
+// applies the weighted ReLU.  The decoded keys never pass through shared
+// memory: the only shared-memory traffic is the codebook lookups and the
+// product's reads of the query tile.  Each thread loads its codes a tile
+// ahead and its page id two tiles ahead.
+constexpr int kPsThreads = 128;     // warps 0-3: every warp can reach its TMEM lane quadrant
+constexpr int kPsCtasPerSm = 2;
 constexpr int kPsTok = 128;         // tokens per tile (the MMA's M)
 constexpr int kPsHeads = 64;        // query heads (the MMA's N)
 
 struct PsLayout {
     static constexpr int CB = 0;                          // codebook, bf16 [32][256][4]
-    static constexpr int COL = (kPsTok / 8) * 1024;       // one 64-dim atom column of a key tile
-    static constexpr int QCOL = (kPsHeads / 8) * 1024;    // one atom column of the query tile
-    static constexpr int KS = 32 * 256 * 8;               // key tiles: 2 buffers x 2 atom columns
-    static constexpr int QS = KS + 4 * COL;               // query tile: 2 atom columns
-    static constexpr int W = QS + 2 * QCOL;               // [2][64] fp32 head weights (the request of
-                                                          // a tile being read, and the next one's)
-    static constexpr int VAL = W + 2 * kPsHeads * 4;      // [2][128] token of each key row (-1: not scored)
-    static constexpr int BAR = VAL + 2 * kPsTok * 4;      // full[2], mma[2], TMEM base address
-    static constexpr int SMEM = BAR + 48;
-    static constexpr int TCOLS = 128;                     // two accumulators of 64 columns
-    static_assert(KS % 1024 == 0 && QS % 1024 == 0, "swizzled atoms are 1024-byte aligned");
-    static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
+    static constexpr int QCOL = (kPsHeads / 8) * 1024;    // one 64-dim atom column of a query tile
+    static constexpr int QS = 32 * 256 * 8;               // query tiles: 2 slots x 2 atom columns
+    static constexpr int W = QS + 4 * QCOL;               // [2][64] fp32 head weights, one slot per query tile
+    static constexpr int BAR = W + 2 * kPsHeads * 4;      // mma[2], TMEM base address
+    static constexpr int SMEM = BAR + 32;
+    static constexpr int TA = 0;                          // TMEM columns: A buffers 2 x 64 (128 dims, two a column)
+    static constexpr int TD = 128;                        // accumulators 2 x 64 (64 heads)
+    static constexpr int TCOLS = 256;
+    static_assert(QS % 1024 == 0, "swizzled atoms are 1024-byte aligned");
+    static_assert(kPsCtasPerSm * TCOLS <= 512, "tensor memory of one SM");
+    static_assert(kPsCtasPerSm * SMEM <= 227 * 1024, "shared memory of one SM");
 };
 
 // Whether block j of a request is a candidate: full and outside the forced
@@ -154,26 +158,12 @@ __device__ __forceinline__ void pq_flush_ext(uint32_t *row_ext, int r, uint32_t 
     }
 }
 
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// CTA barrier that returns whether `ok` holds in every thread (a wait that
+// gave up in one thread ends the loop in every one, so no thread is left at
+// a barrier the others never reach).
+__device__ __forceinline__ bool consumer_all(bool ok) { return __syncthreads_and(ok ? 1 : 0) != 0; }
 
-// Barrier over the consumer warps that returns whether `ok` holds in all
-// of them (a wait that gave up in one thread ends the loop in every one, so
-// no consumer is left at a barrier the others never reach).
-__device__ __forceinline__ bool consumer_all(bool ok)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.and.pred p, 1, 128, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"(ok ? 1u : 0u)
-        : "memory");
-    return r != 0;
-}
-
-__global__ void __launch_bounds__(kPsThreads, 1) k_pq_scores(PqArgs a)
+__global__ void __launch_bounds__(kPsThreads, kPsCtasPerSm) k_pq_scores(PqArgs a)
 {
     pdl_enter();
     using LY = PsLayout;
@@ -184,19 +174,15 @@ __global__ void __launch_bounds__(kPsThreads, 1) k_pq_scores(PqArgs a)
         if (tid == 0) flag_error(a.status, LSA_ERR_INVALID_ARG);
         return;
     }
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + LY::BAR);
-    uint64_t *mma = full + 2;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + LY::BAR + 32);
-    const float *w_s = reinterpret_cast<const float *>(smem + LY::W);
-    int *vtok = reinterpret_cast<int *>(smem + LY::VAL);
+    uint64_t *mma = reinterpret_cast<uint64_t *>(smem + LY::BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + LY::BAR + 16);
+    float *w_s = reinterpret_cast<float *>(smem + LY::W);
     const uint32_t sbase = smem_addr(smem);
     if (warp == 0) {
         tmem_alloc(tslot, LY::TCOLS);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&full[0], 128);
-        mbar_init(&full[1], 128);
         mbar_init(&mma[0], 1);
         mbar_init(&mma[1], 1);
         fence_barrier_init();
@@ -210,6 +196,7 @@ __global__ void __launch_bounds__(kPsThreads, 1) k_pq_scores(PqArgs a)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
 
     const int b = a.ic.b;
     const int T = a.max_blocks * b;
@@ -217,204 +204,187 @@ __global__ void __launch_bounds__(kPsThreads, 1) k_pq_scores(PqArgs a)
     const int total = a.batch * tpr;
     const int ntiles = (int)blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     auto tile_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
-    bool ok = true;
+    const int p = tid;   // this thread's key row
 
-    if (warp >= 4) {
-        // ---------------- producers: thread p decodes key row p
-        const int p = tid - kPsConsumers;
-        // this thread's token of tile i and whether it is scored (the
-        // request's length is read once per request)
-        int len_r = -1, len_v = 0;
-        auto token_of = [&](int i, int &r, int &tok) -> bool {
-            const int tile = tile_of(i);
-            r = tile / tpr;
-            tok = (tile - r * tpr) * kPsTok + p;
-            if (r != len_r) {
-                len_r = r;
-                len_v = a.lens[r];
-                if (!(len_v >= 0 && (int64_t)len_v <= (int64_t)T) && p == 0) flag_error(a.status, LSA_ERR_BOUNDS);
-            }
-            const int L = len_v;
-            const bool len_ok = L >= 0 && (int64_t)L <= (int64_t)T;
-            const int64_t se = len_ok ? min(a.sink, L) : 0;
-            const int64_t rs = len_ok ? max((int64_t)L - a.recent, se) : 0;
-            const int nfull_tok = len_ok ? (L / b) * b : 0;
-            return tok < nfull_tok && pq_block_candidate(tok / b, b, se, rs);
-        };
-        auto codes_ptr = [&](int pg, int tok) {
-            return reinterpret_cast<const uint4 *>(a.codes + ((int64_t)pg * b + tok % b) * 32);
-        };
-        // a two-stage prefetch: while tile i decodes, the codes of tile i + 1
-        // (its page id is here) and the page id of tile i + 2 load
-        int r0 = 0, tok = 0, r1 = 0, tok1 = 0, r2 = 0, tok2 = 0;
-        uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
-        bool v = ntiles > 0 && token_of(0, r0, tok);
-        if (v) {
-            const int pg = a.pt[(int64_t)r0 * a.max_blocks + tok / b];
-            v = pg >= 0 && pg < a.ic.num_pages;
-            if (!v) flag_error(a.status, LSA_ERR_BOUNDS);
+    // this thread's token of tile i and whether it is scored (the request's
+    // length is read once per request)
+    int len_r = -1, len_v = 0;
+    auto token_of = [&](int i, int &r, int &tok) -> bool {
+        const int tile = tile_of(i);
+        r = tile / tpr;
+        tok = (tile - r * tpr) * kPsTok + p;
+        if (r != len_r) {
+            len_r = r;
+            len_v = a.lens[r];
+            if (!(len_v >= 0 && (int64_t)len_v <= (int64_t)T) && p == 0) flag_error(a.status, LSA_ERR_BOUNDS);
+        }
+        const int L = len_v;
+        const bool len_ok = L >= 0 && (int64_t)L <= (int64_t)T;
+        const int64_t se = len_ok ? min(a.sink, L) : 0;
+        const int64_t rs = len_ok ? max((int64_t)L - a.recent, se) : 0;
+        const int nfull_tok = len_ok ? (L / b) * b : 0;
+        return tok < nfull_tok && pq_block_candidate(tok / b, b, se, rs);
+    };
+    auto codes_ptr = [&](int pg, int tok) {
+        return reinterpret_cast<const uint4 *>(a.codes + ((int64_t)pg * b + tok % b) * 32);
+    };
+    // the query tile and head weights of request r into slot `slot` (the
+    // products that read that slot before are done when this is called)
+    auto load_q = [&](int r, int slot) {
+        const uint8_t *qg = reinterpret_cast<const uint8_t *>(a.q + (int64_t)r * a.hq * 128);
+        const int j = tid & 7;
+        for (int task = tid >> 3; task < 2 * kPsHeads; task += kPsThreads / 8) {
+            const int cc = task >> 6, g = task & (kPsHeads - 1);
+            cp_async16(sbase + LY::QS + (2 * slot + cc) * LY::QCOL + atom_offset(g, j),
+                       qg + (int64_t)g * 256 + cc * 128 + j * 16);
+        }
+        cp_async_commit();
+        if (tid < kPsHeads) w_s[slot * kPsHeads + tid] = a.weights[(int64_t)r * a.hq + tid];
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+    };
+
+    // a two-stage prefetch: while tile i decodes, the codes of tile i + 1
+    // (its page id is here) and the page id of tile i + 2 load
+    int r0 = 0, tok = 0, r1 = 0, tok1 = 0, r2 = 0, tok2 = 0;
+    uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
+    bool v = ntiles > 0 && token_of(0, r0, tok);
+    if (v) {
+        const int pg = a.pt[(int64_t)r0 * a.max_blocks + tok / b];
+        v = pg >= 0 && pg < a.ic.num_pages;
+        if (!v) flag_error(a.status, LSA_ERR_BOUNDS);
+        else {
+            c0 = codes_ptr(pg, tok)[0];
+            c1 = codes_ptr(pg, tok)[1];
+        }
+    }
+    bool v1 = ntiles > 1 && token_of(1, r1, tok1);
+    int pg1 = v1 ? a.pt[(int64_t)r1 * a.max_blocks + tok1 / b] : -1;
+
+    // the epilogue of tile i: this thread's token's weighted ReLU of its 64
+    // dots, the row's score extremes, the score out
+    int cur = -1;
+    uint32_t kmax = 0u, kmin = 0xffffffffu;
+    int q_req[2] = {-1, -1};   // request of each query slot
+    int slot_of[2] = {0, 0};   // query slot of the tile in each accumulator
+    int tok_of[2] = {-1, -1};  // this thread's token (-1: not scored) of each accumulator
+    int req_of[2] = {0, 0};
+    int issued[2] = {-1, -1};
+    int slot = 0;
+    bool ok = true;
+    auto epilogue = [&](int i) -> bool {
+        const int buf = i & 1;
+        if (!consumer_all(mbar_wait(&mma[buf], (i >> 1) & 1, a.status, a.spin_budget))) return false;
+        tc_fence_after();
+        float d[32];
+        float s = 0.f;
+        const float *ws = w_s + slot_of[buf] * kPsHeads;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            tmem_ld32(tmem + lane_base + LY::TD + 64 * buf + 32 * half, d);
+#pragma unroll
+            for (int g = 0; g < 32; ++g) s = fmaf(ws[32 * half + g], fmaxf(d[g], 0.f), s);
+        }
+        const int r = req_of[buf];
+        if (r != cur) {
+            if (cur >= 0) pq_flush_ext(a.row_ext, cur, kmax, kmin);
+            kmax = 0u;
+            kmin = 0xffffffffu;
+            cur = r;
+        }
+        const bool valid = tok_of[buf] >= 0;
+        if (valid) {
+            if (isnan(s)) flag_error(a.status, LSA_ERR_NAN);
             else {
-                c0 = codes_ptr(pg, tok)[0];
-                c1 = codes_ptr(pg, tok)[1];
+                const uint32_t key = float_to_key(s);
+                kmax = max(kmax, key);
+                kmin = min(kmin, key);
             }
         }
-        bool v1 = ntiles > 1 && token_of(1, r1, tok1);
-        int pg1 = v1 ? a.pt[(int64_t)r1 * a.max_blocks + tok1 / b] : -1;
-        for (int i = 0; i < ntiles && ok; ++i) {
-            // codes of tile i + 1, page id of tile i + 2: issued now, used later
-            uint4 n0 = make_uint4(0u, 0u, 0u, 0u), n1 = n0;
-            const bool v1ok = v1 && pg1 >= 0 && pg1 < a.ic.num_pages;
-            if (v1 && !v1ok) flag_error(a.status, LSA_ERR_BOUNDS);
-            if (v1ok) {
-                n0 = codes_ptr(pg1, tok1)[0];
-                n1 = codes_ptr(pg1, tok1)[1];
-            }
-            const bool v2 = i + 2 < ntiles && token_of(i + 2, r2, tok2);
-            const int pg2 = v2 ? a.pt[(int64_t)r2 * a.max_blocks + tok2 / b] : -1;
-            const int buf = i & 1;
-            if (i >= 2) {
-                // buffer b's previous product (tile i - 2) is done
-                ok = mbar_wait(&mma[buf], ((i - 2) >> 1) & 1, a.status, a.spin_budget);
-                if (!ok) break;
-            }
-            if (v) {
-                const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-                uint8_t *kt = smem + LY::KS + buf * 2 * LY::COL;
+        const int tok_row = (tile_of(i) - r * tpr) * kPsTok + p;
+        if (tok_row < T) a.coarse[(int64_t)r * T + tok_row] = valid && !isnan(s) ? s : -INFINITY;
+        return true;
+    };
+
+    for (int i = 0; i < ntiles && ok; ++i) {
+        const int buf = i & 1;
+        const int r = tile_of(i) / tpr;
+        // this thread's key row of tile i, two bf16 a word, dims in order
+        uint32_t row[64];
+        {
+            const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-                for (int jj = 0; jj < 32; jj += 2) {
-                    const uint32_t ca = (cw[jj >> 2] >> (8 * (jj & 3))) & 0xffu;
-                    const uint32_t cb = (cw[(jj + 1) >> 2] >> (8 * ((jj + 1) & 3))) & 0xffu;
-                    const uint2 ea = *reinterpret_cast<const uint2 *>(smem + LY::CB + (jj * 256 + ca) * 8);
-                    const uint2 eb = *reinterpret_cast<const uint2 *>(smem + LY::CB + ((jj + 1) * 256 + cb) * 8);
-                    *reinterpret_cast<uint4 *>(kt + (jj >> 4) * LY::COL + atom_offset(p, (jj & 15) >> 1)) =
-                        make_uint4(ea.x, ea.y, eb.x, eb.y);
-                }
+            for (int jj = 0; jj < 32; ++jj) {
+                const uint32_t cj = (cw[jj >> 2] >> (8 * (jj & 3))) & 0xffu;
+                const uint2 e = v ? *reinterpret_cast<const uint2 *>(smem + LY::CB + (jj * 256 + cj) * 8)
+                                  : make_uint2(0u, 0u);
+                row[2 * jj] = e.x;
+                row[2 * jj + 1] = e.y;
             }
-            vtok[buf * kPsTok + p] = v ? tok : -1;
-            fence_proxy_async_smem();
-            mbar_arrive(&full[buf]);
-            v = v1ok;
-            tok = tok1;
-            c0 = n0;
-            c1 = n1;
-            v1 = v2;
-            r1 = r2;
-            tok1 = tok2;
-            pg1 = pg2;
         }
-    } else {
-        // ---------------- consumers: warp w reads TMEM lane quadrant w
-        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-        int cur = -1;
-        uint32_t kmax = 0u, kmin = 0xffffffffu;
-        // the query tile and head weights of request r (every product that
-        // reads the previous ones is done when this is called)
-        auto load_q = [&](int r, int slot) {
-            const uint8_t *qg = reinterpret_cast<const uint8_t *>(a.q + (int64_t)r * a.hq * 128);
-            const int j = tid & 7;
-            for (int task = tid >> 3; task < 2 * kPsHeads; task += kPsConsumers / 8) {
-                const int cc = task >> 6, g = task & (kPsHeads - 1);
-                cp_async16(sbase + LY::QS + cc * LY::QCOL + atom_offset(g, j), qg + (int64_t)g * 256 + cc * 128 + j * 16);
-            }
-            cp_async_commit();
-            if (tid < kPsHeads)
-                reinterpret_cast<float *>(smem + LY::W)[slot * kPsHeads + tid] = a.weights[(int64_t)r * a.hq + tid];
-            cp_async_wait<0>();
-            fence_proxy_async_smem();
-            consumer_sync();
-        };
-        // product of tile i into accumulator i & 1, once its keys are in;
-        // each thread takes its key row's token first (the producers write
-        // the next tile's over it once this product is done)
-        int issued[2] = {-1, -1};
-        int tok_of[2] = {-1, -1};
-        auto issue = [&](int i) -> bool {
-            const int buf = i & 1;
-            if (!consumer_all(mbar_wait(&full[buf], (i >> 1) & 1, a.status, a.spin_budget))) return false;
-            tok_of[buf] = vtok[buf * kPsTok + tid];
-            consumer_sync();
-            tc_fence_after();
-            issued[buf] = i;
-            if (tid == 0) {
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-#pragma unroll
-                    for (int s = 0; s < 4; ++s) {
-                        const uint64_t ad =
-                            umma_desc_sw128(sbase + LY::KS + (2 * buf + cc) * LY::COL + s * 32, 16, 1024);
-                        const uint64_t bd = umma_desc_sw128(sbase + LY::QS + cc * LY::QCOL + s * 32, 16, 1024);
-                        umma_bf16(tmem + 64 * buf, ad, bd, IDESC, cc > 0 || s > 0);
-                    }
-                }
-                umma_commit(&mma[buf]);
-            }
-            return true;
-        };
-        int wslot = 0;      // weights of tile i's request
-        int wslot_n = 0;    // and of tile i + 1's
-        if (ntiles > 0) {
-            cur = tile_of(0) / tpr;
-            load_q(cur, 0);
-            ok = issue(0);
+        tok_of[buf] = v ? tok : -1;
+        req_of[buf] = r;
+        // codes of tile i + 1, page id of tile i + 2: issued now, used later
+        uint4 n0 = make_uint4(0u, 0u, 0u, 0u), n1 = n0;
+        const bool v1ok = v1 && pg1 >= 0 && pg1 < a.ic.num_pages;
+        if (v1 && !v1ok) flag_error(a.status, LSA_ERR_BOUNDS);
+        if (v1ok) {
+            n0 = codes_ptr(pg1, tok1)[0];
+            n1 = codes_ptr(pg1, tok1)[1];
         }
-        for (int i = 0; i < ntiles && ok; ++i) {
-            const int buf = i & 1;
-            const int r = tile_of(i) / tpr;
-            // the next tile's product: the request's query tile stays until
-            // this tile's product is done
-            if (i + 1 < ntiles) {
-                const int rn = tile_of(i + 1) / tpr;
-                wslot_n = wslot;
-                if (rn != r) {
-                    ok = consumer_all(mbar_wait(&mma[buf], (i >> 1) & 1, a.status, a.spin_budget));
-                    if (!ok) break;
-                    wslot_n = wslot ^ 1;   // tile i's weights stay for its scores below
-                    load_q(rn, wslot_n);
-                }
-                tc_fence_before();
-                consumer_sync();   // accumulator (i + 1) & 1 was read (tile i - 1) before it is written
-                ok = issue(i + 1);
-                if (!ok) break;
-            }
-            ok = consumer_all(mbar_wait(&mma[buf], (i >> 1) & 1, a.status, a.spin_budget));
+        const bool v2 = i + 2 < ntiles && token_of(i + 2, r2, tok2);
+        const int pg2 = v2 ? a.pt[(int64_t)r2 * a.max_blocks + tok2 / b] : -1;
+        // A buffer and accumulator `buf` are free once tile i - 2's product
+        // is done (its accumulator was read in the previous iteration)
+        if (i >= 2) {
+            ok = consumer_all(mbar_wait(&mma[buf], ((i - 2) >> 1) & 1, a.status, a.spin_budget));
             if (!ok) break;
+        }
+        if (r != q_req[slot]) {
+            // a new request: its query tile goes to the other slot, whose
+            // last reader (tile i - 2 at the latest) is done
+            slot ^= 1;
+            load_q(r, slot);
+            q_req[slot] = r;
+        }
+        slot_of[buf] = slot;
+        tmem_st32(tmem + lane_base + LY::TA + 64 * buf, *reinterpret_cast<const uint32_t(*)[32]>(row));
+        tmem_st32(tmem + lane_base + LY::TA + 64 * buf + 32, *reinterpret_cast<const uint32_t(*)[32]>(row + 32));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncthreads();   // the tile's A rows and query tile are in place
+        if (tid == 0) {
             tc_fence_after();
-            // ---- this thread's token: the weighted ReLU of its 64 dots
-            const int tok = tok_of[buf];
-            float d[32];
-            float s = 0.f;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                tmem_ld32(tmem + lane_base + 64 * buf + 32 * half, d);
-#pragma unroll
-                for (int g = 0; g < 32; ++g) s = fmaf(w_s[wslot * kPsHeads + 32 * half + g], fmaxf(d[g], 0.f), s);
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t bd =
+                    umma_desc_sw128(sbase + LY::QS + (2 * slot + (ks >> 2)) * LY::QCOL + (ks & 3) * 32, 16, 1024);
+                umma_bf16_ta(tmem + LY::TD + 64 * buf, tmem + LY::TA + 64 * buf + 8 * ks, bd, IDESC, ks > 0);
             }
-            wslot = wslot_n;
-            if (r != cur) {
-                pq_flush_ext(a.row_ext, cur, kmax, kmin);
-                kmax = 0u;
-                kmin = 0xffffffffu;
-                cur = r;
-            }
-            const bool valid = tok >= 0;
-            if (valid) {
-                if (isnan(s)) flag_error(a.status, LSA_ERR_NAN);
-                else {
-                    const uint32_t key = float_to_key(s);
-                    kmax = max(kmax, key);
-                    kmin = min(kmin, key);
-                }
-            }
-            const int tok_row = (tile_of(i) - r * tpr) * kPsTok + tid;
-            if (tok_row < T) a.coarse[(int64_t)r * T + tok_row] = valid && !isnan(s) ? s : -INFINITY;
+            umma_commit(&mma[buf]);
         }
-        if (cur >= 0) pq_flush_ext(a.row_ext, cur, kmax, kmin);
-        if (!ok) {
-            // a wait gave up: wait (bounded) for the products issued before
-            // the tensor memory is freed
-            for (int bb = 0; bb < 2; ++bb)
-                if (issued[bb] >= 0) mbar_wait(&mma[bb], (issued[bb] >> 1) & 1, nullptr, a.spin_budget);
+        issued[buf] = i;
+        // while it runs, the previous tile's scores
+        if (i >= 1) {
+            ok = epilogue(i - 1);
+            if (!ok) break;
         }
+        v = v1ok;
+        tok = tok1;
+        c0 = n0;
+        c1 = n1;
+        v1 = v2;
+        r1 = r2;
+        tok1 = tok2;
+        pg1 = pg2;
+    }
+    if (ok && ntiles > 0) ok = epilogue(ntiles - 1);
+    if (cur >= 0) pq_flush_ext(a.row_ext, cur, kmax, kmin);
+    if (!ok) {
+        // a wait gave up: wait (bounded) for the products issued before the
+        // tensor memory is freed
+        for (int bb = 0; bb < 2; ++bb)
+            if (issued[bb] >= 0) mbar_wait(&mma[bb], (issued[bb] >> 1) & 1, nullptr, a.spin_budget);
     }
     tc_fence_before();
     __syncthreads();
@@ -1083,7 +1053,7 @@ cudaError_t launch_pq_scores(const PqArgs &a, cudaStream_t s, bool *unsupported)
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t tiles = (int64_t)a.batch * ((a.max_blocks * a.ic.b + kPsTok - 1) / kPsTok);
-    const int grid = (int)std::min<int64_t>(tiles, (int64_t)sms);
+    const int grid = (int)std::min<int64_t>(tiles, (int64_t)kPsCtasPerSm * sms);
     e = launch_step_kernel(k_pq_scores, dim3(grid), dim3(kPsThreads), (size_t)PsLayout::SMEM, s, a);
     if (e != cudaSuccess) return e;
     if (!a.hist) return cudaGetLastError();   // scores only
