@@ -422,6 +422,12 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
 }
 
 // cp_async16 with an L2 cache policy (l2_evict_first for bulk streams).
+// 4-byte cp.async (L1-allocating form): dst and src 4-byte aligned.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
 __device__ __forceinline__ void cp_async16_policy(uint32_t dst, const void *src, uint64_t pol)
 {
     asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)

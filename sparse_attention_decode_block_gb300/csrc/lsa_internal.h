@@ -174,6 +174,7 @@ struct PqArgs {
     uint32_t *status;
     long long spin_budget;
     uint8_t *codes_out;         // encoding: [num_pages, 1, b, 32]
+    FastDiv fd_b, fd_tpr;       // coarse scores: block size, 128-token tiles per request
 };
 
 constexpr int kPqBins = 2048;

@@ -129,9 +129,12 @@ struct PsLayout {
     static constexpr int CB = 0;                          // codebook, bf16 [32][256][4]
     static constexpr int QCOL = (kPsHeads / 8) * 1024;    // one 64-dim atom column of a query tile
     static constexpr int QS = 32 * 256 * 8;               // query tiles: 2 slots x 2 atom columns
-    static constexpr int W = QS + 4 * QCOL;               // [2][64] fp32 head weights, one slot per query tile
-    static constexpr int BAR = W + 2 * kPsHeads * 4;      // mma[2], TMEM base address
-    static constexpr int SMEM = BAR + 32;
+    static constexpr int CRING = 3;                       // codes in flight: tiles i, i + 1, i + 2
+    static constexpr int PRING = 4;                       // page ids: tiles i + 2, i + 3 (and two spare)
+    static constexpr int CODES = QS + 4 * QCOL;           // [CRING][128 threads] 32 bytes of codes
+    static constexpr int PGS = CODES + CRING * kPsThreads * 32;  // [PRING][128 threads] page ids
+    static constexpr int BAR = PGS + PRING * kPsThreads * 4;     // mma[2], stored[2], TMEM base address
+    static constexpr int SMEM = BAR + 48;
     static constexpr int TA = 0;                          // TMEM columns: A buffers 2 x 64 (128 dims, two a column)
     static constexpr int TD = 128;                        // accumulators 2 x 64 (64 heads)
     static constexpr int TCOLS = 256;
@@ -158,10 +161,6 @@ __device__ __forceinline__ void pq_flush_ext(uint32_t *row_ext, int r, uint32_t 
     }
 }
 
-// CTA barrier that returns whether `ok` holds in every thread (a wait that
-// gave up in one thread ends the loop in every one, so no thread is left at
-// a barrier the others never reach).
-__device__ __forceinline__ bool consumer_all(bool ok) { return __syncthreads_and(ok ? 1 : 0) != 0; }
 
 __global__ void __launch_bounds__(kPsThreads, kPsCtasPerSm) k_pq_scores(PqArgs a)
 {
@@ -174,9 +173,9 @@ __global__ void __launch_bounds__(kPsThreads, kPsCtasPerSm) k_pq_scores(PqArgs a
         if (tid == 0) flag_error(a.status, LSA_ERR_INVALID_ARG);
         return;
     }
-    uint64_t *mma = reinterpret_cast<uint64_t *>(smem + LY::BAR);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + LY::BAR + 16);
-    float *w_s = reinterpret_cast<float *>(smem + LY::W);
+    uint64_t *mma = reinterpret_cast<uint64_t *>(smem + LY::BAR);   // product of buffer b done
+    uint64_t *stored = mma + 2;                                        // buffer b's rows (and query tile) in place
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + LY::BAR + 32);
     const uint32_t sbase = smem_addr(smem);
     if (warp == 0) {
         tmem_alloc(tslot, LY::TCOLS);
@@ -185,6 +184,8 @@ __global__ void __launch_bounds__(kPsThreads, kPsCtasPerSm) k_pq_scores(PqArgs a
     if (tid == 0) {
         mbar_init(&mma[0], 1);
         mbar_init(&mma[1], 1);
+        mbar_init(&stored[0], kPsThreads);
+        mbar_init(&stored[1], kPsThreads);
         fence_barrier_init();
     }
     // the codebook, once per CTA
@@ -211,7 +212,7 @@ __global__ void __launch_bounds__(kPsThreads, kPsCtasPerSm) k_pq_scores(PqArgs a
     int len_r = -1, len_v = 0;
     auto token_of = [&](int i, int &r, int &tok) -> bool {
         const int tile = tile_of(i);
-        r = tile / tpr;
+        r = (int)fdiv((uint32_t)tile, a.fd_tpr);
         tok = (tile - r * tpr) * kPsTok + p;
         if (r != len_r) {
             len_r = r;
@@ -222,77 +223,107 @@ __global__ void __launch_bounds__(kPsThreads, kPsCtasPerSm) k_pq_scores(PqArgs a
         const bool len_ok = L >= 0 && (int64_t)L <= (int64_t)T;
         const int64_t se = len_ok ? min(a.sink, L) : 0;
         const int64_t rs = len_ok ? max((int64_t)L - a.recent, se) : 0;
-        const int nfull_tok = len_ok ? (L / b) * b : 0;
-        return tok < nfull_tok && pq_block_candidate(tok / b, b, se, rs);
+        const int nfull_tok = len_ok ? (int)fdiv((uint32_t)L, a.fd_b) * b : 0;
+        return tok < nfull_tok && pq_block_candidate(fdiv((uint32_t)tok, a.fd_b), b, se, rs);
     };
-    auto codes_ptr = [&](int pg, int tok) {
-        return reinterpret_cast<const uint4 *>(a.codes + ((int64_t)pg * b + tok % b) * 32);
+
+    // this thread's prefetch ring (its own slots, so no barrier): the page
+    // id of tile i + 3 and the codes of tile i + 2 are requested while tile
+    // i decodes, by cp.async, so that no register waits on a load; stage
+    // s % CRING (codes) and s % PRING (page ids) belong to tile s.  A tile whose token is not
+    // scored (or whose page id is bad) loads nothing and decodes zeros.
+    const uint32_t ring_codes = sbase + LY::CODES + p * 32;
+    const uint32_t ring_pg = sbase + LY::PGS + p * 4;
+    const int *pg_s = reinterpret_cast<const int *>(smem + LY::PGS) + p;
+    auto codes_at = [&](int i) -> const uint4 * {
+        return reinterpret_cast<const uint4 *>(smem + LY::CODES + ((i % LY::CRING) * kPsThreads + p) * 32);
     };
-    // the query tile and head weights of request r into slot `slot` (the
-    // products that read that slot before are done when this is called)
-    auto load_q = [&](int r, int slot) {
-        const uint8_t *qg = reinterpret_cast<const uint8_t *>(a.q + (int64_t)r * a.hq * 128);
-        const int j = tid & 7;
-        for (int task = tid >> 3; task < 2 * kPsHeads; task += kPsThreads / 8) {
-            const int cc = task >> 6, g = task & (kPsHeads - 1);
-            cp_async16(sbase + LY::QS + (2 * slot + cc) * LY::QCOL + atom_offset(g, j),
-                       qg + (int64_t)g * 256 + cc * 128 + j * 16);
+    auto request_pg = [&](int i, bool scored, int r, int tk) {   // page id of tile i's token
+        if (scored)
+            cp_async4(ring_pg + (i % LY::PRING) * kPsThreads * 4,
+                      a.pt + (int64_t)r * a.max_blocks + fdiv((uint32_t)tk, a.fd_b));
+        cp_async_commit();
+    };
+    auto request_codes = [&](int i, bool &scored, int tk) {      // codes of tile i's token, its page id in place
+        if (scored) {
+            const int pg = pg_s[(i % LY::PRING) * kPsThreads];
+            if (pg < 0 || pg >= a.ic.num_pages) {
+                flag_error(a.status, LSA_ERR_BOUNDS);
+                scored = false;
+            } else {
+                const uint8_t *src = a.codes + ((int64_t)pg * b + (tk - (int)fdiv((uint32_t)tk, a.fd_b) * b)) * 32;
+                const uint32_t dst = ring_codes + (i % LY::CRING) * kPsThreads * 32;
+                cp_async16(dst, src);
+                cp_async16(dst + 16, src + 16);
+            }
         }
         cp_async_commit();
-        if (tid < kPsHeads) w_s[slot * kPsHeads + tid] = a.weights[(int64_t)r * a.hq + tid];
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
     };
-
-    // a two-stage prefetch: while tile i decodes, the codes of tile i + 1
-    // (its page id is here) and the page id of tile i + 2 load
-    int r0 = 0, tok = 0, r1 = 0, tok1 = 0, r2 = 0, tok2 = 0;
-    uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
-    bool v = ntiles > 0 && token_of(0, r0, tok);
-    if (v) {
-        const int pg = a.pt[(int64_t)r0 * a.max_blocks + tok / b];
-        v = pg >= 0 && pg < a.ic.num_pages;
-        if (!v) flag_error(a.status, LSA_ERR_BOUNDS);
-        else {
-            c0 = codes_ptr(pg, tok)[0];
-            c1 = codes_ptr(pg, tok)[1];
-        }
+    // tiles 0 .. 2: page ids of 0, 1, 2, then the codes of 0 and 1
+    int rq[3] = {0, 0, 0}, tq[3] = {0, 0, 0};
+    bool vq[3] = {false, false, false};
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        vq[k] = k < ntiles && token_of(k, rq[k], tq[k]);
+        request_pg(k, vq[k], rq[k], tq[k]);
     }
-    bool v1 = ntiles > 1 && token_of(1, r1, tok1);
-    int pg1 = v1 ? a.pt[(int64_t)r1 * a.max_blocks + tok1 / b] : -1;
+    cp_async_wait<0>();
+    request_codes(0, vq[0], tq[0]);
+    request_codes(1, vq[1], tq[1]);
+    // the ring's state entering iteration i: tile i's and i+1's codes are
+    // requested (validity v, v1), tile i+2's page id is requested (v2)
+    bool v = vq[0], v1 = vq[1], v2 = vq[2];
+    int tok = tq[0], tok1 = tq[1], tok2 = tq[2];
 
-    // the epilogue of tile i: this thread's token's weighted ReLU of its 64
-    // dots, the row's score extremes, the score out
-    int cur = -1;
+    // No CTA barrier inside the loop, so that the warps drift apart and one
+    // warp's codebook lookups overlap another's epilogue: a thread arrives
+    // on stored[b] once its rows (and its part of a new query tile) are in
+    // place, warp 0 waits for all of them and issues the product, and every
+    // thread waits for the product's commit itself.  The request's head
+    // weights live in each thread's registers.  A wait that gives up ends
+    // the thread's loop; the others' waits then give up as well.
+    int cur = -1;                // request of the weights in registers and of the row extremes
+    float wreg[kPsHeads];
     uint32_t kmax = 0u, kmin = 0xffffffffu;
-    int q_req[2] = {-1, -1};   // request of each query slot
-    int slot_of[2] = {0, 0};   // query slot of the tile in each accumulator
-    int tok_of[2] = {-1, -1};  // this thread's token (-1: not scored) of each accumulator
-    int req_of[2] = {0, 0};
-    int issued[2] = {-1, -1};
+    int q_req0 = -1, q_req1 = -1;   // request of each query slot
     int slot = 0;
+    int tokA = -1, tokB = -1;      // this thread's token (-1: not scored) of the tile in each accumulator
+    int reqA = 0, reqB = 0;
+    int issued0 = -1, issued1 = -1;
     bool ok = true;
     auto epilogue = [&](int i) -> bool {
         const int buf = i & 1;
-        if (!consumer_all(mbar_wait(&mma[buf], (i >> 1) & 1, a.status, a.spin_budget))) return false;
+        if (!mbar_wait(&mma[buf], (i >> 1) & 1, a.status, a.spin_budget)) return false;
         tc_fence_after();
-        float d[32];
-        float s = 0.f;
-        const float *ws = w_s + slot_of[buf] * kPsHeads;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            tmem_ld32(tmem + lane_base + LY::TD + 64 * buf + 32 * half, d);
-#pragma unroll
-            for (int g = 0; g < 32; ++g) s = fmaf(ws[32 * half + g], fmaxf(d[g], 0.f), s);
-        }
-        const int r = req_of[buf];
+        const int r = buf ? reqB : reqA;
+        const int tk = buf ? tokB : tokA;
         if (r != cur) {
             if (cur >= 0) pq_flush_ext(a.row_ext, cur, kmax, kmin);
             kmax = 0u;
             kmin = 0xffffffffu;
             cur = r;
+            const float4 *wr = reinterpret_cast<const float4 *>(a.weights + (int64_t)r * a.hq);
+#pragma unroll
+            for (int g = 0; g < kPsHeads / 4; ++g) {
+                const float4 w4 = __ldg(wr + g);
+                wreg[4 * g] = w4.x;
+                wreg[4 * g + 1] = w4.y;
+                wreg[4 * g + 2] = w4.z;
+                wreg[4 * g + 3] = w4.w;
+            }
         }
-        const bool valid = tok_of[buf] >= 0;
+        float d[32];
+        float2 s2 = make_float2(0.f, 0.f);   // even and odd heads, added at the end
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            tmem_ld32(tmem + lane_base + LY::TD + 64 * buf + 32 * half, d);
+#pragma unroll
+            for (int g = 0; g < 32; g += 2)
+                s2 = __ffma2_rn(make_float2(wreg[32 * half + g], wreg[32 * half + g + 1]),
+                                make_float2(fmaxf(d[g], 0.f), fmaxf(d[g + 1], 0.f)), s2);
+        }
+        const float s = s2.x + s2.y;
+        const bool valid = tk >= 0;
         if (valid) {
             if (isnan(s)) flag_error(a.status, LSA_ERR_NAN);
             else {
@@ -308,83 +339,108 @@ __global__ void __launch_bounds__(kPsThreads, kPsCtasPerSm) k_pq_scores(PqArgs a
 
     for (int i = 0; i < ntiles && ok; ++i) {
         const int buf = i & 1;
-        const int r = tile_of(i) / tpr;
+        const int r = (int)fdiv((uint32_t)tile_of(i), a.fd_tpr);
         // this thread's key row of tile i, two bf16 a word, dims in order
         uint32_t row[64];
         {
+            // groups committed so far: ..., codes i, [page i+2 | codes i+1]; all
+            // but the last (codes i+1) are complete after this wait
+            cp_async_wait<1>();
+            const uint4 c0 = codes_at(i)[0], c1 = codes_at(i)[1];
             const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
-                const uint32_t cj = (cw[jj >> 2] >> (8 * (jj & 3))) & 0xffu;
+                const uint32_t cj = __byte_perm(cw[jj >> 2], 0u, 0x4440u | (uint32_t)(jj & 3));
                 const uint2 e = v ? *reinterpret_cast<const uint2 *>(smem + LY::CB + (jj * 256 + cj) * 8)
                                   : make_uint2(0u, 0u);
                 row[2 * jj] = e.x;
                 row[2 * jj + 1] = e.y;
             }
         }
-        tok_of[buf] = v ? tok : -1;
-        req_of[buf] = r;
-        // codes of tile i + 1, page id of tile i + 2: issued now, used later
-        uint4 n0 = make_uint4(0u, 0u, 0u, 0u), n1 = n0;
-        const bool v1ok = v1 && pg1 >= 0 && pg1 < a.ic.num_pages;
-        if (v1 && !v1ok) flag_error(a.status, LSA_ERR_BOUNDS);
-        if (v1ok) {
-            n0 = codes_ptr(pg1, tok1)[0];
-            n1 = codes_ptr(pg1, tok1)[1];
+        if (buf) {
+            tokB = v ? tok : -1;
+            reqB = r;
+        } else {
+            tokA = v ? tok : -1;
+            reqA = r;
         }
-        const bool v2 = i + 2 < ntiles && token_of(i + 2, r2, tok2);
-        const int pg2 = v2 ? a.pt[(int64_t)r2 * a.max_blocks + tok2 / b] : -1;
+        // page id of tile i + 3, codes of tile i + 2 (its page id is in:
+        // requested two groups ago)
+        int r3 = 0, tok3 = 0;
+        const bool v3 = i + 3 < ntiles && token_of(i + 3, r3, tok3);
+        request_pg(i + 3, v3, r3, tok3);
+        bool v2c = v2;
+        request_codes(i + 2, v2c, tok2);
         // A buffer and accumulator `buf` are free once tile i - 2's product
-        // is done (its accumulator was read in the previous iteration)
-        if (i >= 2) {
-            ok = consumer_all(mbar_wait(&mma[buf], ((i - 2) >> 1) & 1, a.status, a.spin_budget));
-            if (!ok) break;
+        // is done (this thread read that accumulator in the last iteration)
+        if (i >= 2 && !mbar_wait(&mma[buf], ((i - 2) >> 1) & 1, a.status, a.spin_budget)) {
+            ok = false;
+            break;
         }
-        if (r != q_req[slot]) {
-            // a new request: its query tile goes to the other slot, whose
-            // last reader (tile i - 2 at the latest) is done
+        const int q_cur = slot ? q_req1 : q_req0;
+        if (r != q_cur) {
+            // a new request: its query tile goes to the other slot, whose last
+            // reader (tile i - 2 at the latest) is done; this thread's part
+            // of it is in place before the thread arrives below
             slot ^= 1;
-            load_q(r, slot);
-            q_req[slot] = r;
+            if (slot) q_req1 = r;
+            else q_req0 = r;
+            const uint8_t *qg = reinterpret_cast<const uint8_t *>(a.q + (int64_t)r * a.hq * 128);
+            const int j = tid & 7;
+            for (int task = tid >> 3; task < 2 * kPsHeads; task += kPsThreads / 8) {
+                const int cc = task >> 6, g = task & (kPsHeads - 1);
+                cp_async16(sbase + LY::QS + (2 * slot + cc) * LY::QCOL + atom_offset(g, j),
+                           qg + (int64_t)g * 256 + cc * 128 + j * 16);
+            }
+            cp_async_commit();
+            cp_async_wait<0>();
+            fence_proxy_async_smem();
         }
-        slot_of[buf] = slot;
         tmem_st32(tmem + lane_base + LY::TA + 64 * buf, *reinterpret_cast<const uint32_t(*)[32]>(row));
         tmem_st32(tmem + lane_base + LY::TA + 64 * buf + 32, *reinterpret_cast<const uint32_t(*)[32]>(row + 32));
         tmem_st_wait();
         tc_fence_before();
-        __syncthreads();   // the tile's A rows and query tile are in place
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t bd =
-                    umma_desc_sw128(sbase + LY::QS + (2 * slot + (ks >> 2)) * LY::QCOL + (ks & 3) * 32, 16, 1024);
-                umma_bf16_ta(tmem + LY::TD + 64 * buf, tmem + LY::TA + 64 * buf + 8 * ks, bd, IDESC, ks > 0);
+        mbar_arrive(&stored[buf]);
+        if (warp == 0) {
+            // the tile's product, once every thread's rows are in place
+            if (!mbar_wait(&stored[buf], (i >> 1) & 1, a.status, a.spin_budget)) {
+                ok = false;
+                break;
             }
-            umma_commit(&mma[buf]);
+            if (tid == 0) {
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t bd =
+                        umma_desc_sw128(sbase + LY::QS + (2 * slot + (ks >> 2)) * LY::QCOL + (ks & 3) * 32, 16, 1024);
+                    umma_bf16_ta(tmem + LY::TD + 64 * buf, tmem + LY::TA + 64 * buf + 8 * ks, bd, IDESC, ks > 0);
+                }
+                umma_commit(&mma[buf]);
+            }
+            __syncwarp();
         }
-        issued[buf] = i;
+        if (buf) issued1 = i;
+        else issued0 = i;
         // while it runs, the previous tile's scores
-        if (i >= 1) {
-            ok = epilogue(i - 1);
-            if (!ok) break;
+        if (i >= 1 && !epilogue(i - 1)) {
+            ok = false;
+            break;
         }
-        v = v1ok;
+        v = v1;
         tok = tok1;
-        c0 = n0;
-        c1 = n1;
-        v1 = v2;
-        r1 = r2;
+        v1 = v2c;
         tok1 = tok2;
-        pg1 = pg2;
+        v2 = v3;
+        tok2 = tok3;
     }
+    cp_async_wait<0>();   // nothing of this thread's ring is left in flight
     if (ok && ntiles > 0) ok = epilogue(ntiles - 1);
     if (cur >= 0) pq_flush_ext(a.row_ext, cur, kmax, kmin);
     if (!ok) {
         // a wait gave up: wait (bounded) for the products issued before the
         // tensor memory is freed
-        for (int bb = 0; bb < 2; ++bb)
-            if (issued[bb] >= 0) mbar_wait(&mma[bb], (issued[bb] >> 1) & 1, nullptr, a.spin_budget);
+        if (issued0 >= 0) mbar_wait(&mma[0], (issued0 >> 1) & 1, nullptr, a.spin_budget);
+        if (issued1 >= 0) mbar_wait(&mma[1], (issued1 >> 1) & 1, nullptr, a.spin_budget);
     }
     tc_fence_before();
     __syncthreads();
@@ -1054,7 +1110,10 @@ cudaError_t launch_pq_scores(const PqArgs &a, cudaStream_t s, bool *unsupported)
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t tiles = (int64_t)a.batch * ((a.max_blocks * a.ic.b + kPsTok - 1) / kPsTok);
     const int grid = (int)std::min<int64_t>(tiles, (int64_t)kPsCtasPerSm * sms);
-    e = launch_step_kernel(k_pq_scores, dim3(grid), dim3(kPsThreads), (size_t)PsLayout::SMEM, s, a);
+    PqArgs ka = a;
+    ka.fd_b = make_fastdiv((uint32_t)a.ic.b);
+    ka.fd_tpr = make_fastdiv((uint32_t)((a.max_blocks * a.ic.b + kPsTok - 1) / kPsTok));
+    e = launch_step_kernel(k_pq_scores, dim3(grid), dim3(kPsThreads), (size_t)PsLayout::SMEM, s, ka);
     if (e != cudaSuccess) return e;
     if (!a.hist) return cudaGetLastError();   // scores only
     const int T = a.max_blocks * a.ic.b;
