@@ -186,6 +186,33 @@ def test_pq_scores_within_rounding():
         assert np.all(np.isneginf(coarse[r, rest]))
 
 
+def test_pq_scores_request_changes_every_tile():
+    """Requests of about 150 tiles of 128 tokens each, ragged, so that the
+    scorer's persistent CTAs (tiles strided by the grid) change request at
+    nearly every tile: each change flips the query slot and reloads the head
+    weights, while the prefetch rings run ahead across requests."""
+    w = small("c2f_pq_small", batch=6, seq_lens=(19203, 4100, 17000, 64 * 100 + 3, 12345, 960))
+    cpu = make_inputs(w, "cpu")
+    g = to_dev(cpu)
+    st = GpuStep(w, g)
+    coarse = gpu_coarse(st, w, g)
+    b = w.block_size
+    rng = np.random.default_rng(3)
+    for r in range(w.batch):
+        Lr = int(cpu["seq_lens"][r])
+        nfull = Lr // b
+        se = min(w.sink, Lr)
+        rs = max(Lr - w.recent, se)
+        cand_tok = np.array([t for t in range(nfull * b) if (t // b) * b >= se and (t // b + 1) * b <= rs])
+        if len(cand_tok):
+            check_coarse(w, cpu, coarse, r, np.sort(rng.choice(cand_tok, size=min(400, len(cand_tok)), replace=False)))
+        rest = np.setdiff1d(np.arange(coarse.shape[1]), cand_tok)
+        assert np.all(np.isneginf(coarse[r, rest]))
+    st.run()
+    check_status_clean()
+    check_step(w, cpu, g, st, range(w.batch), coarse)
+
+
 @pytest.mark.parametrize("variant", ["base", "short", "all_hits", "no_hits", "few_candidates"])
 def test_pq_step_stagewise(variant):
     kw = {}
