@@ -524,8 +524,8 @@ struct PqSelLayout {
     static constexpr int CPG = FPG + kFtTok * 4;           // [kFtTok] int32 the candidates' pages
     static constexpr int HIST = CPG + kFtTok * 4;          // [kPqBins] the row's bucket counts
     static constexpr int CKT = HIST + kPqBins * 4;         // [kBkCap] int32 this CTA's boundary tokens
-    static constexpr int DX = CKT + kBkCap * 4;            // [2] fp64 exchange, [kFtWarps] fp64 warp sums
-    static constexpr int SMEM = DX + (2 + kFtWarps) * 8;
+    static constexpr int DX = CKT + kBkCap * 4;            // [4] fp64 exchange slots, [kFtWarps] fp64 warp sums
+    static constexpr int SMEM = DX + (4 + kFtWarps) * 8;
 };
 static_assert(PqSelLayout::SMEM + sizeof(ClusterTopkScratch<kFtThreads, 8>) <= 227 * 1024, "shared memory");
 
@@ -548,29 +548,6 @@ __device__ __forceinline__ double pq_block_dsum(double v, double *ws)
 #pragma unroll
     for (int w = 0; w < kFtWarps; ++w) s += ws[w];
     __syncthreads();
-    return s;
-}
-
-// Sum over the cluster of this CTA's fp64 value v (thread 0's), returned to
-// every thread.  Ends with two CTA barriers; one cluster barrier inside.
-template <int CS>
-__device__ __forceinline__ double pq_cluster_dsum(double *dx, double v)
-{
-    if (threadIdx.x == 0) dx[0] = v;
-    cluster_sync();
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        double x = lane < CS ? ld_cluster_f64(cluster_map(smem_addr(dx), (uint32_t)lane)) : 0.0;
-        // in rank order, so that every CTA adds the same numbers the same way
-        double s = 0.0;
-#pragma unroll
-        for (int c = 0; c < CS; ++c) s += __shfl_sync(0xffffffffu, x, c);
-        if (lane == 0) dx[1] = s;
-    }
-    __syncthreads();
-    const double s = dx[1];
-    __syncthreads();
-    cluster_sync();   // every CTA has read dx[0] before it is reused
     return s;
 }
 
@@ -686,6 +663,9 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
     };
     auto key_of = [](float x) -> uint32_t { return (x == -INFINITY || isnan(x)) ? 0u : float_to_key(x); };
     auto bucket_of = [&](uint32_t k) -> int { return pq_bucket(key_to_float(k), vmin, scale); };
+    // the bucket of a staged score straight from the float, -1 for one that
+    // is not a candidate (-inf or NaN): the same as bucket_of(key_of(x))
+    auto cand_bucket = [&](float x) -> int { return x > -INFINITY ? pq_bucket(x, vmin, scale) : -1; };
     const int nch = (t_hi - t_lo + 3) / 4;   // this thread's chunks inside the row
 
     // the candidate rule, exact in both cases: by bucket (winners above the
@@ -701,11 +681,9 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
             const float xs[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const uint32_t k = key_of(xs[e]);
-                if (k == 0u) continue;
-                const int bk = bucket_of(k);
-                n_a += bk > B1;
-                n_b += bk == B1;
+                const int bk = cand_bucket(xs[e]);
+                n_a += bk >= 0 && bk > B1;
+                n_b += bk >= 0 && bk == B1;
             }
         }
     } else {
@@ -755,9 +733,8 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
             const float xs[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const uint32_t k = key_of(xs[e]);
-                if (k != 0u && bucket_of(k) == B1) {
-                    tsm.ck[pos] = k;
+                if (cand_bucket(xs[e]) == B1) {
+                    tsm.ck[pos] = key_of(xs[e]);
                     ckt[pos] = t_lo + 4 * c + e;
                     ++pos;
                 }
@@ -876,17 +853,19 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
             const float xs[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const uint32_t k = key_of(xs[e]);
-                if (k == 0u) continue;
+                const float x = xs[e];
                 bool take;
                 if (crowded) {
+                    const uint32_t k = key_of(x);
+                    if (k == 0u) continue;
                     if (k > Tk) take = true;
                     else if (k == Tk) {
                         take = (int)bpos < take_eq;
                         ++bpos;
                     } else take = false;
                 } else {
-                    const int bk = bucket_of(k);
+                    const int bk = cand_bucket(x);
+                    if (bk < 0) continue;   // not a candidate
                     if (bk > B1) take = true;
                     else if (bk == B1) {
                         take = tsm.pick[bpos] != 0;
@@ -896,8 +875,10 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
                 if (!take) continue;
                 const int i = t_lo + 4 * c + e;
                 const int owner = (int)pos / CB, slot = (int)pos - owner * CB;
+                // the score as its key maps it back (-0 as +0)
+                const uint32_t xb = __float_as_uint(x) == 0x80000000u ? 0u : __float_as_uint(x);
                 st_cluster_u32(cluster_map(smem_addr(&ctok[slot]), (uint32_t)owner), (uint32_t)i);
-                st_cluster_u32(cluster_map(smem_addr(&csc[slot]), (uint32_t)owner), __float_as_uint(key_to_float(k)));
+                st_cluster_u32(cluster_map(smem_addr(&csc[slot]), (uint32_t)owner), xb);
                 if (cout) cout[pos] = i;
                 ++pos;
             }
@@ -934,30 +915,54 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
         kmin = __reduce_min_sync(0xffffffffu, kmin);
         if ((tid & 31) == 0) tsm.red[tid >> 5][0] = kmin;
         __syncthreads();
+        // the sample standard deviation of the candidates' coarse scores:
+        // the mean, then the sum of squared deviations, in fp64, each summed
+        // in a fixed order (lanes, warps, then the cluster's CTAs in rank
+        // order).  The CTA's sum of scores goes out with its smallest key of
+        // the top k, in one exchange; each exchange has its own slots, so
+        // none waits for the slots to be read
+        double loc = 0.0;
+        for (int i = tid; i < ncb; i += NT) loc += (double)csc[i];
+        const double sx = pq_block_dsum(loc, dx + 4);
         if (tid == 0) {
             uint32_t m = 0xffffffffu;
             for (int w = 0; w < NT / 32; ++w) m = min(m, tsm.red[w][0]);
             tsm.xch[7][0] = ~m;
+            dx[0] = sx;
         }
         cluster_sync();
         if (tid < 32) {
             uint32_t v = tid < CS ? ld_cluster_u32(cluster_map(smem_addr(&tsm.xch[7][0]), (uint32_t)tid)) : 0u;
             v = __reduce_max_sync(0xffffffffu, v);
-            if (tid == 0) s_u[4] = ~v;
+            const double x = tid < CS ? ld_cluster_f64(cluster_map(smem_addr(&dx[0]), (uint32_t)tid)) : 0.0;
+            double t = 0.0;
+#pragma unroll
+            for (int c = 0; c < CS; ++c) t += __shfl_sync(0xffffffffu, x, c);
+            if (tid == 0) {
+                s_u[4] = ~v;
+                dx[1] = t;
+            }
         }
         __syncthreads();
         const double sk = (double)key_to_float(s_u[4]);
-        // the sample standard deviation of the candidates' coarse scores:
-        // the mean, then the sum of squared deviations, in fp64
-        double loc = 0.0;
-        for (int i = tid; i < ncb; i += NT) loc += (double)csc[i];
-        const double mean = pq_cluster_dsum<CS>(dx, pq_block_dsum(loc, dx + 2)) / (double)keff1;
+        const double mean = dx[1] / (double)keff1;
         loc = 0.0;
         for (int i = tid; i < ncb; i += NT) {
             const double d = (double)csc[i] - mean;
             loc += d * d;
         }
-        const double ss = pq_cluster_dsum<CS>(dx, pq_block_dsum(loc, dx + 2));
+        const double sq = pq_block_dsum(loc, dx + 4);
+        if (tid == 0) dx[2] = sq;
+        cluster_sync();
+        if (tid < 32) {
+            const double x = tid < CS ? ld_cluster_f64(cluster_map(smem_addr(&dx[2]), (uint32_t)tid)) : 0.0;
+            double t = 0.0;
+#pragma unroll
+            for (int c = 0; c < CS; ++c) t += __shfl_sync(0xffffffffu, x, c);
+            if (tid == 0) dx[3] = t;
+        }
+        __syncthreads();
+        const double ss = dx[3];
         tau = sk - sqrt(ss / (double)(keff1 - 1));
     }
 
