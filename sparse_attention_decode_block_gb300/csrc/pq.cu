@@ -524,8 +524,8 @@ struct PqSelLayout {
     static constexpr int CPG = FPG + kFtTok * 4;           // [kFtTok] int32 the candidates' pages
     static constexpr int HIST = CPG + kFtTok * 4;          // [kPqBins] the row's bucket counts
     static constexpr int CKT = HIST + kPqBins * 4;         // [kBkCap] int32 this CTA's boundary tokens
-    static constexpr int DX = CKT + kBkCap * 4;            // [4] fp64 exchange slots, [kFtWarps] fp64 warp sums
-    static constexpr int SMEM = DX + (4 + kFtWarps) * 8;
+    static constexpr int DX = CKT + kBkCap * 4;            // [5] fp64 exchange slots, [kFtWarps + 1] fp64 warp sums
+    static constexpr int SMEM = DX + (5 + kFtWarps + 1) * 8;
 };
 static_assert(PqSelLayout::SMEM + sizeof(ClusterTopkScratch<kFtThreads, 8>) <= 227 * 1024, "shared memory");
 
@@ -537,17 +537,24 @@ __host__ __device__ __forceinline__ int pq_slice(int T, int cs)
 }
 
 // Sum over the CTA of every thread's fp64 value, in a fixed order (lanes,
-// then warps), returned to every thread.  ws: kFtWarps doubles.
+// then warps), returned to every thread.  ws: kFtWarps + 1 doubles.  One
+// thread adds the warps' sums (fp64 arithmetic is slow on this part: the
+// other threads only read the result).
 __device__ __forceinline__ double pq_block_dsum(double v, double *ws)
 {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = v;
     __syncthreads();
-    double s = 0.0;
+    if (threadIdx.x == 0) {
+        double s = 0.0;
 #pragma unroll
-    for (int w = 0; w < kFtWarps; ++w) s += ws[w];
+        for (int w = 0; w < kFtWarps; ++w) s += ws[w];
+        ws[kFtWarps] = s;
+    }
     __syncthreads();
+    const double s = ws[kFtWarps];
+    __syncthreads();   // ws may be reused
     return s;
 }
 
@@ -746,15 +753,6 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
         tsm.xch[1][1] = nb_cta;
     }
     cluster_sync();   // (S1) per-CTA totals and boundary keys are in place
-    // every CTA has read the row's counts and extremes: reset them for the
-    // next call
-    if (me == 0) {
-        for (int i = tid; i < kPqBins; i += NT) a.hist[(int64_t)r * kPqBins + i] = 0u;
-        if (tid == 0) {
-            a.row_ext[2 * r] = 0u;
-            a.row_ext[2 * r + 1] = 0u;
-        }
-    }
     if (tid < 32) {
         const int lane = tid;
         uint32_t va = 0, vb = 0;
@@ -923,7 +921,7 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
         // none waits for the slots to be read
         double loc = 0.0;
         for (int i = tid; i < ncb; i += NT) loc += (double)csc[i];
-        const double sx = pq_block_dsum(loc, dx + 4);
+        const double sx = pq_block_dsum(loc, dx + 5);
         if (tid == 0) {
             uint32_t m = 0xffffffffu;
             for (int w = 0; w < NT / 32; ++w) m = min(m, tsm.red[w][0]);
@@ -940,18 +938,18 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
             for (int c = 0; c < CS; ++c) t += __shfl_sync(0xffffffffu, x, c);
             if (tid == 0) {
                 s_u[4] = ~v;
-                dx[1] = t;
+                dx[1] = t / (double)keff1;   // the mean, divided once
             }
         }
         __syncthreads();
         const double sk = (double)key_to_float(s_u[4]);
-        const double mean = dx[1] / (double)keff1;
+        const double mean = dx[1];
         loc = 0.0;
         for (int i = tid; i < ncb; i += NT) {
             const double d = (double)csc[i] - mean;
             loc += d * d;
         }
-        const double sq = pq_block_dsum(loc, dx + 4);
+        const double sq = pq_block_dsum(loc, dx + 5);
         if (tid == 0) dx[2] = sq;
         cluster_sync();
         if (tid < 32) {
@@ -961,9 +959,9 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
             for (int c = 0; c < CS; ++c) t += __shfl_sync(0xffffffffu, x, c);
             if (tid == 0) dx[3] = t;
         }
+        if (tid == 0) dx[4] = sk - sqrt(dx[3] / (double)(keff1 - 1));
         __syncthreads();
-        const double ss = dx[3];
-        tau = sk - sqrt(ss / (double)(keff1 - 1));
+        tau = dx[4];
     }
 
     // ---- E. the tokens this CTA rescores: its kept candidates in order,
@@ -1043,6 +1041,16 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
         });
         if (me == 0)
             for (int i = keff + tid; i < K; i += NT) orow[i] = -1;
+    }
+    // every CTA read the row's counts and extremes before the first cluster
+    // barrier: reset them for the next call (here, where no cluster barrier's
+    // release waits for these stores)
+    if (me == 0) {
+        for (int i = tid; i < kPqBins; i += NT) a.hist[(int64_t)r * kPqBins + i] = 0u;
+        if (tid == 0) {
+            a.row_ext[2 * r] = 0u;
+            a.row_ext[2 * r + 1] = 0u;
+        }
     }
 }
 
