@@ -226,6 +226,12 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t a, uint32_t v)
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
+// Two 32-bit words to an 8-byte aligned shared::cluster address in one store.
+__device__ __forceinline__ void st_cluster_v2_u32(uint32_t a, uint32_t x, uint32_t y)
+{
+    asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(x), "r"(y) : "memory");
+}
+
 __device__ __forceinline__ void red_cluster_add_u32(uint32_t a, uint32_t v)
 {
     asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");

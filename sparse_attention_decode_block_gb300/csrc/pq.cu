@@ -517,9 +517,9 @@ struct PqSelLayout {
     static constexpr int PART = KEYS + kFtTok * 128;       // [4][kFtTok] fp32 head-tile partials
     static constexpr int FS = PART + 4 * kFtTok * 4;       // [kFtTok] fp32 fine scores
     static constexpr int SC = FS + kFtTok * 4;             // [kFtTok] fp32 token scales
-    static constexpr int CTOK = SC + kFtTok * 4;           // [kFtTok] int32 this CTA's candidates (written by the cluster)
-    static constexpr int CSC = CTOK + kFtTok * 4;          // [kFtTok] fp32 their coarse scores
-    static constexpr int FTOK = CSC + kFtTok * 4;          // [kFtTok] int32 the tokens this CTA rescores
+    static constexpr int CAND = SC + kFtTok * 4;           // [kFtTok] (int32 token, fp32 coarse score): this
+                                                           // CTA's candidates, written by the cluster
+    static constexpr int FTOK = CAND + kFtTok * 8;         // [kFtTok] int32 the tokens this CTA rescores
     static constexpr int FPG = FTOK + kFtTok * 4;          // [kFtTok] int32 their pages
     static constexpr int CPG = FPG + kFtTok * 4;           // [kFtTok] int32 the candidates' pages
     static constexpr int HIST = CPG + kFtTok * 4;          // [kPqBins] the row's bucket counts
@@ -577,8 +577,9 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
     float *part = reinterpret_cast<float *>(smem + LY::PART);
     float *fs = reinterpret_cast<float *>(smem + LY::FS);
     float *scl = reinterpret_cast<float *>(smem + LY::SC);
-    int *ctok = reinterpret_cast<int *>(smem + LY::CTOK);
-    float *csc = reinterpret_cast<float *>(smem + LY::CSC);
+    const int2 *cand = reinterpret_cast<const int2 *>(smem + LY::CAND);
+    auto ctok = [&](int i) -> int { return cand[i].x; };
+    auto csc = [&](int i) -> float { return __int_as_float(cand[i].y); };
     int *ftok = reinterpret_cast<int *>(smem + LY::FTOK);
     int *fpg = reinterpret_cast<int *>(smem + LY::FPG);
     int *cpg = reinterpret_cast<int *>(smem + LY::CPG);
@@ -875,8 +876,7 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
                 const int owner = (int)pos / CB, slot = (int)pos - owner * CB;
                 // the score as its key maps it back (-0 as +0)
                 const uint32_t xb = __float_as_uint(x) == 0x80000000u ? 0u : __float_as_uint(x);
-                st_cluster_u32(cluster_map(smem_addr(&ctok[slot]), (uint32_t)owner), (uint32_t)i);
-                st_cluster_u32(cluster_map(smem_addr(&csc[slot]), (uint32_t)owner), xb);
+                st_cluster_v2_u32(cluster_map(smem_addr(&cand[slot]), (uint32_t)owner), (uint32_t)i, xb);
                 if (cout) cout[pos] = i;
                 ++pos;
             }
@@ -891,7 +891,7 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
     const int ncb = min(CB, max(0, keff1 - (int)me * CB));   // this CTA's candidates
     // pages of this CTA's candidates
     for (int i = tid; i < ncb; i += NT) {
-        const int t = ctok[i];
+        const int t = ctok(i);
         const int p = a.pt[(int64_t)r * a.max_blocks + t / b];
         const bool pok = p >= 0 && p < a.ic.num_pages;
         if (!pok) flag_error(a.status, LSA_ERR_BOUNDS);
@@ -905,7 +905,7 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int i = 2 * tid + e;
-            keys[e] = i < ncb ? float_to_key(csc[i]) : 0u;
+            keys[e] = i < ncb ? float_to_key(csc(i)) : 0u;
         }
         uint32_t kmin = 0xffffffffu;
         const int col0 = (int)me * kFtTok + 2 * tid;
@@ -920,7 +920,7 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
         // the top k, in one exchange; each exchange has its own slots, so
         // none waits for the slots to be read
         double loc = 0.0;
-        for (int i = tid; i < ncb; i += NT) loc += (double)csc[i];
+        for (int i = tid; i < ncb; i += NT) loc += (double)csc(i);
         const double sx = pq_block_dsum(loc, dx + 5);
         if (tid == 0) {
             uint32_t m = 0xffffffffu;
@@ -946,7 +946,7 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
         const double mean = dx[1];
         loc = 0.0;
         for (int i = tid; i < ncb; i += NT) {
-            const double d = (double)csc[i] - mean;
+            const double d = (double)csc(i) - mean;
             loc += d * d;
         }
         const double sq = pq_block_dsum(loc, dx + 5);
@@ -971,14 +971,14 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
         const int i = base + tid;
         bool keep = false;
         if (i < ncb) {
-            const int t = ctok[i], p = cpg[i];
+            const int t = ctok(i), p = cpg[i];
             const bool hit = !a.hit || (p >= 0 && a.hit[(int64_t)p * b + t % b] != 0);
-            keep = p >= 0 && (hit || (double)csc[i] >= tau);
+            keep = p >= 0 && (hit || (double)csc(i) >= tau);
         }
         uint32_t tot = 0;
         const uint32_t at = bk_scan<NT>(keep ? 1u : 0u, tsm.red, &tot);
         if (keep) {
-            ftok[nf + (int)at] = ctok[i];
+            ftok[nf + (int)at] = ctok(i);
             fpg[nf + (int)at] = cpg[i];
         }
         nf += (int)tot;
