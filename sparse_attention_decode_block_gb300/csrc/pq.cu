@@ -683,6 +683,11 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
     uint32_t Tk = 0u;
     int take_eq = 0;
     uint32_t n_a = 0, n_b = 0;   // this thread's winners / boundary keys (or > Tk / == Tk)
+    // the positions (4 * chunk + element) of this thread's first kPqList
+    // winners and boundary keys, in token order, 8 bits each, so that the
+    // candidates' pass below visits only them
+    constexpr int kPqList = 8;
+    uint64_t clist = 0;
     if (!crowded) {
         for (int c = 0; c < nch; ++c) {
             const float4 v = chunk_at(c);
@@ -690,8 +695,11 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int bk = cand_bucket(xs[e]);
-                n_a += bk >= 0 && bk > B1;
-                n_b += bk >= 0 && bk == B1;
+                const bool w = bk >= 0 && bk > B1, bd = bk >= 0 && bk == B1;
+                const uint32_t seen = n_a + n_b;
+                if ((w || bd) && seen < (uint32_t)kPqList) clist |= (uint64_t)(4 * c + e) << (8 * seen);
+                n_a += w;
+                n_b += bd;
             }
         }
     } else {
@@ -847,7 +855,34 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
         __syncthreads();
         uint32_t pos = cbase + bk_scan<NT>(mine, tsm.red, &dummy);
         int32_t *cout = a.cand_out ? a.cand_out + (int64_t)r * C : nullptr;
-        for (int c = 0; c < nch && (n_a + n_b) > 0; ++c) {
+        // the candidate at position q (4 * chunk + element) of this thread's
+        // slice: taken or not, then to its owner (and to cand_out)
+        auto emit = [&](int q, float x, bool take) {
+            if (!take) return;
+            const int i = t_lo + q;
+            const int owner = (int)pos / CB, slot = (int)pos - owner * CB;
+            // the score as its key maps it back (-0 as +0)
+            const uint32_t xb = __float_as_uint(x) == 0x80000000u ? 0u : __float_as_uint(x);
+            st_cluster_v2_u32(cluster_map(smem_addr(&cand[slot]), (uint32_t)owner), (uint32_t)i, xb);
+            if (cout) cout[pos] = i;
+            ++pos;
+        };
+        const bool listed = !crowded && n_a + n_b <= (uint32_t)kPqList;
+        if (listed) {
+            for (int n = 0; n < (int)(n_a + n_b); ++n) {
+                const int q = (int)((clist >> (8 * n)) & 0xffu);
+                const float x = reinterpret_cast<const float *>(smem + LY::KEYS + ((size_t)tid * NCH +
+                                                                                   ((uint32_t)(q >> 2) ^ swz)) * 16)[q & 3];
+                const int bk = cand_bucket(x);
+                bool take = bk > B1;
+                if (bk == B1) {
+                    take = tsm.pick[bpos] != 0;
+                    ++bpos;
+                }
+                emit(q, x, take);
+            }
+        }
+        for (int c = 0; !listed && c < nch && (n_a + n_b) > 0; ++c) {
             const float4 v = chunk_at(c);
             const float xs[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -871,14 +906,7 @@ __global__ void __launch_bounds__(kFtThreads, 1) k_pq_select(PqArgs a)
                         ++bpos;
                     } else take = false;
                 }
-                if (!take) continue;
-                const int i = t_lo + 4 * c + e;
-                const int owner = (int)pos / CB, slot = (int)pos - owner * CB;
-                // the score as its key maps it back (-0 as +0)
-                const uint32_t xb = __float_as_uint(x) == 0x80000000u ? 0u : __float_as_uint(x);
-                st_cluster_v2_u32(cluster_map(smem_addr(&cand[slot]), (uint32_t)owner), (uint32_t)i, xb);
-                if (cout) cout[pos] = i;
-                ++pos;
+                emit(4 * c + e, x, take);
             }
         }
         if (cout && me == 0)
