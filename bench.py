@@ -57,7 +57,7 @@ NCU_TRAFFIC = {
     ("c2f", "k_c2f_fine"): 9007488, ("c2f", "k_score"): 8614912, ("c2f_wrelu", "k_c2f_fine"): 9009067,
     ("mla", "k_score"): 76397312, ("mla", "k_topk"): 303104, ("mla", "k_sparse_attn_umma"): 9537920,
     ("c2f", "k_sparse_attn_umma"): 4430720,
-    ("c2f_pq", "k_pq_scores"): 67650475, ("c2f_pq", "k_pq_hist + k_pq_select"): 25298688,
+    ("c2f_pq", "k_pq_scores"): 67523021, ("c2f_pq", "k_pq_hist + k_pq_select"): 25293645,
 }
 
 
