@@ -167,7 +167,8 @@ def assert_attention_close(o_gpu: torch.Tensor, o_ref_bits: np.ndarray, what: st
 def assert_lse_close(lse_gpu: torch.Tensor, lse_ref: np.ndarray, what: str = ""):
     l = lse_gpu.detach().cpu().numpy().astype(np.float64)
     both_inf = np.isneginf(l) & np.isneginf(lse_ref)
-    d = np.where(both_inf, 0.0, np.abs(l - lse_ref))
+    with np.errstate(invalid="ignore"):   # -inf - -inf where both are empty; masked below
+        d = np.where(both_inf, 0.0, np.abs(l - lse_ref))
     lim = LSE_ATOL + LSE_RTOL * np.where(both_inf, 0.0, np.abs(lse_ref))
     assert np.all(d <= lim), f"{what}: lse max err {np.nanmax(d):.3g}"
 
