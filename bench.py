@@ -172,11 +172,12 @@ class Instance:
         self.lse = torch.empty((B, w.num_q_heads), dtype=torch.float32, device=dev)
         self.L = L
 
-    def step(self, q=None, pt=None, lens=None, stream=None):
+    def step(self, q=None, pt=None, lens=None, stream=None, out=None, lse=None):
         g = self.g
         self.L.lsa_decode_step(g["q"] if q is None else q, self.cache, self.summ, self.icache,
                                g["page_table"] if pt is None else pt, g["seq_lens"] if lens is None else lens,
-                               self.params, self.idx, self.out, self.lse, self.ws, stream)
+                               self.params, self.idx, self.out if out is None else out,
+                               self.lse if lse is None else lse, self.ws, stream)
 
 
 
@@ -501,40 +502,63 @@ def run_gpu(args, rank, world, dev):
                 kernels=kernels_per_step(insts[0]), w=w, pq_tokens=pq_tokens)
 
 
+def _packed(tensors, pinned: bool, dev=None):
+    """One uint8 buffer holding the tensors back to back at 16-byte aligned
+    offsets (pinned host memory, or device memory when dev is given), and
+    views of it shaped like each tensor."""
+    offs, n = [], 0
+    for t in tensors:
+        offs.append(n)
+        n += -(-t.numel() * t.element_size() // 16) * 16
+    buf = (torch.empty(n, dtype=torch.uint8).pin_memory() if pinned
+           else torch.empty(n, dtype=torch.uint8, device=dev))
+    views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for o, t in zip(offs, tensors)]
+    return buf, views
+
+
 def e2e_leg(insts, args, stream):
     """The same step through the public call with HOST buffers: every step
     copies its q, page table and lengths from pinned host memory to the
     device, runs lsa_decode_step, and copies out and lse back to pinned host
-    memory.  The copies and the call are captured in CUDA graphs of `chunk`
-    steps rotating over the instances (as the device-side timing does), so
-    that the number is the library's cost plus the copies, not Python's."""
+    memory.  A caller's inputs of one step sit in one pinned staging buffer
+    (q, page table, lengths at 16-byte aligned offsets) and its results in
+    another, so that a step is one copy in and one copy out.  The copies and
+    the call are captured in CUDA graphs of `chunk` steps rotating over the
+    instances (as the device-side timing does), so that the number is the
+    library's cost plus the copies, not Python's.  Before timing, each
+    instance's results through this path are checked to equal, bit for bit,
+    the device-resident step's."""
     R = len(insts)
     host = []
     for it in insts:
         g = it.g
-        host.append(dict(
-            q=g["q"].cpu().pin_memory(), pt=g["page_table"].cpu().pin_memory(),
-            lens=g["seq_lens"].cpu().pin_memory(),
-            out=torch.empty(it.out.shape, dtype=it.out.dtype).pin_memory(),
-            lse=torch.empty(it.lse.shape, dtype=it.lse.dtype).pin_memory(),
-            dq=torch.empty_like(g["q"]), dpt=torch.empty_like(g["page_table"]),
-            dl=torch.empty_like(g["seq_lens"])))
+        hin, (hq, hpt, hl) = _packed([g["q"], g["page_table"], g["seq_lens"]], pinned=True)
+        hq.copy_(g["q"].cpu())
+        hpt.copy_(g["page_table"].cpu())
+        hl.copy_(g["seq_lens"].cpu())
+        din, (dq, dpt, dl) = _packed([g["q"], g["page_table"], g["seq_lens"]], pinned=False, dev=g["q"].device)
+        dout, (do, dlse) = _packed([it.out, it.lse], pinned=False, dev=g["q"].device)
+        hout, (ho, hlse) = _packed([it.out, it.lse], pinned=True)
+        host.append(dict(hin=hin, din=din, dq=dq, dpt=dpt, dl=dl, dout=dout, do=do, dlse=dlse,
+                         hout=hout, ho=ho, hlse=hlse))
 
     def one(i):
         it, h = insts[i % R], host[i % R]
-        h["dq"].copy_(h["q"], non_blocking=True)
-        h["dpt"].copy_(h["pt"], non_blocking=True)
-        h["dl"].copy_(h["lens"], non_blocking=True)
-        it.step(h["dq"], h["dpt"], h["dl"], stream)
-        h["out"].copy_(it.out, non_blocking=True)
-        h["lse"].copy_(it.lse, non_blocking=True)
+        h["din"].copy_(h["hin"], non_blocking=True)
+        it.step(h["dq"], h["dpt"], h["dl"], stream, out=h["do"], lse=h["dlse"])
+        h["hout"].copy_(h["dout"], non_blocking=True)
 
     chunk = R * max(1, 32 // R)
     n = max(chunk, min(args.steps, 4000) // chunk * chunk)
     with torch.cuda.stream(stream):
         for i in range(R):
+            insts[i].step(stream=stream)
             one(i)
         stream.synchronize()
+        for it, h in zip(insts, host):
+            if not (torch.equal(h["ho"].view(torch.int16), it.out.cpu().view(torch.int16))
+                    and torch.equal(h["hlse"], it.lse.cpu())):
+                raise RuntimeError("the host-buffer step differs from the device-resident step")
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr, stream=stream):
             for i in range(chunk):
@@ -549,9 +573,7 @@ def e2e_leg(insts, args, stream):
         stream.synchronize()
     ms = e0.elapsed_time(e1) / n
     h = host[0]
-    h2d = sum(h[k].numel() * h[k].element_size() for k in ("q", "pt", "lens"))
-    d2h = sum(h[k].numel() * h[k].element_size() for k in ("out", "lse"))
-    return dict(ms_per_step=ms, h2d=h2d, d2h=d2h, steps=n)
+    return dict(ms_per_step=ms, h2d=h["hin"].numel(), d2h=h["hout"].numel(), steps=n)
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -772,8 +794,9 @@ def main():
         "e2e": {"value": round(1e3 / e2e["ms_per_step"] * world, 1), "unit": "calls/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e["ms_per_step"], 5),
-                "note": "lsa_decode_step with pinned host buffers copied in and out every step, "
-                        "the copies and the call captured in CUDA graphs"},
+                "note": "lsa_decode_step on host inputs: each step copies one pinned staging buffer "
+                        "(q, page table, lengths) in and one (out, lse) back, the copies and the call "
+                        "captured in CUDA graphs; results checked equal to the device-resident step's"},
         "gpu_launches": res["kernels"] * args.steps,
         "clocks": res["clocks"],
     }
