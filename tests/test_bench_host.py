@@ -66,3 +66,27 @@ def test_reference_arm_other_ranks_exit_without_work():
                        capture_output=True, text=True, env=env, timeout=300)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+def test_e2e_staging_buffer_layout():
+    """The e2e leg's staging buffers: every tensor at a 16-byte aligned offset
+    of one buffer, views that alias it, and the buffer's size the bytes a step
+    copies (checked on CPU memory; the bench pins the host side)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    q = torch.randn(3, 5, 128).to(torch.bfloat16)
+    pt = torch.randint(0, 1000, (3, 7), dtype=torch.int32)
+    lens = torch.arange(3, dtype=torch.int32)
+    buf, (vq, vpt, vl) = bench._packed([q, pt, lens], pinned=False, dev="cpu")
+    offs = [v.data_ptr() - buf.data_ptr() for v in (vq, vpt, vl)]
+    assert offs[0] == 0 and all(o % 16 == 0 for o in offs)
+    assert offs[1] >= q.numel() * 2 and offs[2] >= offs[1] + pt.numel() * 4
+    assert buf.numel() == offs[2] + 16   # 12 bytes of lengths, rounded up to 16
+    vq.copy_(q)
+    vpt.copy_(pt)
+    vl.copy_(lens)
+    assert torch.equal(vq, q) and torch.equal(vpt, pt) and torch.equal(vl, lens)
+    assert vq.shape == q.shape and vpt.dtype == torch.int32
+    # the views write through to the one buffer that a step copies
+    raw = buf[offs[1]:offs[1] + 4].view(torch.int32)
+    assert int(raw[0]) == int(pt[0, 0])
